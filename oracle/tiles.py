@@ -1,0 +1,169 @@
+"""Per-key visibility bound, tile visibility map, work lists: the plan fields.
+
+The tile map is a plain count of visible (query, key) pairs per BM x BN tile of
+the canonical grid, taken from the row form of the mask (ancestor chunks in
+full, own chunk causally; "Tree Training" §3.2 "Attention Mask", App. A.1). A
+tile is EMPTY with no visible pair, FULL when all BM*BN pairs are visible (so
+it also lies entirely inside the sequence), PARTIAL otherwise. A.1 notes that
+the masked blocks are skipped entirely; the map is what lets a kernel do so.
+
+``key_end[j]`` is one past the last row that sees key j: the per-column bound
+in the spirit of A.1's "per-query start/end column bounds", taken here column-wise.
+
+Work orders (longest first) and the q-tile pair lists are conventions of this
+library for scheduling; the pages say nothing about them.
+"""
+from __future__ import annotations
+
+from collections import defaultdict
+
+import numpy as np
+
+from . import trie as T
+from .mask import TrieView
+
+EMPTY, PARTIAL, FULL = 0, 1, 2
+
+
+def key_end(parents, lengths) -> np.ndarray:
+    """key_end[j] = 1 + the largest row i that attends to key j.
+
+    Row i attends to key j in segment s iff seg(i) == s and i >= j, or s is an
+    ancestor of seg(i). The largest such row is the last token of the
+    segments in s's subtree; every descendant d raises the bound of each of its
+    ancestors to the end of d.
+    """
+    view = TrieView(parents, lengths)
+    last = [view.seg_range(s)[1] for s in range(view.S)]
+    for d in range(view.S):
+        for a in view.anc[d]:
+            last[a] = max(last[a], view.seg_range(d)[1])
+    return np.array([last[s] for s in view.token_seg], dtype=np.int32)
+
+
+def tile_counts(parents, lengths, bm: int = 128, bn: int = 128):
+    """Number of visible pairs in each non-empty (q-tile, k-tile)."""
+    view = TrieView(parents, lengths)
+    counts = defaultdict(int)
+    for s in range(view.S):
+        a, b = view.seg_range(s)
+        for qt in range(a // bm, (b - 1) // bm + 1):
+            r0, r1 = max(a, qt * bm), min(b, (qt + 1) * bm)
+            nrows = r1 - r0
+            # ancestor chunks: every row of the segment sees all of them
+            for anc in view.anc[s]:
+                c, d = view.seg_range(anc)
+                for kt in range(c // bn, (d - 1) // bn + 1):
+                    overlap = min(d, (kt + 1) * bn) - max(c, kt * bn)
+                    counts[(qt, kt)] += nrows * overlap
+            # own chunk: row i sees [a, i + 1)
+            rows = np.arange(r0, r1)
+            for kt in range(a // bn, (r1 - 1) // bn + 1):
+                lo, hi = kt * bn, (kt + 1) * bn
+                overlap = np.minimum(rows + 1, hi) - max(a, lo)
+                counts[(qt, kt)] += int(np.clip(overlap, 0, None).sum())
+    return dict(counts)
+
+
+def plan_fields(parents, lengths, bm: int = 128, bn: int = 128) -> dict:
+    """Every plan field as int32/int64 numpy arrays, named as in the C-ABI."""
+    parents_l, lengths_l = T.validate(parents, lengths)
+    S = len(parents_l)
+    N = sum(lengths_l)
+    view = TrieView(parents_l, lengths_l)
+    roots, trie_id = T.tries(parents_l)
+    g = T.paths_through(parents_l)
+    K = T.paths_per_trie(parents_l)
+
+    depth = [len(view.anc[s]) for s in range(S)]
+    # the subtree of s ends where the last of its descendants (or s) ends
+    subtree_end = [view.seg_range(s)[1] for s in range(S)]
+    for d in range(S):
+        for a in view.anc[d]:
+            subtree_end[a] = max(subtree_end[a], view.seg_range(d)[1])
+    anc_ptr = [0]
+    anc_idx = []
+    for s in range(S):
+        anc_idx.extend(view.anc[s])
+        anc_ptr.append(len(anc_idx))
+    cu_seqlens = [view.seg_start[r] for r in roots] + [N]
+
+    T_q = (N + bm - 1) // bm
+    T_k = (N + bn - 1) // bn
+    counts = tile_counts(parents_l, lengths_l, bm, bn)
+    kinds = {key: (FULL if c == bm * bn else PARTIAL) for key, c in counts.items() if c > 0}
+
+    per_q = [[] for _ in range(T_q)]
+    for (qt, kt) in kinds:
+        per_q[qt].append(kt)
+    per_q = [sorted(x) for x in per_q]
+    qt_ptr = [0]
+    qt_kt, qt_kind = [], []
+    for q in range(T_q):
+        for kt in per_q[q]:
+            qt_kt.append(kt)
+            qt_kind.append(kinds[(q, kt)])
+        qt_ptr.append(len(qt_kt))
+
+    kt_qlo = [T_q] * T_k
+    kt_qhi = [0] * T_k
+    for (qt, kt) in kinds:
+        kt_qlo[kt] = min(kt_qlo[kt], qt)
+        kt_qhi[kt] = max(kt_qhi[kt], qt + 1)
+
+    fwd_order = lpt_order([len(per_q[q]) for q in range(T_q)])
+    bwd_order = lpt_order([kt_qhi[k] - kt_qlo[k] for k in range(T_k)])
+
+    n_pairs = (T_q + 1) // 2
+    qp_ptr = [0]
+    qp_kt, qp_kind = [], []
+    pair_work = []
+    for p in range(n_pairs):
+        slots = [2 * p, 2 * p + 1]
+        union = sorted(set(kt for q in slots if q < T_q for kt in per_q[q]))
+        for kt in union:
+            k0 = kinds.get((slots[0], kt), EMPTY)
+            k1 = kinds.get((slots[1], kt), EMPTY) if slots[1] < T_q else EMPTY
+            qp_kt.append(kt)
+            qp_kind.append(k0 | (k1 << 2))
+        qp_ptr.append(len(qp_kt))
+        pair_work.append(sum(len(per_q[q]) for q in slots if q < T_q))
+    qp_order = lpt_order(pair_work)
+
+    pos_id = T.position_ids(parents_l, lengths_l)
+    i32 = lambda x: np.asarray(x, dtype=np.int32)  # noqa: E731
+    return {
+        "num_tokens": N,
+        "num_segments": S,
+        "num_tries": len(roots),
+        "visible_pairs": view.visible_count(),
+        "dfs_order": i32(view.order),
+        "seg_start": i32(view.seg_start),
+        "depth": i32(depth),
+        "subtree_end": i32(subtree_end),
+        "trie_id": i32(trie_id),
+        "g": i32(g),
+        "anc_ptr": i32(anc_ptr),
+        "anc_idx": i32(anc_idx),
+        "token_seg": i32(view.token_seg),
+        "pos_id": i32(pos_id),
+        "key_end": key_end(parents_l, lengths_l),
+        "cu_seqlens": i32(cu_seqlens),
+        "trie_paths": i32(K),
+        "qt_ptr": i32(qt_ptr),
+        "qt_kt": i32(qt_kt),
+        "qt_kind": i32(qt_kind),
+        "kt_qlo": i32(kt_qlo),
+        "kt_qhi": i32(kt_qhi),
+        "fwd_order": i32(fwd_order),
+        "bwd_order": i32(bwd_order),
+        "qp_ptr": i32(qp_ptr),
+        "qp_kt": i32(qp_kt),
+        "qp_kind": i32(qp_kind),
+        "qp_order": i32(qp_order),
+    }
+
+
+def lpt_order(work):
+    """Indices sorted by work, largest first; ties keep ascending index."""
+    return sorted(range(len(work)), key=lambda i: (-work[i], i))
