@@ -1,0 +1,189 @@
+/*
+ * treeattn.h -- C-ABI of libtreeattn: tree-packed attention on one GB300 (sm_103a).
+ *
+ * The method: "Tree Training: Accelerating Agentic LLMs Training via Shared
+ * Prefix Reuse" (arXiv 2511.00413). A trie of token segments is laid out once
+ * in depth-first order (§3.1 eq. 8). Token i attends to token j iff j <= i and
+ * the segments of i and j lie on one root-to-leaf path (§3.2 "Attention
+ * Mask"): its ancestors' segments in full and its own segment causally
+ * (App. A.1). The result for every token equals running each root-to-leaf
+ * path alone (§3.1 eq. 6). The per-token loss weight is g_t/K (§3.1 eq. 4).
+ *
+ * Conventions for every call:
+ *  - Status: every call returns tree_status_t (TREE_OK = 0) and never aborts;
+ *    on failure tree_last_error() holds a message (thread-local). All
+ *    argument, shape and alignment checks run on the host before any launch.
+ *  - Ownership: the caller owns every tensor and the workspace. The library
+ *    owns only the plan (host arrays and the plan's device copy).
+ *  - Streams: calls that take a stream enqueue work on it and return
+ *    without waiting (stream-ordered). `stream` is a cudaStream_t passed as
+ *    void* (NULL = the legacy default stream).
+ *  - Tensor layout: token-major, contiguous, in DFS order. q and o are
+ *    [N, hq, D]; k and v are [N, hkv, D]; lse is [hq, N] fp32, natural log.
+ *    Segment s occupies tokens [seg_start[s], seg_start[s] + lengths[s]).
+ *    Grouped heads: q head h reads kv head h / (hq / hkv).
+ *  - Device pointers must be 16-byte aligned.
+ *  - Dtypes: TREE_DTYPE_BF16 runs the tcgen05 tensor-core kernels (D = 128);
+ *    TREE_DTYPE_F32 runs the fp32 CUDA-core kernels (D = 64 or 128).
+ *  - Tile grid: 128 x 128 (query x key) tiles; a tile with no visible pair
+ *    is never loaded or multiplied.
+ */
+#ifndef TREEATTN_H
+#define TREEATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TREE_OK = 0,
+  TREE_ERR_INVALID_ARG = 1,    /* bad pointer, size, shape, alignment or parent id */
+  TREE_ERR_CYCLE = 2,          /* some segment does not reach a root */
+  TREE_ERR_EMPTY_SEGMENT = 3,  /* a segment with fewer than one token */
+  TREE_ERR_OVERFLOW = 4,       /* a count does not fit int32 */
+  TREE_ERR_UNSUPPORTED = 5,    /* valid, but outside what the kernels handle (e.g. D) */
+  TREE_ERR_CUDA = 6,           /* a CUDA runtime call failed */
+  TREE_ERR_TIMEOUT = 7,        /* a kernel gave up a bounded wait (device status word) */
+  TREE_ERR_OOM = 8,            /* host or device allocation failed */
+  TREE_ERR_NOT_ON_DEVICE = 9   /* tree_plan_to_device has not been called */
+} tree_status_t;
+
+typedef enum { TREE_DTYPE_F32 = 0, TREE_DTYPE_BF16 = 1 } tree_dtype_t;
+
+typedef void* tree_stream_t; /* a cudaStream_t */
+
+typedef struct tree_plan tree_plan_t; /* opaque, library-owned */
+
+typedef struct {
+  int64_t num_tokens;     /* N = sum of segment lengths */
+  int64_t num_segments;   /* S */
+  int64_t num_tries;      /* R = number of roots */
+  int64_t block_m;        /* query rows per tile (128) */
+  int64_t block_n;        /* keys per tile (128) */
+  int64_t num_q_tiles;    /* ceil(N / block_m) */
+  int64_t num_k_tiles;    /* ceil(N / block_n) */
+  int64_t nnz_tiles;      /* non-empty (q-tile, k-tile) tiles */
+  int64_t num_pairs;      /* ceil(num_q_tiles / 2): q-tile pairs (2p, 2p+1) */
+  int64_t nnz_pair_tiles; /* entries of the q-tile-pair union lists */
+  int64_t num_ancestors;  /* sum over segments of the number of ancestors */
+  int64_t visible_pairs;  /* sum over rows of the visible keys, diagonal included */
+} tree_plan_info_t;
+
+/* Plan fields readable with tree_plan_get. All are int32 arrays. */
+typedef enum {
+  TREE_FIELD_DFS_ORDER = 0,   /* [S]   segments in DFS visit order (eq. 8; children and roots in ascending id) */
+  TREE_FIELD_SEG_START = 1,   /* [S]   first DFS token of each segment (by segment id) */
+  TREE_FIELD_DEPTH = 2,       /* [S]   number of ancestors (a root has 0) */
+  TREE_FIELD_SUBTREE_END = 3, /* [S]   one past the last DFS token of the segment's subtree */
+  TREE_FIELD_TRIE_ID = 4,     /* [S]   index of the segment's root among the roots in ascending id */
+  TREE_FIELD_G = 5,           /* [S]   g_n: root-to-leaf paths through the segment (§3.1) */
+  TREE_FIELD_ANC_PTR = 6,     /* [S+1] CSR offsets into ANC_IDX */
+  TREE_FIELD_ANC_IDX = 7,     /* [num_ancestors] ancestors of each segment, root first, itself excluded */
+  TREE_FIELD_TOKEN_SEG = 8,   /* [N]   segment of each DFS token */
+  TREE_FIELD_POS_ID = 9,      /* [N]   position id of eq. 9 (offset within every path through the token) */
+  TREE_FIELD_KEY_END = 10,    /* [N]   rows key_end[j] > i >= j are exactly the rows that see key j */
+  TREE_FIELD_CU_SEQLENS = 11, /* [R+1] token range of each trie */
+  TREE_FIELD_TRIE_PATHS = 12, /* [R]   K of each trie: its number of root-to-leaf paths */
+  TREE_FIELD_QT_PTR = 13,     /* [num_q_tiles+1] CSR offsets of the forward tile lists */
+  TREE_FIELD_QT_KT = 14,      /* [nnz_tiles] non-empty k-tiles of each q-tile, ascending */
+  TREE_FIELD_QT_KIND = 15,    /* [nnz_tiles] 1 = PARTIAL (needs masking), 2 = FULL */
+  TREE_FIELD_KT_QLO = 16,     /* [num_k_tiles] first q-tile that sees the k-tile */
+  TREE_FIELD_KT_QHI = 17,     /* [num_k_tiles] one past the last; every q-tile in between sees it */
+  TREE_FIELD_FWD_ORDER = 18,  /* [num_q_tiles] q-tiles by tile count, largest first (ties: ascending) */
+  TREE_FIELD_BWD_ORDER = 19,  /* [num_k_tiles] k-tiles by q-tile range, largest first (ties: ascending) */
+  TREE_FIELD_QP_PTR = 20,     /* [num_pairs+1] CSR offsets of the q-tile-pair union lists */
+  TREE_FIELD_QP_KT = 21,      /* [nnz_pair_tiles] union of the k-tiles of q-tiles 2p and 2p+1, ascending */
+  TREE_FIELD_QP_KIND = 22,    /* [nnz_pair_tiles] kind for q-tile 2p | (kind for 2p+1) << 2; 0 = EMPTY */
+  TREE_FIELD_QP_ORDER = 23,   /* [num_pairs] pairs by total tile count, largest first (ties: ascending) */
+  TREE_FIELD_COUNT = 24
+} tree_plan_field_t;
+
+/*
+ * Build a plan from a trie (or a forest: several roots pack several tries in
+ * one row). Host only; no GPU needed.
+ *   segment_parents[s]: parent segment id of s, or -1 for a root (host, int32[num_segments]).
+ *   segment_lengths[s]: tokens of segment s, >= 1 (host, int32[num_segments]).
+ * Parents may come after their children in id order. The inputs are copied.
+ * Errors: TREE_ERR_INVALID_ARG (parent out of [-1, S) or equal to s; NULL
+ * pointer with num_segments > 0; num_segments < 0), TREE_ERR_EMPTY_SEGMENT,
+ * TREE_ERR_CYCLE, TREE_ERR_OVERFLOW (more than 2^31-129 tokens, or more than
+ * 2^31-1 ancestor entries or tiles), TREE_ERR_OOM. num_segments == 0 gives an empty plan (N = 0).
+ * Follows §3.1 (trie, g_n, K), eq. 8 (DFS layout), eq. 9 (positions), and the
+ * mask of §3.2 / App. A.1 for the tile map. *out is set only on TREE_OK.
+ */
+tree_status_t tree_plan_build(const int32_t* segment_parents, const int32_t* segment_lengths,
+                              int32_t num_segments, tree_plan_t** out);
+
+/* Sizes of a plan (host). */
+tree_status_t tree_plan_info(const tree_plan_t* plan, tree_plan_info_t* out);
+
+/* Copy one int32 field into host memory `dst` of exactly `bytes` bytes
+ * (field length x 4; TREE_ERR_INVALID_ARG otherwise). */
+tree_status_t tree_plan_get(const tree_plan_t* plan, tree_plan_field_t field, void* dst, size_t bytes);
+
+/* Number of int32 elements of a field. */
+tree_status_t tree_plan_field_len(const tree_plan_t* plan, tree_plan_field_t field, int64_t* out);
+
+/* Copy the fields the kernels read to the current CUDA device (allocated by
+ * and owned by the plan; stream-ordered copy on `stream`). Calling it again
+ * on the same device is a no-op; on another device it replaces the copy. */
+tree_status_t tree_plan_to_device(tree_plan_t* plan, tree_stream_t stream);
+
+/* Free the plan and its device copy (waits for the device first). NULL is a no-op. */
+void tree_plan_destroy(tree_plan_t* plan);
+
+/*
+ * Forward tree attention (§3.2 mask; App. A.1 block skipping).
+ *   q [N,hq,D], k,v [N,hkv,D]: device, dtype `dtype`.
+ *   o [N,hq,D] (device, dtype `dtype`), lse [hq,N] (device, fp32): written.
+ *   softmax_scale: logits are scale * q.k; 0 selects 1/sqrt(D).
+ * o_i = sum_j softmax_j(scale q_i.k_j over the keys visible to i) v_j and
+ * lse_i = log sum_j exp(scale q_i.k_j). Requires hq % hkv == 0, D in {64,128}
+ * for fp32 and D == 128 for bf16 (else TREE_ERR_UNSUPPORTED).
+ */
+tree_status_t tree_attn_fwd(const tree_plan_t* plan, const void* q, const void* k, const void* v,
+                            void* o, float* lse, int32_t hq, int32_t hkv, int32_t head_dim,
+                            tree_dtype_t dtype, float softmax_scale, tree_stream_t stream);
+
+/* Workspace the backward needs, in bytes (device memory the caller provides). */
+size_t tree_attn_bwd_workspace_bytes(const tree_plan_t* plan, int32_t hq, int32_t head_dim,
+                                     tree_dtype_t dtype);
+
+/*
+ * Backward tree attention: the analytic gradients of the forward.
+ *   dout, q, o [N,hq,D] and k, v [N,hkv,D]: device, dtype `dtype`;
+ *   lse [hq,N] fp32 from tree_attn_fwd (same scale).
+ *   dq [N,hq,D], dk, dv [N,hkv,D]: device, dtype `grad_dtype`, written
+ *   (grad_dtype must be F32 when dtype is F32).
+ *   workspace: device, >= tree_attn_bwd_workspace_bytes(...) bytes; its
+ *   contents on entry do not matter.
+ * With P = exp(scale S - lse), Delta_i = dO_i.O_i, dS = P (dO V^T - Delta):
+ * dq = scale dS K, dk = scale dS^T Q, dv = P^T dO (dk, dv summed over the q
+ * heads of a group). Summation order of dq may vary between runs.
+ */
+tree_status_t tree_attn_bwd(const tree_plan_t* plan, const void* dout, const void* q, const void* k,
+                            const void* v, const void* o, const float* lse, void* dq, void* dk,
+                            void* dv, int32_t hq, int32_t hkv, int32_t head_dim, tree_dtype_t dtype,
+                            tree_dtype_t grad_dtype, float softmax_scale, void* workspace,
+                            size_t workspace_bytes, tree_stream_t stream);
+
+/* Per-token loss weights g_t / K of the token's trie (§3.1 eq. 4, §3.2 "Loss
+ * Weights"), each rounded once to fp32, into host memory out_host[N]. */
+tree_status_t tree_weights(const tree_plan_t* plan, float* out_host);
+
+/* Wait for `stream`, then read and clear the device status word of the
+ * current device: TREE_ERR_TIMEOUT if a kernel gave up a bounded wait since
+ * the last check, TREE_ERR_CUDA on a CUDA error, else TREE_OK. */
+tree_status_t tree_status_sync(tree_stream_t stream);
+
+/* Message for the last failing call on this thread ("" if none). */
+const char* tree_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREEATTN_H */

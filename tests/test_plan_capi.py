@@ -1,0 +1,130 @@
+"""The C++ plan builder (through the C-ABI) against the oracle, bit for bit, on CPU.
+
+Also: the library loads and exports every symbol the public header declares,
+error statuses for invalid tries, and the g/K weights.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import treegen
+import tree_packed_attention_gb300 as tpa
+from oracle import tiles as TL
+from oracle import trie as T
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_library_exports_every_declared_symbol():
+    with open(os.path.join(ROOT, "include", "treeattn.h")) as f:
+        header = f.read()
+    declared = set(re.findall(r"^\S[^\n(]*?\b(tree_\w+)\(", header, flags=re.M))
+    assert declared == set(tpa.EXPORTS)
+    lib = ctypes.CDLL(tpa.LIB_PATH)
+    for name in declared:
+        assert getattr(lib, name) is not None
+
+
+def _assert_plan_equal(p, L):
+    plan = tpa.tree_plan_build(p, L)
+    ref = TL.plan_fields(p, L, 128, 128)
+    got = plan.fields()
+    for name in tpa.FIELDS:
+        assert got[name].dtype == np.int32
+        assert np.array_equal(got[name], ref[name]), name
+    info = plan.info
+    assert info["num_tokens"] == ref["num_tokens"]
+    assert info["num_segments"] == ref["num_segments"]
+    assert info["num_tries"] == ref["num_tries"]
+    assert info["visible_pairs"] == ref["visible_pairs"]
+    assert info["nnz_tiles"] == len(ref["qt_kt"])
+    assert info["num_pairs"] == len(ref["qp_ptr"]) - 1
+    w = tpa.tree_weights(plan)
+    assert np.array_equal(w.view(np.uint32), T.token_weights(p, L).view(np.uint32))
+    return plan
+
+
+@pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
+def test_workload_plans_bit_exact(index):
+    w = treegen.workload(index)
+    _assert_plan_equal(w.parents, w.lengths)
+
+
+def test_random_forests_bit_exact():
+    rng = np.random.default_rng(100)
+    for _ in range(60):
+        S = int(rng.integers(1, 40))
+        p, L = treegen.random_forest(rng, S, max_len=int(rng.integers(1, 300)),
+                                     n_roots=int(rng.integers(1, 5)))
+        _assert_plan_equal(p, L)
+
+
+def test_degenerate_tries_bit_exact():
+    cases = [
+        ([-1], [1]),                                     # a single token
+        ([-1], [128]),                                   # exactly one tile
+        ([-1], [129]),                                   # one tile plus one row
+        ([-1] + list(range(0, 299)), [1] * 300),         # deep chain of 1-token segments
+        ([-1] + list(range(0, 99)), [127] * 100),        # deep chain of 127-token segments
+        ([-1] + [0] * 1000, [3] + [1] * 1000),           # 1000-way fan-out
+        ([3, 3, 3, -1], [5, 7, 9, 11]),                  # root listed after its children
+        ([-1, -1, -1], [129, 127, 1]),                   # forest of chains around tile edges
+    ]
+    for p, L in cases:
+        _assert_plan_equal(np.array(p), np.array(L))
+
+
+def test_empty_plan():
+    plan = tpa.tree_plan_build(np.zeros(0, np.int32), np.zeros(0, np.int32))
+    assert plan.info["num_tokens"] == 0
+    assert plan.field("cu_seqlens").tolist() == [0]
+    assert tpa.tree_weights(plan).size == 0
+
+
+@pytest.mark.parametrize("parents,lengths,status", [
+    ([1, 0], [1, 1], "TREE_ERR_CYCLE"),
+    ([-1, 2, 1], [1, 1, 1], "TREE_ERR_CYCLE"),
+    ([-1, 5], [1, 1], "TREE_ERR_INVALID_ARG"),
+    ([-2], [1], "TREE_ERR_INVALID_ARG"),
+    ([0], [1], "TREE_ERR_INVALID_ARG"),
+    ([-1, 0], [1, 0], "TREE_ERR_EMPTY_SEGMENT"),
+    ([-1], [-3], "TREE_ERR_EMPTY_SEGMENT"),
+    ([-1, 0, 0], [2**30, 2**30, 2**30], "TREE_ERR_OVERFLOW"),
+])
+def test_invalid_tries_are_rejected(parents, lengths, status):
+    with pytest.raises(tpa.TreeAttnError) as e:
+        tpa.tree_plan_build(parents, lengths)
+    assert e.value.status_name == status
+    if status != "TREE_ERR_OVERFLOW":
+        kind = {"TREE_ERR_CYCLE": "cycle", "TREE_ERR_INVALID_ARG": "invalid",
+                "TREE_ERR_EMPTY_SEGMENT": "empty"}[status]
+        with pytest.raises(T.TrieError) as e2:
+            T.validate(parents, lengths)
+        assert e2.value.kind == kind
+
+
+def test_field_size_mismatch_and_null_args():
+    plan = tpa.tree_plan_build([-1, 0], [3, 4])
+    buf = np.zeros(5, np.int32)
+    st = tpa.lib.tree_plan_get(plan.handle, 0, buf.ctypes.data, 4)
+    assert st == 1
+    assert b"bytes" in tpa.lib.tree_last_error()
+    h = ctypes.c_void_p()
+    assert tpa.lib.tree_plan_build(None, None, 3, ctypes.byref(h)) == 1
+
+
+def test_device_calls_without_device_copy_are_rejected():
+    """Host-side validation runs before any launch (no GPU needed)."""
+    plan = tpa.tree_plan_build([-1], [8])
+    # D = 96 is rejected before the device is touched
+    st = tpa.lib.tree_attn_fwd(plan.handle, 16, 16, 16, 16, 16, 1, 1, 96, 1, 0.0, None)
+    assert st == 5
+    st = tpa.lib.tree_attn_fwd(plan.handle, 16, 16, 16, 16, 16, 3, 2, 128, 1, 0.0, None)
+    assert st == 1
+    st = tpa.lib.tree_attn_fwd(plan.handle, 17, 16, 16, 16, 16, 1, 1, 128, 1, 0.0, None)
+    assert st == 1  # misaligned pointer
+    ws = tpa.lib.tree_attn_bwd_workspace_bytes(plan.handle, 2, 128, 1)
+    assert ws >= 8 * 2 * 128 * 4

@@ -1,0 +1,213 @@
+"""Tree-packed attention on one GB300: Python binding of libtreeattn.
+
+The calls mirror the C-ABI in ``include/treeattn.h``:
+
+* ``tree_plan_build(segment_parents, segment_lengths) -> Plan`` -- DFS layout,
+  ancestor lists, per-key visibility bounds and the tile visibility map of a
+  trie (or forest) of token segments ("Tree Training", arXiv 2511.00413,
+  §3.1 eq. 8, §3.2 eq. 9, App. A.1);
+* ``tree_attn_fwd(plan, q, k, v) -> (o, lse)``;
+* ``tree_attn_bwd(plan, do, q, k, v, o, lse) -> (dq, dk, dv)``;
+* ``tree_weights(plan) -> w`` with w_t = g_t / K (§3.1 eq. 4).
+
+Tensors are torch CUDA tensors in DFS token order: q/o/do [N, hq, D], k/v
+[N, hkv, D], lse [hq, N] fp32. torch provides device memory and the current
+stream; every step of the computation runs in the library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import numpy as np
+
+from ._lib import (DTYPE_BF16, DTYPE_F32, EXPORTS, FIELDS, LIB_PATH, PlanInfo, TreeAttnError,
+                   check, lib)
+
+__all__ = [
+    "Plan", "tree_plan_build", "tree_attn_fwd", "tree_attn_bwd", "tree_attn_bwd_workspace_bytes",
+    "tree_weights", "tree_status_sync", "TreeAttnFn", "tree_attention", "TreeAttnError",
+    "FIELDS", "EXPORTS", "LIB_PATH",
+]
+
+
+class Plan:
+    """Owns a ``tree_plan_t``: the host plan and, once uploaded, its device copy."""
+
+    def __init__(self, segment_parents, segment_lengths):
+        parents = np.ascontiguousarray(np.asarray(segment_parents, dtype=np.int32))
+        lengths = np.ascontiguousarray(np.asarray(segment_lengths, dtype=np.int32))
+        if parents.shape != lengths.shape or parents.ndim != 1:
+            raise ValueError("segment_parents and segment_lengths must be 1-D and of equal length")
+        h = C.c_void_p()
+        check(lib.tree_plan_build(parents.ctypes.data, lengths.ctypes.data, int(parents.size),
+                                  C.byref(h)))
+        self._h = h
+        info = PlanInfo()
+        check(lib.tree_plan_info(self._h, C.byref(info)))
+        self.info = {name: int(getattr(info, name)) for name, _ in PlanInfo._fields_}
+        self.num_tokens = self.info["num_tokens"]
+
+    @property
+    def handle(self):
+        return self._h
+
+    def field(self, name: str) -> np.ndarray:
+        idx = FIELDS.index(name)
+        n = C.c_int64()
+        check(lib.tree_plan_field_len(self._h, idx, C.byref(n)))
+        out = np.empty(n.value, dtype=np.int32)
+        check(lib.tree_plan_get(self._h, idx, out.ctypes.data, out.nbytes))
+        return out
+
+    def fields(self) -> dict:
+        return {name: self.field(name) for name in FIELDS}
+
+    def to_device(self, stream=None) -> "Plan":
+        check(lib.tree_plan_to_device(self._h, _stream_ptr(stream)))
+        return self
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            lib.tree_plan_destroy(h)
+            self._h = None
+
+
+def tree_plan_build(segment_parents, segment_lengths) -> Plan:
+    return Plan(segment_parents, segment_lengths)
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        import torch
+
+        if not torch.cuda.is_available():
+            return None
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(int(getattr(stream, "cuda_stream", stream)))
+
+
+def _dtype_code(t):
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _check_tensor(name, t, shape, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+
+
+def tree_attn_fwd(plan: Plan, q, k, v, softmax_scale: float = 0.0, out=None, lse=None, stream=None):
+    """(o, lse) of tree attention. ``softmax_scale`` 0 means 1/sqrt(D)."""
+    import torch
+
+    N, hq, D = q.shape
+    hkv = k.shape[1]
+    if N != plan.num_tokens:
+        raise ValueError(f"q has {N} tokens, the plan {plan.num_tokens}")
+    _check_tensor("q", q, (N, hq, D))
+    _check_tensor("k", k, (N, hkv, D), q.dtype)
+    _check_tensor("v", v, (N, hkv, D), q.dtype)
+    o = torch.empty_like(q) if out is None else out
+    lse_t = torch.empty(hq, N, dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_tensor("o", o, (N, hq, D), q.dtype)
+    _check_tensor("lse", lse_t, (hq, N), torch.float32)
+    s = _stream_ptr(stream)
+    plan.to_device(s)
+    check(lib.tree_attn_fwd(plan.handle, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            lse_t.data_ptr(), hq, hkv, D, _dtype_code(q), float(softmax_scale), s))
+    return o, lse_t
+
+
+def tree_attn_bwd_workspace_bytes(plan: Plan, hq: int, head_dim: int, dtype) -> int:
+    import torch
+
+    code = DTYPE_BF16 if dtype == torch.bfloat16 else DTYPE_F32
+    return int(lib.tree_attn_bwd_workspace_bytes(plan.handle, hq, head_dim, code))
+
+
+def tree_attn_bwd(plan: Plan, do, q, k, v, o, lse, softmax_scale: float = 0.0, grad_dtype=None,
+                  workspace=None, out=None, stream=None):
+    """(dq, dk, dv) of tree attention. ``grad_dtype`` defaults to q's dtype."""
+    import torch
+
+    N, hq, D = q.shape
+    hkv = k.shape[1]
+    if N != plan.num_tokens:
+        raise ValueError(f"q has {N} tokens, the plan {plan.num_tokens}")
+    for name, t, shp in (("do", do, (N, hq, D)), ("q", q, (N, hq, D)), ("k", k, (N, hkv, D)),
+                         ("v", v, (N, hkv, D)), ("o", o, (N, hq, D))):
+        _check_tensor(name, t, shp, q.dtype)
+    _check_tensor("lse", lse, (hq, N), torch.float32)
+    gdt = q.dtype if grad_dtype is None else grad_dtype
+    if out is None:
+        dq = torch.empty(N, hq, D, dtype=gdt, device=q.device)
+        dk = torch.empty(N, hkv, D, dtype=gdt, device=q.device)
+        dv = torch.empty(N, hkv, D, dtype=gdt, device=q.device)
+    else:
+        dq, dk, dv = out
+    nbytes = tree_attn_bwd_workspace_bytes(plan, hq, D, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    s = _stream_ptr(stream)
+    plan.to_device(s)
+    check(lib.tree_attn_bwd(plan.handle, do.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                            o.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                            dv.data_ptr(), hq, hkv, D, _dtype_code(q),
+                            DTYPE_BF16 if gdt == torch.bfloat16 else DTYPE_F32,
+                            float(softmax_scale), workspace.data_ptr(), workspace.numel(), s))
+    return dq, dk, dv
+
+
+def tree_weights(plan: Plan) -> np.ndarray:
+    """Per-token loss weights g_t / K as fp32 (host)."""
+    out = np.empty(plan.num_tokens, dtype=np.float32)
+    check(lib.tree_weights(plan.handle, out.ctypes.data))
+    return out
+
+
+def tree_status_sync(stream=None) -> None:
+    """Wait for the stream; raise if a kernel gave up a bounded wait."""
+    check(lib.tree_status_sync(_stream_ptr(stream)))
+
+
+def _make_autograd():
+    import torch
+
+    class TreeAttnFn(torch.autograd.Function):
+        """Autograd wrapper: forward/backward both run the library's kernels."""
+
+        @staticmethod
+        def forward(ctx, q, k, v, plan, softmax_scale=0.0):
+            o, lse = tree_attn_fwd(plan, q, k, v, softmax_scale)
+            ctx.save_for_backward(q, k, v, o, lse)
+            ctx.plan = plan
+            ctx.scale = softmax_scale
+            return o
+
+        @staticmethod
+        def backward(ctx, do):
+            q, k, v, o, lse = ctx.saved_tensors
+            dq, dk, dv = tree_attn_bwd(ctx.plan, do.contiguous(), q, k, v, o, lse, ctx.scale)
+            return dq, dk, dv, None, None
+
+    return TreeAttnFn
+
+
+TreeAttnFn = _make_autograd()
+
+
+def tree_attention(q, k, v, plan: Plan, softmax_scale: float = 0.0):
+    """Differentiable tree attention (o only)."""
+    return TreeAttnFn.apply(q, k, v, plan, softmax_scale)

@@ -1,0 +1,218 @@
+// C-ABI glue: plan upload, argument validation and dispatch to the kernels,
+// the device status word.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "kernels.h"
+#include "plan_internal.h"
+
+namespace treeattn {
+
+// Set by kernels that give up a bounded wait; read and cleared by tree_status_sync.
+__device__ int g_status_word = 0;
+
+namespace {
+
+tree_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(TREE_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+int* status_ptr() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct FieldSlot {
+  tree_plan_field_t f;
+  const int32_t** dst;
+};
+
+void free_device(tree_plan* p) {
+  if (!p->dev.block) return;
+  int cur = -1;
+  cudaGetDevice(&cur);
+  if (cur != p->dev.device) cudaSetDevice(p->dev.device);
+  cudaFree(p->dev.block);  // synchronizes the device
+  if (cur >= 0 && cur != p->dev.device) cudaSetDevice(cur);
+  p->dev = DevicePlan{};
+}
+
+tree_status_t check_plan_on_device(const tree_plan* p) {
+  if (p->N == 0) return TREE_OK;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return fail(TREE_ERR_CUDA, "no CUDA device");
+  if (!p->dev.block || p->dev.device != cur)
+    return fail(TREE_ERR_NOT_ON_DEVICE, "call tree_plan_to_device on the current device first");
+  return TREE_OK;
+}
+
+tree_status_t check_heads(int32_t hq, int32_t hkv, int32_t d, tree_dtype_t dtype) {
+  if (hq <= 0 || hkv <= 0 || hq % hkv != 0)
+    return fail(TREE_ERR_INVALID_ARG, "need hq > 0, hkv > 0 and hq % hkv == 0");
+  if (hq > 65535) return fail(TREE_ERR_UNSUPPORTED, "hq > 65535");
+  if (dtype == TREE_DTYPE_F32) {
+    if (d != 64 && d != 128) return fail(TREE_ERR_UNSUPPORTED, "fp32 path needs head_dim 64 or 128");
+  } else if (dtype == TREE_DTYPE_BF16) {
+    if (d != 128) return fail(TREE_ERR_UNSUPPORTED, "bf16 path needs head_dim 128");
+  } else {
+    return fail(TREE_ERR_INVALID_ARG, "unknown dtype");
+  }
+  return TREE_OK;
+}
+
+float resolve_scale(float s, int d) { return s == 0.f ? 1.f / std::sqrt(static_cast<float>(d)) : s; }
+
+}  // namespace
+
+size_t bwd_workspace_bf16(int64_t n, int hq, int d) {
+  const int64_t acc = n * hq * d * 4;
+  const int64_t delta = n * hq * 4;
+  return static_cast<size_t>((acc + 255) / 256 * 256 + (delta + 255) / 256 * 256);
+}
+
+}  // namespace treeattn
+
+using namespace treeattn;
+
+extern "C" tree_status_t tree_plan_to_device(tree_plan_t* p, tree_stream_t stream) {
+  if (!p) return fail(TREE_ERR_INVALID_ARG, "NULL plan");
+  int cur = -1;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (p->dev.block && p->dev.device == cur) return TREE_OK;
+  free_device(p);
+  if (p->N == 0) return TREE_OK;
+  DevicePlan d;
+  const FieldSlot slots[] = {
+      {TREE_FIELD_KEY_END, &d.key_end},     {TREE_FIELD_QT_PTR, &d.qt_ptr},
+      {TREE_FIELD_QT_KT, &d.qt_kt},         {TREE_FIELD_QT_KIND, &d.qt_kind},
+      {TREE_FIELD_FWD_ORDER, &d.fwd_order}, {TREE_FIELD_QP_PTR, &d.qp_ptr},
+      {TREE_FIELD_QP_KT, &d.qp_kt},         {TREE_FIELD_QP_KIND, &d.qp_kind},
+      {TREE_FIELD_QP_ORDER, &d.qp_order},   {TREE_FIELD_KT_QLO, &d.kt_qlo},
+      {TREE_FIELD_KT_QHI, &d.kt_qhi},       {TREE_FIELD_BWD_ORDER, &d.bwd_order},
+  };
+  size_t offs[sizeof(slots) / sizeof(slots[0])];
+  size_t total = 0;
+  for (size_t s = 0; s < sizeof(slots) / sizeof(slots[0]); ++s) {
+    offs[s] = total;
+    total += (p->field[slots[s].f].size() * 4 + 255) / 256 * 256;
+  }
+  std::vector<uint8_t> host(total, 0);
+  for (size_t s = 0; s < sizeof(slots) / sizeof(slots[0]); ++s) {
+    const auto& v = p->field[slots[s].f];
+    if (!v.empty()) std::memcpy(host.data() + offs[s], v.data(), v.size() * 4);
+  }
+  void* block = nullptr;
+  e = cudaMalloc(&block, total);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(TREE_ERR_OOM, std::string("cudaMalloc of the plan: ") + cudaGetErrorString(e));
+  }
+  e = cudaMemcpyAsync(block, host.data(), total, cudaMemcpyHostToDevice,
+                      static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaFree(block);
+    return cuda_fail(e, "plan upload");
+  }
+  for (size_t s = 0; s < sizeof(slots) / sizeof(slots[0]); ++s)
+    *slots[s].dst = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(block) + offs[s]);
+  d.block = block;
+  d.bytes = total;
+  d.device = cur;
+  p->dev = d;
+  return TREE_OK;
+}
+
+extern "C" void tree_plan_destroy(tree_plan_t* p) {
+  if (!p) return;
+  free_device(p);
+  delete p;
+}
+
+extern "C" tree_status_t tree_attn_fwd(const tree_plan_t* p, const void* q, const void* k,
+                                       const void* v, void* o, float* lse, int32_t hq,
+                                       int32_t hkv, int32_t head_dim, tree_dtype_t dtype,
+                                       float softmax_scale, tree_stream_t stream) {
+  if (!p) return fail(TREE_ERR_INVALID_ARG, "NULL plan");
+  tree_status_t st = check_heads(hq, hkv, head_dim, dtype);
+  if (st != TREE_OK) return st;
+  if (!std::isfinite(softmax_scale)) return fail(TREE_ERR_INVALID_ARG, "softmax_scale not finite");
+  if (p->N == 0) return TREE_OK;
+  if (!q || !k || !v || !o || !lse) return fail(TREE_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(TREE_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if ((st = check_plan_on_device(p)) != TREE_OK) return st;
+  int* status = status_ptr();
+  if (!status) return fail(TREE_ERR_CUDA, "status word unavailable");
+  AttnArgs a{p, q, k, v, o, lse, hq, hkv, head_dim, resolve_scale(softmax_scale, head_dim),
+             static_cast<cudaStream_t>(stream), status};
+  cudaError_t e = dtype == TREE_DTYPE_F32 ? launch_fwd_f32(a) : launch_fwd_bf16(a);
+  if (e != cudaSuccess) return cuda_fail(e, "tree_attn_fwd launch");
+  return TREE_OK;
+}
+
+extern "C" size_t tree_attn_bwd_workspace_bytes(const tree_plan_t* p, int32_t hq, int32_t head_dim,
+                                                tree_dtype_t dtype) {
+  if (!p || hq <= 0 || head_dim <= 0) return 0;
+  return dtype == TREE_DTYPE_F32 ? bwd_workspace_f32(p->N, hq)
+                                 : bwd_workspace_bf16(p->N, hq, head_dim);
+}
+
+extern "C" tree_status_t tree_attn_bwd(const tree_plan_t* p, const void* dout, const void* q,
+                                       const void* k, const void* v, const void* o,
+                                       const float* lse, void* dq, void* dk, void* dv, int32_t hq,
+                                       int32_t hkv, int32_t head_dim, tree_dtype_t dtype,
+                                       tree_dtype_t grad_dtype, float softmax_scale,
+                                       void* workspace, size_t workspace_bytes,
+                                       tree_stream_t stream) {
+  if (!p) return fail(TREE_ERR_INVALID_ARG, "NULL plan");
+  tree_status_t st = check_heads(hq, hkv, head_dim, dtype);
+  if (st != TREE_OK) return st;
+  if (grad_dtype != TREE_DTYPE_F32 && grad_dtype != TREE_DTYPE_BF16)
+    return fail(TREE_ERR_INVALID_ARG, "unknown grad_dtype");
+  if (dtype == TREE_DTYPE_F32 && grad_dtype != TREE_DTYPE_F32)
+    return fail(TREE_ERR_INVALID_ARG, "fp32 inputs need fp32 gradients");
+  if (!std::isfinite(softmax_scale)) return fail(TREE_ERR_INVALID_ARG, "softmax_scale not finite");
+  if (p->N == 0) return TREE_OK;
+  const void* ptrs[] = {dout, q, k, v, o, lse, dq, dk, dv, workspace};
+  for (const void* x : ptrs) {
+    if (!x) return fail(TREE_ERR_INVALID_ARG, "NULL tensor or workspace pointer");
+    if (!aligned16(x)) return fail(TREE_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  }
+  const size_t need = tree_attn_bwd_workspace_bytes(p, hq, head_dim, dtype);
+  if (workspace_bytes < need)
+    return fail(TREE_ERR_INVALID_ARG, "workspace too small: need " + std::to_string(need) + " bytes");
+  if ((st = check_plan_on_device(p)) != TREE_OK) return st;
+  int* status = status_ptr();
+  if (!status) return fail(TREE_ERR_CUDA, "status word unavailable");
+  AttnBwdArgs a{p,  dout, q,   k,   v,        o,        lse,
+                dq, dk,   dv,  hq,  hkv,      head_dim, grad_dtype == TREE_DTYPE_F32,
+                resolve_scale(softmax_scale, head_dim), workspace, workspace_bytes,
+                static_cast<cudaStream_t>(stream), status};
+  cudaError_t e = dtype == TREE_DTYPE_F32 ? launch_bwd_f32(a) : launch_bwd_bf16(a);
+  if (e != cudaSuccess) return cuda_fail(e, "tree_attn_bwd launch");
+  return TREE_OK;
+}
+
+extern "C" tree_status_t tree_status_sync(tree_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (word != 0) {
+    const int zero = 0;
+    cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int));
+    return fail(TREE_ERR_TIMEOUT, "a kernel gave up a bounded wait (status " +
+                                      std::to_string(word) + ")");
+  }
+  return TREE_OK;
+}

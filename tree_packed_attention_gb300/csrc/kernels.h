@@ -1,0 +1,55 @@
+// Internal launcher declarations shared by the C-ABI glue and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "plan_internal.h"
+
+namespace treeattn {
+
+struct AttnArgs {
+  const tree_plan* plan;
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int hq, hkv, d;
+  float scale;  // softmax scale (already resolved; never 0)
+  cudaStream_t stream;
+  int* status;  // device status word
+};
+
+struct AttnBwdArgs {
+  const tree_plan* plan;
+  const void* dout;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  int hq, hkv, d;
+  bool grad_f32;  // gradients written as fp32 (else bf16)
+  float scale;
+  void* workspace;
+  size_t workspace_bytes;
+  cudaStream_t stream;
+  int* status;
+};
+
+// Workspace layouts.
+size_t bwd_workspace_f32(int64_t n, int hq);
+size_t bwd_workspace_bf16(int64_t n, int hq, int d);
+
+// fp32 CUDA-core path (any D in {64, 128}).
+cudaError_t launch_fwd_f32(const AttnArgs& a);
+cudaError_t launch_bwd_f32(const AttnBwdArgs& a);
+
+// bf16 tcgen05 path (D = 128).
+cudaError_t launch_fwd_bf16(const AttnArgs& a);
+cudaError_t launch_bwd_bf16(const AttnBwdArgs& a);
+
+}  // namespace treeattn

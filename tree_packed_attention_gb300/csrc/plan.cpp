@@ -1,0 +1,368 @@
+// Host plan builder: trie -> DFS layout, ancestors, g_n, K, position ids, the
+// per-key visibility bound and the tile visibility map.
+//
+// "Tree Training" (arXiv 2511.00413): §3.1 (trie, g_n, K), eq. 8 (DFS
+// serialization), eq. 9 (position ids), §3.2 "Attention Mask" and App. A.1
+// (ancestor segments in full, own segment causal; masked blocks skipped).
+//
+// Column form of the mask used here (a consequence of eq. 8's pre-order):
+// the rows that see key j (segment s) are exactly [j, subtree_end(s)), since
+// the subtree of s is one contiguous token range in DFS order. For a k-tile
+// the union of these row ranges is the single range [k0, max key_end), so
+// each k-tile is seen by one contiguous run of q-tiles starting at its own
+// diagonal tile.
+#include <algorithm>
+#include <cstring>
+#include <limits>
+#include <new>
+#include <numeric>
+
+#include "plan_internal.h"
+
+namespace treeattn {
+
+thread_local std::string g_last_error;
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+
+tree_status_t fail(tree_status_t st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+
+namespace {
+
+// Indices sorted by work, largest first; ties keep ascending index.
+std::vector<int32_t> lpt_order(const std::vector<int64_t>& work) {
+  std::vector<int32_t> idx(work.size());
+  std::iota(idx.begin(), idx.end(), 0);
+  std::stable_sort(idx.begin(), idx.end(),
+                   [&](int32_t a, int32_t b) { return work[a] > work[b]; });
+  return idx;
+}
+
+tree_status_t build(const int32_t* parents, const int32_t* lengths, int32_t S, tree_plan* p) {
+  auto& F = p->field;
+  // ---- validation
+  for (int32_t s = 0; s < S; ++s) {
+    if (parents[s] < -1 || parents[s] >= S || parents[s] == s)
+      return fail(TREE_ERR_INVALID_ARG, "segment " + std::to_string(s) + ": parent " +
+                                            std::to_string(parents[s]) + " out of range");
+  }
+  int64_t n_tokens = 0;
+  for (int32_t s = 0; s < S; ++s) {
+    if (lengths[s] < 1)
+      return fail(TREE_ERR_EMPTY_SEGMENT, "segment " + std::to_string(s) + " has " +
+                                              std::to_string(lengths[s]) + " tokens");
+    n_tokens += lengths[s];
+  }
+  if (n_tokens > std::numeric_limits<int32_t>::max() - kBlockM)
+    return fail(TREE_ERR_OVERFLOW, "more than 2^31-129 tokens");
+  const int32_t N = static_cast<int32_t>(n_tokens);
+
+  // ---- children (ascending id) and roots (ascending id)
+  std::vector<int32_t> child_ptr(S + 1, 0), child_idx(S);
+  std::vector<int32_t> roots;
+  for (int32_t s = 0; s < S; ++s) {
+    if (parents[s] < 0)
+      roots.push_back(s);
+    else
+      child_ptr[parents[s] + 1]++;
+  }
+  for (int32_t s = 0; s < S; ++s) child_ptr[s + 1] += child_ptr[s];
+  {
+    std::vector<int32_t> fill(child_ptr.begin(), child_ptr.end() - 1);
+    for (int32_t s = 0; s < S; ++s)
+      if (parents[s] >= 0) child_idx[fill[parents[s]]++] = s;
+  }
+
+  // ---- pre-order (eq. 8): a node, then each child's subtree in ascending id
+  std::vector<int32_t>& order = F[TREE_FIELD_DFS_ORDER];
+  order.reserve(S);
+  {
+    std::vector<int32_t> stack;
+    for (auto it = roots.rbegin(); it != roots.rend(); ++it) stack.push_back(*it);
+    while (!stack.empty()) {
+      int32_t s = stack.back();
+      stack.pop_back();
+      order.push_back(s);
+      for (int32_t e = child_ptr[s + 1] - 1; e >= child_ptr[s]; --e) stack.push_back(child_idx[e]);
+    }
+  }
+  if (static_cast<int32_t>(order.size()) != S)
+    return fail(TREE_ERR_CYCLE, "some segment does not reach a root (cycle)");
+
+  // ---- per-segment fields
+  std::vector<int32_t>& seg_start = F[TREE_FIELD_SEG_START];
+  std::vector<int32_t>& depth = F[TREE_FIELD_DEPTH];
+  std::vector<int32_t>& sub_end = F[TREE_FIELD_SUBTREE_END];
+  std::vector<int32_t>& trie_id = F[TREE_FIELD_TRIE_ID];
+  std::vector<int32_t>& g = F[TREE_FIELD_G];
+  seg_start.assign(S, 0);
+  depth.assign(S, 0);
+  sub_end.assign(S, 0);
+  trie_id.assign(S, 0);
+  g.assign(S, 0);
+  std::vector<int32_t> pos_base(S, 0);
+  {
+    int32_t off = 0, root_rank = 0;
+    for (int32_t s : order) {
+      seg_start[s] = off;
+      off += lengths[s];
+      const int32_t par = parents[s];
+      if (par < 0) {
+        depth[s] = 0;
+        pos_base[s] = 0;
+        trie_id[s] = root_rank++;
+      } else {  // the parent precedes its children in pre-order
+        depth[s] = depth[par] + 1;
+        pos_base[s] = pos_base[par] + lengths[par];
+        trie_id[s] = trie_id[par];
+      }
+      sub_end[s] = seg_start[s] + lengths[s];
+    }
+  }
+  for (int32_t e = S - 1; e >= 0; --e) {  // reverse pre-order: children before parents
+    const int32_t s = order[e];
+    if (g[s] == 0) g[s] = 1;  // a leaf carries one path
+    const int32_t par = parents[s];
+    if (par >= 0) {
+      g[par] += g[s];
+      sub_end[par] = std::max(sub_end[par], sub_end[s]);
+    }
+  }
+  const int32_t R = static_cast<int32_t>(roots.size());
+  std::vector<int32_t>& cu = F[TREE_FIELD_CU_SEQLENS];
+  std::vector<int32_t>& K = F[TREE_FIELD_TRIE_PATHS];
+  cu.resize(R + 1);
+  K.resize(R);
+  for (int32_t r = 0; r < R; ++r) {
+    cu[r] = seg_start[roots[r]];
+    K[r] = g[roots[r]];
+  }
+  cu[R] = N;
+
+  // ---- ancestors (CSR by segment id, root first)
+  std::vector<int32_t>& anc_ptr = F[TREE_FIELD_ANC_PTR];
+  std::vector<int32_t>& anc_idx = F[TREE_FIELD_ANC_IDX];
+  anc_ptr.assign(S + 1, 0);
+  {
+    int64_t total = 0;
+    for (int32_t s = 0; s < S; ++s) {
+      total += depth[s];
+      if (total > std::numeric_limits<int32_t>::max())
+        return fail(TREE_ERR_OVERFLOW, "more than 2^31-1 ancestor entries");
+      anc_ptr[s + 1] = static_cast<int32_t>(total);
+    }
+    anc_idx.resize(static_cast<size_t>(total));
+    for (int32_t s = 0; s < S; ++s) {
+      int32_t w = anc_ptr[s + 1];
+      for (int32_t a = parents[s]; a >= 0; a = parents[a]) anc_idx[--w] = a;
+    }
+  }
+
+  // ---- per-token fields
+  std::vector<int32_t>& tok_seg = F[TREE_FIELD_TOKEN_SEG];
+  std::vector<int32_t>& pos_id = F[TREE_FIELD_POS_ID];
+  std::vector<int32_t>& key_end = F[TREE_FIELD_KEY_END];
+  tok_seg.resize(N);
+  pos_id.resize(N);
+  key_end.resize(N);
+  int64_t visible = 0;
+  for (int32_t s : order) {
+    const int32_t a = seg_start[s], L = lengths[s], ke = sub_end[s];
+    for (int32_t j = 0; j < L; ++j) {
+      tok_seg[a + j] = s;
+      pos_id[a + j] = pos_base[s] + j;
+      key_end[a + j] = ke;
+      visible += ke - (a + j);
+    }
+  }
+
+  // ---- tile map on the 128 x 128 grid
+  const int32_t Tq = (N + kBlockM - 1) / kBlockM;
+  const int32_t Tk = (N + kBlockN - 1) / kBlockN;
+  std::vector<int32_t>& kt_qlo = F[TREE_FIELD_KT_QLO];
+  std::vector<int32_t>& kt_qhi = F[TREE_FIELD_KT_QHI];
+  kt_qlo.resize(Tk);
+  kt_qhi.resize(Tk);
+  std::vector<int32_t> min_ke(Tk), max_ke(Tk);
+  for (int32_t kt = 0; kt < Tk; ++kt) {
+    const int32_t j0 = kt * kBlockN, j1 = std::min(N, j0 + kBlockN);
+    int32_t lo = key_end[j0], hi = key_end[j0];
+    for (int32_t j = j0 + 1; j < j1; ++j) {
+      lo = std::min(lo, key_end[j]);
+      hi = std::max(hi, key_end[j]);
+    }
+    min_ke[kt] = lo;
+    max_ke[kt] = hi;
+    kt_qlo[kt] = kt;                               // the diagonal tile: every key sees itself
+    kt_qhi[kt] = (hi - 1) / kBlockM + 1;           // the last row that sees a key of the tile
+  }
+  std::vector<int32_t>& qt_ptr = F[TREE_FIELD_QT_PTR];
+  std::vector<int32_t>& qt_kt = F[TREE_FIELD_QT_KT];
+  std::vector<int32_t>& qt_kind = F[TREE_FIELD_QT_KIND];
+  qt_ptr.assign(Tq + 1, 0);
+  int64_t nnz = 0;
+  for (int32_t kt = 0; kt < Tk; ++kt) {
+    for (int32_t qt = kt_qlo[kt]; qt < kt_qhi[kt]; ++qt) qt_ptr[qt + 1]++;
+    nnz += kt_qhi[kt] - kt_qlo[kt];
+  }
+  if (nnz > std::numeric_limits<int32_t>::max()) return fail(TREE_ERR_OVERFLOW, "too many tiles");
+  for (int32_t qt = 0; qt < Tq; ++qt) qt_ptr[qt + 1] += qt_ptr[qt];
+  qt_kt.resize(nnz);
+  qt_kind.resize(nnz);
+  {
+    std::vector<int32_t> fill(qt_ptr.begin(), qt_ptr.end() - 1);
+    for (int32_t kt = 0; kt < Tk; ++kt) {  // ascending kt -> ascending lists
+      for (int32_t qt = kt_qlo[kt]; qt < kt_qhi[kt]; ++qt) {
+        const int32_t r1 = (qt + 1) * kBlockM;
+        // FULL: all keys precede all rows, every row below every key's bound, tile inside N
+        const bool full = kt < qt && r1 <= N && min_ke[kt] >= r1;
+        const int32_t e = fill[qt]++;
+        qt_kt[e] = kt;
+        qt_kind[e] = full ? kFull : kPartial;
+      }
+    }
+  }
+
+  // ---- q-tile pair union lists (q-tiles 2p and 2p+1)
+  const int32_t P = (Tq + 1) / 2;
+  std::vector<int32_t>& qp_ptr = F[TREE_FIELD_QP_PTR];
+  std::vector<int32_t>& qp_kt = F[TREE_FIELD_QP_KT];
+  std::vector<int32_t>& qp_kind = F[TREE_FIELD_QP_KIND];
+  qp_ptr.assign(P + 1, 0);
+  std::vector<int64_t> pair_work(P, 0);
+  for (int32_t pr = 0; pr < P; ++pr) {
+    const int32_t q0 = 2 * pr, q1 = 2 * pr + 1;
+    int32_t a = qt_ptr[q0], ae = qt_ptr[q0 + 1];
+    int32_t b = q1 < Tq ? qt_ptr[q1] : 0, be = q1 < Tq ? qt_ptr[q1 + 1] : 0;
+    pair_work[pr] = (ae - a) + (be - b);
+    while (a < ae || b < be) {
+      int32_t kt, k0 = kEmpty, k1 = kEmpty;
+      if (b >= be || (a < ae && qt_kt[a] < qt_kt[b])) {
+        kt = qt_kt[a];
+        k0 = qt_kind[a++];
+      } else if (a >= ae || qt_kt[b] < qt_kt[a]) {
+        kt = qt_kt[b];
+        k1 = qt_kind[b++];
+      } else {
+        kt = qt_kt[a];
+        k0 = qt_kind[a++];
+        k1 = qt_kind[b++];
+      }
+      qp_kt.push_back(kt);
+      qp_kind.push_back(k0 | (k1 << 2));
+    }
+    qp_ptr[pr + 1] = static_cast<int32_t>(qp_kt.size());
+  }
+
+  // ---- work orders, longest first
+  {
+    std::vector<int64_t> w(Tq);
+    for (int32_t qt = 0; qt < Tq; ++qt) w[qt] = qt_ptr[qt + 1] - qt_ptr[qt];
+    F[TREE_FIELD_FWD_ORDER] = lpt_order(w);
+    std::vector<int64_t> wb(Tk);
+    for (int32_t kt = 0; kt < Tk; ++kt) wb[kt] = kt_qhi[kt] - kt_qlo[kt];
+    F[TREE_FIELD_BWD_ORDER] = lpt_order(wb);
+    F[TREE_FIELD_QP_ORDER] = lpt_order(pair_work);
+  }
+
+  p->N = N;
+  p->S = S;
+  p->R = R;
+  p->Tq = Tq;
+  p->Tk = Tk;
+  p->P = P;
+  p->visible_pairs = visible;
+  return TREE_OK;
+}
+
+}  // namespace
+}  // namespace treeattn
+
+using namespace treeattn;
+
+extern "C" tree_status_t tree_plan_build(const int32_t* segment_parents,
+                                         const int32_t* segment_lengths, int32_t num_segments,
+                                         tree_plan_t** out) {
+  if (!out) return fail(TREE_ERR_INVALID_ARG, "out is NULL");
+  if (num_segments < 0) return fail(TREE_ERR_INVALID_ARG, "num_segments < 0");
+  if (num_segments > 0 && (!segment_parents || !segment_lengths))
+    return fail(TREE_ERR_INVALID_ARG, "NULL parents or lengths");
+  tree_plan* p = new (std::nothrow) tree_plan();
+  if (!p) return fail(TREE_ERR_OOM, "out of host memory");
+  tree_status_t st;
+  try {
+    st = build(segment_parents, segment_lengths, num_segments, p);
+  } catch (const std::bad_alloc&) {
+    st = fail(TREE_ERR_OOM, "out of host memory");
+  }
+  if (st != TREE_OK) {
+    delete p;
+    return st;
+  }
+  *out = p;
+  set_error("");
+  return TREE_OK;
+}
+
+extern "C" tree_status_t tree_plan_info(const tree_plan_t* p, tree_plan_info_t* out) {
+  if (!p || !out) return fail(TREE_ERR_INVALID_ARG, "NULL plan or out");
+  out->num_tokens = p->N;
+  out->num_segments = p->S;
+  out->num_tries = p->R;
+  out->block_m = kBlockM;
+  out->block_n = kBlockN;
+  out->num_q_tiles = p->Tq;
+  out->num_k_tiles = p->Tk;
+  out->nnz_tiles = static_cast<int64_t>(p->field[TREE_FIELD_QT_KT].size());
+  out->num_pairs = p->P;
+  out->nnz_pair_tiles = static_cast<int64_t>(p->field[TREE_FIELD_QP_KT].size());
+  out->num_ancestors = static_cast<int64_t>(p->field[TREE_FIELD_ANC_IDX].size());
+  out->visible_pairs = p->visible_pairs;
+  return TREE_OK;
+}
+
+extern "C" tree_status_t tree_plan_field_len(const tree_plan_t* p, tree_plan_field_t f,
+                                             int64_t* out) {
+  if (!p || !out) return fail(TREE_ERR_INVALID_ARG, "NULL plan or out");
+  if (static_cast<int>(f) < 0 || f >= TREE_FIELD_COUNT)
+    return fail(TREE_ERR_INVALID_ARG, "unknown field");
+  *out = static_cast<int64_t>(p->field[f].size());
+  return TREE_OK;
+}
+
+extern "C" tree_status_t tree_plan_get(const tree_plan_t* p, tree_plan_field_t f, void* dst,
+                                       size_t bytes) {
+  if (!p) return fail(TREE_ERR_INVALID_ARG, "NULL plan");
+  if (static_cast<int>(f) < 0 || f >= TREE_FIELD_COUNT)
+    return fail(TREE_ERR_INVALID_ARG, "unknown field");
+  const auto& v = p->field[f];
+  if (bytes != v.size() * sizeof(int32_t))
+    return fail(TREE_ERR_INVALID_ARG, "field has " + std::to_string(v.size() * 4) +
+                                          " bytes, got " + std::to_string(bytes));
+  if (!v.empty()) {
+    if (!dst) return fail(TREE_ERR_INVALID_ARG, "NULL dst");
+    std::memcpy(dst, v.data(), bytes);
+  }
+  return TREE_OK;
+}
+
+extern "C" tree_status_t tree_weights(const tree_plan_t* p, float* out_host) {
+  if (!p) return fail(TREE_ERR_INVALID_ARG, "NULL plan");
+  if (p->N > 0 && !out_host) return fail(TREE_ERR_INVALID_ARG, "NULL out");
+  const auto& seg = p->field[TREE_FIELD_TOKEN_SEG];
+  const auto& g = p->field[TREE_FIELD_G];
+  const auto& trie = p->field[TREE_FIELD_TRIE_ID];
+  const auto& K = p->field[TREE_FIELD_TRIE_PATHS];
+  for (int32_t t = 0; t < p->N; ++t) {
+    const int32_t s = seg[t];
+    // g and K are below 2^31; the fp64 quotient rounded to fp32 is the
+    // correctly rounded fp32 quotient when both are below 2^24 (53 >= 2*24+2).
+    out_host[t] = static_cast<float>(static_cast<double>(g[s]) / static_cast<double>(K[trie[s]]));
+  }
+  return TREE_OK;
+}
+
+extern "C" const char* tree_last_error(void) { return g_last_error.c_str(); }

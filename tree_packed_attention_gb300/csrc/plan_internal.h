@@ -1,0 +1,52 @@
+// Internal definition of the plan object shared by the host plan builder and
+// the kernel launchers. Not part of the public C-ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/treeattn.h"
+
+namespace treeattn {
+
+constexpr int kBlockM = 128;  // query rows per tile
+constexpr int kBlockN = 128;  // keys per tile
+
+enum TileKind : int32_t { kEmpty = 0, kPartial = 1, kFull = 2 };
+
+// Device copy of the fields the kernels read (one allocation, int32 arrays).
+struct DevicePlan {
+  int device = -1;
+  void* block = nullptr;
+  size_t bytes = 0;
+  const int32_t* key_end = nullptr;    // [N]
+  const int32_t* qt_ptr = nullptr;     // [Tq+1]
+  const int32_t* qt_kt = nullptr;      // [nnz]
+  const int32_t* qt_kind = nullptr;    // [nnz]
+  const int32_t* fwd_order = nullptr;  // [Tq]
+  const int32_t* qp_ptr = nullptr;     // [P+1]
+  const int32_t* qp_kt = nullptr;      // [nnz_pairs]
+  const int32_t* qp_kind = nullptr;    // [nnz_pairs]
+  const int32_t* qp_order = nullptr;   // [P]
+  const int32_t* kt_qlo = nullptr;     // [Tk]
+  const int32_t* kt_qhi = nullptr;     // [Tk]
+  const int32_t* bwd_order = nullptr;  // [Tk]
+};
+
+}  // namespace treeattn
+
+struct tree_plan {
+  int32_t N = 0, S = 0, R = 0;
+  int32_t Tq = 0, Tk = 0, P = 0;
+  int64_t visible_pairs = 0;
+  std::vector<int32_t> field[TREE_FIELD_COUNT];
+  treeattn::DevicePlan dev;
+};
+
+namespace treeattn {
+// Thread-local error message used by every C-ABI call.
+void set_error(const std::string& msg);
+tree_status_t fail(tree_status_t st, const std::string& msg);
+}  // namespace treeattn
