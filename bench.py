@@ -1,0 +1,343 @@
+"""Benchmark: tree-packed attention forward + backward on one GB300.
+
+A step is one tree_attn_fwd plus one tree_attn_bwd over one synthetic batch
+(the whole hot path: the plan is built once per batch, outside the timed
+region, as the pages build it once per forward on the host). The headline
+workload is the packed batch of 32 GRPO-shaped tries, 131,072 tokens, 64 q
+heads / 8 kv heads, head_dim 128, bf16.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5] [--impl reference]
+
+Prints one JSON line. ``value`` is visible-pair TFLOP/s of fwd+bwd
+((4 + 10) * D * Hq * visible pairs per step), summed over ranks; inputs are
+resident in HBM and larger than L2, and L2 is also flushed between steps.
+``e2e`` is the same metric with host (pinned) buffers: the step's inputs are
+copied host->device and all its outputs device->host inside the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tree-attn fwd+bwd visible-pair TFLOP/s and tokens/s on 1 GB300; % of bf16 peak"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return FALLBACK_PEAKS, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+        return dist, dist.get_rank(), ws
+    return None, 0, 1
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_sample(workload_index: int, seconds_hint: float = 20.0):
+    """Time the CPU oracle (fp64) on a bounded sample of the workload.
+
+    The sample is one trie of the workload (the first root's subtree) with one
+    kv-head group (hq/hkv q heads, one kv head): full forward and backward.
+    Returns (visible-pair TFLOP/s, tokens/s, description, threads).
+    """
+    import numpy as np
+    import torch
+
+    import treegen
+    from oracle import attention as A
+    from oracle import mask as M
+
+    w = treegen.workload(workload_index)
+    parents = np.asarray(w.parents)
+    roots = np.flatnonzero(parents == -1)
+    # the first trie: every segment whose root is roots[0]
+    def root_of(s):
+        while parents[s] != -1:
+            s = parents[s]
+        return s
+
+    members = [s for s in range(len(parents)) if root_of(s) == roots[0]]
+    remap = {s: n for n, s in enumerate(members)}
+    sub_p = np.array([-1 if parents[s] == -1 else remap[parents[s]] for s in members], np.int32)
+    sub_l = np.asarray(w.lengths)[members].astype(np.int32)
+    g = w.hq // w.hkv
+    n = int(sub_l.sum())
+    q, k, v, do = treegen.draw_tensors(n, g, 1, w.head_dim, w.dtype, seed=0)
+    threads = len(os.sched_getaffinity(0))
+    torch.set_num_threads(threads)
+    pvis = M.TrieView(sub_p, sub_l).visible_count()
+    t0 = time.perf_counter()
+    A.forward(q, k, v, sub_p, sub_l)
+    A.backward(q, k, v, do, sub_p, sub_l)
+    dt = time.perf_counter() - t0
+    flops = 14.0 * w.head_dim * g * pvis
+    desc = (f"one trie of the workload ({n} tokens, {len(members)} segments) x one kv group "
+            f"({g} q heads, 1 kv head), fp64 forward + backward")
+    return flops / dt / 1e12, n / dt, desc, threads, dt
+
+
+def reference_arm(args):
+    """The CPU oracle as the reference arm: each step is the bounded sample above."""
+    dist, rank, world = None, int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import treegen
+
+    w = treegen.workload(args.workload)
+    vals, toks, times = [], [], []
+    desc, threads = "", 0
+    for _ in range(args.warmup):
+        cpu_oracle_sample(args.workload)
+    for _ in range(args.steps):
+        v, t, desc, threads, dt = cpu_oracle_sample(args.workload)
+        vals.append(v)
+        toks.append(t)
+        times.append(dt)
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "tokens_per_s": statistics.mean(toks),
+        "config": {"workload": w.name, "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def gpu_arm(args):
+    import numpy as np
+    import torch
+
+    import treegen
+    import tree_packed_attention_gb300 as tpa
+
+    dist, rank, world = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = treegen.workload(args.workload)
+    N, hq, hkv, D = w.num_tokens, w.hq, w.hkv, w.head_dim
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    t0 = time.perf_counter()
+    plan = tpa.tree_plan_build(w.parents, w.lengths)
+    plan_ms = 1e3 * (time.perf_counter() - t0)
+    plan.to_device()
+    pvis = plan.info["visible_pairs"]
+    flops_fwd = 4.0 * D * hq * pvis
+    flops_bwd = 10.0 * D * hq * pvis
+
+    # Seeded synthetic inputs, N(0,1), drawn on the device (one generator per rank).
+    gen = torch.Generator(device=dev).manual_seed(1000 + rank)
+    q = torch.randn(N, hq, D, generator=gen, device=dev, dtype=torch.float32).to(tdt)
+    k = torch.randn(N, hkv, D, generator=gen, device=dev, dtype=torch.float32).to(tdt)
+    v = torch.randn(N, hkv, D, generator=gen, device=dev, dtype=torch.float32).to(tdt)
+    do = torch.randn(N, hq, D, generator=gen, device=dev, dtype=torch.float32).to(tdt)
+    o = torch.empty_like(q)
+    lse = torch.empty(hq, N, dtype=torch.float32, device=dev)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    ws = torch.empty(tpa.tree_attn_bwd_workspace_bytes(plan, hq, D, tdt), dtype=torch.uint8, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        tpa.tree_attn_fwd(plan, q, k, v, out=o, lse=lse)
+        tpa.tree_attn_bwd(plan, do, q, k, v, o, lse, workspace=ws, out=(dq, dk, dv))
+
+    for _ in range(args.warmup):
+        step()
+    tpa.tree_status_sync()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for s in range(args.steps):
+            flush.zero_()  # L2 flush between timed steps (outside the events)
+            ev[s][0].record(stream)
+            tpa.tree_attn_fwd(plan, q, k, v, out=o, lse=lse)
+            ev[s][1].record(stream)
+            tpa.tree_attn_bwd(plan, do, q, k, v, o, lse, workspace=ws, out=(dq, dk, dv))
+            ev[s][2].record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    tpa.tree_status_sync()
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = statistics.mean(f + b for f, b in zip(fwd_ms, bwd_ms))
+    if dist:
+        t = torch.tensor([step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    value = world * (flops_fwd + flops_bwd) / (step_ms * 1e-3) / 1e12
+    tokens_s = world * N / (step_ms * 1e-3)
+
+    # End to end through the public API with pinned host buffers.
+    hq_pin = [x.cpu().pin_memory() for x in (q, k, v, do)]
+    out_pin = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o, lse, dq, dk, dv)]
+    h2d = sum(x.numel() * x.element_size() for x in hq_pin)
+    d2h = sum(x.numel() * x.element_size() for x in out_pin)
+    e2e_steps = max(1, min(args.steps, 5))
+
+    def e2e_step():
+        qq, kk, vv, dd = (x.to(dev, non_blocking=True) for x in hq_pin)
+        oo, ll = tpa.tree_attn_fwd(plan, qq, kk, vv)
+        g = tpa.tree_attn_bwd(plan, dd, qq, kk, vv, oo, ll, workspace=ws)
+        for dst, src in zip(out_pin, (oo, ll) + tuple(g)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * (flops_fwd + flops_bwd) / (e2e_ms * 1e-3) / 1e12
+
+    peaks, peak_kind = _peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    bwd_mean = statistics.mean(bwd_ms)
+    fwd_mean = statistics.mean(fwd_ms)
+    bwd_tf = flops_bwd / (bwd_mean * 1e-3) / 1e12
+    fwd_tf = flops_fwd / (fwd_mean * 1e-3) / 1e12
+    traffic = None
+    traffic_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(traffic_path):
+        with open(traffic_path) as f:
+            traffic = json.load(f).get(w.name, {}).get("bwd_bytes_per_launch")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v_cpu, t_cpu, desc, threads, dt = cpu_oracle_sample(args.workload)
+        cpu = {"value": v_cpu, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc,
+               "tokens_per_s": t_cpu, "seconds": dt}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "tokens": N, "hq": hq, "hkv": hkv, "head_dim": D,
+                       "visible_pairs": pvis, "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2, and L2 flushed between steps"},
+            "tokens_per_s": tokens_s,
+            "fraction_of_bf16_peak": value / world / peak,
+            "fwd": {"ms": fwd_mean, "tflops": fwd_tf, "frac": fwd_tf / peak, "launches": 1},
+            "bwd": {"ms": bwd_mean, "tflops": bwd_tf, "frac": bwd_tf / peak, "launches": 3},
+            "plan_build_ms": plan_ms,
+            "roofline": {"bound": "tensor", "kernel": "tree_attn_bwd (pre + main + finalize)",
+                         "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak,
+                         "peak_source": f"{peak_kind} bf16 dense (burst)", "traffic": traffic},
+            "clocks": clocks.summary(),
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": 4 * args.steps,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

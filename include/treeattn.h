@@ -139,7 +139,7 @@ void tree_plan_destroy(tree_plan_t* plan);
  * Forward tree attention (§3.2 mask; App. A.1 block skipping).
  *   q [N,hq,D], k,v [N,hkv,D]: device, dtype `dtype`.
  *   o [N,hq,D] (device, dtype `dtype`), lse [hq,N] (device, fp32): written.
- *   softmax_scale: logits are scale * q.k; 0 selects 1/sqrt(D).
+ *   softmax_scale: logits are scale * q.k; 0 selects 1/sqrt(D); negative is invalid.
  * o_i = sum_j softmax_j(scale q_i.k_j over the keys visible to i) v_j and
  * lse_i = log sum_j exp(scale q_i.k_j). Requires hq % hkv == 0, D in {64,128}
  * for fp32 and D == 128 for bf16 (else TREE_ERR_UNSUPPORTED).

@@ -35,6 +35,23 @@ def _f64(x):
     return x.detach().to(torch.float64)
 
 
+class _Upcast:
+    """Index first, then upcast the slice to fp64 (no fp64 copy of a whole large tensor)."""
+
+    def __init__(self, x):
+        self.x = x.detach()
+        self.shape = x.shape
+
+    def __getitem__(self, idx):
+        return self.x[idx].to(torch.float64)
+
+
+def _lazy(x):
+    if isinstance(x, _Upcast):
+        return x
+    return x.detach() if x.dtype == torch.float64 else _Upcast(x)
+
+
 def _group(hq, hkv):
     if hq % hkv:
         raise ValueError("hq must be a multiple of hkv")
@@ -118,7 +135,7 @@ def forward(q, k, v, parents, lengths, scale=None, rows=None, view=None):
 
     Returns (o [len(rows), Hq, D], lse [Hq, len(rows)]) in the order of ``rows``.
     """
-    q, k, v = _f64(q), _f64(k), _f64(v)
+    q, k, v = _lazy(q), _lazy(k), _lazy(v)
     view = view or TrieView(parents, lengths)
     N, hq, D = q.shape
     G = _group(hq, k.shape[1])
@@ -174,7 +191,7 @@ def backward(q, k, v, do, parents, lengths, scale=None, view=None):
 
 def backward_rows(q, k, v, do, parents, lengths, rows, scale=None, view=None):
     """dq for the rows asked for only: [len(rows), Hq, D]."""
-    q, k, v, do = map(_f64, (q, k, v, do))
+    q, k, v, do = map(_lazy, (q, k, v, do))
     view = view or TrieView(parents, lengths)
     N, hq, D = q.shape
     G = _group(hq, k.shape[1])
@@ -210,7 +227,7 @@ def rows_seeing(view, j):
 
 def backward_keys(q, k, v, do, parents, lengths, keys, scale=None, view=None):
     """dk, dv for the keys asked for only: [len(keys), Hkv, D] each."""
-    q, k, v, do = map(_f64, (q, k, v, do))
+    q, k, v, do = map(_lazy, (q, k, v, do))
     view = view or TrieView(parents, lengths)
     N, hq, D = q.shape
     hkv = k.shape[1]

@@ -22,7 +22,7 @@ LIB = os.path.join(PKG, "libtreeattn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
                      "--expt-relaxed-constexpr", f"-I{INCLUDE}"]
-CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", f"-I{INCLUDE}"]
+CXX_FLAGS = ["-x", "c++", "-std=c++17", "-O2", "-fPIC"]  # host sources, driven through nvcc
 
 
 def _nvcc() -> str:
@@ -76,8 +76,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
             objs.append(obj)
             if src.endswith(".cu"):
                 cmd = [nvcc] + NVCC_FLAGS + (["-Xptxas", "-v"] if verbose else []) + ["-c", src, "-o", obj]
-            else:
-                cmd = ["g++"] + CXX_FLAGS + ["-c", src, "-o", obj]
+            else:  # host C++: nvcc drives the host compiler with the CUDA include path
+                cmd = [nvcc, "-x", "c++", "-std=c++17", "-O2", "-Xcompiler", "-fPIC",
+                       f"-I{INCLUDE}", "-c", src, "-o", obj]
             jobs.append(cmd)
         with ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
             logs = list(ex.map(_run, jobs))

@@ -71,10 +71,11 @@ float resolve_scale(float s, int d) { return s == 0.f ? 1.f / std::sqrt(static_c
 
 }  // namespace
 
+// fp32 dQ accumulator [n, hq, d], then Delta and lse*log2(e), each [hq, npad].
 size_t bwd_workspace_bf16(int64_t n, int hq, int d) {
+  const int64_t npad = (n + kBlockM - 1) / kBlockM * kBlockM;
   const int64_t acc = n * hq * d * 4;
-  const int64_t delta = n * hq * 4;
-  return static_cast<size_t>((acc + 255) / 256 * 256 + (delta + 255) / 256 * 256);
+  return static_cast<size_t>((acc + 255) / 256 * 256 + 2 * hq * npad * 4);
 }
 
 }  // namespace treeattn
@@ -144,7 +145,8 @@ extern "C" tree_status_t tree_attn_fwd(const tree_plan_t* p, const void* q, cons
   if (!p) return fail(TREE_ERR_INVALID_ARG, "NULL plan");
   tree_status_t st = check_heads(hq, hkv, head_dim, dtype);
   if (st != TREE_OK) return st;
-  if (!std::isfinite(softmax_scale)) return fail(TREE_ERR_INVALID_ARG, "softmax_scale not finite");
+  if (!std::isfinite(softmax_scale) || softmax_scale < 0.f)
+    return fail(TREE_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
   if (p->N == 0) return TREE_OK;
   if (!q || !k || !v || !o || !lse) return fail(TREE_ERR_INVALID_ARG, "NULL tensor pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
@@ -180,7 +182,8 @@ extern "C" tree_status_t tree_attn_bwd(const tree_plan_t* p, const void* dout, c
     return fail(TREE_ERR_INVALID_ARG, "unknown grad_dtype");
   if (dtype == TREE_DTYPE_F32 && grad_dtype != TREE_DTYPE_F32)
     return fail(TREE_ERR_INVALID_ARG, "fp32 inputs need fp32 gradients");
-  if (!std::isfinite(softmax_scale)) return fail(TREE_ERR_INVALID_ARG, "softmax_scale not finite");
+  if (!std::isfinite(softmax_scale) || softmax_scale < 0.f)
+    return fail(TREE_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
   if (p->N == 0) return TREE_OK;
   const void* ptrs[] = {dout, q, k, v, o, lse, dq, dk, dv, workspace};
   for (const void* x : ptrs) {

@@ -1,4 +1,500 @@
+// Forward tree attention, bf16 in / fp32 accumulate, on the sm_103a tensor
+// cores (tcgen05.mma with TMEM accumulators, TMA-staged operands).
+//
+// What it computes ("Tree Training", arXiv 2511.00413, §3.2 "Attention Mask"
+// and App. A.1): o_i = softmax over the keys visible to row i of scale*q_i.k_j,
+// times v, and lse_i = log sum_j exp(scale*q_i.k_j). Key j is visible to row i
+// iff j <= i < key_end[j]. Tiles with no visible pair are never loaded or
+// multiplied (the plan lists only non-empty tiles, as the FlashMask kernel of
+// App. A.1 skips masked blocks); FULL tiles skip the per-element mask.
+//
+// CTA organisation (one persistent CTA per SM, 384 threads):
+//   warp 0     TMA producer: the two Q tiles of a work item, then K/V tiles
+//              into a 2-stage ring (128 keys x 128 dims each, 128B-swizzled).
+//   warp 1     TMEM owner and MMA issuer (one thread issues tcgen05.mma).
+//   warps 4-7  softmax for Q slot 0;  warps 8-11 softmax for Q slot 1.
+// A work item is two 128-row Q tiles that share K/V: two q heads of one kv
+// group at the same q-tile (grouped heads), or q-tiles 2p and 2p+1 of one
+// head (else), walking the union of their tile lists.
+//
+// TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each. The softmax
+// warps read S (one row per thread), write P = exp2(S*c - m) as bf16 over the
+// first 64 columns of S, and the PV MMA reads P straight from TMEM. The MMA
+// order per tile is PV_s(t) then S_s(t+1), so when S_s(t+1) is complete the
+// previous PV into O_s is complete too and O_s may be rescaled in place.
+// The running max is updated lazily: O and l are rescaled only when the max
+// grows by more than 8 (log2 units), which keeps every P <= 2^8.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
 #include "kernels.h"
+#include "sm103_ptx.cuh"
+#include "tma_host.h"
+
 namespace treeattn {
-cudaError_t launch_fwd_bf16(const AttnArgs&) { return cudaErrorNotSupported; }
+namespace {
+
+using namespace dev;
+
+constexpr int kThreads = 384;
+constexpr int kStages = 2;
+constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one 128 x 128 bf16 operand tile
+constexpr uint32_t kHalfBytes = kTileBytes / 2;  // its 64-column half (one TMA box)
+constexpr uint32_t kSmemBytes = 1024 + 2 * kTileBytes + 2 * kStages * kTileBytes;
+constexpr float kRescaleThreshold = 8.0f;
+
+struct FwdParams {
+  const int32_t* key_end;
+  const int32_t* list_ptr;
+  const int32_t* list_kt;
+  const int32_t* list_kind;
+  const int32_t* order;
+  __nv_bfloat16* o;
+  float* lse;
+  int* status;
+  int N, hq, group, n_items, n_inner, mode, Tq;
+  float scale_log2;  // softmax scale * log2(e)
+};
+
+struct Item {
+  int qtile[2];
+  int head[2];
+  int kvh;
+  int beg, end;
+};
+
+// mode 0: two heads of one kv group at one q-tile; mode 1: q-tiles 2p, 2p+1 of one head.
+__device__ __forceinline__ Item decode_item(const FwdParams& p, int it) {
+  Item x;
+  const int idx = it / p.n_inner, inner = it % p.n_inner;
+  if (p.mode == 0) {
+    const int qt = p.order[idx];
+    x.qtile[0] = x.qtile[1] = qt;
+    x.head[0] = 2 * inner;
+    x.head[1] = 2 * inner + 1;
+    x.kvh = (2 * inner) / p.group;
+    x.beg = p.list_ptr[qt];
+    x.end = p.list_ptr[qt + 1];
+  } else {
+    const int pr = p.order[idx];
+    x.qtile[0] = 2 * pr;
+    x.qtile[1] = 2 * pr + 1;
+    x.head[0] = x.head[1] = inner;
+    x.kvh = inner / p.group;
+    x.beg = p.list_ptr[pr];
+    x.end = p.list_ptr[pr + 1];
+  }
+  return x;
 }
+
+// Tile kinds of both slots packed as kind0 | kind1 << 2 (0 empty, 1 partial, 2 full).
+__device__ __forceinline__ int kinds_at(const FwdParams& p, int t) {
+  const int k = p.list_kind[t];
+  return p.mode == 0 ? (k | (k << 2)) : k;
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          int* status) {
+  const bool ok = mbar_wait(bar, parity, abort, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// S = Q K^T over D = 128 (8 MMAs of K = 16); both operands K-major.
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+    mma_ss(d_tmem, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idesc,
+           kk > 0 ? 1u : 0u);
+  }
+}
+
+// O (+)= P V: P (128 x 128 keys, bf16) from TMEM, V (keys x D) MN-major in smem.
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr,
+                                         bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    mma_ts(d_tmem, p_tmem + kk * 8, sdesc_sw128(v_addr + kk * 2048, kHalfBytes, 1024), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tree_attn_fwd_sm103(const __grid_constant__ CUtensorMap map_q,
+                        const __grid_constant__ CUtensorMap map_k,
+                        const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;                   // 2 slots
+  uint8_t* sK = smem + 2 * kTileBytes;  // kStages
+  uint8_t* sV = sK + kStages * kTileBytes;
+
+  __shared__ uint64_t bar_q_full, bar_q_empty, bar_final;
+  __shared__ uint64_t bar_k_full[kStages], bar_k_empty[kStages];
+  __shared__ uint64_t bar_v_full[kStages], bar_v_empty[kStages];
+  __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_o_full[2], bar_o_free[2];
+  __shared__ uint64_t bar_ke[2][2];
+  __shared__ __align__(16) int ke_buf[2][2][128];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  volatile int* abort = &abort_s;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_q_full, 1);
+    mbar_init(&bar_q_empty, 1);
+    mbar_init(&bar_final, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bar_k_full[s], 1);
+      mbar_init(&bar_k_empty[s], 1);
+      mbar_init(&bar_v_full[s], 1);
+      mbar_init(&bar_v_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_s_full[s], 1);
+      mbar_init(&bar_p_full[s], 128);
+      mbar_init(&bar_o_full[s], 1);
+      mbar_init(&bar_o_free[s], 128);
+      mbar_init(&bar_ke[s][0], 128);
+      mbar_init(&bar_ke[s][1], 128);
+    }
+    abort_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&map_q);
+    tma_prefetch_desc(&map_k);
+    tma_prefetch_desc(&map_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_s, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_base_s;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t kv = 0, qn = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+      const Item x = decode_item(p, it);
+      if (qn > 0 && !(ok = warp_wait(&bar_q_empty, (qn - 1) & 1, abort, p.status))) break;
+      if (lane == 0) {
+        const uint32_t bytes = (x.qtile[1] < p.Tq ? 2u : 1u) * kTileBytes;
+        mbar_arrive_expect_tx(&bar_q_full, bytes);
+        for (int s = 0; s < 2; ++s) {
+          if (x.qtile[s] >= p.Tq) continue;
+          tma_load_3d(sQ + s * kTileBytes, &map_q, &bar_q_full, 0, x.head[s], x.qtile[s] * 128);
+          tma_load_3d(sQ + s * kTileBytes + kHalfBytes, &map_q, &bar_q_full, 64, x.head[s],
+                      x.qtile[s] * 128);
+        }
+      }
+      __syncwarp();
+      ++qn;
+      for (int t = x.beg; t < x.end; ++t, ++kv) {
+        const int row0 = p.list_kt[t] * 128;
+        const uint32_t st = kv % kStages, ph = (kv / kStages) & 1;
+        if (kv >= kStages && !(ok = warp_wait(&bar_k_empty[st], ph ^ 1, abort, p.status))) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar_k_full[st], kTileBytes);
+          tma_load_3d(sK + st * kTileBytes, &map_k, &bar_k_full[st], 0, x.kvh, row0);
+          tma_load_3d(sK + st * kTileBytes + kHalfBytes, &map_k, &bar_k_full[st], 64, x.kvh, row0);
+        }
+        __syncwarp();
+        if (kv >= kStages && !(ok = warp_wait(&bar_v_empty[st], ph ^ 1, abort, p.status))) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar_v_full[st], kTileBytes);
+          tma_load_3d(sV + st * kTileBytes, &map_v, &bar_v_full[st], 0, x.kvh, row0);
+          tma_load_3d(sV + st * kTileBytes + kHalfBytes, &map_v, &bar_v_full[st], 64, x.kvh, row0);
+        }
+        __syncwarp();
+      }
+    }
+    if (!ok && lane == 0) {  // let copies in flight land before the CTA exits
+      if (qn > 0) mbar_drain(&bar_q_full, (qn - 1) & 1);
+      for (uint32_t i = kv >= kStages ? kv - kStages : 0; i <= kv; ++i) {
+        mbar_drain(&bar_k_full[i % kStages], (i / kStages) & 1);
+        mbar_drain(&bar_v_full[i % kStages], (i / kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    uint32_t kv = 0, qn = 0;
+    uint32_t pc[2] = {0, 0}, oc[2] = {0, 0};
+    const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+      const Item x = decode_item(p, it);
+      const int T = x.end - x.beg;
+      if (!(ok = warp_wait(&bar_q_full, qn & 1, abort, p.status))) break;
+      ++qn;
+      bool first[2] = {true, true};
+      {  // S(0)
+        const uint32_t st = kv % kStages, ph = (kv / kStages) & 1;
+        if (!(ok = warp_wait(&bar_k_full[st], ph, abort, p.status))) break;
+        tc_fence_after_sync();
+        const int kd = kinds_at(p, x.beg);
+        if (lane == 0) {
+          for (int s = 0; s < 2; ++s) {
+            if ((kd >> (2 * s)) & 3) {
+              issue_qk(tmem + s * 128, q_addr + s * kTileBytes, k_addr + st * kTileBytes);
+              mma_commit(&bar_s_full[s]);
+            }
+          }
+          mma_commit(&bar_k_empty[st]);
+          if (T == 1) mma_commit(&bar_q_empty);
+        }
+        __syncwarp();
+      }
+      for (int t = 0; t < T && ok; ++t) {
+        const uint32_t kvt = kv + t;
+        const uint32_t st = kvt % kStages, ph = (kvt / kStages) & 1;
+        const uint32_t stn = (kvt + 1) % kStages, phn = ((kvt + 1) / kStages) & 1;
+        const int kd = kinds_at(p, x.beg + t);
+        const bool has_next = t + 1 < T;
+        const int kdn = has_next ? kinds_at(p, x.beg + t + 1) : 0;
+        if (!(ok = warp_wait(&bar_v_full[st], ph, abort, p.status))) break;
+        for (int s = 0; s < 2 && ok; ++s) {
+          if ((kd >> (2 * s)) & 3) {
+            if (!(ok = warp_wait(&bar_p_full[s], pc[s] & 1, abort, p.status))) break;
+            ++pc[s];
+            if (first[s] && oc[s] > 0 &&
+                !(ok = warp_wait(&bar_o_free[s], (oc[s] - 1) & 1, abort, p.status)))
+              break;
+            tc_fence_after_sync();
+            if (lane == 0)
+              issue_pv(tmem + 256 + s * 128, tmem + s * 128, v_addr + st * kTileBytes, !first[s]);
+            __syncwarp();
+            first[s] = false;
+          }
+          if (has_next) {
+            if (s == 0) {
+              if (!(ok = warp_wait(&bar_k_full[stn], phn, abort, p.status))) break;
+              tc_fence_after_sync();
+            }
+            if ((kdn >> (2 * s)) & 3) {
+              if (lane == 0) {
+                issue_qk(tmem + s * 128, q_addr + s * kTileBytes, k_addr + stn * kTileBytes);
+                mma_commit(&bar_s_full[s]);
+              }
+              __syncwarp();
+            }
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) {
+          mma_commit(&bar_v_empty[st]);
+          if (has_next) mma_commit(&bar_k_empty[stn]);
+          if (t + 2 == T) mma_commit(&bar_q_empty);  // the item's last S MMAs were just issued
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      kv += T;
+      if (lane == 0) {
+        for (int s = 0; s < 2; ++s)
+          if (x.qtile[s] < p.Tq) mma_commit(&bar_o_full[s]);
+      }
+      __syncwarp();
+      for (int s = 0; s < 2; ++s)
+        if (x.qtile[s] < p.Tq) ++oc[s];
+    }
+    if (lane == 0) {  // every MMA issued by this CTA completes before TMEM is freed
+      mma_commit(&bar_final);
+      mbar_drain(&bar_final, 0);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------- softmax
+    const int s = (warp - 4) / 4;
+    const int quarter = warp % 4;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_off + s * 128;
+    const uint32_t tO = tmem + lane_off + 256 + s * 128;
+    const float sl2 = p.scale_log2;
+    uint32_t sc = 0, oc = 0, kb = 0, ku[2] = {0, 0};
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+      const Item x = decode_item(p, it);
+      if (x.qtile[s] >= p.Tq) continue;
+      const int i = x.qtile[s] * 128 + r;
+      const int h = x.head[s];
+      float m_ref = -INFINITY, l = 0.f;
+      for (int t = x.beg; t < x.end; ++t) {
+        const int kd = (kinds_at(p, t) >> (2 * s)) & 3;
+        if (kd == 0) continue;
+        const int kt = p.list_kt[t];
+        const int* ke = nullptr;
+        if (kd == 1) {  // PARTIAL: the 128 key bounds of this tile, shared through smem
+          const int j = kt * 128 + r;
+          ke_buf[s][kb][r] = j < p.N ? __ldg(p.key_end + j) : 0;
+          mbar_arrive(&bar_ke[s][kb]);
+          if (!(ok = warp_wait(&bar_ke[s][kb], ku[kb] & 1, abort, p.status))) break;
+          ++ku[kb];
+          ke = ke_buf[s][kb];
+          kb ^= 1;
+        }
+        if (!(ok = warp_wait(&bar_s_full[s], sc & 1, abort, p.status))) break;
+        ++sc;
+        tc_fence_after_sync();
+        float sv[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(tS + c * 32, rr);
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) sv[c * 32 + jj] = __uint_as_float(rr[jj]);
+        }
+        if (ke) {
+          const int j0 = kt * 128;
+#pragma unroll
+          for (int c4 = 0; c4 < 32; ++c4) {
+            const int4 b = reinterpret_cast<const int4*>(ke)[c4];
+            const int j = j0 + 4 * c4;
+            if (!(j + 0 <= i && i < b.x)) sv[4 * c4 + 0] = -INFINITY;
+            if (!(j + 1 <= i && i < b.y)) sv[4 * c4 + 1] = -INFINITY;
+            if (!(j + 2 <= i && i < b.z)) sv[4 * c4 + 2] = -INFINITY;
+            if (!(j + 3 <= i && i < b.w)) sv[4 * c4 + 3] = -INFINITY;
+          }
+        }
+        float mx = sv[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, sv[c]);
+        const float m_tile = mx * sl2;
+        const float m_new = fmaxf(m_ref, m_tile);
+        const bool rescale = (m_ref != -INFINITY) && (m_new > m_ref + kRescaleThreshold);
+        const float f = rescale ? ex2_approx(m_ref - m_new) : 1.f;
+        if (rescale) {
+          l *= f;
+          m_ref = m_new;
+        } else if (m_ref == -INFINITY) {
+          m_ref = m_new;  // first visible keys of this row (or still none)
+        }
+        const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const float p0 = ex2_approx(fmaf(sv[c * 32 + 2 * jj], sl2, -mr));
+            const float p1 = ex2_approx(fmaf(sv[c * 32 + 2 * jj + 1], sl2, -mr));
+            rs += p0 + p1;
+            pk[jj] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tS + c * 16, pk);
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O_s is quiescent: its last PV completed before this S did, and the
+          // next PV waits for the P arrival below.
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t rr[32];
+            tmem_ld32(tO + c * 32, rr);
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) rr[jj] = __float_as_uint(__uint_as_float(rr[jj]) * f);
+            tmem_st32(tO + c * 32, rr);
+          }
+        }
+        l += rs;
+        tmem_wait_st();
+        tc_fence_before_sync();
+        mbar_arrive(&bar_p_full[s]);
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l and lse
+      if (!(ok = warp_wait(&bar_o_full[s], oc & 1, abort, p.status))) break;
+      ++oc;
+      tc_fence_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* orow = p.o + (static_cast<size_t>(i) * p.hq + h) * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(tO + c * 32, rr);
+        uint32_t pk[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj)
+          pk[jj] = pack_bf16x2(__uint_as_float(rr[2 * jj]) * inv, __uint_as_float(rr[2 * jj + 1]) * inv);
+        if (i < p.N) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+      if (i < p.N)
+        p.lse[static_cast<size_t>(h) * p.N + i] =
+            l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+      tc_fence_before_sync();
+      mbar_arrive(&bar_o_free[s]);
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16(const AttnArgs& a) {
+  const tree_plan* pl = a.plan;
+  CUtensorMap mq, mk, mv;
+  if (!make_tile_map(&mq, a.q, pl->N, a.hq) || !make_tile_map(&mk, a.k, pl->N, a.hkv) ||
+      !make_tile_map(&mv, a.v, pl->N, a.hkv))
+    return cudaErrorInvalidValue;
+  FwdParams p;
+  const int G = a.hq / a.hkv;
+  p.mode = (G >= 2 && G % 2 == 0) ? 0 : 1;
+  p.key_end = pl->dev.key_end;
+  if (p.mode == 0) {
+    p.list_ptr = pl->dev.qt_ptr;
+    p.list_kt = pl->dev.qt_kt;
+    p.list_kind = pl->dev.qt_kind;
+    p.order = pl->dev.fwd_order;
+    p.n_inner = a.hq / 2;
+    p.n_items = pl->Tq * p.n_inner;
+  } else {
+    p.list_ptr = pl->dev.qp_ptr;
+    p.list_kt = pl->dev.qp_kt;
+    p.list_kind = pl->dev.qp_kind;
+    p.order = pl->dev.qp_order;
+    p.n_inner = a.hq;
+    p.n_items = pl->P * p.n_inner;
+  }
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.status = a.status;
+  p.N = pl->N;
+  p.hq = a.hq;
+  p.group = G;
+  p.Tq = pl->Tq;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(tree_attn_fwd_sm103,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int grid = p.n_items < sm_count() ? p.n_items : sm_count();
+  tree_attn_fwd_sm103<<<grid, kThreads, kSmemBytes, a.stream>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace treeattn
