@@ -78,6 +78,8 @@ def tree_plan_build(segment_parents, segment_lengths) -> Plan:
 
 
 def _stream_ptr(stream):
+    if isinstance(stream, C.c_void_p):
+        return stream
     if stream is None:
         import torch
 
