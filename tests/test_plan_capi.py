@@ -126,5 +126,7 @@ def test_device_calls_without_device_copy_are_rejected():
     assert st == 1
     st = tpa.lib.tree_attn_fwd(plan.handle, 17, 16, 16, 16, 16, 1, 1, 128, 1, 0.0, None)
     assert st == 1  # misaligned pointer
-    ws = tpa.lib.tree_attn_bwd_workspace_bytes(plan.handle, 2, 128, 1)
-    assert ws >= 8 * 2 * 128 * 4
+    # bf16 workspace: lse*log2(e) and Delta, fp32 [hq, 128 * q-tiles] each
+    assert tpa.lib.tree_attn_bwd_workspace_bytes(plan.handle, 2, 128, 1) == 2 * 2 * 128 * 4
+    # fp32 workspace: Delta [hq, N], rounded up to 256 bytes
+    assert tpa.lib.tree_attn_bwd_workspace_bytes(plan.handle, 2, 64, 0) == 256

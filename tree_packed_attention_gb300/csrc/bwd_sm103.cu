@@ -1,27 +1,24 @@
 // Backward tree attention, bf16 in / fp32 accumulate, on the sm_103a tensor
-// cores. Three kernels:
-//   1. preprocess: Delta_i = sum_d dO_id O_id and lse_i*log2(e) into padded
-//      [hq, Tq*128] rows, and zeroing of the fp32 dQ accumulator;
-//   2. main: one persistent CTA per SM; a work item is one 128-key tile of one
-//      kv head ("KV-stationary"); it walks every q head of the group and every
-//      q-tile that sees the key tile -- one contiguous range [kt_qlo, kt_qhi),
-//      because the rows that see key j are exactly [j, key_end[j]);
-//   3. finalize: dQ = scale * accumulator, converted to the gradient dtype.
+// cores, as two kernels with no atomics and no fp32 accumulator in HBM:
 //
-// Per step (q-tile, q head) the main kernel computes, with S^T = K Q^T:
-//   P^T  = exp2(S^T * scale*log2e - lse*log2e)  (masked to j <= i < key_end[j])
-//   dP^T = V dO^T,  dS^T = P^T (dP^T - Delta)
-//   dV += P^T dO,  dK += dS^T Q,  dQ^T = K^T dS^T (added to the fp32 accumulator)
-// ("Tree Training", arXiv 2511.00413, §3.2 mask / App. A.1; the derivatives
-// are the standard softmax-attention ones).
+//  1. dQ kernel (Q-stationary; one 128-row q-tile of one q head per work
+//     item, walking the plan's non-empty k-tiles of that q-tile):
+//        Delta_i = dO_i . O_i,  P = exp2(S*scale*log2e - lse_i*log2e),
+//        dP = dO V^T,  dS = P (dP - Delta),  dQ += dS K,  dq = scale * dQ.
+//     It also writes Delta and lse*log2(e) into padded [hq, Tq*128] rows of
+//     the workspace for kernel 2.
+//  2. dK/dV kernel (KV-stationary; one 128-key tile of one kv head per item,
+//     walking every q head of the group and every q-tile that sees the key
+//     tile -- one contiguous range [kt_qlo, kt_qhi), because the rows that
+//     see key j are exactly [j, key_end[j])):
+//        S^T = K Q^T, P^T, dP^T = V dO^T, dS^T = P^T (dP^T - Delta),
+//        dV += P^T dO,  dK += dS^T Q,  dk = scale * dK.
 //
-// Roles (384 threads): warp 0 TMA producer (K, V per item; Q, dO, lse, Delta
-// per step into a 2-stage ring); warp 1 TMEM owner and MMA issuer; warps 4-7
-// compute P^T (to TMEM, bf16) and dS^T (to shared memory, bf16, 128B-swizzled)
-// with one key row per thread; warps 8-11 drain dQ^T from TMEM into the fp32
-// accumulator (one head-dim row per thread, coalesced reductions) and write
-// dK, dV at the end of an item.
-// TMEM (512 columns): S^T/P^T | dP^T/dQ^T | dV | dK.
+// ("Tree Training", arXiv 2511.00413, §3.2 "Attention Mask" and App. A.1 for
+// the mask; the derivatives are the standard softmax-attention ones.)
+// Recomputing S and dP in both kernels costs two extra 128^3 products per
+// tile pair (7 instead of 5) but removes the dQ reduction traffic, which on
+// this GPU throttled a single-kernel design to a fifth of the tensor rate.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -37,51 +34,9 @@ namespace {
 
 using namespace dev;
 
-constexpr int kThreads = 384;
 constexpr uint32_t kTileBytes = 128 * 128 * 2;
 constexpr uint32_t kHalfBytes = kTileBytes / 2;
-
-// Dynamic shared memory layout (the base must be 1024-byte aligned).
-constexpr uint32_t kOffK = 0;
-constexpr uint32_t kOffV = kOffK + kTileBytes;
-constexpr uint32_t kOffQ = kOffV + kTileBytes;        // 2 stages
-constexpr uint32_t kOffDO = kOffQ + 2 * kTileBytes;   // 2 stages
-constexpr uint32_t kOffDS = kOffDO + 2 * kTileBytes;  // dS^T, 128 keys x 128 q
-constexpr uint32_t kOffLse = kOffDS + kTileBytes;     // 2 stages x 128 fp32
-constexpr uint32_t kOffDelta = kOffLse + 2 * 512;     // 2 stages x 128 fp32
-constexpr uint32_t kOffBar = kOffDelta + 2 * 512;
-constexpr uint32_t kNumBars = 16;
-constexpr uint32_t kSmemBytes = kOffBar + kNumBars * 8 + 16;
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-
-struct BwdParams {
-  const int32_t* key_end;
-  const int32_t* kt_qlo;
-  const int32_t* kt_qhi;
-  const int32_t* order;
-  const float* lse2;   // [hq, Npad]
-  const float* delta;  // [hq, Npad]
-  float* dq_acc;       // [N, hq, 128]
-  void* dk;
-  void* dv;
-  int* status;
-  int N, Npad, hq, hkv, group, n_items, grad_f32;
-  float scale, scale_log2;
-};
-
-struct BwdItem {
-  int kt, kvh, qlo, nq, steps;
-};
-
-__device__ __forceinline__ BwdItem decode_bwd(const BwdParams& p, int it) {
-  BwdItem x;
-  x.kt = p.order[it / p.hkv];
-  x.kvh = it % p.hkv;
-  x.qlo = p.kt_qlo[x.kt];
-  x.nq = p.kt_qhi[x.kt] - x.qlo;
-  x.steps = x.nq * p.group;
-  return x;
-}
+constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           int* status) {
@@ -89,7 +44,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
-// D = A B^T with A [128 x 128] K-major and B [128 x 128] K-major (K = 128).
+// D = A B^T, A and B both K-major 128 x 128 tiles (K = 128).
 __device__ __forceinline__ void mma_kk(uint32_t d, uint32_t a, uint32_t b, uint32_t acc) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
 #pragma unroll
@@ -100,7 +55,7 @@ __device__ __forceinline__ void mma_kk(uint32_t d, uint32_t a, uint32_t b, uint3
   }
 }
 
-// D = A B^T with A K-major and B MN-major (B stored K rows x N contiguous).
+// D = A B^T, A K-major in smem, B MN-major in smem (stored K rows x N contiguous).
 __device__ __forceinline__ void mma_kn(uint32_t d, uint32_t a, uint32_t b, uint32_t acc) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
@@ -111,7 +66,7 @@ __device__ __forceinline__ void mma_kn(uint32_t d, uint32_t a, uint32_t b, uint3
   }
 }
 
-// D = A B^T with A from TMEM (bf16 pairs) and B MN-major.
+// D = A B^T, A from TMEM (bf16 pairs, 128 lanes x 64 columns), B MN-major in smem.
 __device__ __forceinline__ void mma_tn(uint32_t d, uint32_t a_tmem, uint32_t b, uint32_t acc) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
@@ -120,27 +75,419 @@ __device__ __forceinline__ void mma_tn(uint32_t d, uint32_t a_tmem, uint32_t b, 
            (acc || kk > 0) ? 1u : 0u);
 }
 
-// D = A B^T with A MN-major (stored K rows x M contiguous) and B MN-major.
-__device__ __forceinline__ void mma_nn(uint32_t d, uint32_t a, uint32_t b, uint32_t acc) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 1, 1);
+// Write 32 consecutive fp32 values of one 128-wide row, times `mul`, as fp32 or bf16.
+__device__ __forceinline__ void store_row(void* dst_base, size_t off, int c, const uint32_t (&v)[32],
+                                          float mul, int out_f32) {
+  if (out_f32) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(dst_base) + off + c * 32);
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk)
-    mma_ss(d, sdesc_sw128(a + kk * 2048, kHalfBytes, 1024),
-           sdesc_sw128(b + kk * 2048, kHalfBytes, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
+    for (int u = 0; u < 8; ++u)
+      dst[u] = make_float4(__uint_as_float(v[4 * u]) * mul, __uint_as_float(v[4 * u + 1]) * mul,
+                           __uint_as_float(v[4 * u + 2]) * mul, __uint_as_float(v[4 * u + 3]) * mul);
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst_base) + off + c * 32);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      dst[u] = make_uint4(
+          pack_bf16x2(__uint_as_float(v[8 * u + 0]) * mul, __uint_as_float(v[8 * u + 1]) * mul),
+          pack_bf16x2(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul),
+          pack_bf16x2(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul),
+          pack_bf16x2(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul));
+  }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    tree_attn_bwd_sm103(const __grid_constant__ CUtensorMap map_q,
-                        const __grid_constant__ CUtensorMap map_k,
-                        const __grid_constant__ CUtensorMap map_v,
-                        const __grid_constant__ CUtensorMap map_do, const BwdParams p) {
+// ============================================================== dQ kernel
+// 256 threads: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps 4-7
+// one q row per thread. TMEM: S_a | S_b | dP | dQ (128 columns each); dS is
+// written as bf16 over the first 64 columns of the S buffer it came from and
+// read by the dQ MMA from TMEM.
+constexpr int kDqThreads = 256;
+constexpr int kDqStages = 2;
+constexpr uint32_t kDqOffQ = 0;
+constexpr uint32_t kDqOffDO = kTileBytes;
+constexpr uint32_t kDqOffK = 2 * kTileBytes;                    // kDqStages tiles
+constexpr uint32_t kDqOffV = kDqOffK + kDqStages * kTileBytes;  // kDqStages tiles
+constexpr uint32_t kDqSmem = 1024 + kDqOffV + kDqStages * kTileBytes;
+
+struct DqParams {
+  const int32_t* key_end;
+  const int32_t* qt_ptr;
+  const int32_t* qt_kt;
+  const int32_t* qt_kind;
+  const int32_t* order;
+  const __nv_bfloat16* o;
+  const float* lse;
+  float* lse2;   // out: [hq, Npad]
+  float* delta;  // out: [hq, Npad]
+  void* dq;
+  int* status;
+  int N, Npad, hq, group, n_items, out_f32;
+  float scale, scale_log2;
+};
+
+__global__ void __launch_bounds__(kDqThreads, 1)
+    tree_attn_bwd_dq_sm103(const __grid_constant__ CUtensorMap map_q,
+                           const __grid_constant__ CUtensorMap map_k,
+                           const __grid_constant__ CUtensorMap map_v,
+                           const __grid_constant__ CUtensorMap map_do, const DqParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t bar_q_full, bar_q_empty, bar_final;
+  __shared__ uint64_t bar_k_full[kDqStages], bar_k_empty[kDqStages];
+  __shared__ uint64_t bar_v_full[kDqStages], bar_v_empty[kDqStages];
+  __shared__ uint64_t bar_s_full[2];  // one per S buffer: a buffer is refilled only after
+                                     // its dS was consumed, so each barrier is at most one phase ahead
+  __shared__ uint64_t bar_dp_full, bar_ds_full, bar_dq_full, bar_dq_free;
+  __shared__ uint64_t bar_ke[2];
+  __shared__ __align__(16) int ke_buf[2][128];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  volatile int* abort = &abort_s;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_q_full, 1);
+    mbar_init(&bar_q_empty, 1);
+    mbar_init(&bar_final, 1);
+    for (int s = 0; s < kDqStages; ++s) {
+      mbar_init(&bar_k_full[s], 1);
+      mbar_init(&bar_k_empty[s], 1);
+      mbar_init(&bar_v_full[s], 1);
+      mbar_init(&bar_v_empty[s], 1);
+    }
+    mbar_init(&bar_s_full[0], 1);
+    mbar_init(&bar_s_full[1], 1);
+    mbar_init(&bar_dp_full, 1);
+    mbar_init(&bar_ds_full, 128);
+    mbar_init(&bar_dq_full, 1);
+    mbar_init(&bar_dq_free, 128);
+    mbar_init(&bar_ke[0], 128);
+    mbar_init(&bar_ke[1], 128);
+    abort_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&map_q);
+    tma_prefetch_desc(&map_k);
+    tma_prefetch_desc(&map_v);
+    tma_prefetch_desc(&map_do);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_s, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_base_s;
+  const uint32_t tS = tmem, tDP = tmem + 256, tDQ = tmem + 384;  // S_a at 0, S_b at 128
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t kv = 0, qn = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+      const int qt = p.order[it / p.hq], h = it % p.hq, kvh = h / p.group;
+      if (qn > 0 && !(ok = warp_wait(&bar_q_empty, (qn - 1) & 1, abort, p.status))) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bar_q_full, 2 * kTileBytes);
+        tma_load_3d(smem + kDqOffQ, &map_q, &bar_q_full, 0, h, qt * 128);
+        tma_load_3d(smem + kDqOffQ + kHalfBytes, &map_q, &bar_q_full, 64, h, qt * 128);
+        tma_load_3d(smem + kDqOffDO, &map_do, &bar_q_full, 0, h, qt * 128);
+        tma_load_3d(smem + kDqOffDO + kHalfBytes, &map_do, &bar_q_full, 64, h, qt * 128);
+      }
+      __syncwarp();
+      ++qn;
+      for (int t = p.qt_ptr[qt]; t < p.qt_ptr[qt + 1]; ++t, ++kv) {
+        const int row0 = p.qt_kt[t] * 128;
+        const uint32_t st = kv % kDqStages, ph = (kv / kDqStages) & 1;
+        if (kv >= kDqStages && !(ok = warp_wait(&bar_k_empty[st], ph ^ 1, abort, p.status))) break;
+        if (lane == 0) {
+          uint8_t* dst = smem + kDqOffK + st * kTileBytes;
+          mbar_arrive_expect_tx(&bar_k_full[st], kTileBytes);
+          tma_load_3d(dst, &map_k, &bar_k_full[st], 0, kvh, row0);
+          tma_load_3d(dst + kHalfBytes, &map_k, &bar_k_full[st], 64, kvh, row0);
+        }
+        __syncwarp();
+        if (kv >= kDqStages && !(ok = warp_wait(&bar_v_empty[st], ph ^ 1, abort, p.status))) break;
+        if (lane == 0) {
+          uint8_t* dst = smem + kDqOffV + st * kTileBytes;
+          mbar_arrive_expect_tx(&bar_v_full[st], kTileBytes);
+          tma_load_3d(dst, &map_v, &bar_v_full[st], 0, kvh, row0);
+          tma_load_3d(dst + kHalfBytes, &map_v, &bar_v_full[st], 64, kvh, row0);
+        }
+        __syncwarp();
+      }
+    }
+    if (!ok && lane == 0) {
+      if (qn > 0) mbar_drain(&bar_q_full, (qn - 1) & 1);
+      for (uint32_t i = kv >= kDqStages ? kv - kDqStages : 0; i <= kv; ++i) {
+        mbar_drain(&bar_k_full[i % kDqStages], (i / kDqStages) & 1);
+        mbar_drain(&bar_v_full[i % kDqStages], (i / kDqStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    // Per item: S_0, dP_0, S_1; then per tile t: [dS_t] dQ += dS_t K_t,
+    // dP_{t+1}, S_{t+2} (into the S buffer dQ_t just read).
+    const uint32_t aQ = smem_u32(smem + kDqOffQ), aDO = smem_u32(smem + kDqOffDO);
+    const uint32_t aK = smem_u32(smem + kDqOffK), aV = smem_u32(smem + kDqOffV);
+    uint32_t kv = 0, qn = 0, n = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+      const int qt = p.order[it / p.hq];
+      const int T = p.qt_ptr[qt + 1] - p.qt_ptr[qt];
+      if (!(ok = warp_wait(&bar_q_full, qn & 1, abort, p.status))) break;
+      ++qn;
+      auto k_stage = [&](uint32_t i) { return aK + (i % kDqStages) * kTileBytes; };
+      auto v_stage = [&](uint32_t i) { return aV + (i % kDqStages) * kTileBytes; };
+      auto wait_k = [&](uint32_t i) {
+        return warp_wait(&bar_k_full[i % kDqStages], (i / kDqStages) & 1, abort, p.status);
+      };
+      auto wait_v = [&](uint32_t i) {
+        return warp_wait(&bar_v_full[i % kDqStages], (i / kDqStages) & 1, abort, p.status);
+      };
+      if (!(ok = wait_k(kv))) break;
+      tc_fence_after_sync();
+      if (lane == 0) {
+        mma_kk(tS, aQ, k_stage(kv), 0);  // S_0
+        mma_commit(&bar_s_full[0]);
+      }
+      __syncwarp();
+      if (!(ok = wait_v(kv))) break;
+      tc_fence_after_sync();
+      if (lane == 0) {
+        mma_kk(tDP, aDO, v_stage(kv), 0);  // dP_0
+        mma_commit(&bar_dp_full);
+        mma_commit(&bar_v_empty[kv % kDqStages]);
+      }
+      __syncwarp();
+      if (T > 1) {
+        if (!(ok = wait_k(kv + 1))) break;
+        tc_fence_after_sync();
+        if (lane == 0) {
+          mma_kk(tS + 128, aQ, k_stage(kv + 1), 0);  // S_1
+          mma_commit(&bar_s_full[1]);
+        }
+        __syncwarp();
+      }
+      for (int t = 0; t < T && ok; ++t, ++n) {
+        const uint32_t i = kv + t;
+        if (!(ok = warp_wait(&bar_ds_full, n & 1, abort, p.status))) break;
+        if (t == 0 && qn > 1 && !(ok = warp_wait(&bar_dq_free, (qn - 2) & 1, abort, p.status)))
+          break;
+        tc_fence_after_sync();
+        if (lane == 0) {
+          mma_tn(tDQ, tS + (t & 1) * 128, k_stage(i), t > 0);  // dQ += dS_t K_t
+          mma_commit(&bar_k_empty[i % kDqStages]);
+          if (t + 1 == T) {
+            mma_commit(&bar_dq_full);
+            mma_commit(&bar_q_empty);
+          }
+        }
+        __syncwarp();
+        if (t + 1 < T) {
+          if (!(ok = wait_v(i + 1))) break;
+          tc_fence_after_sync();
+          if (lane == 0) {
+            mma_kk(tDP, aDO, v_stage(i + 1), 0);  // dP_{t+1} (dP_t already read)
+            mma_commit(&bar_dp_full);
+            mma_commit(&bar_v_empty[(i + 1) % kDqStages]);
+          }
+          __syncwarp();
+        }
+        if (t + 2 < T) {
+          if (!(ok = wait_k(i + 2))) break;
+          tc_fence_after_sync();
+          if (lane == 0) {
+            mma_kk(tS + (t & 1) * 128, aQ, k_stage(i + 2), 0);  // S_{t+2}
+            mma_commit(&bar_s_full[t & 1]);
+          }
+          __syncwarp();
+        }
+      }
+      kv += T;
+    }
+    if (lane == 0) {
+      mma_commit(&bar_final);
+      mbar_drain(&bar_final, 0);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------------------------------------------- one q row per thread
+    const int quarter = warp % 4;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float sl2 = p.scale_log2;
+    uint32_t n = 0, qn = 0, kb = 0, ku[2] = {0, 0}, su[2] = {0, 0};
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+      const int qt = p.order[it / p.hq], h = it % p.hq;
+      const int i = qt * 128 + r;
+      const size_t row = static_cast<size_t>(i) * p.hq + h;
+      // Delta_i = dO_i . O_i (dO from the swizzled smem tile, O from HBM) and lse_i * log2(e)
+      if (!(ok = warp_wait(&bar_q_full, qn & 1, abort, p.status))) break;
+      float delta = 0.f, lse2 = INFINITY;
+      if (i < p.N) {
+        const uint4* orow = reinterpret_cast<const uint4*>(p.o + row * 128);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint4 ov = __ldg(orow + c);
+          const uint4 dv = *reinterpret_cast<const uint4*>(
+              smem + kDqOffDO + (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) * 16));
+          const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+          const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float2 fa = __bfloat1622float2(o2[u]);
+            const float2 fb = __bfloat1622float2(d2[u]);
+            delta = fmaf(fa.x, fb.x, delta);
+            delta = fmaf(fa.y, fb.y, delta);
+          }
+        }
+        lse2 = p.lse[static_cast<size_t>(h) * p.N + i] * kLog2e;
+      }
+      p.delta[static_cast<size_t>(h) * p.Npad + i] = delta;
+      p.lse2[static_cast<size_t>(h) * p.Npad + i] = lse2;
+      ++qn;
+      const int beg = p.qt_ptr[qt], end = p.qt_ptr[qt + 1];
+      for (int t = beg; t < end; ++t, ++n) {
+        const int kd = p.qt_kind[t];
+        const int kt = p.qt_kt[t];
+        const int* ke = nullptr;
+        if (kd == 1) {  // PARTIAL: the 128 key bounds of this tile, shared through smem
+          const int j = kt * 128 + r;
+          ke_buf[kb][r] = j < p.N ? __ldg(p.key_end + j) : 0;
+          mbar_arrive(&bar_ke[kb]);
+          if (!(ok = warp_wait(&bar_ke[kb], ku[kb] & 1, abort, p.status))) break;
+          ++ku[kb];
+          ke = ke_buf[kb];
+          kb ^= 1;
+        }
+        const int sb = (t - beg) & 1;
+        const uint32_t tSb = tS + lane_off + sb * 128;
+        if (!(ok = warp_wait(&bar_s_full[sb], su[sb] & 1, abort, p.status))) break;
+        ++su[sb];
+        tc_fence_after_sync();
+        float pv[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(tSb + c * 32, rr);
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj)
+            pv[c * 32 + jj] = ex2_approx(fmaf(__uint_as_float(rr[jj]), sl2, -lse2));
+        }
+        if (ke) {
+          const int j0 = kt * 128;
+#pragma unroll
+          for (int c4 = 0; c4 < 32; ++c4) {
+            const int4 b = reinterpret_cast<const int4*>(ke)[c4];
+            const int j = j0 + 4 * c4;
+            if (!(j + 0 <= i && i < b.x)) pv[4 * c4 + 0] = 0.f;
+            if (!(j + 1 <= i && i < b.y)) pv[4 * c4 + 1] = 0.f;
+            if (!(j + 2 <= i && i < b.z)) pv[4 * c4 + 2] = 0.f;
+            if (!(j + 3 <= i && i < b.w)) pv[4 * c4 + 3] = 0.f;
+          }
+        }
+        if (!(ok = warp_wait(&bar_dp_full, n & 1, abort, p.status))) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(tDP + lane_off + c * 32, rr);
+          uint32_t pk[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            pk[jj] = pack_bf16x2(pv[c * 32 + 2 * jj] * (__uint_as_float(rr[2 * jj]) - delta),
+                                 pv[c * 32 + 2 * jj + 1] * (__uint_as_float(rr[2 * jj + 1]) - delta));
+          tmem_st16(tSb + c * 16, pk);  // dS over the first 64 columns of this S buffer
+        }
+        tmem_wait_st();
+        tc_fence_before_sync();
+        mbar_arrive(&bar_ds_full);
+      }
+      if (!ok) break;
+      // epilogue: dq = scale * dQ
+      if (!(ok = warp_wait(&bar_dq_full, (qn - 1) & 1, abort, p.status))) break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tDQ + lane_off + c * 32, v);
+        if (i < p.N) store_row(p.dq, row * 128, c, v, p.scale, p.out_f32);
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&bar_dq_free);
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ============================================================ dK/dV kernel
+// 384 threads: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps 4-7
+// one key row per thread (P^T to TMEM, dS^T to smem), warps 8-11 the dK/dV
+// epilogue. TMEM: S^T/P^T | dP^T | dV | dK.
+constexpr int kKvThreads = 384;
+constexpr uint32_t kKvOffK = 0;
+constexpr uint32_t kKvOffV = kKvOffK + kTileBytes;
+constexpr uint32_t kKvOffQ = kKvOffV + kTileBytes;        // 2 stages
+constexpr uint32_t kKvOffDO = kKvOffQ + 2 * kTileBytes;   // 2 stages
+constexpr uint32_t kKvOffDS = kKvOffDO + 2 * kTileBytes;  // dS^T, 128 keys x 128 q
+constexpr uint32_t kKvOffLse = kKvOffDS + kTileBytes;     // 2 stages x 128 fp32
+constexpr uint32_t kKvOffDelta = kKvOffLse + 2 * 512;     // 2 stages x 128 fp32
+constexpr uint32_t kKvOffBar = kKvOffDelta + 2 * 512;
+constexpr uint32_t kKvNumBars = 16;
+constexpr uint32_t kKvSmem = kKvOffBar + kKvNumBars * 8 + 16;
+static_assert(kKvSmem <= 232448, "shared memory budget");
+
+struct KvParams {
+  const int32_t* key_end;
+  const int32_t* kt_qlo;
+  const int32_t* kt_qhi;
+  const int32_t* order;
+  const float* lse2;   // [hq, Npad]
+  const float* delta;  // [hq, Npad]
+  void* dk;
+  void* dv;
+  int* status;
+  int N, Npad, hq, hkv, group, n_items, out_f32;
+  float scale, scale_log2;
+};
+
+struct KvItem {
+  int kt, kvh, qlo, nq, steps;
+};
+
+__device__ __forceinline__ KvItem decode_kv(const KvParams& p, int it) {
+  KvItem x;
+  x.kt = p.order[it / p.hkv];
+  x.kvh = it % p.hkv;
+  x.qlo = p.kt_qlo[x.kt];
+  x.nq = p.kt_qhi[x.kt] - x.qlo;
+  x.steps = x.nq * p.group;
+  return x;
+}
+
+__global__ void __launch_bounds__(kKvThreads, 1)
+    tree_attn_bwd_dkdv_sm103(const __grid_constant__ CUtensorMap map_q,
+                             const __grid_constant__ CUtensorMap map_k,
+                             const __grid_constant__ CUtensorMap map_v,
+                             const __grid_constant__ CUtensorMap map_do, const KvParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (smem_u32(smem) & 1023u) {  // the layout needs a 1024-aligned base
     if (threadIdx.x == 0) atomicExch(p.status, 9);
     return;
   }
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kKvOffBar);
   uint64_t* bar_kv_full = bars + 0;
   uint64_t* bar_kv_empty = bars + 1;
   uint64_t* bar_qdo_full = bars + 2;   // [2]
@@ -148,13 +495,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_s_full = bars + 6;
   uint64_t* bar_dp_full = bars + 7;
   uint64_t* bar_ds_full = bars + 8;
-  uint64_t* bar_dq_full = bars + 9;
-  uint64_t* bar_dq_free = bars + 10;
-  uint64_t* bar_dkdv_full = bars + 11;
-  uint64_t* bar_dkdv_free = bars + 12;
-  uint64_t* bar_final = bars + 13;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
-  volatile int* abort = reinterpret_cast<volatile int*>(bars + kNumBars) + 1;
+  uint64_t* bar_dkdv_full = bars + 9;
+  uint64_t* bar_dkdv_free = bars + 10;
+  uint64_t* bar_final = bars + 11;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kKvNumBars);
+  volatile int* abort = reinterpret_cast<volatile int*>(bars + kKvNumBars) + 1;
 
   if (threadIdx.x == 0) {
     mbar_init(bar_kv_full, 1);
@@ -166,8 +511,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_s_full, 1);
     mbar_init(bar_dp_full, 1);
     mbar_init(bar_ds_full, 128);
-    mbar_init(bar_dq_full, 1);
-    mbar_init(bar_dq_free, 128);
     mbar_init(bar_dkdv_full, 1);
     mbar_init(bar_dkdv_free, 128);
     mbar_init(bar_final, 1);
@@ -195,15 +538,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t n = 0, items = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++items) {
-      const BwdItem x = decode_bwd(p, it);
+      const KvItem x = decode_kv(p, it);
       if (items > 0 && !(ok = warp_wait(bar_kv_empty, (items - 1) & 1, abort, p.status))) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(bar_kv_full, 2 * kTileBytes);
         const int row0 = x.kt * 128;
-        tma_load_3d(smem + kOffK, &map_k, bar_kv_full, 0, x.kvh, row0);
-        tma_load_3d(smem + kOffK + kHalfBytes, &map_k, bar_kv_full, 64, x.kvh, row0);
-        tma_load_3d(smem + kOffV, &map_v, bar_kv_full, 0, x.kvh, row0);
-        tma_load_3d(smem + kOffV + kHalfBytes, &map_v, bar_kv_full, 64, x.kvh, row0);
+        tma_load_3d(smem + kKvOffK, &map_k, bar_kv_full, 0, x.kvh, row0);
+        tma_load_3d(smem + kKvOffK + kHalfBytes, &map_k, bar_kv_full, 64, x.kvh, row0);
+        tma_load_3d(smem + kKvOffV, &map_v, bar_kv_full, 0, x.kvh, row0);
+        tma_load_3d(smem + kKvOffV + kHalfBytes, &map_v, bar_kv_full, 64, x.kvh, row0);
       }
       __syncwarp();
       for (int j = 0; j < x.steps; ++j, ++n) {
@@ -214,15 +557,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           uint64_t* b = bar_qdo_full + st;
           mbar_arrive_expect_tx(b, 2 * kTileBytes + 1024);
-          uint8_t* q = smem + kOffQ + st * kTileBytes;
-          uint8_t* d = smem + kOffDO + st * kTileBytes;
+          uint8_t* q = smem + kKvOffQ + st * kTileBytes;
+          uint8_t* d = smem + kKvOffDO + st * kTileBytes;
           tma_load_3d(q, &map_q, b, 0, h, qt * 128);
           tma_load_3d(q + kHalfBytes, &map_q, b, 64, h, qt * 128);
           tma_load_3d(d, &map_do, b, 0, h, qt * 128);
           tma_load_3d(d + kHalfBytes, &map_do, b, 64, h, qt * 128);
           const size_t off = static_cast<size_t>(h) * p.Npad + qt * 128;
-          bulk_load(smem + kOffLse + st * 512, p.lse2 + off, 512, b);
-          bulk_load(smem + kOffDelta + st * 512, p.delta + off, 512, b);
+          bulk_load(smem + kKvOffLse + st * 512, p.lse2 + off, 512, b);
+          bulk_load(smem + kKvOffDelta + st * 512, p.delta + off, 512, b);
         }
         __syncwarp();
       }
@@ -233,32 +576,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    const uint32_t aK = smem_u32(smem + kOffK), aV = smem_u32(smem + kOffV);
-    const uint32_t aDS = smem_u32(smem + kOffDS);
+    // Per step n (S^T_n and dP^T_n already issued):
+    //   [dS_n] dV += P^T_n dO_n, S^T_{n+1}, dK += dS^T_n Q_n, dP^T_{n+1}
+    const uint32_t aK = smem_u32(smem + kKvOffK), aV = smem_u32(smem + kKvOffV);
+    const uint32_t aDS = smem_u32(smem + kKvOffDS);
     uint32_t n = 0, items = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++items) {
-      const BwdItem x = decode_bwd(p, it);
+      const KvItem x = decode_kv(p, it);
       if (!(ok = warp_wait(bar_kv_full, items & 1, abort, p.status))) break;
-      // Issue order per step n (S^T_n and dP^T_n already issued):
-      //   dQ^T_n, dV_n, S^T_{n+1}, dK_n, [dQ^T_n drained] dP^T_{n+1}
-      // so the dQ drain overlaps dV/S/dK and the next softmax overlaps dK/dP.
       for (int j = 0; j < x.steps; ++j, ++n) {
         const uint32_t st = n & 1, ph = (n >> 1) & 1;
-        const uint32_t aQ = smem_u32(smem + kOffQ + st * kTileBytes);
-        const uint32_t aDO = smem_u32(smem + kOffDO + st * kTileBytes);
+        const uint32_t aQ = smem_u32(smem + kKvOffQ + st * kTileBytes);
+        const uint32_t aDO = smem_u32(smem + kKvOffDO + st * kTileBytes);
         if (j == 0) {
           if (!(ok = warp_wait(bar_qdo_full + st, ph, abort, p.status))) break;
           tc_fence_after_sync();
           if (lane == 0) {
             mma_kk(tA, aK, aQ, 0);  // S^T = K Q^T
             mma_commit(bar_s_full);
-          }
-          __syncwarp();
-          // dP^T overwrites the dQ^T of the previous step: wait for its drain
-          if (n > 0 && !(ok = warp_wait(bar_dq_free, (n - 1) & 1, abort, p.status))) break;
-          tc_fence_after_sync();
-          if (lane == 0) {
             mma_kk(tB, aV, aDO, 0);  // dP^T = V dO^T
             mma_commit(bar_dp_full);
           }
@@ -269,21 +605,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             !(ok = warp_wait(bar_dkdv_free, (items - 1) & 1, abort, p.status)))
           break;
         tc_fence_after_sync();
-        if (lane == 0) {
-          mma_nn(tB, aK, aDS, 0);      // dQ^T = K^T dS^T
-          mma_commit(bar_dq_full);
-          mma_tn(tC, tA, aDO, j > 0);  // dV += P^T dO
-        }
+        if (lane == 0) mma_tn(tC, tA, aDO, j > 0);  // dV += P^T dO
         __syncwarp();
         const bool has_next = j + 1 < x.steps;
         const uint32_t stn = (n + 1) & 1, phn = ((n + 1) >> 1) & 1;
-        const uint32_t aQn = smem_u32(smem + kOffQ + stn * kTileBytes);
-        const uint32_t aDOn = smem_u32(smem + kOffDO + stn * kTileBytes);
         if (has_next) {
           if (!(ok = warp_wait(bar_qdo_full + stn, phn, abort, p.status))) break;
           tc_fence_after_sync();
           if (lane == 0) {
-            mma_kk(tA, aK, aQn, 0);  // S^T of the next step (P^T_n already consumed by dV)
+            mma_kk(tA, aK, smem_u32(smem + kKvOffQ + stn * kTileBytes), 0);  // next S^T
             mma_commit(bar_s_full);
           }
           __syncwarp();
@@ -291,17 +621,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           mma_kn(tD, aDS, aQ, j > 0);  // dK += dS^T Q
           mma_commit(bar_qdo_empty + st);
-        }
-        __syncwarp();
-        if (has_next) {
-          if (!(ok = warp_wait(bar_dq_free, n & 1, abort, p.status))) break;
-          tc_fence_after_sync();
-          if (lane == 0) {
-            mma_kk(tB, aV, aDOn, 0);  // dP^T of the next step
+          if (has_next) {
+            mma_kk(tB, aV, smem_u32(smem + kKvOffDO + stn * kTileBytes), 0);  // next dP^T
             mma_commit(bar_dp_full);
           }
-          __syncwarp();
         }
+        __syncwarp();
       }
       if (!ok) break;
       if (lane == 0) {
@@ -321,22 +646,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kr = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tSr = tA + lane_off, tPr = tB + lane_off;
-    uint8_t* ds_row = smem + kOffDS + kr * 128;
+    uint8_t* ds_row = smem + kKvOffDS + kr * 128;
     const float sl2 = p.scale_log2;
     uint32_t n = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
-      const BwdItem x = decode_bwd(p, it);
+      const KvItem x = decode_kv(p, it);
       const int jk = x.kt * 128 + kr;
       const int ke = jk < p.N ? __ldg(p.key_end + jk) : 0;  // rows [jk, ke) see this key
       for (int j = 0; j < x.steps; ++j, ++n) {
         const int q0 = (x.qlo + j % x.nq) * 128;
         const uint32_t st = n & 1, ph = (n >> 1) & 1;
-        const float* lse2 = reinterpret_cast<const float*>(smem + kOffLse + st * 512);
-        const float* dlt = reinterpret_cast<const float*>(smem + kOffDelta + st * 512);
+        const float* lse2 = reinterpret_cast<const float*>(smem + kKvOffLse + st * 512);
+        const float* dlt = reinterpret_cast<const float*>(smem + kKvOffDelta + st * 512);
         if (!(ok = warp_wait(bar_qdo_full + st, ph, abort, p.status))) break;
         if (!(ok = warp_wait(bar_s_full, n & 1, abort, p.status))) break;
         tc_fence_after_sync();
+        const bool full_row = jk <= q0 && q0 + 128 <= ke;  // every column visible to this key
         float pv[128];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -350,9 +676,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int q = q0 + c * 32 + jj + u;
-              const bool vis = jk <= q && q < ke;
               const float e = ex2_approx(fmaf(__uint_as_float(rr[jj + u]), sl2, -lv[u]));
-              pv[c * 32 + jj + u] = vis ? e : 0.f;
+              pv[c * 32 + jj + u] = (full_row || (jk <= q && q < ke)) ? e : 0.f;
             }
           }
 #pragma unroll
@@ -393,67 +718,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp >= 8) {
-    // -------------------------------- dQ^T drain and the dK/dV epilogue
+    // ------------------------------------------------- dK/dV epilogue
     const int quarter = warp % 4;
-    const int rr_lane = quarter * 32 + lane;  // head-dim index for dQ^T, key row for dK/dV
+    const int kr = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    uint32_t n = 0, items = 0;
+    uint32_t items = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++items) {
-      const BwdItem x = decode_bwd(p, it);
-      for (int j = 0; j < x.steps; ++j, ++n) {
-        const int h = x.kvh * p.group + j / x.nq;
-        const int q0 = (x.qlo + j % x.nq) * 128;
-        if (!(ok = warp_wait(bar_dq_full, n & 1, abort, p.status))) break;
-        tc_fence_after_sync();
-        float* base = p.dq_acc + static_cast<size_t>(h) * 128 + rr_lane;
-        const size_t row_stride = static_cast<size_t>(p.hq) * 128;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tB + lane_off + c * 32, v);
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int q = q0 + c * 32 + jj;
-            if (q < p.N) atomicAdd(base + static_cast<size_t>(q) * row_stride, __uint_as_float(v[jj]));
-          }
-        }
-        tc_fence_before_sync();
-        mbar_arrive(bar_dq_free);
-      }
-      if (!ok) break;
+      const KvItem x = decode_kv(p, it);
       if (!(ok = warp_wait(bar_dkdv_full, items & 1, abort, p.status))) break;
       tc_fence_after_sync();
-      const int jk = x.kt * 128 + rr_lane;
+      const int jk = x.kt * 128 + kr;
       const size_t out = (static_cast<size_t>(jk) * p.hkv + x.kvh) * 128;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {  // 0: dV (TMEM C), 1: dK (TMEM D, times scale)
-        const uint32_t t = (which ? tD : tC) + lane_off;
-        const float mul = which ? p.scale : 1.f;
-        void* dst_base = which ? p.dk : p.dv;
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tC + lane_off + c * 32, v);
+        if (jk < p.N) store_row(p.dv, out, c, v, 1.f, p.out_f32);
+      }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(t + c * 32, v);
-          if (jk < p.N) {
-            if (p.grad_f32) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(dst_base) + out + c * 32);
-#pragma unroll
-              for (int u = 0; u < 8; ++u)
-                dst[u] = make_float4(__uint_as_float(v[4 * u]) * mul, __uint_as_float(v[4 * u + 1]) * mul,
-                                     __uint_as_float(v[4 * u + 2]) * mul, __uint_as_float(v[4 * u + 3]) * mul);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst_base) + out + c * 32);
-#pragma unroll
-              for (int u = 0; u < 4; ++u)
-                dst[u] = make_uint4(
-                    pack_bf16x2(__uint_as_float(v[8 * u + 0]) * mul, __uint_as_float(v[8 * u + 1]) * mul),
-                    pack_bf16x2(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul),
-                    pack_bf16x2(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul),
-                    pack_bf16x2(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul));
-            }
-          }
-        }
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tD + lane_off + c * 32, v);
+        if (jk < p.N) store_row(p.dk, out, c, v, p.scale, p.out_f32);
       }
       tc_fence_before_sync();
       mbar_arrive(bar_dkdv_free);
@@ -468,112 +755,78 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Delta = rowsum(dO * O) and lse*log2(e), both [hq, Npad] with padded rows
-// (Delta 0, lse +inf); zero the fp32 dQ accumulator. One warp per (row, head).
-__global__ void __launch_bounds__(256) bwd_pre_bf16_kernel(
-    const __nv_bfloat16* __restrict__ dout, const __nv_bfloat16* __restrict__ o,
-    const float* __restrict__ lse, float* __restrict__ delta, float* __restrict__ lse2,
-    float* __restrict__ dq_acc, int N, int Npad, int hq) {
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;  // i * hq + h
-  if (row >= static_cast<long long>(Npad) * hq) return;
-  const int i = static_cast<int>(row / hq), h = static_cast<int>(row % hq);
-  float s = 0.f;
-  if (i < N) {
-    const uint2 a = reinterpret_cast<const uint2*>(dout + row * 128)[lane];
-    const uint2 b = reinterpret_cast<const uint2*>(o + row * 128)[lane];
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const float2 fa = __bfloat1622float2(a2[u]);
-      const float2 fb = __bfloat1622float2(b2[u]);
-      s = fmaf(fa.x, fb.x, s);
-      s = fmaf(fa.y, fb.y, s);
-    }
-    reinterpret_cast<float4*>(dq_acc + row * 128)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (lane == 0) {
-    const size_t idx = static_cast<size_t>(h) * Npad + i;
-    delta[idx] = s;
-    lse2[idx] = i < N ? lse[static_cast<size_t>(h) * N + i] * 1.4426950408889634f : INFINITY;
-  }
-}
-
-// dq = scale * dq_acc, to bf16 or fp32. Each thread converts 4 elements.
-__global__ void __launch_bounds__(256) bwd_finalize_kernel(const float* __restrict__ acc,
-                                                          void* __restrict__ dq, long long n4,
-                                                          float scale, int out_f32) {
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n4) return;
-  const float4 a = reinterpret_cast<const float4*>(acc)[i];
-  if (out_f32) {
-    reinterpret_cast<float4*>(dq)[i] = make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale);
-  } else {
-    reinterpret_cast<uint2*>(dq)[i] =
-        make_uint2(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale));
-  }
-}
-
 }  // namespace
 
 cudaError_t launch_bwd_bf16(const AttnBwdArgs& a) {
   const tree_plan* pl = a.plan;
   const int N = pl->N, Npad = pl->Tq * 128;
-  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  const size_t acc_bytes = (static_cast<size_t>(N) * a.hq * 128 * 4 + 255) / 256 * 256;
-  float* dq_acc = reinterpret_cast<float*>(ws);
-  float* delta = reinterpret_cast<float*>(ws + acc_bytes);
-  float* lse2 = delta + static_cast<size_t>(a.hq) * Npad;
-
-  const long long rows = static_cast<long long>(Npad) * a.hq;
-  bwd_pre_bf16_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, a.stream>>>(
-      static_cast<const __nv_bfloat16*>(a.dout), static_cast<const __nv_bfloat16*>(a.o), a.lse,
-      delta, lse2, dq_acc, N, Npad, a.hq);
+  float* lse2 = static_cast<float*>(a.workspace);
+  float* delta = lse2 + static_cast<size_t>(a.hq) * Npad;
 
   CUtensorMap mq, mk, mv, mdo;
   if (!make_tile_map(&mq, a.q, N, a.hq) || !make_tile_map(&mk, a.k, N, a.hkv) ||
       !make_tile_map(&mv, a.v, N, a.hkv) || !make_tile_map(&mdo, a.dout, N, a.hq))
     return cudaErrorInvalidValue;
-  BwdParams p;
-  p.key_end = pl->dev.key_end;
-  p.kt_qlo = pl->dev.kt_qlo;
-  p.kt_qhi = pl->dev.kt_qhi;
-  p.order = pl->dev.bwd_order;
-  p.lse2 = lse2;
-  p.delta = delta;
-  p.dq_acc = dq_acc;
-  p.dk = a.dk;
-  p.dv = a.dv;
-  p.status = a.status;
-  p.N = N;
-  p.Npad = Npad;
-  p.hq = a.hq;
-  p.hkv = a.hkv;
-  p.group = a.hq / a.hkv;
-  p.n_items = pl->Tk * a.hkv;
-  p.grad_f32 = a.grad_f32 ? 1 : 0;
-  p.scale = a.scale;
-  p.scale_log2 = a.scale * 1.4426950408889634f;
+  const int sms = sm_count();
+
+  DqParams d;
+  d.key_end = pl->dev.key_end;
+  d.qt_ptr = pl->dev.qt_ptr;
+  d.qt_kt = pl->dev.qt_kt;
+  d.qt_kind = pl->dev.qt_kind;
+  d.order = pl->dev.fwd_order;
+  d.o = static_cast<const __nv_bfloat16*>(a.o);
+  d.lse = a.lse;
+  d.lse2 = lse2;
+  d.delta = delta;
+  d.dq = a.dq;
+  d.status = a.status;
+  d.N = N;
+  d.Npad = Npad;
+  d.hq = a.hq;
+  d.group = a.hq / a.hkv;
+  d.n_items = pl->Tq * a.hq;
+  d.out_f32 = a.grad_f32 ? 1 : 0;
+  d.scale = a.scale;
+  d.scale_log2 = a.scale * kLog2e;
+
+  KvParams k;
+  k.key_end = pl->dev.key_end;
+  k.kt_qlo = pl->dev.kt_qlo;
+  k.kt_qhi = pl->dev.kt_qhi;
+  k.order = pl->dev.bwd_order;
+  k.lse2 = lse2;
+  k.delta = delta;
+  k.dk = a.dk;
+  k.dv = a.dv;
+  k.status = a.status;
+  k.N = N;
+  k.Npad = Npad;
+  k.hq = a.hq;
+  k.hkv = a.hkv;
+  k.group = a.hq / a.hkv;
+  k.n_items = pl->Tk * a.hkv;
+  k.out_f32 = a.grad_f32 ? 1 : 0;
+  k.scale = a.scale;
+  k.scale_log2 = a.scale * kLog2e;
+
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tree_attn_bwd_sm103,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(tree_attn_bwd_dq_sm103,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tree_attn_bwd_dkdv_sm103,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int grid = p.n_items < sm_count() ? p.n_items : sm_count();
-  tree_attn_bwd_sm103<<<grid, kThreads, kSmemBytes, a.stream>>>(mq, mk, mv, mdo, p);
+  tree_attn_bwd_dq_sm103<<<d.n_items < sms ? d.n_items : sms, kDqThreads, kDqSmem, a.stream>>>(
+      mq, mk, mv, mdo, d);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-
-  const long long n4 = static_cast<long long>(N) * a.hq * 128 / 4;
-  bwd_finalize_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, a.stream>>>(
-      dq_acc, a.dq, n4, a.scale, a.grad_f32 ? 1 : 0);
+  tree_attn_bwd_dkdv_sm103<<<k.n_items < sms ? k.n_items : sms, kKvThreads, kKvSmem, a.stream>>>(
+      mq, mk, mv, mdo, k);
   return cudaGetLastError();
 }
-
 
 }  // namespace treeattn

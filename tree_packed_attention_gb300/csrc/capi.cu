@@ -71,11 +71,10 @@ float resolve_scale(float s, int d) { return s == 0.f ? 1.f / std::sqrt(static_c
 
 }  // namespace
 
-// fp32 dQ accumulator [n, hq, d], then Delta and lse*log2(e), each [hq, npad].
-size_t bwd_workspace_bf16(int64_t n, int hq, int d) {
+// lse*log2(e) and Delta, each fp32 [hq, npad] (npad = 128 * number of q-tiles).
+size_t bwd_workspace_bf16(int64_t n, int hq, int /*d*/) {
   const int64_t npad = (n + kBlockM - 1) / kBlockM * kBlockM;
-  const int64_t acc = n * hq * d * 4;
-  return static_cast<size_t>((acc + 255) / 256 * 256 + 2 * hq * npad * 4);
+  return static_cast<size_t>(2 * hq * npad * 4);
 }
 
 }  // namespace treeattn
