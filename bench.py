@@ -66,7 +66,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -101,12 +101,14 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_oracle_sample(workload_index: int, seconds_hint: float = 20.0):
+def cpu_oracle_sample(workload_index: int, min_seconds: float = 10.0):
     """Time the CPU oracle (fp64) on a bounded sample of the workload.
 
-    The sample is one trie of the workload (the first root's subtree) with one
-    kv-head group (hq/hkv q heads, one kv head): full forward and backward.
-    Returns (visible-pair TFLOP/s, tokens/s, description, threads).
+    The sample is whole tries of the workload (the subtree of the first root,
+    then the next, ...) with one kv-head group each (hq/hkv q heads, one kv
+    head): full forward and backward, until at least ``min_seconds`` of CPU
+    work or every trie has been done. Returns (visible-pair TFLOP/s,
+    tokens/s, description, threads, seconds).
     """
     import numpy as np
     import torch
@@ -118,30 +120,40 @@ def cpu_oracle_sample(workload_index: int, seconds_hint: float = 20.0):
     w = treegen.workload(workload_index)
     parents = np.asarray(w.parents)
     roots = np.flatnonzero(parents == -1)
-    # the first trie: every segment whose root is roots[0]
+
     def root_of(s):
         while parents[s] != -1:
             s = parents[s]
         return s
 
-    members = [s for s in range(len(parents)) if root_of(s) == roots[0]]
-    remap = {s: n for n, s in enumerate(members)}
-    sub_p = np.array([-1 if parents[s] == -1 else remap[parents[s]] for s in members], np.int32)
-    sub_l = np.asarray(w.lengths)[members].astype(np.int32)
+    owner = np.array([root_of(s) for s in range(len(parents))])
     g = w.hq // w.hkv
-    n = int(sub_l.sum())
-    q, k, v, do = treegen.draw_tensors(n, g, 1, w.head_dim, w.dtype, seed=0)
     threads = len(os.sched_getaffinity(0))
     torch.set_num_threads(threads)
-    pvis = M.TrieView(sub_p, sub_l).visible_count()
-    t0 = time.perf_counter()
-    A.forward(q, k, v, sub_p, sub_l)
-    A.backward(q, k, v, do, sub_p, sub_l)
-    dt = time.perf_counter() - t0
-    flops = 14.0 * w.head_dim * g * pvis
-    desc = (f"one trie of the workload ({n} tokens, {len(members)} segments) x one kv group "
+    flops = 0.0
+    tokens = 0
+    done = 0
+    elapsed = 0.0
+    for t, r in enumerate(roots):
+        members = np.flatnonzero(owner == r).tolist()
+        remap = {s: n for n, s in enumerate(members)}
+        sub_p = np.array([-1 if parents[s] == -1 else remap[parents[s]] for s in members], np.int32)
+        sub_l = np.asarray(w.lengths)[members].astype(np.int32)
+        n = int(sub_l.sum())
+        q, k, v, do = treegen.draw_tensors(n, g, 1, w.head_dim, w.dtype, seed=t)
+        pvis = M.TrieView(sub_p, sub_l).visible_count()
+        t0 = time.perf_counter()
+        A.forward(q, k, v, sub_p, sub_l)
+        A.backward(q, k, v, do, sub_p, sub_l)
+        elapsed += time.perf_counter() - t0
+        flops += 14.0 * w.head_dim * g * pvis
+        tokens += n
+        done += 1
+        if elapsed >= min_seconds:
+            break
+    desc = (f"{done} of {len(roots)} tries of the workload ({tokens} tokens) x one kv group "
             f"({g} q heads, 1 kv head), fp64 forward + backward")
-    return flops / dt / 1e12, n / dt, desc, threads, dt
+    return flops / elapsed / 1e12, tokens / elapsed, desc, threads, elapsed
 
 
 def reference_arm(args):
@@ -154,10 +166,11 @@ def reference_arm(args):
     w = treegen.workload(args.workload)
     vals, toks, times = [], [], []
     desc, threads = "", 0
+    per_step = min(10.0, 150.0 / max(1, args.steps + args.warmup))  # whole run: a few minutes
     for _ in range(args.warmup):
-        cpu_oracle_sample(args.workload)
+        cpu_oracle_sample(args.workload, per_step)
     for _ in range(args.steps):
-        v, t, desc, threads, dt = cpu_oracle_sample(args.workload)
+        v, t, desc, threads, dt = cpu_oracle_sample(args.workload, per_step)
         vals.append(v)
         toks.append(t)
         times.append(dt)
@@ -308,15 +321,15 @@ def gpu_arm(args):
             "tokens_per_s": tokens_s,
             "fraction_of_bf16_peak": value / world / peak,
             "fwd": {"ms": fwd_mean, "tflops": fwd_tf, "frac": fwd_tf / peak, "launches": 1},
-            "bwd": {"ms": bwd_mean, "tflops": bwd_tf, "frac": bwd_tf / peak, "launches": 3},
+            "bwd": {"ms": bwd_mean, "tflops": bwd_tf, "frac": bwd_tf / peak, "launches": 2},
             "plan_build_ms": plan_ms,
-            "roofline": {"bound": "tensor", "kernel": "tree_attn_bwd (pre + main + finalize)",
+            "roofline": {"bound": "tensor", "kernel": "tree_attn_bwd (dQ kernel + dK/dV kernel)",
                          "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak,
                          "peak_source": f"{peak_kind} bf16 dense (burst)", "traffic": traffic},
             "clocks": clocks.summary(),
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": 3 * args.steps,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line))
@@ -327,7 +340,7 @@ def gpu_arm(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
