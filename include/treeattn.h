@@ -92,12 +92,12 @@ typedef enum {
   TREE_FIELD_QT_KIND = 15,    /* [nnz_tiles] 1 = PARTIAL (needs masking), 2 = FULL */
   TREE_FIELD_KT_QLO = 16,     /* [num_k_tiles] first q-tile that sees the k-tile */
   TREE_FIELD_KT_QHI = 17,     /* [num_k_tiles] one past the last; every q-tile in between sees it */
-  TREE_FIELD_FWD_ORDER = 18,  /* [num_q_tiles] q-tiles by tile count, largest first (ties: ascending) */
-  TREE_FIELD_BWD_ORDER = 19,  /* [num_k_tiles] k-tiles by q-tile range, largest first (ties: ascending) */
+  TREE_FIELD_FWD_ORDER = 18,  /* [num_q_tiles] forward/dQ work order: q-tiles last to first */
+  TREE_FIELD_BWD_ORDER = 19,  /* [num_k_tiles] dK/dV work order: k-tiles first to last */
   TREE_FIELD_QP_PTR = 20,     /* [num_pairs+1] CSR offsets of the q-tile-pair union lists */
   TREE_FIELD_QP_KT = 21,      /* [nnz_pair_tiles] union of the k-tiles of q-tiles 2p and 2p+1, ascending */
   TREE_FIELD_QP_KIND = 22,    /* [nnz_pair_tiles] kind for q-tile 2p | (kind for 2p+1) << 2; 0 = EMPTY */
-  TREE_FIELD_QP_ORDER = 23,   /* [num_pairs] pairs by total tile count, largest first (ties: ascending) */
+  TREE_FIELD_QP_ORDER = 23,   /* [num_pairs] forward work order of pairs: last to first */
   TREE_FIELD_COUNT = 24
 } tree_plan_field_t;
 

@@ -10,8 +10,9 @@ the masked blocks are skipped entirely; the map is what lets a kernel do so.
 ``key_end[j]`` is one past the last row that sees key j: the per-column bound
 in the spirit of A.1's "per-query start/end column bounds", taken here column-wise.
 
-Work orders (longest first) and the q-tile pair lists are conventions of this
-library for scheduling; the pages say nothing about them.
+Work orders and the q-tile pair lists are conventions of this library for
+scheduling; the pages say nothing about them. The orders follow DFS position:
+q-tiles and q-tile pairs from last to first, k-tiles from first to last.
 """
 from __future__ import annotations
 
@@ -111,13 +112,12 @@ def plan_fields(parents, lengths, bm: int = 128, bn: int = 128) -> dict:
         kt_qlo[kt] = min(kt_qlo[kt], qt)
         kt_qhi[kt] = max(kt_qhi[kt], qt + 1)
 
-    fwd_order = lpt_order([len(per_q[q]) for q in range(T_q)])
-    bwd_order = lpt_order([kt_qhi[k] - kt_qlo[k] for k in range(T_k)])
+    fwd_order = list(reversed(range(T_q)))
+    bwd_order = list(range(T_k))
 
     n_pairs = (T_q + 1) // 2
     qp_ptr = [0]
     qp_kt, qp_kind = [], []
-    pair_work = []
     for p in range(n_pairs):
         slots = [2 * p, 2 * p + 1]
         union = sorted(set(kt for q in slots if q < T_q for kt in per_q[q]))
@@ -127,8 +127,7 @@ def plan_fields(parents, lengths, bm: int = 128, bn: int = 128) -> dict:
             qp_kt.append(kt)
             qp_kind.append(k0 | (k1 << 2))
         qp_ptr.append(len(qp_kt))
-        pair_work.append(sum(len(per_q[q]) for q in slots if q < T_q))
-    qp_order = lpt_order(pair_work)
+    qp_order = list(reversed(range(n_pairs)))
 
     pos_id = T.position_ids(parents_l, lengths_l)
     i32 = lambda x: np.asarray(x, dtype=np.int32)  # noqa: E731
@@ -162,8 +161,3 @@ def plan_fields(parents, lengths, bm: int = 128, bn: int = 128) -> dict:
         "qp_kind": i32(qp_kind),
         "qp_order": i32(qp_order),
     }
-
-
-def lpt_order(work):
-    """Indices sorted by work, largest first; ties keep ascending index."""
-    return sorted(range(len(work)), key=lambda i: (-work[i], i))

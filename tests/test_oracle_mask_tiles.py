@@ -90,13 +90,10 @@ def test_orders_and_pair_lists():
     for p, L in _forests(60, seed=40, max_segments=12, max_len=20):
         f = TL.plan_fields(p, L, 4, 4)
         Tq = len(f["qt_ptr"]) - 1
-        nnz = np.diff(f["qt_ptr"])
-        assert sorted(f["fwd_order"].tolist()) == list(range(Tq))
-        w = nnz[f["fwd_order"]]
-        assert all(w[i] >= w[i + 1] for i in range(len(w) - 1))
-        span = (f["kt_qhi"] - f["kt_qlo"])[f["bwd_order"]]
-        assert all(span[i] >= span[i + 1] for i in range(len(span) - 1))
         npairs = (Tq + 1) // 2
+        assert f["fwd_order"].tolist() == list(range(Tq))[::-1]
+        assert f["bwd_order"].tolist() == list(range(Tq))
+        assert f["qp_order"].tolist() == list(range(npairs))[::-1]
         assert len(f["qp_ptr"]) == npairs + 1
         for pr in range(npairs):
             lst = f["qp_kt"][f["qp_ptr"][pr]:f["qp_ptr"][pr + 1]].tolist()

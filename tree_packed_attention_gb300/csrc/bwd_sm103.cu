@@ -371,13 +371,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         ++su[sb];
         tc_fence_after_sync();
         float pv[128];
+        {
+          uint32_t rr[128];
+          tmem_ld128(tSb, rr);  // the whole S row, one wait
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(tSb + c * 32, rr);
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj)
-            pv[c * 32 + jj] = ex2_approx(fmaf(__uint_as_float(rr[jj]), sl2, -lse2));
+          for (int jj = 0; jj < 128; ++jj)
+            pv[jj] = ex2_approx(fmaf(__uint_as_float(rr[jj]), sl2, -lse2));
         }
         if (ke) {
           const int j0 = kt * 128;
@@ -394,15 +393,20 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (!(ok = warp_wait(&bar_dp_full, n & 1, abort, p.status))) break;
         tc_fence_after_sync();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(tDP + lane_off + c * 32, rr);
-          uint32_t pk[16];
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t rr[64];
+          tmem_ld64(tDP + lane_off + h2 * 64, rr);  // half of the dP row, one wait
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
-            pk[jj] = pack_bf16x2(pv[c * 32 + 2 * jj] * (__uint_as_float(rr[2 * jj]) - delta),
-                                 pv[c * 32 + 2 * jj + 1] * (__uint_as_float(rr[2 * jj + 1]) - delta));
-          tmem_st16(tSb + c * 16, pk);  // dS over the first 64 columns of this S buffer
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int col = h2 * 64 + c * 32 + 2 * jj;
+              pk[jj] = pack_bf16x2(pv[col] * (__uint_as_float(rr[c * 32 + 2 * jj]) - delta),
+                                   pv[col + 1] * (__uint_as_float(rr[c * 32 + 2 * jj + 1]) - delta));
+            }
+            tmem_st16(tSb + (h2 * 2 + c) * 16, pk);  // dS over the first 64 columns of this S buffer
+          }
         }
         tmem_wait_st();
         tc_fence_before_sync();
@@ -432,10 +436,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 }
 
 // ============================================================ dK/dV kernel
-// 384 threads: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps 4-7
-// one key row per thread (P^T to TMEM, dS^T to smem), warps 8-11 the dK/dV
-// epilogue. TMEM: S^T/P^T | dP^T | dV | dK.
-constexpr int kKvThreads = 384;
+// 256 threads: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps 4-7
+// one key row per thread (P^T to TMEM, dS^T to smem, and at the end of an
+// item its dV and dK rows). TMEM: S^T/P^T | dP^T | dV | dK.
+constexpr int kKvThreads = 256;
 constexpr uint32_t kKvOffK = 0;
 constexpr uint32_t kKvOffV = kKvOffK + kTileBytes;
 constexpr uint32_t kKvOffQ = kKvOffV + kTileBytes;        // 2 stages
@@ -640,17 +644,17 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       mbar_drain(bar_final, 0);
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 8) {
-    // -------------------------------------------- P^T and dS^T, one key per thread
+  } else if (warp >= 4) {
+    // ---------- P^T and dS^T (one key row per thread), then each item's dK/dV
     const int quarter = warp % 4;
     const int kr = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tSr = tA + lane_off, tPr = tB + lane_off;
     uint8_t* ds_row = smem + kKvOffDS + kr * 128;
     const float sl2 = p.scale_log2;
-    uint32_t n = 0;
+    uint32_t n = 0, items = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++items) {
       const KvItem x = decode_kv(p, it);
       const int jk = x.kt * 128 + kr;
       const int ke = jk < p.N ? __ldg(p.key_end + jk) : 0;  // rows [jk, ke) see this key
@@ -664,22 +668,24 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tc_fence_after_sync();
         const bool full_row = jk <= q0 && q0 + 128 <= ke;  // every column visible to this key
         float pv[128];
+        {
+          uint32_t rr[128];
+          tmem_ld128(tSr, rr);  // the whole S^T row, one wait
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(tSr + c * 32, rr);
-          uint32_t pk[16];
-#pragma unroll
-          for (int jj = 0; jj < 32; jj += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c * 32 + jj);
+          for (int jj = 0; jj < 128; jj += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + jj);
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const int q = q0 + c * 32 + jj + u;
+              const int q = q0 + jj + u;
               const float e = ex2_approx(fmaf(__uint_as_float(rr[jj + u]), sl2, -lv[u]));
-              pv[c * 32 + jj + u] = (full_row || (jk <= q && q < ke)) ? e : 0.f;
+              pv[jj + u] = (full_row || (jk <= q && q < ke)) ? e : 0.f;
             }
           }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) pk[jj] = pack_bf16x2(pv[c * 32 + 2 * jj], pv[c * 32 + 2 * jj + 1]);
           tmem_st16(tSr + c * 16, pk);  // P^T over the first 64 columns of S^T
@@ -687,28 +693,31 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         if (!(ok = warp_wait(bar_dp_full, n & 1, abort, p.status))) break;
         tc_fence_after_sync();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(tPr + c * 32, rr);
-          uint32_t pk[16];
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t rr[64];
+          tmem_ld64(tPr + h2 * 64, rr);  // half of the dP^T row, one wait
 #pragma unroll
-          for (int jj = 0; jj < 32; jj += 4) {
-            const float4 d4 = *reinterpret_cast<const float4*>(dlt + c * 32 + jj);
-            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[16];
 #pragma unroll
-            for (int u = 0; u < 4; u += 2) {
-              const float ds0 = pv[c * 32 + jj + u] * (__uint_as_float(rr[jj + u]) - dv4[u]);
-              const float ds1 = pv[c * 32 + jj + u + 1] * (__uint_as_float(rr[jj + u + 1]) - dv4[u + 1]);
-              pk[(jj + u) / 2] = pack_bf16x2(ds0, ds1);
+            for (int jj = 0; jj < 32; jj += 4) {
+              const int col = h2 * 64 + c * 32 + jj;
+              const float4 d4 = *reinterpret_cast<const float4*>(dlt + col);
+              const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+              for (int u = 0; u < 4; u += 2) {
+                const float ds0 = pv[col + u] * (__uint_as_float(rr[c * 32 + jj + u]) - dv4[u]);
+                const float ds1 = pv[col + u + 1] * (__uint_as_float(rr[c * 32 + jj + u + 1]) - dv4[u + 1]);
+                pk[(jj + u) / 2] = pack_bf16x2(ds0, ds1);
+              }
             }
-          }
-          // dS^T row kr, q columns c*32 .. c*32+31: four 16-byte chunks, 128B-swizzled
+            // dS^T row kr, q columns 64*h2 + 32*c ..: four 16-byte chunks, 128B-swizzled
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int chunk = (c & 1) * 4 + u;
-            uint4* dst = reinterpret_cast<uint4*>(ds_row + (c >> 1) * kHalfBytes +
-                                                  ((chunk ^ (kr & 7)) * 16));
-            *dst = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+            for (int u = 0; u < 4; ++u) {
+              const int chunk = c * 4 + u;
+              uint4* dst = reinterpret_cast<uint4*>(ds_row + h2 * kHalfBytes + ((chunk ^ (kr & 7)) * 16));
+              *dst = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+            }
           }
         }
         tmem_wait_st();
@@ -716,19 +725,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tc_fence_before_sync();
         mbar_arrive(bar_ds_full);
       }
-    }
-  } else if (warp >= 8) {
-    // ------------------------------------------------- dK/dV epilogue
-    const int quarter = warp % 4;
-    const int kr = quarter * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    uint32_t items = 0;
-    bool ok = true;
-    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++items) {
-      const KvItem x = decode_kv(p, it);
+      if (!ok) break;
+      // ---- this item's dV and dK (scaled) from TMEM
       if (!(ok = warp_wait(bar_dkdv_full, items & 1, abort, p.status))) break;
       tc_fence_after_sync();
-      const int jk = x.kt * 128 + kr;
       const size_t out = (static_cast<size_t>(jk) * p.hkv + x.kvh) * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {

@@ -349,12 +349,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++sc;
         tc_fence_after_sync();
         float sv[128];
+        {
+          uint32_t rr[128];
+          tmem_ld128(tS, rr);  // the whole S row, one wait
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(tS + c * 32, rr);
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) sv[c * 32 + jj] = __uint_as_float(rr[jj]);
+          for (int jj = 0; jj < 128; ++jj) sv[jj] = __uint_as_float(rr[jj]);
         }
         if (ke) {
           const int j0 = kt * 128;

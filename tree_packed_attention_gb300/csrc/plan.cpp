@@ -32,15 +32,6 @@ tree_status_t fail(tree_status_t st, const std::string& msg) {
 
 namespace {
 
-// Indices sorted by work, largest first; ties keep ascending index.
-std::vector<int32_t> lpt_order(const std::vector<int64_t>& work) {
-  std::vector<int32_t> idx(work.size());
-  std::iota(idx.begin(), idx.end(), 0);
-  std::stable_sort(idx.begin(), idx.end(),
-                   [&](int32_t a, int32_t b) { return work[a] > work[b]; });
-  return idx;
-}
-
 tree_status_t build(const int32_t* parents, const int32_t* lengths, int32_t S, tree_plan* p) {
   auto& F = p->field;
   // ---- validation
@@ -232,12 +223,10 @@ tree_status_t build(const int32_t* parents, const int32_t* lengths, int32_t S, t
   std::vector<int32_t>& qp_kt = F[TREE_FIELD_QP_KT];
   std::vector<int32_t>& qp_kind = F[TREE_FIELD_QP_KIND];
   qp_ptr.assign(P + 1, 0);
-  std::vector<int64_t> pair_work(P, 0);
   for (int32_t pr = 0; pr < P; ++pr) {
     const int32_t q0 = 2 * pr, q1 = 2 * pr + 1;
     int32_t a = qt_ptr[q0], ae = qt_ptr[q0 + 1];
     int32_t b = q1 < Tq ? qt_ptr[q1] : 0, be = q1 < Tq ? qt_ptr[q1 + 1] : 0;
-    pair_work[pr] = (ae - a) + (be - b);
     while (a < ae || b < be) {
       int32_t kt, k0 = kEmpty, k1 = kEmpty;
       if (b >= be || (a < ae && qt_kt[a] < qt_kt[b])) {
@@ -257,15 +246,21 @@ tree_status_t build(const int32_t* parents, const int32_t* lengths, int32_t S, t
     qp_ptr[pr + 1] = static_cast<int32_t>(qp_kt.size());
   }
 
-  // ---- work orders, longest first
+  // ---- work orders: DFS position. Q-tiles (and pairs) last to first: a
+  // q-tile late in a trie sees at least as many keys as the ones before it
+  // on its path, so heavy work starts first, and neighbouring q-tiles, which
+  // share most of their k-tiles, run side by side. K-tiles first to last:
+  // ancestors precede their subtrees, so the longest q-tile ranges start first.
   {
-    std::vector<int64_t> w(Tq);
-    for (int32_t qt = 0; qt < Tq; ++qt) w[qt] = qt_ptr[qt + 1] - qt_ptr[qt];
-    F[TREE_FIELD_FWD_ORDER] = lpt_order(w);
-    std::vector<int64_t> wb(Tk);
-    for (int32_t kt = 0; kt < Tk; ++kt) wb[kt] = kt_qhi[kt] - kt_qlo[kt];
-    F[TREE_FIELD_BWD_ORDER] = lpt_order(wb);
-    F[TREE_FIELD_QP_ORDER] = lpt_order(pair_work);
+    std::vector<int32_t>& fo = F[TREE_FIELD_FWD_ORDER];
+    fo.resize(Tq);
+    for (int32_t t = 0; t < Tq; ++t) fo[t] = Tq - 1 - t;
+    std::vector<int32_t>& po = F[TREE_FIELD_QP_ORDER];
+    po.resize(P);
+    for (int32_t t = 0; t < P; ++t) po[t] = P - 1 - t;
+    std::vector<int32_t>& bo = F[TREE_FIELD_BWD_ORDER];
+    bo.resize(Tk);
+    std::iota(bo.begin(), bo.end(), 0);
   }
 
   p->N = N;

@@ -193,6 +193,9 @@ def workload(index: int, seed: int = 0) -> Workload:
     if index == 5:
         p, L = packed_tries(seed)
         return Workload("packed-32-tries-128k-bf16-hq64-hkv8-d128", p, L, 64, 8, 128, "bf16")
+    if index == 6:  # workload 5's shape at a quarter of the size (profiling captures)
+        p, L = packed_tries(seed, n_tries=8, total=32768)
+        return Workload("packed-8-tries-32k-bf16-hq64-hkv8-d128", p, L, 64, 8, 128, "bf16")
     raise ValueError(f"unknown workload {index}")
 
 
