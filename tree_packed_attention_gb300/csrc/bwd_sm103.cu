@@ -55,17 +55,6 @@ __device__ __forceinline__ void mma_kk(uint32_t d, uint32_t a, uint32_t b, uint3
   }
 }
 
-// D = A B^T, A K-major in smem, B MN-major in smem (stored K rows x N contiguous).
-__device__ __forceinline__ void mma_kn(uint32_t d, uint32_t a, uint32_t b, uint32_t acc) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-    mma_ss(d, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + kk * 2048, kHalfBytes, 1024), idesc,
-           (acc || kk > 0) ? 1u : 0u);
-  }
-}
-
 // D = A B^T, A from TMEM (bf16 pairs, 128 lanes x 64 columns), B MN-major in smem.
 __device__ __forceinline__ void mma_tn(uint32_t d, uint32_t a_tmem, uint32_t b, uint32_t acc) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
@@ -102,12 +91,15 @@ __device__ __forceinline__ void store_row(void* dst_base, size_t off, int c, con
 // written as bf16 over the first 64 columns of the S buffer it came from and
 // read by the dQ MMA from TMEM.
 constexpr int kDqThreads = 256;
-constexpr int kDqStages = 2;
+// K_t is read by S_t and, a step later, by dQ_t; S_{t+2} is issued right after
+// dQ_t, so K needs a third stage for its load to overlap a whole step.
+constexpr int kDqKStages = 3;
+constexpr int kDqVStages = 2;
 constexpr uint32_t kDqOffQ = 0;
 constexpr uint32_t kDqOffDO = kTileBytes;
-constexpr uint32_t kDqOffK = 2 * kTileBytes;                    // kDqStages tiles
-constexpr uint32_t kDqOffV = kDqOffK + kDqStages * kTileBytes;  // kDqStages tiles
-constexpr uint32_t kDqSmem = 1024 + kDqOffV + kDqStages * kTileBytes;
+constexpr uint32_t kDqOffK = 2 * kTileBytes;
+constexpr uint32_t kDqOffV = kDqOffK + kDqKStages * kTileBytes;
+constexpr uint32_t kDqSmem = 1024 + kDqOffV + kDqVStages * kTileBytes;
 
 struct DqParams {
   const int32_t* key_end;
@@ -134,8 +126,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t bar_q_full, bar_q_empty, bar_final;
-  __shared__ uint64_t bar_k_full[kDqStages], bar_k_empty[kDqStages];
-  __shared__ uint64_t bar_v_full[kDqStages], bar_v_empty[kDqStages];
+  __shared__ uint64_t bar_k_full[kDqKStages], bar_k_empty[kDqKStages];
+  __shared__ uint64_t bar_v_full[kDqVStages], bar_v_empty[kDqVStages];
   __shared__ uint64_t bar_s_full[2];  // one per S buffer: a buffer is refilled only after
                                      // its dS was consumed, so each barrier is at most one phase ahead
   __shared__ uint64_t bar_dp_full, bar_ds_full, bar_dq_full, bar_dq_free;
@@ -150,9 +142,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&bar_q_full, 1);
     mbar_init(&bar_q_empty, 1);
     mbar_init(&bar_final, 1);
-    for (int s = 0; s < kDqStages; ++s) {
+    for (int s = 0; s < kDqKStages; ++s) {
       mbar_init(&bar_k_full[s], 1);
       mbar_init(&bar_k_empty[s], 1);
+    }
+    for (int s = 0; s < kDqVStages; ++s) {
       mbar_init(&bar_v_full[s], 1);
       mbar_init(&bar_v_empty[s], 1);
     }
@@ -201,30 +195,31 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       ++qn;
       for (int t = p.qt_ptr[qt]; t < p.qt_ptr[qt + 1]; ++t, ++kv) {
         const int row0 = p.qt_kt[t] * 128;
-        const uint32_t st = kv % kDqStages, ph = (kv / kDqStages) & 1;
-        if (kv >= kDqStages && !(ok = warp_wait(&bar_k_empty[st], ph ^ 1, abort, p.status))) break;
+        const uint32_t sk = kv % kDqKStages, pk = (kv / kDqKStages) & 1;
+        if (kv >= kDqKStages && !(ok = warp_wait(&bar_k_empty[sk], pk ^ 1, abort, p.status))) break;
         if (lane == 0) {
-          uint8_t* dst = smem + kDqOffK + st * kTileBytes;
-          mbar_arrive_expect_tx(&bar_k_full[st], kTileBytes);
-          tma_load_3d(dst, &map_k, &bar_k_full[st], 0, kvh, row0);
-          tma_load_3d(dst + kHalfBytes, &map_k, &bar_k_full[st], 64, kvh, row0);
+          uint8_t* dst = smem + kDqOffK + sk * kTileBytes;
+          mbar_arrive_expect_tx(&bar_k_full[sk], kTileBytes);
+          tma_load_3d(dst, &map_k, &bar_k_full[sk], 0, kvh, row0);
+          tma_load_3d(dst + kHalfBytes, &map_k, &bar_k_full[sk], 64, kvh, row0);
         }
         __syncwarp();
-        if (kv >= kDqStages && !(ok = warp_wait(&bar_v_empty[st], ph ^ 1, abort, p.status))) break;
+        const uint32_t sv = kv % kDqVStages, pv = (kv / kDqVStages) & 1;
+        if (kv >= kDqVStages && !(ok = warp_wait(&bar_v_empty[sv], pv ^ 1, abort, p.status))) break;
         if (lane == 0) {
-          uint8_t* dst = smem + kDqOffV + st * kTileBytes;
-          mbar_arrive_expect_tx(&bar_v_full[st], kTileBytes);
-          tma_load_3d(dst, &map_v, &bar_v_full[st], 0, kvh, row0);
-          tma_load_3d(dst + kHalfBytes, &map_v, &bar_v_full[st], 64, kvh, row0);
+          uint8_t* dst = smem + kDqOffV + sv * kTileBytes;
+          mbar_arrive_expect_tx(&bar_v_full[sv], kTileBytes);
+          tma_load_3d(dst, &map_v, &bar_v_full[sv], 0, kvh, row0);
+          tma_load_3d(dst + kHalfBytes, &map_v, &bar_v_full[sv], 64, kvh, row0);
         }
         __syncwarp();
       }
     }
     if (!ok && lane == 0) {
       if (qn > 0) mbar_drain(&bar_q_full, (qn - 1) & 1);
-      for (uint32_t i = kv >= kDqStages ? kv - kDqStages : 0; i <= kv; ++i) {
-        mbar_drain(&bar_k_full[i % kDqStages], (i / kDqStages) & 1);
-        mbar_drain(&bar_v_full[i % kDqStages], (i / kDqStages) & 1);
+      for (uint32_t i = kv >= kDqKStages ? kv - kDqKStages : 0; i <= kv; ++i) {
+        mbar_drain(&bar_k_full[i % kDqKStages], (i / kDqKStages) & 1);
+        mbar_drain(&bar_v_full[i % kDqVStages], (i / kDqVStages) & 1);
       }
     }
   } else if (warp == 1) {
@@ -240,13 +235,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const int T = p.qt_ptr[qt + 1] - p.qt_ptr[qt];
       if (!(ok = warp_wait(&bar_q_full, qn & 1, abort, p.status))) break;
       ++qn;
-      auto k_stage = [&](uint32_t i) { return aK + (i % kDqStages) * kTileBytes; };
-      auto v_stage = [&](uint32_t i) { return aV + (i % kDqStages) * kTileBytes; };
+      auto k_stage = [&](uint32_t i) { return aK + (i % kDqKStages) * kTileBytes; };
+      auto v_stage = [&](uint32_t i) { return aV + (i % kDqVStages) * kTileBytes; };
       auto wait_k = [&](uint32_t i) {
-        return warp_wait(&bar_k_full[i % kDqStages], (i / kDqStages) & 1, abort, p.status);
+        return warp_wait(&bar_k_full[i % kDqKStages], (i / kDqKStages) & 1, abort, p.status);
       };
       auto wait_v = [&](uint32_t i) {
-        return warp_wait(&bar_v_full[i % kDqStages], (i / kDqStages) & 1, abort, p.status);
+        return warp_wait(&bar_v_full[i % kDqVStages], (i / kDqVStages) & 1, abort, p.status);
       };
       if (!(ok = wait_k(kv))) break;
       tc_fence_after_sync();
@@ -260,7 +255,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       if (lane == 0) {
         mma_kk(tDP, aDO, v_stage(kv), 0);  // dP_0
         mma_commit(&bar_dp_full);
-        mma_commit(&bar_v_empty[kv % kDqStages]);
+        mma_commit(&bar_v_empty[kv % kDqVStages]);
       }
       __syncwarp();
       if (T > 1) {
@@ -280,7 +275,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         tc_fence_after_sync();
         if (lane == 0) {
           mma_tn(tDQ, tS + (t & 1) * 128, k_stage(i), t > 0);  // dQ += dS_t K_t
-          mma_commit(&bar_k_empty[i % kDqStages]);
+          mma_commit(&bar_k_empty[i % kDqKStages]);
           if (t + 1 == T) {
             mma_commit(&bar_dq_full);
             mma_commit(&bar_q_empty);
@@ -293,7 +288,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           if (lane == 0) {
             mma_kk(tDP, aDO, v_stage(i + 1), 0);  // dP_{t+1} (dP_t already read)
             mma_commit(&bar_dp_full);
-            mma_commit(&bar_v_empty[(i + 1) % kDqStages]);
+            mma_commit(&bar_v_empty[(i + 1) % kDqVStages]);
           }
           __syncwarp();
         }
@@ -437,18 +432,23 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
 // ============================================================ dK/dV kernel
 // 256 threads: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps 4-7
-// one key row per thread (P^T to TMEM, dS^T to smem, and at the end of an
-// item its dV and dK rows). TMEM: S^T/P^T | dP^T | dV | dK.
+// one key row per thread (P^T and dS^T into TMEM, and at the end of an item
+// its dV and dK rows). TMEM: S^T, then P^T in its first 64 columns | dP^T,
+// then dS^T in its first 64 columns | dV | dK. Both products that need P^T
+// and dS^T read them from TMEM, so no operand is written to shared memory.
+// Q_n is read by S^T_n and, a step later, by dK_n, so Q is staged three deep;
+// dO_n (with the step's lse and Delta) is released after dV_n, two deep.
 constexpr int kKvThreads = 256;
+constexpr int kKvQStages = 3;
+constexpr int kKvDoStages = 2;
 constexpr uint32_t kKvOffK = 0;
 constexpr uint32_t kKvOffV = kKvOffK + kTileBytes;
-constexpr uint32_t kKvOffQ = kKvOffV + kTileBytes;        // 2 stages
-constexpr uint32_t kKvOffDO = kKvOffQ + 2 * kTileBytes;   // 2 stages
-constexpr uint32_t kKvOffDS = kKvOffDO + 2 * kTileBytes;  // dS^T, 128 keys x 128 q
-constexpr uint32_t kKvOffLse = kKvOffDS + kTileBytes;     // 2 stages x 128 fp32
-constexpr uint32_t kKvOffDelta = kKvOffLse + 2 * 512;     // 2 stages x 128 fp32
-constexpr uint32_t kKvOffBar = kKvOffDelta + 2 * 512;
-constexpr uint32_t kKvNumBars = 16;
+constexpr uint32_t kKvOffQ = kKvOffV + kTileBytes;
+constexpr uint32_t kKvOffDO = kKvOffQ + kKvQStages * kTileBytes;
+constexpr uint32_t kKvOffLse = kKvOffDO + kKvDoStages * kTileBytes;  // per dO stage: 128 fp32
+constexpr uint32_t kKvOffDelta = kKvOffLse + kKvDoStages * 512;     // per dO stage: 128 fp32
+constexpr uint32_t kKvOffBar = kKvOffDelta + kKvDoStages * 512;
+constexpr uint32_t kKvNumBars = 20;
 constexpr uint32_t kKvSmem = kKvOffBar + kKvNumBars * 8 + 16;
 static_assert(kKvSmem <= 232448, "shared memory budget");
 
@@ -494,23 +494,29 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kKvOffBar);
   uint64_t* bar_kv_full = bars + 0;
   uint64_t* bar_kv_empty = bars + 1;
-  uint64_t* bar_qdo_full = bars + 2;   // [2]
-  uint64_t* bar_qdo_empty = bars + 4;  // [2]
-  uint64_t* bar_s_full = bars + 6;
-  uint64_t* bar_dp_full = bars + 7;
-  uint64_t* bar_ds_full = bars + 8;
-  uint64_t* bar_dkdv_full = bars + 9;
-  uint64_t* bar_dkdv_free = bars + 10;
-  uint64_t* bar_final = bars + 11;
+  uint64_t* bar_q_full = bars + 2;    // [kKvQStages]
+  uint64_t* bar_q_empty = bars + 5;   // [kKvQStages]
+  uint64_t* bar_do_full = bars + 8;   // [kKvDoStages]
+  uint64_t* bar_do_empty = bars + 10; // [kKvDoStages]
+  uint64_t* bar_s_full = bars + 12;
+  uint64_t* bar_dp_full = bars + 13;
+  uint64_t* bar_ds_full = bars + 14;
+  uint64_t* bar_dkdv_full = bars + 15;
+  uint64_t* bar_dkdv_free = bars + 16;
+  uint64_t* bar_final = bars + 17;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kKvNumBars);
   volatile int* abort = reinterpret_cast<volatile int*>(bars + kKvNumBars) + 1;
 
   if (threadIdx.x == 0) {
     mbar_init(bar_kv_full, 1);
     mbar_init(bar_kv_empty, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar_qdo_full + s, 1);
-      mbar_init(bar_qdo_empty + s, 1);
+    for (int s = 0; s < kKvQStages; ++s) {
+      mbar_init(bar_q_full + s, 1);
+      mbar_init(bar_q_empty + s, 1);
+    }
+    for (int s = 0; s < kKvDoStages; ++s) {
+      mbar_init(bar_do_full + s, 1);
+      mbar_init(bar_do_empty + s, 1);
     }
     mbar_init(bar_s_full, 1);
     mbar_init(bar_dp_full, 1);
@@ -556,50 +562,68 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       for (int j = 0; j < x.steps; ++j, ++n) {
         const int h = x.kvh * p.group + j / x.nq;
         const int qt = x.qlo + j % x.nq;
-        const uint32_t st = n & 1, ph = (n >> 1) & 1;
-        if (n >= 2 && !(ok = warp_wait(bar_qdo_empty + st, ph ^ 1, abort, p.status))) break;
+        const uint32_t sq = n % kKvQStages, pq = (n / kKvQStages) & 1;
+        if (n >= kKvQStages && !(ok = warp_wait(bar_q_empty + sq, pq ^ 1, abort, p.status))) break;
         if (lane == 0) {
-          uint64_t* b = bar_qdo_full + st;
-          mbar_arrive_expect_tx(b, 2 * kTileBytes + 1024);
-          uint8_t* q = smem + kKvOffQ + st * kTileBytes;
-          uint8_t* d = smem + kKvOffDO + st * kTileBytes;
-          tma_load_3d(q, &map_q, b, 0, h, qt * 128);
-          tma_load_3d(q + kHalfBytes, &map_q, b, 64, h, qt * 128);
+          uint8_t* q = smem + kKvOffQ + sq * kTileBytes;
+          mbar_arrive_expect_tx(bar_q_full + sq, kTileBytes);
+          tma_load_3d(q, &map_q, bar_q_full + sq, 0, h, qt * 128);
+          tma_load_3d(q + kHalfBytes, &map_q, bar_q_full + sq, 64, h, qt * 128);
+        }
+        __syncwarp();
+        const uint32_t sd = n % kKvDoStages, pd = (n / kKvDoStages) & 1;
+        if (n >= kKvDoStages && !(ok = warp_wait(bar_do_empty + sd, pd ^ 1, abort, p.status))) break;
+        if (lane == 0) {
+          uint64_t* b = bar_do_full + sd;
+          uint8_t* d = smem + kKvOffDO + sd * kTileBytes;
+          mbar_arrive_expect_tx(b, kTileBytes + 1024);
           tma_load_3d(d, &map_do, b, 0, h, qt * 128);
           tma_load_3d(d + kHalfBytes, &map_do, b, 64, h, qt * 128);
           const size_t off = static_cast<size_t>(h) * p.Npad + qt * 128;
-          bulk_load(smem + kKvOffLse + st * 512, p.lse2 + off, 512, b);
-          bulk_load(smem + kKvOffDelta + st * 512, p.delta + off, 512, b);
+          bulk_load(smem + kKvOffLse + sd * 512, p.lse2 + off, 512, b);
+          bulk_load(smem + kKvOffDelta + sd * 512, p.delta + off, 512, b);
         }
         __syncwarp();
       }
     }
     if (!ok && lane == 0) {
       if (items > 0) mbar_drain(bar_kv_full, (items - 1) & 1);
-      for (uint32_t i = n >= 2 ? n - 2 : 0; i <= n; ++i) mbar_drain(bar_qdo_full + (i & 1), (i >> 1) & 1);
+      for (uint32_t i = n >= kKvQStages ? n - kKvQStages : 0; i <= n; ++i) {
+        mbar_drain(bar_q_full + i % kKvQStages, (i / kKvQStages) & 1);
+        mbar_drain(bar_do_full + i % kKvDoStages, (i / kKvDoStages) & 1);
+      }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     // Per step n (S^T_n and dP^T_n already issued):
     //   [dS_n] dV += P^T_n dO_n, S^T_{n+1}, dK += dS^T_n Q_n, dP^T_{n+1}
     const uint32_t aK = smem_u32(smem + kKvOffK), aV = smem_u32(smem + kKvOffV);
-    const uint32_t aDS = smem_u32(smem + kKvOffDS);
+    auto q_addr = [&](uint32_t i) { return smem_u32(smem + kKvOffQ + (i % kKvQStages) * kTileBytes); };
+    auto do_addr = [&](uint32_t i) { return smem_u32(smem + kKvOffDO + (i % kKvDoStages) * kTileBytes); };
+    auto wait_q = [&](uint32_t i) {
+      return warp_wait(bar_q_full + i % kKvQStages, (i / kKvQStages) & 1, abort, p.status);
+    };
+    auto wait_do = [&](uint32_t i) {
+      return warp_wait(bar_do_full + i % kKvDoStages, (i / kKvDoStages) & 1, abort, p.status);
+    };
     uint32_t n = 0, items = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++items) {
       const KvItem x = decode_kv(p, it);
       if (!(ok = warp_wait(bar_kv_full, items & 1, abort, p.status))) break;
       for (int j = 0; j < x.steps; ++j, ++n) {
-        const uint32_t st = n & 1, ph = (n >> 1) & 1;
-        const uint32_t aQ = smem_u32(smem + kKvOffQ + st * kTileBytes);
-        const uint32_t aDO = smem_u32(smem + kKvOffDO + st * kTileBytes);
         if (j == 0) {
-          if (!(ok = warp_wait(bar_qdo_full + st, ph, abort, p.status))) break;
+          if (!(ok = wait_q(n))) break;
           tc_fence_after_sync();
           if (lane == 0) {
-            mma_kk(tA, aK, aQ, 0);  // S^T = K Q^T
+            mma_kk(tA, aK, q_addr(n), 0);  // S^T = K Q^T
             mma_commit(bar_s_full);
-            mma_kk(tB, aV, aDO, 0);  // dP^T = V dO^T
+          }
+          __syncwarp();
+          if (!(ok = wait_do(n))) break;
+          tc_fence_after_sync();
+          if (lane == 0) {
+            mma_kk(tB, aV, do_addr(n), 0);  // dP^T = V dO^T
             mma_commit(bar_dp_full);
           }
           __syncwarp();
@@ -609,28 +633,35 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             !(ok = warp_wait(bar_dkdv_free, (items - 1) & 1, abort, p.status)))
           break;
         tc_fence_after_sync();
-        if (lane == 0) mma_tn(tC, tA, aDO, j > 0);  // dV += P^T dO
+        if (lane == 0) {
+          mma_tn(tC, tA, do_addr(n), j > 0);  // dV += P^T dO
+          mma_commit(bar_do_empty + n % kKvDoStages);
+        }
         __syncwarp();
         const bool has_next = j + 1 < x.steps;
-        const uint32_t stn = (n + 1) & 1, phn = ((n + 1) >> 1) & 1;
         if (has_next) {
-          if (!(ok = warp_wait(bar_qdo_full + stn, phn, abort, p.status))) break;
+          if (!(ok = wait_q(n + 1))) break;
           tc_fence_after_sync();
           if (lane == 0) {
-            mma_kk(tA, aK, smem_u32(smem + kKvOffQ + stn * kTileBytes), 0);  // next S^T
+            mma_kk(tA, aK, q_addr(n + 1), 0);  // next S^T (P^T_n already read by dV)
             mma_commit(bar_s_full);
           }
           __syncwarp();
         }
         if (lane == 0) {
-          mma_kn(tD, aDS, aQ, j > 0);  // dK += dS^T Q
-          mma_commit(bar_qdo_empty + st);
-          if (has_next) {
-            mma_kk(tB, aV, smem_u32(smem + kKvOffDO + stn * kTileBytes), 0);  // next dP^T
-            mma_commit(bar_dp_full);
-          }
+          mma_tn(tD, tB, q_addr(n), j > 0);  // dK += dS^T Q (dS^T from TMEM)
+          mma_commit(bar_q_empty + n % kKvQStages);
         }
         __syncwarp();
+        if (has_next) {
+          if (!(ok = wait_do(n + 1))) break;
+          tc_fence_after_sync();
+          if (lane == 0) {
+            mma_kk(tB, aV, do_addr(n + 1), 0);  // next dP^T (dS^T_n already read by dK)
+            mma_commit(bar_dp_full);
+          }
+          __syncwarp();
+        }
       }
       if (!ok) break;
       if (lane == 0) {
@@ -650,7 +681,6 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const int kr = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tSr = tA + lane_off, tPr = tB + lane_off;
-    uint8_t* ds_row = smem + kKvOffDS + kr * 128;
     const float sl2 = p.scale_log2;
     uint32_t n = 0, items = 0;
     bool ok = true;
@@ -660,10 +690,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       const int ke = jk < p.N ? __ldg(p.key_end + jk) : 0;  // rows [jk, ke) see this key
       for (int j = 0; j < x.steps; ++j, ++n) {
         const int q0 = (x.qlo + j % x.nq) * 128;
-        const uint32_t st = n & 1, ph = (n >> 1) & 1;
-        const float* lse2 = reinterpret_cast<const float*>(smem + kKvOffLse + st * 512);
-        const float* dlt = reinterpret_cast<const float*>(smem + kKvOffDelta + st * 512);
-        if (!(ok = warp_wait(bar_qdo_full + st, ph, abort, p.status))) break;
+        const uint32_t sd = n % kKvDoStages, pd = (n / kKvDoStages) & 1;
+        const float* lse2 = reinterpret_cast<const float*>(smem + kKvOffLse + sd * 512);
+        const float* dlt = reinterpret_cast<const float*>(smem + kKvOffDelta + sd * 512);
+        if (!(ok = warp_wait(bar_do_full + sd, pd, abort, p.status))) break;
         if (!(ok = warp_wait(bar_s_full, n & 1, abort, p.status))) break;
         tc_fence_after_sync();
         const bool full_row = jk <= q0 && q0 + 128 <= ke;  // every column visible to this key
@@ -695,7 +725,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           uint32_t rr[64];
-          tmem_ld64(tPr + h2 * 64, rr);  // half of the dP^T row, one wait
+          tmem_ld64(tPr + h2 * 64, rr);  // dP^T columns 64*h2 .. +63, one wait
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t pk[16];
@@ -711,17 +741,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 pk[(jj + u) / 2] = pack_bf16x2(ds0, ds1);
               }
             }
-            // dS^T row kr, q columns 64*h2 + 32*c ..: four 16-byte chunks, 128B-swizzled
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int chunk = c * 4 + u;
-              uint4* dst = reinterpret_cast<uint4*>(ds_row + h2 * kHalfBytes + ((chunk ^ (kr & 7)) * 16));
-              *dst = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-            }
+            // dS^T (q columns 64*h2 + 32*c ..) over columns of dP^T already read
+            tmem_st16(tPr + (h2 * 2 + c) * 16, pk);
           }
         }
         tmem_wait_st();
-        fence_proxy_async_smem();
         tc_fence_before_sync();
         mbar_arrive(bar_ds_full);
       }
