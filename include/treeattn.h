@@ -170,6 +170,32 @@ tree_status_t tree_attn_bwd(const tree_plan_t* plan, const void* dout, const voi
                             tree_dtype_t grad_dtype, float softmax_scale, void* workspace,
                             size_t workspace_bytes, tree_stream_t stream);
 
+/*
+ * Backward for callers that cannot allocate device memory when they call it
+ * (for example a runtime whose memory pool already owns the whole device, or a
+ * latency-critical loop where a cudaMalloc would synchronize the device).
+ * The paper has no counterpart: this is tree_attn_bwd (same arguments, same
+ * results) with its scratch taken from a fixed array of
+ * TREE_STATIC_SCRATCH_BYTES compiled into the library instead of from a
+ * workspace argument. It calls no cudaMalloc, cudaFree or allocating routine.
+ *  - Size limit: requests whose tree_attn_bwd_workspace_bytes exceeds
+ *    TREE_STATIC_SCRATCH_BYTES return TREE_ERR_UNSUPPORTED with a message.
+ *  - Every GPU that loads the library holds the array until the process exits.
+ *  - The first call on a device looks the array's device address up (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture.
+ *  - All calls share the one array: calls that overlap on the GPU (on
+ *    different streams, or from different threads) race on it. Stale contents
+ *    from an earlier call are harmless; nothing needs clearing.
+ */
+#define TREE_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+tree_status_t tree_attn_bwd_static_scratch(const tree_plan_t* plan, const void* dout, const void* q,
+                                           const void* k, const void* v, const void* o,
+                                           const float* lse, void* dq, void* dk, void* dv,
+                                           int32_t hq, int32_t hkv, int32_t head_dim,
+                                           tree_dtype_t dtype, tree_dtype_t grad_dtype,
+                                           float softmax_scale, tree_stream_t stream);
+
 /* Per-token loss weights g_t / K of the token's trie (§3.1 eq. 4, §3.2 "Loss
  * Weights"), each rounded once to fp32, into host memory out_host[N]. */
 tree_status_t tree_weights(const tree_plan_t* plan, float* out_host);

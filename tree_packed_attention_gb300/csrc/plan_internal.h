@@ -7,7 +7,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/treeattn.h"
+#include "treeattn.h"
 
 namespace treeattn {
 
