@@ -45,23 +45,24 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // D = A B^T, A and B both K-major 128 x 128 tiles (K = 128).
+// The GEMM helpers are warp-collective: one elected lane issues each MMA.
 __device__ __forceinline__ void mma_kk(uint32_t d, uint32_t a, uint32_t b, uint32_t acc) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+  const uint64_t ad = sdesc_sw128(a, 16, 1024), bd = sdesc_sw128(b, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-    mma_ss(d, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + off, 16, 1024), idesc,
-           (acc || kk > 0) ? 1u : 0u);
+    mma_ss_warp(d, sdesc_advance(ad, off), sdesc_advance(bd, off), idesc, (acc || kk > 0) ? 1u : 0u);
   }
 }
 
 // D = A B^T, A from TMEM (bf16 pairs, 128 lanes x 64 columns), B MN-major in smem.
 __device__ __forceinline__ void mma_tn(uint32_t d, uint32_t a_tmem, uint32_t b, uint32_t acc) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+  const uint64_t bd = sdesc_sw128(b, kHalfBytes, 1024);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
-    mma_ts(d, a_tmem + kk * 8, sdesc_sw128(b + kk * 2048, kHalfBytes, 1024), idesc,
-           (acc || kk > 0) ? 1u : 0u);
+    mma_ts_warp(d, a_tmem + kk * 8, sdesc_advance(bd, kk * 2048), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
 // Write 32 consecutive fp32 values of one 128-wide row, times `mul`, as fp32 or bf16.
@@ -245,27 +246,18 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       };
       if (!(ok = wait_k(kv))) break;
       tc_fence_after_sync();
-      if (lane == 0) {
-        mma_kk(tS, aQ, k_stage(kv), 0);  // S_0
-        mma_commit(&bar_s_full[0]);
-      }
-      __syncwarp();
+      mma_kk(tS, aQ, k_stage(kv), 0);  // S_0
+      mma_commit_warp(&bar_s_full[0]);
       if (!(ok = wait_v(kv))) break;
       tc_fence_after_sync();
-      if (lane == 0) {
-        mma_kk(tDP, aDO, v_stage(kv), 0);  // dP_0
-        mma_commit(&bar_dp_full);
-        mma_commit(&bar_v_empty[kv % kDqVStages]);
-      }
-      __syncwarp();
+      mma_kk(tDP, aDO, v_stage(kv), 0);  // dP_0
+      mma_commit_warp(&bar_dp_full);
+      mma_commit_warp(&bar_v_empty[kv % kDqVStages]);
       if (T > 1) {
         if (!(ok = wait_k(kv + 1))) break;
         tc_fence_after_sync();
-        if (lane == 0) {
-          mma_kk(tS + 128, aQ, k_stage(kv + 1), 0);  // S_1
-          mma_commit(&bar_s_full[1]);
-        }
-        __syncwarp();
+        mma_kk(tS + 128, aQ, k_stage(kv + 1), 0);  // S_1
+        mma_commit_warp(&bar_s_full[1]);
       }
       for (int t = 0; t < T && ok; ++t, ++n) {
         const uint32_t i = kv + t;
@@ -273,42 +265,30 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (t == 0 && qn > 1 && !(ok = warp_wait(&bar_dq_free, (qn - 2) & 1, abort, p.status)))
           break;
         tc_fence_after_sync();
-        if (lane == 0) {
-          mma_tn(tDQ, tS + (t & 1) * 128, k_stage(i), t > 0);  // dQ += dS_t K_t
-          mma_commit(&bar_k_empty[i % kDqKStages]);
-          if (t + 1 == T) {
-            mma_commit(&bar_dq_full);
-            mma_commit(&bar_q_empty);
-          }
+        mma_tn(tDQ, tS + (t & 1) * 128, k_stage(i), t > 0);  // dQ += dS_t K_t
+        mma_commit_warp(&bar_k_empty[i % kDqKStages]);
+        if (t + 1 == T) {
+          mma_commit_warp(&bar_dq_full);
+          mma_commit_warp(&bar_q_empty);
         }
-        __syncwarp();
         if (t + 1 < T) {
           if (!(ok = wait_v(i + 1))) break;
           tc_fence_after_sync();
-          if (lane == 0) {
-            mma_kk(tDP, aDO, v_stage(i + 1), 0);  // dP_{t+1} (dP_t already read)
-            mma_commit(&bar_dp_full);
-            mma_commit(&bar_v_empty[(i + 1) % kDqVStages]);
-          }
-          __syncwarp();
+          mma_kk(tDP, aDO, v_stage(i + 1), 0);  // dP_{t+1} (dP_t already read)
+          mma_commit_warp(&bar_dp_full);
+          mma_commit_warp(&bar_v_empty[(i + 1) % kDqVStages]);
         }
         if (t + 2 < T) {
           if (!(ok = wait_k(i + 2))) break;
           tc_fence_after_sync();
-          if (lane == 0) {
-            mma_kk(tS + (t & 1) * 128, aQ, k_stage(i + 2), 0);  // S_{t+2}
-            mma_commit(&bar_s_full[t & 1]);
-          }
-          __syncwarp();
+          mma_kk(tS + (t & 1) * 128, aQ, k_stage(i + 2), 0);  // S_{t+2}
+          mma_commit_warp(&bar_s_full[t & 1]);
         }
       }
       kv += T;
     }
-    if (lane == 0) {
-      mma_commit(&bar_final);
-      mbar_drain(&bar_final, 0);
-    }
-    __syncwarp();
+    mma_commit_warp(&bar_final);
+    mbar_drain(&bar_final, 0);
   } else if (warp >= 4) {
     // ---------------------------------------------- one q row per thread
     const int quarter = warp % 4;
@@ -615,66 +595,42 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         if (j == 0) {
           if (!(ok = wait_q(n))) break;
           tc_fence_after_sync();
-          if (lane == 0) {
-            mma_kk(tA, aK, q_addr(n), 0);  // S^T = K Q^T
-            mma_commit(bar_s_full);
-          }
-          __syncwarp();
+          mma_kk(tA, aK, q_addr(n), 0);  // S^T = K Q^T
+          mma_commit_warp(bar_s_full);
           if (!(ok = wait_do(n))) break;
           tc_fence_after_sync();
-          if (lane == 0) {
-            mma_kk(tB, aV, do_addr(n), 0);  // dP^T = V dO^T
-            mma_commit(bar_dp_full);
-          }
-          __syncwarp();
+          mma_kk(tB, aV, do_addr(n), 0);  // dP^T = V dO^T
+          mma_commit_warp(bar_dp_full);
         }
         if (!(ok = warp_wait(bar_ds_full, n & 1, abort, p.status))) break;
         if (j == 0 && items > 0 &&
             !(ok = warp_wait(bar_dkdv_free, (items - 1) & 1, abort, p.status)))
           break;
         tc_fence_after_sync();
-        if (lane == 0) {
-          mma_tn(tC, tA, do_addr(n), j > 0);  // dV += P^T dO
-          mma_commit(bar_do_empty + n % kKvDoStages);
-        }
-        __syncwarp();
+        mma_tn(tC, tA, do_addr(n), j > 0);  // dV += P^T dO
+        mma_commit_warp(bar_do_empty + n % kKvDoStages);
         const bool has_next = j + 1 < x.steps;
         if (has_next) {
           if (!(ok = wait_q(n + 1))) break;
           tc_fence_after_sync();
-          if (lane == 0) {
-            mma_kk(tA, aK, q_addr(n + 1), 0);  // next S^T (P^T_n already read by dV)
-            mma_commit(bar_s_full);
-          }
-          __syncwarp();
+          mma_kk(tA, aK, q_addr(n + 1), 0);  // next S^T (P^T_n already read by dV)
+          mma_commit_warp(bar_s_full);
         }
-        if (lane == 0) {
-          mma_tn(tD, tB, q_addr(n), j > 0);  // dK += dS^T Q (dS^T from TMEM)
-          mma_commit(bar_q_empty + n % kKvQStages);
-        }
-        __syncwarp();
+        mma_tn(tD, tB, q_addr(n), j > 0);  // dK += dS^T Q (dS^T from TMEM)
+        mma_commit_warp(bar_q_empty + n % kKvQStages);
         if (has_next) {
           if (!(ok = wait_do(n + 1))) break;
           tc_fence_after_sync();
-          if (lane == 0) {
-            mma_kk(tB, aV, do_addr(n + 1), 0);  // next dP^T (dS^T_n already read by dK)
-            mma_commit(bar_dp_full);
-          }
-          __syncwarp();
+          mma_kk(tB, aV, do_addr(n + 1), 0);  // next dP^T (dS^T_n already read by dK)
+          mma_commit_warp(bar_dp_full);
         }
       }
       if (!ok) break;
-      if (lane == 0) {
-        mma_commit(bar_dkdv_full);
-        mma_commit(bar_kv_empty);
-      }
-      __syncwarp();
+      mma_commit_warp(bar_dkdv_full);
+      mma_commit_warp(bar_kv_empty);
     }
-    if (lane == 0) {
-      mma_commit(bar_final);
-      mbar_drain(bar_final, 0);
-    }
-    __syncwarp();
+    mma_commit_warp(bar_final);
+    mbar_drain(bar_final, 0);
   } else if (warp >= 4) {
     // ---------- P^T and dS^T (one key row per thread), then each item's dK/dV
     const int quarter = warp % 4;

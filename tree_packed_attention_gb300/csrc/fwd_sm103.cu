@@ -103,13 +103,14 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // S = Q K^T over D = 128 (8 MMAs of K = 16); both operands K-major.
+// Warp-collective: one elected lane issues.
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+  const uint64_t qd = sdesc_sw128(q_addr, 16, 1024), kd = sdesc_sw128(k_addr, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-    mma_ss(d_tmem, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idesc,
-           kk > 0 ? 1u : 0u);
+    mma_ss_warp(d_tmem, sdesc_advance(qd, off), sdesc_advance(kd, off), idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -117,11 +118,11 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint3
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr,
                                          bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+  const uint64_t vd = sdesc_sw128(v_addr, kHalfBytes, 1024);
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    mma_ts(d_tmem, p_tmem + kk * 8, sdesc_sw128(v_addr + kk * 2048, kHalfBytes, 1024), idesc,
-           (accumulate || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ts_warp(d_tmem, p_tmem + kk * 8, sdesc_advance(vd, kk * 2048), idesc,
+                (accumulate || kk > 0) ? 1u : 0u);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -229,6 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
+    // The whole warp runs this branch; one elected lane issues each MMA.
     uint32_t kv = 0, qn = 0;
     uint32_t pc[2] = {0, 0}, oc[2] = {0, 0};
     const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
@@ -244,17 +246,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = warp_wait(&bar_k_full[st], ph, abort, p.status))) break;
         tc_fence_after_sync();
         const int kd = kinds_at(p, x.beg);
-        if (lane == 0) {
-          for (int s = 0; s < 2; ++s) {
-            if ((kd >> (2 * s)) & 3) {
-              issue_qk(tmem + s * 128, q_addr + s * kTileBytes, k_addr + st * kTileBytes);
-              mma_commit(&bar_s_full[s]);
-            }
+        for (int s = 0; s < 2; ++s) {
+          if ((kd >> (2 * s)) & 3) {
+            issue_qk(tmem + s * 128, q_addr + s * kTileBytes, k_addr + st * kTileBytes);
+            mma_commit_warp(&bar_s_full[s]);
           }
-          mma_commit(&bar_k_empty[st]);
-          if (T == 1) mma_commit(&bar_q_empty);
         }
-        __syncwarp();
+        mma_commit_warp(&bar_k_empty[st]);
+        if (T == 1) mma_commit_warp(&bar_q_empty);
       }
       for (int t = 0; t < T && ok; ++t) {
         const uint32_t kvt = kv + t;
@@ -272,9 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 !(ok = warp_wait(&bar_o_free[s], (oc[s] - 1) & 1, abort, p.status)))
               break;
             tc_fence_after_sync();
-            if (lane == 0)
-              issue_pv(tmem + 256 + s * 128, tmem + s * 128, v_addr + st * kTileBytes, !first[s]);
-            __syncwarp();
+            issue_pv(tmem + 256 + s * 128, tmem + s * 128, v_addr + st * kTileBytes, !first[s]);
             first[s] = false;
           }
           if (has_next) {
@@ -283,36 +280,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after_sync();
             }
             if ((kdn >> (2 * s)) & 3) {
-              if (lane == 0) {
-                issue_qk(tmem + s * 128, q_addr + s * kTileBytes, k_addr + stn * kTileBytes);
-                mma_commit(&bar_s_full[s]);
-              }
-              __syncwarp();
+              issue_qk(tmem + s * 128, q_addr + s * kTileBytes, k_addr + stn * kTileBytes);
+              mma_commit_warp(&bar_s_full[s]);
             }
           }
         }
         if (!ok) break;
-        if (lane == 0) {
-          mma_commit(&bar_v_empty[st]);
-          if (has_next) mma_commit(&bar_k_empty[stn]);
-          if (t + 2 == T) mma_commit(&bar_q_empty);  // the item's last S MMAs were just issued
-        }
-        __syncwarp();
+        mma_commit_warp(&bar_v_empty[st]);
+        if (has_next) mma_commit_warp(&bar_k_empty[stn]);
+        if (t + 2 == T) mma_commit_warp(&bar_q_empty);  // the item's last S MMAs were just issued
       }
       if (!ok) break;
       kv += T;
-      if (lane == 0) {
-        for (int s = 0; s < 2; ++s)
-          if (x.qtile[s] < p.Tq) mma_commit(&bar_o_full[s]);
+      for (int s = 0; s < 2; ++s) {
+        if (x.qtile[s] < p.Tq) {
+          mma_commit_warp(&bar_o_full[s]);
+          ++oc[s];
+        }
       }
-      __syncwarp();
-      for (int s = 0; s < 2; ++s)
-        if (x.qtile[s] < p.Tq) ++oc[s];
     }
-    if (lane == 0) {  // every MMA issued by this CTA completes before TMEM is freed
-      mma_commit(&bar_final);
-      mbar_drain(&bar_final, 0);
-    }
+    mma_commit_warp(&bar_final);  // every MMA issued by this CTA completes before TMEM is freed
+    if (lane == 0) mbar_drain(&bar_final, 0);
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------- softmax
@@ -367,9 +355,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(j + 3 <= i && i < b.w)) sv[4 * c4 + 3] = -INFINITY;
           }
         }
-        float mx = sv[0];
+        // row max as 8 independent chains, then a tree (short dependency chains)
+        float m8[8];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, sv[c]);
+        for (int u = 0; u < 8; ++u) m8[u] = sv[u];
+#pragma unroll
+        for (int c = 8; c < 128; c += 8)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) m8[u] = fmaxf(m8[u], sv[c + u]);
+        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         const float m_tile = mx * sl2;
         const float m_new = fmaxf(m_ref, m_tile);
         const bool rescale = (m_ref != -INFINITY) && (m_new > m_ref + kRescaleThreshold);
@@ -381,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = m_new;  // first visible keys of this row (or still none)
         }
         const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float rs = 0.f;
+        float rs4[4] = {0.f, 0.f, 0.f, 0.f};  // row sum in 4 independent chains
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
@@ -389,11 +384,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int jj = 0; jj < 16; ++jj) {
             const float p0 = ex2_approx(fmaf(sv[c * 32 + 2 * jj], sl2, -mr));
             const float p1 = ex2_approx(fmaf(sv[c * 32 + 2 * jj + 1], sl2, -mr));
-            rs += p0 + p1;
+            rs4[jj & 3] += p0 + p1;
             pk[jj] = pack_bf16x2(p0, p1);
           }
           tmem_st16(tS + c * 16, pk);
         }
+        const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
         if (__any_sync(0xffffffffu, rescale)) {
           // O_s is quiescent: its last PV completed before this S did, and the
           // next PV waits for the P arrival below.
