@@ -56,13 +56,17 @@ __device__ __forceinline__ void mma_kk(uint32_t d, uint32_t a, uint32_t b, uint3
   }
 }
 
-// D = A B^T, A from TMEM (bf16 pairs, 128 lanes x 64 columns), B MN-major in smem.
-__device__ __forceinline__ void mma_tn(uint32_t d, uint32_t a_tmem, uint32_t b, uint32_t acc) {
+
+// D = A B^T, A from TMEM split in two halves: K elements 0-63 in columns 0-31
+// and K elements 64-127 in columns 64-95 (each written by one warpgroup over
+// columns it had already read), B MN-major in smem.
+__device__ __forceinline__ void mma_tn_split(uint32_t d, uint32_t a_tmem, uint32_t b, uint32_t acc) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
   const uint64_t bd = sdesc_sw128(b, kHalfBytes, 1024);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
-    mma_ts_warp(d, a_tmem + kk * 8, sdesc_advance(bd, kk * 2048), idesc, (acc || kk > 0) ? 1u : 0u);
+    mma_ts_warp(d, a_tmem + kk * 8 + (kk >= 4 ? 32 : 0), sdesc_advance(bd, kk * 2048), idesc,
+                (acc || kk > 0) ? 1u : 0u);
 }
 
 // Write 32 consecutive fp32 values of one 128-wide row, times `mul`, as fp32 or bf16.
@@ -87,11 +91,11 @@ __device__ __forceinline__ void store_row(void* dst_base, size_t off, int c, con
 }
 
 // ============================================================== dQ kernel
-// 256 threads: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps 4-7
-// one q row per thread. TMEM: S_a | S_b | dP | dQ (128 columns each); dS is
-// written as bf16 over the first 64 columns of the S buffer it came from and
-// read by the dQ MMA from TMEM.
-constexpr int kDqThreads = 256;
+// 384 threads: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps 4-11
+// one q row per thread, two warpgroups splitting the keys of each tile.
+// TMEM: S_a | S_b | dP | dQ (128 columns each); dS is written as bf16 into the
+// S buffer it came from and read by the dQ MMA from TMEM.
+constexpr int kDqThreads = 384;
 // K_t is read by S_t and, a step later, by dQ_t; S_{t+2} is issued right after
 // dQ_t, so K needs a third stage for its load to overlap a whole step.
 constexpr int kDqKStages = 3;
@@ -154,11 +158,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&bar_s_full[0], 1);
     mbar_init(&bar_s_full[1], 1);
     mbar_init(&bar_dp_full, 1);
-    mbar_init(&bar_ds_full, 128);
+    mbar_init(&bar_ds_full, 256);
     mbar_init(&bar_dq_full, 1);
-    mbar_init(&bar_dq_free, 128);
-    mbar_init(&bar_ke[0], 128);
-    mbar_init(&bar_ke[1], 128);
+    mbar_init(&bar_dq_free, 256);
+    mbar_init(&bar_ke[0], 256);
+    mbar_init(&bar_ke[1], 256);
     abort_s = 0;
     fence_mbar_init();
   }
@@ -191,6 +195,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         tma_load_3d(smem + kDqOffQ + kHalfBytes, &map_q, &bar_q_full, 64, h, qt * 128);
         tma_load_3d(smem + kDqOffDO, &map_do, &bar_q_full, 0, h, qt * 128);
         tma_load_3d(smem + kDqOffDO + kHalfBytes, &map_do, &bar_q_full, 64, h, qt * 128);
+        const int nit = it + gridDim.x;  // the next item's Q and dO into L2
+        if (nit < p.n_items) {
+          const int nqt = p.order[nit / p.hq], nh = nit % p.hq;
+          tma_prefetch_l2_3d(&map_q, 0, nh, nqt * 128);
+          tma_prefetch_l2_3d(&map_q, 64, nh, nqt * 128);
+          tma_prefetch_l2_3d(&map_do, 0, nh, nqt * 128);
+          tma_prefetch_l2_3d(&map_do, 64, nh, nqt * 128);
+        }
       }
       __syncwarp();
       ++qn;
@@ -265,7 +277,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (t == 0 && qn > 1 && !(ok = warp_wait(&bar_dq_free, (qn - 2) & 1, abort, p.status)))
           break;
         tc_fence_after_sync();
-        mma_tn(tDQ, tS + (t & 1) * 128, k_stage(i), t > 0);  // dQ += dS_t K_t
+        mma_tn_split(tDQ, tS + (t & 1) * 128, k_stage(i), t > 0);  // dQ += dS_t K_t
         mma_commit_warp(&bar_k_empty[i % kDqKStages]);
         if (t + 1 == T) {
           mma_commit_warp(&bar_dq_full);
@@ -290,10 +302,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mma_commit_warp(&bar_final);
     mbar_drain(&bar_final, 0);
   } else if (warp >= 4) {
-    // ---------------------------------------------- one q row per thread
+    // ---- two warpgroups split each tile's 128 keys: warps 4-7 take keys
+    // 0-63, warps 8-11 keys 64-127; one q row per thread (TMEM lane = row).
+    // Each half writes its dS (bf16) over the first 32 columns of its own S
+    // columns, so the halves never touch each other's unread data.
+    const int half = (warp - 4) / 4;
     const int quarter = warp % 4;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t col0 = half * 64;
     const float sl2 = p.scale_log2;
     uint32_t n = 0, qn = 0, kb = 0, ku[2] = {0, 0}, su[2] = {0, 0};
     bool ok = true;
@@ -301,7 +318,18 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const int qt = p.order[it / p.hq], h = it % p.hq;
       const int i = qt * 128 + r;
       const size_t row = static_cast<size_t>(i) * p.hq + h;
-      // Delta_i = dO_i . O_i (dO from the swizzled smem tile, O from HBM) and lse_i * log2(e)
+      // The next item's O row (for its Delta) is prefetched into L2.
+      {
+        const int nit = it + gridDim.x;
+        if (nit < p.n_items) {
+          const int ni = p.order[nit / p.hq] * 128 + r;
+          if (ni < p.N) {
+            const __nv_bfloat16* nrow = p.o + (static_cast<size_t>(ni) * p.hq + nit % p.hq) * 128;
+            prefetch_l2(nrow);
+            prefetch_l2(nrow + 64);
+          }
+        }
+      }
       if (!(ok = warp_wait(&bar_q_full, qn & 1, abort, p.status))) break;
       float delta = 0.f, lse2 = INFINITY;
       if (i < p.N) {
@@ -323,8 +351,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
         lse2 = p.lse[static_cast<size_t>(h) * p.N + i] * kLog2e;
       }
-      p.delta[static_cast<size_t>(h) * p.Npad + i] = delta;
-      p.lse2[static_cast<size_t>(h) * p.Npad + i] = lse2;
+      if (half == 0) {
+        p.delta[static_cast<size_t>(h) * p.Npad + i] = delta;
+        p.lse2[static_cast<size_t>(h) * p.Npad + i] = lse2;
+      }
       ++qn;
       const int beg = p.qt_ptr[qt], end = p.qt_ptr[qt + 1];
       for (int t = beg; t < end; ++t, ++n) {
@@ -332,31 +362,33 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int kt = p.qt_kt[t];
         const int* ke = nullptr;
         if (kd == 1) {  // PARTIAL: the 128 key bounds of this tile, shared through smem
-          const int j = kt * 128 + r;
-          ke_buf[kb][r] = j < p.N ? __ldg(p.key_end + j) : 0;
+          if (half == 0) {
+            const int j = kt * 128 + r;
+            ke_buf[kb][r] = j < p.N ? __ldg(p.key_end + j) : 0;
+          }
           mbar_arrive(&bar_ke[kb]);
           if (!(ok = warp_wait(&bar_ke[kb], ku[kb] & 1, abort, p.status))) break;
           ++ku[kb];
-          ke = ke_buf[kb];
+          ke = ke_buf[kb] + col0;
           kb ^= 1;
         }
         const int sb = (t - beg) & 1;
-        const uint32_t tSb = tS + lane_off + sb * 128;
+        const uint32_t tSb = tS + lane_off + sb * 128 + col0;
         if (!(ok = warp_wait(&bar_s_full[sb], su[sb] & 1, abort, p.status))) break;
         ++su[sb];
         tc_fence_after_sync();
-        float pv[128];
+        float pv[64];
         {
-          uint32_t rr[128];
-          tmem_ld128(tSb, rr);  // the whole S row, one wait
+          uint32_t rr[64];
+          tmem_ld64(tSb, rr);  // this half of the S row, one wait
 #pragma unroll
-          for (int jj = 0; jj < 128; ++jj)
+          for (int jj = 0; jj < 64; ++jj)
             pv[jj] = ex2_approx(fmaf(__uint_as_float(rr[jj]), sl2, -lse2));
         }
         if (ke) {
-          const int j0 = kt * 128;
+          const int j0 = kt * 128 + col0;
 #pragma unroll
-          for (int c4 = 0; c4 < 32; ++c4) {
+          for (int c4 = 0; c4 < 16; ++c4) {
             const int4 b = reinterpret_cast<const int4*>(ke)[c4];
             const int j = j0 + 4 * c4;
             if (!(j + 0 <= i && i < b.x)) pv[4 * c4 + 0] = 0.f;
@@ -367,20 +399,19 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
         if (!(ok = warp_wait(&bar_dp_full, n & 1, abort, p.status))) break;
         tc_fence_after_sync();
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
+        {
           uint32_t rr[64];
-          tmem_ld64(tDP + lane_off + h2 * 64, rr);  // half of the dP row, one wait
+          tmem_ld64(tDP + lane_off + col0, rr);  // this half of the dP row, one wait
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t pk[16];
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
-              const int col = h2 * 64 + c * 32 + 2 * jj;
-              pk[jj] = pack_bf16x2(pv[col] * (__uint_as_float(rr[c * 32 + 2 * jj]) - delta),
-                                   pv[col + 1] * (__uint_as_float(rr[c * 32 + 2 * jj + 1]) - delta));
+              const int col = c * 32 + 2 * jj;
+              pk[jj] = pack_bf16x2(pv[col] * (__uint_as_float(rr[col]) - delta),
+                                   pv[col + 1] * (__uint_as_float(rr[col + 1]) - delta));
             }
-            tmem_st16(tSb + (h2 * 2 + c) * 16, pk);  // dS over the first 64 columns of this S buffer
+            tmem_st16(tSb + c * 16, pk);  // dS over the first 32 columns of this half
           }
         }
         tmem_wait_st();
@@ -388,14 +419,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         mbar_arrive(&bar_ds_full);
       }
       if (!ok) break;
-      // epilogue: dq = scale * dQ
+      // epilogue: dq = scale * dQ, this half's 64 columns
       if (!(ok = warp_wait(&bar_dq_full, (qn - 1) & 1, abort, p.status))) break;
       tc_fence_after_sync();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
-        tmem_ld32(tDQ + lane_off + c * 32, v);
-        if (i < p.N) store_row(p.dq, row * 128, c, v, p.scale, p.out_f32);
+        tmem_ld32(tDQ + lane_off + col0 + c * 32, v);
+        if (i < p.N) store_row(p.dq, row * 128, half * 2 + c, v, p.scale, p.out_f32);
       }
       tc_fence_before_sync();
       mbar_arrive(&bar_dq_free);
@@ -411,14 +442,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 }
 
 // ============================================================ dK/dV kernel
-// 256 threads: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps 4-7
-// one key row per thread (P^T and dS^T into TMEM, and at the end of an item
-// its dV and dK rows). TMEM: S^T, then P^T in its first 64 columns | dP^T,
-// then dS^T in its first 64 columns | dV | dK. Both products that need P^T
+// 384 threads: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps
+// 4-11 one key row per thread, two warpgroups splitting the q columns (P^T and
+// dS^T into TMEM, and at the end of an item the dV and dK rows). TMEM: S^T,
+// then P^T over the columns read | dP^T, then dS^T likewise | dV | dK. Both products that need P^T
 // and dS^T read them from TMEM, so no operand is written to shared memory.
 // Q_n is read by S^T_n and, a step later, by dK_n, so Q is staged three deep;
 // dO_n (with the step's lse and Delta) is released after dV_n, two deep.
-constexpr int kKvThreads = 256;
+constexpr int kKvThreads = 384;
 constexpr int kKvQStages = 3;
 constexpr int kKvDoStages = 2;
 constexpr uint32_t kKvOffK = 0;
@@ -500,9 +531,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     }
     mbar_init(bar_s_full, 1);
     mbar_init(bar_dp_full, 1);
-    mbar_init(bar_ds_full, 128);
+    mbar_init(bar_ds_full, 256);
     mbar_init(bar_dkdv_full, 1);
-    mbar_init(bar_dkdv_free, 128);
+    mbar_init(bar_dkdv_free, 256);
     mbar_init(bar_final, 1);
     *abort = 0;
     fence_mbar_init();
@@ -537,6 +568,14 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tma_load_3d(smem + kKvOffK + kHalfBytes, &map_k, bar_kv_full, 64, x.kvh, row0);
         tma_load_3d(smem + kKvOffV, &map_v, bar_kv_full, 0, x.kvh, row0);
         tma_load_3d(smem + kKvOffV + kHalfBytes, &map_v, bar_kv_full, 64, x.kvh, row0);
+        const int nit = it + gridDim.x;  // the next item's K and V into L2
+        if (nit < p.n_items) {
+          const KvItem y = decode_kv(p, nit);
+          tma_prefetch_l2_3d(&map_k, 0, y.kvh, y.kt * 128);
+          tma_prefetch_l2_3d(&map_k, 64, y.kvh, y.kt * 128);
+          tma_prefetch_l2_3d(&map_v, 0, y.kvh, y.kt * 128);
+          tma_prefetch_l2_3d(&map_v, 64, y.kvh, y.kt * 128);
+        }
       }
       __syncwarp();
       for (int j = 0; j < x.steps; ++j, ++n) {
@@ -607,7 +646,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             !(ok = warp_wait(bar_dkdv_free, (items - 1) & 1, abort, p.status)))
           break;
         tc_fence_after_sync();
-        mma_tn(tC, tA, do_addr(n), j > 0);  // dV += P^T dO
+        mma_tn_split(tC, tA, do_addr(n), j > 0);  // dV += P^T dO
         mma_commit_warp(bar_do_empty + n % kKvDoStages);
         const bool has_next = j + 1 < x.steps;
         if (has_next) {
@@ -616,7 +655,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           mma_kk(tA, aK, q_addr(n + 1), 0);  // next S^T (P^T_n already read by dV)
           mma_commit_warp(bar_s_full);
         }
-        mma_tn(tD, tB, q_addr(n), j > 0);  // dK += dS^T Q (dS^T from TMEM)
+        mma_tn_split(tD, tB, q_addr(n), j > 0);  // dK += dS^T Q (dS^T from TMEM)
         mma_commit_warp(bar_q_empty + n % kKvQStages);
         if (has_next) {
           if (!(ok = wait_do(n + 1))) break;
@@ -632,11 +671,17 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     mma_commit_warp(bar_final);
     mbar_drain(bar_final, 0);
   } else if (warp >= 4) {
-    // ---------- P^T and dS^T (one key row per thread), then each item's dK/dV
+    // ---- two warpgroups split each step's 128 q columns: warps 4-7 take
+    // columns 0-63, warps 8-11 columns 64-127; one key row per thread. Each
+    // half writes P^T over the first 32 of its own S^T columns and dS^T over
+    // the first 32 of its own dP^T columns. At the end of an item each half
+    // stores its 64 columns of dV and dK.
+    const int half = (warp - 4) / 4;
     const int quarter = warp % 4;
     const int kr = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tSr = tA + lane_off, tPr = tB + lane_off;
+    const uint32_t col0 = half * 64;
+    const uint32_t tSr = tA + lane_off + col0, tPr = tB + lane_off + col0;
     const float sl2 = p.scale_log2;
     uint32_t n = 0, items = 0;
     bool ok = true;
@@ -645,60 +690,67 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       const int jk = x.kt * 128 + kr;
       const int ke = jk < p.N ? __ldg(p.key_end + jk) : 0;  // rows [jk, ke) see this key
       for (int j = 0; j < x.steps; ++j, ++n) {
-        const int q0 = (x.qlo + j % x.nq) * 128;
+        const int q0 = (x.qlo + j % x.nq) * 128 + col0;  // first q column of this half
         const uint32_t sd = n % kKvDoStages, pd = (n / kKvDoStages) & 1;
-        const float* lse2 = reinterpret_cast<const float*>(smem + kKvOffLse + sd * 512);
-        const float* dlt = reinterpret_cast<const float*>(smem + kKvOffDelta + sd * 512);
+        const float* lse2 = reinterpret_cast<const float*>(smem + kKvOffLse + sd * 512) + col0;
+        const float* dlt = reinterpret_cast<const float*>(smem + kKvOffDelta + sd * 512) + col0;
         if (!(ok = warp_wait(bar_do_full + sd, pd, abort, p.status))) break;
         if (!(ok = warp_wait(bar_s_full, n & 1, abort, p.status))) break;
         tc_fence_after_sync();
-        const bool full_row = jk <= q0 && q0 + 128 <= ke;  // every column visible to this key
-        float pv[128];
+        // every column of this half visible to every key of this warp: no mask
+        const bool all_full = __all_sync(0xffffffffu, jk <= q0 && q0 + 64 <= ke);
+        float pv[64];
         {
-          uint32_t rr[128];
-          tmem_ld128(tSr, rr);  // the whole S^T row, one wait
+          uint32_t rr[64];
+          tmem_ld64(tSr, rr);  // this half of the S^T row, one wait
+          if (all_full) {
 #pragma unroll
-          for (int jj = 0; jj < 128; jj += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + jj);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            for (int jj = 0; jj < 64; jj += 4) {
+              const float4 l4 = *reinterpret_cast<const float4*>(lse2 + jj);
+              pv[jj + 0] = ex2_approx(fmaf(__uint_as_float(rr[jj + 0]), sl2, -l4.x));
+              pv[jj + 1] = ex2_approx(fmaf(__uint_as_float(rr[jj + 1]), sl2, -l4.y));
+              pv[jj + 2] = ex2_approx(fmaf(__uint_as_float(rr[jj + 2]), sl2, -l4.z));
+              pv[jj + 3] = ex2_approx(fmaf(__uint_as_float(rr[jj + 3]), sl2, -l4.w));
+            }
+          } else {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int q = q0 + jj + u;
-              const float e = ex2_approx(fmaf(__uint_as_float(rr[jj + u]), sl2, -lv[u]));
-              pv[jj + u] = (full_row || (jk <= q && q < ke)) ? e : 0.f;
+            for (int jj = 0; jj < 64; jj += 4) {
+              const float4 l4 = *reinterpret_cast<const float4*>(lse2 + jj);
+              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int q = q0 + jj + u;
+                const float e = ex2_approx(fmaf(__uint_as_float(rr[jj + u]), sl2, -lv[u]));
+                pv[jj + u] = (jk <= q && q < ke) ? e : 0.f;
+              }
             }
           }
         }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) pk[jj] = pack_bf16x2(pv[c * 32 + 2 * jj], pv[c * 32 + 2 * jj + 1]);
-          tmem_st16(tSr + c * 16, pk);  // P^T over the first 64 columns of S^T
+          tmem_st16(tSr + c * 16, pk);  // P^T over the first 32 columns of this half
         }
         if (!(ok = warp_wait(bar_dp_full, n & 1, abort, p.status))) break;
         tc_fence_after_sync();
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
+        {
           uint32_t rr[64];
-          tmem_ld64(tPr + h2 * 64, rr);  // dP^T columns 64*h2 .. +63, one wait
+          tmem_ld64(tPr, rr);  // this half of the dP^T row, one wait
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t pk[16];
 #pragma unroll
             for (int jj = 0; jj < 32; jj += 4) {
-              const int col = h2 * 64 + c * 32 + jj;
+              const int col = c * 32 + jj;
               const float4 d4 = *reinterpret_cast<const float4*>(dlt + col);
-              const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-              for (int u = 0; u < 4; u += 2) {
-                const float ds0 = pv[col + u] * (__uint_as_float(rr[c * 32 + jj + u]) - dv4[u]);
-                const float ds1 = pv[col + u + 1] * (__uint_as_float(rr[c * 32 + jj + u + 1]) - dv4[u + 1]);
-                pk[(jj + u) / 2] = pack_bf16x2(ds0, ds1);
-              }
+              pk[jj / 2] = pack_bf16x2(pv[col] * (__uint_as_float(rr[col]) - d4.x),
+                                       pv[col + 1] * (__uint_as_float(rr[col + 1]) - d4.y));
+              pk[jj / 2 + 1] = pack_bf16x2(pv[col + 2] * (__uint_as_float(rr[col + 2]) - d4.z),
+                                           pv[col + 3] * (__uint_as_float(rr[col + 3]) - d4.w));
             }
-            // dS^T (q columns 64*h2 + 32*c ..) over columns of dP^T already read
-            tmem_st16(tPr + (h2 * 2 + c) * 16, pk);
+            tmem_st16(tPr + c * 16, pk);  // dS^T over the first 32 columns of this half
           }
         }
         tmem_wait_st();
@@ -706,21 +758,21 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         mbar_arrive(bar_ds_full);
       }
       if (!ok) break;
-      // ---- this item's dV and dK (scaled) from TMEM
+      // ---- this item's dV and dK (scaled) from TMEM, this half's 64 columns
       if (!(ok = warp_wait(bar_dkdv_full, items & 1, abort, p.status))) break;
       tc_fence_after_sync();
       const size_t out = (static_cast<size_t>(jk) * p.hkv + x.kvh) * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
-        tmem_ld32(tC + lane_off + c * 32, v);
-        if (jk < p.N) store_row(p.dv, out, c, v, 1.f, p.out_f32);
+        tmem_ld32(tC + lane_off + col0 + c * 32, v);
+        if (jk < p.N) store_row(p.dv, out, half * 2 + c, v, 1.f, p.out_f32);
       }
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
-        tmem_ld32(tD + lane_off + c * 32, v);
-        if (jk < p.N) store_row(p.dk, out, c, v, p.scale, p.out_f32);
+        tmem_ld32(tD + lane_off + col0 + c * 32, v);
+        if (jk < p.N) store_row(p.dk, out, half * 2 + c, v, p.scale, p.out_f32);
       }
       tc_fence_before_sync();
       mbar_arrive(bar_dkdv_free);

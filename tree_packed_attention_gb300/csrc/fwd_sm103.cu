@@ -199,6 +199,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sQ + s * kTileBytes + kHalfBytes, &map_q, &bar_q_full, 64, x.head[s],
                       x.qtile[s] * 128);
         }
+        const int nit = it + gridDim.x;  // the next item's Q tiles into L2
+        if (nit < p.n_items) {
+          const Item y = decode_item(p, nit);
+          for (int s = 0; s < 2; ++s) {
+            if (y.qtile[s] >= p.Tq) continue;
+            tma_prefetch_l2_3d(&map_q, 0, y.head[s], y.qtile[s] * 128);
+            tma_prefetch_l2_3d(&map_q, 64, y.head[s], y.qtile[s] * 128);
+          }
+        }
       }
       __syncwarp();
       ++qn;
