@@ -1,8 +1,11 @@
 """Benchmark: tree-packed attention forward + backward on one GB300.
 
-A step is one tree_attn_fwd plus one tree_attn_bwd over one synthetic batch
-(the whole hot path: the plan is built once per batch, outside the timed
-region, as the pages build it once per forward on the host). The headline
+A step is one tree_attn_fwd plus the backward over one synthetic batch (the
+whole hot path: the plan is built once per batch, outside the timed region, as
+the pages build it once per forward on the host). The backward is issued as its
+two phases, tree_attn_bwd_dq and tree_attn_bwd_dkdv (the two launches
+tree_attn_bwd makes), so that CUDA events time each of the three kernels; the
+``roofline`` object is for the slowest of them. The headline
 workload is the packed batch of 32 GRPO-shaped tries, 131,072 tokens, 64 q
 heads / 8 kv heads, head_dim 128, bf16.
 
@@ -39,6 +42,37 @@ def _peaks():
             return json.load(f), "measured"
     except OSError:
         return FALLBACK_PEAKS, "fallback"
+
+
+# DRAM bytes per launch from an ncu capture, kept only while the kernel's
+# sources still hash to what they were when the counters were taken.
+KERNEL_SOURCES = {
+    "tree_attn_fwd_sm103": ("fwd_sm103.cu", "sm103_ptx.cuh"),
+    "tree_attn_bwd_dq_sm103": ("bwd_sm103.cu", "sm103_ptx.cuh"),
+    "tree_attn_bwd_dkdv_sm103": ("bwd_sm103.cu", "sm103_ptx.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "tree_packed_attention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(workload: str, kernel: str):
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload, {}).get(kernel)
+    except OSError:
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash(kernel):
+        return None
+    return rec.get("dram_bytes_per_launch")
 
 
 def _dist():
@@ -235,7 +269,9 @@ def gpu_arm(args):
         step()
     tpa.tree_status_sync()
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # The timed step runs the backward as its two phases (exactly what
+    # tree_attn_bwd launches) so that each kernel gets its own events.
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -245,14 +281,18 @@ def gpu_arm(args):
             ev[s][0].record(stream)
             tpa.tree_attn_fwd(plan, q, k, v, out=o, lse=lse)
             ev[s][1].record(stream)
-            tpa.tree_attn_bwd(plan, do, q, k, v, o, lse, workspace=ws, out=(dq, dk, dv))
+            tpa.tree_attn_bwd_dq(plan, do, q, k, v, o, lse, ws, out=dq)
             ev[s][2].record(stream)
+            tpa.tree_attn_bwd_dkdv(plan, do, q, k, v, lse, ws, out=(dk, dv))
+            ev[s][3].record(stream)
         torch.cuda.synchronize()
     if dist:
         dist.barrier()
     tpa.tree_status_sync()
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    dq_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    kv_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    bwd_ms = [a + b for a, b in zip(dq_ms, kv_ms)]
     step_ms = statistics.mean(f + b for f, b in zip(fwd_ms, bwd_ms))
     if dist:
         t = torch.tensor([step_ms], device=dev)
@@ -299,11 +339,17 @@ def gpu_arm(args):
     fwd_mean = statistics.mean(fwd_ms)
     bwd_tf = flops_bwd / (bwd_mean * 1e-3) / 1e12
     fwd_tf = flops_fwd / (fwd_mean * 1e-3) / 1e12
-    traffic = None
-    traffic_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(traffic_path):
-        with open(traffic_path) as f:
-            traffic = json.load(f).get(w.name, {}).get("bwd_bytes_per_launch")
+    # Per kernel: mean event time and the FLOPs its outputs need per visible
+    # pair and q head (fwd: S, PV; dQ: S, dP, dS K; dK/dV: S^T, dP^T, P^T dO, dS^T Q).
+    kernels = {
+        "tree_attn_fwd_sm103": (fwd_mean, 4.0 * D * hq * pvis),
+        "tree_attn_bwd_dq_sm103": (statistics.mean(dq_ms), 6.0 * D * hq * pvis),
+        "tree_attn_bwd_dkdv_sm103": (statistics.mean(kv_ms), 8.0 * D * hq * pvis),
+    }
+    top = max(kernels, key=lambda n: kernels[n][0])
+    top_ms, top_flops = kernels[top]
+    top_tf = top_flops / (top_ms * 1e-3) / 1e12
+    traffic = _traffic(w.name, top)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -322,9 +368,11 @@ def gpu_arm(args):
             "fraction_of_bf16_peak": value / world / peak,
             "fwd": {"ms": fwd_mean, "tflops": fwd_tf, "frac": fwd_tf / peak, "launches": 1},
             "bwd": {"ms": bwd_mean, "tflops": bwd_tf, "frac": bwd_tf / peak, "launches": 2},
+            "kernels": {n: {"ms": t, "tflops_algorithmic": f / (t * 1e-3) / 1e12}
+                        for n, (t, f) in kernels.items()},
             "plan_build_ms": plan_ms,
-            "roofline": {"bound": "tensor", "kernel": "tree_attn_bwd (dQ kernel + dK/dV kernel)",
-                         "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak,
+            "roofline": {"bound": "tensor", "kernel": top, "achieved": top_tf, "peak": peak,
+                         "unit": "TFLOP/s", "frac": top_tf / peak,
                          "peak_source": f"{peak_kind} bf16 dense (burst)", "traffic": traffic},
             "clocks": clocks.summary(),
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,

@@ -162,13 +162,35 @@ size_t tree_attn_bwd_workspace_bytes(const tree_plan_t* plan, int32_t hq, int32_
  *   contents on entry do not matter.
  * With P = exp(scale S - lse), Delta_i = dO_i.O_i, dS = P (dO V^T - Delta):
  * dq = scale dS K, dk = scale dS^T Q, dv = P^T dO (dk, dv summed over the q
- * heads of a group). Summation order of dq may vary between runs.
+ * heads of a group). Every sum is taken in a fixed order: results repeat bit
+ * for bit from run to run.
+ * It is tree_attn_bwd_dq followed by tree_attn_bwd_dkdv on the same stream.
  */
 tree_status_t tree_attn_bwd(const tree_plan_t* plan, const void* dout, const void* q, const void* k,
                             const void* v, const void* o, const float* lse, void* dq, void* dk,
                             void* dv, int32_t hq, int32_t hkv, int32_t head_dim, tree_dtype_t dtype,
                             tree_dtype_t grad_dtype, float softmax_scale, void* workspace,
                             size_t workspace_bytes, tree_stream_t stream);
+
+/*
+ * The two phases of tree_attn_bwd, for callers that schedule (or time) them
+ * apart. Arguments mean what they mean for tree_attn_bwd.
+ * tree_attn_bwd_dq writes Delta_i = dO_i.O_i (and, for bf16, lse_i*log2(e))
+ * into the workspace, then dq. tree_attn_bwd_dkdv reads them back and writes
+ * dk, dv: it must run after a tree_attn_bwd_dq with the same plan, tensors,
+ * heads, dtypes, scale and workspace, ordered after it on the GPU (the same
+ * stream, or an event between streams), with the workspace unchanged between.
+ */
+tree_status_t tree_attn_bwd_dq(const tree_plan_t* plan, const void* dout, const void* q,
+                               const void* k, const void* v, const void* o, const float* lse,
+                               void* dq, int32_t hq, int32_t hkv, int32_t head_dim,
+                               tree_dtype_t dtype, tree_dtype_t grad_dtype, float softmax_scale,
+                               void* workspace, size_t workspace_bytes, tree_stream_t stream);
+tree_status_t tree_attn_bwd_dkdv(const tree_plan_t* plan, const void* dout, const void* q,
+                                 const void* k, const void* v, const float* lse, void* dk, void* dv,
+                                 int32_t hq, int32_t hkv, int32_t head_dim, tree_dtype_t dtype,
+                                 tree_dtype_t grad_dtype, float softmax_scale, void* workspace,
+                                 size_t workspace_bytes, tree_stream_t stream);
 
 /*
  * Backward for callers that cannot allocate device memory when they call it

@@ -153,6 +153,27 @@ def test_bf16_forward_is_deterministic():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_backward_phases_equal_whole_backward_and_repeat(dtype):
+    """tree_attn_bwd_dq then tree_attn_bwd_dkdv gives tree_attn_bwd's bits; so does a rerun."""
+    _need_gpu()
+    p, L = treegen.grpo_tree(3, prompt=300, n_leaves=5, lo=60, hi=260)
+    N = int(L.sum())
+    hq, hkv, D = (8, 2, 128) if dtype == "bf16" else (4, 2, 64)
+    q, k, v, do = (x.cuda() for x in treegen.draw_tensors(N, hq, hkv, D, dtype, 3))
+    plan = tpa.tree_plan_build(p, L)
+    o, lse = tpa.tree_attn_fwd(plan, q, k, v)
+    whole = tpa.tree_attn_bwd(plan, do, q, k, v, o, lse)
+    again = tpa.tree_attn_bwd(plan, do, q, k, v, o, lse)
+    ws = torch.empty(tpa.tree_attn_bwd_workspace_bytes(plan, hq, D, q.dtype), dtype=torch.uint8,
+                     device=q.device)
+    dq = tpa.tree_attn_bwd_dq(plan, do, q, k, v, o, lse, ws)
+    dk, dv = tpa.tree_attn_bwd_dkdv(plan, do, q, k, v, lse, ws)
+    tpa.tree_status_sync()
+    for a, b, c in zip(whole, again, (dq, dk, dv)):
+        assert torch.equal(a, b) and torch.equal(a, c)
+
+
 def test_outputs_untouched_outside_their_rows():
     """Writes stay inside o/lse/dq/dk/dv: guard regions around them keep a NaN pattern."""
     _need_gpu()

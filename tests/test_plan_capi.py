@@ -126,6 +126,16 @@ def test_device_calls_without_device_copy_are_rejected():
     assert st == 1
     st = tpa.lib.tree_attn_fwd(plan.handle, 17, 16, 16, 16, 16, 1, 1, 128, 1, 0.0, None)
     assert st == 1  # misaligned pointer
+    # each backward phase checks the pointers it uses
+    args = (16, 16, 16, 16)  # dout, q, k, v
+    st = tpa.lib.tree_attn_bwd_dq(plan.handle, *args, None, 16, 16, 2, 1, 128, 1, 1, 0.0, 16, 1 << 20, None)
+    assert st == 1 and b"NULL" in tpa.lib.tree_last_error()  # o
+    st = tpa.lib.tree_attn_bwd_dkdv(plan.handle, *args, 16, 16, None, 2, 1, 128, 1, 1, 0.0, 16, 1 << 20, None)
+    assert st == 1 and b"NULL" in tpa.lib.tree_last_error()  # dv
+    st = tpa.lib.tree_attn_bwd_dkdv(plan.handle, *args, 16, 16, 16, 2, 1, 96, 1, 1, 0.0, 16, 1 << 20, None)
+    assert st == 5  # D = 96 unsupported for bf16
+    st = tpa.lib.tree_attn_bwd_dq(plan.handle, *args, 16, 16, 16, 2, 1, 128, 1, 1, 0.0, 16, 4, None)
+    assert st == 1 and b"workspace too small" in tpa.lib.tree_last_error()
     # bf16 workspace: lse*log2(e) and Delta, fp32 [hq, 128 * q-tiles] each
     assert tpa.lib.tree_attn_bwd_workspace_bytes(plan.handle, 2, 128, 1) == 2 * 2 * 128 * 4
     # fp32 workspace: Delta [hq, N], rounded up to 256 bytes

@@ -24,7 +24,8 @@ from ._lib import (DTYPE_BF16, DTYPE_F32, EXPORTS, FIELDS, LIB_PATH, PlanInfo, T
                    check, lib)
 
 __all__ = [
-    "Plan", "tree_plan_build", "tree_attn_fwd", "tree_attn_bwd", "tree_attn_bwd_workspace_bytes",
+    "Plan", "tree_plan_build", "tree_attn_fwd", "tree_attn_bwd", "tree_attn_bwd_dq",
+    "tree_attn_bwd_dkdv", "tree_attn_bwd_workspace_bytes",
     "tree_weights", "tree_status_sync", "TreeAttnFn", "tree_attention", "TreeAttnError",
     "FIELDS", "EXPORTS", "LIB_PATH",
 ]
@@ -139,37 +140,82 @@ def tree_attn_bwd_workspace_bytes(plan: Plan, hq: int, head_dim: int, dtype) -> 
     return int(lib.tree_attn_bwd_workspace_bytes(plan.handle, hq, head_dim, code))
 
 
-def tree_attn_bwd(plan: Plan, do, q, k, v, o, lse, softmax_scale: float = 0.0, grad_dtype=None,
-                  workspace=None, out=None, stream=None):
-    """(dq, dk, dv) of tree attention. ``grad_dtype`` defaults to q's dtype."""
+def _bwd_prepare(plan: Plan, do, q, k, v, o, lse, grad_dtype, workspace, stream):
     import torch
 
     N, hq, D = q.shape
     hkv = k.shape[1]
     if N != plan.num_tokens:
         raise ValueError(f"q has {N} tokens, the plan {plan.num_tokens}")
-    for name, t, shp in (("do", do, (N, hq, D)), ("q", q, (N, hq, D)), ("k", k, (N, hkv, D)),
-                         ("v", v, (N, hkv, D)), ("o", o, (N, hq, D))):
+    checks = [("do", do, (N, hq, D)), ("q", q, (N, hq, D)), ("k", k, (N, hkv, D)),
+              ("v", v, (N, hkv, D))]
+    if o is not None:
+        checks.append(("o", o, (N, hq, D)))
+    for name, t, shp in checks:
         _check_tensor(name, t, shp, q.dtype)
     _check_tensor("lse", lse, (hq, N), torch.float32)
     gdt = q.dtype if grad_dtype is None else grad_dtype
+    nbytes = tree_attn_bwd_workspace_bytes(plan, hq, D, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    s = _stream_ptr(stream)
+    plan.to_device(s)
+    gcode = DTYPE_BF16 if gdt == torch.bfloat16 else DTYPE_F32
+    return N, hq, hkv, D, gdt, gcode, workspace, s
+
+
+def tree_attn_bwd(plan: Plan, do, q, k, v, o, lse, softmax_scale: float = 0.0, grad_dtype=None,
+                  workspace=None, out=None, stream=None):
+    """(dq, dk, dv) of tree attention. ``grad_dtype`` defaults to q's dtype."""
+    import torch
+
+    N, hq, hkv, D, gdt, gcode, workspace, s = _bwd_prepare(plan, do, q, k, v, o, lse, grad_dtype,
+                                                           workspace, stream)
     if out is None:
         dq = torch.empty(N, hq, D, dtype=gdt, device=q.device)
         dk = torch.empty(N, hkv, D, dtype=gdt, device=q.device)
         dv = torch.empty(N, hkv, D, dtype=gdt, device=q.device)
     else:
         dq, dk, dv = out
-    nbytes = tree_attn_bwd_workspace_bytes(plan, hq, D, q.dtype)
-    if workspace is None:
-        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
-    s = _stream_ptr(stream)
-    plan.to_device(s)
     check(lib.tree_attn_bwd(plan.handle, do.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(),
                             o.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                            dv.data_ptr(), hq, hkv, D, _dtype_code(q),
-                            DTYPE_BF16 if gdt == torch.bfloat16 else DTYPE_F32,
+                            dv.data_ptr(), hq, hkv, D, _dtype_code(q), gcode,
                             float(softmax_scale), workspace.data_ptr(), workspace.numel(), s))
     return dq, dk, dv
+
+
+def tree_attn_bwd_dq(plan: Plan, do, q, k, v, o, lse, workspace, softmax_scale: float = 0.0,
+                     grad_dtype=None, out=None, stream=None):
+    """First phase of the backward: Delta into ``workspace``, then dq."""
+    import torch
+
+    N, hq, hkv, D, gdt, gcode, workspace, s = _bwd_prepare(plan, do, q, k, v, o, lse, grad_dtype,
+                                                           workspace, stream)
+    dq = torch.empty(N, hq, D, dtype=gdt, device=q.device) if out is None else out
+    check(lib.tree_attn_bwd_dq(plan.handle, do.data_ptr(), q.data_ptr(), k.data_ptr(),
+                               v.data_ptr(), o.data_ptr(), lse.data_ptr(), dq.data_ptr(), hq, hkv,
+                               D, _dtype_code(q), gcode, float(softmax_scale),
+                               workspace.data_ptr(), workspace.numel(), s))
+    return dq
+
+
+def tree_attn_bwd_dkdv(plan: Plan, do, q, k, v, lse, workspace, softmax_scale: float = 0.0,
+                       grad_dtype=None, out=None, stream=None):
+    """Second phase of the backward: (dk, dv) from the workspace tree_attn_bwd_dq filled."""
+    import torch
+
+    N, hq, hkv, D, gdt, gcode, workspace, s = _bwd_prepare(plan, do, q, k, v, None, lse,
+                                                           grad_dtype, workspace, stream)
+    if out is None:
+        dk = torch.empty(N, hkv, D, dtype=gdt, device=q.device)
+        dv = torch.empty(N, hkv, D, dtype=gdt, device=q.device)
+    else:
+        dk, dv = out
+    check(lib.tree_attn_bwd_dkdv(plan.handle, do.data_ptr(), q.data_ptr(), k.data_ptr(),
+                                 v.data_ptr(), lse.data_ptr(), dk.data_ptr(), dv.data_ptr(), hq,
+                                 hkv, D, _dtype_code(q), gcode, float(softmax_scale),
+                                 workspace.data_ptr(), workspace.numel(), s))
+    return dk, dv
 
 
 def tree_weights(plan: Plan) -> np.ndarray:

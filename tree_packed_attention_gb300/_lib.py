@@ -36,7 +36,8 @@ FIELDS = [
 EXPORTS = [
     "tree_plan_build", "tree_plan_info", "tree_plan_get", "tree_plan_field_len",
     "tree_plan_to_device", "tree_plan_destroy", "tree_attn_fwd", "tree_attn_bwd_workspace_bytes",
-    "tree_attn_bwd", "tree_attn_bwd_static_scratch", "tree_weights", "tree_status_sync",
+    "tree_attn_bwd", "tree_attn_bwd_dq", "tree_attn_bwd_dkdv", "tree_attn_bwd_static_scratch",
+    "tree_weights", "tree_status_sync",
     "tree_last_error",
 ]
 
@@ -73,6 +74,10 @@ def _load():
         "tree_attn_bwd_workspace_bytes": (sz, [vp, i32, i32, i32]),
         "tree_attn_bwd": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                 C.c_float, vp, sz, vp]),
+        "tree_attn_bwd_dq": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                   C.c_float, vp, sz, vp]),
+        "tree_attn_bwd_dkdv": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                     C.c_float, vp, sz, vp]),
         "tree_attn_bwd_static_scratch": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                                                i32, i32, C.c_float, vp]),
         "tree_weights": (i32, [vp, vp]),

@@ -852,10 +852,13 @@ cudaError_t launch_bwd_bf16(const AttnBwdArgs& a) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  tree_attn_bwd_dq_sm103<<<d.n_items < sms ? d.n_items : sms, kDqThreads, kDqSmem, a.stream>>>(
-      mq, mk, mv, mdo, d);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (a.phases & 1) {
+    tree_attn_bwd_dq_sm103<<<d.n_items < sms ? d.n_items : sms, kDqThreads, kDqSmem, a.stream>>>(
+        mq, mk, mv, mdo, d);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (!(a.phases & 2)) return cudaSuccess;
   tree_attn_bwd_dkdv_sm103<<<k.n_items < sms ? k.n_items : sms, kKvThreads, kKvSmem, a.stream>>>(
       mq, mk, mv, mdo, k);
   return cudaGetLastError();

@@ -167,13 +167,15 @@ extern "C" size_t tree_attn_bwd_workspace_bytes(const tree_plan_t* p, int32_t hq
                                  : bwd_workspace_bf16(p->N, hq, head_dim);
 }
 
-extern "C" tree_status_t tree_attn_bwd(const tree_plan_t* p, const void* dout, const void* q,
-                                       const void* k, const void* v, const void* o,
-                                       const float* lse, void* dq, void* dk, void* dv, int32_t hq,
-                                       int32_t hkv, int32_t head_dim, tree_dtype_t dtype,
-                                       tree_dtype_t grad_dtype, float softmax_scale,
-                                       void* workspace, size_t workspace_bytes,
-                                       tree_stream_t stream) {
+namespace {
+
+// Shared by the whole backward and its two phases. phases: bit 0 the dQ phase
+// (Delta, lse*log2e into the workspace, dQ), bit 1 the dK/dV phase.
+tree_status_t bwd_entry(const tree_plan_t* p, const void* dout, const void* q, const void* k,
+                        const void* v, const void* o, const float* lse, void* dq, void* dk,
+                        void* dv, int32_t hq, int32_t hkv, int32_t head_dim, tree_dtype_t dtype,
+                        tree_dtype_t grad_dtype, float softmax_scale, void* workspace,
+                        size_t workspace_bytes, tree_stream_t stream, int phases) {
   if (!p) return fail(TREE_ERR_INVALID_ARG, "NULL plan");
   tree_status_t st = check_heads(hq, hkv, head_dim, dtype);
   if (st != TREE_OK) return st;
@@ -184,11 +186,19 @@ extern "C" tree_status_t tree_attn_bwd(const tree_plan_t* p, const void* dout, c
   if (!std::isfinite(softmax_scale) || softmax_scale < 0.f)
     return fail(TREE_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
   if (p->N == 0) return TREE_OK;
-  const void* ptrs[] = {dout, q, k, v, o, lse, dq, dk, dv, workspace};
-  for (const void* x : ptrs) {
-    if (!x) return fail(TREE_ERR_INVALID_ARG, "NULL tensor or workspace pointer");
-    if (!aligned16(x)) return fail(TREE_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
-  }
+  const void* common[] = {dout, q, k, v, lse, workspace};
+  const void* phase_dq[] = {o, dq};
+  const void* phase_kv[] = {dk, dv};
+  auto check = [](const void* const* xs, size_t n) -> tree_status_t {
+    for (size_t i = 0; i < n; ++i) {
+      if (!xs[i]) return fail(TREE_ERR_INVALID_ARG, "NULL tensor or workspace pointer");
+      if (!aligned16(xs[i])) return fail(TREE_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    }
+    return TREE_OK;
+  };
+  if ((st = check(common, 6)) != TREE_OK) return st;
+  if ((phases & 1) && (st = check(phase_dq, 2)) != TREE_OK) return st;
+  if ((phases & 2) && (st = check(phase_kv, 2)) != TREE_OK) return st;
   const size_t need = tree_attn_bwd_workspace_bytes(p, hq, head_dim, dtype);
   if (workspace_bytes < need)
     return fail(TREE_ERR_INVALID_ARG, "workspace too small: need " + std::to_string(need) + " bytes");
@@ -198,10 +208,45 @@ extern "C" tree_status_t tree_attn_bwd(const tree_plan_t* p, const void* dout, c
   AttnBwdArgs a{p,  dout, q,   k,   v,        o,        lse,
                 dq, dk,   dv,  hq,  hkv,      head_dim, grad_dtype == TREE_DTYPE_F32,
                 resolve_scale(softmax_scale, head_dim), workspace, workspace_bytes,
-                static_cast<cudaStream_t>(stream), status};
+                static_cast<cudaStream_t>(stream), status, phases};
   cudaError_t e = dtype == TREE_DTYPE_F32 ? launch_bwd_f32(a) : launch_bwd_bf16(a);
   if (e != cudaSuccess) return cuda_fail(e, "tree_attn_bwd launch");
   return TREE_OK;
+}
+
+}  // namespace
+
+extern "C" tree_status_t tree_attn_bwd(const tree_plan_t* p, const void* dout, const void* q,
+                                       const void* k, const void* v, const void* o,
+                                       const float* lse, void* dq, void* dk, void* dv, int32_t hq,
+                                       int32_t hkv, int32_t head_dim, tree_dtype_t dtype,
+                                       tree_dtype_t grad_dtype, float softmax_scale,
+                                       void* workspace, size_t workspace_bytes,
+                                       tree_stream_t stream) {
+  return bwd_entry(p, dout, q, k, v, o, lse, dq, dk, dv, hq, hkv, head_dim, dtype, grad_dtype,
+                   softmax_scale, workspace, workspace_bytes, stream, 3);
+}
+
+extern "C" tree_status_t tree_attn_bwd_dq(const tree_plan_t* p, const void* dout, const void* q,
+                                          const void* k, const void* v, const void* o,
+                                          const float* lse, void* dq, int32_t hq, int32_t hkv,
+                                          int32_t head_dim, tree_dtype_t dtype,
+                                          tree_dtype_t grad_dtype, float softmax_scale,
+                                          void* workspace, size_t workspace_bytes,
+                                          tree_stream_t stream) {
+  return bwd_entry(p, dout, q, k, v, o, lse, dq, nullptr, nullptr, hq, hkv, head_dim, dtype,
+                   grad_dtype, softmax_scale, workspace, workspace_bytes, stream, 1);
+}
+
+extern "C" tree_status_t tree_attn_bwd_dkdv(const tree_plan_t* p, const void* dout, const void* q,
+                                            const void* k, const void* v, const float* lse,
+                                            void* dk, void* dv, int32_t hq, int32_t hkv,
+                                            int32_t head_dim, tree_dtype_t dtype,
+                                            tree_dtype_t grad_dtype, float softmax_scale,
+                                            void* workspace, size_t workspace_bytes,
+                                            tree_stream_t stream) {
+  return bwd_entry(p, dout, q, k, v, nullptr, lse, nullptr, dk, dv, hq, hkv, head_dim, dtype,
+                   grad_dtype, softmax_scale, workspace, workspace_bytes, stream, 2);
 }
 
 extern "C" tree_status_t tree_status_sync(tree_stream_t stream) {

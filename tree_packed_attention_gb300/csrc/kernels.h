@@ -38,6 +38,7 @@ struct AttnBwdArgs {
   size_t workspace_bytes;
   cudaStream_t stream;
   int* status;
+  int phases;  // bit 0: Delta + dQ phase; bit 1: dK/dV phase (reads what phase 0 wrote)
 };
 
 // Workspace layouts.

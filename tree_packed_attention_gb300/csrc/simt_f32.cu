@@ -201,13 +201,16 @@ cudaError_t bwd_f32(const AttnBwdArgs& a) {
   const int N = p->N;
   float* delta = static_cast<float*>(a.workspace);
   const long long rows = (long long)N * a.hq;
-  bwd_pre_f32_kernel<D><<<(unsigned)((rows + kWarps - 1) / kWarps), kWarps * 32, 0, a.stream>>>(
-      static_cast<const float*>(a.dout), static_cast<const float*>(a.o), delta, N, a.hq);
-  bwd_dq_f32_kernel<D><<<dim3(p->Tq, a.hq), kWarps * 32, 0, a.stream>>>(
-      static_cast<const float*>(a.q), static_cast<const float*>(a.k),
-      static_cast<const float*>(a.v), static_cast<const float*>(a.dout), a.lse, delta,
-      static_cast<float*>(a.dq), p->dev.key_end, p->dev.qt_ptr, p->dev.qt_kt, N, a.hq, a.hkv,
-      a.scale);
+  if (a.phases & 1) {
+    bwd_pre_f32_kernel<D><<<(unsigned)((rows + kWarps - 1) / kWarps), kWarps * 32, 0, a.stream>>>(
+        static_cast<const float*>(a.dout), static_cast<const float*>(a.o), delta, N, a.hq);
+    bwd_dq_f32_kernel<D><<<dim3(p->Tq, a.hq), kWarps * 32, 0, a.stream>>>(
+        static_cast<const float*>(a.q), static_cast<const float*>(a.k),
+        static_cast<const float*>(a.v), static_cast<const float*>(a.dout), a.lse, delta,
+        static_cast<float*>(a.dq), p->dev.key_end, p->dev.qt_ptr, p->dev.qt_kt, N, a.hq, a.hkv,
+        a.scale);
+  }
+  if (!(a.phases & 2)) return cudaGetLastError();
   bwd_dkdv_f32_kernel<D><<<dim3(p->Tk, a.hkv), kWarps * 32, 0, a.stream>>>(
       static_cast<const float*>(a.q), static_cast<const float*>(a.k),
       static_cast<const float*>(a.v), static_cast<const float*>(a.dout), a.lse, delta,
