@@ -26,6 +26,7 @@
 #include <cmath>
 
 #include "kernels.h"
+#include "sched.cuh"
 #include "sm103_ptx.cuh"
 #include "tma_host.h"
 
@@ -118,6 +119,7 @@ struct DqParams {
   float* delta;  // out: [hq, Npad]
   void* dq;
   int* status;
+  SchedSlot* sched;
   int N, Npad, hq, group, n_items, out_f32;
   float scale, scale_log2;
 };
@@ -138,12 +140,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   __shared__ uint64_t bar_dp_full, bar_ds_full, bar_dq_full, bar_dq_free;
   __shared__ uint64_t bar_ke[2];
   __shared__ __align__(16) int ke_buf[2][128];
+  __shared__ ItemRing ring;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   volatile int* abort = &abort_s;
   if (threadIdx.x == 0) {
+    item_ring_init(&ring, 9);  // consumers: the MMA warp and the 8 softmax warps
     mbar_init(&bar_q_full, 1);
     mbar_init(&bar_q_empty, 1);
     mbar_init(&bar_final, 1);
@@ -184,10 +188,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    uint32_t kv = 0, qn = 0;
-    bool ok = true;
-    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
-      const int qt = p.order[it / p.hq], h = it % p.hq, kvh = h / p.group;
+    uint32_t kv = 0, qn = 0, pub = 0;
+    int cur = item_fetch(p.sched, p.n_items), nxt = -1;  // items are taken one ahead
+    bool ok = item_put(&ring, pub, cur, abort, p.status);
+    if (ok && cur >= 0) {
+      nxt = item_fetch(p.sched, p.n_items);
+      ok = item_put(&ring, pub, nxt, abort, p.status);
+    }
+    while (ok && cur >= 0) {
+      const int qt = p.order[cur / p.hq], h = cur % p.hq, kvh = h / p.group;
       if (qn > 0 && !(ok = warp_wait(&bar_q_empty, (qn - 1) & 1, abort, p.status))) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bar_q_full, 2 * kTileBytes);
@@ -195,9 +204,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         tma_load_3d(smem + kDqOffQ + kHalfBytes, &map_q, &bar_q_full, 64, h, qt * 128);
         tma_load_3d(smem + kDqOffDO, &map_do, &bar_q_full, 0, h, qt * 128);
         tma_load_3d(smem + kDqOffDO + kHalfBytes, &map_do, &bar_q_full, 64, h, qt * 128);
-        const int nit = it + gridDim.x;  // the next item's Q and dO into L2
-        if (nit < p.n_items) {
-          const int nqt = p.order[nit / p.hq], nh = nit % p.hq;
+        if (nxt >= 0) {  // the next item's Q and dO into L2
+          const int nqt = p.order[nxt / p.hq], nh = nxt % p.hq;
           tma_prefetch_l2_3d(&map_q, 0, nh, nqt * 128);
           tma_prefetch_l2_3d(&map_q, 64, nh, nqt * 128);
           tma_prefetch_l2_3d(&map_do, 0, nh, nqt * 128);
@@ -227,6 +235,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
         __syncwarp();
       }
+      if (!ok) break;
+      cur = nxt;
+      if (cur >= 0) {
+        nxt = item_fetch(p.sched, p.n_items);
+        ok = item_put(&ring, pub, nxt, abort, p.status);
+      }
     }
     if (!ok && lane == 0) {
       if (qn > 0) mbar_drain(&bar_q_full, (qn - 1) & 1);
@@ -241,10 +255,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     // dP_{t+1}, S_{t+2} (into the S buffer dQ_t just read).
     const uint32_t aQ = smem_u32(smem + kDqOffQ), aDO = smem_u32(smem + kDqOffDO);
     const uint32_t aK = smem_u32(smem + kDqOffK), aV = smem_u32(smem + kDqOffV);
-    uint32_t kv = 0, qn = 0, n = 0;
+    uint32_t kv = 0, qn = 0, n = 0, got = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
-      const int qt = p.order[it / p.hq];
+    for (int cur; (ok = item_get(&ring, got, cur, abort, p.status)) && cur >= 0;) {
+      const int qt = p.order[cur / p.hq];
       const int T = p.qt_ptr[qt + 1] - p.qt_ptr[qt];
       if (!(ok = warp_wait(&bar_q_full, qn & 1, abort, p.status))) break;
       ++qn;
@@ -279,16 +293,18 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         tc_fence_after_sync();
         mma_tn_split(tDQ, tS + (t & 1) * 128, k_stage(i), t > 0);  // dQ += dS_t K_t
         mma_commit_warp(&bar_k_empty[i % kDqKStages]);
-        if (t + 1 == T) {
-          mma_commit_warp(&bar_dq_full);
-          mma_commit_warp(&bar_q_empty);
-        }
+        if (t + 1 == T) mma_commit_warp(&bar_dq_full);
+        if (T == 1) mma_commit_warp(&bar_q_empty);  // the softmax warps read dO for Delta
+                                                    // before the first dS arrives
         if (t + 1 < T) {
           if (!(ok = wait_v(i + 1))) break;
           tc_fence_after_sync();
           mma_kk(tDP, aDO, v_stage(i + 1), 0);  // dP_{t+1} (dP_t already read)
           mma_commit_warp(&bar_dp_full);
           mma_commit_warp(&bar_v_empty[(i + 1) % kDqVStages]);
+          // dP_{T-1} is the item's last reader of Q and dO (S_{T-1} came
+          // before it): the next item's Q and dO load during the last step.
+          if (t + 2 == T) mma_commit_warp(&bar_q_empty);
         }
         if (t + 2 < T) {
           if (!(ok = wait_k(i + 2))) break;
@@ -314,17 +330,39 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const float sl2 = p.scale_log2;
     uint32_t n = 0, qn = 0, kb = 0, ku[2] = {0, 0}, su[2] = {0, 0};
     bool ok = true;
-    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
-      const int qt = p.order[it / p.hq], h = it % p.hq;
+    // The next item's q-tile and tile range are read one item ahead, and each
+    // tile's kind, k-tile and key_end entry one tile ahead, so no global load
+    // latency sits between two passes over S.
+    int n_qt = 0, n_beg = 0, n_end = 0;
+    auto fetch_header = [&](int at) {
+      n_qt = __ldg(p.order + at / p.hq);
+      n_beg = __ldg(p.qt_ptr + n_qt);
+      n_end = __ldg(p.qt_ptr + n_qt + 1);
+    };
+    int nt_kind = 0, nt_kt = 0, nt_kev = 0, nt_at = -1;
+    auto fetch_tile = [&](int t) {
+      nt_kind = __ldg(p.qt_kind + t);
+      nt_kt = __ldg(p.qt_kt + t);
+      const int j = nt_kt * 128 + r;
+      nt_kev = j < p.N ? __ldg(p.key_end + j) : 0;
+      nt_at = t;
+    };
+    uint32_t got = 0;
+    int nxt = -1;
+    ok = item_get(&ring, got, nxt, abort, p.status);
+    if (ok && nxt >= 0) fetch_header(nxt);
+    while (ok && nxt >= 0) {
+      const int qt = n_qt, h = nxt % p.hq, beg = n_beg, end = n_end;
+      if (!(ok = item_get(&ring, got, nxt, abort, p.status))) break;
+      if (nxt >= 0) fetch_header(nxt);
       const int i = qt * 128 + r;
       const size_t row = static_cast<size_t>(i) * p.hq + h;
       // The next item's O row (for its Delta) is prefetched into L2.
       {
-        const int nit = it + gridDim.x;
-        if (nit < p.n_items) {
-          const int ni = p.order[nit / p.hq] * 128 + r;
+        if (nxt >= 0) {
+          const int ni = n_qt * 128 + r;
           if (ni < p.N) {
-            const __nv_bfloat16* nrow = p.o + (static_cast<size_t>(ni) * p.hq + nit % p.hq) * 128;
+            const __nv_bfloat16* nrow = p.o + (static_cast<size_t>(ni) * p.hq + nxt % p.hq) * 128;
             prefetch_l2(nrow);
             prefetch_l2(nrow + 64);
           }
@@ -356,16 +394,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         p.lse2[static_cast<size_t>(h) * p.Npad + i] = lse2;
       }
       ++qn;
-      const int beg = p.qt_ptr[qt], end = p.qt_ptr[qt + 1];
+      if (nt_at != beg) fetch_tile(beg);
       for (int t = beg; t < end; ++t, ++n) {
-        const int kd = p.qt_kind[t];
-        const int kt = p.qt_kt[t];
+        const int kd = nt_kind, kt = nt_kt, kev = nt_kev;
+        if (t + 1 < end)
+          fetch_tile(t + 1);
+        else if (nxt >= 0)
+          fetch_tile(n_beg);
         const int* ke = nullptr;
         if (kd == 1) {  // PARTIAL: the 128 key bounds of this tile, shared through smem
-          if (half == 0) {
-            const int j = kt * 128 + r;
-            ke_buf[kb][r] = j < p.N ? __ldg(p.key_end + j) : 0;
-          }
+          if (half == 0) ke_buf[kb][r] = kev;
           mbar_arrive(&bar_ke[kb]);
           if (!(ok = warp_wait(&bar_ke[kb], ku[kb] & 1, abort, p.status))) break;
           ++ku[kb];
@@ -435,6 +473,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  if (threadIdx.x == 0) sched_finish(p.sched);
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
@@ -460,7 +499,8 @@ constexpr uint32_t kKvOffLse = kKvOffDO + kKvDoStages * kTileBytes;  // per dO s
 constexpr uint32_t kKvOffDelta = kKvOffLse + kKvDoStages * 512;     // per dO stage: 128 fp32
 constexpr uint32_t kKvOffBar = kKvOffDelta + kKvDoStages * 512;
 constexpr uint32_t kKvNumBars = 20;
-constexpr uint32_t kKvSmem = kKvOffBar + kKvNumBars * 8 + 16;
+constexpr uint32_t kKvOffRing = kKvOffBar + kKvNumBars * 8 + 16;
+constexpr uint32_t kKvSmem = kKvOffRing + sizeof(ItemRing);
 static_assert(kKvSmem <= 232448, "shared memory budget");
 
 struct KvParams {
@@ -473,6 +513,7 @@ struct KvParams {
   void* dk;
   void* dv;
   int* status;
+  SchedSlot* sched;
   int N, Npad, hq, hkv, group, n_items, out_f32;
   float scale, scale_log2;
 };
@@ -517,8 +558,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   uint64_t* bar_final = bars + 17;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kKvNumBars);
   volatile int* abort = reinterpret_cast<volatile int*>(bars + kKvNumBars) + 1;
+  ItemRing* ring = reinterpret_cast<ItemRing*>(smem + kKvOffRing);
 
   if (threadIdx.x == 0) {
+    item_ring_init(ring, 9);  // consumers: the MMA warp and the 8 softmax warps
     mbar_init(bar_kv_full, 1);
     mbar_init(bar_kv_empty, 1);
     for (int s = 0; s < kKvQStages; ++s) {
@@ -556,10 +599,15 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    uint32_t n = 0, items = 0;
-    bool ok = true;
-    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++items) {
-      const KvItem x = decode_kv(p, it);
+    uint32_t n = 0, items = 0, pub = 0;
+    int cur = item_fetch(p.sched, p.n_items), nxt = -1;  // items are taken one ahead
+    bool ok = item_put(ring, pub, cur, abort, p.status);
+    if (ok && cur >= 0) {
+      nxt = item_fetch(p.sched, p.n_items);
+      ok = item_put(ring, pub, nxt, abort, p.status);
+    }
+    while (ok && cur >= 0) {
+      const KvItem x = decode_kv(p, cur);
       if (items > 0 && !(ok = warp_wait(bar_kv_empty, (items - 1) & 1, abort, p.status))) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(bar_kv_full, 2 * kTileBytes);
@@ -568,9 +616,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tma_load_3d(smem + kKvOffK + kHalfBytes, &map_k, bar_kv_full, 64, x.kvh, row0);
         tma_load_3d(smem + kKvOffV, &map_v, bar_kv_full, 0, x.kvh, row0);
         tma_load_3d(smem + kKvOffV + kHalfBytes, &map_v, bar_kv_full, 64, x.kvh, row0);
-        const int nit = it + gridDim.x;  // the next item's K and V into L2
-        if (nit < p.n_items) {
-          const KvItem y = decode_kv(p, nit);
+        if (nxt >= 0) {  // the next item's K and V into L2
+          const KvItem y = decode_kv(p, nxt);
           tma_prefetch_l2_3d(&map_k, 0, y.kvh, y.kt * 128);
           tma_prefetch_l2_3d(&map_k, 64, y.kvh, y.kt * 128);
           tma_prefetch_l2_3d(&map_v, 0, y.kvh, y.kt * 128);
@@ -604,6 +651,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         }
         __syncwarp();
       }
+      if (!ok) break;
+      ++items;
+      cur = nxt;
+      if (cur >= 0) {
+        nxt = item_fetch(p.sched, p.n_items);
+        ok = item_put(ring, pub, nxt, abort, p.status);
+      }
     }
     if (!ok && lane == 0) {
       if (items > 0) mbar_drain(bar_kv_full, (items - 1) & 1);
@@ -625,10 +679,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     auto wait_do = [&](uint32_t i) {
       return warp_wait(bar_do_full + i % kKvDoStages, (i / kKvDoStages) & 1, abort, p.status);
     };
-    uint32_t n = 0, items = 0;
+    uint32_t n = 0, items = 0, got = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++items) {
-      const KvItem x = decode_kv(p, it);
+    for (int cur; (ok = item_get(ring, got, cur, abort, p.status)) && cur >= 0; ++items) {
+      const KvItem x = decode_kv(p, cur);
       if (!(ok = warp_wait(bar_kv_full, items & 1, abort, p.status))) break;
       for (int j = 0; j < x.steps; ++j, ++n) {
         if (j == 0) {
@@ -683,10 +737,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const uint32_t col0 = half * 64;
     const uint32_t tSr = tA + lane_off + col0, tPr = tB + lane_off + col0;
     const float sl2 = p.scale_log2;
-    uint32_t n = 0, items = 0;
+    uint32_t n = 0, items = 0, got = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++items) {
-      const KvItem x = decode_kv(p, it);
+    for (int cur; (ok = item_get(ring, got, cur, abort, p.status)) && cur >= 0; ++items) {
+      const KvItem x = decode_kv(p, cur);
       const int jk = x.kt * 128 + kr;
       const int ke = jk < p.N ? __ldg(p.key_end + jk) : 0;  // rows [jk, ke) see this key
       for (int j = 0; j < x.steps; ++j, ++n) {
@@ -781,6 +835,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  if (threadIdx.x == 0) sched_finish(p.sched);
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
@@ -813,6 +868,7 @@ cudaError_t launch_bwd_bf16(const AttnBwdArgs& a) {
   d.delta = delta;
   d.dq = a.dq;
   d.status = a.status;
+  d.sched = next_sched_slot();
   d.N = N;
   d.Npad = Npad;
   d.hq = a.hq;
@@ -832,6 +888,8 @@ cudaError_t launch_bwd_bf16(const AttnBwdArgs& a) {
   k.dk = a.dk;
   k.dv = a.dv;
   k.status = a.status;
+  k.sched = next_sched_slot();
+  if (!d.sched || !k.sched) return cudaErrorInvalidDevicePointer;
   k.N = N;
   k.Npad = Npad;
   k.hq = a.hq;

@@ -2,6 +2,7 @@
 // the device status word.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <string>
@@ -9,11 +10,23 @@
 
 #include "kernels.h"
 #include "plan_internal.h"
+#include "sched.cuh"
 
 namespace treeattn {
 
 // Set by kernels that give up a bounded wait; read and cleared by tree_status_sync.
 __device__ int g_status_word = 0;
+
+// Work counters of the persistent kernels, one slot per launch in turn; a
+// launch's last CTA zeroes its slot.
+__device__ SchedSlot g_sched[kSchedSlots];
+
+SchedSlot* next_sched_slot() {
+  static std::atomic<uint32_t> seq{0};
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_sched) != cudaSuccess) return nullptr;
+  return static_cast<SchedSlot*>(p) + seq.fetch_add(1u) % kSchedSlots;
+}
 
 namespace {
 

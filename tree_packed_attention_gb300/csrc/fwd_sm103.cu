@@ -31,6 +31,7 @@
 #include <cmath>
 
 #include "kernels.h"
+#include "sched.cuh"
 #include "sm103_ptx.cuh"
 #include "tma_host.h"
 
@@ -45,6 +46,7 @@ constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one 128 x 128 bf16 operand ti
 constexpr uint32_t kHalfBytes = kTileBytes / 2;  // its 64-column half (one TMA box)
 constexpr uint32_t kSmemBytes = 1024 + 2 * kTileBytes + 2 * kStages * kTileBytes;
 constexpr float kRescaleThreshold = 8.0f;
+constexpr uint32_t kRegsCtl = 72, kRegsSoftmax = 216;
 
 struct FwdParams {
   const int32_t* key_end;
@@ -55,6 +57,7 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   int* status;
+  SchedSlot* sched;
   int N, hq, group, n_items, n_inner, mode, Tq;
   float scale_log2;  // softmax scale * log2(e)
 };
@@ -94,6 +97,21 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int it) {
 __device__ __forceinline__ int kinds_at(const FwdParams& p, int t) {
   const int k = p.list_kind[t];
   return p.mode == 0 ? (k | (k << 2)) : k;
+}
+
+// One tile of a slot's list as the softmax warps need it: its kind, its k-tile
+// and this thread's entry of key_end for that k-tile (key kt*128 + r).
+struct TileInfo {
+  int kind, kt, kev;
+};
+
+__device__ __forceinline__ TileInfo load_tile(const FwdParams& p, int t, int s, int r) {
+  TileInfo x;
+  x.kind = (kinds_at(p, t) >> (2 * s)) & 3;
+  x.kt = __ldg(p.list_kt + t);
+  const int j = x.kt * 128 + r;
+  x.kev = j < p.N ? __ldg(p.key_end + j) : 0;
+  return x;
 }
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
@@ -142,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_o_full[2], bar_o_free[2];
   __shared__ uint64_t bar_ke[2][2];
   __shared__ __align__(16) int ke_buf[2][2][128];
+  __shared__ ItemRing ring;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
 
@@ -149,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = &abort_s;
 
   if (threadIdx.x == 0) {
+    item_ring_init(&ring, 9);  // consumers: the MMA warp and the 8 softmax warps
     mbar_init(&bar_q_full, 1);
     mbar_init(&bar_q_empty, 1);
     mbar_init(&bar_final, 1);
@@ -182,13 +202,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = tmem_base_s;
+  // Registers: launched with 168 a thread (384 x 168 = 64512); warps 0-3 give
+  // theirs down to 72 and the two softmax warpgroups take 216:
+  // 128 x 72 + 256 x 216 = 64512.
+  static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kThreads * 168, "register split");
 
   if (warp == 0) {
+    regs_dec<kRegsCtl>();
     // ------------------------------------------------------------ producer
-    uint32_t kv = 0, qn = 0;
-    bool ok = true;
-    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
-      const Item x = decode_item(p, it);
+    uint32_t kv = 0, qn = 0, pub = 0;
+    // Items are taken one ahead: the ring holds the next item's number while
+    // this one loads.
+    int cur = item_fetch(p.sched, p.n_items), nxt = -1;
+    bool ok = item_put(&ring, pub, cur, abort, p.status);
+    if (ok && cur >= 0) {
+      nxt = item_fetch(p.sched, p.n_items);
+      ok = item_put(&ring, pub, nxt, abort, p.status);
+    }
+    while (ok && cur >= 0) {
+      const Item x = decode_item(p, cur);
       if (qn > 0 && !(ok = warp_wait(&bar_q_empty, (qn - 1) & 1, abort, p.status))) break;
       if (lane == 0) {
         const uint32_t bytes = (x.qtile[1] < p.Tq ? 2u : 1u) * kTileBytes;
@@ -199,9 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sQ + s * kTileBytes + kHalfBytes, &map_q, &bar_q_full, 64, x.head[s],
                       x.qtile[s] * 128);
         }
-        const int nit = it + gridDim.x;  // the next item's Q tiles into L2
-        if (nit < p.n_items) {
-          const Item y = decode_item(p, nit);
+        if (nxt >= 0) {  // the next item's Q tiles into L2
+          const Item y = decode_item(p, nxt);
           for (int s = 0; s < 2; ++s) {
             if (y.qtile[s] >= p.Tq) continue;
             tma_prefetch_l2_3d(&map_q, 0, y.head[s], y.qtile[s] * 128);
@@ -229,6 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
+      if (!ok) break;
+      cur = nxt;
+      if (cur >= 0) {
+        nxt = item_fetch(p.sched, p.n_items);
+        ok = item_put(&ring, pub, nxt, abort, p.status);
+      }
     }
     if (!ok && lane == 0) {  // let copies in flight land before the CTA exits
       if (qn > 0) mbar_drain(&bar_q_full, (qn - 1) & 1);
@@ -238,14 +275,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
+    regs_dec<kRegsCtl>();
     // ---------------------------------------------------------- MMA issuer
     // The whole warp runs this branch; one elected lane issues each MMA.
-    uint32_t kv = 0, qn = 0;
+    uint32_t kv = 0, qn = 0, got = 0;
     uint32_t pc[2] = {0, 0}, oc[2] = {0, 0};
     const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
     bool ok = true;
-    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
-      const Item x = decode_item(p, it);
+    for (int cur; (ok = item_get(&ring, got, cur, abort, p.status)) && cur >= 0;) {
+      const Item x = decode_item(p, cur);
       const int T = x.end - x.beg;
       if (!(ok = warp_wait(&bar_q_full, qn & 1, abort, p.status))) break;
       ++qn;
@@ -311,7 +349,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_commit_warp(&bar_final);  // every MMA issued by this CTA completes before TMEM is freed
     if (lane == 0) mbar_drain(&bar_final, 0);
     __syncwarp();
-  } else if (warp >= 4) {
+  } else if (warp < 4) {
+    regs_dec<kRegsCtl>();  // warps 2-3: idle
+  } else {
+    regs_inc<kRegsSoftmax>();
     // ------------------------------------------------------------- softmax
     const int s = (warp - 4) / 4;
     const int quarter = warp % 4;
@@ -322,20 +363,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     uint32_t sc = 0, oc = 0, kb = 0, ku[2] = {0, 0};
     bool ok = true;
-    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
-      const Item x = decode_item(p, it);
-      if (x.qtile[s] >= p.Tq) continue;
-      const int i = x.qtile[s] * 128 + r;
-      const int h = x.head[s];
+    // The tile after the current one (in this item, else the next item's
+    // first) is loaded one tile ahead, and the next item's header one item
+    // ahead, so no global load latency sits between two softmax passes.
+    int n_qt = 0, n_h = 0, n_beg = 0, n_end = 0;  // next item: q-tile, head, tile range
+    auto fetch_header = [&](int at) {
+      const Item y = decode_item(p, at);
+      n_qt = y.qtile[s];
+      n_h = y.head[s];
+      n_beg = y.beg;
+      n_end = y.end;
+    };
+    uint32_t got = 0;
+    int nxt = -1;
+    ok = item_get(&ring, got, nxt, abort, p.status);
+    if (ok && nxt >= 0) fetch_header(nxt);
+    TileInfo nt;
+    int nt_at = -1;
+    while (ok && nxt >= 0) {
+      const int qt = n_qt, h = n_h, beg = n_beg, end = n_end;
+      if (!(ok = item_get(&ring, got, nxt, abort, p.status))) break;
+      if (nxt >= 0) fetch_header(nxt);
+      if (qt >= p.Tq) continue;
+      const int i = qt * 128 + r;
       float m_ref = -INFINITY, l = 0.f;
-      for (int t = x.beg; t < x.end; ++t) {
-        const int kd = (kinds_at(p, t) >> (2 * s)) & 3;
+      if (nt_at != beg) nt = load_tile(p, beg, s, r);
+      for (int t = beg; t < end; ++t) {
+        const TileInfo cur = nt;
+        nt_at = t + 1 < end ? t + 1 : (nxt >= 0 ? n_beg : -1);
+        if (nt_at >= 0) nt = load_tile(p, nt_at, s, r);
+        const int kd = cur.kind;
         if (kd == 0) continue;
-        const int kt = p.list_kt[t];
+        const int kt = cur.kt;
         const int* ke = nullptr;
         if (kd == 1) {  // PARTIAL: the 128 key bounds of this tile, shared through smem
-          const int j = kt * 128 + r;
-          ke_buf[s][kb][r] = j < p.N ? __ldg(p.key_end + j) : 0;
+          ke_buf[s][kb][r] = cur.kev;
           mbar_arrive(&bar_ke[s][kb]);
           if (!(ok = warp_wait(&bar_ke[s][kb], ku[kb] & 1, abort, p.status))) break;
           ++ku[kb];
@@ -448,6 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  if (threadIdx.x == 0) sched_finish(p.sched);
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
@@ -484,6 +547,8 @@ cudaError_t launch_fwd_bf16(const AttnArgs& a) {
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
   p.status = a.status;
+  p.sched = next_sched_slot();
+  if (!p.sched) return cudaErrorInvalidDevicePointer;
   p.N = pl->N;
   p.hq = a.hq;
   p.group = G;

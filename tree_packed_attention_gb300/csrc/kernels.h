@@ -7,6 +7,10 @@
 
 namespace treeattn {
 
+struct SchedSlot;
+// A fresh run-time scheduler counter for one kernel launch (nullptr on error).
+SchedSlot* next_sched_slot();
+
 struct AttnArgs {
   const tree_plan* plan;
   const void* q;

@@ -153,6 +153,19 @@ __device__ __forceinline__ void tmem_alloc(uint32_t* smem_result, uint32_t ncols
                : "memory");
 }
 
+// Per-warpgroup register budgets (every warp of a warpgroup executes the same
+// one). A kernel's splits must add up to at most the registers it was
+// launched with (threads x registers per thread): .inc waits for the
+// registers that the .dec of other warpgroups returned to the CTA's pool.
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegs));
+}
+
 __device__ __forceinline__ void tmem_relinquish() {
   asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
