@@ -100,6 +100,10 @@ constexpr int kDqThreads = 384;
 // K_t is read by S_t and, a step later, by dQ_t; S_{t+2} is issued right after
 // dQ_t, so K needs a third stage for its load to overlap a whole step.
 constexpr int kDqKStages = 3;
+// Launched at 168 registers a thread; warps 0-3 drop to 72 and the softmax
+// warpgroups rise to 216 (128 x 72 + 256 x 216 = 384 x 168).
+constexpr uint32_t kDqRegsCtl = 72, kDqRegsSoftmax = 216;
+static_assert(128 * kDqRegsCtl + 256 * kDqRegsSoftmax <= 384 * 168, "register split");
 constexpr int kDqVStages = 2;
 constexpr uint32_t kDqOffQ = 0;
 constexpr uint32_t kDqOffDO = kTileBytes;
@@ -140,6 +144,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   __shared__ uint64_t bar_dp_full, bar_ds_full, bar_dq_full, bar_dq_free;
   __shared__ uint64_t bar_ke[2];
   __shared__ __align__(16) int ke_buf[2][128];
+  __shared__ int2 ke_mm[2][4];  // per 32 keys of ke_buf: min and max key_end
   __shared__ ItemRing ring;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
@@ -187,14 +192,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const uint32_t tS = tmem, tDP = tmem + 256, tDQ = tmem + 384;  // S_a at 0, S_b at 128
 
   if (warp == 0) {
+    regs_dec<kDqRegsCtl>();
     // ------------------------------------------------------------ producer
     uint32_t kv = 0, qn = 0, pub = 0;
-    int cur = item_fetch(p.sched, p.n_items), nxt = -1;  // items are taken one ahead
+    // The next item is taken once every load of this one is issued (taking
+    // it earlier can leave two long items on one CTA).
+    int cur = item_fetch(p.sched, p.n_items);
     bool ok = item_put(&ring, pub, cur, abort, p.status);
-    if (ok && cur >= 0) {
-      nxt = item_fetch(p.sched, p.n_items);
-      ok = item_put(&ring, pub, nxt, abort, p.status);
-    }
     while (ok && cur >= 0) {
       const int qt = p.order[cur / p.hq], h = cur % p.hq, kvh = h / p.group;
       if (qn > 0 && !(ok = warp_wait(&bar_q_empty, (qn - 1) & 1, abort, p.status))) break;
@@ -204,13 +208,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         tma_load_3d(smem + kDqOffQ + kHalfBytes, &map_q, &bar_q_full, 64, h, qt * 128);
         tma_load_3d(smem + kDqOffDO, &map_do, &bar_q_full, 0, h, qt * 128);
         tma_load_3d(smem + kDqOffDO + kHalfBytes, &map_do, &bar_q_full, 64, h, qt * 128);
-        if (nxt >= 0) {  // the next item's Q and dO into L2
-          const int nqt = p.order[nxt / p.hq], nh = nxt % p.hq;
-          tma_prefetch_l2_3d(&map_q, 0, nh, nqt * 128);
-          tma_prefetch_l2_3d(&map_q, 64, nh, nqt * 128);
-          tma_prefetch_l2_3d(&map_do, 0, nh, nqt * 128);
-          tma_prefetch_l2_3d(&map_do, 64, nh, nqt * 128);
-        }
       }
       __syncwarp();
       ++qn;
@@ -236,11 +233,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         __syncwarp();
       }
       if (!ok) break;
-      cur = nxt;
-      if (cur >= 0) {
-        nxt = item_fetch(p.sched, p.n_items);
-        ok = item_put(&ring, pub, nxt, abort, p.status);
+      cur = item_fetch(p.sched, p.n_items);
+      if (!(ok = item_put(&ring, pub, cur, abort, p.status))) break;
+      if (cur >= 0 && lane == 0) {  // its Q and dO into L2 while this item finishes
+        const int nqt = p.order[cur / p.hq], nh = cur % p.hq;
+        tma_prefetch_l2_3d(&map_q, 0, nh, nqt * 128);
+        tma_prefetch_l2_3d(&map_q, 64, nh, nqt * 128);
+        tma_prefetch_l2_3d(&map_do, 0, nh, nqt * 128);
+        tma_prefetch_l2_3d(&map_do, 64, nh, nqt * 128);
       }
+      __syncwarp();
     }
     if (!ok && lane == 0) {
       if (qn > 0) mbar_drain(&bar_q_full, (qn - 1) & 1);
@@ -250,6 +252,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       }
     }
   } else if (warp == 1) {
+    regs_dec<kDqRegsCtl>();
     // ---------------------------------------------------------- MMA issuer
     // Per item: S_0, dP_0, S_1; then per tile t: [dS_t] dQ += dS_t K_t,
     // dP_{t+1}, S_{t+2} (into the S buffer dQ_t just read).
@@ -317,7 +320,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
     mma_commit_warp(&bar_final);
     mbar_drain(&bar_final, 0);
-  } else if (warp >= 4) {
+  } else if (warp < 4) {
+    regs_dec<kDqRegsCtl>();  // warps 2-3: idle
+  } else {
+    regs_inc<kDqRegsSoftmax>();
     // ---- two warpgroups split each tile's 128 keys: warps 4-7 take keys
     // 0-63, warps 8-11 keys 64-127; one q row per thread (TMEM lane = row).
     // Each half writes its dS (bf16) over the first 32 columns of its own S
@@ -347,27 +353,31 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       nt_kev = j < p.N ? __ldg(p.key_end + j) : 0;
       nt_at = t;
     };
+    // The next item's number is read once this item's tiles are done (the
+    // producer publishes it when this item's loads are issued); its header
+    // loads overlap the wait for the last dQ product.
     uint32_t got = 0;
-    int nxt = -1;
-    ok = item_get(&ring, got, nxt, abort, p.status);
-    if (ok && nxt >= 0) fetch_header(nxt);
-    while (ok && nxt >= 0) {
-      const int qt = n_qt, h = nxt % p.hq, beg = n_beg, end = n_end;
-      if (!(ok = item_get(&ring, got, nxt, abort, p.status))) break;
-      if (nxt >= 0) fetch_header(nxt);
-      const int i = qt * 128 + r;
-      const size_t row = static_cast<size_t>(i) * p.hq + h;
-      // The next item's O row (for its Delta) is prefetched into L2.
-      {
-        if (nxt >= 0) {
-          const int ni = n_qt * 128 + r;
-          if (ni < p.N) {
-            const __nv_bfloat16* nrow = p.o + (static_cast<size_t>(ni) * p.hq + nxt % p.hq) * 128;
-            prefetch_l2(nrow);
-            prefetch_l2(nrow + 64);
-          }
+    int cur = -1;
+    ok = item_get(&ring, got, cur, abort, p.status);
+    if (ok && cur >= 0) fetch_header(cur);
+    auto next_item = [&](int& nxt) -> bool {
+      if (!item_get(&ring, got, nxt, abort, p.status)) return false;
+      if (nxt >= 0) {
+        fetch_header(nxt);
+        const int ni = n_qt * 128 + r;  // its O row (for its Delta) into L2
+        if (ni < p.N) {
+          const __nv_bfloat16* nrow = p.o + (static_cast<size_t>(ni) * p.hq + nxt % p.hq) * 128;
+          prefetch_l2(nrow);
+          prefetch_l2(nrow + 64);
         }
       }
+      return true;
+    };
+    while (ok && cur >= 0) {
+      const int qt = n_qt, h = cur % p.hq, beg = n_beg, end = n_end;
+      int nxt = -1;
+      const int i = qt * 128 + r;
+      const size_t row = static_cast<size_t>(i) * p.hq + h;
       if (!(ok = warp_wait(&bar_q_full, qn & 1, abort, p.status))) break;
       float delta = 0.f, lse2 = INFINITY;
       if (i < p.N) {
@@ -397,16 +407,34 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       if (nt_at != beg) fetch_tile(beg);
       for (int t = beg; t < end; ++t, ++n) {
         const int kd = nt_kind, kt = nt_kt, kev = nt_kev;
-        if (t + 1 < end)
-          fetch_tile(t + 1);
-        else if (nxt >= 0)
-          fetch_tile(n_beg);
+        if (t + 1 < end) fetch_tile(t + 1);
+        // What this warp's 32 rows x 64 keys of the tile hold: 1 every pair
+        // visible (no mask), 0 a mix (mask per element; the j <= i half only
+        // where some key follows a row), 2 no visible pair (P = dS = 0: no
+        // exponentials, no dP read).
+        int mode = kd == 2 ? 1 : 0;
+        bool diag = false;
         const int* ke = nullptr;
         if (kd == 1) {  // PARTIAL: the 128 key bounds of this tile, shared through smem
-          if (half == 0) ke_buf[kb][r] = kev;
+          if (half == 0) {
+            ke_buf[kb][r] = kev;
+            int mn = kev, mx = kev;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+              mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            }
+            if (lane == 0) ke_mm[kb][quarter] = make_int2(mn, mx);
+          }
           mbar_arrive(&bar_ke[kb]);
           if (!(ok = warp_wait(&bar_ke[kb], ku[kb] & 1, abort, p.status))) break;
           ++ku[kb];
+          const int2 a = ke_mm[kb][2 * half], b = ke_mm[kb][2 * half + 1];
+          const int kmin = min(a.x, b.x), kmax = max(a.y, b.y);
+          const int r0 = qt * 128 + quarter * 32, jlo = kt * 128 + col0;
+          // rows [r0, r0+32) see key j iff j <= row < key_end[j]
+          diag = jlo + 63 > r0;
+          mode = (kmax <= r0 || jlo > r0 + 31) ? 2 : (!diag && kmin > r0 + 31) ? 1 : 0;
           ke = ke_buf[kb] + col0;
           kb ^= 1;
         }
@@ -416,14 +444,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         ++su[sb];
         tc_fence_after_sync();
         float pv[64];
-        {
+        if (mode != 2) {
           uint32_t rr[64];
           tmem_ld64(tSb, rr);  // this half of the S row, one wait
 #pragma unroll
           for (int jj = 0; jj < 64; ++jj)
             pv[jj] = ex2_approx(fmaf(__uint_as_float(rr[jj]), sl2, -lse2));
         }
-        if (ke) {
+        if (mode == 0 && diag) {
           const int j0 = kt * 128 + col0;
 #pragma unroll
           for (int c4 = 0; c4 < 16; ++c4) {
@@ -434,10 +462,25 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             if (!(j + 2 <= i && i < b.z)) pv[4 * c4 + 2] = 0.f;
             if (!(j + 3 <= i && i < b.w)) pv[4 * c4 + 3] = 0.f;
           }
+        } else if (mode == 0) {  // every key of this half precedes every row of this warp
+#pragma unroll
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const int4 b = reinterpret_cast<const int4*>(ke)[c4];
+            if (!(i < b.x)) pv[4 * c4 + 0] = 0.f;
+            if (!(i < b.y)) pv[4 * c4 + 1] = 0.f;
+            if (!(i < b.z)) pv[4 * c4 + 2] = 0.f;
+            if (!(i < b.w)) pv[4 * c4 + 3] = 0.f;
+          }
         }
         if (!(ok = warp_wait(&bar_dp_full, n & 1, abort, p.status))) break;
         tc_fence_after_sync();
-        {
+        if (mode == 2) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) pk[jj] = 0u;
+          tmem_st16(tSb, pk);
+          tmem_st16(tSb + 16, pk);
+        } else {
           uint32_t rr[64];
           tmem_ld64(tDP + lane_off + col0, rr);  // this half of the dP row, one wait
 #pragma unroll
@@ -457,6 +500,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         mbar_arrive(&bar_ds_full);
       }
       if (!ok) break;
+      if (!(ok = next_item(nxt))) break;
       // epilogue: dq = scale * dQ, this half's 64 columns
       if (!(ok = warp_wait(&bar_dq_full, (qn - 1) & 1, abort, p.status))) break;
       tc_fence_after_sync();
@@ -468,6 +512,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       }
       tc_fence_before_sync();
       mbar_arrive(&bar_dq_free);
+      if (nxt >= 0) fetch_tile(n_beg);  // the next item's first tile
+      cur = nxt;
     }
   }
 
@@ -600,12 +646,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     uint32_t n = 0, items = 0, pub = 0;
-    int cur = item_fetch(p.sched, p.n_items), nxt = -1;  // items are taken one ahead
+    // The next item is taken once every load of this one is issued: items
+    // differ in length by two orders of magnitude, and taking one early can
+    // leave two long ones on one CTA while the others finish.
+    int cur = item_fetch(p.sched, p.n_items);
     bool ok = item_put(ring, pub, cur, abort, p.status);
-    if (ok && cur >= 0) {
-      nxt = item_fetch(p.sched, p.n_items);
-      ok = item_put(ring, pub, nxt, abort, p.status);
-    }
     while (ok && cur >= 0) {
       const KvItem x = decode_kv(p, cur);
       if (items > 0 && !(ok = warp_wait(bar_kv_empty, (items - 1) & 1, abort, p.status))) break;
@@ -616,18 +661,14 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tma_load_3d(smem + kKvOffK + kHalfBytes, &map_k, bar_kv_full, 64, x.kvh, row0);
         tma_load_3d(smem + kKvOffV, &map_v, bar_kv_full, 0, x.kvh, row0);
         tma_load_3d(smem + kKvOffV + kHalfBytes, &map_v, bar_kv_full, 64, x.kvh, row0);
-        if (nxt >= 0) {  // the next item's K and V into L2
-          const KvItem y = decode_kv(p, nxt);
-          tma_prefetch_l2_3d(&map_k, 0, y.kvh, y.kt * 128);
-          tma_prefetch_l2_3d(&map_k, 64, y.kvh, y.kt * 128);
-          tma_prefetch_l2_3d(&map_v, 0, y.kvh, y.kt * 128);
-          tma_prefetch_l2_3d(&map_v, 64, y.kvh, y.kt * 128);
-        }
       }
       __syncwarp();
       for (int j = 0; j < x.steps; ++j, ++n) {
-        const int h = x.kvh * p.group + j / x.nq;
-        const int qt = x.qlo + j % x.nq;
+        // q-tile major, the group's heads inner: the CTAs that share a key
+        // prefix walk the same q-tiles a fixed distance apart, so the Q and dO
+        // tiles they all read stay in L2 between them
+        const int qt = x.qlo + j / p.group;
+        const int h = x.kvh * p.group + j % p.group;
         const uint32_t sq = n % kKvQStages, pq = (n / kKvQStages) & 1;
         if (n >= kKvQStages && !(ok = warp_wait(bar_q_empty + sq, pq ^ 1, abort, p.status))) break;
         if (lane == 0) {
@@ -653,11 +694,16 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       }
       if (!ok) break;
       ++items;
-      cur = nxt;
-      if (cur >= 0) {
-        nxt = item_fetch(p.sched, p.n_items);
-        ok = item_put(ring, pub, nxt, abort, p.status);
+      cur = item_fetch(p.sched, p.n_items);
+      if (!(ok = item_put(ring, pub, cur, abort, p.status))) break;
+      if (cur >= 0 && lane == 0) {  // its K and V into L2 while this item finishes
+        const KvItem y = decode_kv(p, cur);
+        tma_prefetch_l2_3d(&map_k, 0, y.kvh, y.kt * 128);
+        tma_prefetch_l2_3d(&map_k, 64, y.kvh, y.kt * 128);
+        tma_prefetch_l2_3d(&map_v, 0, y.kvh, y.kt * 128);
+        tma_prefetch_l2_3d(&map_v, 64, y.kvh, y.kt * 128);
       }
+      __syncwarp();
     }
     if (!ok && lane == 0) {
       if (items > 0) mbar_drain(bar_kv_full, (items - 1) & 1);
@@ -744,7 +790,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       const int jk = x.kt * 128 + kr;
       const int ke = jk < p.N ? __ldg(p.key_end + jk) : 0;  // rows [jk, ke) see this key
       for (int j = 0; j < x.steps; ++j, ++n) {
-        const int q0 = (x.qlo + j % x.nq) * 128 + col0;  // first q column of this half
+        const int q0 = (x.qlo + j / p.group) * 128 + col0;  // first q column of this half
         const uint32_t sd = n % kKvDoStages, pd = (n / kKvDoStages) & 1;
         const float* lse2 = reinterpret_cast<const float*>(smem + kKvOffLse + sd * 512) + col0;
         const float* dlt = reinterpret_cast<const float*>(smem + kKvOffDelta + sd * 512) + col0;

@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_o_full[2], bar_o_free[2];
   __shared__ uint64_t bar_ke[2][2];
   __shared__ __align__(16) int ke_buf[2][2][128];
+  __shared__ int2 ke_mm[2][2][4];  // per 32 keys of ke_buf: min and max key_end
   __shared__ ItemRing ring;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
@@ -211,14 +212,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_dec<kRegsCtl>();
     // ------------------------------------------------------------ producer
     uint32_t kv = 0, qn = 0, pub = 0;
-    // Items are taken one ahead: the ring holds the next item's number while
-    // this one loads.
-    int cur = item_fetch(p.sched, p.n_items), nxt = -1;
+    // The next item is taken from the launch's counter once every load of
+    // this one is issued, a couple of tiles before the CTA is free: taking it
+    // earlier can leave two long items on one CTA while another sits idle.
+    int cur = item_fetch(p.sched, p.n_items);
     bool ok = item_put(&ring, pub, cur, abort, p.status);
-    if (ok && cur >= 0) {
-      nxt = item_fetch(p.sched, p.n_items);
-      ok = item_put(&ring, pub, nxt, abort, p.status);
-    }
     while (ok && cur >= 0) {
       const Item x = decode_item(p, cur);
       if (qn > 0 && !(ok = warp_wait(&bar_q_empty, (qn - 1) & 1, abort, p.status))) break;
@@ -230,14 +228,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sQ + s * kTileBytes, &map_q, &bar_q_full, 0, x.head[s], x.qtile[s] * 128);
           tma_load_3d(sQ + s * kTileBytes + kHalfBytes, &map_q, &bar_q_full, 64, x.head[s],
                       x.qtile[s] * 128);
-        }
-        if (nxt >= 0) {  // the next item's Q tiles into L2
-          const Item y = decode_item(p, nxt);
-          for (int s = 0; s < 2; ++s) {
-            if (y.qtile[s] >= p.Tq) continue;
-            tma_prefetch_l2_3d(&map_q, 0, y.head[s], y.qtile[s] * 128);
-            tma_prefetch_l2_3d(&map_q, 64, y.head[s], y.qtile[s] * 128);
-          }
         }
       }
       __syncwarp();
@@ -261,11 +251,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
       if (!ok) break;
-      cur = nxt;
-      if (cur >= 0) {
-        nxt = item_fetch(p.sched, p.n_items);
-        ok = item_put(&ring, pub, nxt, abort, p.status);
+      cur = item_fetch(p.sched, p.n_items);
+      if (!(ok = item_put(&ring, pub, cur, abort, p.status))) break;
+      if (cur >= 0 && lane == 0) {  // its Q tiles into L2 while this item finishes
+        const Item y = decode_item(p, cur);
+        for (int s = 0; s < 2; ++s) {
+          if (y.qtile[s] >= p.Tq) continue;
+          tma_prefetch_l2_3d(&map_q, 0, y.head[s], y.qtile[s] * 128);
+          tma_prefetch_l2_3d(&map_q, 64, y.head[s], y.qtile[s] * 128);
+        }
       }
+      __syncwarp();
     }
     if (!ok && lane == 0) {  // let copies in flight land before the CTA exits
       if (qn > 0) mbar_drain(&bar_q_full, (qn - 1) & 1);
@@ -374,39 +370,80 @@ __global__ void __launch_bounds__(kThreads, 1)
       n_beg = y.beg;
       n_end = y.end;
     };
+    // The next item's number is read once this item's tiles are done (the
+    // producer publishes it when this item's loads are issued); its header
+    // loads overlap the wait for the last PV.
     uint32_t got = 0;
-    int nxt = -1;
-    ok = item_get(&ring, got, nxt, abort, p.status);
-    if (ok && nxt >= 0) fetch_header(nxt);
+    int cur = -1;
+    ok = item_get(&ring, got, cur, abort, p.status);
+    if (ok && cur >= 0) fetch_header(cur);
     TileInfo nt;
     int nt_at = -1;
-    while (ok && nxt >= 0) {
+    while (ok && cur >= 0) {
       const int qt = n_qt, h = n_h, beg = n_beg, end = n_end;
-      if (!(ok = item_get(&ring, got, nxt, abort, p.status))) break;
-      if (nxt >= 0) fetch_header(nxt);
-      if (qt >= p.Tq) continue;
+      int nxt = -1;
+      if (qt >= p.Tq) {  // this slot has no rows in the item
+        if ((ok = item_get(&ring, got, nxt, abort, p.status)) && nxt >= 0) fetch_header(nxt);
+        cur = nxt;
+        continue;
+      }
       const int i = qt * 128 + r;
       float m_ref = -INFINITY, l = 0.f;
       if (nt_at != beg) nt = load_tile(p, beg, s, r);
       for (int t = beg; t < end; ++t) {
-        const TileInfo cur = nt;
-        nt_at = t + 1 < end ? t + 1 : (nxt >= 0 ? n_beg : -1);
-        if (nt_at >= 0) nt = load_tile(p, nt_at, s, r);
-        const int kd = cur.kind;
+        const TileInfo tl = nt;
+        if (t + 1 < end) {
+          nt_at = t + 1;
+          nt = load_tile(p, nt_at, s, r);
+        }
+        const int kd = tl.kind;
         if (kd == 0) continue;
-        const int kt = cur.kt;
+        const int kt = tl.kt;
+        // What this warp's 32 rows of the tile hold: 1 every pair visible (no
+        // mask), 0 a mix (mask per element; the j <= i half only where some
+        // key follows a row), 2 no visible pair (P = 0, no exponentials).
+        int mode = kd == 2 ? 1 : 0;
+        bool diag = false;
         const int* ke = nullptr;
         if (kd == 1) {  // PARTIAL: the 128 key bounds of this tile, shared through smem
-          ke_buf[s][kb][r] = cur.kev;
+          ke_buf[s][kb][r] = tl.kev;
+          int mn = tl.kev, mx = tl.kev;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          }
+          if (lane == 0) ke_mm[s][kb][quarter] = make_int2(mn, mx);
           mbar_arrive(&bar_ke[s][kb]);
           if (!(ok = warp_wait(&bar_ke[s][kb], ku[kb] & 1, abort, p.status))) break;
           ++ku[kb];
+          int kmin = ke_mm[s][kb][0].x, kmax = ke_mm[s][kb][0].y;
+#pragma unroll
+          for (int w4 = 1; w4 < 4; ++w4) {
+            kmin = min(kmin, ke_mm[s][kb][w4].x);
+            kmax = max(kmax, ke_mm[s][kb][w4].y);
+          }
+          const int r0 = qt * 128 + quarter * 32, jlo = kt * 128;
+          // rows [r0, r0+32) see key j iff j <= row < key_end[j]
+          diag = jlo + 127 > r0;
+          mode = (kmax <= r0 || jlo > r0 + 31) ? 2 : (!diag && kmin > r0 + 31) ? 1 : 0;
           ke = ke_buf[s][kb];
           kb ^= 1;
         }
         if (!(ok = warp_wait(&bar_s_full[s], sc & 1, abort, p.status))) break;
         ++sc;
         tc_fence_after_sync();
+        if (mode == 2) {  // P = 0; m and l of the row are unchanged
+          uint32_t pk[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) pk[jj] = 0u;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_st16(tS + c * 16, pk);
+          tmem_wait_st();
+          tc_fence_before_sync();
+          mbar_arrive(&bar_p_full[s]);
+          continue;
+        }
         float sv[128];
         {
           uint32_t rr[128];
@@ -414,16 +451,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < 128; ++jj) sv[jj] = __uint_as_float(rr[jj]);
         }
-        if (ke) {
+        if (mode == 0) {
           const int j0 = kt * 128;
+          if (diag) {
 #pragma unroll
-          for (int c4 = 0; c4 < 32; ++c4) {
-            const int4 b = reinterpret_cast<const int4*>(ke)[c4];
-            const int j = j0 + 4 * c4;
-            if (!(j + 0 <= i && i < b.x)) sv[4 * c4 + 0] = -INFINITY;
-            if (!(j + 1 <= i && i < b.y)) sv[4 * c4 + 1] = -INFINITY;
-            if (!(j + 2 <= i && i < b.z)) sv[4 * c4 + 2] = -INFINITY;
-            if (!(j + 3 <= i && i < b.w)) sv[4 * c4 + 3] = -INFINITY;
+            for (int c4 = 0; c4 < 32; ++c4) {
+              const int4 b = reinterpret_cast<const int4*>(ke)[c4];
+              const int j = j0 + 4 * c4;
+              if (!(j + 0 <= i && i < b.x)) sv[4 * c4 + 0] = -INFINITY;
+              if (!(j + 1 <= i && i < b.y)) sv[4 * c4 + 1] = -INFINITY;
+              if (!(j + 2 <= i && i < b.z)) sv[4 * c4 + 2] = -INFINITY;
+              if (!(j + 3 <= i && i < b.w)) sv[4 * c4 + 3] = -INFINITY;
+            }
+          } else {  // every key of the tile precedes every row of this warp
+#pragma unroll
+            for (int c4 = 0; c4 < 32; ++c4) {
+              const int4 b = reinterpret_cast<const int4*>(ke)[c4];
+              if (!(i < b.x)) sv[4 * c4 + 0] = -INFINITY;
+              if (!(i < b.y)) sv[4 * c4 + 1] = -INFINITY;
+              if (!(i < b.z)) sv[4 * c4 + 2] = -INFINITY;
+              if (!(i < b.w)) sv[4 * c4 + 3] = -INFINITY;
+            }
           }
         }
         // row max as 8 independent chains, then a tree (short dependency chains)
@@ -479,6 +527,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bar_p_full[s]);
       }
       if (!ok) break;
+      if (!(ok = item_get(&ring, got, nxt, abort, p.status))) break;
+      if (nxt >= 0) fetch_header(nxt);
       // ---- epilogue: O / l and lse
       if (!(ok = warp_wait(&bar_o_full[s], oc & 1, abort, p.status))) break;
       ++oc;
@@ -505,6 +555,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
       tc_fence_before_sync();
       mbar_arrive(&bar_o_free[s]);
+      if (nxt >= 0) {  // the next item's first tile
+        nt_at = n_beg;
+        nt = load_tile(p, nt_at, s, r);
+      }
+      cur = nxt;
     }
   }
 
