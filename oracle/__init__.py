@@ -24,7 +24,8 @@ Modules:
 Parity pins: every function here is pinned by a ``-m "not gpu"`` test in
 ``tests/test_oracle_*.py`` against the pages' worked numbers, closed forms,
 library routines (torch SDPA, autograd, gradcheck) or brute force. The tile
-work orders (``tiles.lpt_order``) and the q-tile pair lists are scheduling
-conventions of this library, not of the pages; they are pinned only by
-invariants (permutation, ordering, union) -- parity unpinned by the pages.
+work orders (``fwd_order``, ``bwd_order``, ``qp_order`` in ``tiles.plan_fields``)
+and the q-tile pair lists are scheduling conventions of this library, not of
+the pages; they are pinned only by invariants (permutation, ordering, union)
+-- parity unpinned by the pages.
 """
