@@ -109,7 +109,14 @@ constexpr uint32_t kDqOffQ = 0;
 constexpr uint32_t kDqOffDO = kTileBytes;
 constexpr uint32_t kDqOffK = 2 * kTileBytes;
 constexpr uint32_t kDqOffV = kDqOffK + kDqKStages * kTileBytes;
-constexpr uint32_t kDqSmem = 1024 + kDqOffV + kDqVStages * kTileBytes;
+constexpr uint32_t kDqOffKe = kDqOffV + kDqVStages * kTileBytes;  // per K stage: 128 key_end
+// mbarriers, then the item ring, then the TMEM base and the abort flag
+constexpr uint32_t kDqOffBar = kDqOffKe + kDqKStages * 512;
+constexpr uint32_t kDqNumBars = 3 + 2 * kDqKStages + 2 * kDqVStages + 2 + 4;
+constexpr uint32_t kDqOffRing = kDqOffBar + kDqNumBars * 8;
+constexpr uint32_t kDqOffMisc = kDqOffRing + sizeof(ItemRing);
+constexpr uint32_t kDqSmem = kDqOffMisc + 16;
+static_assert(kDqSmem <= 232448, "shared memory budget");
 
 struct DqParams {
   const int32_t* key_end;
@@ -133,21 +140,36 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                            const __grid_constant__ CUtensorMap map_k,
                            const __grid_constant__ CUtensorMap map_v,
                            const __grid_constant__ CUtensorMap map_do, const DqParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t bar_q_full, bar_q_empty, bar_final;
-  __shared__ uint64_t bar_k_full[kDqKStages], bar_k_empty[kDqKStages];
-  __shared__ uint64_t bar_v_full[kDqVStages], bar_v_empty[kDqVStages];
-  __shared__ uint64_t bar_s_full[2];  // one per S buffer: a buffer is refilled only after
-                                     // its dS was consumed, so each barrier is at most one phase ahead
-  __shared__ uint64_t bar_dp_full, bar_ds_full, bar_dq_full, bar_dq_free;
-  __shared__ uint64_t bar_ke[2];
-  __shared__ __align__(16) int ke_buf[2][128];
-  __shared__ int2 ke_mm[2][4];  // per 32 keys of ke_buf: min and max key_end
-  __shared__ ItemRing ring;
-  __shared__ uint32_t tmem_base_s;
-  __shared__ int abort_s;
+  // All shared state sits in the dynamic block (no static shared memory), so
+  // the block starts 1024-aligned as the 128B-swizzled tiles need.
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) atomicExch(p.status, 9);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDqOffBar);
+  uint64_t& bar_q_full = bars[0];
+  uint64_t& bar_q_empty = bars[1];
+  uint64_t& bar_final = bars[2];
+  uint64_t (&bar_k_full)[kDqKStages] = *reinterpret_cast<uint64_t(*)[kDqKStages]>(bars + 3);
+  uint64_t (&bar_k_empty)[kDqKStages] =
+      *reinterpret_cast<uint64_t(*)[kDqKStages]>(bars + 3 + kDqKStages);
+  uint64_t (&bar_v_full)[kDqVStages] =
+      *reinterpret_cast<uint64_t(*)[kDqVStages]>(bars + 3 + 2 * kDqKStages);
+  uint64_t (&bar_v_empty)[kDqVStages] =
+      *reinterpret_cast<uint64_t(*)[kDqVStages]>(bars + 3 + 2 * kDqKStages + kDqVStages);
+  // one per S buffer: a buffer is refilled only after its dS was consumed, so
+  // each barrier is at most one phase ahead
+  uint64_t (&bar_s_full)[2] =
+      *reinterpret_cast<uint64_t(*)[2]>(bars + 3 + 2 * kDqKStages + 2 * kDqVStages);
+  uint64_t* tail = bars + 5 + 2 * kDqKStages + 2 * kDqVStages;
+  uint64_t& bar_dp_full = tail[0];
+  uint64_t& bar_ds_full = tail[1];
+  uint64_t& bar_dq_full = tail[2];
+  uint64_t& bar_dq_free = tail[3];
+  ItemRing& ring = *reinterpret_cast<ItemRing*>(smem + kDqOffRing);
+  uint32_t& tmem_base_s = *reinterpret_cast<uint32_t*>(smem + kDqOffMisc);
+  int& abort_s = *reinterpret_cast<int*>(smem + kDqOffMisc + 4);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   volatile int* abort = &abort_s;
@@ -170,8 +192,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&bar_ds_full, 256);
     mbar_init(&bar_dq_full, 1);
     mbar_init(&bar_dq_free, 256);
-    mbar_init(&bar_ke[0], 256);
-    mbar_init(&bar_ke[1], 256);
     abort_s = 0;
     fence_mbar_init();
   }
@@ -217,9 +237,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (kv >= kDqKStages && !(ok = warp_wait(&bar_k_empty[sk], pk ^ 1, abort, p.status))) break;
         if (lane == 0) {
           uint8_t* dst = smem + kDqOffK + sk * kTileBytes;
-          mbar_arrive_expect_tx(&bar_k_full[sk], kTileBytes);
+          // the tile's 128 key bounds travel with it (key_end is padded to
+          // whole tiles on the device)
+          mbar_arrive_expect_tx(&bar_k_full[sk], kTileBytes + 512);
           tma_load_3d(dst, &map_k, &bar_k_full[sk], 0, kvh, row0);
           tma_load_3d(dst + kHalfBytes, &map_k, &bar_k_full[sk], 64, kvh, row0);
+          bulk_load(smem + kDqOffKe + sk * 512, p.key_end + row0, 512, &bar_k_full[sk]);
         }
         __syncwarp();
         const uint32_t sv = kv % kDqVStages, pv = (kv / kDqVStages) & 1;
@@ -334,23 +357,21 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t col0 = half * 64;
     const float sl2 = p.scale_log2;
-    uint32_t n = 0, qn = 0, kb = 0, ku[2] = {0, 0}, su[2] = {0, 0};
+    uint32_t n = 0, qn = 0, su[2] = {0, 0};
     bool ok = true;
     // The next item's q-tile and tile range are read one item ahead, and each
-    // tile's kind, k-tile and key_end entry one tile ahead, so no global load
-    // latency sits between two passes over S.
+    // tile's kind and k-tile one tile ahead, so no global load latency sits
+    // between two passes over S. A tile's key bounds come with its K stage.
     int n_qt = 0, n_beg = 0, n_end = 0;
     auto fetch_header = [&](int at) {
       n_qt = __ldg(p.order + at / p.hq);
       n_beg = __ldg(p.qt_ptr + n_qt);
       n_end = __ldg(p.qt_ptr + n_qt + 1);
     };
-    int nt_kind = 0, nt_kt = 0, nt_kev = 0, nt_at = -1;
+    int nt_kind = 0, nt_kt = 0, nt_at = -1;
     auto fetch_tile = [&](int t) {
       nt_kind = __ldg(p.qt_kind + t);
       nt_kt = __ldg(p.qt_kt + t);
-      const int j = nt_kt * 128 + r;
-      nt_kev = j < p.N ? __ldg(p.key_end + j) : 0;
       nt_at = t;
     };
     // The next item's number is read once this item's tiles are done (the
@@ -406,7 +427,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       ++qn;
       if (nt_at != beg) fetch_tile(beg);
       for (int t = beg; t < end; ++t, ++n) {
-        const int kd = nt_kind, kt = nt_kt, kev = nt_kev;
+        const int kd = nt_kind, kt = nt_kt;
         if (t + 1 < end) fetch_tile(t + 1);
         // What this warp's 32 rows x 64 keys of the tile hold: 1 every pair
         // visible (no mask), 0 a mix (mask per element; the j <= i half only
@@ -415,28 +436,22 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         int mode = kd == 2 ? 1 : 0;
         bool diag = false;
         const int* ke = nullptr;
-        if (kd == 1) {  // PARTIAL: the 128 key bounds of this tile, shared through smem
-          if (half == 0) {
-            ke_buf[kb][r] = kev;
-            int mn = kev, mx = kev;
+        if (kd == 1) {  // PARTIAL: the tile's key bounds arrived with its K stage
+          // (the stage is refilled only after this tile's dQ product, which
+          // waits for every softmax thread's dS)
+          if (!(ok = warp_wait(&bar_k_full[n % kDqKStages], (n / kDqKStages) & 1, abort, p.status)))
+            break;
+          ke = reinterpret_cast<const int*>(smem + kDqOffKe + (n % kDqKStages) * 512) + col0;
+          int mn = min(ke[lane], ke[lane + 32]), mx = max(ke[lane], ke[lane + 32]);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-              mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-              mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            }
-            if (lane == 0) ke_mm[kb][quarter] = make_int2(mn, mx);
+          for (int o = 16; o > 0; o >>= 1) {
+            mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
           }
-          mbar_arrive(&bar_ke[kb]);
-          if (!(ok = warp_wait(&bar_ke[kb], ku[kb] & 1, abort, p.status))) break;
-          ++ku[kb];
-          const int2 a = ke_mm[kb][2 * half], b = ke_mm[kb][2 * half + 1];
-          const int kmin = min(a.x, b.x), kmax = max(a.y, b.y);
           const int r0 = qt * 128 + quarter * 32, jlo = kt * 128 + col0;
           // rows [r0, r0+32) see key j iff j <= row < key_end[j]
           diag = jlo + 63 > r0;
-          mode = (kmax <= r0 || jlo > r0 + 31) ? 2 : (!diag && kmin > r0 + 31) ? 1 : 0;
-          ke = ke_buf[kb] + col0;
-          kb ^= 1;
+          mode = (mx <= r0 || jlo > r0 + 31) ? 2 : (!diag && mn > r0 + 31) ? 1 : 0;
         }
         const int sb = (t - beg) & 1;
         const uint32_t tSb = tS + lane_off + sb * 128 + col0;

@@ -111,11 +111,19 @@ extern "C" tree_status_t tree_plan_to_device(tree_plan_t* p, tree_stream_t strea
       {TREE_FIELD_QP_ORDER, &d.qp_order},   {TREE_FIELD_KT_QLO, &d.kt_qlo},
       {TREE_FIELD_KT_QHI, &d.kt_qhi},       {TREE_FIELD_BWD_ORDER, &d.bwd_order},
   };
+  // key_end is padded with zeros to whole 128-key tiles: the kernels copy it
+  // a tile at a time, and a zero bound hides the keys past N from every row.
+  auto slot_elems = [&](size_t s) {
+    const size_t n = p->field[slots[s].f].size();
+    if (slots[s].f != TREE_FIELD_KEY_END) return n;
+    const size_t padded = static_cast<size_t>(p->Tk) * kBlockM;
+    return n > padded ? n : padded;
+  };
   size_t offs[sizeof(slots) / sizeof(slots[0])];
   size_t total = 0;
   for (size_t s = 0; s < sizeof(slots) / sizeof(slots[0]); ++s) {
     offs[s] = total;
-    total += (p->field[slots[s].f].size() * 4 + 255) / 256 * 256;
+    total += (slot_elems(s) * 4 + 255) / 256 * 256;
   }
   std::vector<uint8_t> host(total, 0);
   for (size_t s = 0; s < sizeof(slots) / sizeof(slots[0]); ++s) {

@@ -100,17 +100,19 @@ __device__ __forceinline__ int kinds_at(const FwdParams& p, int t) {
 }
 
 // One tile of a slot's list as the softmax warps need it: its kind, its k-tile
-// and this thread's entry of key_end for that k-tile (key kt*128 + r).
+// and the tile's 128 key bounds, four per lane (keys kt*128 + lane + 32c;
+// key_end is zero-padded to whole tiles on the device).
 struct TileInfo {
-  int kind, kt, kev;
+  int kind, kt;
+  int kev[4];
 };
 
-__device__ __forceinline__ TileInfo load_tile(const FwdParams& p, int t, int s, int r) {
+__device__ __forceinline__ TileInfo load_tile(const FwdParams& p, int t, int s, int lane) {
   TileInfo x;
   x.kind = (kinds_at(p, t) >> (2 * s)) & 3;
   x.kt = __ldg(p.list_kt + t);
-  const int j = x.kt * 128 + r;
-  x.kev = j < p.N ? __ldg(p.key_end + j) : 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) x.kev[c] = __ldg(p.key_end + x.kt * 128 + lane + 32 * c);
   return x;
 }
 
@@ -158,9 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t bar_k_full[kStages], bar_k_empty[kStages];
   __shared__ uint64_t bar_v_full[kStages], bar_v_empty[kStages];
   __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_o_full[2], bar_o_free[2];
-  __shared__ uint64_t bar_ke[2][2];
-  __shared__ __align__(16) int ke_buf[2][2][128];
-  __shared__ int2 ke_mm[2][2][4];  // per 32 keys of ke_buf: min and max key_end
+  __shared__ __align__(16) int ke_w[8][128];  // each softmax warp's copy of a tile's key bounds
   __shared__ ItemRing ring;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
@@ -184,8 +184,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_p_full[s], 128);
       mbar_init(&bar_o_full[s], 1);
       mbar_init(&bar_o_free[s], 128);
-      mbar_init(&bar_ke[s][0], 128);
-      mbar_init(&bar_ke[s][1], 128);
     }
     abort_s = 0;
     fence_mbar_init();
@@ -357,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off + s * 128;
     const uint32_t tO = tmem + lane_off + 256 + s * 128;
     const float sl2 = p.scale_log2;
-    uint32_t sc = 0, oc = 0, kb = 0, ku[2] = {0, 0};
+    uint32_t sc = 0, oc = 0;
     bool ok = true;
     // The tile after the current one (in this item, else the next item's
     // first) is loaded one tile ahead, and the next item's header one item
@@ -389,12 +387,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int i = qt * 128 + r;
       float m_ref = -INFINITY, l = 0.f;
-      if (nt_at != beg) nt = load_tile(p, beg, s, r);
+      if (nt_at != beg) nt = load_tile(p, beg, s, lane);
       for (int t = beg; t < end; ++t) {
         const TileInfo tl = nt;
         if (t + 1 < end) {
           nt_at = t + 1;
-          nt = load_tile(p, nt_at, s, r);
+          nt = load_tile(p, nt_at, s, lane);
         }
         const int kd = tl.kind;
         if (kd == 0) continue;
@@ -405,30 +403,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         int mode = kd == 2 ? 1 : 0;
         bool diag = false;
         const int* ke = nullptr;
-        if (kd == 1) {  // PARTIAL: the 128 key bounds of this tile, shared through smem
-          ke_buf[s][kb][r] = tl.kev;
-          int mn = tl.kev, mx = tl.kev;
+        if (kd == 1) {  // PARTIAL: the warp's own copy of the tile's key bounds
+          int* kw = ke_w[warp - 4];
+          __syncwarp();  // every lane is done with the previous tile's copy
+#pragma unroll
+          for (int c = 0; c < 4; ++c) kw[lane + 32 * c] = tl.kev[c];
+          __syncwarp();
+          ke = kw;
+          int mn = min(min(tl.kev[0], tl.kev[1]), min(tl.kev[2], tl.kev[3]));
+          int mx = max(max(tl.kev[0], tl.kev[1]), max(tl.kev[2], tl.kev[3]));
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) {
             mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
             mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
           }
-          if (lane == 0) ke_mm[s][kb][quarter] = make_int2(mn, mx);
-          mbar_arrive(&bar_ke[s][kb]);
-          if (!(ok = warp_wait(&bar_ke[s][kb], ku[kb] & 1, abort, p.status))) break;
-          ++ku[kb];
-          int kmin = ke_mm[s][kb][0].x, kmax = ke_mm[s][kb][0].y;
-#pragma unroll
-          for (int w4 = 1; w4 < 4; ++w4) {
-            kmin = min(kmin, ke_mm[s][kb][w4].x);
-            kmax = max(kmax, ke_mm[s][kb][w4].y);
-          }
           const int r0 = qt * 128 + quarter * 32, jlo = kt * 128;
           // rows [r0, r0+32) see key j iff j <= row < key_end[j]
           diag = jlo + 127 > r0;
-          mode = (kmax <= r0 || jlo > r0 + 31) ? 2 : (!diag && kmin > r0 + 31) ? 1 : 0;
-          ke = ke_buf[s][kb];
-          kb ^= 1;
+          mode = (mx <= r0 || jlo > r0 + 31) ? 2 : (!diag && mn > r0 + 31) ? 1 : 0;
         }
         if (!(ok = warp_wait(&bar_s_full[s], sc & 1, abort, p.status))) break;
         ++sc;
@@ -557,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bar_o_free[s]);
       if (nxt >= 0) {  // the next item's first tile
         nt_at = n_beg;
-        nt = load_tile(p, nt_at, s, r);
+        nt = load_tile(p, nt_at, s, lane);
       }
       cur = nxt;
     }
