@@ -217,10 +217,22 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     uint32_t kv = 0, qn = 0, pub = 0;
     // The next item is taken once every load of this one is issued (taking
     // it earlier can leave two long items on one CTA).
-    int cur = item_fetch(p.sched, p.n_items);
-    bool ok = item_put(&ring, pub, cur, abort, p.status);
+    // Items are published with their header (q-tile, tile range) so the
+    // other roles need no global loads to start one.
+    int nqt = 0, nbeg = 0, nend = 0;
+    auto take = [&]() {
+      const int id = item_fetch(p.sched, p.n_items);
+      if (id >= 0) {
+        nqt = __ldg(p.order + id / p.hq);
+        nbeg = __ldg(p.qt_ptr + nqt);
+        nend = __ldg(p.qt_ptr + nqt + 1);
+      }
+      return id;
+    };
+    int cur = take();
+    bool ok = item_put(&ring, pub, cur, abort, p.status, nqt, nbeg, nend);
     while (ok && cur >= 0) {
-      const int qt = p.order[cur / p.hq], h = cur % p.hq, kvh = h / p.group;
+      const int qt = nqt, h = cur % p.hq, kvh = h / p.group, beg = nbeg, end = nend;
       if (qn > 0 && !(ok = warp_wait(&bar_q_empty, (qn - 1) & 1, abort, p.status))) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bar_q_full, 2 * kTileBytes);
@@ -231,7 +243,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       }
       __syncwarp();
       ++qn;
-      for (int t = p.qt_ptr[qt]; t < p.qt_ptr[qt + 1]; ++t, ++kv) {
+      for (int t = beg; t < end; ++t, ++kv) {
         const int row0 = p.qt_kt[t] * 128;
         const uint32_t sk = kv % kDqKStages, pk = (kv / kDqKStages) & 1;
         if (kv >= kDqKStages && !(ok = warp_wait(&bar_k_empty[sk], pk ^ 1, abort, p.status))) break;
@@ -256,10 +268,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         __syncwarp();
       }
       if (!ok) break;
-      cur = item_fetch(p.sched, p.n_items);
-      if (!(ok = item_put(&ring, pub, cur, abort, p.status))) break;
+      cur = take();
+      if (!(ok = item_put(&ring, pub, cur, abort, p.status, nqt, nbeg, nend))) break;
       if (cur >= 0 && lane == 0) {  // its Q and dO into L2 while this item finishes
-        const int nqt = p.order[cur / p.hq], nh = cur % p.hq;
+        const int nh = cur % p.hq;
         tma_prefetch_l2_3d(&map_q, 0, nh, nqt * 128);
         tma_prefetch_l2_3d(&map_q, 64, nh, nqt * 128);
         tma_prefetch_l2_3d(&map_do, 0, nh, nqt * 128);
@@ -283,9 +295,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const uint32_t aK = smem_u32(smem + kDqOffK), aV = smem_u32(smem + kDqOffV);
     uint32_t kv = 0, qn = 0, n = 0, got = 0;
     bool ok = true;
-    for (int cur; (ok = item_get(&ring, got, cur, abort, p.status)) && cur >= 0;) {
-      const int qt = p.order[cur / p.hq];
-      const int T = p.qt_ptr[qt + 1] - p.qt_ptr[qt];
+    int hdr[3];
+    for (int cur; (ok = item_get(&ring, got, cur, abort, p.status, hdr)) && cur >= 0;) {
+      const int T = hdr[2] - hdr[1];
       if (!(ok = warp_wait(&bar_q_full, qn & 1, abort, p.status))) break;
       ++qn;
       auto k_stage = [&](uint32_t i) { return aK + (i % kDqKStages) * kTileBytes; };
@@ -362,12 +374,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     // The next item's q-tile and tile range are read one item ahead, and each
     // tile's kind and k-tile one tile ahead, so no global load latency sits
     // between two passes over S. A tile's key bounds come with its K stage.
-    int n_qt = 0, n_beg = 0, n_end = 0;
-    auto fetch_header = [&](int at) {
-      n_qt = __ldg(p.order + at / p.hq);
-      n_beg = __ldg(p.qt_ptr + n_qt);
-      n_end = __ldg(p.qt_ptr + n_qt + 1);
-    };
+    int hdr[3] = {0, 0, 0};  // the next item's q-tile and tile range, from the ring
     int nt_kind = 0, nt_kt = 0, nt_at = -1;
     auto fetch_tile = [&](int t) {
       nt_kind = __ldg(p.qt_kind + t);
@@ -379,46 +386,72 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     // loads overlap the wait for the last dQ product.
     uint32_t got = 0;
     int cur = -1;
-    ok = item_get(&ring, got, cur, abort, p.status);
-    if (ok && cur >= 0) fetch_header(cur);
+    ok = item_get(&ring, got, cur, abort, p.status, hdr);
+    // The loads an item's Delta needs are issued as soon as the item is known
+    // (right after the previous item's last tile), so their latency passes
+    // during the previous epilogue: this warp's 32 O rows, a row per
+    // instruction (lane l: dims 4l..4l+3, one contiguous 256-byte row; rows
+    // past N read the last row and count zero), and the thread's lse.
+    uint2 ov[32];
+    float lse_pre = INFINITY;
+    auto load_o = [&](int item) {
+      const int r0 = hdr[0] * 128 + quarter * 32, hh = item % p.hq;
+      const int nvalid = min(32, p.N - r0);
+      const __nv_bfloat16* obase = p.o + (static_cast<size_t>(r0) * p.hq + hh) * 128 + 4 * lane;
+      const size_t ostride = static_cast<size_t>(p.hq) * 128;
+#pragma unroll
+      for (int rr = 0; rr < 32; ++rr)
+        ov[rr] = nvalid > 0 ? __ldg(reinterpret_cast<const uint2*>(obase + min(rr, nvalid - 1) * ostride))
+                            : make_uint2(0u, 0u);
+      const int ii = hdr[0] * 128 + r;
+      lse_pre = ii < p.N ? __ldg(p.lse + static_cast<size_t>(hh) * p.N + ii) : INFINITY;
+    };
+    if (ok && cur >= 0) load_o(cur);
     auto next_item = [&](int& nxt) -> bool {
-      if (!item_get(&ring, got, nxt, abort, p.status)) return false;
-      if (nxt >= 0) {
-        fetch_header(nxt);
-        const int ni = n_qt * 128 + r;  // its O row (for its Delta) into L2
-        if (ni < p.N) {
-          const __nv_bfloat16* nrow = p.o + (static_cast<size_t>(ni) * p.hq + nxt % p.hq) * 128;
-          prefetch_l2(nrow);
-          prefetch_l2(nrow + 64);
-        }
-      }
+      if (!item_get(&ring, got, nxt, abort, p.status, hdr)) return false;
+      if (nxt >= 0) load_o(nxt);
       return true;
     };
     while (ok && cur >= 0) {
-      const int qt = n_qt, h = cur % p.hq, beg = n_beg, end = n_end;
+      const int qt = hdr[0], h = cur % p.hq, beg = hdr[1], end = hdr[2];
       int nxt = -1;
       const int i = qt * 128 + r;
       const size_t row = static_cast<size_t>(i) * p.hq + h;
       if (!(ok = warp_wait(&bar_q_full, qn & 1, abort, p.status))) break;
+      // Delta = dO . O of this thread's row: each lane's part of the warp's
+      // 32 dot products (its 4 dims of O, loaded ahead, and of dO in smem),
+      // then a transposing reduction leaves row r0 + l's sum in lane l.
       float delta = 0.f, lse2 = INFINITY;
-      if (i < p.N) {
-        const uint4* orow = reinterpret_cast<const uint4*>(p.o + row * 128);
+      {
+        float part[32];
+        const int r0 = qt * 128 + quarter * 32;
+        const uint8_t* dbase = smem + kDqOffDO + (lane >> 4) * kHalfBytes + (lane & 1) * 8;
+        const int chunk = (lane >> 1) & 7;
+        const int nvalid = min(32, p.N - r0);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint4 ov = __ldg(orow + c);
-          const uint4 dv = *reinterpret_cast<const uint4*>(
-              smem + kDqOffDO + (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) * 16));
-          const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-          const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+        for (int rr = 0; rr < 32; ++rr) {
+          const int rt = quarter * 32 + rr;  // row within the tile
+          const uint2 dv = *reinterpret_cast<const uint2*>(dbase + rt * 128 + ((chunk ^ (rt & 7)) * 16));
+          const float2 o01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov[rr].x));
+          const float2 o23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov[rr].y));
+          const float2 d01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dv.x));
+          const float2 d23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dv.y));
+          const float acc = fmaf(o01.x, d01.x, fmaf(o01.y, d01.y, fmaf(o23.x, d23.x, o23.y * d23.y)));
+          part[rr] = rr < nvalid ? acc : 0.f;
+        }
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float2 fa = __bfloat1622float2(o2[u]);
-            const float2 fb = __bfloat1622float2(d2[u]);
-            delta = fmaf(fa.x, fb.x, delta);
-            delta = fmaf(fa.y, fb.y, delta);
+        for (int st = 0; st < 5; ++st) {
+          const int k = 16 >> st;  // lanes with bit k keep the upper half of the rows
+          const bool up = (lane & k) != 0;
+#pragma unroll
+          for (int j = 0; j < (16 >> st); ++j) {
+            const float send = up ? part[j] : part[j + (16 >> st)];
+            const float keep = up ? part[j + (16 >> st)] : part[j];
+            part[j] = keep + __shfl_xor_sync(0xffffffffu, send, k);
           }
         }
-        lse2 = p.lse[static_cast<size_t>(h) * p.N + i] * kLog2e;
+        delta = part[0];
+        lse2 = lse_pre * kLog2e;
       }
       if (half == 0) {
         p.delta[static_cast<size_t>(h) * p.Npad + i] = delta;
@@ -527,7 +560,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       }
       tc_fence_before_sync();
       mbar_arrive(&bar_dq_free);
-      if (nxt >= 0) fetch_tile(n_beg);  // the next item's first tile
+      if (nxt >= 0) fetch_tile(hdr[1]);  // the next item's first tile
       cur = nxt;
     }
   }

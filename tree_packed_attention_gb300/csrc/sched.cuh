@@ -32,6 +32,7 @@ constexpr uint32_t kItemRing = 8;
 
 struct ItemRing {
   int id[kItemRing];
+  int info[kItemRing][3];     // the item's header as the producer decoded it
   uint64_t full[kItemRing];   // one arrival: the producer wrote the entry
   uint64_t empty[kItemRing];  // one arrival per consumer warp: every consumer read it
 };
@@ -52,15 +53,19 @@ __device__ __forceinline__ int item_fetch(SchedSlot* s, int n_items) {
   return v < n_items ? v : -1;
 }
 
-// Producer warp (warp-collective): publish this CTA's n-th item number.
+// Producer warp (warp-collective): publish this CTA's n-th item number and
+// (optionally) three ints of its decoded header.
 __device__ __forceinline__ bool item_put(ItemRing* r, uint32_t& n, int id, volatile int* abort,
-                                         int* status) {
+                                         int* status, int a = 0, int b = 0, int c = 0) {
   const uint32_t e = n % kItemRing, ph = (n / kItemRing) & 1;
   bool ok = true;
   if (n >= kItemRing) ok = mbar_wait(&r->empty[e], ph ^ 1, abort, status);
   if (!__all_sync(0xffffffffu, ok)) return false;
   if ((threadIdx.x & 31) == 0) {
     reinterpret_cast<volatile int*>(r->id)[e] = id;
+    reinterpret_cast<volatile int*>(r->info[e])[0] = a;
+    reinterpret_cast<volatile int*>(r->info[e])[1] = b;
+    reinterpret_cast<volatile int*>(r->info[e])[2] = c;
     mbar_arrive(&r->full[e]);  // release: the entry is visible to whoever sees the phase flip
   }
   __syncwarp();
@@ -71,11 +76,16 @@ __device__ __forceinline__ bool item_put(ItemRing* r, uint32_t& n, int id, volat
 // Consumer warp (warp-collective): this CTA's n-th item number; the entry is
 // released as soon as it is read.
 __device__ __forceinline__ bool item_get(ItemRing* r, uint32_t& n, int& id, volatile int* abort,
-                                         int* status) {
+                                         int* status, int* info = nullptr) {
   const uint32_t e = n % kItemRing, ph = (n / kItemRing) & 1;
   const bool ok = mbar_wait(&r->full[e], ph, abort, status);
   if (!__all_sync(0xffffffffu, ok)) return false;
   id = reinterpret_cast<volatile int*>(r->id)[e];
+  if (info) {
+    info[0] = reinterpret_cast<volatile int*>(r->info[e])[0];
+    info[1] = reinterpret_cast<volatile int*>(r->info[e])[1];
+    info[2] = reinterpret_cast<volatile int*>(r->info[e])[2];
+  }
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(&r->empty[e]);
   ++n;
