@@ -201,6 +201,36 @@ def test_outputs_untouched_outside_their_rows():
         assert torch.isfinite(inner).all()
 
 
+@pytest.mark.parametrize("grad_dtype", [torch.bfloat16, torch.float32])
+def test_outputs_at_16_byte_offsets_match(grad_dtype):
+    """Outputs 16- but not 32-byte aligned (the C ABI's minimum) give the same bits."""
+    _need_gpu()
+    p, L = treegen.grpo_tree(4, prompt=200, n_leaves=3, lo=60, hi=180)
+    N = int(L.sum())
+    hq, hkv = 4, 2
+    q, k, v, do = (x.cuda() for x in treegen.draw_tensors(N, hq, hkv, 128, "bf16", 4))
+    plan = tpa.tree_plan_build(p, L)
+
+    def offset16(shape, dtype):
+        n = int(np.prod(shape))
+        pad = 16 // torch.tensor([], dtype=dtype).element_size()
+        buf = torch.empty(n + 2 * pad, dtype=dtype, device="cuda")
+        t = buf[pad:pad + n].view(*shape)
+        assert t.data_ptr() % 16 == 0 and t.data_ptr() % 32 != 0
+        return t
+
+    o, lse = tpa.tree_attn_fwd(plan, q, k, v)
+    o16 = offset16((N, hq, 128), torch.bfloat16)
+    tpa.tree_attn_fwd(plan, q, k, v, out=o16, lse=torch.empty_like(lse))
+    g = tpa.tree_attn_bwd(plan, do, q, k, v, o, lse, grad_dtype=grad_dtype)
+    g16 = tuple(offset16(x.shape, grad_dtype) for x in g)
+    tpa.tree_attn_bwd(plan, do, q, k, v, o, lse, grad_dtype=grad_dtype, out=g16)
+    tpa.tree_status_sync()
+    assert torch.equal(o, o16)
+    for a, b in zip(g, g16):
+        assert torch.equal(a, b)
+
+
 def test_empty_plan_is_a_no_op():
     _need_gpu()
     plan = tpa.tree_plan_build(np.zeros(0, np.int32), np.zeros(0, np.int32))

@@ -70,24 +70,40 @@ __device__ __forceinline__ void mma_tn_split(uint32_t d, uint32_t a_tmem, uint32
                 (acc || kk > 0) ? 1u : 0u);
 }
 
-// Write 32 consecutive fp32 values of one 128-wide row, times `mul`, as fp32 or bf16.
+// Write 32 consecutive fp32 values of one 128-wide row, times `mul`, as fp32 or
+// bf16; with 32-byte stores when the destination allows (`v8`).
 __device__ __forceinline__ void store_row(void* dst_base, size_t off, int c, const uint32_t (&v)[32],
-                                          float mul, int out_f32) {
+                                          float mul, int out_f32, int v8) {
   if (out_f32) {
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(dst_base) + off + c * 32);
+    float* dst = static_cast<float*>(dst_base) + off + c * 32;
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      dst[u] = make_float4(__uint_as_float(v[4 * u]) * mul, __uint_as_float(v[4 * u + 1]) * mul,
-                           __uint_as_float(v[4 * u + 2]) * mul, __uint_as_float(v[4 * u + 3]) * mul);
+    for (int u = 0; u < 4; ++u) {
+      uint32_t w[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(__uint_as_float(v[8 * u + e]) * mul);
+      if (v8) {
+        st_global_v8(dst + 8 * u, w);
+      } else {
+        reinterpret_cast<uint4*>(dst + 8 * u)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<uint4*>(dst + 8 * u)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    }
   } else {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst_base) + off + c * 32);
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(dst_base) + off + c * 32;
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-      dst[u] = make_uint4(
-          pack_bf16x2(__uint_as_float(v[8 * u + 0]) * mul, __uint_as_float(v[8 * u + 1]) * mul),
-          pack_bf16x2(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul),
-          pack_bf16x2(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul),
-          pack_bf16x2(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul));
+    for (int u = 0; u < 2; ++u) {
+      uint32_t w[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        w[e] = pack_bf16x2(__uint_as_float(v[16 * u + 2 * e]) * mul,
+                           __uint_as_float(v[16 * u + 2 * e + 1]) * mul);
+      if (v8) {
+        st_global_v8(dst + 16 * u, w);
+      } else {
+        reinterpret_cast<uint4*>(dst + 16 * u)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<uint4*>(dst + 16 * u)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    }
   }
 }
 
@@ -132,6 +148,7 @@ struct DqParams {
   int* status;
   SchedSlot* sched;
   int N, Npad, hq, group, n_items, out_f32;
+  int out_v8;  // dq is 32-byte aligned
   float scale, scale_log2;
 };
 
@@ -556,7 +573,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
         tmem_ld32(tDQ + lane_off + col0 + c * 32, v);
-        if (i < p.N) store_row(p.dq, row * 128, half * 2 + c, v, p.scale, p.out_f32);
+        if (i < p.N) store_row(p.dq, row * 128, half * 2 + c, v, p.scale, p.out_f32, p.out_v8);
       }
       tc_fence_before_sync();
       mbar_arrive(&bar_dq_free);
@@ -609,6 +626,7 @@ struct KvParams {
   int* status;
   SchedSlot* sched;
   int N, Npad, hq, hkv, group, n_items, out_f32;
+  int out_v8;  // dk and dv are 32-byte aligned
   float scale, scale_log2;
 };
 
@@ -914,13 +932,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
         tmem_ld32(tC + lane_off + col0 + c * 32, v);
-        if (jk < p.N) store_row(p.dv, out, half * 2 + c, v, 1.f, p.out_f32);
+        if (jk < p.N) store_row(p.dv, out, half * 2 + c, v, 1.f, p.out_f32, p.out_v8);
       }
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
         tmem_ld32(tD + lane_off + col0 + c * 32, v);
-        if (jk < p.N) store_row(p.dk, out, half * 2 + c, v, p.scale, p.out_f32);
+        if (jk < p.N) store_row(p.dk, out, half * 2 + c, v, p.scale, p.out_f32, p.out_v8);
       }
       tc_fence_before_sync();
       mbar_arrive(bar_dkdv_free);
@@ -969,6 +987,7 @@ cudaError_t launch_bwd_bf16(const AttnBwdArgs& a) {
   d.group = a.hq / a.hkv;
   d.n_items = pl->Tq * a.hq;
   d.out_f32 = a.grad_f32 ? 1 : 0;
+  d.out_v8 = (reinterpret_cast<uintptr_t>(a.dq) & 31u) == 0;
   d.scale = a.scale;
   d.scale_log2 = a.scale * kLog2e;
 
@@ -991,6 +1010,7 @@ cudaError_t launch_bwd_bf16(const AttnBwdArgs& a) {
   k.group = a.hq / a.hkv;
   k.n_items = pl->Tk * a.hkv;
   k.out_f32 = a.grad_f32 ? 1 : 0;
+  k.out_v8 = ((reinterpret_cast<uintptr_t>(a.dk) | reinterpret_cast<uintptr_t>(a.dv)) & 31u) == 0;
   k.scale = a.scale;
   k.scale_log2 = a.scale * kLog2e;
 

@@ -59,6 +59,7 @@ struct FwdParams {
   int* status;
   SchedSlot* sched;
   int N, hq, group, n_items, n_inner, mode, Tq;
+  int o_v8;  // o is 32-byte aligned: rows are written with 32-byte stores
   float scale_log2;  // softmax scale * log2(e)
 };
 
@@ -525,28 +526,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = warp_wait(&bar_o_full[s], oc & 1, abort, p.status))) break;
       ++oc;
       tc_fence_after_sync();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = p.o + (static_cast<size_t>(i) * p.hq + h) * 128;
+      uint32_t ov[128];
+      tmem_ld128(tO, ov);  // the whole O row, one wait
+      tc_fence_before_sync();
+      mbar_arrive(&bar_o_free[s]);  // O_s is in registers: the next item's PV may start
+      if (i < p.N) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16* orow = p.o + (static_cast<size_t>(i) * p.hq + h) * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(tO + c * 32, rr);
-        uint32_t pk[16];
+        for (int c = 0; c < 8; ++c) {  // 16 columns = 32 bytes at a time
+          uint32_t pk[8];
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj)
-          pk[jj] = pack_bf16x2(__uint_as_float(rr[2 * jj]) * inv, __uint_as_float(rr[2 * jj + 1]) * inv);
-        if (i < p.N) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          for (int jj = 0; jj < 8; ++jj)
+            pk[jj] = pack_bf16x2(__uint_as_float(ov[16 * c + 2 * jj]) * inv,
+                                 __uint_as_float(ov[16 * c + 2 * jj + 1]) * inv);
+          if (p.o_v8) {
+            st_global_v8(orow + 16 * c, pk);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 16 * c);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
         }
-      }
-      if (i < p.N)
         p.lse[static_cast<size_t>(h) * p.N + i] =
             l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
-      tc_fence_before_sync();
-      mbar_arrive(&bar_o_free[s]);
+      }
       if (nxt >= 0) {  // the next item's first tile
         nt_at = n_beg;
         nt = load_tile(p, nt_at, s, lane);
@@ -595,6 +599,7 @@ cudaError_t launch_fwd_bf16(const AttnArgs& a) {
   p.lse = a.lse;
   p.status = a.status;
   p.sched = next_sched_slot();
+  p.o_v8 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;
   if (!p.sched) return cudaErrorInvalidDevicePointer;
   p.N = pl->N;
   p.hq = a.hq;
