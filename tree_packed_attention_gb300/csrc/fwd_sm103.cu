@@ -71,27 +71,31 @@ struct Item {
 };
 
 // mode 0: two heads of one kv group at one q-tile; mode 1: q-tiles 2p, 2p+1 of one head.
-__device__ __forceinline__ Item decode_item(const FwdParams& p, int it) {
+// hdr = {order entry (q-tile or pair), first and end of its tile list}: the
+// producer reads it once and publishes it with the item number.
+__device__ __forceinline__ Item decode_item(const FwdParams& p, int it, const int (&hdr)[3]) {
   Item x;
-  const int idx = it / p.n_inner, inner = it % p.n_inner;
+  const int inner = it % p.n_inner;
   if (p.mode == 0) {
-    const int qt = p.order[idx];
-    x.qtile[0] = x.qtile[1] = qt;
+    x.qtile[0] = x.qtile[1] = hdr[0];
     x.head[0] = 2 * inner;
     x.head[1] = 2 * inner + 1;
     x.kvh = (2 * inner) / p.group;
-    x.beg = p.list_ptr[qt];
-    x.end = p.list_ptr[qt + 1];
   } else {
-    const int pr = p.order[idx];
-    x.qtile[0] = 2 * pr;
-    x.qtile[1] = 2 * pr + 1;
+    x.qtile[0] = 2 * hdr[0];
+    x.qtile[1] = 2 * hdr[0] + 1;
     x.head[0] = x.head[1] = inner;
     x.kvh = inner / p.group;
-    x.beg = p.list_ptr[pr];
-    x.end = p.list_ptr[pr + 1];
   }
+  x.beg = hdr[1];
+  x.end = hdr[2];
   return x;
+}
+
+__device__ __forceinline__ void read_header(const FwdParams& p, int it, int (&hdr)[3]) {
+  hdr[0] = __ldg(p.order + it / p.n_inner);
+  hdr[1] = __ldg(p.list_ptr + hdr[0]);
+  hdr[2] = __ldg(p.list_ptr + hdr[0] + 1);
 }
 
 // Tile kinds of both slots packed as kind0 | kind1 << 2 (0 empty, 1 partial, 2 full).
@@ -214,10 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The next item is taken from the launch's counter once every load of
     // this one is issued, a couple of tiles before the CTA is free: taking it
     // earlier can leave two long items on one CTA while another sits idle.
+    int hdr[3] = {0, 0, 0};
     int cur = item_fetch(p.sched, p.n_items);
-    bool ok = item_put(&ring, pub, cur, abort, p.status);
+    if (cur >= 0) read_header(p, cur, hdr);
+    bool ok = item_put(&ring, pub, cur, abort, p.status, hdr[0], hdr[1], hdr[2]);
     while (ok && cur >= 0) {
-      const Item x = decode_item(p, cur);
+      const Item x = decode_item(p, cur, hdr);
       if (qn > 0 && !(ok = warp_wait(&bar_q_empty, (qn - 1) & 1, abort, p.status))) break;
       if (lane == 0) {
         const uint32_t bytes = (x.qtile[1] < p.Tq ? 2u : 1u) * kTileBytes;
@@ -251,9 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       cur = item_fetch(p.sched, p.n_items);
-      if (!(ok = item_put(&ring, pub, cur, abort, p.status))) break;
+      if (cur >= 0) read_header(p, cur, hdr);
+      if (!(ok = item_put(&ring, pub, cur, abort, p.status, hdr[0], hdr[1], hdr[2]))) break;
       if (cur >= 0 && lane == 0) {  // its Q tiles into L2 while this item finishes
-        const Item y = decode_item(p, cur);
+        const Item y = decode_item(p, cur, hdr);
         for (int s = 0; s < 2; ++s) {
           if (y.qtile[s] >= p.Tq) continue;
           tma_prefetch_l2_3d(&map_q, 0, y.head[s], y.qtile[s] * 128);
@@ -277,8 +284,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t pc[2] = {0, 0}, oc[2] = {0, 0};
     const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
     bool ok = true;
-    for (int cur; (ok = item_get(&ring, got, cur, abort, p.status)) && cur >= 0;) {
-      const Item x = decode_item(p, cur);
+    int hdr[3];
+    for (int cur; (ok = item_get(&ring, got, cur, abort, p.status, hdr)) && cur >= 0;) {
+      const Item x = decode_item(p, cur, hdr);
       const int T = x.end - x.beg;
       if (!(ok = warp_wait(&bar_q_full, qn & 1, abort, p.status))) break;
       ++qn;
@@ -362,19 +370,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // first) is loaded one tile ahead, and the next item's header one item
     // ahead, so no global load latency sits between two softmax passes.
     int n_qt = 0, n_h = 0, n_beg = 0, n_end = 0;  // next item: q-tile, head, tile range
+    int hdr[3];
     auto fetch_header = [&](int at) {
-      const Item y = decode_item(p, at);
+      const Item y = decode_item(p, at, hdr);
       n_qt = y.qtile[s];
       n_h = y.head[s];
       n_beg = y.beg;
       n_end = y.end;
     };
-    // The next item's number is read once this item's tiles are done (the
-    // producer publishes it when this item's loads are issued); its header
-    // loads overlap the wait for the last PV.
+    // The next item's number and header are read from the ring once this
+    // item's tiles are done (the producer publishes them when this item's
+    // loads are issued); its first tile's loads overlap this epilogue.
     uint32_t got = 0;
     int cur = -1;
-    ok = item_get(&ring, got, cur, abort, p.status);
+    ok = item_get(&ring, got, cur, abort, p.status, hdr);
     if (ok && cur >= 0) fetch_header(cur);
     TileInfo nt;
     int nt_at = -1;
@@ -382,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qt = n_qt, h = n_h, beg = n_beg, end = n_end;
       int nxt = -1;
       if (qt >= p.Tq) {  // this slot has no rows in the item
-        if ((ok = item_get(&ring, got, nxt, abort, p.status)) && nxt >= 0) fetch_header(nxt);
+        if ((ok = item_get(&ring, got, nxt, abort, p.status, hdr)) && nxt >= 0) fetch_header(nxt);
         cur = nxt;
         continue;
       }
@@ -520,8 +529,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bar_p_full[s]);
       }
       if (!ok) break;
-      if (!(ok = item_get(&ring, got, nxt, abort, p.status))) break;
-      if (nxt >= 0) fetch_header(nxt);
+      if (!(ok = item_get(&ring, got, nxt, abort, p.status, hdr))) break;
+      if (nxt >= 0) {  // its header, and its first tile's loads during this epilogue
+        fetch_header(nxt);
+        nt_at = n_beg;
+        nt = load_tile(p, nt_at, s, lane);
+      }
       // ---- epilogue: O / l and lse
       if (!(ok = warp_wait(&bar_o_full[s], oc & 1, abort, p.status))) break;
       ++oc;
@@ -550,10 +563,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         p.lse[static_cast<size_t>(h) * p.N + i] =
             l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
-      }
-      if (nxt >= 0) {  // the next item's first tile
-        nt_at = n_beg;
-        nt = load_tile(p, nt_at, s, lane);
       }
       cur = nxt;
     }
