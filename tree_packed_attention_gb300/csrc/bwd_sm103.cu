@@ -593,13 +593,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
 // ============================================================ dK/dV kernel
 // 384 threads: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps
-// 4-11 one key row per thread, two warpgroups splitting the q columns (P^T and
-// dS^T into TMEM, and at the end of an item the dV and dK rows). TMEM: S^T,
-// then P^T over the columns read | dP^T, then dS^T likewise | dV | dK. Both products that need P^T
-// and dS^T read them from TMEM, so no operand is written to shared memory.
+// 4-11 one key row per thread, two warpgroups splitting the q columns (at the
+// end of an item they store the dV and dK rows). TMEM: S^T | dP^T, then dS^T
+// and P^T over it | dV | dK. Both products that need P^T and dS^T read them
+// from TMEM, so no operand is written to shared memory.
 // Q_n is read by S^T_n and, a step later, by dK_n, so Q is staged three deep;
 // dO_n (with the step's lse and Delta) is released after dV_n, two deep.
 constexpr int kKvThreads = 384;
+constexpr uint32_t kKvRegsCtl = 72, kKvRegsSoftmax = 216;  // 128 x 72 + 256 x 216 = 384 x 168
+static_assert(128 * kKvRegsCtl + 256 * kKvRegsSoftmax <= 384 * 168, "register split");
 constexpr int kKvQStages = 3;
 constexpr int kKvDoStages = 2;
 constexpr uint32_t kKvOffK = 0;
@@ -668,6 +670,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   uint64_t* bar_dkdv_full = bars + 15;
   uint64_t* bar_dkdv_free = bars + 16;
   uint64_t* bar_final = bars + 17;
+  uint64_t* bar_s_read = bars + 18;  // the softmax warps hold S^T_n in registers
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kKvNumBars);
   volatile int* abort = reinterpret_cast<volatile int*>(bars + kKvNumBars) + 1;
   ItemRing* ring = reinterpret_cast<ItemRing*>(smem + kKvOffRing);
@@ -690,6 +693,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     mbar_init(bar_dkdv_full, 1);
     mbar_init(bar_dkdv_free, 256);
     mbar_init(bar_final, 1);
+    mbar_init(bar_s_read, 256);
     *abort = 0;
     fence_mbar_init();
   }
@@ -710,6 +714,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   const uint32_t tA = tmem, tB = tmem + 128, tC = tmem + 256, tD = tmem + 384;
 
   if (warp == 0) {
+    regs_dec<kKvRegsCtl>();
     // ------------------------------------------------------------ producer
     uint32_t n = 0, items = 0, pub = 0;
     // The next item is taken once every load of this one is issued: items
@@ -779,9 +784,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       }
     }
   } else if (warp == 1) {
+    regs_dec<kKvRegsCtl>();
     // ---------------------------------------------------------- MMA issuer
     // Per step n (S^T_n and dP^T_n already issued):
-    //   [dS_n] dV += P^T_n dO_n, S^T_{n+1}, dK += dS^T_n Q_n, dP^T_{n+1}
+    //   [S^T_n read] S^T_{n+1};  [dS_n] dV += P^T_n dO_n, dK += dS^T_n Q_n, dP^T_{n+1}
+    // P^T_n and dS^T_n both sit in the dP^T buffer, so the S^T buffer is free
+    // as soon as the softmax warps have S^T_n in registers, and S^T_{n+1}
+    // runs while they compute P_n and dS_n.
     const uint32_t aK = smem_u32(smem + kKvOffK), aV = smem_u32(smem + kKvOffV);
     auto q_addr = [&](uint32_t i) { return smem_u32(smem + kKvOffQ + (i % kKvQStages) * kTileBytes); };
     auto do_addr = [&](uint32_t i) { return smem_u32(smem + kKvOffDO + (i % kKvDoStages) * kTileBytes); };
@@ -807,20 +816,21 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           mma_kk(tB, aV, do_addr(n), 0);  // dP^T = V dO^T
           mma_commit_warp(bar_dp_full);
         }
+        const bool has_next = j + 1 < x.steps;
+        if (has_next) {
+          if (!(ok = warp_wait(bar_s_read, n & 1, abort, p.status))) break;
+          if (!(ok = wait_q(n + 1))) break;
+          tc_fence_after_sync();
+          mma_kk(tA, aK, q_addr(n + 1), 0);  // next S^T
+          mma_commit_warp(bar_s_full);
+        }
         if (!(ok = warp_wait(bar_ds_full, n & 1, abort, p.status))) break;
         if (j == 0 && items > 0 &&
             !(ok = warp_wait(bar_dkdv_free, (items - 1) & 1, abort, p.status)))
           break;
         tc_fence_after_sync();
-        mma_tn_split(tC, tA, do_addr(n), j > 0);  // dV += P^T dO
+        mma_tn_split(tC, tB + 32, do_addr(n), j > 0);  // dV += P^T dO (P^T from TMEM)
         mma_commit_warp(bar_do_empty + n % kKvDoStages);
-        const bool has_next = j + 1 < x.steps;
-        if (has_next) {
-          if (!(ok = wait_q(n + 1))) break;
-          tc_fence_after_sync();
-          mma_kk(tA, aK, q_addr(n + 1), 0);  // next S^T (P^T_n already read by dV)
-          mma_commit_warp(bar_s_full);
-        }
         mma_tn_split(tD, tB, q_addr(n), j > 0);  // dK += dS^T Q (dS^T from TMEM)
         mma_commit_warp(bar_q_empty + n % kKvQStages);
         if (has_next) {
@@ -836,12 +846,16 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     }
     mma_commit_warp(bar_final);
     mbar_drain(bar_final, 0);
-  } else if (warp >= 4) {
+  } else if (warp < 4) {
+    regs_dec<kKvRegsCtl>();  // warps 2-3: idle
+  } else {
+    regs_inc<kKvRegsSoftmax>();
     // ---- two warpgroups split each step's 128 q columns: warps 4-7 take
     // columns 0-63, warps 8-11 columns 64-127; one key row per thread. Each
-    // half writes P^T over the first 32 of its own S^T columns and dS^T over
-    // the first 32 of its own dP^T columns. At the end of an item each half
-    // stores its 64 columns of dV and dK.
+    // half reads its S^T columns (then releases the S^T buffer) and its dP^T
+    // columns, and writes dS^T over the first 32 and P^T over the second 32
+    // of its own dP^T columns. At the end of an item each half stores its 64
+    // columns of dV and dK.
     const int half = (warp - 4) / 4;
     const int quarter = warp % 4;
     const int kr = quarter * 32 + lane;
@@ -869,6 +883,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         {
           uint32_t rr[64];
           tmem_ld64(tSr, rr);  // this half of the S^T row, one wait
+          tc_fence_before_sync();
+          mbar_arrive(bar_s_read);  // the S^T buffer may take the next S^T
           if (all_full) {
 #pragma unroll
             for (int jj = 0; jj < 64; jj += 4) {
@@ -892,18 +908,19 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             }
           }
         }
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) pk[jj] = pack_bf16x2(pv[c * 32 + 2 * jj], pv[c * 32 + 2 * jj + 1]);
-          tmem_st16(tSr + c * 16, pk);  // P^T over the first 32 columns of this half
-        }
         if (!(ok = warp_wait(bar_dp_full, n & 1, abort, p.status))) break;
         tc_fence_after_sync();
         {
           uint32_t rr[64];
           tmem_ld64(tPr, rr);  // this half of the dP^T row, one wait
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+              pk[jj] = pack_bf16x2(pv[c * 32 + 2 * jj], pv[c * 32 + 2 * jj + 1]);
+            tmem_st16(tPr + 32 + c * 16, pk);  // P^T over the second 32 columns of this half
+          }
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t pk[16];
