@@ -128,7 +128,7 @@ constexpr uint32_t kDqOffV = kDqOffK + kDqKStages * kTileBytes;
 constexpr uint32_t kDqOffKe = kDqOffV + kDqVStages * kTileBytes;  // per K stage: 128 key_end
 // mbarriers, then the item ring, then the TMEM base and the abort flag
 constexpr uint32_t kDqOffBar = kDqOffKe + kDqKStages * 512;
-constexpr uint32_t kDqNumBars = 3 + 2 * kDqKStages + 2 * kDqVStages + 2 + 4;
+constexpr uint32_t kDqNumBars = 3 + 2 * kDqKStages + 2 * kDqVStages + 2 + 5;
 constexpr uint32_t kDqOffRing = kDqOffBar + kDqNumBars * 8;
 constexpr uint32_t kDqOffMisc = kDqOffRing + sizeof(ItemRing);
 constexpr uint32_t kDqSmem = kDqOffMisc + 16;
@@ -184,6 +184,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   uint64_t& bar_ds_full = tail[1];
   uint64_t& bar_dq_full = tail[2];
   uint64_t& bar_dq_free = tail[3];
+  uint64_t& bar_dp_read = tail[4];  // the softmax warps hold dP_t in registers
   ItemRing& ring = *reinterpret_cast<ItemRing*>(smem + kDqOffRing);
   uint32_t& tmem_base_s = *reinterpret_cast<uint32_t*>(smem + kDqOffMisc);
   int& abort_s = *reinterpret_cast<int*>(smem + kDqOffMisc + 4);
@@ -209,6 +210,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&bar_ds_full, 256);
     mbar_init(&bar_dq_full, 1);
     mbar_init(&bar_dq_free, 256);
+    mbar_init(&bar_dp_read, 256);
     abort_s = 0;
     fence_mbar_init();
   }
@@ -306,8 +308,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   } else if (warp == 1) {
     regs_dec<kDqRegsCtl>();
     // ---------------------------------------------------------- MMA issuer
-    // Per item: S_0, dP_0, S_1; then per tile t: [dS_t] dQ += dS_t K_t,
-    // dP_{t+1}, S_{t+2} (into the S buffer dQ_t just read).
+    // Per item: S_0, dP_0, S_1; then per tile t: [dP_t read] dP_{t+1};
+    // [dS_t] dQ += dS_t K_t, S_{t+2} (into the S buffer dQ_t just read).
     const uint32_t aQ = smem_u32(smem + kDqOffQ), aDO = smem_u32(smem + kDqOffDO);
     const uint32_t aK = smem_u32(smem + kDqOffK), aV = smem_u32(smem + kDqOffV);
     uint32_t kv = 0, qn = 0, n = 0, got = 0;
@@ -342,6 +344,19 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       }
       for (int t = 0; t < T && ok; ++t, ++n) {
         const uint32_t i = kv + t;
+        // dP_{t+1} as soon as the softmax warps hold dP_t, ahead of dQ_t
+        if (t + 1 < T) {
+          if (!(ok = warp_wait(&bar_dp_read, n & 1, abort, p.status))) break;
+          if (!(ok = wait_v(i + 1))) break;
+          tc_fence_after_sync();
+          mma_kk(tDP, aDO, v_stage(i + 1), 0);
+          mma_commit_warp(&bar_dp_full);
+          mma_commit_warp(&bar_v_empty[(i + 1) % kDqVStages]);
+          // dP_{T-1} is the item's last reader of Q and dO (S_{T-1} came
+          // before it, and Delta read dO before the first dP was released):
+          // the next item's Q and dO load during the last step.
+          if (t + 2 == T) mma_commit_warp(&bar_q_empty);
+        }
         if (!(ok = warp_wait(&bar_ds_full, n & 1, abort, p.status))) break;
         if (t == 0 && qn > 1 && !(ok = warp_wait(&bar_dq_free, (qn - 2) & 1, abort, p.status)))
           break;
@@ -351,16 +366,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (t + 1 == T) mma_commit_warp(&bar_dq_full);
         if (T == 1) mma_commit_warp(&bar_q_empty);  // the softmax warps read dO for Delta
                                                     // before the first dS arrives
-        if (t + 1 < T) {
-          if (!(ok = wait_v(i + 1))) break;
-          tc_fence_after_sync();
-          mma_kk(tDP, aDO, v_stage(i + 1), 0);  // dP_{t+1} (dP_t already read)
-          mma_commit_warp(&bar_dp_full);
-          mma_commit_warp(&bar_v_empty[(i + 1) % kDqVStages]);
-          // dP_{T-1} is the item's last reader of Q and dO (S_{T-1} came
-          // before it): the next item's Q and dO load during the last step.
-          if (t + 2 == T) mma_commit_warp(&bar_q_empty);
-        }
         if (t + 2 < T) {
           if (!(ok = wait_k(i + 2))) break;
           tc_fence_after_sync();
@@ -540,6 +545,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (!(ok = warp_wait(&bar_dp_full, n & 1, abort, p.status))) break;
         tc_fence_after_sync();
         if (mode == 2) {
+          mbar_arrive(&bar_dp_read);  // nothing to read
           uint32_t pk[16];
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) pk[jj] = 0u;
@@ -548,6 +554,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         } else {
           uint32_t rr[64];
           tmem_ld64(tDP + lane_off + col0, rr);  // this half of the dP row, one wait
+          tc_fence_before_sync();
+          mbar_arrive(&bar_dp_read);  // the dP buffer may take dP_{t+1}
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t pk[16];
