@@ -39,9 +39,10 @@ constexpr uint32_t kTileBytes = 128 * 128 * 2;
 constexpr uint32_t kHalfBytes = kTileBytes / 2;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// (a wait that gives up records the line it was called from)
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          int* status) {
-  const bool ok = mbar_wait(bar, parity, abort, status);
+                                          int* status, int line = __builtin_LINE()) {
+  const bool ok = mbar_wait(bar, parity, abort, status, kSiteBwd + line);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -279,7 +279,9 @@ extern "C" tree_status_t tree_status_sync(tree_stream_t stream) {
   if (word != 0) {
     const int zero = 0;
     cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int));
-    return fail(TREE_ERR_TIMEOUT, "a kernel gave up a bounded wait (status " +
+    if (word == 9)
+      return fail(TREE_ERR_CUDA, "a kernel's shared memory block was not 1024-byte aligned");
+    return fail(TREE_ERR_TIMEOUT, "a kernel gave up a bounded wait (wait site " +
                                       std::to_string(word) + ")");
   }
   return TREE_OK;

@@ -121,9 +121,10 @@ __device__ __forceinline__ TileInfo load_tile(const FwdParams& p, int t, int s, 
   return x;
 }
 
+// (a wait that gives up records the line it was called from)
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          int* status) {
-  const bool ok = mbar_wait(bar, parity, abort, status);
+                                          int* status, int line = __builtin_LINE()) {
+  const bool ok = mbar_wait(bar, parity, abort, status, kSiteFwd + line);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -59,7 +59,7 @@ __device__ __forceinline__ bool item_put(ItemRing* r, uint32_t& n, int id, volat
                                          int* status, int a = 0, int b = 0, int c = 0) {
   const uint32_t e = n % kItemRing, ph = (n / kItemRing) & 1;
   bool ok = true;
-  if (n >= kItemRing) ok = mbar_wait(&r->empty[e], ph ^ 1, abort, status);
+  if (n >= kItemRing) ok = mbar_wait(&r->empty[e], ph ^ 1, abort, status, kSiteRing + static_cast<int>(threadIdx.x / 32));
   if (!__all_sync(0xffffffffu, ok)) return false;
   if ((threadIdx.x & 31) == 0) {
     reinterpret_cast<volatile int*>(r->id)[e] = id;
@@ -78,7 +78,7 @@ __device__ __forceinline__ bool item_put(ItemRing* r, uint32_t& n, int id, volat
 __device__ __forceinline__ bool item_get(ItemRing* r, uint32_t& n, int& id, volatile int* abort,
                                          int* status, int* info = nullptr) {
   const uint32_t e = n % kItemRing, ph = (n / kItemRing) & 1;
-  const bool ok = mbar_wait(&r->full[e], ph, abort, status);
+  const bool ok = mbar_wait(&r->full[e], ph, abort, status, kSiteRing + static_cast<int>(threadIdx.x / 32));
   if (!__all_sync(0xffffffffu, ok)) return false;
   id = reinterpret_cast<volatile int*>(r->id)[e];
   if (info) {

@@ -14,6 +14,10 @@ namespace dev {
 
 // Status word values (a kernel that gives up a wait stores one of these).
 constexpr int kStatusTimeout = 7;
+// A wait that gives up stores a code naming where it waited instead:
+// kSiteFwd / kSiteBwd + the source line of the wait in that kernel's file,
+// or kSiteRing + the warp for the work ring.
+constexpr int kSiteFwd = 10000, kSiteBwd = 20000, kSiteRing = 30000;
 
 // A bounded wait gives up after this long (ns of %globaltimer).
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
@@ -62,7 +66,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // (returns false) after kWaitLimitNs or once *abort is set by another thread;
 // on a timeout it sets *abort and the device status word.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          int* status) {
+                                          int* status, int site = kStatusTimeout) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -71,7 +75,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       if (*abort) return false;
       if (global_timer_ns() - t0 > kWaitLimitNs) {
         *abort = 1;
-        if (status) atomicExch(status, kStatusTimeout);
+        if (status) atomicExch(status, site);
         return false;
       }
     }
