@@ -127,9 +127,11 @@ constexpr uint32_t kDqOffDO = kTileBytes;
 constexpr uint32_t kDqOffK = 2 * kTileBytes;
 constexpr uint32_t kDqOffV = kDqOffK + kDqKStages * kTileBytes;
 constexpr uint32_t kDqOffKe = kDqOffV + kDqVStages * kTileBytes;  // per K stage: 128 key_end
+// Delta of the tile's 128 rows, two buffers (items alternate)
+constexpr uint32_t kDqOffDelta = kDqOffKe + kDqKStages * 512;
 // mbarriers, then the item ring, then the TMEM base and the abort flag
-constexpr uint32_t kDqOffBar = kDqOffKe + kDqKStages * 512;
-constexpr uint32_t kDqNumBars = 3 + 2 * kDqKStages + 2 * kDqVStages + 2 + 5;
+constexpr uint32_t kDqOffBar = kDqOffDelta + 2 * 512;
+constexpr uint32_t kDqNumBars = 3 + 2 * kDqKStages + 2 * kDqVStages + 2 + 5 + 4;
 constexpr uint32_t kDqOffRing = kDqOffBar + kDqNumBars * 8;
 constexpr uint32_t kDqOffMisc = kDqOffRing + sizeof(ItemRing);
 constexpr uint32_t kDqSmem = kDqOffMisc + 16;
@@ -157,7 +159,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     tree_attn_bwd_dq_sm103(const __grid_constant__ CUtensorMap map_q,
                            const __grid_constant__ CUtensorMap map_k,
                            const __grid_constant__ CUtensorMap map_v,
-                           const __grid_constant__ CUtensorMap map_do, const DqParams p) {
+                           const __grid_constant__ CUtensorMap map_do,
+                           const __grid_constant__ CUtensorMap map_o, const DqParams p) {
   // All shared state sits in the dynamic block (no static shared memory), so
   // the block starts 1024-aligned as the 128B-swizzled tiles need.
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -186,6 +189,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   uint64_t& bar_dq_full = tail[2];
   uint64_t& bar_dq_free = tail[3];
   uint64_t& bar_dp_read = tail[4];  // the softmax warps hold dP_t in registers
+  // per row quarter: both warps of the quarter wrote their half of its Delta
+  uint64_t* bar_delta = tail + 5;
   ItemRing& ring = *reinterpret_cast<ItemRing*>(smem + kDqOffRing);
   uint32_t& tmem_base_s = *reinterpret_cast<uint32_t*>(smem + kDqOffMisc);
   int& abort_s = *reinterpret_cast<int*>(smem + kDqOffMisc + 4);
@@ -212,6 +217,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&bar_dq_full, 1);
     mbar_init(&bar_dq_free, 256);
     mbar_init(&bar_dp_read, 256);
+    for (int qq = 0; qq < 4; ++qq) mbar_init(&bar_delta[qq], 2);
     abort_s = 0;
     fence_mbar_init();
   }
@@ -220,6 +226,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     tma_prefetch_desc(&map_k);
     tma_prefetch_desc(&map_v);
     tma_prefetch_desc(&map_do);
+    tma_prefetch_desc(&map_o);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_s, 512);
@@ -296,6 +303,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         tma_prefetch_l2_3d(&map_q, 64, nh, nqt * 128);
         tma_prefetch_l2_3d(&map_do, 0, nh, nqt * 128);
         tma_prefetch_l2_3d(&map_do, 64, nh, nqt * 128);
+        tma_prefetch_l2_3d(&map_o, 0, nh, nqt * 128);
+        tma_prefetch_l2_3d(&map_o, 64, nh, nqt * 128);
       }
       __syncwarp();
     }
@@ -412,18 +421,19 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     ok = item_get(&ring, got, cur, abort, p.status, hdr);
     // The loads an item's Delta needs are issued as soon as the item is known
     // (right after the previous item's last tile), so their latency passes
-    // during the previous epilogue: this warp's 32 O rows, a row per
-    // instruction (lane l: dims 4l..4l+3, one contiguous 256-byte row; rows
-    // past N read the last row and count zero), and the thread's lse.
-    uint2 ov[32];
+    // during the previous epilogue. The two warps of a row quarter split its
+    // 32 rows, 16 each (warps 4-7 the first 16): a row per instruction (lane l:
+    // dims 4l..4l+3, one contiguous 256-byte row; rows past N read the last
+    // row and count zero), and the thread's lse.
+    uint2 ov[16];
     float lse_pre = INFINITY;
     auto load_o = [&](int item) {
-      const int r0 = hdr[0] * 128 + quarter * 32, hh = item % p.hq;
-      const int nvalid = min(32, p.N - r0);
+      const int r0 = hdr[0] * 128 + quarter * 32 + half * 16, hh = item % p.hq;
+      const int nvalid = min(16, p.N - r0);
       const __nv_bfloat16* obase = p.o + (static_cast<size_t>(r0) * p.hq + hh) * 128 + 4 * lane;
       const size_t ostride = static_cast<size_t>(p.hq) * 128;
 #pragma unroll
-      for (int rr = 0; rr < 32; ++rr)
+      for (int rr = 0; rr < 16; ++rr)
         ov[rr] = nvalid > 0 ? __ldg(reinterpret_cast<const uint2*>(obase + min(rr, nvalid - 1) * ostride))
                             : make_uint2(0u, 0u);
       const int ii = hdr[0] * 128 + r;
@@ -441,19 +451,20 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const int i = qt * 128 + r;
       const size_t row = static_cast<size_t>(i) * p.hq + h;
       if (!(ok = warp_wait(&bar_q_full, qn & 1, abort, p.status))) break;
-      // Delta = dO . O of this thread's row: each lane's part of the warp's
-      // 32 dot products (its 4 dims of O, loaded ahead, and of dO in smem),
-      // then a transposing reduction leaves row r0 + l's sum in lane l.
+      // Delta = dO . O of this thread's row. Each lane forms its part of the
+      // warp's 16 dot products (its 4 dims of O, loaded ahead, and of dO in
+      // smem); a transposing reduction leaves row 2m's sum in lanes 2m and
+      // 2m+1; the two warps of the quarter swap halves through smem.
       float delta = 0.f, lse2 = INFINITY;
       {
-        float part[32];
-        const int r0 = qt * 128 + quarter * 32;
+        float part[16];
+        const int r0 = qt * 128 + quarter * 32 + half * 16;
         const uint8_t* dbase = smem + kDqOffDO + (lane >> 4) * kHalfBytes + (lane & 1) * 8;
         const int chunk = (lane >> 1) & 7;
-        const int nvalid = min(32, p.N - r0);
+        const int nvalid = min(16, p.N - r0);
 #pragma unroll
-        for (int rr = 0; rr < 32; ++rr) {
-          const int rt = quarter * 32 + rr;  // row within the tile
+        for (int rr = 0; rr < 16; ++rr) {
+          const int rt = quarter * 32 + half * 16 + rr;  // row within the tile
           const uint2 dv = *reinterpret_cast<const uint2*>(dbase + rt * 128 + ((chunk ^ (rt & 7)) * 16));
           const float2 o01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov[rr].x));
           const float2 o23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov[rr].y));
@@ -463,17 +474,23 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           part[rr] = rr < nvalid ? acc : 0.f;
         }
 #pragma unroll
-        for (int st = 0; st < 5; ++st) {
+        for (int st = 0; st < 4; ++st) {
           const int k = 16 >> st;  // lanes with bit k keep the upper half of the rows
           const bool up = (lane & k) != 0;
 #pragma unroll
-          for (int j = 0; j < (16 >> st); ++j) {
-            const float send = up ? part[j] : part[j + (16 >> st)];
-            const float keep = up ? part[j + (16 >> st)] : part[j];
+          for (int j = 0; j < (8 >> st); ++j) {
+            const float send = up ? part[j] : part[j + (8 >> st)];
+            const float keep = up ? part[j + (8 >> st)] : part[j];
             part[j] = keep + __shfl_xor_sync(0xffffffffu, send, k);
           }
         }
-        delta = part[0];
+        part[0] += __shfl_xor_sync(0xffffffffu, part[0], 1);
+        float* sd = reinterpret_cast<float*>(smem + kDqOffDelta + (qn & 1) * 512) + quarter * 32;
+        if ((lane & 1) == 0) sd[half * 16 + (lane >> 1)] = part[0];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_delta[quarter]);
+        if (!(ok = warp_wait(&bar_delta[quarter], qn & 1, abort, p.status))) break;
+        delta = sd[lane];
         lse2 = lse_pre * kLog2e;
       }
       if (half == 0) {
@@ -1051,8 +1068,10 @@ cudaError_t launch_bwd_bf16(const AttnBwdArgs& a) {
     attr_set = true;
   }
   if (a.phases & 1) {
+    CUtensorMap mo;
+    if (!make_tile_map(&mo, a.o, N, a.hq)) return cudaErrorInvalidValue;
     tree_attn_bwd_dq_sm103<<<d.n_items < sms ? d.n_items : sms, kDqThreads, kDqSmem, a.stream>>>(
-        mq, mk, mv, mdo, d);
+        mq, mk, mv, mdo, mo, d);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
