@@ -131,7 +131,7 @@ constexpr uint32_t kDqOffKe = kDqOffV + kDqVStages * kTileBytes;  // per K stage
 constexpr uint32_t kDqOffDelta = kDqOffKe + kDqKStages * 512;
 // mbarriers, then the item ring, then the TMEM base and the abort flag
 constexpr uint32_t kDqOffBar = kDqOffDelta + 2 * 512;
-constexpr uint32_t kDqNumBars = 3 + 2 * kDqKStages + 2 * kDqVStages + 2 + 5 + 4;
+constexpr uint32_t kDqNumBars = 3 + 2 * kDqKStages + 2 * kDqVStages + 2 + 5 + 4 + 1;
 constexpr uint32_t kDqOffRing = kDqOffBar + kDqNumBars * 8;
 constexpr uint32_t kDqOffMisc = kDqOffRing + sizeof(ItemRing);
 constexpr uint32_t kDqSmem = kDqOffMisc + 16;
@@ -191,6 +191,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   uint64_t& bar_dp_read = tail[4];  // the softmax warps hold dP_t in registers
   // per row quarter: both warps of the quarter wrote their half of its Delta
   uint64_t* bar_delta = tail + 5;
+  uint64_t& bar_o_read = tail[9];  // the softmax warps read the item's O tile
   ItemRing& ring = *reinterpret_cast<ItemRing*>(smem + kDqOffRing);
   uint32_t& tmem_base_s = *reinterpret_cast<uint32_t*>(smem + kDqOffMisc);
   int& abort_s = *reinterpret_cast<int*>(smem + kDqOffMisc + 4);
@@ -218,6 +219,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&bar_dq_free, 256);
     mbar_init(&bar_dp_read, 256);
     for (int qq = 0; qq < 4; ++qq) mbar_init(&bar_delta[qq], 2);
+    mbar_init(&bar_o_read, 8);
     abort_s = 0;
     fence_mbar_init();
   }
@@ -241,7 +243,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   if (warp == 0) {
     regs_dec<kDqRegsCtl>();
     // ------------------------------------------------------------ producer
-    uint32_t kv = 0, qn = 0, pub = 0;
+    // kv counts tiles (the V ring); kk counts entries of the K ring, which
+    // carries each item's O tile (read once, for Delta) ahead of its K tiles.
+    uint32_t kv = 0, kk = 0, qn = 0, pub = 0;
+    auto k_slot_free = [&](uint32_t e) {
+      return e < kDqKStages ||
+             warp_wait(&bar_k_empty[e % kDqKStages], ((e / kDqKStages) & 1) ^ 1, abort, p.status);
+    };
     // The next item is taken once every load of this one is issued (taking
     // it earlier can leave two long items on one CTA).
     // Items are published with their header (q-tile, tile range) so the
@@ -270,10 +278,20 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       }
       __syncwarp();
       ++qn;
-      for (int t = beg; t < end; ++t, ++kv) {
+      if (!(ok = k_slot_free(kk))) break;
+      if (lane == 0) {
+        const uint32_t so = kk % kDqKStages;
+        uint8_t* dst = smem + kDqOffK + so * kTileBytes;
+        mbar_arrive_expect_tx(&bar_k_full[so], kTileBytes);
+        tma_load_3d(dst, &map_o, &bar_k_full[so], 0, h, qt * 128);
+        tma_load_3d(dst + kHalfBytes, &map_o, &bar_k_full[so], 64, h, qt * 128);
+      }
+      __syncwarp();
+      ++kk;
+      for (int t = beg; t < end; ++t, ++kv, ++kk) {
         const int row0 = p.qt_kt[t] * 128;
-        const uint32_t sk = kv % kDqKStages, pk = (kv / kDqKStages) & 1;
-        if (kv >= kDqKStages && !(ok = warp_wait(&bar_k_empty[sk], pk ^ 1, abort, p.status))) break;
+        const uint32_t sk = kk % kDqKStages;
+        if (!(ok = k_slot_free(kk))) break;
         if (lane == 0) {
           uint8_t* dst = smem + kDqOffK + sk * kTileBytes;
           // the tile's 128 key bounds travel with it (key_end is padded to
@@ -310,19 +328,20 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
     if (!ok && lane == 0) {
       if (qn > 0) mbar_drain(&bar_q_full, (qn - 1) & 1);
-      for (uint32_t i = kv >= kDqKStages ? kv - kDqKStages : 0; i <= kv; ++i) {
+      for (uint32_t i = kk >= kDqKStages ? kk - kDqKStages : 0; i <= kk; ++i)
         mbar_drain(&bar_k_full[i % kDqKStages], (i / kDqKStages) & 1);
+      for (uint32_t i = kv >= kDqVStages ? kv - kDqVStages : 0; i <= kv; ++i)
         mbar_drain(&bar_v_full[i % kDqVStages], (i / kDqVStages) & 1);
-      }
     }
   } else if (warp == 1) {
     regs_dec<kDqRegsCtl>();
     // ---------------------------------------------------------- MMA issuer
-    // Per item: S_0, dP_0, S_1; then per tile t: [dP_t read] dP_{t+1};
-    // [dS_t] dQ += dS_t K_t, S_{t+2} (into the S buffer dQ_t just read).
+    // Per item: S_0, dP_0, [O read] release of the O entry, S_1; then per
+    // tile t: [dP_t read] dP_{t+1}; [dS_t] dQ += dS_t K_t, S_{t+2} (into the S
+    // buffer dQ_t just read).
     const uint32_t aQ = smem_u32(smem + kDqOffQ), aDO = smem_u32(smem + kDqOffDO);
     const uint32_t aK = smem_u32(smem + kDqOffK), aV = smem_u32(smem + kDqOffV);
-    uint32_t kv = 0, qn = 0, n = 0, got = 0;
+    uint32_t kv = 0, kk = 0, qn = 0, n = 0, got = 0;
     bool ok = true;
     int hdr[3];
     for (int cur; (ok = item_get(&ring, got, cur, abort, p.status, hdr)) && cur >= 0;) {
@@ -337,23 +356,32 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       auto wait_v = [&](uint32_t i) {
         return warp_wait(&bar_v_full[i % kDqVStages], (i / kDqVStages) & 1, abort, p.status);
       };
-      if (!(ok = wait_k(kv))) break;
+      // K ring: the item's O tile at entry eo, its K tiles from eo + 1. The
+      // O entry is waited for like a K tile so this warp keeps step with
+      // every phase of the ring.
+      const uint32_t eo = kk;
+      if (!(ok = wait_k(eo))) break;
+      if (!(ok = wait_k(eo + 1))) break;
       tc_fence_after_sync();
-      mma_kk(tS, aQ, k_stage(kv), 0);  // S_0
+      mma_kk(tS, aQ, k_stage(eo + 1), 0);  // S_0
       mma_commit_warp(&bar_s_full[0]);
       if (!(ok = wait_v(kv))) break;
       tc_fence_after_sync();
       mma_kk(tDP, aDO, v_stage(kv), 0);  // dP_0
       mma_commit_warp(&bar_dp_full);
       mma_commit_warp(&bar_v_empty[kv % kDqVStages]);
+      // the O entry's slot is free once every softmax warp has read it
+      if (!(ok = warp_wait(&bar_o_read, (qn - 1) & 1, abort, p.status))) break;
+      if (lane == 0) mbar_arrive(&bar_k_empty[eo % kDqKStages]);
+      __syncwarp();
       if (T > 1) {
-        if (!(ok = wait_k(kv + 1))) break;
+        if (!(ok = wait_k(eo + 2))) break;
         tc_fence_after_sync();
-        mma_kk(tS + 128, aQ, k_stage(kv + 1), 0);  // S_1
+        mma_kk(tS + 128, aQ, k_stage(eo + 2), 0);  // S_1
         mma_commit_warp(&bar_s_full[1]);
       }
       for (int t = 0; t < T && ok; ++t, ++n) {
-        const uint32_t i = kv + t;
+        const uint32_t i = kv + t, ik = eo + 1 + t;  // V ring, K ring
         // dP_{t+1} as soon as the softmax warps hold dP_t, ahead of dQ_t
         if (t + 1 < T) {
           if (!(ok = warp_wait(&bar_dp_read, n & 1, abort, p.status))) break;
@@ -371,19 +399,20 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (t == 0 && qn > 1 && !(ok = warp_wait(&bar_dq_free, (qn - 2) & 1, abort, p.status)))
           break;
         tc_fence_after_sync();
-        mma_tn_split(tDQ, tS + (t & 1) * 128, k_stage(i), t > 0);  // dQ += dS_t K_t
-        mma_commit_warp(&bar_k_empty[i % kDqKStages]);
+        mma_tn_split(tDQ, tS + (t & 1) * 128, k_stage(ik), t > 0);  // dQ += dS_t K_t
+        mma_commit_warp(&bar_k_empty[ik % kDqKStages]);
         if (t + 1 == T) mma_commit_warp(&bar_dq_full);
         if (T == 1) mma_commit_warp(&bar_q_empty);  // the softmax warps read dO for Delta
                                                     // before the first dS arrives
         if (t + 2 < T) {
-          if (!(ok = wait_k(i + 2))) break;
+          if (!(ok = wait_k(ik + 2))) break;
           tc_fence_after_sync();
-          mma_kk(tS + (t & 1) * 128, aQ, k_stage(i + 2), 0);  // S_{t+2}
+          mma_kk(tS + (t & 1) * 128, aQ, k_stage(ik + 2), 0);  // S_{t+2}
           mma_commit_warp(&bar_s_full[t & 1]);
         }
       }
       kv += T;
+      kk += T + 1;
     }
     mma_commit_warp(&bar_final);
     mbar_drain(&bar_final, 0);
@@ -401,7 +430,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t col0 = half * 64;
     const float sl2 = p.scale_log2;
-    uint32_t n = 0, qn = 0, su[2] = {0, 0};
+    uint32_t n = 0, kk = 0, qn = 0, su[2] = {0, 0};  // kk: K ring entries (O, then K tiles)
     bool ok = true;
     // The next item's q-tile and tile range are read one item ahead, and each
     // tile's kind and k-tile one tile ahead, so no global load latency sits
@@ -409,8 +438,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     int hdr[3] = {0, 0, 0};  // the next item's q-tile and tile range, from the ring
     int nt_kind = 0, nt_kt = 0, nt_at = -1;
     auto fetch_tile = [&](int t) {
-      nt_kind = __ldg(p.qt_kind + t);
-      nt_kt = __ldg(p.qt_kt + t);
+      nt_kind = ldg_pinned(p.qt_kind + t);
+      nt_kt = ldg_pinned(p.qt_kt + t);
       nt_at = t;
     };
     // The next item's number is read once this item's tiles are done (the
@@ -419,30 +448,18 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     uint32_t got = 0;
     int cur = -1;
     ok = item_get(&ring, got, cur, abort, p.status, hdr);
-    // The loads an item's Delta needs are issued as soon as the item is known
-    // (right after the previous item's last tile), so their latency passes
-    // during the previous epilogue. The two warps of a row quarter split its
-    // 32 rows, 16 each (warps 4-7 the first 16): a row per instruction (lane l:
-    // dims 4l..4l+3, one contiguous 256-byte row; rows past N read the last
-    // row and count zero), and the thread's lse.
-    uint2 ov[16];
+    // The thread's lse is loaded as soon as the item is known (right after
+    // the previous item's last tile), so its latency passes during the
+    // previous epilogue.
     float lse_pre = INFINITY;
-    auto load_o = [&](int item) {
-      const int r0 = hdr[0] * 128 + quarter * 32 + half * 16, hh = item % p.hq;
-      const int nvalid = min(16, p.N - r0);
-      const __nv_bfloat16* obase = p.o + (static_cast<size_t>(r0) * p.hq + hh) * 128 + 4 * lane;
-      const size_t ostride = static_cast<size_t>(p.hq) * 128;
-#pragma unroll
-      for (int rr = 0; rr < 16; ++rr)
-        ov[rr] = nvalid > 0 ? __ldg(reinterpret_cast<const uint2*>(obase + min(rr, nvalid - 1) * ostride))
-                            : make_uint2(0u, 0u);
+    auto load_lse = [&](int item) {
       const int ii = hdr[0] * 128 + r;
-      lse_pre = ii < p.N ? __ldg(p.lse + static_cast<size_t>(hh) * p.N + ii) : INFINITY;
+      lse_pre = ii < p.N ? __ldg(p.lse + static_cast<size_t>(item % p.hq) * p.N + ii) : INFINITY;
     };
-    if (ok && cur >= 0) load_o(cur);
+    if (ok && cur >= 0) load_lse(cur);
     auto next_item = [&](int& nxt) -> bool {
       if (!item_get(&ring, got, nxt, abort, p.status, hdr)) return false;
-      if (nxt >= 0) load_o(nxt);
+      if (nxt >= 0) load_lse(nxt);
       return true;
     };
     while (ok && cur >= 0) {
@@ -451,28 +468,40 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const int i = qt * 128 + r;
       const size_t row = static_cast<size_t>(i) * p.hq + h;
       if (!(ok = warp_wait(&bar_q_full, qn & 1, abort, p.status))) break;
-      // Delta = dO . O of this thread's row. Each lane forms its part of the
-      // warp's 16 dot products (its 4 dims of O, loaded ahead, and of dO in
-      // smem); a transposing reduction leaves row 2m's sum in lanes 2m and
-      // 2m+1; the two warps of the quarter swap halves through smem.
+      // the item's O tile, in the K ring ahead of its K tiles
+      if (!(ok = warp_wait(&bar_k_full[kk % kDqKStages], (kk / kDqKStages) & 1, abort, p.status)))
+        break;
+      // Delta = dO . O of this thread's row. The two warps of a row quarter
+      // split its 32 rows, 16 each (warps 4-7 the first 16). Each lane forms
+      // its part of the warp's 16 dot products (lane l: dims 4l..4l+3 of O
+      // and dO, both 128B-swizzled tiles in smem; rows past N count zero); a
+      // transposing reduction leaves row 2m's sum in lanes 2m and 2m+1; the
+      // two warps of the quarter swap halves through smem.
       float delta = 0.f, lse2 = INFINITY;
       {
         float part[16];
         const int r0 = qt * 128 + quarter * 32 + half * 16;
-        const uint8_t* dbase = smem + kDqOffDO + (lane >> 4) * kHalfBytes + (lane & 1) * 8;
+        const uint32_t lane_byte = (lane >> 4) * kHalfBytes + (lane & 1) * 8;
+        const uint8_t* dbase = smem + kDqOffDO + lane_byte;
+        const uint8_t* obase = smem + kDqOffK + (kk % kDqKStages) * kTileBytes + lane_byte;
         const int chunk = (lane >> 1) & 7;
         const int nvalid = min(16, p.N - r0);
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
           const int rt = quarter * 32 + half * 16 + rr;  // row within the tile
-          const uint2 dv = *reinterpret_cast<const uint2*>(dbase + rt * 128 + ((chunk ^ (rt & 7)) * 16));
-          const float2 o01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov[rr].x));
-          const float2 o23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov[rr].y));
+          const uint32_t off = rt * 128 + ((chunk ^ (rt & 7)) * 16);
+          const uint2 dv = *reinterpret_cast<const uint2*>(dbase + off);
+          const uint2 ov = *reinterpret_cast<const uint2*>(obase + off);
+          const float2 o01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov.x));
+          const float2 o23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov.y));
           const float2 d01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dv.x));
           const float2 d23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dv.y));
           const float acc = fmaf(o01.x, d01.x, fmaf(o01.y, d01.y, fmaf(o23.x, d23.x, o23.y * d23.y)));
           part[rr] = rr < nvalid ? acc : 0.f;
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_o_read);  // the O entry's slot may be refilled
+        ++kk;
 #pragma unroll
         for (int st = 0; st < 4; ++st) {
           const int k = 16 >> st;  // lanes with bit k keep the upper half of the rows
@@ -499,7 +528,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       }
       ++qn;
       if (nt_at != beg) fetch_tile(beg);
-      for (int t = beg; t < end; ++t, ++n) {
+      for (int t = beg; t < end; ++t, ++n, ++kk) {
         const int kd = nt_kind, kt = nt_kt;
         if (t + 1 < end) fetch_tile(t + 1);
         // What this warp's 32 rows x 64 keys of the tile hold: 1 every pair
@@ -512,9 +541,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (kd == 1) {  // PARTIAL: the tile's key bounds arrived with its K stage
           // (the stage is refilled only after this tile's dQ product, which
           // waits for every softmax thread's dS)
-          if (!(ok = warp_wait(&bar_k_full[n % kDqKStages], (n / kDqKStages) & 1, abort, p.status)))
+          if (!(ok = warp_wait(&bar_k_full[kk % kDqKStages], (kk / kDqKStages) & 1, abort, p.status)))
             break;
-          ke = reinterpret_cast<const int*>(smem + kDqOffKe + (n % kDqKStages) * 512) + col0;
+          ke = reinterpret_cast<const int*>(smem + kDqOffKe + (kk % kDqKStages) * 512) + col0;
           int mn = min(ke[lane], ke[lane + 32]), mx = max(ke[lane], ke[lane + 32]);
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) {

@@ -112,13 +112,31 @@ struct TileInfo {
   int kev[4];
 };
 
-__device__ __forceinline__ TileInfo load_tile(const FwdParams& p, int t, int s, int lane) {
-  TileInfo x;
-  x.kind = (kinds_at(p, t) >> (2 * s)) & 3;
-  x.kt = __ldg(p.list_kt + t);
-#pragma unroll
-  for (int c = 0; c < 4; ++c) x.kev[c] = __ldg(p.key_end + x.kt * 128 + lane + 32 * c);
+// A tile's kind and k-tile, loaded two tiles ahead; its key bounds, which
+// need the k-tile, one tile ahead (no dependent load inside a tile's time).
+struct TileHead {
+  int kind, kt;
+};
+
+__device__ __forceinline__ TileHead load_head(const FwdParams& p, int t, int s) {
+  TileHead x;
+  const int k = ldg_pinned(p.list_kind + t);
+  x.kind = ((p.mode == 0 ? (k | (k << 2)) : k) >> (2 * s)) & 3;
+  x.kt = ldg_pinned(p.list_kt + t);
   return x;
+}
+
+__device__ __forceinline__ TileInfo complete_tile(const FwdParams& p, TileHead h, int lane) {
+  TileInfo x;
+  x.kind = h.kind;
+  x.kt = h.kt;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) x.kev[c] = ldg_pinned(p.key_end + x.kt * 128 + lane + 32 * c);
+  return x;
+}
+
+__device__ __forceinline__ TileInfo load_tile(const FwdParams& p, int t, int s, int lane) {
+  return complete_tile(p, load_head(p, t, s), lane);
 }
 
 // (a wait that gives up records the line it was called from)
@@ -386,7 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int cur = -1;
     ok = item_get(&ring, got, cur, abort, p.status, hdr);
     if (ok && cur >= 0) fetch_header(cur);
-    TileInfo nt;
+    TileInfo nt;      // the next tile
+    TileHead nn{};    // the one after it
     int nt_at = -1;
     while (ok && cur >= 0) {
       const int qt = n_qt, h = n_h, beg = n_beg, end = n_end;
@@ -398,13 +417,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int i = qt * 128 + r;
       float m_ref = -INFINITY, l = 0.f;
-      if (nt_at != beg) nt = load_tile(p, beg, s, lane);
+      if (nt_at != beg) {
+        nt = load_tile(p, beg, s, lane);
+        if (beg + 1 < end) nn = load_head(p, beg + 1, s);
+      }
       for (int t = beg; t < end; ++t) {
         const TileInfo tl = nt;
         if (t + 1 < end) {
           nt_at = t + 1;
-          nt = load_tile(p, nt_at, s, lane);
+          nt = complete_tile(p, nn, lane);
         }
+        if (t + 2 < end) nn = load_head(p, t + 2, s);
         const int kd = tl.kind;
         if (kd == 0) continue;
         const int kt = tl.kt;
@@ -535,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fetch_header(nxt);
         nt_at = n_beg;
         nt = load_tile(p, nt_at, s, lane);
+        if (n_beg + 1 < n_end) nn = load_head(p, n_beg + 1, s);
       }
       // ---- epilogue: O / l and lse
       if (!(ok = warp_wait(&bar_o_full[s], oc & 1, abort, p.status))) break;
