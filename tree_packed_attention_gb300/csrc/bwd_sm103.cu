@@ -108,6 +108,17 @@ __device__ __forceinline__ void store_row(void* dst_base, size_t off, int c, con
   }
 }
 
+// 32 bytes to global memory: one 32-byte store if the destination is 32-byte
+// aligned (v8), else two 16-byte stores.
+__device__ __forceinline__ void store32(void* dst, const uint32_t (&w)[8], int v8) {
+  if (v8) {
+    st_global_v8(dst, w);
+  } else {
+    reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
 // ============================================================== dQ kernel
 // 384 threads: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps 4-11
 // one q row per thread, two warpgroups splitting the keys of each tile.
@@ -466,7 +477,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const int qt = hdr[0], h = cur % p.hq, beg = hdr[1], end = hdr[2];
       int nxt = -1;
       const int i = qt * 128 + r;
-      const size_t row = static_cast<size_t>(i) * p.hq + h;
       if (!(ok = warp_wait(&bar_q_full, qn & 1, abort, p.status))) break;
       // the item's O tile, in the K ring ahead of its K tiles
       if (!(ok = warp_wait(&bar_k_full[kk % kDqKStages], (kk / kDqKStages) & 1, abort, p.status)))
@@ -621,17 +631,51 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       }
       if (!ok) break;
       if (!(ok = next_item(nxt))) break;
-      // epilogue: dq = scale * dQ, this half's 64 columns
+      // epilogue: dq = scale * dQ, this half's 64 columns. Once they are in
+      // registers the accumulator is free for the next item; chunks are then
+      // exchanged within lane groups (exchange_chunks) so each store
+      // instruction writes whole 128- or 256-byte pieces of rows.
       if (!(ok = warp_wait(&bar_dq_full, (qn - 1) & 1, abort, p.status))) break;
       tc_fence_after_sync();
+      {
+        uint32_t v[64];
+        tmem_ld64(tDQ + lane_off + col0, v);
+        tc_fence_before_sync();
+        mbar_arrive(&bar_dq_free);
+        const int rq = qt * 128 + quarter * 32;  // the warp's first row
+        if (!p.out_f32) {  // 4 chunks of 16 bf16 columns, groups of 4 lanes
+          uint32_t pk[4][8];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tDQ + lane_off + col0 + c * 32, v);
-        if (i < p.N) store_row(p.dq, row * 128, half * 2 + c, v, p.scale, p.out_f32, p.out_v8);
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              pk[c][e] = pack_bf16x2(__uint_as_float(v[16 * c + 2 * e]) * p.scale,
+                                     __uint_as_float(v[16 * c + 2 * e + 1]) * p.scale);
+          exchange_chunks<4>(pk, lane);
+          const int i0 = rq + (lane & ~3), pos = lane & 3;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if (i0 + k >= p.N) continue;
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.dq) +
+                                 (static_cast<size_t>(i0 + k) * p.hq + h) * 128 + col0 + 16 * pos;
+            store32(dst, pk[k], p.out_v8);
+          }
+        } else {  // 8 chunks of 8 fp32 columns, groups of 8 lanes
+          uint32_t pk[8][8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pk[c][e] = __float_as_uint(__uint_as_float(v[8 * c + e]) * p.scale);
+          exchange_chunks<8>(pk, lane);
+          const int i0 = rq + (lane & ~7), pos = lane & 7;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            if (i0 + k >= p.N) continue;
+            float* dst = static_cast<float*>(p.dq) + (static_cast<size_t>(i0 + k) * p.hq + h) * 128 + col0 + 8 * pos;
+            store32(dst, pk[k], p.out_v8);
+          }
+        }
       }
-      tc_fence_before_sync();
-      mbar_arrive(&bar_dq_free);
       if (nxt >= 0) fetch_tile(hdr[1]);  // the next item's first tile
       cur = nxt;
     }

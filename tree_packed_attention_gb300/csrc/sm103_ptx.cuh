@@ -139,6 +139,33 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
 }
 
+// Chunk exchange for coalesced row stores. Lane j of each group of G lanes
+// (G a power of two up to 32) holds G chunks of 8 words of its own row; after
+// log2(G) xor-butterfly steps lane j holds chunk j of the group's rows, row k
+// of the group in pk[k]. A store of pk[k] by the G lanes then writes row k's
+// G chunks side by side.
+template <int G>
+__device__ __forceinline__ void exchange_chunks(uint32_t (&pk)[G][8], int lane) {
+  const int pos = lane & (G - 1);
+#pragma unroll
+  for (int m = 1; m < G; m <<= 1) {
+    const bool hi = (pos & m) != 0;
+#pragma unroll
+    for (int y0 = 0; y0 < G; ++y0) {
+      if (y0 & m) continue;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const uint32_t send = hi ? pk[y0][w] : pk[y0 | m][w];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
+        if (hi)
+          pk[y0][w] = recv;
+        else
+          pk[y0 | m][w] = recv;
+      }
+    }
+  }
+}
+
 // A read-only global load that stays where it is written: the compiler may
 // not sink it towards its first use, so its latency overlaps the work in
 // between (for values wanted a tile later).
