@@ -293,3 +293,36 @@ def test_full_size_workloads_sampled(index):
     # properties at every row and key
     for t in (o, lse, dq, dk, dv) + tuple(g16):
         assert torch.isfinite(t).all()
+
+
+@pytest.mark.parametrize("index", [4, 5])
+def test_full_size_every_element_written_and_repeatable(index):
+    """Outputs and workspace prefilled with NaN: every element of o, lse, dq, dk
+    and dv comes out finite, and a second run with fresh NaN buffers gives the
+    same bits (the backward sums in a fixed order), for both gradient dtypes.
+    A missed row, a read before a write or a race between the kernels' warps
+    shows up here at the bench's full sizes."""
+    _need_gpu()
+    w = treegen.workload(index)
+    N, hq, hkv, D = w.num_tokens, w.hq, w.hkv, w.head_dim
+    q, k, v, do = (x.cuda() for x in treegen.draw_tensors(N, hq, hkv, D, w.dtype, 0))
+    plan = tpa.tree_plan_build(w.parents, w.lengths)
+    nan = float("nan")
+    for gdt in (torch.float32, torch.bfloat16):
+        runs = []
+        for _ in range(2):
+            o = torch.full_like(q, nan)
+            lse = torch.full((hq, N), nan, device="cuda")
+            tpa.tree_attn_fwd(plan, q, k, v, out=o, lse=lse)
+            ws = torch.full((tpa.tree_attn_bwd_workspace_bytes(plan, hq, D, q.dtype) // 4 + 4,), nan,
+                            device="cuda")
+            grads = tuple(torch.full(x.shape, nan, dtype=gdt, device="cuda") for x in (q, k, v))
+            tpa.tree_attn_bwd(plan, do, q, k, v, o, lse, grad_dtype=gdt, workspace=ws.view(torch.uint8),
+                              out=grads)
+            tpa.tree_status_sync()
+            outs = (o, lse) + grads
+            for name, t in zip(("o", "lse", "dq", "dk", "dv"), outs):
+                assert torch.isfinite(t).all(), f"{name} ({gdt}): {int((~torch.isfinite(t)).sum())} elements not finite"
+            runs.append(outs)
+        for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), *runs):
+            assert torch.equal(a, b), f"{name} ({gdt}) differs between two runs"
