@@ -126,7 +126,8 @@ __device__ __forceinline__ void store32(void* dst, const uint32_t (&w)[8], int v
 // S buffer it came from and read by the dQ MMA from TMEM.
 constexpr int kDqThreads = 384;
 // K_t is read by S_t and, a step later, by dQ_t; S_{t+2} is issued right after
-// dQ_t, so K needs a third stage for its load to overlap a whole step.
+// dQ_t, so K needs a third stage for its load to overlap a whole step. The
+// same ring carries each item's O tile (for Delta) ahead of its K tiles.
 constexpr int kDqKStages = 3;
 // Launched at 168 registers a thread; warps 0-3 drop to 72 and the softmax
 // warpgroups rise to 216 (128 x 72 + 256 x 216 = 384 x 168).
