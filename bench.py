@@ -77,14 +77,30 @@ def _traffic(workload: str, kernel: str):
     return rec.get("dram_bytes_per_launch")
 
 
-def _dist():
+def _dist(backend: str = "nccl"):
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws > 1:
         import torch.distributed as dist
 
-        dist.init_process_group("nccl")
+        dist.init_process_group(backend)
         return dist, dist.get_rank(), ws
     return None, 0, 1
+
+
+def max_over_ranks(x: float, dist, device="cpu") -> float:
+    """The largest of every rank's x: a job of replicas is as slow as its slowest one."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, work_per_replica: float, ms: float) -> float:
+    """Units per second over all replicas, each doing work_per_replica in (max) ms."""
+    return world * work_per_replica / (ms * 1e-3)
 
 
 class ClockSampler:
@@ -296,12 +312,9 @@ def gpu_arm(args):
     kv_ms = [e[2].elapsed_time(e[3]) for e in ev]
     bwd_ms = [a + b for a, b in zip(dq_ms, kv_ms)]
     step_ms = statistics.mean(f + b for f, b in zip(fwd_ms, bwd_ms))
-    if dist:
-        t = torch.tensor([step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
-    value = world * (flops_fwd + flops_bwd) / (step_ms * 1e-3) / 1e12
-    tokens_s = world * N / (step_ms * 1e-3)
+    step_ms = max_over_ranks(step_ms, dist, dev)
+    value = whole_job_rate(world, flops_fwd + flops_bwd, step_ms) / 1e12
+    tokens_s = whole_job_rate(world, N, step_ms)
 
     # End to end through the public API with pinned host buffers. Every step
     # copies its inputs host->device, runs forward and backward, and copies
@@ -359,11 +372,8 @@ def gpu_arm(args):
     torch.cuda.synchronize()
     e2e_ms = 1e3 * (time.perf_counter() - t_e2e) / e2e_steps
     tpa.tree_status_sync()
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * (flops_fwd + flops_bwd) / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    e2e_value = whole_job_rate(world, flops_fwd + flops_bwd, e2e_ms) / 1e12
 
     peaks, peak_kind = _peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
