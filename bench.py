@@ -49,6 +49,7 @@ def _peaks():
 # DRAM bytes per launch from an ncu capture, kept only while the kernel's
 # sources still hash to what they were when the counters were taken.
 KERNEL_SOURCES = {
+    "tree_rope_kernel": ("rope.cu",),
     "tree_attn_fwd_sm103": ("fwd_sm103.cu", "sm103_ptx.cuh"),
     "tree_attn_bwd_dq_sm103": ("bwd_sm103.cu", "sm103_ptx.cuh"),
     "tree_attn_bwd_dkdv_sm103": ("bwd_sm103.cu", "sm103_ptx.cuh"),
@@ -427,6 +428,60 @@ def gpu_arm(args):
         dist.destroy_process_group()
 
 
+def rope_arm(args):
+    """--op rope: tree RoPE (position ids of eq. 9) applied in place to the
+    workload's q and k, bf16, one GPU. HBM-bound: every element is read and
+    written once, so the figure is algorithmic bytes / event time against the
+    measured copy bandwidth."""
+    import torch
+
+    import treegen
+    import tree_packed_attention_gb300 as tpa
+
+    torch.cuda.set_device(0)
+    w = treegen.workload(args.workload)
+    N, hq, hkv, D = w.num_tokens, w.hq, w.hkv, w.head_dim
+    plan = tpa.tree_plan_build(w.parents, w.lengths)
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    q = torch.randn(N, hq, D, device="cuda", generator=gen).to(torch.bfloat16)
+    k = torch.randn(N, hkv, D, device="cuda", generator=gen).to(torch.bfloat16)
+    stream = torch.cuda.current_stream()
+    plan.to_device(stream)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    nbytes = 2 * (q.numel() + k.numel()) * q.element_size()  # read and write each element once
+    for _ in range(args.warmup):
+        tpa.tree_rope(plan, q)
+        tpa.tree_rope(plan, k)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(0) as clocks:
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            tpa.tree_rope(plan, q)
+            tpa.tree_rope(plan, k)
+            b.record(stream)
+        torch.cuda.synchronize()
+    tpa.tree_status_sync()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peaks, kind = _peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    traffic = _traffic(w.name, "tree_rope_kernel")
+    print(json.dumps({
+        "metric": "tree RoPE at eq. 9 position ids, q and k in place, GB/s on 1 GB300", "value": gbs,
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "tokens": N, "hq": hq, "hkv": hkv, "head_dim": D,
+                   "l2": "inputs larger than L2, and L2 flushed between steps"},
+        "roofline": {"bound": "hbm", "kernel": "tree_rope_kernel", "achieved": gbs, "peak": peak,
+                     "unit": "GB/s", "frac": gbs / peak, "peak_source": f"{kind} copy bandwidth",
+                     "traffic": traffic},  # the step's two launches together
+        "bytes_per_step": nbytes, "clocks": clocks.summary(), "gpu_launches": 2 * args.steps,
+    }))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -435,8 +490,12 @@ def main():
     ap.add_argument("--workload", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="attention", choices=["attention", "rope"],
+                    help="attention (the default and the headline) or rope (tree RoPE on q and k)")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.op == "rope":
+        rope_arm(args)
+    elif args.impl == "reference":
         reference_arm(args)
     else:
         gpu_arm(args)

@@ -222,6 +222,38 @@ tree_status_t tree_attn_bwd_static_scratch(const tree_plan_t* plan, const void* 
  * Weights"), each rounded once to fp32, into host memory out_host[N]. */
 tree_status_t tree_weights(const tree_plan_t* plan, float* out_host);
 
+/* Per-token weights for any path weighting (§3.1, after eq. 5: with path
+ * weights w_k, token t carries lambda_t = sum of w_k over the paths k through
+ * it; w_k = 1/K of the trie gives tree_weights). path_weights_host has one
+ * fp64 weight per root-to-leaf path of the whole forest, TREE_FIELD_TRIE_PATHS
+ * summed; paths are numbered by their leaf segments in DFS order (the order
+ * the leaves' tokens appear in the layout). The sums are formed in fp64 and
+ * each lambda_t is rounded once to fp32 into host memory out_host[N].
+ * Errors: NULL pointers (with N > 0), num_paths different from the forest's
+ * path count, or a non-finite weight -> TREE_ERR_INVALID_ARG. */
+tree_status_t tree_weights_paths(const tree_plan_t* plan, const double* path_weights_host,
+                                 int32_t num_paths, float* out_host);
+
+/* Rotary position embedding at tree position ids, in place on the device
+ * tensor x[N, heads, head_dim] (token-major, the plan's DFS token order,
+ * contiguous, 16-byte aligned, bf16 or fp32 by dtype). Token t takes the
+ * position TREE_FIELD_POS_ID[t] of §3.2 "Position Embedding" (eq. 9), the one
+ * it has in every standalone root-to-leaf sequence, so the result equals
+ * RoPE (RoFormer, Su et al. 2023) applied to each path on its own.
+ *  - Dimension pair i turns by pos * base^(-2i/head_dim): pairs (2i, 2i+1)
+ *    when rotate_half = 0, pairs (i, i + head_dim/2) when rotate_half = 1.
+ *  - inverse = 1 turns by the opposite angle: the backward of the forward
+ *    rotation (grad_x = R^T grad_y) and its exact inverse up to rounding.
+ *  - Arithmetic in fp32 (angle reduced in fp64); bf16 results rounded once.
+ * Asynchronous on `stream`; the plan must be on the current device.
+ * Errors: head_dim odd or above 128 -> TREE_ERR_UNSUPPORTED; heads <= 0, a bad
+ * dtype, base not finite and positive, rotate_half or inverse not 0/1, NULL
+ * or misaligned x -> TREE_ERR_INVALID_ARG; plan not on the device ->
+ * TREE_ERR_NOT_ON_DEVICE. */
+tree_status_t tree_rope(const tree_plan_t* plan, void* x, int32_t heads, int32_t head_dim,
+                        tree_dtype_t dtype, float base, int32_t rotate_half, int32_t inverse,
+                        tree_stream_t stream);
+
 /* Wait for `stream`, then read and clear the device status word of the
  * current device: TREE_ERR_TIMEOUT if a kernel gave up a bounded wait since
  * the last check (the message names the wait: 10000 + source line in the

@@ -4,8 +4,9 @@ A plain, slow, fp64 restatement of what tree-packed attention computes, written
 from "Tree Training: Accelerating Agentic LLMs Training via Shared Prefix Reuse"
 (arXiv 2511.00413): the trie and DFS serialization (§3.1, eq. 7-8), the tree
 attention mask (§3.2 "Attention Mask"; App. A.1), tree position ids (§3.2
-eq. 9), the per-token loss weight g_n/K (§3.1 eq. 2-4; §3.2 "Loss Weights")
-and plain masked-softmax attention with its analytic backward.
+eq. 9) and RoPE at them, the per-token loss weight g_n/K (§3.1 eq. 2-4; §3.2
+"Loss Weights") and its general form for any path weights, and plain
+masked-softmax attention with its analytic backward.
 
 Only the test suite, the package's smoke check and the benchmark's CPU
 baseline leg may import this package. It shares no code with the CUDA path
@@ -20,6 +21,9 @@ Modules:
   tiles     -- tile visibility map by brute-force counting, the backward
                row ranges, work lists and orders
   attention -- fp64 forward (o, lse) and analytic backward (dq, dk, dv)
+  rope      -- rotary position embedding at the eq. 9 position ids
+               (§3.2 "Position Embedding"); trie.path_weight_tokens gives the
+               general per-token weights lambda_t of §3.1 for any path weights
 
 Parity pins: every function here is pinned by a ``-m "not gpu"`` test in
 ``tests/test_oracle_*.py`` against the pages' worked numbers, closed forms,

@@ -208,6 +208,26 @@ def token_weights(parents, lengths):
     return w.astype(np.float32)
 
 
+def path_weight_tokens(parents, lengths, path_weights):
+    """§3.1 after eq. 5: with path weights w_k, lambda_t = sum of w_k over the
+    paths k that contain token t, per DFS token, summed in fp64 and rounded
+    once to fp32. Paths are numbered by their leaves in DFS order (the order
+    the leaves' tokens appear in the layout), each enumerated explicitly as its
+    list of segments, root first."""
+    parents, lengths = validate(parents, lengths)
+    order, _ = dfs_serialize(parents, lengths)
+    leaf_set = set(leaves(parents))
+    dfs_leaves = [s for s in order if s in leaf_set]
+    w = np.asarray(path_weights, dtype=np.float64)
+    assert w.shape == (len(dfs_leaves),)
+    lam = [0.0] * len(parents)
+    for k, leaf in enumerate(dfs_leaves):
+        for seg in ancestors(parents, leaf) + [leaf]:
+            lam[seg] += float(w[k])
+    tok = token_segments(parents, lengths)
+    return np.array([lam[s] for s in tok], dtype=np.float64).astype(np.float32)
+
+
 def por(n_tree: float, n_base: float) -> float:
     """eq. 12: Potential Overlap Ratio = 1 - N_tree / N_Xbase(root)."""
     return 1.0 - n_tree / n_base

@@ -140,3 +140,55 @@ def test_device_calls_without_device_copy_are_rejected():
     assert tpa.lib.tree_attn_bwd_workspace_bytes(plan.handle, 2, 128, 1) == 2 * 2 * 128 * 4
     # fp32 workspace: Delta [hq, N], rounded up to 256 bytes
     assert tpa.lib.tree_attn_bwd_workspace_bytes(plan.handle, 2, 64, 0) == 256
+
+
+def _dfs_leaf_count(parents, lengths):
+    order, _ = T.dfs_serialize(parents, lengths)
+    leaf_set = set(T.leaves(parents))
+    return sum(1 for s in order if s in leaf_set)
+
+
+@pytest.mark.parametrize("index,seed", [(1, 0), (3, 0), (4, 0), (5, 0), (1, 2)])
+def test_path_weights_match_the_oracle(index, seed):
+    w = treegen.workload(index, seed)
+    plan = tpa.tree_plan_build(w.parents, w.lengths)
+    nk = _dfs_leaf_count(w.parents, w.lengths)
+    pw = np.random.default_rng(seed + 100).uniform(-1.0, 3.0, nk)
+    got = tpa.tree_weights_paths(plan, pw)
+    ref = T.path_weight_tokens(w.parents, w.lengths, pw)
+    # same fp64 additions in the same order, one rounding to fp32
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_path_weights_of_random_forests_match_the_oracle():
+    rng = np.random.default_rng(11)
+    for _ in range(20):
+        S = int(rng.integers(1, 40))
+        parents = [-1] + [int(rng.integers(-1, s)) for s in range(1, S)]
+        lengths = [int(x) for x in rng.integers(1, 300, S)]
+        plan = tpa.tree_plan_build(parents, lengths)
+        pw = rng.standard_normal(_dfs_leaf_count(parents, lengths))
+        got = tpa.tree_weights_paths(plan, pw)
+        assert np.array_equal(got.view(np.uint32), T.path_weight_tokens(parents, lengths, pw).view(np.uint32))
+
+
+def test_path_weights_and_rope_validate_their_arguments():
+    plan = tpa.tree_plan_build([-1, 0, 0], [4, 3, 5])  # two paths
+    with pytest.raises(tpa.TreeAttnError) as e:
+        tpa.tree_weights_paths(plan, [1.0, 2.0, 3.0])
+    assert e.value.status == 1 and "2 paths" in str(e.value)
+    with pytest.raises(tpa.TreeAttnError):
+        tpa.tree_weights_paths(plan, [1.0, float("nan")])
+    # tree_rope: checks that need no device (the last argument is the stream)
+    lib = tpa.lib
+    assert lib.tree_rope(None, 16, 2, 64, 1, 10000.0, 0, 0, None) == 1
+    assert lib.tree_rope(plan.handle, 16, 2, 63, 1, 10000.0, 0, 0, None) == 5  # odd head_dim
+    assert lib.tree_rope(plan.handle, 16, 2, 130, 1, 10000.0, 0, 0, None) == 5  # above 128
+    assert lib.tree_rope(plan.handle, 16, 0, 64, 1, 10000.0, 0, 0, None) == 1  # heads
+    assert lib.tree_rope(plan.handle, 16, 2, 64, 7, 10000.0, 0, 0, None) == 1  # dtype
+    assert lib.tree_rope(plan.handle, 16, 2, 64, 1, 0.0, 0, 0, None) == 1  # base
+    assert lib.tree_rope(plan.handle, 16, 2, 64, 1, float("inf"), 0, 0, None) == 1
+    assert lib.tree_rope(plan.handle, 16, 2, 64, 1, 10000.0, 2, 0, None) == 1  # rotate_half
+    assert lib.tree_rope(plan.handle, 16, 2, 64, 1, 10000.0, 0, 3, None) == 1  # inverse
+    assert lib.tree_rope(plan.handle, None, 2, 64, 1, 10000.0, 0, 0, None) == 1  # NULL x
+    assert lib.tree_rope(plan.handle, 20, 2, 64, 1, 10000.0, 0, 0, None) == 1  # misaligned

@@ -26,7 +26,8 @@ from ._lib import (DTYPE_BF16, DTYPE_F32, EXPORTS, FIELDS, LIB_PATH, PlanInfo, T
 __all__ = [
     "Plan", "tree_plan_build", "tree_attn_fwd", "tree_attn_bwd", "tree_attn_bwd_dq",
     "tree_attn_bwd_dkdv", "tree_attn_bwd_workspace_bytes",
-    "tree_weights", "tree_status_sync", "TreeAttnFn", "tree_attention", "TreeAttnError",
+    "tree_weights", "tree_weights_paths", "tree_rope", "tree_rope_apply", "TreeRopeFn",
+    "tree_status_sync", "TreeAttnFn", "tree_attention", "TreeAttnError",
     "FIELDS", "EXPORTS", "LIB_PATH",
 ]
 
@@ -225,6 +226,36 @@ def tree_weights(plan: Plan) -> np.ndarray:
     return out
 
 
+def tree_weights_paths(plan: Plan, path_weights) -> np.ndarray:
+    """Per-token weights lambda_t = sum of the weights of the paths through t (fp32, host).
+
+    ``path_weights`` holds one weight per root-to-leaf path of the forest, the
+    paths numbered by their leaves in DFS order."""
+    w = np.ascontiguousarray(path_weights, dtype=np.float64)
+    out = np.empty(plan.num_tokens, dtype=np.float32)
+    check(lib.tree_weights_paths(plan.handle, w.ctypes.data, int(w.size), out.ctypes.data))
+    return out
+
+
+def tree_rope(plan: Plan, x, base: float = 10000.0, rotate_half: bool = False,
+              inverse: bool = False, stream=None):
+    """Rotary embedding of x[N, H, D] (bf16 or fp32, on the GPU) at the plan's
+    tree position ids, in place; returns x. ``inverse`` applies the backward."""
+    import torch
+
+    if x.dim() != 3 or x.shape[0] != plan.num_tokens:
+        raise ValueError(f"x must be [N={plan.num_tokens}, H, D], got {tuple(x.shape)}")
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError(f"x must be bf16 or fp32, got {x.dtype}")
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    s = _stream_ptr(stream)
+    plan.to_device(s)
+    check(lib.tree_rope(plan.handle, x.data_ptr(), x.shape[1], x.shape[2], _dtype_code(x),
+                        float(base), int(bool(rotate_half)), int(bool(inverse)), s))
+    return x
+
+
 def tree_status_sync(stream=None) -> None:
     """Wait for the stream; raise if a kernel gave up a bounded wait."""
     check(lib.tree_status_sync(_stream_ptr(stream)))
@@ -254,6 +285,34 @@ def _make_autograd():
 
 
 TreeAttnFn = _make_autograd()
+
+
+def _make_rope_autograd():
+    import torch
+
+    class TreeRopeFn(torch.autograd.Function):
+        """Autograd wrapper: the forward rotates a copy of x, the backward applies
+        the inverse rotation to the incoming gradient; both run the library's kernel."""
+
+        @staticmethod
+        def forward(ctx, x, plan, base=10000.0, rotate_half=False):
+            ctx.plan, ctx.base, ctx.rotate_half = plan, base, rotate_half
+            return tree_rope(plan, x.contiguous().clone(), base, rotate_half)
+
+        @staticmethod
+        def backward(ctx, gy):
+            gx = tree_rope(ctx.plan, gy.contiguous().clone(), ctx.base, ctx.rotate_half, inverse=True)
+            return gx, None, None, None
+
+    return TreeRopeFn
+
+
+TreeRopeFn = _make_rope_autograd()
+
+
+def tree_rope_apply(x, plan: Plan, base: float = 10000.0, rotate_half: bool = False):
+    """Differentiable tree RoPE (returns a rotated copy of x)."""
+    return TreeRopeFn.apply(x, plan, base, rotate_half)
 
 
 def tree_attention(q, k, v, plan: Plan, softmax_scale: float = 0.0):

@@ -37,7 +37,7 @@ EXPORTS = [
     "tree_plan_build", "tree_plan_info", "tree_plan_get", "tree_plan_field_len",
     "tree_plan_to_device", "tree_plan_destroy", "tree_attn_fwd", "tree_attn_bwd_workspace_bytes",
     "tree_attn_bwd", "tree_attn_bwd_dq", "tree_attn_bwd_dkdv", "tree_attn_bwd_static_scratch",
-    "tree_weights", "tree_status_sync",
+    "tree_weights", "tree_weights_paths", "tree_rope", "tree_status_sync",
     "tree_last_error",
 ]
 
@@ -81,6 +81,8 @@ def _load():
         "tree_attn_bwd_static_scratch": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                                                i32, i32, C.c_float, vp]),
         "tree_weights": (i32, [vp, vp]),
+        "tree_weights_paths": (i32, [vp, vp, i32, vp]),
+        "tree_rope": (i32, [vp, vp, i32, i32, i32, C.c_float, i32, i32, vp]),
         "tree_status_sync": (i32, [vp]),
         "tree_last_error": (C.c_char_p, []),
     }

@@ -110,6 +110,7 @@ extern "C" tree_status_t tree_plan_to_device(tree_plan_t* p, tree_stream_t strea
       {TREE_FIELD_QP_KT, &d.qp_kt},         {TREE_FIELD_QP_KIND, &d.qp_kind},
       {TREE_FIELD_QP_ORDER, &d.qp_order},   {TREE_FIELD_KT_QLO, &d.kt_qlo},
       {TREE_FIELD_KT_QHI, &d.kt_qhi},       {TREE_FIELD_BWD_ORDER, &d.bwd_order},
+      {TREE_FIELD_POS_ID, &d.pos_id},
   };
   // key_end is padded with zeros to whole 128-key tiles: the kernels copy it
   // a tile at a time, and a zero bound hides the keys past N from every row.
@@ -178,6 +179,32 @@ extern "C" tree_status_t tree_attn_fwd(const tree_plan_t* p, const void* q, cons
              static_cast<cudaStream_t>(stream), status};
   cudaError_t e = dtype == TREE_DTYPE_F32 ? launch_fwd_f32(a) : launch_fwd_bf16(a);
   if (e != cudaSuccess) return cuda_fail(e, "tree_attn_fwd launch");
+  return TREE_OK;
+}
+
+extern "C" tree_status_t tree_rope(const tree_plan_t* p, void* x, int32_t heads, int32_t head_dim,
+                                   tree_dtype_t dtype, float base, int32_t rotate_half,
+                                   int32_t inverse, tree_stream_t stream) {
+  if (!p) return fail(TREE_ERR_INVALID_ARG, "NULL plan");
+  if (heads <= 0) return fail(TREE_ERR_INVALID_ARG, "heads must be positive");
+  if (!rope_shape_ok(head_dim))
+    return fail(TREE_ERR_UNSUPPORTED, "head_dim must be even and at most 128");
+  if (dtype != TREE_DTYPE_BF16 && dtype != TREE_DTYPE_F32)
+    return fail(TREE_ERR_INVALID_ARG, "dtype must be TREE_DTYPE_BF16 or TREE_DTYPE_F32");
+  if (!std::isfinite(base) || base <= 0.f) return fail(TREE_ERR_INVALID_ARG, "base must be finite and > 0");
+  if ((rotate_half != 0 && rotate_half != 1) || (inverse != 0 && inverse != 1))
+    return fail(TREE_ERR_INVALID_ARG, "rotate_half and inverse must be 0 or 1");
+  if (p->N == 0) return TREE_OK;
+  if (!x) return fail(TREE_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!aligned16(x)) return fail(TREE_ERR_INVALID_ARG, "tensor pointer must be 16-byte aligned");
+  if (static_cast<int64_t>(p->N) * heads * head_dim > (int64_t{1} << 40))
+    return fail(TREE_ERR_OVERFLOW, "tensor too large");
+  tree_status_t st = check_plan_on_device(p);
+  if (st != TREE_OK) return st;
+  RopeArgs a{p->dev.pos_id, x, p->N, heads, head_dim, rotate_half, inverse,
+             dtype == TREE_DTYPE_F32 ? 1 : 0, base, static_cast<cudaStream_t>(stream)};
+  cudaError_t e = launch_rope(a);
+  if (e != cudaSuccess) return cuda_fail(e, "tree_rope launch");
   return TREE_OK;
 }
 

@@ -11,6 +11,17 @@ struct SchedSlot;
 // A fresh run-time scheduler counter for one kernel launch (nullptr on error).
 SchedSlot* next_sched_slot();
 
+// Rotary position embedding at tree position ids, in place (rope.cu).
+struct RopeArgs {
+  const int32_t* pos;  // device [N]
+  void* x;             // device [N, heads, head_dim]
+  int N, heads, head_dim, rotate_half, inverse, f32;
+  float base;
+  cudaStream_t stream;
+};
+bool rope_shape_ok(int head_dim);
+cudaError_t launch_rope(const RopeArgs& a);
+
 struct AttnArgs {
   const tree_plan* plan;
   const void* q;

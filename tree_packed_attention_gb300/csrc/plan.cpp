@@ -12,6 +12,7 @@
 // each k-tile is seen by one contiguous run of q-tiles starting at its own
 // diagonal tile.
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <limits>
 #include <new>
@@ -357,6 +358,41 @@ extern "C" tree_status_t tree_weights(const tree_plan_t* p, float* out_host) {
     // correctly rounded fp32 quotient when both are below 2^24 (53 >= 2*24+2).
     out_host[t] = static_cast<float>(static_cast<double>(g[s]) / static_cast<double>(K[trie[s]]));
   }
+  return TREE_OK;
+}
+
+extern "C" tree_status_t tree_weights_paths(const tree_plan_t* p, const double* w, int32_t num_paths,
+                                           float* out_host) {
+  if (!p) return fail(TREE_ERR_INVALID_ARG, "NULL plan");
+  int64_t K_total = 0;
+  for (int32_t k : p->field[TREE_FIELD_TRIE_PATHS]) K_total += k;
+  if (num_paths != K_total)
+    return fail(TREE_ERR_INVALID_ARG, "the forest has " + std::to_string(K_total) + " paths, got " +
+                                          std::to_string(num_paths) + " weights");
+  if (p->N == 0) return TREE_OK;
+  if (!w || !out_host) return fail(TREE_ERR_INVALID_ARG, "NULL pointer");
+  for (int32_t k = 0; k < num_paths; ++k)
+    if (!std::isfinite(w[k])) return fail(TREE_ERR_INVALID_ARG, "non-finite path weight");
+  const auto& order = p->field[TREE_FIELD_DFS_ORDER];
+  const auto& start = p->field[TREE_FIELD_SEG_START];
+  const auto& sub_end = p->field[TREE_FIELD_SUBTREE_END];
+  const auto& anc_ptr = p->field[TREE_FIELD_ANC_PTR];
+  const auto& anc_idx = p->field[TREE_FIELD_ANC_IDX];
+  const auto& seg = p->field[TREE_FIELD_TOKEN_SEG];
+  // A segment is a leaf when its subtree holds nothing past its own tokens;
+  // leaves meet in DFS order, which numbers the paths. Each path adds its
+  // weight to its leaf and to every ancestor of it.
+  std::vector<int32_t> len(p->S, 0);
+  for (int32_t t = 0; t < p->N; ++t) ++len[seg[t]];
+  std::vector<double> lam(p->S, 0.0);
+  int32_t k = 0;
+  for (int32_t s : order) {
+    if (sub_end[s] != start[s] + len[s]) continue;
+    lam[s] += w[k];
+    for (int32_t a = anc_ptr[s]; a < anc_ptr[s + 1]; ++a) lam[anc_idx[a]] += w[k];
+    ++k;
+  }
+  for (int32_t t = 0; t < p->N; ++t) out_host[t] = static_cast<float>(lam[seg[t]]);
   return TREE_OK;
 }
 

@@ -33,6 +33,7 @@ struct DevicePlan {
   const int32_t* kt_qlo = nullptr;     // [Tk]
   const int32_t* kt_qhi = nullptr;     // [Tk]
   const int32_t* bwd_order = nullptr;  // [Tk]
+  const int32_t* pos_id = nullptr;     // [N]
 };
 
 }  // namespace treeattn
