@@ -482,6 +482,34 @@ def rope_arm(args):
     }))
 
 
+def partition_arm(args):
+    """--op partition: the host partition planner (§3.3) on the workload at a
+    token cap; no GPU. Reports the partitions, their lower bound and the peak
+    tokens along a chain of partitions, with the planner's time."""
+    import treegen
+    import tree_packed_attention_gb300 as tpa
+
+    w = treegen.workload(args.workload)
+    plan = tpa.tree_plan_build(w.parents, w.lengths)
+    N = plan.num_tokens
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        r = tpa.tree_partition(plan, args.cap)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    tries = int(plan.info["num_tries"])
+    print(json.dumps({
+        "metric": "node-boundary partitions under a token cap (host planner)", "value": r["num_parts"],
+        "unit": "partitions", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": False, "vs_baseline": None, "data": "synthetic",
+        "config": {"workload": w.name, "tokens": N, "cap_tokens": args.cap, "tries": tries},
+        "lower_bound": max(-(-N // args.cap), tries), "peak_path_tokens": r["peak_path_tokens"],
+        "largest_partition": int(r["tokens"].max()) if r["num_parts"] else 0,
+        "planner_ms": 1e3 * statistics.median(times),
+    }))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -490,11 +518,15 @@ def main():
     ap.add_argument("--workload", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="attention", choices=["attention", "rope"],
-                    help="attention (the default and the headline) or rope (tree RoPE on q and k)")
+    ap.add_argument("--op", default="attention", choices=["attention", "rope", "partition"],
+                    help="attention (the default and the headline), rope (tree RoPE on q and k) "
+                         "or partition (the host planner, no GPU)")
+    ap.add_argument("--cap", type=int, default=16384, help="token cap for --op partition")
     args = ap.parse_args()
     if args.op == "rope":
         rope_arm(args)
+    elif args.op == "partition":
+        partition_arm(args)
     elif args.impl == "reference":
         reference_arm(args)
     else:

@@ -234,6 +234,37 @@ tree_status_t tree_weights(const tree_plan_t* plan, float* out_host);
 tree_status_t tree_weights_paths(const tree_plan_t* plan, const double* path_weights_host,
                                  int32_t num_paths, float* out_host);
 
+/* One partition of the redundancy-free tree partitioning (§3.3
+ * "Partitioning"; App. B). A partition is a connected piece of one trie, cut
+ * only at node boundaries, processed as one DFS forward pass. */
+typedef struct {
+  int32_t root;       /* segment at the top of the partition */
+  int32_t parent;     /* partition holding the root's parent segment; -1 at a trie root */
+  int64_t tokens;     /* tokens of the partition's own segments (at most the cap) */
+  int64_t pos_offset; /* App. B.4 eq. 17: position id of the root's first token */
+  int64_t past_len;   /* App. B.2 gateway length: the parent's past_len plus the parent's DFS
+                         tokens up to and including the cut node (the root's parent); 0 at a
+                         trie root */
+} tree_partition_t;
+
+/* Partition the forest into the fewest connected pieces of at most cap_tokens
+ * tokens each, cutting only between a segment and its parent (§3.3
+ * "Partitioning": node-boundary cuts keep the partitions' dependency graph a
+ * tree). Bottom-up, each segment keeps its children's uncut remainders and,
+ * while its total exceeds the cap, cuts off the heaviest one (ties: the
+ * lowest segment id) -- the greedy of Kundu and Misra (1977), optimal for the
+ * number of pieces. Outputs (host memory):
+ *  - part_of_segment[S]: the partition of each segment;
+ *  - parts[S] (the first *num_parts used): partitions numbered by their roots
+ *    in DFS order, so a parent partition precedes its children;
+ *  - *peak_path_tokens: the largest sum of partition sizes along a chain of
+ *    parent partitions (what the backward keeps alive at once, §3.3).
+ * Errors: NULL pointers (S > 0) or cap_tokens < 1 -> TREE_ERR_INVALID_ARG; a
+ * segment longer than cap_tokens -> TREE_ERR_UNSUPPORTED (no node-boundary
+ * partition exists). */
+tree_status_t tree_partition(const tree_plan_t* plan, int64_t cap_tokens, int32_t* part_of_segment,
+                             tree_partition_t* parts, int32_t* num_parts, int64_t* peak_path_tokens);
+
 /* Rotary position embedding at tree position ids, in place on the device
  * tensor x[N, heads, head_dim] (token-major, the plan's DFS token order,
  * contiguous, 16-byte aligned, bf16 or fp32 by dtype). Token t takes the

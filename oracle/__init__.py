@@ -21,6 +21,9 @@ Modules:
   tiles     -- tile visibility map by brute-force counting, the backward
                row ranges, work lists and orders
   attention -- fp64 forward (o, lse) and analytic backward (dq, dk, dv)
+  partition -- node-boundary partitions under a token cap by brute force,
+               their validity, App. B.2 gateway lengths and B.4 eq. 17
+               position offsets, peak tokens along a path (§3.3)
   rope      -- rotary position embedding at the eq. 9 position ids
                (§3.2 "Position Embedding"); trie.path_weight_tokens gives the
                general per-token weights lambda_t of §3.1 for any path weights

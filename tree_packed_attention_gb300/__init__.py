@@ -20,13 +20,14 @@ import ctypes as C
 
 import numpy as np
 
-from ._lib import (DTYPE_BF16, DTYPE_F32, EXPORTS, FIELDS, LIB_PATH, PlanInfo, TreeAttnError,
-                   check, lib)
+from ._lib import (DTYPE_BF16, DTYPE_F32, EXPORTS, FIELDS, LIB_PATH, PartitionRec, PlanInfo,
+                   TreeAttnError, check, lib)
 
 __all__ = [
     "Plan", "tree_plan_build", "tree_attn_fwd", "tree_attn_bwd", "tree_attn_bwd_dq",
     "tree_attn_bwd_dkdv", "tree_attn_bwd_workspace_bytes",
-    "tree_weights", "tree_weights_paths", "tree_rope", "tree_rope_apply", "TreeRopeFn",
+    "tree_weights", "tree_weights_paths", "tree_partition", "tree_rope", "tree_rope_apply",
+    "TreeRopeFn",
     "tree_status_sync", "TreeAttnFn", "tree_attention", "TreeAttnError",
     "FIELDS", "EXPORTS", "LIB_PATH",
 ]
@@ -234,6 +235,26 @@ def tree_weights_paths(plan: Plan, path_weights) -> np.ndarray:
     w = np.ascontiguousarray(path_weights, dtype=np.float64)
     out = np.empty(plan.num_tokens, dtype=np.float32)
     check(lib.tree_weights_paths(plan.handle, w.ctypes.data, int(w.size), out.ctypes.data))
+    return out
+
+
+def tree_partition(plan: Plan, cap_tokens: int) -> dict:
+    """Fewest node-boundary partitions of at most ``cap_tokens`` tokens (§3.3).
+
+    Returns part_of_segment [S], and per partition (parents first) root,
+    parent, tokens, pos_offset and past_len, plus num_parts and
+    peak_path_tokens."""
+    S = plan.info["num_segments"]
+    part = np.empty(max(S, 1), dtype=np.int32)
+    recs = (PartitionRec * max(S, 1))()
+    n = C.c_int32()
+    peak = C.c_int64()
+    check(lib.tree_partition(plan.handle, int(cap_tokens), part.ctypes.data, recs, C.byref(n),
+                             C.byref(peak)))
+    k = n.value
+    out = {"part_of_segment": part[:S].copy(), "num_parts": k, "peak_path_tokens": peak.value}
+    for name in ("root", "parent", "tokens", "pos_offset", "past_len"):
+        out[name] = np.array([getattr(recs[i], name) for i in range(k)], dtype=np.int64)
     return out
 
 

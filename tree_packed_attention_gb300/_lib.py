@@ -37,7 +37,7 @@ EXPORTS = [
     "tree_plan_build", "tree_plan_info", "tree_plan_get", "tree_plan_field_len",
     "tree_plan_to_device", "tree_plan_destroy", "tree_attn_fwd", "tree_attn_bwd_workspace_bytes",
     "tree_attn_bwd", "tree_attn_bwd_dq", "tree_attn_bwd_dkdv", "tree_attn_bwd_static_scratch",
-    "tree_weights", "tree_weights_paths", "tree_rope", "tree_status_sync",
+    "tree_weights", "tree_weights_paths", "tree_partition", "tree_rope", "tree_status_sync",
     "tree_last_error",
 ]
 
@@ -54,6 +54,11 @@ class TreeAttnError(RuntimeError):
         super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
         self.status = status
         self.status_name = STATUS_NAMES.get(status, str(status))
+
+
+class PartitionRec(C.Structure):
+    _fields_ = [("root", C.c_int32), ("parent", C.c_int32), ("tokens", C.c_int64),
+                ("pos_offset", C.c_int64), ("past_len", C.c_int64)]
 
 
 def _load():
@@ -82,6 +87,7 @@ def _load():
                                                i32, i32, C.c_float, vp]),
         "tree_weights": (i32, [vp, vp]),
         "tree_weights_paths": (i32, [vp, vp, i32, vp]),
+        "tree_partition": (i32, [vp, i64, vp, vp, C.POINTER(i32), C.POINTER(i64)]),
         "tree_rope": (i32, [vp, vp, i32, i32, i32, C.c_float, i32, i32, vp]),
         "tree_status_sync": (i32, [vp]),
         "tree_last_error": (C.c_char_p, []),

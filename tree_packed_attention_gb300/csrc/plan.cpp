@@ -396,4 +396,81 @@ extern "C" tree_status_t tree_weights_paths(const tree_plan_t* p, const double* 
   return TREE_OK;
 }
 
+extern "C" tree_status_t tree_partition(const tree_plan_t* p, int64_t cap, int32_t* part_of,
+                                       tree_partition_t* parts, int32_t* num_parts,
+                                       int64_t* peak_path_tokens) {
+  if (!p) return fail(TREE_ERR_INVALID_ARG, "NULL plan");
+  if (cap < 1) return fail(TREE_ERR_INVALID_ARG, "cap_tokens must be at least 1");
+  if (!num_parts || !peak_path_tokens) return fail(TREE_ERR_INVALID_ARG, "NULL output");
+  *num_parts = 0;
+  *peak_path_tokens = 0;
+  const int32_t S = p->S;
+  if (S == 0) return TREE_OK;
+  if (!part_of || !parts) return fail(TREE_ERR_INVALID_ARG, "NULL output");
+  const auto& order = p->field[TREE_FIELD_DFS_ORDER];
+  const auto& anc_ptr = p->field[TREE_FIELD_ANC_PTR];
+  const auto& anc_idx = p->field[TREE_FIELD_ANC_IDX];
+  const auto& seg = p->field[TREE_FIELD_TOKEN_SEG];
+  const auto& start = p->field[TREE_FIELD_SEG_START];
+  const auto& pos = p->field[TREE_FIELD_POS_ID];
+  std::vector<int64_t> len(S, 0);
+  for (int32_t t = 0; t < p->N; ++t) ++len[seg[t]];
+  std::vector<int32_t> parent(S);
+  for (int32_t v = 0; v < S; ++v) parent[v] = anc_ptr[v + 1] > anc_ptr[v] ? anc_idx[anc_ptr[v + 1] - 1] : -1;
+  for (int32_t v = 0; v < S; ++v)
+    if (len[v] > cap)
+      return fail(TREE_ERR_UNSUPPORTED, "segment " + std::to_string(v) + " has " + std::to_string(len[v]) +
+                                            " tokens, above the cap of " + std::to_string(cap));
+  std::vector<std::vector<int32_t>> children(S);
+  for (int32_t v = 0; v < S; ++v)
+    if (parent[v] >= 0) children[parent[v]].push_back(v);  // ascending id
+  // bottom-up: residual[v] = tokens of v's piece below and at v (uncut part)
+  std::vector<int64_t> residual(S, 0);
+  std::vector<char> is_root(S, 0);
+  for (int32_t e = S - 1; e >= 0; --e) {  // reverse DFS order: children first
+    const int32_t v = order[e];
+    int64_t total = len[v];
+    for (int32_t c : children[v]) total += residual[c];
+    while (total > cap) {
+      int32_t best = -1;
+      for (int32_t c : children[v])
+        if (!is_root[c] && (best < 0 || residual[c] > residual[best])) best = c;
+      is_root[best] = 1;  // len[v] <= cap, so an uncut child remains while total > cap
+      total -= residual[best];
+    }
+    residual[v] = total;
+    if (parent[v] < 0) is_root[v] = 1;
+  }
+  // number the partitions by their roots in DFS order; run[] counts each
+  // partition's DFS tokens so far (its DFS sequence is the global one restricted)
+  std::vector<int64_t> run, upto(S, 0);
+  int32_t n = 0;
+  for (int32_t v : order) {
+    if (is_root[v]) {
+      tree_partition_t& q = parts[n];
+      q.root = v;
+      q.parent = parent[v] < 0 ? -1 : part_of[parent[v]];
+      q.tokens = 0;
+      q.pos_offset = pos[start[v]];
+      q.past_len = q.parent < 0 ? 0 : parts[q.parent].past_len + upto[parent[v]];
+      part_of[v] = n++;
+      run.push_back(0);
+    } else {
+      part_of[v] = part_of[parent[v]];
+    }
+    run[part_of[v]] += len[v];
+    upto[v] = run[part_of[v]];
+    parts[part_of[v]].tokens += len[v];
+  }
+  std::vector<int64_t> chain(n, 0);
+  int64_t peak = 0;
+  for (int32_t i = 0; i < n; ++i) {  // parents have smaller numbers
+    chain[i] = parts[i].tokens + (parts[i].parent >= 0 ? chain[parts[i].parent] : 0);
+    peak = chain[i] > peak ? chain[i] : peak;
+  }
+  *num_parts = n;
+  *peak_path_tokens = peak;
+  return TREE_OK;
+}
+
 extern "C" const char* tree_last_error(void) { return g_last_error.c_str(); }
