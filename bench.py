@@ -482,6 +482,65 @@ def rope_arm(args):
     }))
 
 
+def conv_arm(args):
+    """--op conv: the tree-correct causal conv (App. A.3) forward and backward
+    on the workload's tokens, bf16, K = 4, SiLU, C = --channels. Memory-bound:
+    the figure is the algorithmic bytes (forward reads x and writes y; the
+    backward reads x and dy and writes dx) over the CUDA-event time."""
+    import torch
+
+    import treegen
+    import tree_packed_attention_gb300 as tpa
+
+    torch.cuda.set_device(0)
+    w = treegen.workload(args.workload)
+    plan = tpa.tree_plan_build(w.parents, w.lengths)
+    N, C, K = plan.num_tokens, args.channels, 4
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    x = torch.randn(N, C, device="cuda", generator=gen).to(torch.bfloat16)
+    dy = torch.randn(N, C, device="cuda", generator=gen).to(torch.bfloat16)
+    wt = torch.randn(C, K, device="cuda", generator=gen) * 0.5
+    b = torch.randn(C, device="cuda", generator=gen)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    y = torch.empty_like(x)
+    for _ in range(args.warmup):
+        tpa.tree_conv_fwd(plan, x, wt, b, out=y)
+        tpa.tree_conv_bwd(plan, x, wt, b, dy)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(0) as clocks:
+        for e in ev:
+            flush.zero_()
+            e[0].record(stream)
+            tpa.tree_conv_fwd(plan, x, wt, b, out=y)
+            e[1].record(stream)
+            tpa.tree_conv_bwd(plan, x, wt, b, dy)
+            e[2].record(stream)
+        torch.cuda.synchronize()
+    tpa.tree_status_sync()
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    row = C * x.element_size()
+    fwd_bytes, bwd_bytes = 2 * N * row, 3 * N * row
+    gbs = (fwd_bytes + bwd_bytes) / ((fwd_ms + bwd_ms) * 1e-3) / 1e9
+    peaks, kind = _peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    print(json.dumps({
+        "metric": "tree-correct causal conv (K=4, SiLU) forward+backward, algorithmic GB/s on 1 GB300",
+        "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": fwd_ms + bwd_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": N, "channels": C, "kernel_size": K,
+                   "l2": "inputs larger than L2, and L2 flushed between steps"},
+        "fwd": {"ms": fwd_ms, "gbs": fwd_bytes / (fwd_ms * 1e-3) / 1e9},
+        "bwd": {"ms": bwd_ms, "gbs": bwd_bytes / (bwd_ms * 1e-3) / 1e9},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "peak_source": f"{kind} copy bandwidth", "traffic": None},
+        "clocks": clocks.summary(), "gpu_launches": 5 * args.steps,
+    }))
+
+
 def partition_arm(args):
     """--op partition: the host partition planner (§3.3) on the workload at a
     token cap; no GPU. Reports the partitions, their lower bound and the peak
@@ -518,13 +577,16 @@ def main():
     ap.add_argument("--workload", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="attention", choices=["attention", "rope", "partition"],
-                    help="attention (the default and the headline), rope (tree RoPE on q and k) "
-                         "or partition (the host planner, no GPU)")
+    ap.add_argument("--op", default="attention", choices=["attention", "rope", "conv", "partition"],
+                    help="attention (the default and the headline), rope (tree RoPE on q and k), "
+                         "conv (the tree-correct causal conv) or partition (the host planner, no GPU)")
+    ap.add_argument("--channels", type=int, default=4096, help="channels for --op conv")
     ap.add_argument("--cap", type=int, default=16384, help="token cap for --op partition")
     args = ap.parse_args()
     if args.op == "rope":
         rope_arm(args)
+    elif args.op == "conv":
+        conv_arm(args)
     elif args.op == "partition":
         partition_arm(args)
     elif args.impl == "reference":

@@ -265,6 +265,46 @@ typedef struct {
 tree_status_t tree_partition(const tree_plan_t* plan, int64_t cap_tokens, int32_t* part_of_segment,
                              tree_partition_t* parts, int32_t* num_parts, int64_t* peak_path_tokens);
 
+/* Tree-correct causal depthwise convolution (App. A.3 "Tree-Correct Causal
+ * Convolution"; eq. 11): each segment takes its left context from its
+ * parent's last K-1 effective tokens, so every token sees the K-1 tokens
+ * before it on its own root-to-leaf path (zeros before the root), as in a
+ * standalone per-path forward:
+ *   y[t, c] = act(bias[c] + sum_{k=0}^{K-1} weight[c, K-1-k] x[pred_k(t), c]),
+ * pred_0(t) = t and pred_k(t) the k-th token before t on its path (weight
+ * index K-1 on the token itself, the causal conv1d convention).
+ * Tensors are token-major in the plan's DFS order: x, y, dy, dx [N, channels]
+ * (bf16 or fp32 by dtype, 16-byte aligned); weight, dweight [channels, K] and
+ * bias, dbias [channels] in fp32. Arithmetic is fp32; the backward is
+ * deterministic. activation: TREE_ACT_NONE or TREE_ACT_SILU. */
+typedef enum { TREE_ACT_NONE = 0, TREE_ACT_SILU = 1 } tree_activation_t;
+
+/* Build and upload the path-predecessor tables for kernel size K (1 to 8) on
+ * the current device; the plan keeps one kernel size at a time and frees them
+ * with the plan. Errors: K out of range -> TREE_ERR_UNSUPPORTED. */
+tree_status_t tree_conv_prepare(tree_plan_t* plan, int32_t kernel_size, tree_stream_t stream);
+
+/* y = conv(x). bias may be NULL. Errors: channels not a positive multiple of
+ * 8 -> TREE_ERR_UNSUPPORTED; NULL or misaligned pointers, a bad dtype or
+ * activation -> TREE_ERR_INVALID_ARG; tables not prepared on this device ->
+ * TREE_ERR_NOT_ON_DEVICE. */
+tree_status_t tree_conv_fwd(const tree_plan_t* plan, const void* x, const float* weight,
+                            const float* bias, void* y, int32_t channels, tree_dtype_t dtype,
+                            int32_t activation, tree_stream_t stream);
+
+/* Scratch the backward needs (fp32 dy * act'(pre) and the reduction's
+ * partial sums), for the prepared kernel size. */
+size_t tree_conv_bwd_workspace_bytes(const tree_plan_t* plan, int32_t channels);
+
+/* dx, dweight (and dbias unless NULL) of the conv, overwritten (not
+ * accumulated). The pre-activation is recomputed from x, weight and bias.
+ * Errors as tree_conv_fwd, and a workspace below
+ * tree_conv_bwd_workspace_bytes -> TREE_ERR_INVALID_ARG. */
+tree_status_t tree_conv_bwd(const tree_plan_t* plan, const void* x, const float* weight,
+                            const float* bias, const void* dy, void* dx, float* dweight,
+                            float* dbias, int32_t channels, tree_dtype_t dtype, int32_t activation,
+                            void* workspace, size_t workspace_bytes, tree_stream_t stream);
+
 /* Rotary position embedding at tree position ids, in place on the device
  * tensor x[N, heads, head_dim] (token-major, the plan's DFS token order,
  * contiguous, 16-byte aligned, bf16 or fp32 by dtype). Token t takes the

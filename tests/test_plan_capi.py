@@ -192,3 +192,18 @@ def test_path_weights_and_rope_validate_their_arguments():
     assert lib.tree_rope(plan.handle, 16, 2, 64, 1, 10000.0, 0, 3, None) == 1  # inverse
     assert lib.tree_rope(plan.handle, None, 2, 64, 1, 10000.0, 0, 0, None) == 1  # NULL x
     assert lib.tree_rope(plan.handle, 20, 2, 64, 1, 10000.0, 0, 0, None) == 1  # misaligned
+
+
+def test_conv_validates_its_arguments():
+    plan = tpa.tree_plan_build([-1, 0], [5, 7])
+    lib = tpa.lib
+    assert lib.tree_conv_prepare(None, 4, None) == 1
+    assert lib.tree_conv_prepare(plan.handle, 0, None) == 5  # kernel size out of range
+    assert lib.tree_conv_prepare(plan.handle, 9, None) == 5
+    # checks that need no device: channels, dtype, activation
+    args = (16, 16, None, 16)  # x, weight, bias, y
+    assert lib.tree_conv_fwd(None, *args, 8, 1, 1, None) == 1
+    assert lib.tree_conv_fwd(plan.handle, *args, 12, 1, 1, None) == 5  # not a multiple of 8
+    assert lib.tree_conv_fwd(plan.handle, *args, 8, 5, 1, None) == 1  # dtype
+    assert lib.tree_conv_fwd(plan.handle, *args, 8, 1, 2, None) == 1  # activation
+    assert lib.tree_conv_bwd_workspace_bytes(plan.handle, 8) == 0  # nothing prepared yet

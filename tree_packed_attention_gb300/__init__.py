@@ -20,14 +20,14 @@ import ctypes as C
 
 import numpy as np
 
-from ._lib import (DTYPE_BF16, DTYPE_F32, EXPORTS, FIELDS, LIB_PATH, PartitionRec, PlanInfo,
-                   TreeAttnError, check, lib)
+from ._lib import (ACT_NONE, ACT_SILU, DTYPE_BF16, DTYPE_F32, EXPORTS, FIELDS, LIB_PATH,
+                   PartitionRec, PlanInfo, TreeAttnError, check, lib)
 
 __all__ = [
     "Plan", "tree_plan_build", "tree_attn_fwd", "tree_attn_bwd", "tree_attn_bwd_dq",
     "tree_attn_bwd_dkdv", "tree_attn_bwd_workspace_bytes",
     "tree_weights", "tree_weights_paths", "tree_partition", "tree_rope", "tree_rope_apply",
-    "TreeRopeFn",
+    "TreeRopeFn", "tree_conv_fwd", "tree_conv_bwd", "tree_conv", "TreeConvFn",
     "tree_status_sync", "TreeAttnFn", "tree_attention", "TreeAttnError",
     "FIELDS", "EXPORTS", "LIB_PATH",
 ]
@@ -258,6 +258,60 @@ def tree_partition(plan: Plan, cap_tokens: int) -> dict:
     return out
 
 
+def _conv_prepare(plan: Plan, kernel_size: int, stream):
+    s = _stream_ptr(stream)
+    plan.to_device(s)
+    check(lib.tree_conv_prepare(plan.handle, int(kernel_size), s))
+    return s
+
+
+def _conv_check(plan: Plan, x, weight, bias):
+    import torch
+
+    if x.dim() != 2 or x.shape[0] != plan.num_tokens or not x.is_contiguous():
+        raise ValueError(f"x must be contiguous [N={plan.num_tokens}, C], got {tuple(x.shape)}")
+    C = x.shape[1]
+    if weight.dtype != torch.float32 or weight.dim() != 2 or weight.shape[0] != C or not weight.is_contiguous():
+        raise ValueError("weight must be contiguous fp32 [C, K]")
+    if bias is not None and (bias.dtype != torch.float32 or bias.shape != (C,)):
+        raise ValueError("bias must be fp32 [C]")
+    return C, weight.shape[1]
+
+
+def tree_conv_fwd(plan: Plan, x, weight, bias=None, activation: str = "silu", out=None, stream=None):
+    """Tree-correct causal depthwise conv of x[N, C] (App. A.3): y[N, C]."""
+    import torch
+
+    C, K = _conv_check(plan, x, weight, bias)
+    s = _conv_prepare(plan, K, stream)
+    y = torch.empty_like(x) if out is None else out
+    act = ACT_SILU if activation == "silu" else ACT_NONE
+    check(lib.tree_conv_fwd(plan.handle, x.data_ptr(), weight.data_ptr(),
+                            bias.data_ptr() if bias is not None else None, y.data_ptr(), C,
+                            _dtype_code(x), act, s))
+    return y
+
+
+def tree_conv_bwd(plan: Plan, x, weight, bias, dy, activation: str = "silu", stream=None):
+    """(dx, dweight, dbias) of tree_conv_fwd; dbias is None when bias is None."""
+    import torch
+
+    C, K = _conv_check(plan, x, weight, bias)
+    s = _conv_prepare(plan, K, stream)
+    dy = dy.contiguous()
+    dx = torch.empty_like(x)
+    dw = torch.empty_like(weight)
+    db = torch.empty_like(bias) if bias is not None else None
+    nbytes = lib.tree_conv_bwd_workspace_bytes(plan.handle, C)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=x.device)
+    act = ACT_SILU if activation == "silu" else ACT_NONE
+    check(lib.tree_conv_bwd(plan.handle, x.data_ptr(), weight.data_ptr(),
+                            bias.data_ptr() if bias is not None else None, dy.data_ptr(),
+                            dx.data_ptr(), dw.data_ptr(), db.data_ptr() if db is not None else None,
+                            C, _dtype_code(x), act, ws.data_ptr(), ws.numel(), s))
+    return dx, dw, db
+
+
 def tree_rope(plan: Plan, x, base: float = 10000.0, rotate_half: bool = False,
               inverse: bool = False, stream=None):
     """Rotary embedding of x[N, H, D] (bf16 or fp32, on the GPU) at the plan's
@@ -329,6 +383,36 @@ def _make_rope_autograd():
 
 
 TreeRopeFn = _make_rope_autograd()
+
+
+def _make_conv_autograd():
+    import torch
+
+    class TreeConvFn(torch.autograd.Function):
+        """Autograd wrapper: forward and backward both run the library's kernels."""
+
+        @staticmethod
+        def forward(ctx, x, weight, bias, plan, activation="silu"):
+            x = x.contiguous()
+            ctx.save_for_backward(x, weight, bias)
+            ctx.plan, ctx.activation = plan, activation
+            return tree_conv_fwd(plan, x, weight, bias, activation)
+
+        @staticmethod
+        def backward(ctx, dy):
+            x, weight, bias = ctx.saved_tensors
+            dx, dw, db = tree_conv_bwd(ctx.plan, x, weight, bias, dy, ctx.activation)
+            return dx, dw, db, None, None
+
+    return TreeConvFn
+
+
+TreeConvFn = _make_conv_autograd()
+
+
+def tree_conv(x, weight, bias, plan: Plan, activation: str = "silu"):
+    """Differentiable tree-correct causal conv (App. A.3)."""
+    return TreeConvFn.apply(x, weight, bias, plan, activation)
 
 
 def tree_rope_apply(x, plan: Plan, base: float = 10000.0, rotate_half: bool = False):

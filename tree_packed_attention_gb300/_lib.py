@@ -25,6 +25,7 @@ STATUS_NAMES = {
     9: "TREE_ERR_NOT_ON_DEVICE",
 }
 DTYPE_F32, DTYPE_BF16 = 0, 1
+ACT_NONE, ACT_SILU = 0, 1
 
 FIELDS = [
     "dfs_order", "seg_start", "depth", "subtree_end", "trie_id", "g", "anc_ptr", "anc_idx",
@@ -37,7 +38,8 @@ EXPORTS = [
     "tree_plan_build", "tree_plan_info", "tree_plan_get", "tree_plan_field_len",
     "tree_plan_to_device", "tree_plan_destroy", "tree_attn_fwd", "tree_attn_bwd_workspace_bytes",
     "tree_attn_bwd", "tree_attn_bwd_dq", "tree_attn_bwd_dkdv", "tree_attn_bwd_static_scratch",
-    "tree_weights", "tree_weights_paths", "tree_partition", "tree_rope", "tree_status_sync",
+    "tree_weights", "tree_weights_paths", "tree_partition", "tree_conv_prepare", "tree_conv_fwd",
+    "tree_conv_bwd_workspace_bytes", "tree_conv_bwd", "tree_rope", "tree_status_sync",
     "tree_last_error",
 ]
 
@@ -89,6 +91,10 @@ def _load():
         "tree_weights_paths": (i32, [vp, vp, i32, vp]),
         "tree_partition": (i32, [vp, i64, vp, vp, C.POINTER(i32), C.POINTER(i64)]),
         "tree_rope": (i32, [vp, vp, i32, i32, i32, C.c_float, i32, i32, vp]),
+        "tree_conv_prepare": (i32, [vp, i32, vp]),
+        "tree_conv_fwd": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, vp]),
+        "tree_conv_bwd_workspace_bytes": (sz, [vp, i32]),
+        "tree_conv_bwd": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, sz, vp]),
         "tree_status_sync": (i32, [vp]),
         "tree_last_error": (C.c_char_p, []),
     }

@@ -156,6 +156,7 @@ extern "C" tree_status_t tree_plan_to_device(tree_plan_t* p, tree_stream_t strea
 extern "C" void tree_plan_destroy(tree_plan_t* p) {
   if (!p) return;
   free_device(p);
+  conv_tables_free(p);
   delete p;
 }
 
@@ -205,6 +206,95 @@ extern "C" tree_status_t tree_rope(const tree_plan_t* p, void* x, int32_t heads,
              dtype == TREE_DTYPE_F32 ? 1 : 0, base, static_cast<cudaStream_t>(stream)};
   cudaError_t e = launch_rope(a);
   if (e != cudaSuccess) return cuda_fail(e, "tree_rope launch");
+  return TREE_OK;
+}
+
+namespace {
+
+tree_status_t conv_check(const tree_plan_t* p, int32_t channels, tree_dtype_t dtype, int32_t activation) {
+  if (!p) return fail(TREE_ERR_INVALID_ARG, "NULL plan");
+  if (channels <= 0 || channels % 8 != 0)
+    return fail(TREE_ERR_UNSUPPORTED, "channels must be a positive multiple of 8");
+  if (dtype != TREE_DTYPE_BF16 && dtype != TREE_DTYPE_F32)
+    return fail(TREE_ERR_INVALID_ARG, "dtype must be TREE_DTYPE_BF16 or TREE_DTYPE_F32");
+  if (activation != TREE_ACT_NONE && activation != TREE_ACT_SILU)
+    return fail(TREE_ERR_INVALID_ARG, "activation must be TREE_ACT_NONE or TREE_ACT_SILU");
+  if (p->N == 0) return TREE_OK;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return fail(TREE_ERR_CUDA, "no CUDA device");
+  if (!p->conv.block || p->conv.device != cur)
+    return fail(TREE_ERR_NOT_ON_DEVICE, "call tree_conv_prepare on the current device first");
+  return TREE_OK;
+}
+
+ConvArgs conv_args(const tree_plan_t* p, const void* x, const float* weight, const float* bias,
+                   int32_t channels, tree_dtype_t dtype, int32_t activation, tree_stream_t stream) {
+  ConvArgs a{};
+  a.pred = p->conv.pred;
+  a.succ_ptr = p->conv.succ_ptr;
+  a.succ = p->conv.succ;
+  a.x = x;
+  a.weight = weight;
+  a.bias = bias;
+  a.N = p->N;
+  a.C = channels;
+  a.K = p->conv.K;
+  a.act = activation;
+  a.f32 = dtype == TREE_DTYPE_F32 ? 1 : 0;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return a;
+}
+
+}  // namespace
+
+extern "C" tree_status_t tree_conv_prepare(tree_plan_t* p, int32_t kernel_size, tree_stream_t stream) {
+  if (!p) return fail(TREE_ERR_INVALID_ARG, "NULL plan");
+  if (kernel_size < 1 || kernel_size > kConvMaxK)
+    return fail(TREE_ERR_UNSUPPORTED, "kernel_size must be 1 to " + std::to_string(kConvMaxK));
+  if (p->N >= (1 << 28)) return fail(TREE_ERR_OVERFLOW, "too many tokens for the conv tables");
+  if (p->N == 0) return TREE_OK;
+  return conv_tables_build(p, kernel_size, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" tree_status_t tree_conv_fwd(const tree_plan_t* p, const void* x, const float* weight,
+                                       const float* bias, void* y, int32_t channels,
+                                       tree_dtype_t dtype, int32_t activation, tree_stream_t stream) {
+  tree_status_t st = conv_check(p, channels, dtype, activation);
+  if (st != TREE_OK || p->N == 0) return st;
+  if (!x || !weight || !y) return fail(TREE_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned16(x) || !aligned16(y)) return fail(TREE_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
+  ConvArgs a = conv_args(p, x, weight, bias, channels, dtype, activation, stream);
+  a.y = y;
+  cudaError_t e = launch_conv_fwd(a);
+  if (e != cudaSuccess) return cuda_fail(e, "tree_conv_fwd launch");
+  return TREE_OK;
+}
+
+extern "C" size_t tree_conv_bwd_workspace_bytes(const tree_plan_t* p, int32_t channels) {
+  if (!p || channels <= 0 || p->conv.K == 0) return 0;
+  return conv_bwd_workspace(p->N, channels, p->conv.K);
+}
+
+extern "C" tree_status_t tree_conv_bwd(const tree_plan_t* p, const void* x, const float* weight,
+                                       const float* bias, const void* dy, void* dx, float* dweight,
+                                       float* dbias, int32_t channels, tree_dtype_t dtype,
+                                       int32_t activation, void* workspace, size_t workspace_bytes,
+                                       tree_stream_t stream) {
+  tree_status_t st = conv_check(p, channels, dtype, activation);
+  if (st != TREE_OK || p->N == 0) return st;
+  if (!x || !weight || !dy || !dx || !dweight || !workspace) return fail(TREE_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned16(x) || !aligned16(dy) || !aligned16(dx) || !aligned16(workspace))
+    return fail(TREE_ERR_INVALID_ARG, "x, dy, dx and workspace must be 16-byte aligned");
+  if (workspace_bytes < conv_bwd_workspace(p->N, channels, p->conv.K))
+    return fail(TREE_ERR_INVALID_ARG, "workspace too small");
+  ConvArgs a = conv_args(p, x, weight, bias, channels, dtype, activation, stream);
+  a.dy = dy;
+  a.dx = dx;
+  a.dweight = dweight;
+  a.dbias = dbias;
+  a.g = static_cast<float*>(workspace);
+  cudaError_t e = launch_conv_bwd(a);
+  if (e != cudaSuccess) return cuda_fail(e, "tree_conv_bwd launch");
   return TREE_OK;
 }
 

@@ -1,0 +1,517 @@
+// Tree-correct causal depthwise convolution.
+//
+// Tree Training (arXiv 2511.00413) App. A.3 "Tree-Correct Causal Convolution"
+// (eq. 11 in §3.2): in DFS order the K-1 tokens just before a child segment
+// belong to a sibling branch, so each segment takes its left context from its
+// parent's last K-1 effective tokens instead (and those reach further up for
+// short segments). Equivalently, token t sees its k-th predecessor on its own
+// root-to-leaf path, pred_k(t), with zeros before the root:
+//   y[t, c] = act(b[c] + sum_{k=0}^{K-1} w[c, K-1-k] x[pred_k(t), c])
+// (weight index K-1 on the token itself, as in a causal conv1d). The host
+// builds pred_k for k = 1..K-1 once per kernel size, and the inverse lists
+// (which (t, k) read token u) for the backward's gather.
+//
+// All kernels stream rows of C channels (token-major [N, C], 8 channels per
+// thread and access), so they are bound by memory bandwidth. The backward is
+// deterministic: dx gathers over the inverse lists in a fixed order, and
+// dweight / dbias reduce fixed token ranges per block and then the blocks in
+// order.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <string>
+#include <vector>
+
+#include "kernels.h"
+
+namespace treeattn {
+namespace {
+
+constexpr int kConvThreads = 256;
+constexpr int kConvPartialBlocks = 256;  // token ranges of the dweight / dbias reduction
+
+template <typename T>
+struct Vec8;
+template <>
+struct Vec8<__nv_bfloat16> {
+  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));
+      v[2 * j] = f.x;
+      v[2 * j + 1] = f.y;
+    }
+  }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&v)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+      w[j] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+template <>
+struct Vec8<float> {
+  static __device__ __forceinline__ void load(const float* p, float (&v)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+  static __device__ __forceinline__ void store(float* p, const float (&v)[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+};
+
+// A chunk of 8 channels held raw (4 registers for bf16) while its load is in
+// flight, widened to fp32 when used.
+template <typename T>
+struct RawChunk;
+template <>
+struct RawChunk<__nv_bfloat16> {
+  uint4 u;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { u = *reinterpret_cast<const uint4*>(p); }
+  __device__ __forceinline__ void widen(float (&v)[8]) const {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));
+      v[2 * j] = f.x;
+      v[2 * j + 1] = f.y;
+    }
+  }
+};
+template <>
+struct RawChunk<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* p) {
+    a = reinterpret_cast<const float4*>(p)[0];
+    b = reinterpret_cast<const float4*>(p)[1];
+  }
+  __device__ __forceinline__ void widen(float (&v)[8]) const {
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+};
+
+// SiLU and its derivative, from expf (a library call).
+__device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
+__device__ __forceinline__ float silu_grad(float z) {
+  const float s = 1.f / (1.f + expf(-z));
+  return s * (1.f + z * (1.f - s));
+}
+
+// Each thread owns one chunk of 8 channels (q) for the whole launch and keeps
+// their K weights (and biases) in registers; blocks stride over tokens, and
+// blockIdx.y picks the group of 256 chunks.
+template <int K>
+struct Taps {
+  float w[8][K];
+  __device__ __forceinline__ void load(const float* weight, int q) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int k = 0; k < K; ++k) w[j][k] = __ldg(weight + (8 * q + j) * K + k);
+  }
+};
+
+// token read by token t at distance k (k = 0 is t itself); -1 before the root
+template <int K>
+__device__ __forceinline__ int pred_of(const ConvArgs& a, int t, int k) {
+  return k == 0 ? t : __ldg(a.pred + static_cast<size_t>(t) * (K - 1) + (k - 1));
+}
+
+// The K rows token t reads, x[pred_k(t)] for k = 0..K-1, for one chunk of 8
+// channels. A thread walks a contiguous token range: when t's immediate path
+// predecessor is t-1 (inside a segment, or a first child right after its
+// parent) the window shifts by one row; otherwise it is reloaded from the
+// predecessor table (segment starts). The next token's row and predecessor
+// are loaded one token ahead.
+template <typename T, int K>
+struct Window {
+  float v[K][8];
+  __device__ __forceinline__ void reload(const ConvArgs& a, int t, int q, const float (&xt)[8]) {
+    const T* x = static_cast<const T*>(a.x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[0][j] = xt[j];
+#pragma unroll
+    for (int k = 1; k < K; ++k) {
+      const int u = pred_of<K>(a, t, k);
+      if (u < 0) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[k][j] = 0.f;  // before the root
+      } else {
+        Vec8<T>::load(x + static_cast<size_t>(u) * a.C + 8 * q, v[k]);
+      }
+    }
+  }
+  __device__ __forceinline__ void shift(const float (&xt)[8]) {
+#pragma unroll
+    for (int k = K - 1; k > 0; --k)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[k][j] = v[k - 1][j];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[0][j] = xt[j];
+  }
+  __device__ __forceinline__ void pre(const Taps<K>& tp, const float (&b)[8], float (&z)[8]) const {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) z[j] = b[j];
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) z[j] = fmaf(tp.w[j][K - 1 - k], v[k][j], z[j]);
+  }
+};
+
+// a block's contiguous token range
+__device__ __forceinline__ void token_range(const ConvArgs& a, int& t0, int& t1) {
+  const int per = (a.N + gridDim.x - 1) / gridDim.x;
+  t0 = blockIdx.x * per;
+  t1 = min(a.N, t0 + per);
+}
+
+// walks [t0, t1) calling f(t, window) with the window of token t; rows and
+// immediate predecessors of the next kConvAhead tokens are kept in flight
+constexpr int kConvAhead = 4;
+
+template <typename T, int K, typename F>
+__device__ __forceinline__ void walk(const ConvArgs& a, int q, int t0, int t1, F&& f) {
+  if (t0 >= t1) return;
+  const T* x = static_cast<const T*>(a.x);
+  RawChunk<T> ring[kConvAhead];
+  int pr[kConvAhead];
+#pragma unroll
+  for (int d = 0; d < kConvAhead; ++d) {
+    const int t = t0 + d;
+    pr[d] = -1;
+    if (t < t1) {
+      ring[d].load(x + static_cast<size_t>(t) * a.C + 8 * q);
+      pr[d] = K > 1 ? pred_of<K>(a, t, 1) : t - 1;
+    }
+  }
+  Window<T, K> win;
+  for (int tb = t0; tb < t1; tb += kConvAhead) {
+#pragma unroll
+    for (int d = 0; d < kConvAhead; ++d) {
+      const int t = tb + d;
+      if (t >= t1) break;
+      float xt[8];
+      ring[d].widen(xt);
+      const int p1 = pr[d];
+      const int tn = t + kConvAhead;  // refill this slot with a later token
+      if (tn < t1) {
+        ring[d].load(x + static_cast<size_t>(tn) * a.C + 8 * q);
+        pr[d] = K > 1 ? pred_of<K>(a, tn, 1) : tn - 1;
+      }
+      if (t > t0 && p1 == t - 1)
+        win.shift(xt);
+      else
+        win.reload(a, t, q, xt);
+      f(t, win);
+    }
+  }
+}
+
+template <typename T, int K>
+__global__ void __launch_bounds__(kConvThreads) conv_fwd_kernel(const ConvArgs a) {
+  const int q = blockIdx.y * kConvThreads + threadIdx.x;
+  if (q >= a.C / 8) return;
+  Taps<K> tp;
+  tp.load(a.weight, q);
+  float b[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) b[j] = a.bias ? __ldg(a.bias + 8 * q + j) : 0.f;
+  T* y = static_cast<T*>(a.y);
+  int t0, t1;
+  token_range(a, t0, t1);
+  walk<T, K>(a, q, t0, t1, [&](int t, const Window<T, K>& win) {
+    float z[8];
+    win.pre(tp, b, z);
+    if (a.act == 1) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) z[j] = silu(z[j]);
+    }
+    Vec8<T>::store(y + static_cast<size_t>(t) * a.C + 8 * q, z);
+  });
+}
+
+// g = dy * act'(pre), fp32, into the workspace
+template <typename T, int K>
+__global__ void __launch_bounds__(kConvThreads) conv_bwd_g_kernel(const ConvArgs a) {
+  const int q = blockIdx.y * kConvThreads + threadIdx.x;
+  if (q >= a.C / 8) return;
+  Taps<K> tp;
+  tp.load(a.weight, q);
+  float b[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) b[j] = a.bias ? __ldg(a.bias + 8 * q + j) : 0.f;
+  const T* dy = static_cast<const T*>(a.dy);
+  int t0, t1;
+  token_range(a, t0, t1);
+  if (a.act != 1) {  // g = dy
+    for (int t = t0; t < t1; ++t) {
+      float g[8];
+      Vec8<T>::load(dy + static_cast<size_t>(t) * a.C + 8 * q, g);
+      Vec8<float>::store(a.g + static_cast<size_t>(t) * a.C + 8 * q, g);
+    }
+    return;
+  }
+  walk<T, K>(a, q, t0, t1, [&](int t, const Window<T, K>& win) {
+    float z[8], g[8];
+    Vec8<T>::load(dy + static_cast<size_t>(t) * a.C + 8 * q, g);
+    win.pre(tp, b, z);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) g[j] *= silu_grad(z[j]);
+    Vec8<float>::store(a.g + static_cast<size_t>(t) * a.C + 8 * q, g);
+  });
+}
+
+// dx[u] = sum over the (t, k) that read u of w[c, K-1-k] g[t], in list order
+template <typename T, int K>
+__global__ void __launch_bounds__(kConvThreads) conv_bwd_dx_kernel(const ConvArgs a) {
+  const int q = blockIdx.y * kConvThreads + threadIdx.x;
+  if (q >= a.C / 8) return;
+  Taps<K> tp;
+  tp.load(a.weight, q);
+  T* dx = static_cast<T*>(a.dx);
+  for (int u = blockIdx.x; u < a.N; u += gridDim.x) {
+    const int e0 = __ldg(a.succ_ptr + u), e1 = __ldg(a.succ_ptr + u + 1);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int e = e0; e < e1; ++e) {
+      const int packed = __ldg(a.succ + e), t = packed >> 3, k = packed & 7;
+      float g[8];
+      Vec8<float>::load(a.g + static_cast<size_t>(t) * a.C + 8 * q, g);
+#pragma unroll
+      for (int kk = 0; kk < K; ++kk) {  // select tap k without indexing registers at run time
+        if (kk != k) continue;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = fmaf(tp.w[j][K - 1 - kk], g[j], acc[j]);
+      }
+    }
+    Vec8<T>::store(dx + static_cast<size_t>(u) * a.C + 8 * q, acc);
+  }
+}
+
+// per block: sums over its token range of g[t, c] x[pred_k(t), c] (k < K)
+// and of g[t, c]; written to the block's slice of the partial sums
+template <typename T, int K>
+__global__ void __launch_bounds__(kConvThreads) conv_bwd_dw_partial_kernel(const ConvArgs a) {
+  const int q = blockIdx.y * kConvThreads + threadIdx.x;
+  if (q >= a.C / 8) return;
+  const T* x = static_cast<const T*>(a.x);
+  int t0, t1;
+  token_range(a, t0, t1);
+  float acc[K + 1][8];
+#pragma unroll
+  for (int k = 0; k <= K; ++k)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[k][j] = 0.f;
+  for (int t = t0; t < t1; ++t) {
+    float g[8];
+    Vec8<float>::load(a.g + static_cast<size_t>(t) * a.C + 8 * q, g);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[K][j] += g[j];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int u = pred_of<K>(a, t, k);
+      if (u < 0) continue;
+      float v[8];
+      Vec8<T>::load(x + static_cast<size_t>(u) * a.C + 8 * q, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[k][j] = fmaf(g[j], v[j], acc[k][j]);
+    }
+  }
+  float* part = a.partial + static_cast<size_t>(blockIdx.x) * (K + 1) * a.C;
+#pragma unroll
+  for (int k = 0; k <= K; ++k)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) part[static_cast<size_t>(k) * a.C + 8 * q + j] = acc[k][j];
+}
+
+// dweight[c, K-1-k] and dbias[c]: the blocks' partial sums in block order
+__global__ void __launch_bounds__(kConvThreads) conv_bwd_dw_reduce_kernel(const ConvArgs a, int blocks) {
+  const int total = (a.K + 1) * a.C;
+  for (int e = blockIdx.x * kConvThreads + threadIdx.x; e < total; e += gridDim.x * kConvThreads) {
+    float s = 0.f;
+    for (int b = 0; b < blocks; ++b) s += a.partial[static_cast<size_t>(b) * total + e];
+    const int k = e / a.C, c = e % a.C;
+    if (k < a.K)
+      a.dweight[c * a.K + (a.K - 1 - k)] = s;
+    else if (a.dbias)
+      a.dbias[c] = s;
+  }
+}
+
+
+}  // namespace
+
+// pred[t][k-1] for k = 1..K-1 (-1 before the root) and the inverse lists,
+// from the plan's DFS layout; uploaded into one device block owned by the plan.
+tree_status_t conv_tables_build(tree_plan* p, int K, cudaStream_t stream) {
+  if (p->conv.block && p->conv.K == K) {
+    int cur = -1;
+    if (cudaGetDevice(&cur) == cudaSuccess && cur == p->conv.device) return TREE_OK;
+  }
+  conv_tables_free(p);
+  const int32_t N = p->N, S = p->S;
+  const auto& seg = p->field[TREE_FIELD_TOKEN_SEG];
+  const auto& start = p->field[TREE_FIELD_SEG_START];
+  const auto& anc_ptr = p->field[TREE_FIELD_ANC_PTR];
+  const auto& anc_idx = p->field[TREE_FIELD_ANC_IDX];
+  std::vector<int32_t> parent(S), len(S, 0);
+  for (int32_t t = 0; t < N; ++t) ++len[seg[t]];
+  for (int32_t s = 0; s < S; ++s) parent[s] = anc_ptr[s + 1] > anc_ptr[s] ? anc_idx[anc_ptr[s + 1] - 1] : -1;
+  const int W = K - 1;
+  std::vector<int32_t> pred(static_cast<size_t>(N) * (W > 0 ? W : 1), -1);
+  for (int32_t t = 0; t < N; ++t)
+    for (int k = 1; k <= W; ++k) {
+      int32_t u = t, m = k;  // step back m tokens along the path from u
+      while (u >= 0 && m > 0) {
+        const int32_t s = seg[u], off = u - start[s];
+        if (m <= off) {
+          u -= m;
+          m = 0;
+        } else {  // leave the segment: continue from the parent's last token
+          m -= off + 1;
+          u = parent[s] < 0 ? -1 : start[parent[s]] + len[parent[s]] - 1;
+        }
+      }
+      pred[static_cast<size_t>(t) * W + (k - 1)] = u;
+    }
+  std::vector<int32_t> ptr(N + 1, 0);
+  for (int32_t t = 0; t < N; ++t) {
+    ++ptr[t + 1];  // k = 0: itself
+    for (int k = 1; k <= W; ++k) {
+      const int32_t u = pred[static_cast<size_t>(t) * W + (k - 1)];
+      if (u >= 0) ++ptr[u + 1];
+    }
+  }
+  for (int32_t u = 0; u < N; ++u) ptr[u + 1] += ptr[u];
+  std::vector<int32_t> succ(ptr[N]), fill(ptr.begin(), ptr.end() - 1);
+  for (int32_t t = 0; t < N; ++t) {  // entries in increasing t: a fixed order
+    succ[fill[t]++] = t << 3;
+    for (int k = 1; k <= W; ++k) {
+      const int32_t u = pred[static_cast<size_t>(t) * W + (k - 1)];
+      if (u >= 0) succ[fill[u]++] = (t << 3) | k;
+    }
+  }
+  auto round256 = [](size_t b) { return (b + 255) / 256 * 256; };
+  const size_t b_pred = round256(pred.size() * 4), b_ptr = round256(ptr.size() * 4),
+               b_succ = round256(succ.size() * 4 + 4);
+  void* block = nullptr;
+  cudaError_t e = cudaMalloc(&block, b_pred + b_ptr + b_succ);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(TREE_ERR_OOM, std::string("cudaMalloc of the conv tables: ") + cudaGetErrorString(e));
+  }
+  uint8_t* base = static_cast<uint8_t*>(block);
+  e = cudaMemcpyAsync(base, pred.data(), pred.size() * 4, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(base + b_pred, ptr.data(), ptr.size() * 4, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess && !succ.empty())
+    e = cudaMemcpyAsync(base + b_pred + b_ptr, succ.data(), succ.size() * 4, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) {
+    cudaFree(block);
+    return fail(TREE_ERR_CUDA, std::string("conv table upload: ") + cudaGetErrorString(e));
+  }
+  int cur = 0;
+  cudaGetDevice(&cur);
+  p->conv.block = block;
+  p->conv.device = cur;
+  p->conv.K = K;
+  p->conv.pred = reinterpret_cast<const int32_t*>(base);
+  p->conv.succ_ptr = reinterpret_cast<const int32_t*>(base + b_pred);
+  p->conv.succ = reinterpret_cast<const int32_t*>(base + b_pred + b_ptr);
+  return TREE_OK;
+}
+
+void conv_tables_free(tree_plan* p) {
+  if (!p->conv.block) return;
+  int cur = -1;
+  cudaGetDevice(&cur);
+  if (cur != p->conv.device) cudaSetDevice(p->conv.device);
+  cudaFree(p->conv.block);
+  if (cur >= 0 && cur != p->conv.device) cudaSetDevice(cur);
+  p->conv = ConvTables{};
+}
+
+size_t conv_bwd_workspace(int N, int C, int K) {
+  return static_cast<size_t>(N) * C * 4 + static_cast<size_t>(kConvPartialBlocks) * (K + 1) * C * 4 + 256;
+}
+
+template <int K>
+void conv_fwd_k(const ConvArgs& a, dim3 grid) {
+  if (a.f32)
+    conv_fwd_kernel<float, K><<<grid, kConvThreads, 0, a.stream>>>(a);
+  else
+    conv_fwd_kernel<__nv_bfloat16, K><<<grid, kConvThreads, 0, a.stream>>>(a);
+}
+
+template <int K>
+void conv_bwd_k(const ConvArgs& a, dim3 grid, dim3 pgrid) {
+  if (a.f32) {
+    conv_bwd_g_kernel<float, K><<<grid, kConvThreads, 0, a.stream>>>(a);
+    conv_bwd_dx_kernel<float, K><<<grid, kConvThreads, 0, a.stream>>>(a);
+    conv_bwd_dw_partial_kernel<float, K><<<pgrid, kConvThreads, 0, a.stream>>>(a);
+  } else {
+    conv_bwd_g_kernel<__nv_bfloat16, K><<<grid, kConvThreads, 0, a.stream>>>(a);
+    conv_bwd_dx_kernel<__nv_bfloat16, K><<<grid, kConvThreads, 0, a.stream>>>(a);
+    conv_bwd_dw_partial_kernel<__nv_bfloat16, K><<<pgrid, kConvThreads, 0, a.stream>>>(a);
+  }
+}
+
+// blocks: groups of 256 channel chunks (y) times token strides (x), about
+// eight blocks per SM in all
+dim3 conv_grid(const ConvArgs& a) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 1;
+  const int groups = (a.C / 8 + kConvThreads - 1) / kConvThreads;
+  int tx = sms * 8 / groups;
+  tx = tx < 1 ? 1 : (tx > a.N ? a.N : tx);
+  return dim3(tx, groups);
+}
+
+cudaError_t launch_conv_fwd(const ConvArgs& a) {
+  const dim3 grid = conv_grid(a);
+  switch (a.K) {
+    case 1: conv_fwd_k<1>(a, grid); break;
+    case 2: conv_fwd_k<2>(a, grid); break;
+    case 3: conv_fwd_k<3>(a, grid); break;
+    case 4: conv_fwd_k<4>(a, grid); break;
+    case 5: conv_fwd_k<5>(a, grid); break;
+    case 6: conv_fwd_k<6>(a, grid); break;
+    case 7: conv_fwd_k<7>(a, grid); break;
+    case 8: conv_fwd_k<8>(a, grid); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_conv_bwd(ConvArgs a) {
+  a.partial = a.g + static_cast<size_t>(a.N) * a.C;
+  const dim3 grid = conv_grid(a);
+  const int pblocks = a.N < kConvPartialBlocks ? a.N : kConvPartialBlocks;
+  const dim3 pgrid(pblocks, grid.y);
+  switch (a.K) {
+    case 1: conv_bwd_k<1>(a, grid, pgrid); break;
+    case 2: conv_bwd_k<2>(a, grid, pgrid); break;
+    case 3: conv_bwd_k<3>(a, grid, pgrid); break;
+    case 4: conv_bwd_k<4>(a, grid, pgrid); break;
+    case 5: conv_bwd_k<5>(a, grid, pgrid); break;
+    case 6: conv_bwd_k<6>(a, grid, pgrid); break;
+    case 7: conv_bwd_k<7>(a, grid, pgrid); break;
+    case 8: conv_bwd_k<8>(a, grid, pgrid); break;
+    default: return cudaErrorInvalidValue;
+  }
+  const int total = (a.K + 1) * a.C;
+  const int rblocks = (total + kConvThreads - 1) / kConvThreads;
+  conv_bwd_dw_reduce_kernel<<<rblocks, kConvThreads, 0, a.stream>>>(a, pblocks);
+  return cudaGetLastError();
+}
+
+}  // namespace treeattn

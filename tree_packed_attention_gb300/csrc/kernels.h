@@ -22,6 +22,31 @@ struct RopeArgs {
 bool rope_shape_ok(int head_dim);
 cudaError_t launch_rope(const RopeArgs& a);
 
+// Tree-correct causal depthwise conv (conv.cu).
+constexpr int kConvMaxK = 8;
+struct ConvArgs {
+  const int32_t* pred;
+  const int32_t* succ_ptr;
+  const int32_t* succ;
+  const void* x;         // [N, C]
+  const float* weight;   // [C, K]
+  const float* bias;     // [C] or nullptr
+  void* y;               // forward output [N, C]
+  const void* dy;        // backward input [N, C]
+  void* dx;              // backward output [N, C]
+  float* dweight;        // [C, K]
+  float* dbias;          // [C] or nullptr
+  float* g;              // workspace: dy * act'(pre) [N, C], then the partial sums
+  float* partial;
+  int N, C, K, act, f32;
+  cudaStream_t stream;
+};
+tree_status_t conv_tables_build(tree_plan* p, int K, cudaStream_t stream);
+void conv_tables_free(tree_plan* p);
+size_t conv_bwd_workspace(int N, int C, int K);
+cudaError_t launch_conv_fwd(const ConvArgs& a);
+cudaError_t launch_conv_bwd(ConvArgs a);
+
 struct AttnArgs {
   const tree_plan* plan;
   const void* q;

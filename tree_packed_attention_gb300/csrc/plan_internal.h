@@ -36,6 +36,17 @@ struct DevicePlan {
   const int32_t* pos_id = nullptr;     // [N]
 };
 
+// Tables of the tree-correct causal conv for one kernel size (conv.cu): the
+// path predecessors of every token and their inverse lists, on one device.
+struct ConvTables {
+  int device = -1;
+  int K = 0;
+  void* block = nullptr;
+  const int32_t* pred = nullptr;      // [N, K-1]: k-th path predecessor (k = 1..K-1), -1 before the root
+  const int32_t* succ_ptr = nullptr;  // [N+1]
+  const int32_t* succ = nullptr;      // (t << 3) | k for every (t, k) with pred_k(t) = u, t increasing
+};
+
 }  // namespace treeattn
 
 struct tree_plan {
@@ -44,6 +55,7 @@ struct tree_plan {
   int64_t visible_pairs = 0;
   std::vector<int32_t> field[TREE_FIELD_COUNT];
   treeattn::DevicePlan dev;
+  treeattn::ConvTables conv;
 };
 
 namespace treeattn {
