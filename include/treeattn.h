@@ -281,7 +281,12 @@ typedef enum { TREE_ACT_NONE = 0, TREE_ACT_SILU = 1 } tree_activation_t;
 
 /* Build and upload the path-predecessor tables for kernel size K (1 to 8) on
  * the current device; the plan keeps one kernel size at a time and frees them
- * with the plan. Errors: K out of range -> TREE_ERR_UNSUPPORTED. */
+ * with the plan. Preparing another size frees the previous tables (after a
+ * device synchronization) and rebuilds them, so alternating sizes on one plan
+ * pays a rebuild each time, and a plan must not be prepared for a different
+ * size while another thread is calling tree_conv_fwd / tree_conv_bwd with it:
+ * threads that need different kernel sizes build their own plans.
+ * Errors: K out of range -> TREE_ERR_UNSUPPORTED. */
 tree_status_t tree_conv_prepare(tree_plan_t* plan, int32_t kernel_size, tree_stream_t stream);
 
 /* y = conv(x). bias may be NULL. Errors: channels not a positive multiple of

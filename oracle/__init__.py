@@ -22,8 +22,8 @@ Modules:
                row ranges, work lists and orders
   attention -- fp64 forward (o, lse) and analytic backward (dq, dk, dv)
   conv      -- the tree-correct causal depthwise conv of App. A.3 (eq. 11),
-               segment by segment with the parent's context, in torch fp64
-               so autograd gives its backward
+               written per token over its root-to-leaf path predecessors,
+               in torch fp64 so autograd gives its backward
   partition -- node-boundary partitions under a token cap by brute force,
                their validity, App. B.2 gateway lengths and B.4 eq. 17
                position offsets, peak tokens along a path (§3.3)

@@ -75,6 +75,33 @@ def test_conv_forward_and_backward_match_oracle(dtype, K):
                 assert db is None
 
 
+@pytest.mark.parametrize("C", [2056, 4096])
+def test_conv_wide_channels_use_every_channel_group(C):
+    """Channel counts past one launch row of channel groups (grid.y > 1) and,
+    for C = 2056, a last group that holds only part of its channels."""
+    _need_gpu()
+    parents, lengths = [-1, 0, 0, 1, 2, 2], [9, 5, 3, 12, 1, 7]
+    plan = tpa.tree_plan_build(parents, lengths)
+    N, K = plan.num_tokens, 4
+    g = torch.Generator().manual_seed(C)
+    x = torch.randn(N, C, generator=g).to(torch.bfloat16)
+    w = torch.randn(C, K, generator=g) * 0.5
+    b = torch.randn(C, generator=g)
+    dy = torch.randn(N, C, generator=g).to(torch.bfloat16)
+    y = tpa.tree_conv_fwd(plan, x.cuda(), w.cuda(), b.cuda(), "silu")
+    dx, dw, db = tpa.tree_conv_bwd(plan, x.cuda(), w.cuda(), b.cuda(), dy.cuda(), "silu")
+    tpa.tree_status_sync()
+    xr = x.double().requires_grad_(True)
+    wr = w.double().requires_grad_(True)
+    br = b.double().requires_grad_(True)
+    yr = CV.tree_conv(parents, lengths, xr, wr, br, "silu")
+    yr.backward(dy.double())
+    _cmp(y, yr.detach(), torch.bfloat16, f"y C={C}")
+    _cmp(dx, xr.grad, torch.bfloat16, f"dx C={C}")
+    _cmp(dw, wr.grad, torch.float32, "dweight", float(wr.grad.abs().max()))
+    _cmp(db, br.grad, torch.float32, "dbias", float(br.grad.abs().max()))
+
+
 def test_conv_backward_repeats_bit_for_bit_and_autograd_runs_the_kernels():
     _need_gpu()
     w = treegen.workload(4)

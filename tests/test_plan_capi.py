@@ -118,12 +118,18 @@ def test_field_size_mismatch_and_null_args():
 
 def test_device_calls_without_device_copy_are_rejected():
     """Host-side validation runs before any launch (no GPU needed)."""
+    # The plan has no device copy, so none of these calls could reach a launch
+    # even if a check were skipped. Pointers are NULL wherever the case does
+    # not test the pointers themselves.
     plan = tpa.tree_plan_build([-1], [8])
+    nul = (None,) * 5  # q, k, v, o, lse
     # D = 96 is rejected before the device is touched
-    st = tpa.lib.tree_attn_fwd(plan.handle, 16, 16, 16, 16, 16, 1, 1, 96, 1, 0.0, None)
+    st = tpa.lib.tree_attn_fwd(plan.handle, *nul, 1, 1, 96, 1, 0.0, None)
     assert st == 5
-    st = tpa.lib.tree_attn_fwd(plan.handle, 16, 16, 16, 16, 16, 3, 2, 128, 1, 0.0, None)
+    st = tpa.lib.tree_attn_fwd(plan.handle, *nul, 3, 2, 128, 1, 0.0, None)
     assert st == 1
+    st = tpa.lib.tree_attn_fwd(plan.handle, *nul, 1, 1, 128, 1, 0.0, None)
+    assert st == 1 and b"NULL" in tpa.lib.tree_last_error()
     st = tpa.lib.tree_attn_fwd(plan.handle, 17, 16, 16, 16, 16, 1, 1, 128, 1, 0.0, None)
     assert st == 1  # misaligned pointer
     # each backward phase checks the pointers it uses
@@ -132,7 +138,8 @@ def test_device_calls_without_device_copy_are_rejected():
     assert st == 1 and b"NULL" in tpa.lib.tree_last_error()  # o
     st = tpa.lib.tree_attn_bwd_dkdv(plan.handle, *args, 16, 16, None, 2, 1, 128, 1, 1, 0.0, 16, 1 << 20, None)
     assert st == 1 and b"NULL" in tpa.lib.tree_last_error()  # dv
-    st = tpa.lib.tree_attn_bwd_dkdv(plan.handle, *args, 16, 16, 16, 2, 1, 96, 1, 1, 0.0, 16, 1 << 20, None)
+    nul4 = (None,) * 4
+    st = tpa.lib.tree_attn_bwd_dkdv(plan.handle, *nul4, None, None, None, 2, 1, 96, 1, 1, 0.0, None, 1 << 20, None)
     assert st == 5  # D = 96 unsupported for bf16
     st = tpa.lib.tree_attn_bwd_dq(plan.handle, *args, 16, 16, 16, 2, 1, 128, 1, 1, 0.0, 16, 4, None)
     assert st == 1 and b"workspace too small" in tpa.lib.tree_last_error()
@@ -181,15 +188,15 @@ def test_path_weights_and_rope_validate_their_arguments():
         tpa.tree_weights_paths(plan, [1.0, float("nan")])
     # tree_rope: checks that need no device (the last argument is the stream)
     lib = tpa.lib
-    assert lib.tree_rope(None, 16, 2, 64, 1, 10000.0, 0, 0, None) == 1
-    assert lib.tree_rope(plan.handle, 16, 2, 63, 1, 10000.0, 0, 0, None) == 5  # odd head_dim
-    assert lib.tree_rope(plan.handle, 16, 2, 130, 1, 10000.0, 0, 0, None) == 5  # above 128
-    assert lib.tree_rope(plan.handle, 16, 0, 64, 1, 10000.0, 0, 0, None) == 1  # heads
-    assert lib.tree_rope(plan.handle, 16, 2, 64, 7, 10000.0, 0, 0, None) == 1  # dtype
-    assert lib.tree_rope(plan.handle, 16, 2, 64, 1, 0.0, 0, 0, None) == 1  # base
-    assert lib.tree_rope(plan.handle, 16, 2, 64, 1, float("inf"), 0, 0, None) == 1
-    assert lib.tree_rope(plan.handle, 16, 2, 64, 1, 10000.0, 2, 0, None) == 1  # rotate_half
-    assert lib.tree_rope(plan.handle, 16, 2, 64, 1, 10000.0, 0, 3, None) == 1  # inverse
+    assert lib.tree_rope(None, None, 2, 64, 1, 10000.0, 0, 0, None) == 1
+    assert lib.tree_rope(plan.handle, None, 2, 63, 1, 10000.0, 0, 0, None) == 5  # odd head_dim
+    assert lib.tree_rope(plan.handle, None, 2, 130, 1, 10000.0, 0, 0, None) == 5  # above 128
+    assert lib.tree_rope(plan.handle, None, 0, 64, 1, 10000.0, 0, 0, None) == 1  # heads
+    assert lib.tree_rope(plan.handle, None, 2, 64, 7, 10000.0, 0, 0, None) == 1  # dtype
+    assert lib.tree_rope(plan.handle, None, 2, 64, 1, 0.0, 0, 0, None) == 1  # base
+    assert lib.tree_rope(plan.handle, None, 2, 64, 1, float("inf"), 0, 0, None) == 1
+    assert lib.tree_rope(plan.handle, None, 2, 64, 1, 10000.0, 2, 0, None) == 1  # rotate_half
+    assert lib.tree_rope(plan.handle, None, 2, 64, 1, 10000.0, 0, 3, None) == 1  # inverse
     assert lib.tree_rope(plan.handle, None, 2, 64, 1, 10000.0, 0, 0, None) == 1  # NULL x
     assert lib.tree_rope(plan.handle, 20, 2, 64, 1, 10000.0, 0, 0, None) == 1  # misaligned
 
@@ -201,7 +208,7 @@ def test_conv_validates_its_arguments():
     assert lib.tree_conv_prepare(plan.handle, 0, None) == 5  # kernel size out of range
     assert lib.tree_conv_prepare(plan.handle, 9, None) == 5
     # checks that need no device: channels, dtype, activation
-    args = (16, 16, None, 16)  # x, weight, bias, y
+    args = (None, None, None, None)  # x, weight, bias, y: rejected before they are read
     assert lib.tree_conv_fwd(None, *args, 8, 1, 1, None) == 1
     assert lib.tree_conv_fwd(plan.handle, *args, 12, 1, 1, None) == 5  # not a multiple of 8
     assert lib.tree_conv_fwd(plan.handle, *args, 8, 5, 1, None) == 1  # dtype

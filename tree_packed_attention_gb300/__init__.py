@@ -268,24 +268,43 @@ def _conv_prepare(plan: Plan, kernel_size: int, stream):
 def _conv_check(plan: Plan, x, weight, bias):
     import torch
 
-    if x.dim() != 2 or x.shape[0] != plan.num_tokens or not x.is_contiguous():
-        raise ValueError(f"x must be contiguous [N={plan.num_tokens}, C], got {tuple(x.shape)}")
+    if x.dim() != 2 or x.shape[0] != plan.num_tokens:
+        raise ValueError(f"x must be [N={plan.num_tokens}, C], got {tuple(x.shape)}")
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError(f"x must be bf16 or fp32, got {x.dtype}")
     C = x.shape[1]
-    if weight.dtype != torch.float32 or weight.dim() != 2 or weight.shape[0] != C or not weight.is_contiguous():
-        raise ValueError("weight must be contiguous fp32 [C, K]")
-    if bias is not None and (bias.dtype != torch.float32 or bias.shape != (C,)):
-        raise ValueError("bias must be fp32 [C]")
+    _check_tensor("x", x, (plan.num_tokens, C))
+    if weight.dim() != 2 or weight.shape[0] != C:
+        raise ValueError(f"weight must be fp32 [C={C}, K], got {tuple(weight.shape)}")
+    _check_tensor("weight", weight, (C, weight.shape[1]), torch.float32)
+    if weight.device != x.device:
+        raise ValueError("weight must be on x's device")
+    if bias is not None:
+        _check_tensor("bias", bias, (C,), torch.float32)
+        if bias.device != x.device:
+            raise ValueError("bias must be on x's device")
     return C, weight.shape[1]
+
+
+def _act_code(activation: str) -> int:
+    if activation == "silu":
+        return ACT_SILU
+    if activation == "none":
+        return ACT_NONE
+    raise ValueError(f"activation must be 'silu' or 'none', got {activation!r}")
 
 
 def tree_conv_fwd(plan: Plan, x, weight, bias=None, activation: str = "silu", out=None, stream=None):
     """Tree-correct causal depthwise conv of x[N, C] (App. A.3): y[N, C]."""
     import torch
 
+    act = _act_code(activation)
     C, K = _conv_check(plan, x, weight, bias)
-    s = _conv_prepare(plan, K, stream)
     y = torch.empty_like(x) if out is None else out
-    act = ACT_SILU if activation == "silu" else ACT_NONE
+    _check_tensor("out", y, tuple(x.shape), x.dtype)
+    if y.device != x.device:
+        raise ValueError("out must be on x's device")
+    s = _conv_prepare(plan, K, stream)
     check(lib.tree_conv_fwd(plan.handle, x.data_ptr(), weight.data_ptr(),
                             bias.data_ptr() if bias is not None else None, y.data_ptr(), C,
                             _dtype_code(x), act, s))
@@ -296,15 +315,17 @@ def tree_conv_bwd(plan: Plan, x, weight, bias, dy, activation: str = "silu", str
     """(dx, dweight, dbias) of tree_conv_fwd; dbias is None when bias is None."""
     import torch
 
+    act = _act_code(activation)
     C, K = _conv_check(plan, x, weight, bias)
+    _check_tensor("dy", dy, tuple(x.shape), x.dtype)
+    if dy.device != x.device:
+        raise ValueError("dy must be on x's device")
     s = _conv_prepare(plan, K, stream)
-    dy = dy.contiguous()
     dx = torch.empty_like(x)
     dw = torch.empty_like(weight)
     db = torch.empty_like(bias) if bias is not None else None
     nbytes = lib.tree_conv_bwd_workspace_bytes(plan.handle, C)
     ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=x.device)
-    act = ACT_SILU if activation == "silu" else ACT_NONE
     check(lib.tree_conv_bwd(plan.handle, x.data_ptr(), weight.data_ptr(),
                             bias.data_ptr() if bias is not None else None, dy.data_ptr(),
                             dx.data_ptr(), dw.data_ptr(), db.data_ptr() if db is not None else None,
@@ -322,8 +343,7 @@ def tree_rope(plan: Plan, x, base: float = 10000.0, rotate_half: bool = False,
         raise ValueError(f"x must be [N={plan.num_tokens}, H, D], got {tuple(x.shape)}")
     if x.dtype not in (torch.bfloat16, torch.float32):
         raise TypeError(f"x must be bf16 or fp32, got {x.dtype}")
-    if not x.is_contiguous():
-        raise ValueError("x must be contiguous")
+    _check_tensor("x", x, tuple(x.shape))
     s = _stream_ptr(stream)
     plan.to_device(s)
     check(lib.tree_rope(plan.handle, x.data_ptr(), x.shape[1], x.shape[2], _dtype_code(x),
@@ -401,7 +421,8 @@ def _make_conv_autograd():
         @staticmethod
         def backward(ctx, dy):
             x, weight, bias = ctx.saved_tensors
-            dx, dw, db = tree_conv_bwd(ctx.plan, x, weight, bias, dy, ctx.activation)
+            dx, dw, db = tree_conv_bwd(ctx.plan, x, weight, bias, dy.contiguous().to(x.dtype),
+                                       ctx.activation)
             return dx, dw, db, None, None
 
     return TreeConvFn
