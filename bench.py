@@ -241,18 +241,17 @@ def reference_arm(args):
     print(json.dumps(line))
 
 
-def gpu_arm(args):
-    import numpy as np
+def time_workload(index: int, steps: int, warmup: int, dev, rank: int, clock_gpu=None):
+    """Build the plan of workload ``index``, draw its inputs on the device and
+    time ``steps`` steps (forward, then the backward's two phases) with CUDA
+    events around each kernel, L2 flushed between steps. Returns a dict of the
+    per-step event times and what the end-to-end leg needs."""
     import torch
 
     import treegen
     import tree_packed_attention_gb300 as tpa
 
-    dist, rank, world = _dist()
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    w = treegen.workload(args.workload)
+    w = treegen.workload(index)
     N, hq, hkv, D = w.num_tokens, w.hq, w.hkv, w.head_dim
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
 
@@ -260,9 +259,6 @@ def gpu_arm(args):
     plan = tpa.tree_plan_build(w.parents, w.lengths)
     plan_ms = 1e3 * (time.perf_counter() - t0)
     plan.to_device()
-    pvis = plan.info["visible_pairs"]
-    flops_fwd = 4.0 * D * hq * pvis
-    flops_bwd = 10.0 * D * hq * pvis
 
     # Seeded synthetic inputs, N(0,1), drawn on the device (one generator per rank).
     gen = torch.Generator(device=dev).manual_seed(1000 + rank)
@@ -280,37 +276,109 @@ def gpu_arm(args):
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
+    for _ in range(warmup):
         tpa.tree_attn_fwd(plan, q, k, v, out=o, lse=lse)
         tpa.tree_attn_bwd(plan, do, q, k, v, o, lse, workspace=ws, out=(dq, dk, dv))
-
-    for _ in range(args.warmup):
-        step()
     tpa.tree_status_sync()
 
     # The timed step runs the backward as its two phases (exactly what
     # tree_attn_bwd launches) so that each kernel gets its own events.
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    if dist:
-        dist.barrier()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        for s in range(args.steps):
-            flush.zero_()  # L2 flush between timed steps (outside the events)
-            ev[s][0].record(stream)
-            tpa.tree_attn_fwd(plan, q, k, v, out=o, lse=lse)
-            ev[s][1].record(stream)
-            tpa.tree_attn_bwd_dq(plan, do, q, k, v, o, lse, ws, out=dq)
-            ev[s][2].record(stream)
-            tpa.tree_attn_bwd_dkdv(plan, do, q, k, v, lse, ws, out=(dk, dv))
-            ev[s][3].record(stream)
-        torch.cuda.synchronize()
+    clocks = ClockSampler(clock_gpu) if clock_gpu is not None else None
+    if clocks:
+        clocks.__enter__()
+    for st in range(steps):
+        flush.zero_()  # L2 flush between timed steps (outside the events)
+        ev[st][0].record(stream)
+        tpa.tree_attn_fwd(plan, q, k, v, out=o, lse=lse)
+        ev[st][1].record(stream)
+        tpa.tree_attn_bwd_dq(plan, do, q, k, v, o, lse, ws, out=dq)
+        ev[st][2].record(stream)
+        tpa.tree_attn_bwd_dkdv(plan, do, q, k, v, lse, ws, out=(dk, dv))
+        ev[st][3].record(stream)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.__exit__(None, None, None)
+    tpa.tree_status_sync()
+    return {
+        "w": w, "plan": plan, "plan_ms": plan_ms, "pvis": plan.info["visible_pairs"],
+        "tensors": (q, k, v, do, o, lse, dq, dk, dv, ws), "clocks": clocks,
+        "fwd_ms": [e[0].elapsed_time(e[1]) for e in ev],
+        "dq_ms": [e[1].elapsed_time(e[2]) for e in ev],
+        "kv_ms": [e[2].elapsed_time(e[3]) for e in ev],
+    }
+
+
+def kernel_table(r):
+    """Mean event time of each kernel and the FLOPs its outputs need per
+    visible pair and q head (fwd: S, PV; dQ: S, dP, dS K; dK/dV: S^T, dP^T,
+    P^T dO, dS^T Q)."""
+    w, pvis = r["w"], r["pvis"]
+    D, hq = w.head_dim, w.hq
+    return {
+        "tree_attn_fwd_sm103": (statistics.mean(r["fwd_ms"]), 4.0 * D * hq * pvis),
+        "tree_attn_bwd_dq_sm103": (statistics.mean(r["dq_ms"]), 6.0 * D * hq * pvis),
+        "tree_attn_bwd_dkdv_sm103": (statistics.mean(r["kv_ms"]), 8.0 * D * hq * pvis),
+    }
+
+
+def workload_summary(r, peak):
+    """fwd / bwd / fwd+bwd visible-pair TFLOP/s and fractions of the bf16 peak
+    for one timed workload (metric accounting: 4*D and 10*D per pair and head)."""
+    w, pvis = r["w"], r["pvis"]
+    D, hq = w.head_dim, w.hq
+    fwd = statistics.mean(r["fwd_ms"])
+    bwd = statistics.mean(a + b for a, b in zip(r["dq_ms"], r["kv_ms"]))
+    f_tf = 4.0 * D * hq * pvis / (fwd * 1e-3) / 1e12
+    b_tf = 10.0 * D * hq * pvis / (bwd * 1e-3) / 1e12
+    t_tf = 14.0 * D * hq * pvis / ((fwd + bwd) * 1e-3) / 1e12
+    return {
+        "workload": w.name, "tokens": w.num_tokens, "hq": hq, "hkv": w.hkv, "head_dim": D,
+        "visible_pairs": pvis, "ms_per_step": fwd + bwd,
+        "fwd_bwd": {"tflops": t_tf, "frac": t_tf / peak},
+        "fwd": {"ms": fwd, "tflops": f_tf, "frac": f_tf / peak},
+        "bwd": {"ms": bwd, "tflops": b_tf, "frac": b_tf / peak},
+        "kernels": {n: {"ms": t, "tflops_algorithmic": f / (t * 1e-3) / 1e12}
+                    for n, (t, f) in kernel_table(r).items()},
+    }
+
+
+def gpu_arm(args):
+    import torch
+
+    import tree_packed_attention_gb300 as tpa
+
+    dist, rank, world = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_kind = _peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+
+    # Secondary workloads first (their tensors are freed before the headline's).
+    extras = []
+    for idx in [int(x) for x in args.extra_workloads.split(",") if x.strip()]:
+        if idx == args.workload:
+            continue
+        r = time_workload(idx, max(3, min(args.steps, 10)), args.warmup, dev, rank)
+        for key in ("fwd_ms", "dq_ms", "kv_ms"):
+            r[key] = [max_over_ranks(statistics.mean(r[key]), dist, dev)]
+        extras.append(workload_summary(r, peak))
+        del r
+        torch.cuda.empty_cache()
+
     if dist:
         dist.barrier()
-    tpa.tree_status_sync()
-    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    dq_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    kv_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    r = time_workload(args.workload, args.steps, args.warmup, dev, rank, clock_gpu=local)
+    if dist:
+        dist.barrier()
+    w, plan, plan_ms, pvis, clocks = r["w"], r["plan"], r["plan_ms"], r["pvis"], r["clocks"]
+    q, k, v, do, o, lse, dq, dk, dv, ws = r["tensors"]
+    N, hq, hkv, D = w.num_tokens, w.hq, w.hkv, w.head_dim
+    flops_fwd = 4.0 * D * hq * pvis
+    flops_bwd = 10.0 * D * hq * pvis
+    fwd_ms, dq_ms, kv_ms = r["fwd_ms"], r["dq_ms"], r["kv_ms"]
     bwd_ms = [a + b for a, b in zip(dq_ms, kv_ms)]
     step_ms = statistics.mean(f + b for f, b in zip(fwd_ms, bwd_ms))
     step_ms = max_over_ranks(step_ms, dist, dev)
@@ -376,19 +444,11 @@ def gpu_arm(args):
     e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     e2e_value = whole_job_rate(world, flops_fwd + flops_bwd, e2e_ms) / 1e12
 
-    peaks, peak_kind = _peaks()
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     bwd_mean = statistics.mean(bwd_ms)
     fwd_mean = statistics.mean(fwd_ms)
     bwd_tf = flops_bwd / (bwd_mean * 1e-3) / 1e12
     fwd_tf = flops_fwd / (fwd_mean * 1e-3) / 1e12
-    # Per kernel: mean event time and the FLOPs its outputs need per visible
-    # pair and q head (fwd: S, PV; dQ: S, dP, dS K; dK/dV: S^T, dP^T, P^T dO, dS^T Q).
-    kernels = {
-        "tree_attn_fwd_sm103": (fwd_mean, 4.0 * D * hq * pvis),
-        "tree_attn_bwd_dq_sm103": (statistics.mean(dq_ms), 6.0 * D * hq * pvis),
-        "tree_attn_bwd_dkdv_sm103": (statistics.mean(kv_ms), 8.0 * D * hq * pvis),
-    }
+    kernels = kernel_table(r)
     top = max(kernels, key=lambda n: kernels[n][0])
     top_ms, top_flops = kernels[top]
     top_tf = top_flops / (top_ms * 1e-3) / 1e12
@@ -422,6 +482,9 @@ def gpu_arm(args):
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": 3 * args.steps,
             "cpu_baseline": cpu,
+            # the other tree-shaped workloads, timed the same way in this run
+            # (fewer steps), so their fractions sit in the same record
+            "workloads": extras,
         }
         print(json.dumps(line))
     if dist:
@@ -577,6 +640,9 @@ def main():
     ap.add_argument("--workload", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra-workloads", default="3,4",
+                    help="comma-separated workloads also timed and reported under 'workloads' "
+                         "('' for none)")
     ap.add_argument("--op", default="attention", choices=["attention", "rope", "conv", "partition"],
                     help="attention (the default and the headline), rope (tree RoPE on q and k), "
                          "conv (the tree-correct causal conv) or partition (the host planner, no GPU)")

@@ -236,9 +236,14 @@ def backward_keys(q, k, v, do, parents, lengths, keys, scale=None, view=None):
     keys = np.asarray(keys, dtype=np.int64)
     dk = torch.zeros(len(keys), hkv, D, dtype=torch.float64)
     dv = torch.zeros(len(keys), hkv, D, dtype=torch.float64)
+    seen = [rows_seeing(view, int(j)) for j in keys]
+    # o and lse of every row that sees one of the keys, computed once
+    union = np.unique(np.concatenate(seen)) if len(keys) else np.zeros(0, np.int64)
+    o_all, lse_all = forward(q, k, v, parents, lengths, scale, rows=union, view=view)
     for n, j in enumerate(keys):
-        rows = rows_seeing(view, int(j))
-        o, lse = forward(q, k, v, parents, lengths, scale, rows=rows, view=view)
+        rows = seen[n]
+        at = torch.as_tensor(np.searchsorted(union, rows))
+        o, lse = o_all[at], lse_all[:, at]
         rr = torch.as_tensor(rows)
         for h in range(hq):
             kv = h // G

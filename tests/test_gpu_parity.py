@@ -270,13 +270,36 @@ def _leaf_tail_keys(parents, lengths, rng, n=4):
     return sorted(out)
 
 
-@pytest.mark.parametrize("index", [2, 3, 4, 5])
-def test_full_size_workloads_sampled(index):
+def _long_walk_keys(parents, lengths, max_rows):
+    """First and last token of the segment whose keys are seen by the most rows,
+    among segments whose subtree holds at most ``max_rows`` tokens: the longest
+    walks of the key-stationary backward that the oracle can still afford (a
+    key's rows are its own segment from the key on plus every descendant)."""
+    parents = [int(x) for x in parents]
+    lengths = [int(x) for x in lengths]
+    order, seg_start = T.dfs_serialize(parents, lengths)
+    sub = [0] * len(parents)
+    for s in reversed(order):
+        sub[s] += lengths[s]
+        if parents[s] >= 0:
+            sub[parents[s]] += sub[s]
+    best = max((s for s in range(len(parents)) if sub[s] <= max_rows), key=lambda s: (sub[s], -s))
+    return [seg_start[best], seg_start[best] + lengths[best] - 1]
+
+
+# (workload, seed): seeds 1 and 2 redraw the structure and tensors of the two
+# tree-shaped workloads; seed 0 also checks the longest key walks.
+FULL_SIZE_CASES = [(2, 0), (3, 0), (3, 1), (3, 2), (4, 0), (5, 0), (5, 1), (5, 2)]
+
+
+@pytest.mark.parametrize("index,seed", FULL_SIZE_CASES)
+def test_full_size_workloads_sampled(index, seed):
     _need_gpu()
-    w = treegen.workload(index)
-    (q, k, v, do), (o, lse, g32, g16) = _run(w.parents, w.lengths, w.hq, w.hkv, w.head_dim, w.dtype, 0)
+    w = treegen.workload(index, seed)
+    (q, k, v, do), (o, lse, g32, g16) = _run(w.parents, w.lengths, w.hq, w.hkv, w.head_dim, w.dtype,
+                                              seed)
     dq, dk, dv = g32
-    rng = np.random.default_rng(index)
+    rng = np.random.default_rng(index + 10 * seed)
     rows = _sample_rows(w.parents, w.lengths, rng)
     ro, rlse = A.forward(q, k, v, w.parents, w.lengths, rows=rows)
     _check_bf16_store("o", o[rows], ro)
@@ -285,6 +308,11 @@ def test_full_size_workloads_sampled(index):
     _check("dq", dq[rows], rdq, BF16_MAX, BF16_MEAN)
     _check_bf16_store("dq(bf16)", g16[0][rows], rdq)
     keys = _leaf_tail_keys(w.parents, w.lengths, rng)
+    if seed == 0:
+        # keys seen by tens of q-tiles x every head of the group: the chain's
+        # first and last key, the GRPO prompt, a depth-3 agentic subtree of 16k
+        # tokens, the prompt of the largest packed trie
+        keys = sorted(set(keys) | set(_long_walk_keys(w.parents, w.lengths, 23000)))
     rdk, rdv = A.backward_keys(q, k, v, do, w.parents, w.lengths, keys)
     _check("dk", dk[keys], rdk, BF16_MAX, BF16_MEAN)
     _check("dv", dv[keys], rdv, BF16_MAX, BF16_MEAN)

@@ -1,5 +1,8 @@
 """The partition planner (C-ABI, host) against brute force and the pages'
 definitions (§3.3 "Partitioning"; App. B.2, B.4 eq. 17). CPU only."""
+import json
+import os
+
 import numpy as np
 import pytest
 
@@ -7,6 +10,9 @@ import treegen
 import tree_packed_attention_gb300 as tpa
 from oracle import partition as PO
 from oracle import trie as T
+
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
 def _random_forest(rng, S_max, len_max):
@@ -85,3 +91,76 @@ def test_caps_below_a_segment_are_rejected():
     assert e.value.status == 1
     r = tpa.tree_partition(tpa.tree_plan_build(np.zeros(0, np.int32), np.zeros(0, np.int32)), 5)
     assert r["num_parts"] == 0 and r["peak_path_tokens"] == 0
+
+
+def test_hand_worked_gateway_example():
+    """App. B.2-B.4 worked by hand on a three-level chain of partitions whose
+    gateways hold a non-ancestor sibling (the App. B.3 case)."""
+    with open(os.path.join(GOLDEN, "partition_gateway_example.json")) as f:
+        g = json.load(f)
+    parents, lengths, cap = g["parents"], g["lengths"], g["cap"]
+    assert PO.min_partitions_bruteforce(parents, lengths, cap) == g["num_parts"]
+    part = g["part_of_segment"]
+    assert PO.is_valid_partition(parents, lengths, cap, part)
+    rec = PO.partition_records(parents, lengths, part)
+    for i in range(g["num_parts"]):
+        for key in ("root", "parent", "tokens", "past_len", "pos_offset"):
+            assert rec[i][key] == g[key][i], (key, i)
+    assert PO.peak_path_tokens(parents, lengths, part) == g["peak_path_tokens"]
+    r = tpa.tree_partition(tpa.tree_plan_build(parents, lengths), cap)
+    assert r["part_of_segment"].tolist() == part
+    for key in ("root", "parent", "tokens", "past_len", "pos_offset"):
+        assert r[key].tolist() == g[key], key
+    assert r["peak_path_tokens"] == g["peak_path_tokens"]
+
+
+def _gateway_len_by_tokens(parents, lengths, part):
+    """App. B.2 counted token by token in the global DFS sequence: the gateway
+    of piece C holds, for every piece A above C on its chain, A's tokens that
+    come before the end of A's cut node (the deepest segment of A on the way
+    down to C's root). A piece is a connected subtree, so the global DFS order
+    restricted to A is A's own DFS order."""
+    order, seg_start = T.dfs_serialize(parents, lengths)
+    seg = T.token_segments(parents, lengths)
+    out = {}
+    for c in set(part):
+        top = next(s for s in order if part[s] == c)
+        chain = T.ancestors(parents, top)  # root first
+        total = 0
+        for a in {part[s] for s in chain}:
+            cut = [s for s in chain if part[s] == a][-1]
+            end = seg_start[cut] + lengths[cut]
+            total += sum(1 for t in range(end) if part[seg[t]] == a)
+        out[c] = total
+    return out
+
+
+def _peak_by_tokens(parents, lengths, part):
+    """Peak partition tokens along a path, from each path's token list (eq. 7
+    layout): the pieces its tokens fall in, summed by piece size."""
+    seg = T.token_segments(parents, lengths)
+    size = {}
+    for t in range(len(seg)):
+        size[part[seg[t]]] = size.get(part[seg[t]], 0) + 1
+    best = 0
+    for _, ids in T.base_serialization(parents, lengths):
+        best = max(best, sum(size[p] for p in {part[seg[t]] for t in ids}))
+    return best
+
+
+def test_gateway_lengths_and_peak_by_token_counting():
+    rng = np.random.default_rng(7)
+    cases = [treegen.workload(1, s) for s in range(3)]
+    forests = [_random_forest(rng, 14, 30) for _ in range(80)]
+    for parents, lengths in [(w.parents, w.lengths) for w in cases] + forests:
+        parents = [int(x) for x in parents]
+        lengths = [int(x) for x in lengths]
+        for cap in (max(lengths), max(lengths) * 2, sum(lengths)):
+            r = tpa.tree_partition(tpa.tree_plan_build(parents, lengths), cap)
+            part = [int(x) for x in r["part_of_segment"]]
+            rec = PO.partition_records(parents, lengths, part)
+            by_tokens = _gateway_len_by_tokens(parents, lengths, part)
+            for i in range(r["num_parts"]):
+                assert rec[i]["past_len"] == by_tokens[i] == r["past_len"][i]
+            peak = _peak_by_tokens(parents, lengths, part)
+            assert PO.peak_path_tokens(parents, lengths, part) == peak == r["peak_path_tokens"]
