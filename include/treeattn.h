@@ -70,6 +70,7 @@ typedef struct {
   int64_t nnz_pair_tiles; /* entries of the q-tile-pair union lists */
   int64_t num_ancestors;  /* sum over segments of the number of ancestors */
   int64_t visible_pairs;  /* sum over rows of the visible keys, diagonal included */
+  int64_t num_gathered_tiles; /* entries of TREE_FIELD_GT_KIND (both unit sizes) */
 } tree_plan_info_t;
 
 /* Plan fields readable with tree_plan_get. All are int32 arrays. */
@@ -98,7 +99,26 @@ typedef enum {
   TREE_FIELD_QP_KT = 21,      /* [nnz_pair_tiles] union of the k-tiles of q-tiles 2p and 2p+1, ascending */
   TREE_FIELD_QP_KIND = 22,    /* [nnz_pair_tiles] kind for q-tile 2p | (kind for 2p+1) << 2; 0 = EMPTY */
   TREE_FIELD_QP_ORDER = 23,   /* [num_pairs] forward work order of pairs: last to first */
-  TREE_FIELD_COUNT = 24
+  /* Gathered key tiles: for a unit of q rows (a q-tile of 128 rows, or a
+   * pair of q-tiles, 256 rows) the keys that at least one of its rows sees,
+   * the keys that every one of its rows sees first, each part ascending, are
+   * packed into tiles of 128 key columns. A run of consecutive keys starts at
+   * a column that is a multiple of 8 (an "atom" of 8 columns), so a tile's
+   * keys load as 16 atoms of 8 consecutive rows each; columns left over in a
+   * run's last atom, and atoms after the unit's last run, are padding. */
+  TREE_FIELD_GQ_PTR = 24,     /* [num_q_tiles+1] tiles of each q-tile (units of 128 rows) */
+  TREE_FIELD_GP_PTR = 25,     /* [num_pairs+1] tiles of each q-tile pair (units of 256 rows), after
+                                 the q-tiles' tiles in the same tile table */
+  TREE_FIELD_GT_KIND = 26,    /* [num_gathered_tiles] kind of the first 128 rows | kind of the next
+                                 128 rows << 2 (0 EMPTY, 1 PARTIAL, 2 FULL: all 128x128 pairs visible) */
+  TREE_FIELD_GT_ATOM = 27,    /* [num_gathered_tiles*16] first key row of each atom; -8 for an atom
+                                 with no key (loaded as zeros) */
+  TREE_FIELD_GT_BIDX = 28,    /* [num_gathered_tiles] row of the tile in GT_BOUNDS, -1 when no slot of
+                                 the tile is PARTIAL */
+  TREE_FIELD_GT_BOUNDS = 29,  /* [num_bounds*128] key_end of each column's key, 0 for padding.
+                                 Column c holds key GT_ATOM[c/8] + c%8, and row i sees it iff
+                                 key <= i < key_end[c] */
+  TREE_FIELD_COUNT = 30
 } tree_plan_field_t;
 
 /*

@@ -66,6 +66,112 @@ def tile_counts(parents, lengths, bm: int = 128, bn: int = 128):
     return dict(counts)
 
 
+def _unit_key_sets(view, r0, r1):
+    """(keys some row of [r0, r1) sees, keys every row of [r0, r1) sees), ascending,
+    from the row form of the mask: a row of segment s sees the ancestors' chunks
+    and its own chunk up to itself."""
+    some, every = [], None
+    r = r0
+    while r < r1:
+        s = int(view.token_seg[r])
+        a, b = view.seg_range(s)
+        ra, rb = r, min(r1, b)
+        anc = view.ancestor_keys(s)
+        some.append(np.concatenate([anc, np.arange(a, rb)]))
+        first = np.concatenate([anc, np.arange(a, ra + 1)])  # what the segment's first row sees
+        every = first if every is None else np.intersect1d(every, first)
+        r = rb
+    if every is None:
+        return np.zeros(0, np.int64), np.zeros(0, np.int64)
+    return np.unique(np.concatenate(some)), np.asarray(every, np.int64)
+
+
+def gathered_tiles(parents, lengths, unit_rows: int, bn: int = 128, atom: int = 8):
+    """Gathered key tiles of every unit of ``unit_rows`` query rows.
+
+    For the unit's rows, the keys every row sees come first and the keys only
+    some rows see after them, each part ascending; runs of consecutive keys
+    are laid into tiles of ``bn`` columns, each run from a column that is a
+    multiple of ``atom``. Per tile: the kind for each block of 128 rows (EMPTY
+    no visible pair, FULL every pair visible, PARTIAL otherwise), the first
+    key of each atom (-8 if the atom holds none) and the key of each column
+    (None for padding), and for tiles with a PARTIAL block the key_end of each
+    column (0 for padding). A layout convention of this library for loading and
+    skipping keys; the pages say nothing about it."""
+    view = TrieView(parents, lengths)
+    N = view.N
+    kend = key_end(parents, lengths)
+    out = []
+    for r0 in range(0, N, unit_rows):
+        r1 = min(N, r0 + unit_rows)
+        some, every = _unit_key_sets(view, r0, r1)
+        seq = list(every) + sorted(set(some.tolist()) - set(every.tolist()))
+        runs = []
+        for j in seq:
+            if runs and runs[-1][1] == j:
+                runs[-1][1] = j + 1
+            else:
+                runs.append([j, j + 1])
+        tiles = []
+        col = bn
+        for a, b in runs:
+            while a < b:
+                if col >= bn:
+                    tiles.append([None] * bn)
+                    col = 0
+                m = min(b - a, bn - col)
+                for c in range(m):
+                    tiles[-1][col + c] = a + c
+                col += m
+                a += m
+            col = -(-col // atom) * atom
+        slots = []
+        for sa in range(r0, r0 + unit_rows, 128):
+            sb = min(r1, sa + 128)
+            slots.append(_unit_key_sets(view, sa, sb) + (sb - sa,) if sa < sb else None)
+        unit = []
+        for cols in tiles:
+            kinds = []
+            keys = [c for c in cols if c is not None]
+            for sl in slots:
+                if sl is None:
+                    kinds.append(EMPTY)
+                    continue
+                s_some, s_every, nrows = sl
+                if nrows == 128 and len(keys) == bn and np.isin(keys, s_every).all():
+                    kinds.append(FULL)
+                elif np.isin(keys, s_some).any():
+                    kinds.append(PARTIAL)
+                else:
+                    kinds.append(EMPTY)
+            atoms = [cols[g * atom] if cols[g * atom] is not None else -8 for g in range(bn // atom)]
+            bnd = None
+            if PARTIAL in kinds:
+                bnd = [int(kend[c]) if c is not None else 0 for c in cols]
+            unit.append({"kinds": kinds, "atoms": atoms, "cols": cols, "bounds": bnd})
+        out.append(unit)
+    return out
+
+
+def _gathered_fields(parents, lengths):
+    kind, atoms, bidx, bounds = [], [], [], []
+    ptrs = []
+    for rows in (128, 256):
+        ptr = [len(kind)]
+        for unit in gathered_tiles(parents, lengths, rows):
+            for t in unit:
+                kind.append(sum(k << (2 * n) for n, k in enumerate(t["kinds"])))
+                atoms.extend(t["atoms"])
+                if t["bounds"] is None:
+                    bidx.append(-1)
+                else:
+                    bidx.append(len(bounds) // 128)
+                    bounds.extend(t["bounds"])
+            ptr.append(len(kind))
+        ptrs.append(ptr)
+    return ptrs[0], ptrs[1], kind, atoms, bidx, bounds
+
+
 def plan_fields(parents, lengths, bm: int = 128, bn: int = 128) -> dict:
     """Every plan field as int32/int64 numpy arrays, named as in the C-ABI."""
     parents_l, lengths_l = T.validate(parents, lengths)
@@ -130,6 +236,7 @@ def plan_fields(parents, lengths, bm: int = 128, bn: int = 128) -> dict:
     qp_order = list(reversed(range(n_pairs)))
 
     pos_id = T.position_ids(parents_l, lengths_l)
+    gq_ptr, gp_ptr, gt_kind, gt_atom, gt_bidx, gt_bounds = _gathered_fields(parents_l, lengths_l)
     i32 = lambda x: np.asarray(x, dtype=np.int32)  # noqa: E731
     return {
         "num_tokens": N,
@@ -160,4 +267,10 @@ def plan_fields(parents, lengths, bm: int = 128, bn: int = 128) -> dict:
         "qp_kt": i32(qp_kt),
         "qp_kind": i32(qp_kind),
         "qp_order": i32(qp_order),
+        "gq_ptr": i32(gq_ptr),
+        "gp_ptr": i32(gp_ptr),
+        "gt_kind": i32(gt_kind),
+        "gt_atom": i32(gt_atom),
+        "gt_bidx": i32(gt_bidx),
+        "gt_bounds": i32(gt_bounds),
     }

@@ -354,3 +354,30 @@ def test_full_size_every_element_written_and_repeatable(index):
             runs.append(outs)
         for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), *runs):
             assert torch.equal(a, b), f"{name} ({gdt}) differs between two runs"
+
+
+def test_dq_repeats_bit_for_bit_on_packed_tries():
+    """Sixteen backward passes over the packed workload (seed 2) give the same
+    bits. The dQ kernel keeps two S buffers; its dS arrivals are counted per
+    buffer, since with one shared counter a warp that finished tile t+1 early
+    could complete tile t's count before another warp had stored its dS of
+    tile t, and the dQ product then read S bits as dS (non-finite rows in
+    about one pass in six on this workload)."""
+    _need_gpu()
+    w = treegen.workload(5, 2)
+    N, hq, hkv, D = w.num_tokens, w.hq, w.hkv, w.head_dim
+    q, k, v, do = (x.cuda() for x in treegen.draw_tensors(N, hq, hkv, D, w.dtype, 2))
+    plan = tpa.tree_plan_build(w.parents, w.lengths)
+    o, lse = tpa.tree_attn_fwd(plan, q, k, v)
+    for gdt in (torch.float32, torch.bfloat16):
+        first = None
+        for rep in range(8):
+            g = tpa.tree_attn_bwd(plan, do, q, k, v, o, lse, grad_dtype=gdt)
+            tpa.tree_status_sync()
+            if first is None:
+                first = g
+                for name, t in zip(("dq", "dk", "dv"), g):
+                    assert torch.isfinite(t).all(), f"{name} ({gdt}) not finite"
+                continue
+            for name, a, b in zip(("dq", "dk", "dv"), first, g):
+                assert torch.equal(a, b), f"{name} ({gdt}) differs in pass {rep}"

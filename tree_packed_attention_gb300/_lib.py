@@ -31,6 +31,7 @@ FIELDS = [
     "dfs_order", "seg_start", "depth", "subtree_end", "trie_id", "g", "anc_ptr", "anc_idx",
     "token_seg", "pos_id", "key_end", "cu_seqlens", "trie_paths", "qt_ptr", "qt_kt", "qt_kind",
     "kt_qlo", "kt_qhi", "fwd_order", "bwd_order", "qp_ptr", "qp_kt", "qp_kind", "qp_order",
+    "gq_ptr", "gp_ptr", "gt_kind", "gt_atom", "gt_bidx", "gt_bounds",
 ]
 
 # Every symbol the public header declares.
@@ -48,7 +49,7 @@ class PlanInfo(C.Structure):
     _fields_ = [(name, C.c_int64) for name in (
         "num_tokens", "num_segments", "num_tries", "block_m", "block_n", "num_q_tiles",
         "num_k_tiles", "nnz_tiles", "num_pairs", "nnz_pair_tiles", "num_ancestors",
-        "visible_pairs")]
+        "visible_pairs", "num_gathered_tiles")]
 
 
 class TreeAttnError(RuntimeError):

@@ -26,6 +26,7 @@
 #include <cmath>
 
 #include "kernels.h"
+#include "gather.cuh"
 #include "sched.cuh"
 #include "sm103_ptx.cuh"
 #include "tma_host.h"
@@ -143,17 +144,18 @@ constexpr uint32_t kDqOffKe = kDqOffV + kDqVStages * kTileBytes;  // per K stage
 constexpr uint32_t kDqOffDelta = kDqOffKe + kDqKStages * 512;
 // mbarriers, then the item ring, then the TMEM base and the abort flag
 constexpr uint32_t kDqOffBar = kDqOffDelta + 2 * 512;
-constexpr uint32_t kDqNumBars = 3 + 2 * kDqKStages + 2 * kDqVStages + 2 + 5 + 4 + 1;
+constexpr uint32_t kDqNumBars = 3 + 2 * kDqKStages + 2 * kDqVStages + 2 + 5 + 4 + 1 + 1;
 constexpr uint32_t kDqOffRing = kDqOffBar + kDqNumBars * 8;
 constexpr uint32_t kDqOffMisc = kDqOffRing + sizeof(ItemRing);
 constexpr uint32_t kDqSmem = kDqOffMisc + 16;
 static_assert(kDqSmem <= 232448, "shared memory budget");
 
 struct DqParams {
-  const int32_t* key_end;
-  const int32_t* qt_ptr;
-  const int32_t* qt_kt;
-  const int32_t* qt_kind;
+  const int32_t* gq_ptr;     // q-tile -> its gathered key tiles
+  const int32_t* gt_kind;    // per tile: 0 empty, 1 partial, 2 full
+  const int32_t* gt_atom;    // per tile: first key row of each 8-column atom (-8: zeros)
+  const int32_t* gt_bidx;    // per tile: row of its key bounds, -1 if not PARTIAL
+  const int32_t* gt_bounds;  // per bounds row: key_end of each column
   const int32_t* order;
   const __nv_bfloat16* o;
   const float* lse;
@@ -167,12 +169,15 @@ struct DqParams {
   float scale, scale_log2;
 };
 
+
 __global__ void __launch_bounds__(kDqThreads, 1)
     tree_attn_bwd_dq_sm103(const __grid_constant__ CUtensorMap map_q,
                            const __grid_constant__ CUtensorMap map_k,
                            const __grid_constant__ CUtensorMap map_v,
                            const __grid_constant__ CUtensorMap map_do,
-                           const __grid_constant__ CUtensorMap map_o, const DqParams p) {
+                           const __grid_constant__ CUtensorMap map_o,
+                           const __grid_constant__ GatherMaps gmap_k,
+                           const __grid_constant__ GatherMaps gmap_v, const DqParams p) {
   // All shared state sits in the dynamic block (no static shared memory), so
   // the block starts 1024-aligned as the 128B-swizzled tiles need.
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -197,7 +202,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       *reinterpret_cast<uint64_t(*)[2]>(bars + 3 + 2 * kDqKStages + 2 * kDqVStages);
   uint64_t* tail = bars + 5 + 2 * kDqKStages + 2 * kDqVStages;
   uint64_t& bar_dp_full = tail[0];
-  uint64_t& bar_ds_full = tail[1];
+  // one per S buffer, like bar_s_full: the dS of tile t sits in buffer t % 2,
+  // and with the S buffers doubled a warp can finish tile t+1 before another
+  // has stored its dS of tile t, so one shared barrier could complete tile t's
+  // phase with a tile t+1 arrival and let the dQ product read a dS that is not
+  // there yet. Buffer b's next dS needs S_{t+2}, which waits for this phase.
+  uint64_t& bar_ds_full0 = tail[1];
+  uint64_t& bar_ds_full1 = tail[10];
   uint64_t& bar_dq_full = tail[2];
   uint64_t& bar_dq_free = tail[3];
   uint64_t& bar_dp_read = tail[4];  // the softmax warps hold dP_t in registers
@@ -226,7 +237,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&bar_s_full[0], 1);
     mbar_init(&bar_s_full[1], 1);
     mbar_init(&bar_dp_full, 1);
-    mbar_init(&bar_ds_full, 256);
+    mbar_init(&bar_ds_full0, 256);
+    mbar_init(&bar_ds_full1, 256);
     mbar_init(&bar_dq_full, 1);
     mbar_init(&bar_dq_free, 256);
     mbar_init(&bar_dp_read, 256);
@@ -241,6 +253,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     tma_prefetch_desc(&map_v);
     tma_prefetch_desc(&map_do);
     tma_prefetch_desc(&map_o);
+    for (int b = 0; b < 5; ++b) {
+      tma_prefetch_desc(&gmap_k.box[b]);
+      tma_prefetch_desc(&gmap_v.box[b]);
+    }
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_s, 512);
@@ -271,8 +287,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const int id = item_fetch(p.sched, p.n_items);
       if (id >= 0) {
         nqt = __ldg(p.order + id / p.hq);
-        nbeg = __ldg(p.qt_ptr + nqt);
-        nend = __ldg(p.qt_ptr + nqt + 1);
+        nbeg = __ldg(p.gq_ptr + nqt);
+        nend = __ldg(p.gq_ptr + nqt + 1);
       }
       return id;
     };
@@ -300,28 +316,36 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       }
       __syncwarp();
       ++kk;
+      // this lane's atom and the bounds row of the next tile, one tile ahead
+      int arow_next = 0, bidx_next = -1;
+      if (beg < end) {
+        arow_next = ldg_pinned(p.gt_atom + 16 * beg + (lane & 15));
+        bidx_next = ldg_pinned(p.gt_bidx + beg);
+      }
       for (int t = beg; t < end; ++t, ++kv, ++kk) {
-        const int row0 = p.qt_kt[t] * 128;
+        const int arow = arow_next, bidx = bidx_next;
+        if (t + 1 < end) {
+          arow_next = ldg_pinned(p.gt_atom + 16 * (t + 1) + (lane & 15));
+          bidx_next = ldg_pinned(p.gt_bidx + t + 1);
+        }
         const uint32_t sk = kk % kDqKStages;
         if (!(ok = k_slot_free(kk))) break;
+        uint8_t* kdst = smem + kDqOffK + sk * kTileBytes;
         if (lane == 0) {
-          uint8_t* dst = smem + kDqOffK + sk * kTileBytes;
-          // the tile's 128 key bounds travel with it (key_end is padded to
-          // whole tiles on the device)
-          mbar_arrive_expect_tx(&bar_k_full[sk], kTileBytes + 512);
-          tma_load_3d(dst, &map_k, &bar_k_full[sk], 0, kvh, row0);
-          tma_load_3d(dst + kHalfBytes, &map_k, &bar_k_full[sk], 64, kvh, row0);
-          bulk_load(smem + kDqOffKe + sk * 512, p.key_end + row0, 512, &bar_k_full[sk]);
+          // a PARTIAL tile's 128 key bounds travel with it
+          mbar_arrive_expect_tx(&bar_k_full[sk], kTileBytes + (bidx >= 0 ? 512u : 0u));
+          if (bidx >= 0)
+            bulk_load(smem + kDqOffKe + sk * 512, p.gt_bounds + static_cast<size_t>(bidx) * 128, 512,
+                      &bar_k_full[sk]);
         }
+        __syncwarp();
+        load_gathered(kdst, gmap_k, &bar_k_full[sk], kvh, arow, lane);
         __syncwarp();
         const uint32_t sv = kv % kDqVStages, pv = (kv / kDqVStages) & 1;
         if (kv >= kDqVStages && !(ok = warp_wait(&bar_v_empty[sv], pv ^ 1, abort, p.status))) break;
-        if (lane == 0) {
-          uint8_t* dst = smem + kDqOffV + sv * kTileBytes;
-          mbar_arrive_expect_tx(&bar_v_full[sv], kTileBytes);
-          tma_load_3d(dst, &map_v, &bar_v_full[sv], 0, kvh, row0);
-          tma_load_3d(dst + kHalfBytes, &map_v, &bar_v_full[sv], 64, kvh, row0);
-        }
+        if (lane == 0) mbar_arrive_expect_tx(&bar_v_full[sv], kTileBytes);
+        __syncwarp();
+        load_gathered(smem + kDqOffV + sv * kTileBytes, gmap_v, &bar_v_full[sv], kvh, arow, lane);
         __syncwarp();
       }
       if (!ok) break;
@@ -354,6 +378,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const uint32_t aQ = smem_u32(smem + kDqOffQ), aDO = smem_u32(smem + kDqOffDO);
     const uint32_t aK = smem_u32(smem + kDqOffK), aV = smem_u32(smem + kDqOffV);
     uint32_t kv = 0, kk = 0, qn = 0, n = 0, got = 0;
+    uint32_t dsu0 = 0, dsu1 = 0;  // dS phases consumed per S buffer
     bool ok = true;
     int hdr[3];
     for (int cur; (ok = item_get(&ring, got, cur, abort, p.status, hdr)) && cur >= 0;) {
@@ -407,7 +432,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           // the next item's Q and dO load during the last step.
           if (t + 2 == T) mma_commit_warp(&bar_q_empty);
         }
-        if (!(ok = warp_wait(&bar_ds_full, n & 1, abort, p.status))) break;
+        {
+          const bool odd = (t & 1) != 0;
+          if (!(ok = warp_wait(odd ? &bar_ds_full1 : &bar_ds_full0, (odd ? dsu1 : dsu0) & 1, abort,
+                               p.status)))
+            break;
+          dsu1 += odd ? 1u : 0u;
+          dsu0 += odd ? 0u : 1u;
+        }
         if (t == 0 && qn > 1 && !(ok = warp_wait(&bar_dq_free, (qn - 2) & 1, abort, p.status)))
           break;
         tc_fence_after_sync();
@@ -442,16 +474,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t col0 = half * 64;
     const float sl2 = p.scale_log2;
-    uint32_t n = 0, kk = 0, qn = 0, su[2] = {0, 0};  // kk: K ring entries (O, then K tiles)
+    uint32_t n = 0, kk = 0, qn = 0, su0 = 0, su1 = 0;  // kk: K ring entries (O, then K tiles)
     bool ok = true;
     // The next item's q-tile and tile range are read one item ahead, and each
     // tile's kind and k-tile one tile ahead, so no global load latency sits
     // between two passes over S. A tile's key bounds come with its K stage.
     int hdr[3] = {0, 0, 0};  // the next item's q-tile and tile range, from the ring
-    int nt_kind = 0, nt_kt = 0, nt_at = -1;
+    int nt_kind = 0, nt_arow = 0, nt_at = -1;  // nt_arow: first key of atom lane % 16
     auto fetch_tile = [&](int t) {
-      nt_kind = ldg_pinned(p.qt_kind + t);
-      nt_kt = ldg_pinned(p.qt_kt + t);
+      nt_kind = ldg_pinned(p.gt_kind + t) & 3;
+      nt_arow = ldg_pinned(p.gt_atom + 16 * t + (lane & 15));
       nt_at = t;
     };
     // The next item's number is read once this item's tiles are done (the
@@ -540,15 +572,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       ++qn;
       if (nt_at != beg) fetch_tile(beg);
       for (int t = beg; t < end; ++t, ++n, ++kk) {
-        const int kd = nt_kind, kt = nt_kt;
+        const int kd = nt_kind, tile_arow = nt_arow;
         if (t + 1 < end) fetch_tile(t + 1);
         // What this warp's 32 rows x 64 keys of the tile hold: 1 every pair
-        // visible (no mask), 0 a mix (mask per element; the j <= i half only
-        // where some key follows a row), 2 no visible pair (P = dS = 0: no
+        // visible (no mask), 0 a mix (mask per element; the key <= i half only
+        // where some key may follow a row), 2 no visible pair (P = dS = 0: no
         // exponentials, no dP read).
         int mode = kd == 2 ? 1 : 0;
         bool diag = false;
         const int* ke = nullptr;
+        int arow[8];  // first key of each atom of this half (column c: arow[c/8] + c%8)
         if (kd == 1) {  // PARTIAL: the tile's key bounds arrived with its K stage
           // (the stage is refilled only after this tile's dQ product, which
           // waits for every softmax thread's dS)
@@ -556,20 +589,29 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             break;
           ke = reinterpret_cast<const int*>(smem + kDqOffKe + (kk % kDqKStages) * 512) + col0;
           int mn = min(ke[lane], ke[lane + 32]), mx = max(ke[lane], ke[lane + 32]);
+          // this half's atoms are lanes 8*half .. 8*half+7 of the atom word
+          const bool mine = (lane & 15) >> 3 == half;
+          int amax = mine ? tile_arow : -8;
+          int amin = mine && tile_arow >= 0 ? tile_arow : 0x7fffffff;
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) {
             mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
             mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            amin = min(amin, __shfl_xor_sync(0xffffffffu, amin, o));
           }
-          const int r0 = qt * 128 + quarter * 32, jlo = kt * 128 + col0;
+#pragma unroll
+          for (int a = 0; a < 8; ++a) arow[a] = __shfl_sync(0xffffffffu, tile_arow, half * 8 + a);
+          const int r0 = qt * 128 + quarter * 32;
           // rows [r0, r0+32) see key j iff j <= row < key_end[j]
-          diag = jlo + 63 > r0;
-          mode = (mx <= r0 || jlo > r0 + 31) ? 2 : (!diag && mn > r0 + 31) ? 1 : 0;
+          diag = amax + 7 > r0;
+          mode = (mx <= r0 || amin > r0 + 31) ? 2 : (!diag && mn > r0 + 31) ? 1 : 0;
         }
         const int sb = (t - beg) & 1;
         const uint32_t tSb = tS + lane_off + sb * 128 + col0;
-        if (!(ok = warp_wait(&bar_s_full[sb], su[sb] & 1, abort, p.status))) break;
-        ++su[sb];
+        if (!(ok = warp_wait(&bar_s_full[sb], (sb ? su1 : su0) & 1, abort, p.status))) break;
+        su1 += sb ? 1u : 0u;
+        su0 += sb ? 0u : 1u;
         tc_fence_after_sync();
         float pv[64];
         if (mode != 2) {
@@ -580,11 +622,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             pv[jj] = ex2_approx(fmaf(__uint_as_float(rr[jj]), sl2, -lse2));
         }
         if (mode == 0 && diag) {
-          const int j0 = kt * 128 + col0;
 #pragma unroll
           for (int c4 = 0; c4 < 16; ++c4) {
             const int4 b = reinterpret_cast<const int4*>(ke)[c4];
-            const int j = j0 + 4 * c4;
+            const int j = arow[c4 >> 1] + 4 * (c4 & 1);  // key of this half's column 4*c4
             if (!(j + 0 <= i && i < b.x)) pv[4 * c4 + 0] = 0.f;
             if (!(j + 1 <= i && i < b.y)) pv[4 * c4 + 1] = 0.f;
             if (!(j + 2 <= i && i < b.z)) pv[4 * c4 + 2] = 0.f;
@@ -628,7 +669,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
         tmem_wait_st();
         tc_fence_before_sync();
-        mbar_arrive(&bar_ds_full);
+        mbar_arrive(sb ? &bar_ds_full1 : &bar_ds_full0);
       }
       if (!ok) break;
       if (!(ok = next_item(nxt))) break;
@@ -1086,10 +1127,11 @@ cudaError_t launch_bwd_bf16(const AttnBwdArgs& a) {
   const int sms = sm_count();
 
   DqParams d;
-  d.key_end = pl->dev.key_end;
-  d.qt_ptr = pl->dev.qt_ptr;
-  d.qt_kt = pl->dev.qt_kt;
-  d.qt_kind = pl->dev.qt_kind;
+  d.gq_ptr = pl->dev.gq_ptr;
+  d.gt_kind = pl->dev.gt_kind;
+  d.gt_atom = pl->dev.gt_atom;
+  d.gt_bidx = pl->dev.gt_bidx;
+  d.gt_bounds = pl->dev.gt_bounds;
   d.order = pl->dev.fwd_order;
   d.o = static_cast<const __nv_bfloat16*>(a.o);
   d.lse = a.lse;
@@ -1143,9 +1185,12 @@ cudaError_t launch_bwd_bf16(const AttnBwdArgs& a) {
   }
   if (a.phases & 1) {
     CUtensorMap mo;
-    if (!make_tile_map(&mo, a.o, N, a.hq)) return cudaErrorInvalidValue;
+    GatherMaps gk, gv;
+    if (!make_tile_map(&mo, a.o, N, a.hq) || !make_gather_maps(&gk, a.k, N, a.hkv) ||
+        !make_gather_maps(&gv, a.v, N, a.hkv))
+      return cudaErrorInvalidValue;
     tree_attn_bwd_dq_sm103<<<d.n_items < sms ? d.n_items : sms, kDqThreads, kDqSmem, a.stream>>>(
-        mq, mk, mv, mdo, mo, d);
+        mq, mk, mv, mdo, mo, gk, gv, d);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

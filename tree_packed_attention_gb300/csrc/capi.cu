@@ -110,7 +110,10 @@ extern "C" tree_status_t tree_plan_to_device(tree_plan_t* p, tree_stream_t strea
       {TREE_FIELD_QP_KT, &d.qp_kt},         {TREE_FIELD_QP_KIND, &d.qp_kind},
       {TREE_FIELD_QP_ORDER, &d.qp_order},   {TREE_FIELD_KT_QLO, &d.kt_qlo},
       {TREE_FIELD_KT_QHI, &d.kt_qhi},       {TREE_FIELD_BWD_ORDER, &d.bwd_order},
-      {TREE_FIELD_POS_ID, &d.pos_id},
+      {TREE_FIELD_POS_ID, &d.pos_id},       {TREE_FIELD_GQ_PTR, &d.gq_ptr},
+      {TREE_FIELD_GP_PTR, &d.gp_ptr},       {TREE_FIELD_GT_KIND, &d.gt_kind},
+      {TREE_FIELD_GT_ATOM, &d.gt_atom},     {TREE_FIELD_GT_BIDX, &d.gt_bidx},
+      {TREE_FIELD_GT_BOUNDS, &d.gt_bounds},
   };
   // key_end is padded with zeros to whole 128-key tiles: the kernels copy it
   // a tile at a time, and a zero bound hides the keys past N from every row.

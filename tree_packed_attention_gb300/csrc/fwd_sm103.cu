@@ -8,6 +8,14 @@
 // multiplied (the plan lists only non-empty tiles, as the FlashMask kernel of
 // App. A.1 skips masked blocks); FULL tiles skip the per-element mask.
 //
+// Key tiles are gathered: a work item's tiles hold the keys its rows see,
+// the keys every row sees first, packed as runs of consecutive keys starting
+// at multiples of 8 columns. A tile arrives as 16 TMA boxes of 8 key rows (one
+// per 128B-swizzle atom, each landing where a 128-row box would put those
+// rows), or as one 128-row box when its keys are consecutive. Column c holds
+// key atom_row[c/8] + c%8; on a PARTIAL tile row i sees it iff
+// key <= i < key_end[c] (key_end 0 for padding columns).
+//
 // CTA organisation (one persistent CTA per SM, 384 threads):
 //   warp 0     TMA producer: the two Q tiles of a work item, then K/V tiles
 //              into a 2-stage ring (128 keys x 128 dims each, 128B-swizzled).
@@ -31,6 +39,7 @@
 #include <cmath>
 
 #include "kernels.h"
+#include "gather.cuh"
 #include "sched.cuh"
 #include "sm103_ptx.cuh"
 #include "tma_host.h"
@@ -49,10 +58,11 @@ constexpr float kRescaleThreshold = 8.0f;
 constexpr uint32_t kRegsCtl = 72, kRegsSoftmax = 216;
 
 struct FwdParams {
-  const int32_t* key_end;
-  const int32_t* list_ptr;
-  const int32_t* list_kt;
-  const int32_t* list_kind;
+  const int32_t* list_ptr;   // item (q-tile or pair) -> its tiles in the gathered table
+  const int32_t* gt_kind;    // per tile: kind of slot 0 | kind of slot 1 << 2 (pairs)
+  const int32_t* gt_atom;    // per tile: first key row of each 8-column atom (-8: zeros)
+  const int32_t* gt_bidx;    // per tile: row of its key bounds, -1 if not PARTIAL
+  const int32_t* gt_bounds;  // per bounds row: key_end of each column
   const int32_t* order;
   __nv_bfloat16* o;
   float* lse;
@@ -100,44 +110,52 @@ __device__ __forceinline__ void read_header(const FwdParams& p, int it, int (&hd
 
 // Tile kinds of both slots packed as kind0 | kind1 << 2 (0 empty, 1 partial, 2 full).
 __device__ __forceinline__ int kinds_at(const FwdParams& p, int t) {
-  const int k = p.list_kind[t];
+  const int k = p.gt_kind[t];
   return p.mode == 0 ? (k | (k << 2)) : k;
 }
 
-// One tile of a slot's list as the softmax warps need it: its kind, its k-tile
-// and the tile's 128 key bounds, four per lane (keys kt*128 + lane + 32c;
-// key_end is zero-padded to whole tiles on the device).
+// One tile of a slot's list as the softmax warps need it: its kind, the first
+// key of atom (lane % 16), and on a PARTIAL tile the 128 key bounds, four per
+// lane (columns lane + 32c).
 struct TileInfo {
-  int kind, kt;
+  int kind, arow;
   int kev[4];
 };
 
-// A tile's kind and k-tile, loaded two tiles ahead; its key bounds, which
-// need the k-tile, one tile ahead (no dependent load inside a tile's time).
+// A tile's kind, bounds row and atom, loaded two tiles ahead; its key bounds,
+// which need the bounds row, one tile ahead (no dependent load inside a
+// tile's time).
 struct TileHead {
-  int kind, kt;
+  int kind, bidx, arow;
 };
 
-__device__ __forceinline__ TileHead load_head(const FwdParams& p, int t, int s) {
+__device__ __forceinline__ TileHead load_head(const FwdParams& p, int t, int s, int lane) {
   TileHead x;
-  const int k = ldg_pinned(p.list_kind + t);
+  const int k = ldg_pinned(p.gt_kind + t);
   x.kind = ((p.mode == 0 ? (k | (k << 2)) : k) >> (2 * s)) & 3;
-  x.kt = ldg_pinned(p.list_kt + t);
+  x.bidx = ldg_pinned(p.gt_bidx + t);
+  x.arow = ldg_pinned(p.gt_atom + 16 * t + (lane & 15));
   return x;
 }
 
 __device__ __forceinline__ TileInfo complete_tile(const FwdParams& p, TileHead h, int lane) {
   TileInfo x;
   x.kind = h.kind;
-  x.kt = h.kt;
+  x.arow = h.arow;
+  if (h.kind == 1) {
 #pragma unroll
-  for (int c = 0; c < 4; ++c) x.kev[c] = ldg_pinned(p.key_end + x.kt * 128 + lane + 32 * c);
+    for (int c = 0; c < 4; ++c) x.kev[c] = ldg_pinned(p.gt_bounds + h.bidx * 128 + lane + 32 * c);
+  } else {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) x.kev[c] = 0;
+  }
   return x;
 }
 
 __device__ __forceinline__ TileInfo load_tile(const FwdParams& p, int t, int s, int lane) {
-  return complete_tile(p, load_head(p, t, s), lane);
+  return complete_tile(p, load_head(p, t, s, lane), lane);
 }
+
 
 // (a wait that gives up records the line it was called from)
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
@@ -171,8 +189,8 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
 
 __global__ void __launch_bounds__(kThreads, 1)
     tree_attn_fwd_sm103(const __grid_constant__ CUtensorMap map_q,
-                        const __grid_constant__ CUtensorMap map_k,
-                        const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
+                        const __grid_constant__ GatherMaps map_k,
+                        const __grid_constant__ GatherMaps map_v, const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -214,8 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&map_q);
-    tma_prefetch_desc(&map_k);
-    tma_prefetch_desc(&map_v);
+    for (int b = 0; b < 5; ++b) {
+      tma_prefetch_desc(&map_k.box[b]);
+      tma_prefetch_desc(&map_v.box[b]);
+    }
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_s, 512);
@@ -256,22 +276,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       ++qn;
+      int arow_next = x.beg < x.end ? ldg_pinned(p.gt_atom + 16 * x.beg + (lane & 15)) : 0;
       for (int t = x.beg; t < x.end; ++t, ++kv) {
-        const int row0 = p.list_kt[t] * 128;
+        const int arow = arow_next;  // this lane's atom of tile t; the next tile's one ahead
+        if (t + 1 < x.end) arow_next = ldg_pinned(p.gt_atom + 16 * (t + 1) + (lane & 15));
         const uint32_t st = kv % kStages, ph = (kv / kStages) & 1;
         if (kv >= kStages && !(ok = warp_wait(&bar_k_empty[st], ph ^ 1, abort, p.status))) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bar_k_full[st], kTileBytes);
-          tma_load_3d(sK + st * kTileBytes, &map_k, &bar_k_full[st], 0, x.kvh, row0);
-          tma_load_3d(sK + st * kTileBytes + kHalfBytes, &map_k, &bar_k_full[st], 64, x.kvh, row0);
-        }
+        if (lane == 0) mbar_arrive_expect_tx(&bar_k_full[st], kTileBytes);
+        __syncwarp();
+        load_gathered(sK + st * kTileBytes, map_k, &bar_k_full[st], x.kvh, arow, lane);
         __syncwarp();
         if (kv >= kStages && !(ok = warp_wait(&bar_v_empty[st], ph ^ 1, abort, p.status))) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bar_v_full[st], kTileBytes);
-          tma_load_3d(sV + st * kTileBytes, &map_v, &bar_v_full[st], 0, x.kvh, row0);
-          tma_load_3d(sV + st * kTileBytes + kHalfBytes, &map_v, &bar_v_full[st], 64, x.kvh, row0);
-        }
+        if (lane == 0) mbar_arrive_expect_tx(&bar_v_full[st], kTileBytes);
+        __syncwarp();
+        load_gathered(sV + st * kTileBytes, map_v, &bar_v_full[st], x.kvh, arow, lane);
         __syncwarp();
       }
       if (!ok) break;
@@ -419,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_ref = -INFINITY, l = 0.f;
       if (nt_at != beg) {
         nt = load_tile(p, beg, s, lane);
-        if (beg + 1 < end) nn = load_head(p, beg + 1, s);
+        if (beg + 1 < end) nn = load_head(p, beg + 1, s, lane);
       }
       for (int t = beg; t < end; ++t) {
         const TileInfo tl = nt;
@@ -427,16 +445,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           nt_at = t + 1;
           nt = complete_tile(p, nn, lane);
         }
-        if (t + 2 < end) nn = load_head(p, t + 2, s);
+        if (t + 2 < end) nn = load_head(p, t + 2, s, lane);
         const int kd = tl.kind;
         if (kd == 0) continue;
-        const int kt = tl.kt;
         // What this warp's 32 rows of the tile hold: 1 every pair visible (no
-        // mask), 0 a mix (mask per element; the j <= i half only where some
-        // key follows a row), 2 no visible pair (P = 0, no exponentials).
+        // mask), 0 a mix (mask per element; the key <= i half only where some
+        // key may follow a row), 2 no visible pair (P = 0, no exponentials).
         int mode = kd == 2 ? 1 : 0;
         bool diag = false;
         const int* ke = nullptr;
+        int arow[16];  // first key of each atom (column c holds arow[c/8] + c%8)
         if (kd == 1) {  // PARTIAL: the warp's own copy of the tile's key bounds
           int* kw = ke_w[warp - 4];
           __syncwarp();  // every lane is done with the previous tile's copy
@@ -446,15 +464,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           ke = kw;
           int mn = min(min(tl.kev[0], tl.kev[1]), min(tl.kev[2], tl.kev[3]));
           int mx = max(max(tl.kev[0], tl.kev[1]), max(tl.kev[2], tl.kev[3]));
+          // over the atoms that hold keys: the largest first key (keys reach
+          // at most 7 past it) and the smallest
+          int amax = tl.arow, amin = tl.arow >= 0 ? tl.arow : 0x7fffffff;
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) {
             mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
             mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            amin = min(amin, __shfl_xor_sync(0xffffffffu, amin, o));
           }
-          const int r0 = qt * 128 + quarter * 32, jlo = kt * 128;
+#pragma unroll
+          for (int a = 0; a < 16; ++a) arow[a] = __shfl_sync(0xffffffffu, tl.arow, a);
+          const int r0 = qt * 128 + quarter * 32;
           // rows [r0, r0+32) see key j iff j <= row < key_end[j]
-          diag = jlo + 127 > r0;
-          mode = (mx <= r0 || jlo > r0 + 31) ? 2 : (!diag && mn > r0 + 31) ? 1 : 0;
+          diag = amax + 7 > r0;
+          mode = (mx <= r0 || amin > r0 + 31) ? 2 : (!diag && mn > r0 + 31) ? 1 : 0;
         }
         if (!(ok = warp_wait(&bar_s_full[s], sc & 1, abort, p.status))) break;
         ++sc;
@@ -478,12 +503,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int jj = 0; jj < 128; ++jj) sv[jj] = __uint_as_float(rr[jj]);
         }
         if (mode == 0) {
-          const int j0 = kt * 128;
           if (diag) {
 #pragma unroll
             for (int c4 = 0; c4 < 32; ++c4) {
               const int4 b = reinterpret_cast<const int4*>(ke)[c4];
-              const int j = j0 + 4 * c4;
+              const int j = arow[c4 >> 1] + 4 * (c4 & 1);  // key of column 4*c4
               if (!(j + 0 <= i && i < b.x)) sv[4 * c4 + 0] = -INFINITY;
               if (!(j + 1 <= i && i < b.y)) sv[4 * c4 + 1] = -INFINITY;
               if (!(j + 2 <= i && i < b.z)) sv[4 * c4 + 2] = -INFINITY;
@@ -558,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fetch_header(nxt);
         nt_at = n_beg;
         nt = load_tile(p, nt_at, s, lane);
-        if (n_beg + 1 < n_end) nn = load_head(p, n_beg + 1, s);
+        if (n_beg + 1 < n_end) nn = load_head(p, n_beg + 1, s, lane);
       }
       // ---- epilogue: O / l and lse
       if (!(ok = warp_wait(&bar_o_full[s], oc & 1, abort, p.status))) break;
@@ -606,25 +630,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_fwd_bf16(const AttnArgs& a) {
   const tree_plan* pl = a.plan;
-  CUtensorMap mq, mk, mv;
-  if (!make_tile_map(&mq, a.q, pl->N, a.hq) || !make_tile_map(&mk, a.k, pl->N, a.hkv) ||
-      !make_tile_map(&mv, a.v, pl->N, a.hkv))
+  CUtensorMap mq;
+  GatherMaps mk, mv;
+  if (!make_tile_map(&mq, a.q, pl->N, a.hq) || !make_gather_maps(&mk, a.k, pl->N, a.hkv) ||
+      !make_gather_maps(&mv, a.v, pl->N, a.hkv))
     return cudaErrorInvalidValue;
   FwdParams p;
   const int G = a.hq / a.hkv;
   p.mode = (G >= 2 && G % 2 == 0) ? 0 : 1;
-  p.key_end = pl->dev.key_end;
+  p.gt_kind = pl->dev.gt_kind;
+  p.gt_atom = pl->dev.gt_atom;
+  p.gt_bidx = pl->dev.gt_bidx;
+  p.gt_bounds = pl->dev.gt_bounds;
   if (p.mode == 0) {
-    p.list_ptr = pl->dev.qt_ptr;
-    p.list_kt = pl->dev.qt_kt;
-    p.list_kind = pl->dev.qt_kind;
+    p.list_ptr = pl->dev.gq_ptr;
     p.order = pl->dev.fwd_order;
     p.n_inner = a.hq / 2;
     p.n_items = pl->Tq * p.n_inner;
   } else {
-    p.list_ptr = pl->dev.qp_ptr;
-    p.list_kt = pl->dev.qp_kt;
-    p.list_kind = pl->dev.qp_kind;
+    p.list_ptr = pl->dev.gp_ptr;
     p.order = pl->dev.qp_order;
     p.n_inner = a.hq;
     p.n_items = pl->P * p.n_inner;

@@ -33,6 +33,154 @@ tree_status_t fail(tree_status_t st, const std::string& msg) {
 
 namespace {
 
+// Visible pairs between rows [ra, rb) and keys [k0, k1) that all share the
+// bound E (one segment): row i sees key j iff j <= i < E.
+int64_t run_pairs(int64_t k0, int64_t k1, int64_t E, int64_t ra, int64_t rb) {
+  const int64_t hi = std::min(rb, E);
+  if (hi <= ra || k1 <= k0) return 0;
+  int64_t total = 0;
+  const int64_t c = std::min(k1, ra + 1);  // keys at or before the first row see every row up to hi
+  if (c > k0) total += (c - k0) * (hi - ra);
+  const int64_t d0 = std::max(k0, ra + 1), d1 = std::min(k1, hi);  // key j sees rows [j, hi)
+  if (d1 > d0) total += (d1 - d0) * (2 * hi - d0 - d1 + 1) / 2;
+  return total;
+}
+
+// Gathered key tiles for units of U query rows (U = 128 or 256); appends to
+// the tile table and writes the unit -> tile CSR into ptr.
+void build_gathered(tree_plan* p, int32_t U, std::vector<int32_t>& ptr) {
+  auto& F = p->field;
+  const int32_t N = p->N;
+  const auto& tok_seg = F[TREE_FIELD_TOKEN_SEG];
+  const auto& seg_start = F[TREE_FIELD_SEG_START];
+  const auto& sub_end = F[TREE_FIELD_SUBTREE_END];
+  const auto& anc_ptr = F[TREE_FIELD_ANC_PTR];
+  const auto& anc_idx = F[TREE_FIELD_ANC_IDX];
+  const auto& key_end = F[TREE_FIELD_KEY_END];
+  auto& kind = F[TREE_FIELD_GT_KIND];
+  auto& atom = F[TREE_FIELD_GT_ATOM];
+  auto& bidx = F[TREE_FIELD_GT_BIDX];
+  auto& bounds = F[TREE_FIELD_GT_BOUNDS];
+  const int32_t units = (N + U - 1) / U;
+  const int32_t slots = U / kBlockM;
+  ptr.assign(units + 1, static_cast<int32_t>(kind.size()));
+  std::vector<int32_t> len_of(p->S);
+  for (int32_t s = 0; s < p->S; ++s) len_of[s] = 0;
+  for (int32_t t = 0; t < N; ++t) ++len_of[tok_seg[t]];
+  using Iv = std::pair<int32_t, int32_t>;
+  std::vector<Iv> iv, merged, common, rest, runs;
+  struct Piece { int32_t col, key, n; };
+  for (int32_t u = 0; u < units; ++u) {
+    const int32_t r0 = u * U, r1 = std::min(N, r0 + U);
+    // keys seen by some row: per spanned segment its ancestors and its own
+    // prefix up to its last row in the unit
+    iv.clear();
+    for (int32_t r = r0; r < r1;) {
+      const int32_t s = tok_seg[r];
+      const int32_t se = seg_start[s] + len_of[s];
+      const int32_t rb = std::min(r1, se);
+      for (int32_t e = anc_ptr[s]; e < anc_ptr[s + 1]; ++e) {
+        const int32_t a = anc_idx[e];
+        iv.emplace_back(seg_start[a], seg_start[a] + len_of[a]);
+      }
+      iv.emplace_back(seg_start[s], rb);
+      r = rb;
+    }
+    std::sort(iv.begin(), iv.end());
+    merged.clear();
+    for (const Iv& x : iv) {
+      if (!merged.empty() && x.first <= merged.back().second)
+        merged.back().second = std::max(merged.back().second, x.second);
+      else
+        merged.push_back(x);
+    }
+    // split into keys every row sees (j <= r0 and key_end[j] >= r1) and the rest
+    common.clear();
+    rest.clear();
+    auto push = [](std::vector<Iv>& v, int32_t a, int32_t b) {
+      if (b <= a) return;
+      if (!v.empty() && v.back().second == a)
+        v.back().second = b;
+      else
+        v.emplace_back(a, b);
+    };
+    for (const Iv& x : merged) {
+      for (int32_t j = x.first; j < x.second;) {  // walk the interval by segments
+        const int32_t s = tok_seg[j];
+        const int32_t e = std::min(x.second, seg_start[s] + len_of[s]);
+        if (sub_end[s] >= r1) {
+          const int32_t c = std::min(e, r0 + 1);
+          push(common, j, std::max(j, c));
+          push(rest, std::max(j, c), e);
+        } else {
+          push(rest, j, e);
+        }
+        j = e;
+      }
+    }
+    runs.clear();
+    for (const Iv& x : common) push(runs, x.first, x.second);
+    for (const Iv& x : rest) push(runs, x.first, x.second);
+    // place the runs: each starts at an 8-aligned column, a tile holds 128
+    std::vector<std::vector<Piece>> tiles;
+    int32_t col = kBlockN;
+    for (const Iv& x : runs) {
+      int32_t k = x.first, n = x.second - x.first;
+      while (n > 0) {
+        if (col >= kBlockN) {
+          tiles.emplace_back();
+          col = 0;
+        }
+        const int32_t m = std::min(n, kBlockN - col);
+        tiles.back().push_back({col, k, m});
+        col += m;
+        k += m;
+        n -= m;
+      }
+      col = (col + 7) & ~7;
+    }
+    for (const auto& tp : tiles) {
+      int32_t kw = 0;
+      bool partial = false;
+      for (int32_t sl = 0; sl < slots; ++sl) {
+        const int32_t ra = r0 + sl * kBlockM, rb = std::min(r1, ra + kBlockM);
+        int32_t kd = kEmpty;
+        if (ra < rb) {
+          int64_t pairs = 0;
+          for (const Piece& pc : tp) {
+            for (int32_t j = pc.key; j < pc.key + pc.n;) {
+              const int32_t s = tok_seg[j];
+              const int32_t e = std::min(pc.key + pc.n, seg_start[s] + len_of[s]);
+              pairs += run_pairs(j, e, sub_end[s], ra, rb);
+              j = e;
+            }
+          }
+          if (pairs == int64_t{kBlockM} * kBlockN) kd = kFull;
+          else if (pairs > 0) kd = kPartial;
+        }
+        partial = partial || kd == kPartial;
+        kw |= kd << (2 * sl);
+      }
+      kind.push_back(kw);
+      int32_t a_row[kBlockN / 8];
+      for (int32_t a = 0; a < kBlockN / 8; ++a) a_row[a] = -8;
+      for (const Piece& pc : tp)
+        for (int32_t c = pc.col; c < pc.col + pc.n; c += 8) a_row[c / 8] = pc.key + (c - pc.col);
+      atom.insert(atom.end(), a_row, a_row + kBlockN / 8);
+      if (partial) {
+        bidx.push_back(static_cast<int32_t>(bounds.size() / kBlockN));
+        const size_t b0 = bounds.size();
+        bounds.resize(b0 + kBlockN, 0);
+        for (const Piece& pc : tp)
+          for (int32_t c = 0; c < pc.n; ++c) bounds[b0 + pc.col + c] = key_end[pc.key + c];
+      } else {
+        bidx.push_back(-1);
+      }
+    }
+    ptr[u + 1] = static_cast<int32_t>(kind.size());
+  }
+}
+
 tree_status_t build(const int32_t* parents, const int32_t* lengths, int32_t S, tree_plan* p) {
   auto& F = p->field;
   // ---- validation
@@ -271,6 +419,12 @@ tree_status_t build(const int32_t* parents, const int32_t* lengths, int32_t S, t
   p->Tk = Tk;
   p->P = P;
   p->visible_pairs = visible;
+
+  // ---- gathered key tiles: q-tiles first, then q-tile pairs, one table
+  build_gathered(p, kBlockM, F[TREE_FIELD_GQ_PTR]);
+  build_gathered(p, 2 * kBlockM, F[TREE_FIELD_GP_PTR]);
+  if (F[TREE_FIELD_GT_KIND].size() > static_cast<size_t>(std::numeric_limits<int32_t>::max() / 16))
+    return fail(TREE_ERR_OVERFLOW, "too many gathered tiles");
   return TREE_OK;
 }
 
@@ -317,6 +471,7 @@ extern "C" tree_status_t tree_plan_info(const tree_plan_t* p, tree_plan_info_t* 
   out->nnz_pair_tiles = static_cast<int64_t>(p->field[TREE_FIELD_QP_KT].size());
   out->num_ancestors = static_cast<int64_t>(p->field[TREE_FIELD_ANC_IDX].size());
   out->visible_pairs = p->visible_pairs;
+  out->num_gathered_tiles = static_cast<int64_t>(p->field[TREE_FIELD_GT_KIND].size());
   return TREE_OK;
 }
 

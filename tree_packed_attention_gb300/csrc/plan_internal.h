@@ -34,6 +34,12 @@ struct DevicePlan {
   const int32_t* kt_qhi = nullptr;     // [Tk]
   const int32_t* bwd_order = nullptr;  // [Tk]
   const int32_t* pos_id = nullptr;     // [N]
+  const int32_t* gq_ptr = nullptr;     // [Tq+1]
+  const int32_t* gp_ptr = nullptr;     // [P+1]
+  const int32_t* gt_kind = nullptr;    // [gathered tiles]
+  const int32_t* gt_atom = nullptr;    // [gathered tiles * 16]
+  const int32_t* gt_bidx = nullptr;    // [gathered tiles]
+  const int32_t* gt_bounds = nullptr;  // [bounds rows * 256]
 };
 
 // Tables of the tree-correct causal conv for one kernel size (conv.cu): the

@@ -25,17 +25,23 @@ EncodeTiledFn encode_fn() {
 }
 }  // namespace
 
-bool make_tile_map(CUtensorMap* map, const void* base, int n, int heads) {
+bool make_tile_map(CUtensorMap* map, const void* base, int n, int heads, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(n)};
   const cuuint64_t strides[2] = {128 * 2, static_cast<cuuint64_t>(heads) * 128 * 2};
-  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t elem[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                   box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool make_gather_maps(GatherMaps* maps, const void* base, int n, int heads) {
+  for (int k = 0; k < 5; ++k)
+    if (!make_tile_map(&maps->box[k], base, n, heads, 8 << k)) return false;
+  return true;
 }
 
 int sm_count() {
