@@ -69,7 +69,8 @@ void build_gathered(tree_plan* p, int32_t U, std::vector<int32_t>& ptr) {
   for (int32_t t = 0; t < N; ++t) ++len_of[tok_seg[t]];
   using Iv = std::pair<int32_t, int32_t>;
   std::vector<Iv> iv, merged, common, rest, runs;
-  struct Piece { int32_t col, key, n; };
+  struct Piece { int32_t tile, col, key, n, every; };  // n keys from key at column col of a tile
+  std::vector<Piece> pieces;
   for (int32_t u = 0; u < units; ++u) {
     const int32_t r0 = u * U, r1 = std::min(N, r0 + U);
     // keys seen by some row: per spanned segment its ancestors and its own
@@ -120,26 +121,36 @@ void build_gathered(tree_plan* p, int32_t U, std::vector<int32_t>& ptr) {
     }
     runs.clear();
     for (const Iv& x : common) push(runs, x.first, x.second);
-    for (const Iv& x : rest) push(runs, x.first, x.second);
+    // runs[0 .. n_common) hold only keys every row of the unit sees (the run
+    // that joins the two lists, if any, counts as mixed)
+    size_t n_common = runs.size();
+    for (const Iv& x : rest) {
+      if (!runs.empty() && runs.back().second == x.first && runs.size() == n_common) --n_common;
+      push(runs, x.first, x.second);
+    }
     // place the runs: each starts at an 8-aligned column, a tile holds 128
-    std::vector<std::vector<Piece>> tiles;
-    int32_t col = kBlockN;
-    for (const Iv& x : runs) {
+    pieces.clear();
+    int32_t ntiles = 0, col = kBlockN;
+    for (size_t ri = 0; ri < runs.size(); ++ri) {
+      const Iv& x = runs[ri];
+      const int32_t every = ri < n_common ? 1 : 0;
       int32_t k = x.first, n = x.second - x.first;
       while (n > 0) {
         if (col >= kBlockN) {
-          tiles.emplace_back();
+          ++ntiles;
           col = 0;
         }
         const int32_t m = std::min(n, kBlockN - col);
-        tiles.back().push_back({col, k, m});
+        pieces.push_back({ntiles - 1, col, k, m, every});
         col += m;
         k += m;
         n -= m;
       }
       col = (col + 7) & ~7;
     }
-    for (const auto& tp : tiles) {
+    for (size_t b = 0, e = 0; b < pieces.size(); b = e) {
+      const int32_t tile = pieces[b].tile;
+      while (e < pieces.size() && pieces[e].tile == tile) ++e;
       int32_t kw = 0;
       bool partial = false;
       for (int32_t sl = 0; sl < slots; ++sl) {
@@ -147,12 +158,17 @@ void build_gathered(tree_plan* p, int32_t U, std::vector<int32_t>& ptr) {
         int32_t kd = kEmpty;
         if (ra < rb) {
           int64_t pairs = 0;
-          for (const Piece& pc : tp) {
+          for (size_t q = b; q < e; ++q) {
+            const Piece& pc = pieces[q];
+            if (pc.every) {  // every row of the unit sees every key of the piece
+              pairs += static_cast<int64_t>(pc.n) * (rb - ra);
+              continue;
+            }
             for (int32_t j = pc.key; j < pc.key + pc.n;) {
               const int32_t s = tok_seg[j];
-              const int32_t e = std::min(pc.key + pc.n, seg_start[s] + len_of[s]);
-              pairs += run_pairs(j, e, sub_end[s], ra, rb);
-              j = e;
+              const int32_t se = std::min(pc.key + pc.n, seg_start[s] + len_of[s]);
+              pairs += run_pairs(j, se, sub_end[s], ra, rb);
+              j = se;
             }
           }
           if (pairs == int64_t{kBlockM} * kBlockN) kd = kFull;
@@ -164,15 +180,17 @@ void build_gathered(tree_plan* p, int32_t U, std::vector<int32_t>& ptr) {
       kind.push_back(kw);
       int32_t a_row[kBlockN / 8];
       for (int32_t a = 0; a < kBlockN / 8; ++a) a_row[a] = -8;
-      for (const Piece& pc : tp)
-        for (int32_t c = pc.col; c < pc.col + pc.n; c += 8) a_row[c / 8] = pc.key + (c - pc.col);
+      for (size_t q = b; q < e; ++q)
+        for (int32_t c = pieces[q].col; c < pieces[q].col + pieces[q].n; c += 8)
+          a_row[c / 8] = pieces[q].key + (c - pieces[q].col);
       atom.insert(atom.end(), a_row, a_row + kBlockN / 8);
       if (partial) {
         bidx.push_back(static_cast<int32_t>(bounds.size() / kBlockN));
         const size_t b0 = bounds.size();
         bounds.resize(b0 + kBlockN, 0);
-        for (const Piece& pc : tp)
-          for (int32_t c = 0; c < pc.n; ++c) bounds[b0 + pc.col + c] = key_end[pc.key + c];
+        for (size_t q = b; q < e; ++q)
+          for (int32_t c = 0; c < pieces[q].n; ++c)
+            bounds[b0 + pieces[q].col + c] = key_end[pieces[q].key + c];
       } else {
         bidx.push_back(-1);
       }
@@ -421,6 +439,12 @@ tree_status_t build(const int32_t* parents, const int32_t* lengths, int32_t S, t
   p->visible_pairs = visible;
 
   // ---- gathered key tiles: q-tiles first, then q-tile pairs, one table
+  {
+    const size_t est = static_cast<size_t>(nnz) * 3 / 2 + 16;  // about nnz + nnz / 2 tiles
+    F[TREE_FIELD_GT_KIND].reserve(est);
+    F[TREE_FIELD_GT_BIDX].reserve(est);
+    F[TREE_FIELD_GT_ATOM].reserve(est * (kBlockN / 8));
+  }
   build_gathered(p, kBlockM, F[TREE_FIELD_GQ_PTR]);
   build_gathered(p, 2 * kBlockM, F[TREE_FIELD_GP_PTR]);
   if (F[TREE_FIELD_GT_KIND].size() > static_cast<size_t>(std::numeric_limits<int32_t>::max() / 16))
