@@ -18,7 +18,8 @@
 //
 // CTA organisation (one persistent CTA per SM, 384 threads):
 //   warp 0     TMA producer: the two Q tiles of a work item, then K/V tiles
-//              into a 2-stage ring (128 keys x 128 dims each, 128B-swizzled).
+//              into a 2-stage ring (128 keys x 128 dims each, 128B-swizzled);
+//              a PARTIAL tile's 128 key bounds travel with its V tile.
 //   warp 1     TMEM owner and MMA issuer (one thread issues tcgen05.mma).
 //   warps 4-7  softmax for Q slot 0;  warps 8-11 softmax for Q slot 1.
 // A work item is two 128-row Q tiles that share K/V: two q heads of one kv
@@ -32,6 +33,9 @@
 // previous PV into O_s is complete too and O_s may be rescaled in place.
 // The running max is updated lazily: O and l are rescaled only when the max
 // grows by more than 8 (log2 units), which keeps every P <= 2^8.
+// The epilogue writes O / l as bf16 into a 16 KB staging tile per slot, 64
+// columns at a time, and one thread of the slot stores it with TMA, so the
+// softmax warps do not wait for the global stores.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -53,7 +57,20 @@ constexpr int kThreads = 384;
 constexpr int kStages = 2;
 constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one 128 x 128 bf16 operand tile
 constexpr uint32_t kHalfBytes = kTileBytes / 2;  // its 64-column half (one TMA box)
-constexpr uint32_t kSmemBytes = 1024 + 2 * kTileBytes + 2 * kStages * kTileBytes;
+// Shared memory (dynamic, 1024-byte aligned; no static shared variables, so
+// the block starts aligned as the 128B-swizzled tiles need).
+constexpr uint32_t kOffQ = 0;                                    // 2 slots
+constexpr uint32_t kOffK = kOffQ + 2 * kTileBytes;               // kStages
+constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;         // kStages
+constexpr uint32_t kStageBytes = kHalfBytes;                     // 128 rows x 64 columns bf16
+constexpr uint32_t kOffStage = kOffV + kStages * kTileBytes;     // 2 slots
+constexpr uint32_t kOffBounds = kOffStage + 2 * kStageBytes;     // per V stage: 128 key_end
+constexpr uint32_t kOffBar = kOffBounds + kStages * 512;
+constexpr uint32_t kNumBars = 3 + 4 * kStages + 6 * 2;
+constexpr uint32_t kOffRing = kOffBar + kNumBars * 8;
+constexpr uint32_t kOffMisc = kOffRing + sizeof(ItemRing);
+constexpr uint32_t kSmemBytes = kOffMisc + 16;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr float kRescaleThreshold = 8.0f;
 constexpr uint32_t kRegsCtl = 72, kRegsSoftmax = 216;
 
@@ -64,12 +81,10 @@ struct FwdParams {
   const int32_t* gt_bidx;    // per tile: row of its key bounds, -1 if not PARTIAL
   const int32_t* gt_bounds;  // per bounds row: key_end of each column
   const int32_t* order;
-  __nv_bfloat16* o;
   float* lse;
   int* status;
   SchedSlot* sched;
   int N, hq, group, n_items, n_inner, mode, Tq;
-  int o_v8;  // o is 32-byte aligned: rows are written with 32-byte stores
   float scale_log2;  // softmax scale * log2(e)
 };
 
@@ -108,52 +123,19 @@ __device__ __forceinline__ void read_header(const FwdParams& p, int it, int (&hd
   hdr[2] = __ldg(p.list_ptr + hdr[0] + 1);
 }
 
-// Tile kinds of both slots packed as kind0 | kind1 << 2 (0 empty, 1 partial, 2 full).
-__device__ __forceinline__ int kinds_at(const FwdParams& p, int t) {
-  const int k = p.gt_kind[t];
-  return p.mode == 0 ? (k | (k << 2)) : k;
-}
-
-// One tile of a slot's list as the softmax warps need it: its kind, the first
-// key of atom (lane % 16), and on a PARTIAL tile the 128 key bounds, four per
-// lane (columns lane + 32c).
+// One tile of a slot's list as the softmax warps need it, loaded two tiles
+// ahead: its kind for this slot and the first key of atom (lane % 16). A
+// PARTIAL tile's key bounds come with its V stage.
 struct TileInfo {
   int kind, arow;
-  int kev[4];
 };
-
-// A tile's kind, bounds row and atom, loaded two tiles ahead; its key bounds,
-// which need the bounds row, one tile ahead (no dependent load inside a
-// tile's time).
-struct TileHead {
-  int kind, bidx, arow;
-};
-
-__device__ __forceinline__ TileHead load_head(const FwdParams& p, int t, int s, int lane) {
-  TileHead x;
-  const int k = ldg_pinned(p.gt_kind + t);
-  x.kind = ((p.mode == 0 ? (k | (k << 2)) : k) >> (2 * s)) & 3;
-  x.bidx = ldg_pinned(p.gt_bidx + t);
-  x.arow = ldg_pinned(p.gt_atom + 16 * t + (lane & 15));
-  return x;
-}
-
-__device__ __forceinline__ TileInfo complete_tile(const FwdParams& p, TileHead h, int lane) {
-  TileInfo x;
-  x.kind = h.kind;
-  x.arow = h.arow;
-  if (h.kind == 1) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) x.kev[c] = ldg_pinned(p.gt_bounds + h.bidx * 128 + lane + 32 * c);
-  } else {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) x.kev[c] = 0;
-  }
-  return x;
-}
 
 __device__ __forceinline__ TileInfo load_tile(const FwdParams& p, int t, int s, int lane) {
-  return complete_tile(p, load_head(p, t, s, lane), lane);
+  TileInfo x;
+  const int k = ldg_pinned(p.gt_kind + t);
+  x.kind = ((p.mode == 0 ? (k | (k << 2)) : k) >> (2 * s)) & 3;
+  x.arow = ldg_pinned(p.gt_atom + 16 * t + (lane & 15));
+  return x;
 }
 
 
@@ -190,22 +172,33 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
 __global__ void __launch_bounds__(kThreads, 1)
     tree_attn_fwd_sm103(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ GatherMaps map_k,
-                        const __grid_constant__ GatherMaps map_v, const FwdParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;                   // 2 slots
-  uint8_t* sK = smem + 2 * kTileBytes;  // kStages
-  uint8_t* sV = sK + kStages * kTileBytes;
-
-  __shared__ uint64_t bar_q_full, bar_q_empty, bar_final;
-  __shared__ uint64_t bar_k_full[kStages], bar_k_empty[kStages];
-  __shared__ uint64_t bar_v_full[kStages], bar_v_empty[kStages];
-  __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_o_full[2], bar_o_free[2];
-  __shared__ __align__(16) int ke_w[8][128];  // each softmax warp's copy of a tile's key bounds
-  __shared__ ItemRing ring;
-  __shared__ uint32_t tmem_base_s;
-  __shared__ int abort_s;
+                        const __grid_constant__ GatherMaps map_v,
+                        const __grid_constant__ CUtensorMap map_o, const FwdParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) atomicExch(p.status, 9);
+    return;
+  }
+  uint8_t* sQ = smem + kOffQ;
+  uint8_t* sK = smem + kOffK;
+  uint8_t* sV = smem + kOffV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t& bar_q_full = bars[0];
+  uint64_t& bar_q_empty = bars[1];
+  uint64_t& bar_final = bars[2];
+  uint64_t* bar_k_full = bars + 3;
+  uint64_t* bar_k_empty = bar_k_full + kStages;
+  uint64_t* bar_v_full = bar_k_empty + kStages;
+  uint64_t* bar_v_empty = bar_v_full + kStages;
+  uint64_t* bar_s_full = bar_v_empty + kStages;  // [2] per slot from here on
+  uint64_t* bar_p_full = bar_s_full + 2;
+  uint64_t* bar_o_full = bar_p_full + 2;
+  uint64_t* bar_o_free = bar_o_full + 2;
+  uint64_t* bar_stage_full = bar_o_free + 2;  // the slot's 128 threads wrote a staging half
+  uint64_t* bar_stage_free = bar_stage_full + 2;  // its TMA store has read the staging tile
+  ItemRing& ring = *reinterpret_cast<ItemRing*>(smem + kOffRing);
+  uint32_t& tmem_base_s = *reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  int& abort_s = *reinterpret_cast<int*>(smem + kOffMisc + 4);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   volatile int* abort = &abort_s;
@@ -226,12 +219,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_p_full[s], 128);
       mbar_init(&bar_o_full[s], 1);
       mbar_init(&bar_o_free[s], 128);
+      mbar_init(&bar_stage_full[s], 128);
+      mbar_init(&bar_stage_free[s], 1);
     }
     abort_s = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&map_q);
+    tma_prefetch_desc(&map_o);
     for (int b = 0; b < 5; ++b) {
       tma_prefetch_desc(&map_k.box[b]);
       tma_prefetch_desc(&map_v.box[b]);
@@ -276,10 +272,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       ++qn;
-      int arow_next = x.beg < x.end ? ldg_pinned(p.gt_atom + 16 * x.beg + (lane & 15)) : 0;
+      // this lane's atom and the bounds row of the next tile, one tile ahead
+      int arow_next = 0, bidx_next = -1;
+      if (x.beg < x.end) {
+        arow_next = ldg_pinned(p.gt_atom + 16 * x.beg + (lane & 15));
+        bidx_next = ldg_pinned(p.gt_bidx + x.beg);
+      }
       for (int t = x.beg; t < x.end; ++t, ++kv) {
-        const int arow = arow_next;  // this lane's atom of tile t; the next tile's one ahead
-        if (t + 1 < x.end) arow_next = ldg_pinned(p.gt_atom + 16 * (t + 1) + (lane & 15));
+        const int arow = arow_next, bidx = bidx_next;
+        if (t + 1 < x.end) {
+          arow_next = ldg_pinned(p.gt_atom + 16 * (t + 1) + (lane & 15));
+          bidx_next = ldg_pinned(p.gt_bidx + t + 1);
+        }
         const uint32_t st = kv % kStages, ph = (kv / kStages) & 1;
         if (kv >= kStages && !(ok = warp_wait(&bar_k_empty[st], ph ^ 1, abort, p.status))) break;
         if (lane == 0) mbar_arrive_expect_tx(&bar_k_full[st], kTileBytes);
@@ -287,7 +291,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         load_gathered(sK + st * kTileBytes, map_k, &bar_k_full[st], x.kvh, arow, lane);
         __syncwarp();
         if (kv >= kStages && !(ok = warp_wait(&bar_v_empty[st], ph ^ 1, abort, p.status))) break;
-        if (lane == 0) mbar_arrive_expect_tx(&bar_v_full[st], kTileBytes);
+        if (lane == 0) {
+          // a PARTIAL tile's key bounds travel with its V tile: the stage is
+          // refilled only after the tile's PV products, which wait for P
+          mbar_arrive_expect_tx(&bar_v_full[st], kTileBytes + (bidx >= 0 ? 512u : 0u));
+          if (bidx >= 0)
+            bulk_load(smem + kOffBounds + st * 512, p.gt_bounds + static_cast<size_t>(bidx) * 128,
+                      512, &bar_v_full[st]);
+        }
         __syncwarp();
         load_gathered(sV + st * kTileBytes, map_v, &bar_v_full[st], x.kvh, arow, lane);
         __syncwarp();
@@ -318,26 +329,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- MMA issuer
     // The whole warp runs this branch; one elected lane issues each MMA.
     uint32_t kv = 0, qn = 0, got = 0;
-    uint32_t pc[2] = {0, 0}, oc[2] = {0, 0};
+    uint32_t pc0 = 0, pc1 = 0, oc0 = 0, oc1 = 0;  // P and O phases per slot
     const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
     bool ok = true;
     int hdr[3];
+    // Kinds of a tile for both slots (0 = no rows of the slot see it). With
+    // grouped heads both slots hold the same rows and every listed tile has
+    // a visible pair, so nothing is loaded; else they are read two tiles ahead.
+    auto kinds_ahead = [&](int t) { return p.mode == 0 ? 5 : ldg_pinned(p.gt_kind + t); };
     for (int cur; (ok = item_get(&ring, got, cur, abort, p.status, hdr)) && cur >= 0;) {
       const Item x = decode_item(p, cur, hdr);
       const int T = x.end - x.beg;
+      int kd_next = kinds_ahead(x.beg);                       // tile t
+      int kd_next2 = T > 1 ? kinds_ahead(x.beg + 1) : 0;      // tile t + 1
       if (!(ok = warp_wait(&bar_q_full, qn & 1, abort, p.status))) break;
       ++qn;
-      bool first[2] = {true, true};
+      bool first0 = true, first1 = true;
       {  // S(0)
         const uint32_t st = kv % kStages, ph = (kv / kStages) & 1;
         if (!(ok = warp_wait(&bar_k_full[st], ph, abort, p.status))) break;
         tc_fence_after_sync();
-        const int kd = kinds_at(p, x.beg);
-        for (int s = 0; s < 2; ++s) {
-          if ((kd >> (2 * s)) & 3) {
-            issue_qk(tmem + s * 128, q_addr + s * kTileBytes, k_addr + st * kTileBytes);
-            mma_commit_warp(&bar_s_full[s]);
-          }
+        if (kd_next & 3) {
+          issue_qk(tmem, q_addr, k_addr + st * kTileBytes);
+          mma_commit_warp(&bar_s_full[0]);
+        }
+        if ((kd_next >> 2) & 3) {
+          issue_qk(tmem + 128, q_addr + kTileBytes, k_addr + st * kTileBytes);
+          mma_commit_warp(&bar_s_full[1]);
         }
         mma_commit_warp(&bar_k_empty[st]);
         if (T == 1) mma_commit_warp(&bar_q_empty);
@@ -346,45 +364,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t kvt = kv + t;
         const uint32_t st = kvt % kStages, ph = (kvt / kStages) & 1;
         const uint32_t stn = (kvt + 1) % kStages, phn = ((kvt + 1) / kStages) & 1;
-        const int kd = kinds_at(p, x.beg + t);
+        const int kd = kd_next, kdn = kd_next2;
+        kd_next = kd_next2;
+        kd_next2 = t + 2 < T ? kinds_ahead(x.beg + t + 2) : 0;
         const bool has_next = t + 1 < T;
-        const int kdn = has_next ? kinds_at(p, x.beg + t + 1) : 0;
         if (!(ok = warp_wait(&bar_v_full[st], ph, abort, p.status))) break;
-        for (int s = 0; s < 2 && ok; ++s) {
-          if ((kd >> (2 * s)) & 3) {
-            if (!(ok = warp_wait(&bar_p_full[s], pc[s] & 1, abort, p.status))) break;
-            ++pc[s];
-            if (first[s] && oc[s] > 0 &&
-                !(ok = warp_wait(&bar_o_free[s], (oc[s] - 1) & 1, abort, p.status)))
-              break;
-            tc_fence_after_sync();
-            issue_pv(tmem + 256 + s * 128, tmem + s * 128, v_addr + st * kTileBytes, !first[s]);
-            first[s] = false;
-          }
-          if (has_next) {
-            if (s == 0) {
-              if (!(ok = warp_wait(&bar_k_full[stn], phn, abort, p.status))) break;
-              tc_fence_after_sync();
-            }
-            if ((kdn >> (2 * s)) & 3) {
-              issue_qk(tmem + s * 128, q_addr + s * kTileBytes, k_addr + stn * kTileBytes);
-              mma_commit_warp(&bar_s_full[s]);
-            }
+        // slot 0: PV(t), then S(t+1); slot 1 likewise
+        if (kd & 3) {
+          if (!(ok = warp_wait(&bar_p_full[0], pc0 & 1, abort, p.status))) break;
+          ++pc0;
+          if (first0 && oc0 > 0 && !(ok = warp_wait(&bar_o_free[0], (oc0 - 1) & 1, abort, p.status)))
+            break;
+          tc_fence_after_sync();
+          issue_pv(tmem + 256, tmem, v_addr + st * kTileBytes, !first0);
+          first0 = false;
+        }
+        if (!has_next && x.qtile[0] < p.Tq) {  // slot 0's O is final once this PV completes
+          mma_commit_warp(&bar_o_full[0]);
+          ++oc0;
+        }
+        if (has_next) {
+          if (!(ok = warp_wait(&bar_k_full[stn], phn, abort, p.status))) break;
+          tc_fence_after_sync();
+          if (kdn & 3) {
+            issue_qk(tmem, q_addr, k_addr + stn * kTileBytes);
+            mma_commit_warp(&bar_s_full[0]);
           }
         }
-        if (!ok) break;
+        if ((kd >> 2) & 3) {
+          if (!(ok = warp_wait(&bar_p_full[1], pc1 & 1, abort, p.status))) break;
+          ++pc1;
+          if (first1 && oc1 > 0 && !(ok = warp_wait(&bar_o_free[1], (oc1 - 1) & 1, abort, p.status)))
+            break;
+          tc_fence_after_sync();
+          issue_pv(tmem + 384, tmem + 128, v_addr + st * kTileBytes, !first1);
+          first1 = false;
+        }
+        if (!has_next && x.qtile[1] < p.Tq) {
+          mma_commit_warp(&bar_o_full[1]);
+          ++oc1;
+        }
+        if (has_next && ((kdn >> 2) & 3)) {
+          issue_qk(tmem + 128, q_addr + kTileBytes, k_addr + stn * kTileBytes);
+          mma_commit_warp(&bar_s_full[1]);
+        }
         mma_commit_warp(&bar_v_empty[st]);
         if (has_next) mma_commit_warp(&bar_k_empty[stn]);
         if (t + 2 == T) mma_commit_warp(&bar_q_empty);  // the item's last S MMAs were just issued
       }
       if (!ok) break;
       kv += T;
-      for (int s = 0; s < 2; ++s) {
-        if (x.qtile[s] < p.Tq) {
-          mma_commit_warp(&bar_o_full[s]);
-          ++oc[s];
-        }
-      }
     }
     mma_commit_warp(&bar_final);  // every MMA issued by this CTA completes before TMEM is freed
     if (lane == 0) mbar_drain(&bar_final, 0);
@@ -401,11 +430,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off + s * 128;
     const uint32_t tO = tmem + lane_off + 256 + s * 128;
     const float sl2 = p.scale_log2;
-    uint32_t sc = 0, oc = 0;
+    const bool issuer = quarter == 0 && lane == 0;  // stores the slot's staging tile
+    uint8_t* stage = smem + kOffStage + s * kStageBytes;
+    uint32_t sc = 0, oc = 0, halves = 0;  // S and O phases; staging halves written
+    uint32_t kvs = 0;                     // tiles so far (the V ring's counter)
     bool ok = true;
-    // The tile after the current one (in this item, else the next item's
-    // first) is loaded one tile ahead, and the next item's header one item
-    // ahead, so no global load latency sits between two softmax passes.
+    // The next item's header is read one item ahead, and the kind and atom of
+    // each tile two tiles ahead, so no global load latency sits between two
+    // softmax passes.
     int n_qt = 0, n_h = 0, n_beg = 0, n_end = 0;  // next item: q-tile, head, tile range
     int hdr[3];
     auto fetch_header = [&](int at) {
@@ -417,18 +449,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // The next item's number and header are read from the ring once this
     // item's tiles are done (the producer publishes them when this item's
-    // loads are issued); its first tile's loads overlap this epilogue.
+    // loads are issued); its first tiles' loads overlap this epilogue.
     uint32_t got = 0;
     int cur = -1;
     ok = item_get(&ring, got, cur, abort, p.status, hdr);
     if (ok && cur >= 0) fetch_header(cur);
-    TileInfo nt;      // the next tile
-    TileHead nn{};    // the one after it
+    TileInfo nt{}, nn{};  // tiles t+1 and t+2 of the walk
     int nt_at = -1;
     while (ok && cur >= 0) {
       const int qt = n_qt, h = n_h, beg = n_beg, end = n_end;
       int nxt = -1;
       if (qt >= p.Tq) {  // this slot has no rows in the item
+        kvs += end - beg;
         if ((ok = item_get(&ring, got, nxt, abort, p.status, hdr)) && nxt >= 0) fetch_header(nxt);
         cur = nxt;
         continue;
@@ -437,15 +469,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_ref = -INFINITY, l = 0.f;
       if (nt_at != beg) {
         nt = load_tile(p, beg, s, lane);
-        if (beg + 1 < end) nn = load_head(p, beg + 1, s, lane);
+        if (beg + 1 < end) nn = load_tile(p, beg + 1, s, lane);
       }
-      for (int t = beg; t < end; ++t) {
+      for (int t = beg; t < end; ++t, ++kvs) {
         const TileInfo tl = nt;
-        if (t + 1 < end) {
-          nt_at = t + 1;
-          nt = complete_tile(p, nn, lane);
-        }
-        if (t + 2 < end) nn = load_head(p, t + 2, s, lane);
+        nt = nn;
+        nt_at = t + 1;
+        if (t + 2 < end) nn = load_tile(p, t + 2, s, lane);
         const int kd = tl.kind;
         if (kd == 0) continue;
         // What this warp's 32 rows of the tile hold: 1 every pair visible (no
@@ -455,35 +485,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool diag = false;
         const int* ke = nullptr;
         int arow[16];  // first key of each atom (column c holds arow[c/8] + c%8)
-        if (kd == 1) {  // PARTIAL: the warp's own copy of the tile's key bounds
-          int* kw = ke_w[warp - 4];
-          __syncwarp();  // every lane is done with the previous tile's copy
-#pragma unroll
-          for (int c = 0; c < 4; ++c) kw[lane + 32 * c] = tl.kev[c];
-          __syncwarp();
-          ke = kw;
-          int mn = min(min(tl.kev[0], tl.kev[1]), min(tl.kev[2], tl.kev[3]));
-          int mx = max(max(tl.kev[0], tl.kev[1]), max(tl.kev[2], tl.kev[3]));
+        int amax = 0, amin = 0;
+        if (kd == 1) {
           // over the atoms that hold keys: the largest first key (keys reach
           // at most 7 past it) and the smallest
-          int amax = tl.arow, amin = tl.arow >= 0 ? tl.arow : 0x7fffffff;
+          amax = tl.arow;
+          amin = tl.arow >= 0 ? tl.arow : 0x7fffffff;
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) {
-            mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
             amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, o));
             amin = min(amin, __shfl_xor_sync(0xffffffffu, amin, o));
           }
 #pragma unroll
           for (int a = 0; a < 16; ++a) arow[a] = __shfl_sync(0xffffffffu, tl.arow, a);
+        }
+        if (!(ok = warp_wait(&bar_s_full[s], sc & 1, abort, p.status))) break;
+        ++sc;
+        tc_fence_after_sync();
+        if (kd == 1) {
+          // PARTIAL: the key bounds arrived with the tile's V stage. Waited for
+          // after S: S(t) was issued once the V loads of earlier tiles landed,
+          // so this stage's barrier cannot still be a phase behind tile t.
+          const uint32_t st = kvs % kStages, ph = (kvs / kStages) & 1;
+          if (!(ok = warp_wait(&bar_v_full[st], ph, abort, p.status))) break;
+          ke = reinterpret_cast<const int*>(smem + kOffBounds + st * 512);
+          const int4 kq = reinterpret_cast<const int4*>(ke)[lane];  // columns 4*lane .. +3
+          int mn = min(min(kq.x, kq.y), min(kq.z, kq.w));
+          int mx = max(max(kq.x, kq.y), max(kq.z, kq.w));
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          }
           const int r0 = qt * 128 + quarter * 32;
           // rows [r0, r0+32) see key j iff j <= row < key_end[j]
           diag = amax + 7 > r0;
           mode = (mx <= r0 || amin > r0 + 31) ? 2 : (!diag && mn > r0 + 31) ? 1 : 0;
         }
-        if (!(ok = warp_wait(&bar_s_full[s], sc & 1, abort, p.status))) break;
-        ++sc;
-        tc_fence_after_sync();
         if (mode == 2) {  // P = 0; m and l of the row are unchanged
           uint32_t pk[16];
 #pragma unroll
@@ -578,13 +616,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       if (!(ok = item_get(&ring, got, nxt, abort, p.status, hdr))) break;
-      if (nxt >= 0) {  // its header, and its first tile's loads during this epilogue
+      if (nxt >= 0) {  // its header, and its first tiles' loads during this epilogue
         fetch_header(nxt);
         nt_at = n_beg;
-        nt = load_tile(p, nt_at, s, lane);
-        if (n_beg + 1 < n_end) nn = load_head(p, n_beg + 1, s, lane);
+        nt = load_tile(p, n_beg, s, lane);
+        if (n_beg + 1 < n_end) nn = load_tile(p, n_beg + 1, s, lane);
       }
-      // ---- epilogue: O / l and lse
+      // ---- epilogue: O / l as bf16 through the staging tile, 64 columns at
+      // a time; the slot's first thread issues each half's TMA store (rows
+      // past N are not written by it)
       if (!(ok = warp_wait(&bar_o_full[s], oc & 1, abort, p.status))) break;
       ++oc;
       tc_fence_after_sync();
@@ -592,29 +632,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld128(tO, ov);  // the whole O row, one wait
       tc_fence_before_sync();
       mbar_arrive(&bar_o_free[s]);  // O_s is in registers: the next item's PV may start
-      if (i < p.N) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16* orow = p.o + (static_cast<size_t>(i) * p.hq + h) * 128;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {  // 16 columns = 32 bytes at a time
-          uint32_t pk[8];
+      for (int hf = 0; hf < 2; ++hf, ++halves) {
+        // the store of the previous half has read the staging tile
+        if (halves > 0 && !(ok = warp_wait(&bar_stage_free[s], (halves - 1) & 1, abort, p.status)))
+          break;
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj)
-            pk[jj] = pack_bf16x2(__uint_as_float(ov[16 * c + 2 * jj]) * inv,
-                                 __uint_as_float(ov[16 * c + 2 * jj + 1]) * inv);
-          if (p.o_v8) {
-            st_global_v8(orow + 16 * c, pk);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(orow + 16 * c);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          }
+        for (int c = 0; c < 8; ++c) {  // 16-byte chunk c of the row, 128B-swizzled
+          const int col = hf * 64 + c * 8;
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(ov[col + 0]) * inv, __uint_as_float(ov[col + 1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(ov[col + 2]) * inv, __uint_as_float(ov[col + 3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(ov[col + 4]) * inv, __uint_as_float(ov[col + 5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(ov[col + 6]) * inv, __uint_as_float(ov[col + 7]) * inv);
+          *reinterpret_cast<uint4*>(stage + r * 128 + ((c ^ (r & 7)) * 16)) = w;
         }
+        fence_proxy_async_shared();
+        mbar_arrive(&bar_stage_full[s]);
+        if (issuer) {
+          if (!(ok = mbar_wait(&bar_stage_full[s], halves & 1, abort, p.status, kSiteFwd + __LINE__)))
+            break;
+          tma_store_3d(&map_o, stage, hf * 64, h, qt * 128);
+          bulk_commit_group();
+          bulk_wait_group_read<0>();
+          mbar_arrive(&bar_stage_free[s]);
+        }
+      }
+      if (!__all_sync(0xffffffffu, ok)) break;
+      if (i < p.N)
         p.lse[static_cast<size_t>(h) * p.N + i] =
             l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
-      }
       cur = nxt;
     }
+    if (issuer) bulk_wait_group<0>();  // every O store has landed
   }
 
   tc_fence_before_sync();
@@ -630,10 +681,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_fwd_bf16(const AttnArgs& a) {
   const tree_plan* pl = a.plan;
-  CUtensorMap mq;
+  CUtensorMap mq, mo;
   GatherMaps mk, mv;
   if (!make_tile_map(&mq, a.q, pl->N, a.hq) || !make_gather_maps(&mk, a.k, pl->N, a.hkv) ||
-      !make_gather_maps(&mv, a.v, pl->N, a.hkv))
+      !make_gather_maps(&mv, a.v, pl->N, a.hkv) || !make_tile_map(&mo, a.o, pl->N, a.hq))
     return cudaErrorInvalidValue;
   FwdParams p;
   const int G = a.hq / a.hkv;
@@ -653,11 +704,9 @@ cudaError_t launch_fwd_bf16(const AttnArgs& a) {
     p.n_inner = a.hq;
     p.n_items = pl->P * p.n_inner;
   }
-  p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
   p.status = a.status;
   p.sched = next_sched_slot();
-  p.o_v8 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;
   if (!p.sched) return cudaErrorInvalidDevicePointer;
   p.N = pl->N;
   p.hq = a.hq;
@@ -672,7 +721,7 @@ cudaError_t launch_fwd_bf16(const AttnArgs& a) {
     attr_set = true;
   }
   const int grid = p.n_items < sm_count() ? p.n_items : sm_count();
-  tree_attn_fwd_sm103<<<grid, kThreads, kSmemBytes, a.stream>>>(mq, mk, mv, p);
+  tree_attn_fwd_sm103<<<grid, kThreads, kSmemBytes, a.stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
 }
 
