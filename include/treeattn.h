@@ -71,6 +71,8 @@ typedef struct {
   int64_t num_ancestors;  /* sum over segments of the number of ancestors */
   int64_t visible_pairs;  /* sum over rows of the visible keys, diagonal included */
   int64_t num_gathered_tiles; /* entries of TREE_FIELD_GT_KIND (both unit sizes) */
+  int64_t past_len;       /* gateway keys of a partition plan (0 otherwise) */
+  int64_t past_visible;   /* of which visible to the partition's rows */
 } tree_plan_info_t;
 
 /* Plan fields readable with tree_plan_get. All are int32 arrays. */
@@ -110,15 +112,21 @@ typedef enum {
   TREE_FIELD_GP_PTR = 25,     /* [num_pairs+1] tiles of each q-tile pair (units of 256 rows), after
                                  the q-tiles' tiles in the same tile table */
   TREE_FIELD_GT_KIND = 26,    /* [num_gathered_tiles] kind of the first 128 rows | kind of the next
-                                 128 rows << 2 (0 EMPTY, 1 PARTIAL, 2 FULL: all 128x128 pairs visible) */
+                                 128 rows << 2 (0 EMPTY, 1 PARTIAL, 2 FULL: all 128x128 pairs visible)
+                                 | 16 when the tile holds gateway keys (partition plans, below) */
   TREE_FIELD_GT_ATOM = 27,    /* [num_gathered_tiles*16] first key row of each atom; -8 for an atom
                                  with no key (loaded as zeros) */
   TREE_FIELD_GT_BIDX = 28,    /* [num_gathered_tiles] row of the tile in GT_BOUNDS, -1 when no slot of
                                  the tile is PARTIAL */
   TREE_FIELD_GT_BOUNDS = 29,  /* [num_bounds*128] key_end of each column's key, 0 for padding.
                                  Column c holds key GT_ATOM[c/8] + c%8, and row i sees it iff
-                                 key <= i < key_end[c] */
-  TREE_FIELD_COUNT = 30
+                                 key <= i < key_end[c]; gateway keys (kind bit 16) precede
+                                 every row, so only i < key_end[c] applies to them */
+  /* Partition plans only (tree_plan_build_partition), empty otherwise: */
+  TREE_FIELD_GW_KEND = 30,    /* [128*ceil(past_len/128)] N for a visible gateway key, 0 for a
+                                 hidden one and past past_len */
+  TREE_FIELD_GW_KT = 31,      /* [gateway key tiles with a visible key] their indices (128 keys each) */
+  TREE_FIELD_COUNT = 32
 } tree_plan_field_t;
 
 /*
@@ -136,6 +144,24 @@ typedef enum {
  */
 tree_status_t tree_plan_build(const int32_t* segment_parents, const int32_t* segment_lengths,
                               int32_t num_segments, tree_plan_t** out);
+
+/*
+ * Plan for one partition of a partitioned trie (§3.3 "Partitioning"; App. B):
+ * the partition's own segments as in tree_plan_build, plus a gateway of
+ * past_len cached keys (App. B.2: the parent partition's own gateway
+ * followed by its DFS tokens up to the end of the cut node). Every row of the
+ * partition sees gateway key j iff past_visible[j] != 0 (App. B.3 eq. 16: the
+ * parent's gateway and the cut node's ancestors within the parent are
+ * visible, the parent's other subtrees are not); the partition's own keys
+ * keep the tree mask (eq. 14). past_visible is a host array of past_len bytes
+ * (copied); past_len == 0 gives the plan of tree_plan_build.
+ * Errors as tree_plan_build, and past_len < 0, or a NULL past_visible with
+ * past_len > 0 -> TREE_ERR_INVALID_ARG.
+ */
+tree_status_t tree_plan_build_partition(const int32_t* segment_parents,
+                                        const int32_t* segment_lengths, int32_t num_segments,
+                                        const uint8_t* past_visible, int32_t past_len,
+                                        tree_plan_t** out);
 
 /* Sizes of a plan (host). */
 tree_status_t tree_plan_info(const tree_plan_t* plan, tree_plan_info_t* out);
@@ -211,6 +237,37 @@ tree_status_t tree_attn_bwd_dkdv(const tree_plan_t* plan, const void* dout, cons
                                  int32_t hq, int32_t hkv, int32_t head_dim, tree_dtype_t dtype,
                                  tree_dtype_t grad_dtype, float softmax_scale, void* workspace,
                                  size_t workspace_bytes, tree_stream_t stream);
+
+/*
+ * Attention of a partition with its gateway (App. B.2 eq. 14): rows attend
+ * to the visible gateway keys past_k / past_v [past_len, hkv, D] (device,
+ * same dtype and layout as k and v) and to their own keys under the tree
+ * mask, in one softmax. The plan must come from tree_plan_build_partition;
+ * other arguments and outputs as tree_attn_fwd. bf16 only (D = 128);
+ * fp32 -> TREE_ERR_UNSUPPORTED. A plan with a gateway is refused by
+ * tree_attn_fwd / tree_attn_bwd (TREE_ERR_INVALID_ARG).
+ */
+tree_status_t tree_attn_fwd_gateway(const tree_plan_t* plan, const void* q, const void* k,
+                                    const void* v, const void* past_k, const void* past_v, void* o,
+                                    float* lse, int32_t hq, int32_t hkv, int32_t head_dim,
+                                    tree_dtype_t dtype, float softmax_scale, tree_stream_t stream);
+
+/*
+ * Backward of tree_attn_fwd_gateway: dq, dk, dv as tree_attn_bwd (written),
+ * and the gateway keys' gradients ADDED in fp32 to past_dk_acc /
+ * past_dv_acc [past_len, hkv, D] (device fp32, caller-initialised): several
+ * child partitions that share a cut node accumulate into the same gateway
+ * gradients without bf16 rounding in between (App. B.5 eq. 18). Hidden
+ * gateway keys get + 0. Workspace as tree_attn_bwd (same size). Errors as
+ * tree_attn_bwd and tree_attn_fwd_gateway.
+ */
+tree_status_t tree_attn_bwd_gateway(const tree_plan_t* plan, const void* dout, const void* q,
+                                    const void* k, const void* v, const void* past_k,
+                                    const void* past_v, const void* o, const float* lse, void* dq,
+                                    void* dk, void* dv, float* past_dk_acc, float* past_dv_acc,
+                                    int32_t hq, int32_t hkv, int32_t head_dim, tree_dtype_t dtype,
+                                    tree_dtype_t grad_dtype, float softmax_scale, void* workspace,
+                                    size_t workspace_bytes, tree_stream_t stream);
 
 /*
  * Backward for callers that cannot allocate device memory when they call it

@@ -86,7 +86,33 @@ def _unit_key_sets(view, r0, r1):
     return np.unique(np.concatenate(some)), np.asarray(every, np.int64)
 
 
-def gathered_tiles(parents, lengths, unit_rows: int, bn: int = 128, atom: int = 8):
+def _place_runs(seq, bn, atom):
+    """Lay a key sequence into tiles of bn columns: runs of consecutive keys,
+    each run from a column that is a multiple of ``atom``."""
+    runs = []
+    for j in seq:
+        if runs and runs[-1][1] == j:
+            runs[-1][1] = j + 1
+        else:
+            runs.append([j, j + 1])
+    tiles = []
+    col = bn
+    for a, b in runs:
+        while a < b:
+            if col >= bn:
+                tiles.append([None] * bn)
+                col = 0
+            m = min(b - a, bn - col)
+            for c in range(m):
+                tiles[-1][col + c] = a + c
+            col += m
+            a += m
+        col = -(-col // atom) * atom
+    return tiles
+
+
+def gathered_tiles(parents, lengths, unit_rows: int, bn: int = 128, atom: int = 8,
+                   past_visible=None):
     """Gathered key tiles of every unit of ``unit_rows`` query rows.
 
     For the unit's rows, the keys every row sees come first and the keys only
@@ -97,39 +123,39 @@ def gathered_tiles(parents, lengths, unit_rows: int, bn: int = 128, atom: int = 
     key of each atom (-8 if the atom holds none) and the key of each column
     (None for padding), and for tiles with a PARTIAL block the key_end of each
     column (0 for padding). A layout convention of this library for loading and
-    skipping keys; the pages say nothing about it."""
+    skipping keys; the pages say nothing about it.
+
+    With ``past_visible`` (a partition's gateway, App. B.2-B.3), each unit's
+    tiles start with the visible gateway keys, which every row sees, laid out
+    the same way in tiles of their own (flag "gateway": atoms are rows of the
+    gateway keys, bounds N, and no key-before-row condition applies)."""
     view = TrieView(parents, lengths)
     N = view.N
     kend = key_end(parents, lengths)
+    gw_vis = [] if past_visible is None else [j for j, x in enumerate(past_visible) if x]
     out = []
     for r0 in range(0, N, unit_rows):
         r1 = min(N, r0 + unit_rows)
+        unit = []
+        for cols in _place_runs(gw_vis, bn, atom):
+            kinds = []
+            full_cols = all(c is not None for c in cols)
+            for sa in range(r0, r0 + unit_rows, 128):
+                sb = min(r1, sa + 128)
+                if sa >= sb:
+                    kinds.append(EMPTY)
+                else:
+                    kinds.append(FULL if full_cols and sb - sa == 128 else PARTIAL)
+            atoms = [cols[g * atom] if cols[g * atom] is not None else -8 for g in range(bn // atom)]
+            bnd = [N if c is not None else 0 for c in cols] if PARTIAL in kinds else None
+            unit.append({"kinds": kinds, "atoms": atoms, "cols": cols, "bounds": bnd, "gateway": True})
         some, every = _unit_key_sets(view, r0, r1)
         seq = list(every) + sorted(set(some.tolist()) - set(every.tolist()))
-        runs = []
-        for j in seq:
-            if runs and runs[-1][1] == j:
-                runs[-1][1] = j + 1
-            else:
-                runs.append([j, j + 1])
-        tiles = []
-        col = bn
-        for a, b in runs:
-            while a < b:
-                if col >= bn:
-                    tiles.append([None] * bn)
-                    col = 0
-                m = min(b - a, bn - col)
-                for c in range(m):
-                    tiles[-1][col + c] = a + c
-                col += m
-                a += m
-            col = -(-col // atom) * atom
+        tiles = _place_runs(seq, bn, atom)
         slots = []
         for sa in range(r0, r0 + unit_rows, 128):
             sb = min(r1, sa + 128)
             slots.append(_unit_key_sets(view, sa, sb) + (sb - sa,) if sa < sb else None)
-        unit = []
         for cols in tiles:
             kinds = []
             keys = [c for c in cols if c is not None]
@@ -148,19 +174,20 @@ def gathered_tiles(parents, lengths, unit_rows: int, bn: int = 128, atom: int = 
             bnd = None
             if PARTIAL in kinds:
                 bnd = [int(kend[c]) if c is not None else 0 for c in cols]
-            unit.append({"kinds": kinds, "atoms": atoms, "cols": cols, "bounds": bnd})
+            unit.append({"kinds": kinds, "atoms": atoms, "cols": cols, "bounds": bnd, "gateway": False})
         out.append(unit)
     return out
 
 
-def _gathered_fields(parents, lengths):
+def _gathered_fields(parents, lengths, past_visible=None):
     kind, atoms, bidx, bounds = [], [], [], []
     ptrs = []
     for rows in (128, 256):
         ptr = [len(kind)]
-        for unit in gathered_tiles(parents, lengths, rows):
+        for unit in gathered_tiles(parents, lengths, rows, past_visible=past_visible):
             for t in unit:
-                kind.append(sum(k << (2 * n) for n, k in enumerate(t["kinds"])))
+                kind.append(sum(k << (2 * n) for n, k in enumerate(t["kinds"])) +
+                            (16 if t["gateway"] else 0))
                 atoms.extend(t["atoms"])
                 if t["bounds"] is None:
                     bidx.append(-1)
@@ -172,8 +199,19 @@ def _gathered_fields(parents, lengths):
     return ptrs[0], ptrs[1], kind, atoms, bidx, bounds
 
 
-def plan_fields(parents, lengths, bm: int = 128, bn: int = 128) -> dict:
-    """Every plan field as int32/int64 numpy arrays, named as in the C-ABI."""
+def gateway_fields(N, past_visible, bn: int = 128):
+    """GW_KEND (N for a visible gateway key, 0 for a hidden one, padded to whole
+    tiles) and GW_KT (gateway key tiles holding a visible key)."""
+    vis = [bool(x) for x in past_visible]
+    tiles = -(-len(vis) // bn)
+    kend = [N if x else 0 for x in vis] + [0] * (tiles * bn - len(vis))
+    kt = [t for t in range(tiles) if any(vis[t * bn:(t + 1) * bn])]
+    return kend, kt
+
+
+def plan_fields(parents, lengths, bm: int = 128, bn: int = 128, past_visible=None) -> dict:
+    """Every plan field as int32/int64 numpy arrays, named as in the C-ABI
+    (with ``past_visible``, those of a partition plan with that gateway)."""
     parents_l, lengths_l = T.validate(parents, lengths)
     S = len(parents_l)
     N = sum(lengths_l)
@@ -236,7 +274,10 @@ def plan_fields(parents, lengths, bm: int = 128, bn: int = 128) -> dict:
     qp_order = list(reversed(range(n_pairs)))
 
     pos_id = T.position_ids(parents_l, lengths_l)
-    gq_ptr, gp_ptr, gt_kind, gt_atom, gt_bidx, gt_bounds = _gathered_fields(parents_l, lengths_l)
+    gq_ptr, gp_ptr, gt_kind, gt_atom, gt_bidx, gt_bounds = _gathered_fields(parents_l, lengths_l,
+                                                                          past_visible)
+    gw_kend, gw_kt = ([], []) if past_visible is None or len(past_visible) == 0 else \
+        gateway_fields(N, past_visible, bn)
     i32 = lambda x: np.asarray(x, dtype=np.int32)  # noqa: E731
     return {
         "num_tokens": N,
@@ -273,4 +314,6 @@ def plan_fields(parents, lengths, bm: int = 128, bn: int = 128) -> dict:
         "gt_atom": i32(gt_atom),
         "gt_bidx": i32(gt_bidx),
         "gt_bounds": i32(gt_bounds),
+        "gw_kend": i32(gw_kend),
+        "gw_kt": i32(gw_kt),
     }

@@ -77,3 +77,49 @@ def test_gathered_tiles_of_single_tokens_and_tile_edges():
         parents = [-1] + list(range(len(lengths) - 1))
         _check_plan(parents, lengths)
     _check_plan([-1, 0, 0, 1, 1, 2, 2], [140, 60, 70, 129, 1, 127, 128])
+
+
+def test_gathered_tiles_with_a_gateway_cover_the_combined_mask():
+    """Partition plans: gateway tiles first, then the own tiles, cover the
+    App. B.2 eq. 14 mask over [gateway keys, own keys] exactly once."""
+    from oracle import gateway as GW
+
+    rng = np.random.default_rng(31)
+    for n in range(10):
+        S = int(rng.integers(1, 12))
+        parents = [-1] + [int(rng.integers(0, s)) for s in range(1, S)]
+        lengths = [int(x) for x in rng.integers(1, 150, S)]
+        vis = (rng.random(int(rng.integers(0, 400))) < [0.2, 0.6, 1.0][n % 3]).tolist()
+        plan = tpa.tree_plan_build_partition(parents, lengths, vis)
+        f = plan.fields()
+        N, P = plan.num_tokens, len(vis)
+        combined = GW.combined_mask(parents, lengths, vis)
+        bounds = f["gt_bounds"].reshape(-1, 128)
+        for ptr, rows in ((f["gq_ptr"], 128), (f["gp_ptr"], 256)):
+            for u in range(len(ptr) - 1):
+                r0, r1 = u * rows, min(N, u * rows + rows)
+                covered = np.zeros((r1 - r0, P + N), dtype=np.int64)
+                for t in range(ptr[u], ptr[u + 1]):
+                    atoms = f["gt_atom"][16 * t:16 * t + 16]
+                    word = f["gt_kind"][t]
+                    gwt = (word >> 4) & 1
+                    loaded = np.array([atoms[c // 8] + c % 8 for c in range(128)])
+                    b = f["gt_bidx"][t]
+                    for sl in range(rows // 128):
+                        kd = (word >> (2 * sl)) & 3
+                        sa, sb = r0 + 128 * sl, min(r1, r0 + 128 * sl + 128)
+                        if sa >= sb or kd == 0:
+                            continue
+                        rr = np.arange(sa, sb)[:, None]
+                        if kd == 2:
+                            vis_m = np.ones((sb - sa, 128), dtype=bool)
+                            cols = loaded
+                        else:
+                            kend = bounds[b]
+                            cols = np.where(kend > 0, loaded, 0)
+                            vis_m = (rr < kend[None, :]) & (gwt | (loaded[None, :] <= rr))
+                        cols = cols if gwt else cols + P
+                        for c in range(128):
+                            np.add.at(covered, (np.flatnonzero(vis_m[:, c]) + sa - r0, cols[c]), 1)
+                assert covered.max(initial=0) <= 1
+                assert np.array_equal(covered.astype(bool), combined[r0:r1])

@@ -24,7 +24,8 @@ from ._lib import (ACT_NONE, ACT_SILU, DTYPE_BF16, DTYPE_F32, EXPORTS, FIELDS, L
                    PartitionRec, PlanInfo, TreeAttnError, check, lib)
 
 __all__ = [
-    "Plan", "tree_plan_build", "tree_attn_fwd", "tree_attn_bwd", "tree_attn_bwd_dq",
+    "Plan", "tree_plan_build", "tree_plan_build_partition", "tree_attn_fwd_gateway",
+    "tree_attn_bwd_gateway", "tree_attn_fwd", "tree_attn_bwd", "tree_attn_bwd_dq",
     "tree_attn_bwd_dkdv", "tree_attn_bwd_workspace_bytes",
     "tree_weights", "tree_weights_paths", "tree_partition", "tree_rope", "tree_rope_apply",
     "TreeRopeFn", "tree_conv_fwd", "tree_conv_bwd", "tree_conv", "TreeConvFn",
@@ -36,14 +37,23 @@ __all__ = [
 class Plan:
     """Owns a ``tree_plan_t``: the host plan and, once uploaded, its device copy."""
 
-    def __init__(self, segment_parents, segment_lengths):
+    def __init__(self, segment_parents, segment_lengths, past_visible=None):
         parents = np.ascontiguousarray(np.asarray(segment_parents, dtype=np.int32))
         lengths = np.ascontiguousarray(np.asarray(segment_lengths, dtype=np.int32))
         if parents.shape != lengths.shape or parents.ndim != 1:
             raise ValueError("segment_parents and segment_lengths must be 1-D and of equal length")
         h = C.c_void_p()
-        check(lib.tree_plan_build(parents.ctypes.data, lengths.ctypes.data, int(parents.size),
-                                  C.byref(h)))
+        if past_visible is None:
+            check(lib.tree_plan_build(parents.ctypes.data, lengths.ctypes.data, int(parents.size),
+                                      C.byref(h)))
+        else:
+            vis = np.ascontiguousarray(np.asarray(past_visible, dtype=bool).astype(np.uint8))
+            if vis.ndim != 1:
+                raise ValueError("past_visible must be 1-D")
+            check(lib.tree_plan_build_partition(parents.ctypes.data, lengths.ctypes.data,
+                                                int(parents.size),
+                                                vis.ctypes.data if vis.size else None,
+                                                int(vis.size), C.byref(h)))
         self._h = h
         info = PlanInfo()
         check(lib.tree_plan_info(self._h, C.byref(info)))
@@ -78,6 +88,13 @@ class Plan:
 
 def tree_plan_build(segment_parents, segment_lengths) -> Plan:
     return Plan(segment_parents, segment_lengths)
+
+
+def tree_plan_build_partition(segment_parents, segment_lengths, past_visible) -> Plan:
+    """Plan of one partition (§3.3; App. B): its own segments plus a gateway of
+    len(past_visible) cached keys, key j visible to every row iff past_visible[j]
+    (App. B.3 eq. 16)."""
+    return Plan(segment_parents, segment_lengths, past_visible)
 
 
 def _stream_ptr(stream):
@@ -218,6 +235,66 @@ def tree_attn_bwd_dkdv(plan: Plan, do, q, k, v, lse, workspace, softmax_scale: f
                                  hkv, D, _dtype_code(q), gcode, float(softmax_scale),
                                  workspace.data_ptr(), workspace.numel(), s))
     return dk, dv
+
+
+def tree_attn_fwd_gateway(plan: Plan, q, k, v, past_k, past_v, softmax_scale: float = 0.0,
+                          out=None, lse=None, stream=None):
+    """(o, lse) of a partition with its gateway (App. B.2 eq. 14): past_k, past_v
+    [past_len, hkv, D] hold the gateway keys and values. bf16 only."""
+    import torch
+
+    N, hq, D = q.shape
+    hkv = k.shape[1]
+    P = plan.info["past_len"]
+    if N != plan.num_tokens:
+        raise ValueError(f"q has {N} tokens, the plan {plan.num_tokens}")
+    _check_tensor("q", q, (N, hq, D))
+    _check_tensor("k", k, (N, hkv, D), q.dtype)
+    _check_tensor("v", v, (N, hkv, D), q.dtype)
+    _check_tensor("past_k", past_k, (P, hkv, D), q.dtype)
+    _check_tensor("past_v", past_v, (P, hkv, D), q.dtype)
+    o = torch.empty_like(q) if out is None else out
+    lse_t = torch.empty(hq, N, dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_tensor("o", o, (N, hq, D), q.dtype)
+    _check_tensor("lse", lse_t, (hq, N), torch.float32)
+    s = _stream_ptr(stream)
+    plan.to_device(s)
+    check(lib.tree_attn_fwd_gateway(plan.handle, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                    past_k.data_ptr(), past_v.data_ptr(), o.data_ptr(),
+                                    lse_t.data_ptr(), hq, hkv, D, _dtype_code(q),
+                                    float(softmax_scale), s))
+    return o, lse_t
+
+
+def tree_attn_bwd_gateway(plan: Plan, do, q, k, v, past_k, past_v, o, lse, past_dk_acc=None,
+                          past_dv_acc=None, softmax_scale: float = 0.0, grad_dtype=None,
+                          workspace=None, stream=None):
+    """(dq, dk, dv, past_dk_acc, past_dv_acc) of tree_attn_fwd_gateway. The gateway
+    gradients are added in fp32 to past_dk_acc / past_dv_acc (created as zeros when
+    None), as several children sharing a cut node accumulate them (App. B.5)."""
+    import torch
+
+    N, hq, hkv, D, gdt, gcode, workspace, s = _bwd_prepare(plan, do, q, k, v, o, lse, grad_dtype,
+                                                           workspace, stream)
+    P = plan.info["past_len"]
+    _check_tensor("past_k", past_k, (P, hkv, D), q.dtype)
+    _check_tensor("past_v", past_v, (P, hkv, D), q.dtype)
+    if past_dk_acc is None:
+        past_dk_acc = torch.zeros(P, hkv, D, dtype=torch.float32, device=q.device)
+    if past_dv_acc is None:
+        past_dv_acc = torch.zeros(P, hkv, D, dtype=torch.float32, device=q.device)
+    _check_tensor("past_dk_acc", past_dk_acc, (P, hkv, D), torch.float32)
+    _check_tensor("past_dv_acc", past_dv_acc, (P, hkv, D), torch.float32)
+    dq = torch.empty(N, hq, D, dtype=gdt, device=q.device)
+    dk = torch.empty(N, hkv, D, dtype=gdt, device=q.device)
+    dv = torch.empty(N, hkv, D, dtype=gdt, device=q.device)
+    check(lib.tree_attn_bwd_gateway(plan.handle, do.data_ptr(), q.data_ptr(), k.data_ptr(),
+                                    v.data_ptr(), past_k.data_ptr(), past_v.data_ptr(), o.data_ptr(),
+                                    lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                    past_dk_acc.data_ptr(), past_dv_acc.data_ptr(), hq, hkv, D,
+                                    _dtype_code(q), gcode, float(softmax_scale),
+                                    workspace.data_ptr(), workspace.numel(), s))
+    return dq, dk, dv, past_dk_acc, past_dv_acc
 
 
 def tree_weights(plan: Plan) -> np.ndarray:

@@ -31,7 +31,7 @@ FIELDS = [
     "dfs_order", "seg_start", "depth", "subtree_end", "trie_id", "g", "anc_ptr", "anc_idx",
     "token_seg", "pos_id", "key_end", "cu_seqlens", "trie_paths", "qt_ptr", "qt_kt", "qt_kind",
     "kt_qlo", "kt_qhi", "fwd_order", "bwd_order", "qp_ptr", "qp_kt", "qp_kind", "qp_order",
-    "gq_ptr", "gp_ptr", "gt_kind", "gt_atom", "gt_bidx", "gt_bounds",
+    "gq_ptr", "gp_ptr", "gt_kind", "gt_atom", "gt_bidx", "gt_bounds", "gw_kend", "gw_kt",
 ]
 
 # Every symbol the public header declares.
@@ -41,7 +41,7 @@ EXPORTS = [
     "tree_attn_bwd", "tree_attn_bwd_dq", "tree_attn_bwd_dkdv", "tree_attn_bwd_static_scratch",
     "tree_weights", "tree_weights_paths", "tree_partition", "tree_conv_prepare", "tree_conv_fwd",
     "tree_conv_bwd_workspace_bytes", "tree_conv_bwd", "tree_rope", "tree_status_sync",
-    "tree_last_error",
+    "tree_last_error", "tree_plan_build_partition", "tree_attn_fwd_gateway", "tree_attn_bwd_gateway",
 ]
 
 
@@ -49,7 +49,7 @@ class PlanInfo(C.Structure):
     _fields_ = [(name, C.c_int64) for name in (
         "num_tokens", "num_segments", "num_tries", "block_m", "block_n", "num_q_tiles",
         "num_k_tiles", "nnz_tiles", "num_pairs", "nnz_pair_tiles", "num_ancestors",
-        "visible_pairs", "num_gathered_tiles")]
+        "visible_pairs", "num_gathered_tiles", "past_len", "past_visible")]
 
 
 class TreeAttnError(RuntimeError):
@@ -98,6 +98,11 @@ def _load():
         "tree_conv_bwd": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, sz, vp]),
         "tree_status_sync": (i32, [vp]),
         "tree_last_error": (C.c_char_p, []),
+        "tree_plan_build_partition": (i32, [vp, vp, i32, vp, i32, C.POINTER(vp)]),
+        "tree_attn_fwd_gateway": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, C.c_float,
+                                        vp]),
+        "tree_attn_bwd_gateway": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                        i32, i32, i32, i32, C.c_float, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -166,6 +166,7 @@ struct DqParams {
   SchedSlot* sched;
   int N, Npad, hq, group, n_items, out_f32;
   int out_v8;  // dq is 32-byte aligned
+  int has_gateway;
   float scale, scale_log2;
 };
 
@@ -177,7 +178,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                            const __grid_constant__ CUtensorMap map_do,
                            const __grid_constant__ CUtensorMap map_o,
                            const __grid_constant__ GatherMaps gmap_k,
-                           const __grid_constant__ GatherMaps gmap_v, const DqParams p) {
+                           const __grid_constant__ GatherMaps gmap_v,
+                           const __grid_constant__ GatherMaps gmap_pk,
+                           const __grid_constant__ GatherMaps gmap_pv, const DqParams p) {
   // All shared state sits in the dynamic block (no static shared memory), so
   // the block starts 1024-aligned as the 128B-swizzled tiles need.
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -256,6 +259,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     for (int b = 0; b < 5; ++b) {
       tma_prefetch_desc(&gmap_k.box[b]);
       tma_prefetch_desc(&gmap_v.box[b]);
+      if (p.has_gateway) {
+        tma_prefetch_desc(&gmap_pk.box[b]);
+        tma_prefetch_desc(&gmap_pv.box[b]);
+      }
     }
   }
   if (warp == 1) {
@@ -317,16 +324,19 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       __syncwarp();
       ++kk;
       // this lane's atom and the bounds row of the next tile, one tile ahead
-      int arow_next = 0, bidx_next = -1;
+      int arow_next = 0, bidx_next = -1, kind_next = 0;
       if (beg < end) {
         arow_next = ldg_pinned(p.gt_atom + 16 * beg + (lane & 15));
         bidx_next = ldg_pinned(p.gt_bidx + beg);
+        kind_next = ldg_pinned(p.gt_kind + beg);
       }
       for (int t = beg; t < end; ++t, ++kv, ++kk) {
         const int arow = arow_next, bidx = bidx_next;
+        const bool gw = (kind_next >> 4) & 1;  // gateway keys: the past K/V tensors
         if (t + 1 < end) {
           arow_next = ldg_pinned(p.gt_atom + 16 * (t + 1) + (lane & 15));
           bidx_next = ldg_pinned(p.gt_bidx + t + 1);
+          kind_next = ldg_pinned(p.gt_kind + t + 1);
         }
         const uint32_t sk = kk % kDqKStages;
         if (!(ok = k_slot_free(kk))) break;
@@ -339,13 +349,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                       &bar_k_full[sk]);
         }
         __syncwarp();
-        load_gathered(kdst, gmap_k, &bar_k_full[sk], kvh, arow, lane);
+        load_gathered(kdst, gw ? gmap_pk : gmap_k, &bar_k_full[sk], kvh, arow, lane);
         __syncwarp();
         const uint32_t sv = kv % kDqVStages, pv = (kv / kDqVStages) & 1;
         if (kv >= kDqVStages && !(ok = warp_wait(&bar_v_empty[sv], pv ^ 1, abort, p.status))) break;
         if (lane == 0) mbar_arrive_expect_tx(&bar_v_full[sv], kTileBytes);
         __syncwarp();
-        load_gathered(smem + kDqOffV + sv * kTileBytes, gmap_v, &bar_v_full[sv], kvh, arow, lane);
+        load_gathered(smem + kDqOffV + sv * kTileBytes, gw ? gmap_pv : gmap_v, &bar_v_full[sv], kvh, arow,
+                      lane);
         __syncwarp();
       }
       if (!ok) break;
@@ -482,7 +493,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     int hdr[3] = {0, 0, 0};  // the next item's q-tile and tile range, from the ring
     int nt_kind = 0, nt_arow = 0, nt_at = -1;  // nt_arow: first key of atom lane % 16
     auto fetch_tile = [&](int t) {
-      nt_kind = ldg_pinned(p.gt_kind + t) & 3;
+      nt_kind = ldg_pinned(p.gt_kind + t) & 19;  // kind, and 16 for gateway keys
       nt_arow = ldg_pinned(p.gt_atom + 16 * t + (lane & 15));
       nt_at = t;
     };
@@ -572,7 +583,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       ++qn;
       if (nt_at != beg) fetch_tile(beg);
       for (int t = beg; t < end; ++t, ++n, ++kk) {
-        const int kd = nt_kind, tile_arow = nt_arow;
+        const int kd = nt_kind & 3, tile_arow = nt_arow;
+        const bool tile_gw = (nt_kind >> 4) & 1;  // gateway keys precede every row
         if (t + 1 < end) fetch_tile(t + 1);
         // What this warp's 32 rows x 64 keys of the tile hold: 1 every pair
         // visible (no mask), 0 a mix (mask per element; the key <= i half only
@@ -603,9 +615,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
           for (int a = 0; a < 8; ++a) arow[a] = __shfl_sync(0xffffffffu, tile_arow, half * 8 + a);
           const int r0 = qt * 128 + quarter * 32;
-          // rows [r0, r0+32) see key j iff j <= row < key_end[j]
-          diag = amax + 7 > r0;
-          mode = (mx <= r0 || amin > r0 + 31) ? 2 : (!diag && mn > r0 + 31) ? 1 : 0;
+          // rows [r0, r0+32) see key j iff j <= row < key_end[j]; gateway
+          // keys come before every row, so only the key_end bound applies
+          diag = !tile_gw && amax + 7 > r0;
+          mode = (mx <= r0 || (!tile_gw && amin > r0 + 31)) ? 2 : (!diag && mn > r0 + 31) ? 1 : 0;
         }
         const int sb = (t - beg) & 1;
         const uint32_t tSb = tS + lane_off + sb * 128 + col0;
@@ -762,6 +775,11 @@ struct KvParams {
   const int32_t* kt_qlo;
   const int32_t* kt_qhi;
   const int32_t* order;
+  const int32_t* gw_kend;  // gateway keys: N if visible, else 0 (partition plans)
+  const int32_t* gw_kt;    // gateway key tiles with a visible key
+  float* past_dk;          // gateway gradients, accumulated in fp32
+  float* past_dv;
+  int n_gw, past_len, Tq;
   const float* lse2;   // [hq, Npad]
   const float* delta;  // [hq, Npad]
   void* dk;
@@ -774,24 +792,52 @@ struct KvParams {
 };
 
 struct KvItem {
-  int kt, kvh, qlo, nq, steps;
+  int kt, kvh, qlo, nq, steps, gw;  // gw: a tile of gateway keys (seen by every row)
 };
 
+// Items: the gateway key tiles first (they walk every q-tile), then the
+// partition's own key tiles in the plan's order.
 __device__ __forceinline__ KvItem decode_kv(const KvParams& p, int it) {
   KvItem x;
-  x.kt = p.order[it / p.hkv];
+  const int u = it / p.hkv;
   x.kvh = it % p.hkv;
-  x.qlo = p.kt_qlo[x.kt];
-  x.nq = p.kt_qhi[x.kt] - x.qlo;
+  if (u < p.n_gw) {
+    x.gw = 1;
+    x.kt = p.gw_kt[u];
+    x.qlo = 0;
+    x.nq = p.Tq;
+  } else {
+    x.gw = 0;
+    x.kt = p.order[u - p.n_gw];
+    x.qlo = p.kt_qlo[x.kt];
+    x.nq = p.kt_qhi[x.kt] - x.qlo;
+  }
   x.steps = x.nq * p.group;
   return x;
+}
+
+// Add 32 consecutive fp32 values of one 128-wide row, times `mul`, into dst.
+__device__ __forceinline__ void accumulate_row(float* dst_base, size_t off, int c,
+                                               const uint32_t (&v)[32], float mul) {
+  float4* dst = reinterpret_cast<float4*>(dst_base + off + c * 32);
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    float4 a = dst[u];
+    a.x += __uint_as_float(v[4 * u + 0]) * mul;
+    a.y += __uint_as_float(v[4 * u + 1]) * mul;
+    a.z += __uint_as_float(v[4 * u + 2]) * mul;
+    a.w += __uint_as_float(v[4 * u + 3]) * mul;
+    dst[u] = a;
+  }
 }
 
 __global__ void __launch_bounds__(kKvThreads, 1)
     tree_attn_bwd_dkdv_sm103(const __grid_constant__ CUtensorMap map_q,
                              const __grid_constant__ CUtensorMap map_k,
                              const __grid_constant__ CUtensorMap map_v,
-                             const __grid_constant__ CUtensorMap map_do, const KvParams p) {
+                             const __grid_constant__ CUtensorMap map_do,
+                             const __grid_constant__ CUtensorMap map_pk,
+                             const __grid_constant__ CUtensorMap map_pv, const KvParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (smem_u32(smem) & 1023u) {  // the layout needs a 1024-aligned base
@@ -843,6 +889,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     tma_prefetch_desc(&map_k);
     tma_prefetch_desc(&map_v);
     tma_prefetch_desc(&map_do);
+    if (p.n_gw > 0) {
+      tma_prefetch_desc(&map_pk);
+      tma_prefetch_desc(&map_pv);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -869,10 +919,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       if (lane == 0) {
         mbar_arrive_expect_tx(bar_kv_full, 2 * kTileBytes);
         const int row0 = x.kt * 128;
-        tma_load_3d(smem + kKvOffK, &map_k, bar_kv_full, 0, x.kvh, row0);
-        tma_load_3d(smem + kKvOffK + kHalfBytes, &map_k, bar_kv_full, 64, x.kvh, row0);
-        tma_load_3d(smem + kKvOffV, &map_v, bar_kv_full, 0, x.kvh, row0);
-        tma_load_3d(smem + kKvOffV + kHalfBytes, &map_v, bar_kv_full, 64, x.kvh, row0);
+        const CUtensorMap* mk = x.gw ? &map_pk : &map_k;
+        const CUtensorMap* mv = x.gw ? &map_pv : &map_v;
+        tma_load_3d(smem + kKvOffK, mk, bar_kv_full, 0, x.kvh, row0);
+        tma_load_3d(smem + kKvOffK + kHalfBytes, mk, bar_kv_full, 64, x.kvh, row0);
+        tma_load_3d(smem + kKvOffV, mv, bar_kv_full, 0, x.kvh, row0);
+        tma_load_3d(smem + kKvOffV + kHalfBytes, mv, bar_kv_full, 64, x.kvh, row0);
       }
       __syncwarp();
       for (int j = 0; j < x.steps; ++j, ++n) {
@@ -910,10 +962,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       if (!(ok = item_put(ring, pub, cur, abort, p.status))) break;
       if (cur >= 0 && lane == 0) {  // its K and V into L2 while this item finishes
         const KvItem y = decode_kv(p, cur);
-        tma_prefetch_l2_3d(&map_k, 0, y.kvh, y.kt * 128);
-        tma_prefetch_l2_3d(&map_k, 64, y.kvh, y.kt * 128);
-        tma_prefetch_l2_3d(&map_v, 0, y.kvh, y.kt * 128);
-        tma_prefetch_l2_3d(&map_v, 64, y.kvh, y.kt * 128);
+        const CUtensorMap* mk = y.gw ? &map_pk : &map_k;
+        const CUtensorMap* mv = y.gw ? &map_pv : &map_v;
+        tma_prefetch_l2_3d(mk, 0, y.kvh, y.kt * 128);
+        tma_prefetch_l2_3d(mk, 64, y.kvh, y.kt * 128);
+        tma_prefetch_l2_3d(mv, 0, y.kvh, y.kt * 128);
+        tma_prefetch_l2_3d(mv, 64, y.kvh, y.kt * 128);
       }
       __syncwarp();
     }
@@ -1008,8 +1062,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     bool ok = true;
     for (int cur; (ok = item_get(ring, got, cur, abort, p.status)) && cur >= 0; ++items) {
       const KvItem x = decode_kv(p, cur);
-      const int jk = x.kt * 128 + kr;
-      const int ke = jk < p.N ? __ldg(p.key_end + jk) : 0;  // rows [jk, ke) see this key
+      // rows [jk, ke) see this key; a gateway key comes before every row and is
+      // seen by all of them if visible (ke = N), by none otherwise (ke = 0)
+      const int krow = x.kt * 128 + kr;
+      const int jk = x.gw ? -1 : krow;
+      const int ke = x.gw ? __ldg(p.gw_kend + krow) : (krow < p.N ? __ldg(p.key_end + krow) : 0);
       for (int j = 0; j < x.steps; ++j, ++n) {
         const int q0 = (x.qlo + j / p.group) * 128 + col0;  // first q column of this half
         const uint32_t sd = n % kKvDoStages, pd = (n / kKvDoStages) & 1;
@@ -1085,18 +1142,29 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       // ---- this item's dV and dK (scaled) from TMEM, this half's 64 columns
       if (!(ok = warp_wait(bar_dkdv_full, items & 1, abort, p.status))) break;
       tc_fence_after_sync();
-      const size_t out = (static_cast<size_t>(jk) * p.hkv + x.kvh) * 128;
+      const size_t out = (static_cast<size_t>(krow) * p.hkv + x.kvh) * 128;
+      const bool keep = x.gw ? krow < p.past_len : krow < p.N;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
         tmem_ld32(tC + lane_off + col0 + c * 32, v);
-        if (jk < p.N) store_row(p.dv, out, half * 2 + c, v, 1.f, p.out_f32, p.out_v8);
+        if (keep) {
+          if (x.gw)
+            accumulate_row(p.past_dv, out, half * 2 + c, v, 1.f);
+          else
+            store_row(p.dv, out, half * 2 + c, v, 1.f, p.out_f32, p.out_v8);
+        }
       }
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
         tmem_ld32(tD + lane_off + col0 + c * 32, v);
-        if (jk < p.N) store_row(p.dk, out, half * 2 + c, v, p.scale, p.out_f32, p.out_v8);
+        if (keep) {
+          if (x.gw)
+            accumulate_row(p.past_dk, out, half * 2 + c, v, p.scale);
+          else
+            store_row(p.dk, out, half * 2 + c, v, p.scale, p.out_f32, p.out_v8);
+        }
       }
       tc_fence_before_sync();
       mbar_arrive(bar_dkdv_free);
@@ -1147,6 +1215,7 @@ cudaError_t launch_bwd_bf16(const AttnBwdArgs& a) {
   d.n_items = pl->Tq * a.hq;
   d.out_f32 = a.grad_f32 ? 1 : 0;
   d.out_v8 = (reinterpret_cast<uintptr_t>(a.dq) & 31u) == 0;
+  d.has_gateway = pl->past_len > 0 ? 1 : 0;
   d.scale = a.scale;
   d.scale_log2 = a.scale * kLog2e;
 
@@ -1155,6 +1224,13 @@ cudaError_t launch_bwd_bf16(const AttnBwdArgs& a) {
   k.kt_qlo = pl->dev.kt_qlo;
   k.kt_qhi = pl->dev.kt_qhi;
   k.order = pl->dev.bwd_order;
+  k.gw_kend = pl->dev.gw_kend;
+  k.gw_kt = pl->dev.gw_kt;
+  k.past_dk = a.past_dk;
+  k.past_dv = a.past_dv;
+  k.n_gw = static_cast<int>(pl->field[TREE_FIELD_GW_KT].size());
+  k.past_len = pl->past_len;
+  k.Tq = pl->Tq;
   k.lse2 = lse2;
   k.delta = delta;
   k.dk = a.dk;
@@ -1167,7 +1243,7 @@ cudaError_t launch_bwd_bf16(const AttnBwdArgs& a) {
   k.hq = a.hq;
   k.hkv = a.hkv;
   k.group = a.hq / a.hkv;
-  k.n_items = pl->Tk * a.hkv;
+  k.n_items = (pl->Tk + k.n_gw) * a.hkv;
   k.out_f32 = a.grad_f32 ? 1 : 0;
   k.out_v8 = ((reinterpret_cast<uintptr_t>(a.dk) | reinterpret_cast<uintptr_t>(a.dv)) & 31u) == 0;
   k.scale = a.scale;
@@ -1185,18 +1261,30 @@ cudaError_t launch_bwd_bf16(const AttnBwdArgs& a) {
   }
   if (a.phases & 1) {
     CUtensorMap mo;
-    GatherMaps gk, gv;
+    GatherMaps gk, gv, gpk, gpv;
     if (!make_tile_map(&mo, a.o, N, a.hq) || !make_gather_maps(&gk, a.k, N, a.hkv) ||
         !make_gather_maps(&gv, a.v, N, a.hkv))
       return cudaErrorInvalidValue;
+    if (pl->past_len > 0) {
+      if (!make_gather_maps(&gpk, a.past_k, pl->past_len, a.hkv) ||
+          !make_gather_maps(&gpv, a.past_v, pl->past_len, a.hkv))
+        return cudaErrorInvalidValue;
+    } else {
+      gpk = gk;
+      gpv = gv;
+    }
     tree_attn_bwd_dq_sm103<<<d.n_items < sms ? d.n_items : sms, kDqThreads, kDqSmem, a.stream>>>(
-        mq, mk, mv, mdo, mo, gk, gv, d);
+        mq, mk, mv, mdo, mo, gk, gv, gpk, gpv, d);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (!(a.phases & 2)) return cudaSuccess;
+  CUtensorMap mpk = mk, mpv = mv;
+  if (pl->past_len > 0 && (!make_tile_map(&mpk, a.past_k, pl->past_len, a.hkv) ||
+                           !make_tile_map(&mpv, a.past_v, pl->past_len, a.hkv)))
+    return cudaErrorInvalidValue;
   tree_attn_bwd_dkdv_sm103<<<k.n_items < sms ? k.n_items : sms, kKvThreads, kKvSmem, a.stream>>>(
-      mq, mk, mv, mdo, k);
+      mq, mk, mv, mdo, mpk, mpv, k);
   return cudaGetLastError();
 }
 

@@ -113,7 +113,8 @@ extern "C" tree_status_t tree_plan_to_device(tree_plan_t* p, tree_stream_t strea
       {TREE_FIELD_POS_ID, &d.pos_id},       {TREE_FIELD_GQ_PTR, &d.gq_ptr},
       {TREE_FIELD_GP_PTR, &d.gp_ptr},       {TREE_FIELD_GT_KIND, &d.gt_kind},
       {TREE_FIELD_GT_ATOM, &d.gt_atom},     {TREE_FIELD_GT_BIDX, &d.gt_bidx},
-      {TREE_FIELD_GT_BOUNDS, &d.gt_bounds},
+      {TREE_FIELD_GT_BOUNDS, &d.gt_bounds}, {TREE_FIELD_GW_KEND, &d.gw_kend},
+      {TREE_FIELD_GW_KT, &d.gw_kt},
   };
   // key_end is padded with zeros to whole 128-key tiles: the kernels copy it
   // a tile at a time, and a zero bound hides the keys past N from every row.
@@ -163,27 +164,59 @@ extern "C" void tree_plan_destroy(tree_plan_t* p) {
   delete p;
 }
 
-extern "C" tree_status_t tree_attn_fwd(const tree_plan_t* p, const void* q, const void* k,
-                                       const void* v, void* o, float* lse, int32_t hq,
-                                       int32_t hkv, int32_t head_dim, tree_dtype_t dtype,
-                                       float softmax_scale, tree_stream_t stream) {
+namespace {
+
+tree_status_t fwd_entry(const tree_plan_t* p, const void* q, const void* k, const void* v,
+                        const void* past_k, const void* past_v, void* o, float* lse, int32_t hq,
+                        int32_t hkv, int32_t head_dim, tree_dtype_t dtype, float softmax_scale,
+                        tree_stream_t stream, bool gateway_call) {
   if (!p) return fail(TREE_ERR_INVALID_ARG, "NULL plan");
   tree_status_t st = check_heads(hq, hkv, head_dim, dtype);
   if (st != TREE_OK) return st;
   if (!std::isfinite(softmax_scale) || softmax_scale < 0.f)
     return fail(TREE_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+  if (p->past_len > 0 && !gateway_call)
+    return fail(TREE_ERR_INVALID_ARG, "the plan has a gateway: use tree_attn_fwd_gateway");
+  if (gateway_call && dtype != TREE_DTYPE_BF16)
+    return fail(TREE_ERR_UNSUPPORTED, "gateway attention is bf16 only");
   if (p->N == 0) return TREE_OK;
   if (!q || !k || !v || !o || !lse) return fail(TREE_ERR_INVALID_ARG, "NULL tensor pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return fail(TREE_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (p->past_len > 0) {
+    if (!past_k || !past_v) return fail(TREE_ERR_INVALID_ARG, "NULL gateway key or value pointer");
+    if (!aligned16(past_k) || !aligned16(past_v))
+      return fail(TREE_ERR_INVALID_ARG, "gateway pointers must be 16-byte aligned");
+  }
   if ((st = check_plan_on_device(p)) != TREE_OK) return st;
   int* status = status_ptr();
   if (!status) return fail(TREE_ERR_CUDA, "status word unavailable");
   AttnArgs a{p, q, k, v, o, lse, hq, hkv, head_dim, resolve_scale(softmax_scale, head_dim),
              static_cast<cudaStream_t>(stream), status};
+  a.past_k = past_k;
+  a.past_v = past_v;
   cudaError_t e = dtype == TREE_DTYPE_F32 ? launch_fwd_f32(a) : launch_fwd_bf16(a);
   if (e != cudaSuccess) return cuda_fail(e, "tree_attn_fwd launch");
   return TREE_OK;
+}
+
+}  // namespace
+
+extern "C" tree_status_t tree_attn_fwd(const tree_plan_t* p, const void* q, const void* k,
+                                       const void* v, void* o, float* lse, int32_t hq,
+                                       int32_t hkv, int32_t head_dim, tree_dtype_t dtype,
+                                       float softmax_scale, tree_stream_t stream) {
+  return fwd_entry(p, q, k, v, nullptr, nullptr, o, lse, hq, hkv, head_dim, dtype, softmax_scale,
+                   stream, false);
+}
+
+extern "C" tree_status_t tree_attn_fwd_gateway(const tree_plan_t* p, const void* q, const void* k,
+                                               const void* v, const void* past_k,
+                                               const void* past_v, void* o, float* lse, int32_t hq,
+                                               int32_t hkv, int32_t head_dim, tree_dtype_t dtype,
+                                               float softmax_scale, tree_stream_t stream) {
+  return fwd_entry(p, q, k, v, past_k, past_v, o, lse, hq, hkv, head_dim, dtype, softmax_scale,
+                   stream, true);
 }
 
 extern "C" tree_status_t tree_rope(const tree_plan_t* p, void* x, int32_t heads, int32_t head_dim,
@@ -316,10 +349,17 @@ tree_status_t bwd_entry(const tree_plan_t* p, const void* dout, const void* q, c
                         const void* v, const void* o, const float* lse, void* dq, void* dk,
                         void* dv, int32_t hq, int32_t hkv, int32_t head_dim, tree_dtype_t dtype,
                         tree_dtype_t grad_dtype, float softmax_scale, void* workspace,
-                        size_t workspace_bytes, tree_stream_t stream, int phases) {
+                        size_t workspace_bytes, tree_stream_t stream, int phases,
+                        const void* past_k = nullptr, const void* past_v = nullptr,
+                        float* past_dk = nullptr, float* past_dv = nullptr,
+                        bool gateway_call = false) {
   if (!p) return fail(TREE_ERR_INVALID_ARG, "NULL plan");
   tree_status_t st = check_heads(hq, hkv, head_dim, dtype);
   if (st != TREE_OK) return st;
+  if (p->past_len > 0 && !gateway_call)
+    return fail(TREE_ERR_INVALID_ARG, "the plan has a gateway: use tree_attn_bwd_gateway");
+  if (gateway_call && dtype != TREE_DTYPE_BF16)
+    return fail(TREE_ERR_UNSUPPORTED, "gateway attention is bf16 only");
   if (grad_dtype != TREE_DTYPE_F32 && grad_dtype != TREE_DTYPE_BF16)
     return fail(TREE_ERR_INVALID_ARG, "unknown grad_dtype");
   if (dtype == TREE_DTYPE_F32 && grad_dtype != TREE_DTYPE_F32)
@@ -340,6 +380,10 @@ tree_status_t bwd_entry(const tree_plan_t* p, const void* dout, const void* q, c
   if ((st = check(common, 6)) != TREE_OK) return st;
   if ((phases & 1) && (st = check(phase_dq, 2)) != TREE_OK) return st;
   if ((phases & 2) && (st = check(phase_kv, 2)) != TREE_OK) return st;
+  if (p->past_len > 0) {
+    const void* gws[] = {past_k, past_v, past_dk, past_dv};
+    if ((st = check(gws, 4)) != TREE_OK) return st;
+  }
   const size_t need = tree_attn_bwd_workspace_bytes(p, hq, head_dim, dtype);
   if (workspace_bytes < need)
     return fail(TREE_ERR_INVALID_ARG, "workspace too small: need " + std::to_string(need) + " bytes");
@@ -350,12 +394,30 @@ tree_status_t bwd_entry(const tree_plan_t* p, const void* dout, const void* q, c
                 dq, dk,   dv,  hq,  hkv,      head_dim, grad_dtype == TREE_DTYPE_F32,
                 resolve_scale(softmax_scale, head_dim), workspace, workspace_bytes,
                 static_cast<cudaStream_t>(stream), status, phases};
+  a.past_k = past_k;
+  a.past_v = past_v;
+  a.past_dk = past_dk;
+  a.past_dv = past_dv;
   cudaError_t e = dtype == TREE_DTYPE_F32 ? launch_bwd_f32(a) : launch_bwd_bf16(a);
   if (e != cudaSuccess) return cuda_fail(e, "tree_attn_bwd launch");
   return TREE_OK;
 }
 
 }  // namespace
+
+extern "C" tree_status_t tree_attn_bwd_gateway(const tree_plan_t* p, const void* dout,
+                                               const void* q, const void* k, const void* v,
+                                               const void* past_k, const void* past_v,
+                                               const void* o, const float* lse, void* dq, void* dk,
+                                               void* dv, float* past_dk_acc, float* past_dv_acc,
+                                               int32_t hq, int32_t hkv, int32_t head_dim,
+                                               tree_dtype_t dtype, tree_dtype_t grad_dtype,
+                                               float softmax_scale, void* workspace,
+                                               size_t workspace_bytes, tree_stream_t stream) {
+  return bwd_entry(p, dout, q, k, v, o, lse, dq, dk, dv, hq, hkv, head_dim, dtype, grad_dtype,
+                   softmax_scale, workspace, workspace_bytes, stream, 3, past_k, past_v,
+                   past_dk_acc, past_dv_acc, true);
+}
 
 extern "C" tree_status_t tree_attn_bwd(const tree_plan_t* p, const void* dout, const void* q,
                                        const void* k, const void* v, const void* o,

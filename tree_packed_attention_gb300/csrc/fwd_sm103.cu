@@ -85,6 +85,7 @@ struct FwdParams {
   int* status;
   SchedSlot* sched;
   int N, hq, group, n_items, n_inner, mode, Tq;
+  int has_gateway;   // the plan's tiles include gateway keys
   float scale_log2;  // softmax scale * log2(e)
 };
 
@@ -127,7 +128,7 @@ __device__ __forceinline__ void read_header(const FwdParams& p, int it, int (&hd
 // ahead: its kind for this slot and the first key of atom (lane % 16). A
 // PARTIAL tile's key bounds come with its V stage.
 struct TileInfo {
-  int kind, arow;
+  int kind, arow, gw;  // gw: the tile holds gateway keys (past K/V, before every row)
 };
 
 __device__ __forceinline__ TileInfo load_tile(const FwdParams& p, int t, int s, int lane) {
@@ -135,6 +136,7 @@ __device__ __forceinline__ TileInfo load_tile(const FwdParams& p, int t, int s, 
   const int k = ldg_pinned(p.gt_kind + t);
   x.kind = ((p.mode == 0 ? (k | (k << 2)) : k) >> (2 * s)) & 3;
   x.arow = ldg_pinned(p.gt_atom + 16 * t + (lane & 15));
+  x.gw = (k >> 4) & 1;
   return x;
 }
 
@@ -173,6 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tree_attn_fwd_sm103(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ GatherMaps map_k,
                         const __grid_constant__ GatherMaps map_v,
+                        const __grid_constant__ GatherMaps map_pk,
+                        const __grid_constant__ GatherMaps map_pv,
                         const __grid_constant__ CUtensorMap map_o, const FwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {
@@ -231,6 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 5; ++b) {
       tma_prefetch_desc(&map_k.box[b]);
       tma_prefetch_desc(&map_v.box[b]);
+      if (p.has_gateway) {
+        tma_prefetch_desc(&map_pk.box[b]);
+        tma_prefetch_desc(&map_pv.box[b]);
+      }
     }
   }
   if (warp == 1) {
@@ -273,22 +281,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       ++qn;
       // this lane's atom and the bounds row of the next tile, one tile ahead
-      int arow_next = 0, bidx_next = -1;
+      int arow_next = 0, bidx_next = -1, kind_next = 0;
       if (x.beg < x.end) {
         arow_next = ldg_pinned(p.gt_atom + 16 * x.beg + (lane & 15));
         bidx_next = ldg_pinned(p.gt_bidx + x.beg);
+        kind_next = ldg_pinned(p.gt_kind + x.beg);
       }
       for (int t = x.beg; t < x.end; ++t, ++kv) {
         const int arow = arow_next, bidx = bidx_next;
+        const bool gw = (kind_next >> 4) & 1;  // gateway keys: the past K/V tensors
         if (t + 1 < x.end) {
           arow_next = ldg_pinned(p.gt_atom + 16 * (t + 1) + (lane & 15));
           bidx_next = ldg_pinned(p.gt_bidx + t + 1);
+          kind_next = ldg_pinned(p.gt_kind + t + 1);
         }
         const uint32_t st = kv % kStages, ph = (kv / kStages) & 1;
         if (kv >= kStages && !(ok = warp_wait(&bar_k_empty[st], ph ^ 1, abort, p.status))) break;
         if (lane == 0) mbar_arrive_expect_tx(&bar_k_full[st], kTileBytes);
         __syncwarp();
-        load_gathered(sK + st * kTileBytes, map_k, &bar_k_full[st], x.kvh, arow, lane);
+        load_gathered(sK + st * kTileBytes, gw ? map_pk : map_k, &bar_k_full[st], x.kvh, arow, lane);
         __syncwarp();
         if (kv >= kStages && !(ok = warp_wait(&bar_v_empty[st], ph ^ 1, abort, p.status))) break;
         if (lane == 0) {
@@ -300,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       512, &bar_v_full[st]);
         }
         __syncwarp();
-        load_gathered(sV + st * kTileBytes, map_v, &bar_v_full[st], x.kvh, arow, lane);
+        load_gathered(sV + st * kTileBytes, gw ? map_pv : map_v, &bar_v_full[st], x.kvh, arow, lane);
         __syncwarp();
       }
       if (!ok) break;
@@ -518,9 +529,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
           }
           const int r0 = qt * 128 + quarter * 32;
-          // rows [r0, r0+32) see key j iff j <= row < key_end[j]
-          diag = amax + 7 > r0;
-          mode = (mx <= r0 || amin > r0 + 31) ? 2 : (!diag && mn > r0 + 31) ? 1 : 0;
+          // rows [r0, r0+32) see key j iff j <= row < key_end[j]; gateway
+          // keys come before every row, so only the key_end bound applies
+          diag = !tl.gw && amax + 7 > r0;
+          mode = (mx <= r0 || (!tl.gw && amin > r0 + 31)) ? 2 : (!diag && mn > r0 + 31) ? 1 : 0;
         }
         if (mode == 2) {  // P = 0; m and l of the row are unchanged
           uint32_t pk[16];
@@ -682,10 +694,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_fwd_bf16(const AttnArgs& a) {
   const tree_plan* pl = a.plan;
   CUtensorMap mq, mo;
-  GatherMaps mk, mv;
+  GatherMaps mk, mv, mpk, mpv;
   if (!make_tile_map(&mq, a.q, pl->N, a.hq) || !make_gather_maps(&mk, a.k, pl->N, a.hkv) ||
       !make_gather_maps(&mv, a.v, pl->N, a.hkv) || !make_tile_map(&mo, a.o, pl->N, a.hq))
     return cudaErrorInvalidValue;
+  const bool gw = pl->past_len > 0;
+  if (gw) {
+    if (!make_gather_maps(&mpk, a.past_k, pl->past_len, a.hkv) ||
+        !make_gather_maps(&mpv, a.past_v, pl->past_len, a.hkv))
+      return cudaErrorInvalidValue;
+  } else {
+    mpk = mk;
+    mpv = mv;
+  }
   FwdParams p;
   const int G = a.hq / a.hkv;
   p.mode = (G >= 2 && G % 2 == 0) ? 0 : 1;
@@ -713,6 +734,7 @@ cudaError_t launch_fwd_bf16(const AttnArgs& a) {
   p.group = G;
   p.Tq = pl->Tq;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.has_gateway = gw ? 1 : 0;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(tree_attn_fwd_sm103,
@@ -721,7 +743,7 @@ cudaError_t launch_fwd_bf16(const AttnArgs& a) {
     attr_set = true;
   }
   const int grid = p.n_items < sm_count() ? p.n_items : sm_count();
-  tree_attn_fwd_sm103<<<grid, kThreads, kSmemBytes, a.stream>>>(mq, mk, mv, mo, p);
+  tree_attn_fwd_sm103<<<grid, kThreads, kSmemBytes, a.stream>>>(mq, mk, mv, mpk, mpv, mo, p);
   return cudaGetLastError();
 }
 

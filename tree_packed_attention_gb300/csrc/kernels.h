@@ -58,6 +58,8 @@ struct AttnArgs {
   float scale;  // softmax scale (already resolved; never 0)
   cudaStream_t stream;
   int* status;  // device status word
+  const void* past_k = nullptr;  // gateway keys and values of a partition plan
+  const void* past_v = nullptr;
 };
 
 struct AttnBwdArgs {
@@ -79,6 +81,10 @@ struct AttnBwdArgs {
   cudaStream_t stream;
   int* status;
   int phases;  // bit 0: Delta + dQ phase; bit 1: dK/dV phase (reads what phase 0 wrote)
+  const void* past_k = nullptr;  // gateway keys and values of a partition plan
+  const void* past_v = nullptr;
+  float* past_dk = nullptr;      // their gradients, accumulated in fp32
+  float* past_dv = nullptr;
 };
 
 // Workspace layouts.

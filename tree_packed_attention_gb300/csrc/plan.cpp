@@ -119,6 +119,58 @@ void build_gathered(tree_plan* p, int32_t U, std::vector<int32_t>& ptr) {
         j = e;
       }
     }
+    // gateway keys first: every row of the partition sees the visible ones
+    // (their own tiles, flagged; atoms hold rows of the past keys)
+    if (!p->gw_runs.empty()) {
+      int32_t gcol = kBlockN;
+      pieces.clear();
+      int32_t gtiles = 0;
+      for (const Iv& x : p->gw_runs) {
+        int32_t k = x.first, n = x.second - x.first;
+        while (n > 0) {
+          if (gcol >= kBlockN) {
+            ++gtiles;
+            gcol = 0;
+          }
+          const int32_t m = std::min(n, kBlockN - gcol);
+          pieces.push_back({gtiles - 1, gcol, k, m, 1});
+          gcol += m;
+          k += m;
+          n -= m;
+        }
+        gcol = (gcol + 7) & ~7;
+      }
+      for (size_t b = 0, e = 0; b < pieces.size(); b = e) {
+        const int32_t tile = pieces[b].tile;
+        int32_t cols = 0;
+        while (e < pieces.size() && pieces[e].tile == tile) cols += pieces[e++].n;
+        int32_t kw = 16;
+        bool partial = false;
+        for (int32_t sl = 0; sl < slots; ++sl) {
+          const int32_t ra = r0 + sl * kBlockM, rb = std::min(r1, ra + kBlockM);
+          int32_t kd = kEmpty;
+          if (ra < rb) kd = (cols == kBlockN && rb - ra == kBlockM) ? kFull : kPartial;
+          partial = partial || kd == kPartial;
+          kw |= kd << (2 * sl);
+        }
+        kind.push_back(kw);
+        int32_t a_row[kBlockN / 8];
+        for (int32_t a = 0; a < kBlockN / 8; ++a) a_row[a] = -8;
+        for (size_t q = b; q < e; ++q)
+          for (int32_t c = pieces[q].col; c < pieces[q].col + pieces[q].n; c += 8)
+            a_row[c / 8] = pieces[q].key + (c - pieces[q].col);
+        atom.insert(atom.end(), a_row, a_row + kBlockN / 8);
+        if (partial) {
+          bidx.push_back(static_cast<int32_t>(bounds.size() / kBlockN));
+          const size_t b0 = bounds.size();
+          bounds.resize(b0 + kBlockN, 0);
+          for (size_t q = b; q < e; ++q)
+            for (int32_t c = 0; c < pieces[q].n; ++c) bounds[b0 + pieces[q].col + c] = N;
+        } else {
+          bidx.push_back(-1);
+        }
+      }
+    }
     runs.clear();
     for (const Iv& x : common) push(runs, x.first, x.second);
     // runs[0 .. n_common) hold only keys every row of the unit sees (the run
@@ -199,7 +251,39 @@ void build_gathered(tree_plan* p, int32_t U, std::vector<int32_t>& ptr) {
   }
 }
 
-tree_status_t build(const int32_t* parents, const int32_t* lengths, int32_t S, tree_plan* p) {
+// The gateway of a partition plan: visible key runs and the per-key bound.
+void build_gateway(tree_plan* p, const uint8_t* visible, int32_t past_len) {
+  auto& F = p->field;
+  p->past_len = past_len;
+  p->gw_runs.clear();
+  int64_t nvis = 0;
+  for (int32_t j = 0; j < past_len;) {
+    if (!visible[j]) {
+      ++j;
+      continue;
+    }
+    int32_t e = j;
+    while (e < past_len && visible[e]) ++e;
+    p->gw_runs.emplace_back(j, e);
+    nvis += e - j;
+    j = e;
+  }
+  p->past_visible = nvis;
+  const int32_t tiles = (past_len + kBlockN - 1) / kBlockN;
+  auto& kend = F[TREE_FIELD_GW_KEND];
+  kend.assign(static_cast<size_t>(tiles) * kBlockN, 0);
+  for (int32_t j = 0; j < past_len; ++j) kend[j] = visible[j] ? p->N : 0;
+  auto& kt = F[TREE_FIELD_GW_KT];
+  kt.clear();
+  for (int32_t t = 0; t < tiles; ++t) {
+    bool any = false;
+    for (int32_t j = t * kBlockN; j < std::min(past_len, (t + 1) * kBlockN) && !any; ++j) any = visible[j] != 0;
+    if (any) kt.push_back(t);
+  }
+}
+
+tree_status_t build(const int32_t* parents, const int32_t* lengths, int32_t S, tree_plan* p,
+                    const uint8_t* past_visible = nullptr, int32_t past_len = 0) {
   auto& F = p->field;
   // ---- validation
   for (int32_t s = 0; s < S; ++s) {
@@ -438,6 +522,7 @@ tree_status_t build(const int32_t* parents, const int32_t* lengths, int32_t S, t
   p->P = P;
   p->visible_pairs = visible;
 
+  if (past_len > 0) build_gateway(p, past_visible, past_len);
   // ---- gathered key tiles: q-tiles first, then q-tile pairs, one table
   {
     const size_t est = static_cast<size_t>(nnz) * 3 / 2 + 16;  // about nnz + nnz / 2 tiles
@@ -457,18 +542,21 @@ tree_status_t build(const int32_t* parents, const int32_t* lengths, int32_t S, t
 
 using namespace treeattn;
 
-extern "C" tree_status_t tree_plan_build(const int32_t* segment_parents,
-                                         const int32_t* segment_lengths, int32_t num_segments,
-                                         tree_plan_t** out) {
+namespace {
+tree_status_t plan_entry(const int32_t* segment_parents, const int32_t* segment_lengths,
+                         int32_t num_segments, const uint8_t* past_visible, int32_t past_len,
+                         tree_plan_t** out) {
   if (!out) return fail(TREE_ERR_INVALID_ARG, "out is NULL");
   if (num_segments < 0) return fail(TREE_ERR_INVALID_ARG, "num_segments < 0");
   if (num_segments > 0 && (!segment_parents || !segment_lengths))
     return fail(TREE_ERR_INVALID_ARG, "NULL parents or lengths");
+  if (past_len < 0) return fail(TREE_ERR_INVALID_ARG, "past_len < 0");
+  if (past_len > 0 && !past_visible) return fail(TREE_ERR_INVALID_ARG, "NULL past_visible");
   tree_plan* p = new (std::nothrow) tree_plan();
   if (!p) return fail(TREE_ERR_OOM, "out of host memory");
   tree_status_t st;
   try {
-    st = build(segment_parents, segment_lengths, num_segments, p);
+    st = build(segment_parents, segment_lengths, num_segments, p, past_visible, past_len);
   } catch (const std::bad_alloc&) {
     st = fail(TREE_ERR_OOM, "out of host memory");
   }
@@ -479,6 +567,20 @@ extern "C" tree_status_t tree_plan_build(const int32_t* segment_parents,
   *out = p;
   set_error("");
   return TREE_OK;
+}
+}  // namespace
+
+extern "C" tree_status_t tree_plan_build(const int32_t* segment_parents,
+                                         const int32_t* segment_lengths, int32_t num_segments,
+                                         tree_plan_t** out) {
+  return plan_entry(segment_parents, segment_lengths, num_segments, nullptr, 0, out);
+}
+
+extern "C" tree_status_t tree_plan_build_partition(const int32_t* segment_parents,
+                                                   const int32_t* segment_lengths,
+                                                   int32_t num_segments, const uint8_t* past_visible,
+                                                   int32_t past_len, tree_plan_t** out) {
+  return plan_entry(segment_parents, segment_lengths, num_segments, past_visible, past_len, out);
 }
 
 extern "C" tree_status_t tree_plan_info(const tree_plan_t* p, tree_plan_info_t* out) {
@@ -496,6 +598,8 @@ extern "C" tree_status_t tree_plan_info(const tree_plan_t* p, tree_plan_info_t* 
   out->num_ancestors = static_cast<int64_t>(p->field[TREE_FIELD_ANC_IDX].size());
   out->visible_pairs = p->visible_pairs;
   out->num_gathered_tiles = static_cast<int64_t>(p->field[TREE_FIELD_GT_KIND].size());
+  out->past_len = p->past_len;
+  out->past_visible = p->past_visible;
   return TREE_OK;
 }
 

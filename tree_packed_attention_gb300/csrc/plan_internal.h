@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "treeattn.h"
@@ -39,7 +40,9 @@ struct DevicePlan {
   const int32_t* gt_kind = nullptr;    // [gathered tiles]
   const int32_t* gt_atom = nullptr;    // [gathered tiles * 16]
   const int32_t* gt_bidx = nullptr;    // [gathered tiles]
-  const int32_t* gt_bounds = nullptr;  // [bounds rows * 256]
+  const int32_t* gt_bounds = nullptr;  // [bounds rows * 128]
+  const int32_t* gw_kend = nullptr;    // [128 * gateway key tiles]
+  const int32_t* gw_kt = nullptr;      // [gateway key tiles with a visible key]
 };
 
 // Tables of the tree-correct causal conv for one kernel size (conv.cu): the
@@ -59,6 +62,9 @@ struct tree_plan {
   int32_t N = 0, S = 0, R = 0;
   int32_t Tq = 0, Tk = 0, P = 0;
   int64_t visible_pairs = 0;
+  int32_t past_len = 0;      // gateway keys of a partition plan
+  int64_t past_visible = 0;  // of which visible
+  std::vector<std::pair<int32_t, int32_t>> gw_runs;  // visible gateway key runs [a, b)
   std::vector<int32_t> field[TREE_FIELD_COUNT];
   treeattn::DevicePlan dev;
   treeattn::ConvTables conv;
