@@ -159,8 +159,8 @@ struct DqParams {
   const int32_t* order;
   const __nv_bfloat16* o;
   const float* lse;
-  float* lse2;   // out: [hq, Npad]
-  float* delta;  // out: [hq, Npad]
+  float* lse2;   // out: [hq, Npad], -lse * log2(e)
+  float* delta;  // out: [hq, Npad], -Delta
   void* dq;
   int* status;
   SchedSlot* sched;
@@ -531,7 +531,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       // and dO, both 128B-swizzled tiles in smem; rows past N count zero); a
       // transposing reduction leaves row 2m's sum in lanes 2m and 2m+1; the
       // two warps of the quarter swap halves through smem.
-      float delta = 0.f, lse2 = INFINITY;
+      // both kept negated (they are addends below), and stored so for dK/dV
+      float ndelta = 0.f, nlse2 = -INFINITY;
       {
         float part[16];
         const int r0 = qt * 128 + quarter * 32 + half * 16;
@@ -573,12 +574,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_delta[quarter]);
         if (!(ok = warp_wait(&bar_delta[quarter], qn & 1, abort, p.status))) break;
-        delta = sd[lane];
-        lse2 = lse_pre * kLog2e;
+        ndelta = -sd[lane];
+        nlse2 = -(lse_pre * kLog2e);
       }
       if (half == 0) {
-        p.delta[static_cast<size_t>(h) * p.Npad + i] = delta;
-        p.lse2[static_cast<size_t>(h) * p.Npad + i] = lse2;
+        p.delta[static_cast<size_t>(h) * p.Npad + i] = ndelta;
+        p.lse2[static_cast<size_t>(h) * p.Npad + i] = nlse2;
       }
       ++qn;
       if (nt_at != beg) fetch_tile(beg);
@@ -630,9 +631,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (mode != 2) {
           uint32_t rr[64];
           tmem_ld64(tSb, rr);  // this half of the S row, one wait
+          const float2 sc2 = make_float2(sl2, sl2), nl2 = make_float2(nlse2, nlse2);
 #pragma unroll
-          for (int jj = 0; jj < 64; ++jj)
-            pv[jj] = ex2_approx(fmaf(__uint_as_float(rr[jj]), sl2, -lse2));
+          for (int jj = 0; jj < 64; jj += 2) {
+            const float2 x = fma2(make_float2(__uint_as_float(rr[jj]), __uint_as_float(rr[jj + 1])), sc2, nl2);
+            pv[jj] = ex2_approx(x.x);
+            pv[jj + 1] = ex2_approx(x.y);
+          }
         }
         if (mode == 0 && diag) {
 #pragma unroll
@@ -668,14 +673,17 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           tmem_ld64(tDP + lane_off + col0, rr);  // this half of the dP row, one wait
           tc_fence_before_sync();
           mbar_arrive(&bar_dp_read);  // the dP buffer may take dP_{t+1}
+          const float2 nd2 = make_float2(ndelta, ndelta);
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t pk[16];
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const int col = c * 32 + 2 * jj;
-              pk[jj] = pack_bf16x2(pv[col] * (__uint_as_float(rr[col]) - delta),
-                                   pv[col + 1] * (__uint_as_float(rr[col + 1]) - delta));
+              const float2 y = mul2(make_float2(pv[col], pv[col + 1]),
+                                    add2(make_float2(__uint_as_float(rr[col]), __uint_as_float(rr[col + 1])),
+                                         nd2));
+              pk[jj] = pack_bf16x2(y.x, y.y);
             }
             tmem_st16(tSb + c * 16, pk);  // dS over the first 32 columns of this half
           }
@@ -780,8 +788,8 @@ struct KvParams {
   float* past_dk;          // gateway gradients, accumulated in fp32
   float* past_dv;
   int n_gw, past_len, Tq;
-  const float* lse2;   // [hq, Npad]
-  const float* delta;  // [hq, Npad]
+  const float* lse2;   // [hq, Npad], -lse * log2(e) (from the dQ phase)
+  const float* delta;  // [hq, Npad], -Delta
   void* dk;
   void* dv;
   int* status;
@@ -1070,8 +1078,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       for (int j = 0; j < x.steps; ++j, ++n) {
         const int q0 = (x.qlo + j / p.group) * 128 + col0;  // first q column of this half
         const uint32_t sd = n % kKvDoStages, pd = (n / kKvDoStages) & 1;
-        const float* lse2 = reinterpret_cast<const float*>(smem + kKvOffLse + sd * 512) + col0;
-        const float* dlt = reinterpret_cast<const float*>(smem + kKvOffDelta + sd * 512) + col0;
+        const float* nlse2 = reinterpret_cast<const float*>(smem + kKvOffLse + sd * 512) + col0;
+        const float* ndlt = reinterpret_cast<const float*>(smem + kKvOffDelta + sd * 512) + col0;
         if (!(ok = warp_wait(bar_do_full + sd, pd, abort, p.status))) break;
         if (!(ok = warp_wait(bar_s_full, n & 1, abort, p.status))) break;
         tc_fence_after_sync();
@@ -1083,26 +1091,26 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           tmem_ld64(tSr, rr);  // this half of the S^T row, one wait
           tc_fence_before_sync();
           mbar_arrive(bar_s_read);  // the S^T buffer may take the next S^T
-          if (all_full) {
+          // P^T = 2^(S^T * scale * log2e - lse * log2e); the workspace holds
+          // -lse * log2e, so each column pair is one packed fma
+          const float2 sc2 = make_float2(sl2, sl2);
 #pragma unroll
-            for (int jj = 0; jj < 64; jj += 4) {
-              const float4 l4 = *reinterpret_cast<const float4*>(lse2 + jj);
-              pv[jj + 0] = ex2_approx(fmaf(__uint_as_float(rr[jj + 0]), sl2, -l4.x));
-              pv[jj + 1] = ex2_approx(fmaf(__uint_as_float(rr[jj + 1]), sl2, -l4.y));
-              pv[jj + 2] = ex2_approx(fmaf(__uint_as_float(rr[jj + 2]), sl2, -l4.z));
-              pv[jj + 3] = ex2_approx(fmaf(__uint_as_float(rr[jj + 3]), sl2, -l4.w));
-            }
-          } else {
+          for (int jj = 0; jj < 64; jj += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(nlse2 + jj);
+            const float2 x01 = fma2(make_float2(__uint_as_float(rr[jj + 0]), __uint_as_float(rr[jj + 1])),
+                                    sc2, make_float2(l4.x, l4.y));
+            const float2 x23 = fma2(make_float2(__uint_as_float(rr[jj + 2]), __uint_as_float(rr[jj + 3])),
+                                    sc2, make_float2(l4.z, l4.w));
+            pv[jj + 0] = ex2_approx(x01.x);
+            pv[jj + 1] = ex2_approx(x01.y);
+            pv[jj + 2] = ex2_approx(x23.x);
+            pv[jj + 3] = ex2_approx(x23.y);
+          }
+          if (!all_full) {
 #pragma unroll
-            for (int jj = 0; jj < 64; jj += 4) {
-              const float4 l4 = *reinterpret_cast<const float4*>(lse2 + jj);
-              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int q = q0 + jj + u;
-                const float e = ex2_approx(fmaf(__uint_as_float(rr[jj + u]), sl2, -lv[u]));
-                pv[jj + u] = (jk <= q && q < ke) ? e : 0.f;
-              }
+            for (int jj = 0; jj < 64; ++jj) {
+              const int q = q0 + jj;
+              if (!(jk <= q && q < ke)) pv[jj] = 0.f;
             }
           }
         }
@@ -1125,11 +1133,15 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
             for (int jj = 0; jj < 32; jj += 4) {
               const int col = c * 32 + jj;
-              const float4 d4 = *reinterpret_cast<const float4*>(dlt + col);
-              pk[jj / 2] = pack_bf16x2(pv[col] * (__uint_as_float(rr[col]) - d4.x),
-                                       pv[col + 1] * (__uint_as_float(rr[col + 1]) - d4.y));
-              pk[jj / 2 + 1] = pack_bf16x2(pv[col + 2] * (__uint_as_float(rr[col + 2]) - d4.z),
-                                           pv[col + 3] * (__uint_as_float(rr[col + 3]) - d4.w));
+              const float4 d4 = *reinterpret_cast<const float4*>(ndlt + col);  // -Delta
+              const float2 y01 = mul2(make_float2(pv[col], pv[col + 1]),
+                                      add2(make_float2(__uint_as_float(rr[col]), __uint_as_float(rr[col + 1])),
+                                           make_float2(d4.x, d4.y)));
+              const float2 y23 = mul2(make_float2(pv[col + 2], pv[col + 3]),
+                                      add2(make_float2(__uint_as_float(rr[col + 2]), __uint_as_float(rr[col + 3])),
+                                           make_float2(d4.z, d4.w)));
+              pk[jj / 2] = pack_bf16x2(y01.x, y01.y);
+              pk[jj / 2 + 1] = pack_bf16x2(y23.x, y23.y);
             }
             tmem_st16(tPr + c * 16, pk);  // dS^T over the first 32 columns of this half
           }

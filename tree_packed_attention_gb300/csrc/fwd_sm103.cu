@@ -574,16 +574,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        // row max as 8 independent chains, then a tree (short dependency chains)
+        // row max: three-input maxima in 8 independent chains, then a tree
         float m8[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) m8[u] = sv[u];
+        for (int u = 0; u < 8; ++u) m8[u] = fmaxf(sv[u], sv[8 + u]);
 #pragma unroll
-        for (int c = 8; c < 128; c += 8)
+        for (int c = 16; c < 128; c += 16)
 #pragma unroll
-          for (int u = 0; u < 8; ++u) m8[u] = fmaxf(m8[u], sv[c + u]);
-        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          for (int u = 0; u < 8; ++u) m8[u] = max3f(m8[u], sv[c + u], sv[c + 8 + u]);
+        const float mx = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]),
+                               fmaxf(m8[6], m8[7]));
         const float m_tile = mx * sl2;
         const float m_new = fmaxf(m_ref, m_tile);
         const bool rescale = (m_ref != -INFINITY) && (m_new > m_ref + kRescaleThreshold);
@@ -595,20 +595,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = m_new;  // first visible keys of this row (or still none)
         }
         const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float rs4[4] = {0.f, 0.f, 0.f, 0.f};  // row sum in 4 independent chains
+        // P = 2^(S * scale * log2e - m), the scaling in column pairs; the row
+        // sum in two independent pair chains
+        const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-mr, -mr);
+        float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
-            const float p0 = ex2_approx(fmaf(sv[c * 32 + 2 * jj], sl2, -mr));
-            const float p1 = ex2_approx(fmaf(sv[c * 32 + 2 * jj + 1], sl2, -mr));
-            rs4[jj & 3] += p0 + p1;
-            pk[jj] = pack_bf16x2(p0, p1);
+            const float2 x = fma2(make_float2(sv[c * 32 + 2 * jj], sv[c * 32 + 2 * jj + 1]), sc2, nm2);
+            const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            rs2[jj & 1] = add2(rs2[jj & 1], pp);
+            pk[jj] = pack_bf16x2(pp.x, pp.y);
           }
           tmem_st16(tS + c * 16, pk);
         }
-        const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+        const float rs = (rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y);
         if (__any_sync(0xffffffffu, rescale)) {
           // O_s is quiescent: its last PV completed before this S did, and the
           // next PV waits for the P arrival below.
@@ -645,6 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before_sync();
       mbar_arrive(&bar_o_free[s]);  // O_s is in registers: the next item's PV may start
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf, ++halves) {
         // the store of the previous half has read the staging tile
@@ -653,11 +657,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 8; ++c) {  // 16-byte chunk c of the row, 128B-swizzled
           const int col = hf * 64 + c * 8;
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(ov[col + 0]) * inv, __uint_as_float(ov[col + 1]) * inv);
-          w.y = pack_bf16x2(__uint_as_float(ov[col + 2]) * inv, __uint_as_float(ov[col + 3]) * inv);
-          w.z = pack_bf16x2(__uint_as_float(ov[col + 4]) * inv, __uint_as_float(ov[col + 5]) * inv);
-          w.w = pack_bf16x2(__uint_as_float(ov[col + 6]) * inv, __uint_as_float(ov[col + 7]) * inv);
+          uint32_t w4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float2 y = mul2(make_float2(__uint_as_float(ov[col + 2 * u]),
+                                              __uint_as_float(ov[col + 2 * u + 1])), inv2);
+            w4[u] = pack_bf16x2(y.x, y.y);
+          }
+          const uint4 w = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           *reinterpret_cast<uint4*>(stage + r * 128 + ((c ^ (r & 7)) * 16)) = w;
         }
         fence_proxy_async_shared();

@@ -4,7 +4,7 @@
 // backward: a runtime whose memory pool already owns the whole device, or a
 // latency-critical loop where a cudaMalloc would synchronize the device. This
 // entry point runs the same backward as tree_attn_bwd with its scratch (the
-// per-row lse*log2(e) and Delta rows) taken from a fixed array compiled into
+// per-row -lse*log2(e) and -Delta rows) taken from a fixed array compiled into
 // the library instead of from a workspace argument. It allocates nothing.
 #include <cuda_runtime.h>
 
