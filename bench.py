@@ -604,6 +604,61 @@ def conv_arm(args):
     }))
 
 
+def ce_arm(args):
+    """--op ce: the fused weighted next-token cross-entropy (§3.1 eq. 3-5) with its
+    gradient, bf16 logits [N, V] of the workload (default 6: the packed shape at
+    32,768 tokens) and V = --vocab, lambda = g/K. HBM-bound: the figure is the
+    algorithmic bytes (logits read once, dlogits written once) over the
+    CUDA-event time; the kernel reads each row a second time from L2."""
+    import torch
+
+    import treegen
+    import tree_packed_attention_gb300 as tpa
+
+    torch.cuda.set_device(0)
+    w = treegen.workload(args.workload)
+    plan = tpa.tree_plan_build(w.parents, w.lengths)
+    N, V = plan.num_tokens, args.vocab
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    z = torch.empty(N, V, dtype=torch.bfloat16, device="cuda")
+    for r0 in range(0, N, 4096):  # drawn in slices to bound the fp32 temporary
+        r1 = min(N, r0 + 4096)
+        z[r0:r1] = (torch.randn(r1 - r0, V, device="cuda", generator=gen) * 3).to(torch.bfloat16)
+    tokens = torch.randint(0, V, (N,), device="cuda", generator=gen, dtype=torch.int32)
+    lam = torch.as_tensor(tpa.tree_weights(plan), device="cuda")
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        loss, row_loss, dz = tpa.tree_weighted_ce(plan, z, tokens, lam)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    with ClockSampler(0) as clocks:
+        for e in ev:
+            flush.zero_()
+            e[0].record(stream)
+            loss, row_loss, dz = tpa.tree_weighted_ce(plan, z, tokens, lam)
+            e[1].record(stream)
+        torch.cuda.synchronize()
+    tpa.tree_status_sync()
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    algo = 2 * N * V * z.element_size()
+    gbs = algo / (ms * 1e-3) / 1e9
+    peaks, kind = _peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    print(json.dumps({
+        "metric": "fused weighted tree cross-entropy (loss + dlogits), algorithmic GB/s on 1 GB300",
+        "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": N, "vocab": V, "weights": "g/K",
+                   "l2": "inputs larger than L2, and L2 flushed between steps"},
+        "tokens_per_s": N / (ms * 1e-3), "loss": float(loss),
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "peak_source": f"{kind} copy bandwidth", "traffic": None},
+        "clocks": clocks.summary(), "gpu_launches": 2 * args.steps,
+    }))
+
+
 def partition_arm(args):
     """--op partition: the host partition planner (§3.3) on the workload at a
     token cap; no GPU. Reports the partitions, their lower bound and the peak
@@ -643,9 +698,11 @@ def main():
     ap.add_argument("--extra-workloads", default="3,4",
                     help="comma-separated workloads also timed and reported under 'workloads' "
                          "('' for none)")
-    ap.add_argument("--op", default="attention", choices=["attention", "rope", "conv", "partition"],
+    ap.add_argument("--op", default="attention", choices=["attention", "rope", "conv", "ce", "partition"],
                     help="attention (the default and the headline), rope (tree RoPE on q and k), "
-                         "conv (the tree-correct causal conv) or partition (the host planner, no GPU)")
+                         "conv (the tree-correct causal conv), ce (the fused weighted cross-entropy; "
+                         "workload 6 unless --workload is given) or partition (the host planner, no GPU)")
+    ap.add_argument("--vocab", type=int, default=151936, help="vocabulary for --op ce")
     ap.add_argument("--channels", type=int, default=4096, help="channels for --op conv")
     ap.add_argument("--cap", type=int, default=16384, help="token cap for --op partition")
     args = ap.parse_args()
@@ -653,6 +710,10 @@ def main():
         rope_arm(args)
     elif args.op == "conv":
         conv_arm(args)
+    elif args.op == "ce":
+        if "--workload" not in sys.argv:
+            args.workload = 6
+        ce_arm(args)
     elif args.op == "partition":
         partition_arm(args)
     elif args.impl == "reference":

@@ -407,11 +407,45 @@ tree_status_t tree_rope(const tree_plan_t* plan, void* x, int32_t heads, int32_t
                         tree_dtype_t dtype, float base, int32_t rotate_half, int32_t inverse,
                         tree_stream_t stream);
 
+/* Fused weighted next-token cross-entropy over the trie, loss and gradient in
+ * one pass ("Tree Training" §3.1 eq. 3-5: the tree loss is sum_t lambda_t *
+ * l_t over unique tokens; §3.2 "Loss Weights").
+ * On every root-to-leaf path the token after position r is predicted from the
+ * logits row r: in the DFS layout token r + 1 when it is in r's segment, else
+ * the first token of each child segment of r's segment (a leaf's last token
+ * predicts nothing, a root's first token is predicted by nothing). With t
+ * predicted from r:
+ *   row_loss[r] = sum over r -> t of lambda[t] * (logsumexp(z_r) - z_r[tokens[t]])
+ *   dlogits[r]  = grad_scale * sum over r -> t of lambda[t] * (softmax(z_r) - e_tokens[t])
+ *   *loss       = sum of row_loss (fp64, fixed order)
+ *  - logits, dlogits: device [N, vocab] row-major, bf16 or fp32 by dtype,
+ *    16-byte aligned; dlogits may be logits itself (in place) but must not
+ *    overlap it otherwise; every element of dlogits is written, each rounded
+ *    once from fp32.
+ *  - tokens: device int32 [N], the token ids of the DFS sequence; a negative id
+ *    means the token is not predicted (an ignored position); an id >= vocab is
+ *    skipped and reported by tree_status_sync (TREE_ERR_INVALID_ARG).
+ *  - lambda: device fp32 [N], the weight of the prediction of each token (e.g.
+ *    tree_weights: g_t / K; any sign; 0 skips it).
+ *  - row_loss: device fp32 [N] out; loss: device fp64 out, or NULL.
+ *  - vocab: a positive multiple of 8. Arithmetic in fp32 with hardware ex2;
+ *    one CTA per row, two passes over it (the second from L2).
+ * Asynchronous on `stream`; the plan must be on the current device (an N = 0
+ * plan only clears *loss). Errors: NULL plan or pointer, bad dtype or vocab,
+ * misaligned or partially overlapping logits/dlogits, grad_scale not finite
+ * -> TREE_ERR_INVALID_ARG; a segment with more than 1024 children ->
+ * TREE_ERR_UNSUPPORTED; plan not on the device -> TREE_ERR_NOT_ON_DEVICE. */
+tree_status_t tree_weighted_ce(const tree_plan_t* plan, const void* logits, void* dlogits,
+                               const int32_t* tokens, const float* lambda, int32_t vocab,
+                               tree_dtype_t dtype, float grad_scale, float* row_loss, double* loss,
+                               tree_stream_t stream);
+
 /* Wait for `stream`, then read and clear the device status word of the
  * current device: TREE_ERR_TIMEOUT if a kernel gave up a bounded wait since
  * the last check (the message names the wait: 10000 + source line in the
  * forward kernel file, 20000 + line in the backward one, 30000 + warp for
- * the work ring), TREE_ERR_CUDA on a CUDA error, else TREE_OK. */
+ * the work ring), TREE_ERR_INVALID_ARG if tree_weighted_ce met a token id >=
+ * vocab, TREE_ERR_CUDA on a CUDA error, else TREE_OK. */
 tree_status_t tree_status_sync(tree_stream_t stream);
 
 /* Message for the last failing call on this thread ("" if none). */

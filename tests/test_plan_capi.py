@@ -214,3 +214,16 @@ def test_conv_validates_its_arguments():
     assert lib.tree_conv_fwd(plan.handle, *args, 8, 5, 1, None) == 1  # dtype
     assert lib.tree_conv_fwd(plan.handle, *args, 8, 1, 2, None) == 1  # activation
     assert lib.tree_conv_bwd_workspace_bytes(plan.handle, 8) == 0  # nothing prepared yet
+
+
+def test_weighted_ce_host_checks():
+    """Rejected before any device use: bad vocab, dtype, grad_scale, NULL pointers."""
+    plan = tpa.tree_plan_build([-1, 0], [3, 2])
+    L = tpa.lib.tree_weighted_ce
+    assert L(plan.handle, None, None, None, None, 7, 1, 1.0, None, None, None) == 1
+    assert b"multiple of 8" in tpa.lib.tree_last_error()
+    assert L(plan.handle, None, None, None, None, 8, 9, 1.0, None, None, None) == 1
+    assert L(plan.handle, None, None, None, None, 8, 1, float("inf"), None, None, None) == 1
+    assert L(plan.handle, None, None, None, None, 8, 1, 1.0, None, None, None) == 1
+    assert b"NULL" in tpa.lib.tree_last_error()
+    assert L(None, None, None, None, None, 8, 1, 1.0, None, None, None) == 1

@@ -29,7 +29,7 @@ __all__ = [
     "tree_attn_bwd_dkdv", "tree_attn_bwd_workspace_bytes",
     "tree_weights", "tree_weights_paths", "tree_partition", "tree_rope", "tree_rope_apply",
     "TreeRopeFn", "tree_conv_fwd", "tree_conv_bwd", "tree_conv", "TreeConvFn",
-    "tree_status_sync", "TreeAttnFn", "tree_attention", "TreeAttnError",
+    "tree_weighted_ce", "tree_status_sync", "TreeAttnFn", "tree_attention", "TreeAttnError",
     "FIELDS", "EXPORTS", "LIB_PATH",
 ]
 
@@ -426,6 +426,41 @@ def tree_rope(plan: Plan, x, base: float = 10000.0, rotate_half: bool = False,
     check(lib.tree_rope(plan.handle, x.data_ptr(), x.shape[1], x.shape[2], _dtype_code(x),
                         float(base), int(bool(rotate_half)), int(bool(inverse)), s))
     return x
+
+
+def tree_weighted_ce(plan: Plan, logits, tokens, lam, grad_scale: float = 1.0, in_place: bool = False,
+                     stream=None):
+    """Fused weighted next-token cross-entropy over the trie (§3.1 eq. 3-5, §3.2
+    "Loss Weights"); returns (loss fp64 scalar tensor, row_loss [N] fp32, dlogits).
+
+    logits [N, V] (bf16 or fp32, V a multiple of 8); tokens [N] int32 token ids of
+    the DFS sequence (< 0: that token is not predicted); lam [N] fp32 weight of the
+    prediction of each token (e.g. tree_weights: g_t / K). dlogits is the gradient
+    of grad_scale * loss; with ``in_place`` it overwrites logits."""
+    import torch
+
+    N = plan.num_tokens
+    if logits.dim() != 2 or logits.shape[0] != N:
+        raise ValueError(f"logits must be [N={N}, V], got {tuple(logits.shape)}")
+    if logits.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError(f"logits must be bf16 or fp32, got {logits.dtype}")
+    V = logits.shape[1]
+    _check_tensor("logits", logits, (N, V))
+    if tokens.dtype != torch.int32 or tuple(tokens.shape) != (N,):
+        raise ValueError("tokens must be int32 [N]")
+    if lam.dtype != torch.float32 or tuple(lam.shape) != (N,):
+        raise ValueError("lam must be fp32 [N]")
+    _check_tensor("tokens", tokens, (N,))
+    _check_tensor("lam", lam, (N,))
+    dlogits = logits if in_place else torch.empty_like(logits)
+    row_loss = torch.empty(N, dtype=torch.float32, device=logits.device)
+    loss = torch.empty((), dtype=torch.float64, device=logits.device)
+    s = _stream_ptr(stream)
+    plan.to_device(s)
+    check(lib.tree_weighted_ce(plan.handle, logits.data_ptr(), dlogits.data_ptr(), tokens.data_ptr(),
+                               lam.data_ptr(), V, _dtype_code(logits), float(grad_scale),
+                               row_loss.data_ptr(), loss.data_ptr(), s))
+    return loss, row_loss, dlogits
 
 
 def tree_status_sync(stream=None) -> None:

@@ -114,7 +114,8 @@ extern "C" tree_status_t tree_plan_to_device(tree_plan_t* p, tree_stream_t strea
       {TREE_FIELD_GP_PTR, &d.gp_ptr},       {TREE_FIELD_GT_KIND, &d.gt_kind},
       {TREE_FIELD_GT_ATOM, &d.gt_atom},     {TREE_FIELD_GT_BIDX, &d.gt_bidx},
       {TREE_FIELD_GT_BOUNDS, &d.gt_bounds}, {TREE_FIELD_GW_KEND, &d.gw_kend},
-      {TREE_FIELD_GW_KT, &d.gw_kt},
+      {TREE_FIELD_GW_KT, &d.gw_kt},         {TREE_FIELD_TOKEN_SEG, &d.token_seg},
+      {TREE_FIELD_SUBTREE_END, &d.subtree_end},
   };
   // key_end is padded with zeros to whole 128-key tiles: the kernels copy it
   // a tile at a time, and a zero bound hides the keys past N from every row.
@@ -217,6 +218,64 @@ extern "C" tree_status_t tree_attn_fwd_gateway(const tree_plan_t* p, const void*
                                                float softmax_scale, tree_stream_t stream) {
   return fwd_entry(p, q, k, v, past_k, past_v, o, lse, hq, hkv, head_dim, dtype, softmax_scale,
                    stream, true);
+}
+
+extern "C" tree_status_t tree_weighted_ce(const tree_plan_t* p, const void* logits, void* dlogits,
+                                          const int32_t* tokens, const float* lambda, int32_t vocab,
+                                          tree_dtype_t dtype, float grad_scale, float* row_loss,
+                                          double* loss, tree_stream_t stream) {
+  if (!p) return fail(TREE_ERR_INVALID_ARG, "NULL plan");
+  if (dtype != TREE_DTYPE_BF16 && dtype != TREE_DTYPE_F32) return fail(TREE_ERR_INVALID_ARG, "unknown dtype");
+  if (vocab <= 0 || vocab % 8 != 0) return fail(TREE_ERR_INVALID_ARG, "vocab must be a positive multiple of 8");
+  if (!std::isfinite(grad_scale)) return fail(TREE_ERR_INVALID_ARG, "grad_scale must be finite");
+  if (p->N == 0) {
+    if (loss && cudaMemsetAsync(loss, 0, sizeof(double), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return fail(TREE_ERR_CUDA, "loss clear");
+    return TREE_OK;
+  }
+  if (!logits || !dlogits || !tokens || !lambda || !row_loss) return fail(TREE_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned16(logits) || !aligned16(dlogits))
+    return fail(TREE_ERR_INVALID_ARG, "logits and dlogits must be 16-byte aligned");
+  const size_t row_bytes = static_cast<size_t>(vocab) * (dtype == TREE_DTYPE_F32 ? 4 : 2);
+  const size_t bytes = row_bytes * static_cast<size_t>(p->N);
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(logits), b0 = reinterpret_cast<uintptr_t>(dlogits);
+  if (a0 != b0 && a0 < b0 + bytes && b0 < a0 + bytes)
+    return fail(TREE_ERR_INVALID_ARG, "dlogits must be logits itself or not overlap it");
+  // the distinct targets of one row are the first tokens of one segment's
+  // children: bound the fan-out on the host
+  {
+    const auto& ap = p->field[TREE_FIELD_ANC_PTR];
+    const auto& ai = p->field[TREE_FIELD_ANC_IDX];
+    std::vector<int32_t> fan(static_cast<size_t>(p->S), 0);
+    for (int32_t s = 0; s < p->S; ++s)
+      if (ap[s + 1] > ap[s]) ++fan[ai[ap[s + 1] - 1]];
+    for (int32_t s = 0; s < p->S; ++s)
+      if (fan[s] > kCeMaxTargets)
+        return fail(TREE_ERR_UNSUPPORTED, "a segment has more than " + std::to_string(kCeMaxTargets) +
+                                              " children");
+  }
+  tree_status_t st = check_plan_on_device(p);
+  if (st != TREE_OK) return st;
+  int* status = status_ptr();
+  if (!status) return fail(TREE_ERR_CUDA, "status word unavailable");
+  CeArgs a;
+  a.logits = logits;
+  a.dlogits = dlogits;
+  a.tokens = tokens;
+  a.lam = lambda;
+  a.token_seg = p->dev.token_seg;
+  a.subtree_end = p->dev.subtree_end;
+  a.row_loss = row_loss;
+  a.loss = loss;
+  a.status = status;
+  a.N = p->N;
+  a.V = vocab;
+  a.f32 = dtype == TREE_DTYPE_F32 ? 1 : 0;
+  a.grad_scale = grad_scale;
+  a.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_weighted_ce(a);
+  if (e != cudaSuccess) return cuda_fail(e, "tree_weighted_ce launch");
+  return TREE_OK;
 }
 
 extern "C" tree_status_t tree_rope(const tree_plan_t* p, void* x, int32_t heads, int32_t head_dim,
@@ -463,6 +522,10 @@ extern "C" tree_status_t tree_status_sync(tree_stream_t stream) {
     cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int));
     if (word == 9)
       return fail(TREE_ERR_CUDA, "a kernel's shared memory block was not 1024-byte aligned");
+    if (word == 8)
+      return fail(TREE_ERR_INVALID_ARG, "a token id was >= vocab (its prediction was skipped)");
+    if (word == 7)
+      return fail(TREE_ERR_UNSUPPORTED, "a logits row had more distinct targets than it can hold");
     return fail(TREE_ERR_TIMEOUT, "a kernel gave up a bounded wait (wait site " +
                                       std::to_string(word) + ")");
   }

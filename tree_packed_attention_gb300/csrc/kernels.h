@@ -47,6 +47,23 @@ size_t conv_bwd_workspace(int N, int C, int K);
 cudaError_t launch_conv_fwd(const ConvArgs& a);
 cudaError_t launch_conv_bwd(ConvArgs a);
 
+// Fused weighted next-token cross-entropy over the trie (loss.cu).
+constexpr int kCeMaxTargets = 1024;  // distinct target ids predicted from one row
+struct CeArgs {
+  const void* logits;  // [N, V]
+  void* dlogits;       // [N, V] (may be logits itself)
+  const int32_t* tokens;
+  const float* lam;
+  const int32_t* token_seg;    // plan (device)
+  const int32_t* subtree_end;  // plan (device)
+  float* row_loss;             // [N]
+  double* loss;                // sum of row_loss, or nullptr
+  int* status;
+  int N, V, f32;
+  float grad_scale;
+  cudaStream_t stream;
+};
+cudaError_t launch_weighted_ce(const CeArgs& a);
 struct AttnArgs {
   const tree_plan* plan;
   const void* q;

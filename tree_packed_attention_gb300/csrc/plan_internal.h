@@ -43,6 +43,8 @@ struct DevicePlan {
   const int32_t* gt_bounds = nullptr;  // [bounds rows * 128]
   const int32_t* gw_kend = nullptr;    // [128 * gateway key tiles]
   const int32_t* gw_kt = nullptr;      // [gateway key tiles with a visible key]
+  const int32_t* token_seg = nullptr;  // [N]
+  const int32_t* subtree_end = nullptr;  // [S]
 };
 
 // Tables of the tree-correct causal conv for one kernel size (conv.cu): the
