@@ -328,6 +328,9 @@ ConvArgs conv_args(const tree_plan_t* p, const void* x, const float* weight, con
   a.pred = p->conv.pred;
   a.succ_ptr = p->conv.succ_ptr;
   a.succ = p->conv.succ;
+  a.irr_bits = p->conv.irr_bits;
+  a.irr_list = p->conv.irr_list;
+  a.num_irr = p->conv.num_irr;
   a.x = x;
   a.weight = weight;
   a.bias = bias;
@@ -387,7 +390,7 @@ extern "C" tree_status_t tree_conv_bwd(const tree_plan_t* p, const void* x, cons
   a.dx = dx;
   a.dweight = dweight;
   a.dbias = dbias;
-  a.g = static_cast<float*>(workspace);
+  a.partial = static_cast<float*>(workspace);
   cudaError_t e = launch_conv_bwd(a);
   if (e != cudaSuccess) return cuda_fail(e, "tree_conv_bwd launch");
   return TREE_OK;

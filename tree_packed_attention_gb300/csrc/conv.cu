@@ -12,8 +12,11 @@
 // (which (t, k) read token u) for the backward's gather.
 //
 // All kernels stream rows of C channels (token-major [N, C], 8 channels per
-// thread and access), so they are bound by memory bandwidth. The backward is
-// deterministic: dx gathers over the inverse lists in a fixed order, and
+// thread and access), so they are bound by memory bandwidth. The backward reads
+// x and dy and writes dx once (one pass over each block's token range, the
+// gradient at the pre-activation kept in registers), plus a gather over the
+// inverse lists for the few tokens just before a branch into several
+// children. It is deterministic: every dx is a sum in a fixed order, and
 // dweight / dbias reduce fixed token ranges per block and then the blocks in
 // order.
 #include <cuda_bf16.h>
@@ -29,7 +32,7 @@ namespace treeattn {
 namespace {
 
 constexpr int kConvThreads = 256;
-constexpr int kConvPartialBlocks = 256;  // token ranges of the dweight / dbias reduction
+constexpr int kConvPartialBlocks = 512;  // token ranges of the backward (and its dweight / dbias sums)
 
 template <typename T>
 struct Vec8;
@@ -238,9 +241,20 @@ __global__ void __launch_bounds__(kConvThreads) conv_fwd_kernel(const ConvArgs a
   });
 }
 
-// g = dy * act'(pre), fp32, into the workspace
+// The backward in one pass over each block's token range, in DFS order:
+//   g[t]  = dy[t] * act'(pre_t), from the window that the forward also walks;
+//   dweight[c, K-1-k] += g[t] x[pred_k(t)] and dbias[c] += g[t] for t in the
+//   range (per-block sums, reduced in block order afterwards);
+//   dx[u] = sum over k of w[c, K-1-k] g[u+k] over the k for which u, u+1, ..,
+//   u+k is an unbroken run of path steps (each token's path predecessor is
+//   the one before it in DFS order), which is every (t, k) with pred_k(t) = u
+//   unless u is listed as irregular (some reader of u lies after a jump in
+//   the DFS order: a second or later child); those get dx from
+//   conv_bwd_dx_irregular_kernel. The walk runs K-1 tokens past the range
+//   (g only) so the range's last tokens see their readers; g never leaves
+//   registers.
 template <typename T, int K>
-__global__ void __launch_bounds__(kConvThreads) conv_bwd_g_kernel(const ConvArgs a) {
+__global__ void __launch_bounds__(kConvThreads) conv_bwd_fused_kernel(const ConvArgs a) {
   const int q = blockIdx.y * kConvThreads + threadIdx.x;
   if (q >= a.C / 8) return;
   Taps<K> tp;
@@ -248,60 +262,9 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_g_kernel(const ConvArgs
   float b[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) b[j] = a.bias ? __ldg(a.bias + 8 * q + j) : 0.f;
-  const T* dy = static_cast<const T*>(a.dy);
-  int t0, t1;
-  token_range(a, t0, t1);
-  if (a.act != 1) {  // g = dy
-    for (int t = t0; t < t1; ++t) {
-      float g[8];
-      Vec8<T>::load(dy + static_cast<size_t>(t) * a.C + 8 * q, g);
-      Vec8<float>::store(a.g + static_cast<size_t>(t) * a.C + 8 * q, g);
-    }
-    return;
-  }
-  walk<T, K>(a, q, t0, t1, [&](int t, const Window<T, K>& win) {
-    float z[8], g[8];
-    Vec8<T>::load(dy + static_cast<size_t>(t) * a.C + 8 * q, g);
-    win.pre(tp, b, z);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) g[j] *= silu_grad(z[j]);
-    Vec8<float>::store(a.g + static_cast<size_t>(t) * a.C + 8 * q, g);
-  });
-}
-
-// dx[u] = sum over the (t, k) that read u of w[c, K-1-k] g[t], in list order
-template <typename T, int K>
-__global__ void __launch_bounds__(kConvThreads) conv_bwd_dx_kernel(const ConvArgs a) {
-  const int q = blockIdx.y * kConvThreads + threadIdx.x;
-  if (q >= a.C / 8) return;
-  Taps<K> tp;
-  tp.load(a.weight, q);
-  T* dx = static_cast<T*>(a.dx);
-  for (int u = blockIdx.x; u < a.N; u += gridDim.x) {
-    const int e0 = __ldg(a.succ_ptr + u), e1 = __ldg(a.succ_ptr + u + 1);
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int e = e0; e < e1; ++e) {
-      const int packed = __ldg(a.succ + e), t = packed >> 3, k = packed & 7;
-      float g[8];
-      Vec8<float>::load(a.g + static_cast<size_t>(t) * a.C + 8 * q, g);
-#pragma unroll
-      for (int kk = 0; kk < K; ++kk) {  // select tap k without indexing registers at run time
-        if (kk != k) continue;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = fmaf(tp.w[j][K - 1 - kk], g[j], acc[j]);
-      }
-    }
-    Vec8<T>::store(dx + static_cast<size_t>(u) * a.C + 8 * q, acc);
-  }
-}
-
-// per block: sums over its token range of g[t, c] x[pred_k(t), c] (k < K)
-// and of g[t, c]; written to the block's slice of the partial sums
-template <typename T, int K>
-__global__ void __launch_bounds__(kConvThreads) conv_bwd_dw_partial_kernel(const ConvArgs a) {
-  const int q = blockIdx.y * kConvThreads + threadIdx.x;
-  if (q >= a.C / 8) return;
   const T* x = static_cast<const T*>(a.x);
+  const T* dy = static_cast<const T*>(a.dy);
+  T* dx = static_cast<T*>(a.dx);
   int t0, t1;
   token_range(a, t0, t1);
   float acc[K + 1][8];
@@ -309,19 +272,93 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_dw_partial_kernel(const
   for (int k = 0; k <= K; ++k)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[k][j] = 0.f;
-  for (int t = t0; t < t1; ++t) {
-    float g[8];
-    Vec8<float>::load(a.g + static_cast<size_t>(t) * a.C + 8 * q, g);
+  if (t0 < t1) {
+    const int te = min(a.N, t1 + K - 1);  // the last real token walked, plus one
+    float gh[K][8];                       // gh[k] = g of the token k steps back in DFS order
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[K][j] += g[j];
+    for (int k = 0; k < K; ++k)
 #pragma unroll
-    for (int k = 0; k < K; ++k) {
-      const int u = pred_of<K>(a, t, k);
-      if (u < 0) continue;
-      float v[8];
-      Vec8<T>::load(x + static_cast<size_t>(u) * a.C + 8 * q, v);
+      for (int j = 0; j < 8; ++j) gh[k][j] = 0.f;
+    uint32_t cont = 0;  // bit k: the token k steps back follows its DFS predecessor on its path
+    RawChunk<T> rx[kConvAhead], rd[kConvAhead];
+    int pr[kConvAhead];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[k][j] = fmaf(g[j], v[j], acc[k][j]);
+    for (int d = 0; d < kConvAhead; ++d) {
+      const int t = t0 + d;
+      pr[d] = -1;
+      if (t < te) {
+        rx[d].load(x + static_cast<size_t>(t) * a.C + 8 * q);
+        rd[d].load(dy + static_cast<size_t>(t) * a.C + 8 * q);
+        pr[d] = K > 1 ? pred_of<K>(a, t, 1) : t - 1;
+      }
+    }
+    Window<T, K> win;
+    for (int tb = t0; tb < t1 + K - 1; tb += kConvAhead) {
+#pragma unroll
+      for (int d = 0; d < kConvAhead; ++d) {
+        const int t = tb + d;
+        if (t >= t1 + K - 1) break;
+        float g[8];
+        bool step = false;
+        if (t < te) {
+          float xt[8];
+          rx[d].widen(xt);
+          rd[d].widen(g);
+          const int p1 = pr[d];
+          const int tn = t + kConvAhead;
+          if (tn < te) {
+            rx[d].load(x + static_cast<size_t>(tn) * a.C + 8 * q);
+            rd[d].load(dy + static_cast<size_t>(tn) * a.C + 8 * q);
+            pr[d] = K > 1 ? pred_of<K>(a, tn, 1) : tn - 1;
+          }
+          step = p1 == t - 1;
+          if (t > t0 && step)
+            win.shift(xt);
+          else
+            win.reload(a, t, q, xt);
+          if (a.act == 1) {
+            float z[8];
+            win.pre(tp, b, z);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) g[j] *= silu_grad(z[j]);
+          }
+          if (t < t1) {
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+              for (int j = 0; j < 8; ++j) acc[k][j] = fmaf(g[j], win.v[k][j], acc[k][j]);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[K][j] += g[j];
+          }
+        } else {  // past the last token: no readers
+#pragma unroll
+          for (int j = 0; j < 8; ++j) g[j] = 0.f;
+        }
+#pragma unroll
+        for (int k = K - 1; k > 0; --k)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) gh[k][j] = gh[k - 1][j];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) gh[0][j] = g[j];
+        cont = (cont << 1) | (step ? 1u : 0u);
+        // token u = t - (K-1) now has all of its run readers u .. t
+        const int u = t - (K - 1);
+        if (u >= t0 && u < a.N && !(__ldg(a.irr_bits + (u >> 5)) >> (u & 31) & 1u)) {
+          float o[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) o[j] = tp.w[j][K - 1] * gh[K - 1][j];  // k = 0: u itself
+          bool run = true;
+#pragma unroll
+          for (int k = 1; k < K; ++k) {
+            run = run && ((cont >> (K - 1 - k)) & 1u);  // u + k follows u + k - 1
+            if (run) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) o[j] = fmaf(tp.w[j][K - 1 - k], gh[K - 1 - k][j], o[j]);
+            }
+          }
+          Vec8<T>::store(dx + static_cast<size_t>(u) * a.C + 8 * q, o);
+        }
+      }
     }
   }
   float* part = a.partial + static_cast<size_t>(blockIdx.x) * (K + 1) * a.C;
@@ -329,6 +366,49 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_dw_partial_kernel(const
   for (int k = 0; k <= K; ++k)
 #pragma unroll
     for (int j = 0; j < 8; ++j) part[static_cast<size_t>(k) * a.C + 8 * q + j] = acc[k][j];
+}
+
+// dx of the irregular tokens: the gather over every (t, k) with pred_k(t) = u
+// in list order, g[t] recomputed from t's window and dy[t]
+template <typename T, int K>
+__global__ void __launch_bounds__(kConvThreads) conv_bwd_dx_irregular_kernel(const ConvArgs a) {
+  const int q = blockIdx.y * kConvThreads + threadIdx.x;
+  if (q >= a.C / 8) return;
+  Taps<K> tp;
+  tp.load(a.weight, q);
+  float b[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) b[j] = a.bias ? __ldg(a.bias + 8 * q + j) : 0.f;
+  const T* x = static_cast<const T*>(a.x);
+  const T* dy = static_cast<const T*>(a.dy);
+  T* dx = static_cast<T*>(a.dx);
+  for (int i = blockIdx.x; i < a.num_irr; i += gridDim.x) {
+    const int u = __ldg(a.irr_list + i);
+    const int e0 = __ldg(a.succ_ptr + u), e1 = __ldg(a.succ_ptr + u + 1);
+    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int e = e0; e < e1; ++e) {
+      const int packed = __ldg(a.succ + e), t = packed >> 3, k = packed & 7;
+      float g[8];
+      Vec8<T>::load(dy + static_cast<size_t>(t) * a.C + 8 * q, g);
+      if (a.act == 1) {
+        float xt[8];
+        Vec8<T>::load(x + static_cast<size_t>(t) * a.C + 8 * q, xt);
+        Window<T, K> win;
+        win.reload(a, t, q, xt);
+        float z[8];
+        win.pre(tp, b, z);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] *= silu_grad(z[j]);
+      }
+#pragma unroll
+      for (int kk = 0; kk < K; ++kk) {  // select tap k without indexing registers at run time
+        if (kk != k) continue;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[j] = fmaf(tp.w[j][K - 1 - kk], g[j], o[j]);
+      }
+    }
+    Vec8<T>::store(dx + static_cast<size_t>(u) * a.C + 8 * q, o);
+  }
 }
 
 // dweight[c, K-1-k] and dbias[c]: the blocks' partial sums in block order
@@ -398,11 +478,37 @@ tree_status_t conv_tables_build(tree_plan* p, int K, cudaStream_t stream) {
       if (u >= 0) succ[fill[u]++] = (t << 3) | k;
     }
   }
+  // Irregular tokens: some reader (t, k) of u is not u + k reached by k
+  // single path steps along the DFS order (step[t]: t's path predecessor is
+  // t - 1).
+  std::vector<uint32_t> irr_bits((static_cast<size_t>(N) + 31) / 32, 0u);
+  std::vector<int32_t> irr_list;
+  {
+    std::vector<uint8_t> step(N, 0);
+    for (int32_t t = 1; t < N; ++t) step[t] = W > 0 && pred[static_cast<size_t>(t) * W] == t - 1;
+    for (int32_t u = 0; u < N; ++u) {
+      bool regular = true;
+      for (int32_t e = ptr[u]; e < ptr[u + 1] && regular; ++e) {
+        const int32_t t = succ[e] >> 3, k = succ[e] & 7;
+        if (t != u + k) {
+          regular = false;
+          break;
+        }
+        for (int32_t j = 1; j <= k; ++j)
+          if (!step[u + j]) regular = false;
+      }
+      if (!regular) {
+        irr_bits[u >> 5] |= 1u << (u & 31);
+        irr_list.push_back(u);
+      }
+    }
+  }
   auto round256 = [](size_t b) { return (b + 255) / 256 * 256; };
   const size_t b_pred = round256(pred.size() * 4), b_ptr = round256(ptr.size() * 4),
-               b_succ = round256(succ.size() * 4 + 4);
+               b_succ = round256(succ.size() * 4 + 4), b_bits = round256(irr_bits.size() * 4 + 4),
+               b_irr = round256(irr_list.size() * 4 + 4);
   void* block = nullptr;
-  cudaError_t e = cudaMalloc(&block, b_pred + b_ptr + b_succ);
+  cudaError_t e = cudaMalloc(&block, b_pred + b_ptr + b_succ + b_bits + b_irr);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return fail(TREE_ERR_OOM, std::string("cudaMalloc of the conv tables: ") + cudaGetErrorString(e));
@@ -412,6 +518,11 @@ tree_status_t conv_tables_build(tree_plan* p, int K, cudaStream_t stream) {
   if (e == cudaSuccess) e = cudaMemcpyAsync(base + b_pred, ptr.data(), ptr.size() * 4, cudaMemcpyHostToDevice, stream);
   if (e == cudaSuccess && !succ.empty())
     e = cudaMemcpyAsync(base + b_pred + b_ptr, succ.data(), succ.size() * 4, cudaMemcpyHostToDevice, stream);
+  uint8_t* const p_bits = base + b_pred + b_ptr + b_succ;
+  if (e == cudaSuccess && !irr_bits.empty())
+    e = cudaMemcpyAsync(p_bits, irr_bits.data(), irr_bits.size() * 4, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess && !irr_list.empty())
+    e = cudaMemcpyAsync(p_bits + b_bits, irr_list.data(), irr_list.size() * 4, cudaMemcpyHostToDevice, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) {
     cudaFree(block);
@@ -425,6 +536,9 @@ tree_status_t conv_tables_build(tree_plan* p, int K, cudaStream_t stream) {
   p->conv.pred = reinterpret_cast<const int32_t*>(base);
   p->conv.succ_ptr = reinterpret_cast<const int32_t*>(base + b_pred);
   p->conv.succ = reinterpret_cast<const int32_t*>(base + b_pred + b_ptr);
+  p->conv.irr_bits = reinterpret_cast<const uint32_t*>(p_bits);
+  p->conv.irr_list = reinterpret_cast<const int32_t*>(p_bits + b_bits);
+  p->conv.num_irr = static_cast<int>(irr_list.size());
   return TREE_OK;
 }
 
@@ -439,7 +553,8 @@ void conv_tables_free(tree_plan* p) {
 }
 
 size_t conv_bwd_workspace(int N, int C, int K) {
-  return static_cast<size_t>(N) * C * 4 + static_cast<size_t>(kConvPartialBlocks) * (K + 1) * C * 4 + 256;
+  (void)N;
+  return static_cast<size_t>(kConvPartialBlocks) * (K + 1) * C * 4 + 256;
 }
 
 template <int K>
@@ -452,14 +567,14 @@ void conv_fwd_k(const ConvArgs& a, dim3 grid) {
 
 template <int K>
 void conv_bwd_k(const ConvArgs& a, dim3 grid, dim3 pgrid) {
+  const dim3 igrid(a.num_irr < 1024 ? (a.num_irr > 0 ? a.num_irr : 1) : 1024, grid.y);
   if (a.f32) {
-    conv_bwd_g_kernel<float, K><<<grid, kConvThreads, 0, a.stream>>>(a);
-    conv_bwd_dx_kernel<float, K><<<grid, kConvThreads, 0, a.stream>>>(a);
-    conv_bwd_dw_partial_kernel<float, K><<<pgrid, kConvThreads, 0, a.stream>>>(a);
+    conv_bwd_fused_kernel<float, K><<<pgrid, kConvThreads, 0, a.stream>>>(a);
+    if (a.num_irr > 0) conv_bwd_dx_irregular_kernel<float, K><<<igrid, kConvThreads, 0, a.stream>>>(a);
   } else {
-    conv_bwd_g_kernel<__nv_bfloat16, K><<<grid, kConvThreads, 0, a.stream>>>(a);
-    conv_bwd_dx_kernel<__nv_bfloat16, K><<<grid, kConvThreads, 0, a.stream>>>(a);
-    conv_bwd_dw_partial_kernel<__nv_bfloat16, K><<<pgrid, kConvThreads, 0, a.stream>>>(a);
+    conv_bwd_fused_kernel<__nv_bfloat16, K><<<pgrid, kConvThreads, 0, a.stream>>>(a);
+    if (a.num_irr > 0)
+      conv_bwd_dx_irregular_kernel<__nv_bfloat16, K><<<igrid, kConvThreads, 0, a.stream>>>(a);
   }
 }
 
@@ -493,7 +608,6 @@ cudaError_t launch_conv_fwd(const ConvArgs& a) {
 }
 
 cudaError_t launch_conv_bwd(ConvArgs a) {
-  a.partial = a.g + static_cast<size_t>(a.N) * a.C;
   const dim3 grid = conv_grid(a);
   const int pblocks = a.N < kConvPartialBlocks ? a.N : kConvPartialBlocks;
   const dim3 pgrid(pblocks, grid.y);

@@ -28,6 +28,9 @@ struct ConvArgs {
   const int32_t* pred;
   const int32_t* succ_ptr;
   const int32_t* succ;
+  const uint32_t* irr_bits;
+  const int32_t* irr_list;
+  int num_irr;
   const void* x;         // [N, C]
   const float* weight;   // [C, K]
   const float* bias;     // [C] or nullptr
@@ -36,8 +39,7 @@ struct ConvArgs {
   void* dx;              // backward output [N, C]
   float* dweight;        // [C, K]
   float* dbias;          // [C] or nullptr
-  float* g;              // workspace: dy * act'(pre) [N, C], then the partial sums
-  float* partial;
+  float* partial;        // workspace: per token range, the sums of dweight and dbias
   int N, C, K, act, f32;
   cudaStream_t stream;
 };

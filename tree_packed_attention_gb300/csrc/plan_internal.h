@@ -56,6 +56,12 @@ struct ConvTables {
   const int32_t* pred = nullptr;      // [N, K-1]: k-th path predecessor (k = 1..K-1), -1 before the root
   const int32_t* succ_ptr = nullptr;  // [N+1]
   const int32_t* succ = nullptr;      // (t << 3) | k for every (t, k) with pred_k(t) = u, t increasing
+  // Tokens whose readers are not all t = u + k along an unbroken run of the DFS
+  // order (the last K-1 tokens before a branch into several children): their
+  // dx is gathered over the full lists by a separate pass.
+  const uint32_t* irr_bits = nullptr;  // [ceil(N / 32)]
+  const int32_t* irr_list = nullptr;   // [num_irr]
+  int num_irr = 0;
 };
 
 }  // namespace treeattn
