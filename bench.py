@@ -659,6 +659,69 @@ def ce_arm(args):
     }))
 
 
+def gdn_arm(args):
+    """--op gdn: the Gated DeltaNet forward with tree state routing (eq. 10,
+    App. A.2) over the workload's trie, bf16 q/k/v, --gdn-heads query/key heads
+    and twice as many value heads (head_dim 128; a Qwen3-Next-shaped layer).
+    Bound by the FMA pipe: the figure is 3 * 128 * 128 fused multiply-adds per
+    token and value head (the key product, the state update, the query
+    product) over the CUDA-event time, against 152 SMs x 128 FP32 lanes x 2
+    flops x the sampled SM clock."""
+    import torch
+
+    import treegen
+    import tree_packed_attention_gb300 as tpa
+
+    torch.cuda.set_device(0)
+    w = treegen.workload(args.workload)
+    plan = tpa.tree_plan_build(w.parents, w.lengths)
+    N = plan.num_tokens
+    hk = args.gdn_heads
+    hv = 2 * hk
+    gen = torch.Generator(device="cuda").manual_seed(0)
+
+    def unit(x):
+        return x / x.norm(dim=-1, keepdim=True)
+
+    q = unit(torch.randn(N, hk, 128, device="cuda", generator=gen)).to(torch.bfloat16)
+    k = unit(torch.randn(N, hk, 128, device="cuda", generator=gen)).to(torch.bfloat16)
+    v = torch.randn(N, hv, 128, device="cuda", generator=gen).to(torch.bfloat16)
+    g = -0.5 * torch.rand(N, hv, device="cuda", generator=gen)
+    beta = torch.rand(N, hv, device="cuda", generator=gen)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        o, states = tpa.tree_gdn_fwd(plan, q, k, v, g, beta)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    with ClockSampler(0) as clocks:
+        for e in ev:
+            flush.zero_()
+            e[0].record(stream)
+            o, states = tpa.tree_gdn_fwd(plan, q, k, v, g, beta)
+            e[1].record(stream)
+        torch.cuda.synchronize()
+    tpa.tree_status_sync()
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    flops = 2.0 * 3 * 128 * 128 * N * hv
+    tf = flops / (ms * 1e-3) / 1e12
+    cs = clocks.summary()
+    mhz = cs.get("sm_mhz") or 2070.0
+    peak = 152 * 128 * 2 * mhz * 1e6 / 1e12
+    print(json.dumps({
+        "metric": "GDN forward with tree state routing, FP32 TFLOP/s on 1 GB300",
+        "value": tf, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": N, "qk_heads": hk, "v_heads": hv, "head_dim": 128,
+                   "l2": "inputs larger than L2, and L2 flushed between steps"},
+        "tokens_per_s": N / (ms * 1e-3),
+        "roofline": {"bound": "alu", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                     "peak_source": "152 SMs x 128 FP32 lanes x 2 flops x sampled SM clock", "traffic": None},
+        "clocks": cs, "gpu_launches": args.steps,
+    }))
+
+
 def partition_arm(args):
     """--op partition: the host partition planner (§3.3) on the workload at a
     token cap; no GPU. Reports the partitions, their lower bound and the peak
@@ -698,10 +761,12 @@ def main():
     ap.add_argument("--extra-workloads", default="3,4",
                     help="comma-separated workloads also timed and reported under 'workloads' "
                          "('' for none)")
-    ap.add_argument("--op", default="attention", choices=["attention", "rope", "conv", "ce", "partition"],
+    ap.add_argument("--op", default="attention", choices=["attention", "rope", "conv", "ce", "gdn", "partition"],
                     help="attention (the default and the headline), rope (tree RoPE on q and k), "
                          "conv (the tree-correct causal conv), ce (the fused weighted cross-entropy; "
-                         "workload 6 unless --workload is given) or partition (the host planner, no GPU)")
+                         "workload 6 unless --workload is given), gdn (GDN with tree state routing) "
+                         "or partition (the host planner, no GPU)")
+    ap.add_argument("--gdn-heads", type=int, default=16, help="query/key heads for --op gdn (value heads: 2x)")
     ap.add_argument("--vocab", type=int, default=151936, help="vocabulary for --op ce")
     ap.add_argument("--channels", type=int, default=4096, help="channels for --op conv")
     ap.add_argument("--cap", type=int, default=16384, help="token cap for --op partition")
@@ -710,6 +775,8 @@ def main():
         rope_arm(args)
     elif args.op == "conv":
         conv_arm(args)
+    elif args.op == "gdn":
+        gdn_arm(args)
     elif args.op == "ce":
         if "--workload" not in sys.argv:
             args.workload = 6

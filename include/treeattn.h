@@ -440,6 +440,32 @@ tree_status_t tree_weighted_ce(const tree_plan_t* plan, const void* logits, void
                                tree_dtype_t dtype, float grad_scale, float* row_loss, double* loss,
                                tree_stream_t stream);
 
+/* Gated DeltaNet forward with tree state routing ("Tree Training" §3.2 "SSM
+ * Layers (GDN)" eq. 10, App. A.2): every segment is one chunk and starts from
+ * the end state of its parent segment (a root from initial_state, or zeros),
+ * never from the segment before it in DFS order. Per value head h (query/key
+ * head h / (hv / hk)) with state S [128, 128] (key dim x value dim), token t:
+ *   S_t = exp(g_t) S_{t-1} + k_t (beta_t (v_t - exp(g_t) S_{t-1}^T k_t))^T
+ *   o_t = S_t^T q_t
+ * q and k are used as given (a GDN layer's L2 normalisation and query scale
+ * are applied by the caller).
+ *  - q, k: device [N, hk, 128]; v, o: device [N, hv, 128]; bf16 or fp32 by
+ *    dtype, token-major in the plan's DFS order, contiguous, 16-byte aligned.
+ *  - g (log decay), beta: device fp32 [N, hv].
+ *  - initial_state: device fp32 [hv, 128, 128] or NULL (zeros).
+ *  - segment_states: device fp32 [S, hv, 128, 128] out (by segment id): the
+ *    state after each segment's last token (what a child partition's gateway
+ *    carries, App. B.7); also the routing's own store of parent states.
+ *  - Arithmetic in fp32 (CUDA cores); o rounded once to its dtype.
+ * Asynchronous on `stream`; the plan must be on the current device. Errors:
+ * head_dim != 128 or hv > 65535 -> TREE_ERR_UNSUPPORTED; NULL plan or pointer,
+ * bad dtype, hv % hk != 0, misaligned pointers -> TREE_ERR_INVALID_ARG; plan
+ * not on the device -> TREE_ERR_NOT_ON_DEVICE. */
+tree_status_t tree_gdn_fwd(const tree_plan_t* plan, const void* q, const void* k, const void* v,
+                           const float* g, const float* beta, const float* initial_state, void* o,
+                           float* segment_states, int32_t hk, int32_t hv, int32_t head_dim,
+                           tree_dtype_t dtype, tree_stream_t stream);
+
 /* Wait for `stream`, then read and clear the device status word of the
  * current device: TREE_ERR_TIMEOUT if a kernel gave up a bounded wait since
  * the last check (the message names the wait: 10000 + source line in the

@@ -29,7 +29,7 @@ __all__ = [
     "tree_attn_bwd_dkdv", "tree_attn_bwd_workspace_bytes",
     "tree_weights", "tree_weights_paths", "tree_partition", "tree_rope", "tree_rope_apply",
     "TreeRopeFn", "tree_conv_fwd", "tree_conv_bwd", "tree_conv", "TreeConvFn",
-    "tree_weighted_ce", "tree_status_sync", "TreeAttnFn", "tree_attention", "TreeAttnError",
+    "tree_weighted_ce", "tree_gdn_fwd", "tree_status_sync", "TreeAttnFn", "tree_attention", "TreeAttnError",
     "FIELDS", "EXPORTS", "LIB_PATH",
 ]
 
@@ -461,6 +461,38 @@ def tree_weighted_ce(plan: Plan, logits, tokens, lam, grad_scale: float = 1.0, i
                                lam.data_ptr(), V, _dtype_code(logits), float(grad_scale),
                                row_loss.data_ptr(), loss.data_ptr(), s))
     return loss, row_loss, dlogits
+
+
+def tree_gdn_fwd(plan: Plan, q, k, v, g, beta, initial_state=None, stream=None):
+    """Gated DeltaNet forward with tree state routing (eq. 10, App. A.2); returns
+    (o [N, hv, 128], segment_states [S, hv, 128, 128] fp32, by segment id).
+
+    q, k [N, hk, 128] and v [N, hv, 128] (bf16 or fp32, one dtype), g and beta
+    [N, hv] fp32, initial_state [hv, 128, 128] fp32 or None (zeros)."""
+    import torch
+
+    N = plan.num_tokens
+    if q.dim() != 3 or q.shape[0] != N or q.shape[2] != 128:
+        raise ValueError(f"q must be [N={N}, hk, 128], got {tuple(q.shape)}")
+    hk, hv = q.shape[1], v.shape[1]
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError(f"q must be bf16 or fp32, got {q.dtype}")
+    _check_tensor("q", q, (N, hk, 128))
+    _check_tensor("k", k, (N, hk, 128), q.dtype)
+    _check_tensor("v", v, (N, hv, 128), q.dtype)
+    _check_tensor("g", g, (N, hv), torch.float32)
+    _check_tensor("beta", beta, (N, hv), torch.float32)
+    if initial_state is not None:
+        _check_tensor("initial_state", initial_state, (hv, 128, 128), torch.float32)
+    o = torch.empty_like(v)
+    S = plan.info["num_segments"]
+    states = torch.empty(S, hv, 128, 128, dtype=torch.float32, device=q.device)
+    s = _stream_ptr(stream)
+    plan.to_device(s)
+    check(lib.tree_gdn_fwd(plan.handle, q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(),
+                           beta.data_ptr(), None if initial_state is None else initial_state.data_ptr(),
+                           o.data_ptr(), states.data_ptr(), hk, hv, 128, _dtype_code(q), s))
+    return o, states
 
 
 def tree_status_sync(stream=None) -> None:

@@ -42,7 +42,7 @@ EXPORTS = [
     "tree_weights", "tree_weights_paths", "tree_partition", "tree_conv_prepare", "tree_conv_fwd",
     "tree_conv_bwd_workspace_bytes", "tree_conv_bwd", "tree_rope", "tree_status_sync",
     "tree_last_error", "tree_plan_build_partition", "tree_attn_fwd_gateway", "tree_attn_bwd_gateway",
-    "tree_weighted_ce",
+    "tree_weighted_ce", "tree_gdn_fwd",
 ]
 
 
@@ -105,6 +105,7 @@ def _load():
         "tree_attn_bwd_gateway": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
                                         i32, i32, i32, i32, C.c_float, vp, sz, vp]),
         "tree_weighted_ce": (i32, [vp, vp, vp, vp, vp, i32, i32, C.c_float, vp, vp, vp]),
+        "tree_gdn_fwd": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

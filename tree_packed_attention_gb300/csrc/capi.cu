@@ -2,6 +2,7 @@
 // the device status word.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -115,7 +116,7 @@ extern "C" tree_status_t tree_plan_to_device(tree_plan_t* p, tree_stream_t strea
       {TREE_FIELD_GT_ATOM, &d.gt_atom},     {TREE_FIELD_GT_BIDX, &d.gt_bidx},
       {TREE_FIELD_GT_BOUNDS, &d.gt_bounds}, {TREE_FIELD_GW_KEND, &d.gw_kend},
       {TREE_FIELD_GW_KT, &d.gw_kt},         {TREE_FIELD_TOKEN_SEG, &d.token_seg},
-      {TREE_FIELD_SUBTREE_END, &d.subtree_end},
+      {TREE_FIELD_SUBTREE_END, &d.subtree_end}, {TREE_FIELD_CU_SEQLENS, &d.cu_seqlens},
   };
   // key_end is padded with zeros to whole 128-key tiles: the kernels copy it
   // a tile at a time, and a zero bound hides the keys past N from every row.
@@ -131,11 +132,49 @@ extern "C" tree_status_t tree_plan_to_device(tree_plan_t* p, tree_stream_t strea
     offs[s] = total;
     total += (slot_elems(s) * 4 + 255) / 256 * 256;
   }
+  // the GDN segment table, built from the DFS layout
+  std::vector<int32_t> seg_table(static_cast<size_t>(p->S) * 4), trie_seg_ptr(static_cast<size_t>(p->R) + 1, 0);
+  {
+    const auto& order = p->field[TREE_FIELD_DFS_ORDER];
+    const auto& start = p->field[TREE_FIELD_SEG_START];
+    const auto& tseg = p->field[TREE_FIELD_TOKEN_SEG];
+    const auto& trie = p->field[TREE_FIELD_TRIE_ID];
+    const auto& ap = p->field[TREE_FIELD_ANC_PTR];
+    const auto& ai = p->field[TREE_FIELD_ANC_IDX];
+    std::vector<int32_t> len(static_cast<size_t>(p->S), 0);
+    for (int32_t t = 0; t < p->N; ++t) ++len[tseg[t]];
+    for (int32_t d = 0; d < p->S; ++d) {
+      const int32_t s = order[d];
+      seg_table[4 * d + 0] = s;
+      seg_table[4 * d + 1] = start[s];
+      seg_table[4 * d + 2] = len[s];
+      seg_table[4 * d + 3] = ap[s + 1] > ap[s] ? ai[ap[s + 1] - 1] : -1;
+      ++trie_seg_ptr[trie[s] + 1];
+    }
+    for (int32_t r = 0; r < p->R; ++r) trie_seg_ptr[r + 1] += trie_seg_ptr[r];
+  }
+  // tries by descending token count (ties by index), for the GDN launch order
+  std::vector<int32_t> trie_order(static_cast<size_t>(p->R));
+  {
+    const auto& cu = p->field[TREE_FIELD_CU_SEQLENS];
+    for (int32_t r = 0; r < p->R; ++r) trie_order[r] = r;
+    std::stable_sort(trie_order.begin(), trie_order.end(),
+                     [&](int32_t x, int32_t y) { return cu[x + 1] - cu[x] > cu[y + 1] - cu[y]; });
+  }
+  const size_t off_segs = total;
+  total += (seg_table.size() * 4 + 255) / 256 * 256;
+  const size_t off_tptr = total;
+  total += (trie_seg_ptr.size() * 4 + 255) / 256 * 256;
+  const size_t off_torder = total;
+  total += (trie_order.size() * 4 + 255) / 256 * 256;
   std::vector<uint8_t> host(total, 0);
   for (size_t s = 0; s < sizeof(slots) / sizeof(slots[0]); ++s) {
     const auto& v = p->field[slots[s].f];
     if (!v.empty()) std::memcpy(host.data() + offs[s], v.data(), v.size() * 4);
   }
+  std::memcpy(host.data() + off_segs, seg_table.data(), seg_table.size() * 4);
+  std::memcpy(host.data() + off_tptr, trie_seg_ptr.data(), trie_seg_ptr.size() * 4);
+  if (!trie_order.empty()) std::memcpy(host.data() + off_torder, trie_order.data(), trie_order.size() * 4);
   void* block = nullptr;
   e = cudaMalloc(&block, total);
   if (e != cudaSuccess) {
@@ -151,6 +190,9 @@ extern "C" tree_status_t tree_plan_to_device(tree_plan_t* p, tree_stream_t strea
   }
   for (size_t s = 0; s < sizeof(slots) / sizeof(slots[0]); ++s)
     *slots[s].dst = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(block) + offs[s]);
+  d.seg_table = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(block) + off_segs);
+  d.trie_seg_ptr = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(block) + off_tptr);
+  d.trie_order = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(block) + off_torder);
   d.block = block;
   d.bytes = total;
   d.device = cur;
@@ -275,6 +317,46 @@ extern "C" tree_status_t tree_weighted_ce(const tree_plan_t* p, const void* logi
   a.stream = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_weighted_ce(a);
   if (e != cudaSuccess) return cuda_fail(e, "tree_weighted_ce launch");
+  return TREE_OK;
+}
+
+extern "C" tree_status_t tree_gdn_fwd(const tree_plan_t* p, const void* q, const void* k, const void* v,
+                                      const float* g, const float* beta, const float* initial_state,
+                                      void* o, float* segment_states, int32_t hk, int32_t hv,
+                                      int32_t head_dim, tree_dtype_t dtype, tree_stream_t stream) {
+  if (!p) return fail(TREE_ERR_INVALID_ARG, "NULL plan");
+  if (dtype != TREE_DTYPE_BF16 && dtype != TREE_DTYPE_F32) return fail(TREE_ERR_INVALID_ARG, "unknown dtype");
+  if (hk <= 0 || hv <= 0 || hv % hk != 0) return fail(TREE_ERR_INVALID_ARG, "need hk > 0, hv > 0 and hv % hk == 0");
+  if (hv > 65535) return fail(TREE_ERR_UNSUPPORTED, "hv > 65535");
+  if (head_dim != 128) return fail(TREE_ERR_UNSUPPORTED, "GDN head_dim must be 128");
+  if (p->N == 0) return TREE_OK;
+  if (!q || !k || !v || !g || !beta || !o || !segment_states) return fail(TREE_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(segment_states) ||
+      (initial_state && !aligned16(initial_state)))
+    return fail(TREE_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  tree_status_t st = check_plan_on_device(p);
+  if (st != TREE_OK) return st;
+  GdnArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.g = g;
+  a.beta = beta;
+  a.s0 = initial_state;
+  a.o = o;
+  a.states = segment_states;
+  a.segs = reinterpret_cast<const int4*>(p->dev.seg_table);
+  a.trie_ptr = p->dev.trie_seg_ptr;
+  a.cu = p->dev.cu_seqlens;
+  a.trie_order = p->dev.trie_order;
+  a.R = p->R;
+  a.hk = hk;
+  a.hv = hv;
+  a.group = hv / hk;
+  a.f32 = dtype == TREE_DTYPE_F32 ? 1 : 0;
+  a.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_gdn_fwd(a);
+  if (e != cudaSuccess) return cuda_fail(e, "tree_gdn_fwd launch");
   return TREE_OK;
 }
 

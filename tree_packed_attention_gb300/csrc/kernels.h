@@ -66,6 +66,24 @@ struct CeArgs {
   cudaStream_t stream;
 };
 cudaError_t launch_weighted_ce(const CeArgs& a);
+// Gated DeltaNet forward with tree state routing (gdn.cu).
+struct GdnArgs {
+  const void* q;       // [N, hk, 128]
+  const void* k;       // [N, hk, 128]
+  const void* v;       // [N, hv, 128]
+  const float* g;      // [N, hv] log decay
+  const float* beta;   // [N, hv]
+  const float* s0;     // [hv, 128, 128] or nullptr (zeros)
+  void* o;             // [N, hv, 128]
+  float* states;       // [S, hv, 128, 128]: each segment's end state
+  const int4* segs;    // per DFS position: (segment id, first token, length, parent id)
+  const int32_t* trie_ptr;  // [R+1] DFS positions of each trie
+  const int32_t* cu;        // [R+1] token range of each trie
+  const int32_t* trie_order;  // [R] tries by descending token count
+  int R, hk, hv, group, f32;
+  cudaStream_t stream;
+};
+cudaError_t launch_gdn_fwd(const GdnArgs& a);
 struct AttnArgs {
   const tree_plan* plan;
   const void* q;

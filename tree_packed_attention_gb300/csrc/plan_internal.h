@@ -45,6 +45,12 @@ struct DevicePlan {
   const int32_t* gw_kt = nullptr;      // [gateway key tiles with a visible key]
   const int32_t* token_seg = nullptr;  // [N]
   const int32_t* subtree_end = nullptr;  // [S]
+  const int32_t* cu_seqlens = nullptr;   // [R+1]
+  // GDN state routing: per DFS position (segment, first token, length,
+  // parent or -1) as int4, and the DFS positions of each trie [R+1]
+  const int32_t* seg_table = nullptr;
+  const int32_t* trie_seg_ptr = nullptr;
+  const int32_t* trie_order = nullptr;  // [R] tries by descending token count
 };
 
 // Tables of the tree-correct causal conv for one kernel size (conv.cu): the

@@ -221,3 +221,31 @@ def draw_tensors(n_tokens: int, hq: int, hkv: int, head_dim: int, dtype: str = "
         return q, k, v
     do = torch.randn(n_tokens, hq, head_dim, generator=g, dtype=torch.float32).to(tdt)
     return q, k, v, do
+
+
+def draw_gdn(n_tokens: int, hk: int, hv: int, head_dim: int = 128, dtype: str = "bf16", seed: int = 0,
+             with_state: bool = True):
+    """Inputs of a Gated DeltaNet layer, as its kernel receives them.
+
+    From one seeded CPU generator, in this order: q, k [N, hk, D] drawn N(0,1)
+    and scaled to unit L2 norm per head (the layer normalises them), v
+    [N, hv, D] N(0,1), g [N, hv] = -U(0, 0.5) (log decays, per-token decay
+    exp(g) in (0.6, 1]), beta [N, hv] U(0, 1), and the initial state
+    [hv, D, D] N(0, 0.3^2). q, k, v are rounded to ``dtype``; g, beta and the
+    state stay fp32.
+    """
+    import torch
+
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    tdt = {"bf16": torch.bfloat16, "fp32": torch.float32}[dtype]
+
+    def unit(x):
+        return x / x.norm(dim=-1, keepdim=True)
+
+    q = unit(torch.randn(n_tokens, hk, head_dim, generator=g)).to(tdt)
+    k = unit(torch.randn(n_tokens, hk, head_dim, generator=g)).to(tdt)
+    v = torch.randn(n_tokens, hv, head_dim, generator=g).to(tdt)
+    lg = -0.5 * torch.rand(n_tokens, hv, generator=g)
+    beta = torch.rand(n_tokens, hv, generator=g)
+    s0 = 0.3 * torch.randn(hv, head_dim, head_dim, generator=g) if with_state else None
+    return q, k, v, lg, beta, s0
