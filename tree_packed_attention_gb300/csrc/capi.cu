@@ -422,6 +422,7 @@ ConvArgs conv_args(const tree_plan_t* p, const void* x, const float* weight, con
   a.act = activation;
   a.f32 = dtype == TREE_DTYPE_F32 ? 1 : 0;
   a.stream = static_cast<cudaStream_t>(stream);
+  a.status = status_ptr();
   return a;
 }
 

@@ -27,11 +27,20 @@
 #include <vector>
 
 #include "kernels.h"
+#include "sm103_ptx.cuh"
 
 namespace treeattn {
 namespace {
 
+using namespace dev;
+
 constexpr int kConvThreads = 256;
+// The forward and the backward stage the rows they stream (x; x and dy) through
+// shared memory with bulk copies: a block's slice of a row (its 2048 channels)
+// per token, kConvBatchBytes per tensor and batch, kConvBufs batches in flight.
+constexpr uint32_t kConvBatchBytes = 16 * 1024;
+constexpr int kConvBufs = 3;
+constexpr int kSiteConv = 40000;  // status word of a conv wait that gave up: 40000 + line
 constexpr int kConvPartialBlocks = 512;  // token ranges of the backward (and its dweight / dbias sums)
 
 template <typename T>
@@ -70,40 +79,12 @@ struct Vec8<float> {
   }
 };
 
-// A chunk of 8 channels held raw (4 registers for bf16) while its load is in
-// flight, widened to fp32 when used.
-template <typename T>
-struct RawChunk;
-template <>
-struct RawChunk<__nv_bfloat16> {
-  uint4 u;
-  __device__ __forceinline__ void load(const __nv_bfloat16* p) { u = *reinterpret_cast<const uint4*>(p); }
-  __device__ __forceinline__ void widen(float (&v)[8]) const {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));
-      v[2 * j] = f.x;
-      v[2 * j + 1] = f.y;
-    }
-  }
-};
-template <>
-struct RawChunk<float> {
-  float4 a, b;
-  __device__ __forceinline__ void load(const float* p) {
-    a = reinterpret_cast<const float4*>(p)[0];
-    b = reinterpret_cast<const float4*>(p)[1];
-  }
-  __device__ __forceinline__ void widen(float (&v)[8]) const {
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-  }
-};
-
-// SiLU and its derivative, from expf (a library call).
-__device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
+// SiLU and its derivative, from the fast exponential and division intrinsics
+// (relative error near 1e-7: within the fp32 tolerance of the outputs).
+__device__ __forceinline__ float sigmoid(float z) { return __fdividef(1.f, 1.f + __expf(-z)); }
+__device__ __forceinline__ float silu(float z) { return z * sigmoid(z); }
 __device__ __forceinline__ float silu_grad(float z) {
-  const float s = 1.f / (1.f + expf(-z));
+  const float s = sigmoid(z);
   return s * (1.f + z * (1.f - s));
 }
 
@@ -176,69 +157,104 @@ __device__ __forceinline__ void token_range(const ConvArgs& a, int& t0, int& t1)
   t1 = min(a.N, t0 + per);
 }
 
-// walks [t0, t1) calling f(t, window) with the window of token t; rows and
-// immediate predecessors of the next kConvAhead tokens are kept in flight
-constexpr int kConvAhead = 4;
-
-template <typename T, int K, typename F>
-__device__ __forceinline__ void walk(const ConvArgs& a, int q, int t0, int t1, F&& f) {
-  if (t0 >= t1) return;
-  const T* x = static_cast<const T*>(a.x);
-  RawChunk<T> ring[kConvAhead];
-  int pr[kConvAhead];
+// Bulk-copy staging of NT token-major tensors for one block: batch i (tokens
+// tb .. tb+n-1) of tensor s sits at buf + (i % kConvBufs) * NT * kConvBatchBytes
+// + s * kConvBatchBytes, token u of the batch at u * (row stride).
+template <typename T, int NT>
+struct Stage {
+  static constexpr uint32_t kStride = kConvThreads * 8 * sizeof(T);  // smem bytes per token row
+  static constexpr int kBatch = static_cast<int>(kConvBatchBytes / kStride);
+  uint8_t* buf;
+  uint64_t* bar;       // [kConvBufs]
+  const T* src[NT];
+  int C, g0;           // channels; the group's first channel
+  uint32_t row_bytes;  // bytes of a token's slice (the group's channels)
+  int t0, te;          // tokens staged: [t0, te)
+  __device__ int batches() const { return (te - t0 + kBatch - 1) / kBatch; }
+  // issued by one thread
+  __device__ void issue(int i) const {
+    const int s = i % kConvBufs, tb = t0 + i * kBatch, n = min(kBatch, te - tb);
+    uint64_t* b = bar + s;
+    mbar_arrive_expect_tx(b, static_cast<uint32_t>(n) * row_bytes * NT);
+    for (int u = 0; u < n; ++u)
 #pragma unroll
-  for (int d = 0; d < kConvAhead; ++d) {
-    const int t = t0 + d;
-    pr[d] = -1;
-    if (t < t1) {
-      ring[d].load(x + static_cast<size_t>(t) * a.C + 8 * q);
-      pr[d] = K > 1 ? pred_of<K>(a, t, 1) : t - 1;
-    }
+      for (int k = 0; k < NT; ++k)
+        bulk_load(buf + (s * NT + k) * kConvBatchBytes + u * kStride,
+                  src[k] + static_cast<size_t>(tb + u) * C + g0, row_bytes, b);
   }
-  Window<T, K> win;
-  for (int tb = t0; tb < t1; tb += kConvAhead) {
-#pragma unroll
-    for (int d = 0; d < kConvAhead; ++d) {
-      const int t = tb + d;
-      if (t >= t1) break;
-      float xt[8];
-      ring[d].widen(xt);
-      const int p1 = pr[d];
-      const int tn = t + kConvAhead;  // refill this slot with a later token
-      if (tn < t1) {
-        ring[d].load(x + static_cast<size_t>(tn) * a.C + 8 * q);
-        pr[d] = K > 1 ? pred_of<K>(a, tn, 1) : tn - 1;
-      }
-      if (t > t0 && p1 == t - 1)
-        win.shift(xt);
-      else
-        win.reload(a, t, q, xt);
-      f(t, win);
-    }
+  __device__ const uint8_t* row(int i, int k, int u) const {
+    return buf + ((i % kConvBufs) * NT + k) * kConvBatchBytes + u * kStride;
   }
-}
+};
 
 template <typename T, int K>
 __global__ void __launch_bounds__(kConvThreads) conv_fwd_kernel(const ConvArgs a) {
+  extern __shared__ __align__(128) uint8_t cbuf[];
+  __shared__ uint64_t bar[kConvBufs];
+  __shared__ int abort_s;
   const int q = blockIdx.y * kConvThreads + threadIdx.x;
-  if (q >= a.C / 8) return;
+  const bool valid = q < a.C / 8;
+  Stage<T, 1> st;
+  st.buf = cbuf;
+  st.bar = bar;
+  st.src[0] = static_cast<const T*>(a.x);
+  st.C = a.C;
+  st.g0 = blockIdx.y * kConvThreads * 8;
+  st.row_bytes = static_cast<uint32_t>(min(kConvThreads * 8, a.C - st.g0) * sizeof(T));
+  token_range(a, st.t0, st.te);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kConvBufs; ++i) mbar_init(&bar[i], 1);
+    abort_s = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int nb = st.t0 < st.te ? st.batches() : 0;
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kConvBufs && i < nb; ++i) st.issue(i);
   Taps<K> tp;
-  tp.load(a.weight, q);
   float b[8];
+  if (valid) {
+    tp.load(a.weight, q);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) b[j] = a.bias ? __ldg(a.bias + 8 * q + j) : 0.f;
+    for (int j = 0; j < 8; ++j) b[j] = a.bias ? __ldg(a.bias + 8 * q + j) : 0.f;
+  }
   T* y = static_cast<T*>(a.y);
-  int t0, t1;
-  token_range(a, t0, t1);
-  walk<T, K>(a, q, t0, t1, [&](int t, const Window<T, K>& win) {
-    float z[8];
-    win.pre(tp, b, z);
-    if (a.act == 1) {
+  Window<T, K> win;
+  constexpr int B = Stage<T, 1>::kBatch;
+  int i = 0;
+  for (; i < nb; ++i) {
+    const int tb = st.t0 + i * B, n = min(B, st.te - tb);
+    int p1[B];  // the batch's immediate path predecessors
 #pragma unroll
-      for (int j = 0; j < 8; ++j) z[j] = silu(z[j]);
+    for (int u = 0; u < B; ++u) p1[u] = u < n ? (K > 1 ? pred_of<K>(a, tb + u, 1) : tb + u - 1) : -1;
+    const bool ok = mbar_wait(&bar[i % kConvBufs], (i / kConvBufs) & 1, &abort_s, a.status,
+                              kSiteConv + __LINE__);
+    if (!__syncthreads_and(ok)) break;
+    if (valid) {
+#pragma unroll
+      for (int u = 0; u < B; ++u) {
+        if (u >= n) break;
+        const int t = tb + u;
+        float xt[8];
+        Vec8<T>::load(reinterpret_cast<const T*>(st.row(i, 0, u)) + 8 * threadIdx.x, xt);
+        if (t > st.t0 && p1[u] == t - 1)
+          win.shift(xt);
+        else
+          win.reload(a, t, q, xt);
+        float z[8];
+        win.pre(tp, b, z);
+        if (a.act == 1) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) z[j] = silu(z[j]);
+        }
+        Vec8<T>::store(y + static_cast<size_t>(t) * a.C + 8 * q, z);
+      }
     }
-    Vec8<T>::store(y + static_cast<size_t>(t) * a.C + 8 * q, z);
-  });
+    __syncthreads();  // every thread is done with this batch's buffer
+    if (threadIdx.x == 0 && i + kConvBufs < nb) st.issue(i + kConvBufs);
+  }
+  if (i < nb && threadIdx.x == 0)  // gave up a wait: let the copies in flight land
+    for (int k = i; k < nb && k < i + kConvBufs; ++k) mbar_drain(&bar[k % kConvBufs], (k / kConvBufs) & 1);
 }
 
 // The backward in one pass over each block's token range, in DFS order:
@@ -255,63 +271,79 @@ __global__ void __launch_bounds__(kConvThreads) conv_fwd_kernel(const ConvArgs a
 //   registers.
 template <typename T, int K>
 __global__ void __launch_bounds__(kConvThreads) conv_bwd_fused_kernel(const ConvArgs a) {
+  extern __shared__ __align__(128) uint8_t cbuf[];
+  __shared__ uint64_t bar[kConvBufs];
+  __shared__ int abort_s;
   const int q = blockIdx.y * kConvThreads + threadIdx.x;
-  if (q >= a.C / 8) return;
-  Taps<K> tp;
-  tp.load(a.weight, q);
-  float b[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) b[j] = a.bias ? __ldg(a.bias + 8 * q + j) : 0.f;
-  const T* x = static_cast<const T*>(a.x);
-  const T* dy = static_cast<const T*>(a.dy);
-  T* dx = static_cast<T*>(a.dx);
+  const bool valid = q < a.C / 8;
   int t0, t1;
   token_range(a, t0, t1);
+  Stage<T, 2> st;
+  st.buf = cbuf;
+  st.bar = bar;
+  st.src[0] = static_cast<const T*>(a.x);
+  st.src[1] = static_cast<const T*>(a.dy);
+  st.C = a.C;
+  st.g0 = blockIdx.y * kConvThreads * 8;
+  st.row_bytes = static_cast<uint32_t>(min(kConvThreads * 8, a.C - st.g0) * sizeof(T));
+  st.t0 = t0;
+  st.te = t0 < t1 ? min(a.N, t1 + K - 1) : t0;  // K-1 tokens past the range: their g
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kConvBufs; ++i) mbar_init(&bar[i], 1);
+    abort_s = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int nb = st.t0 < st.te ? st.batches() : 0;
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kConvBufs && i < nb; ++i) st.issue(i);
+  Taps<K> tp;
+  float b[8];
+  if (valid) {
+    tp.load(a.weight, q);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) b[j] = a.bias ? __ldg(a.bias + 8 * q + j) : 0.f;
+  }
+  T* dx = static_cast<T*>(a.dx);
   float acc[K + 1][8];
 #pragma unroll
   for (int k = 0; k <= K; ++k)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[k][j] = 0.f;
-  if (t0 < t1) {
-    const int te = min(a.N, t1 + K - 1);  // the last real token walked, plus one
-    float gh[K][8];                       // gh[k] = g of the token k steps back in DFS order
+  float gh[K][8];  // gh[k] = g of the token k steps back in DFS order
 #pragma unroll
-    for (int k = 0; k < K; ++k)
+  for (int k = 0; k < K; ++k)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) gh[k][j] = 0.f;
-    uint32_t cont = 0;  // bit k: the token k steps back follows its DFS predecessor on its path
-    RawChunk<T> rx[kConvAhead], rd[kConvAhead];
-    int pr[kConvAhead];
+    for (int j = 0; j < 8; ++j) gh[k][j] = 0.f;
+  uint32_t cont = 0;  // bit k: the token k steps back follows its DFS predecessor on its path
+  Window<T, K> win;
+  constexpr int B = Stage<T, 2>::kBatch;
+  const int tend = t0 < t1 ? t1 + K - 1 : t0;  // walk end, virtual tokens past N included
+  const int nsteps = (tend - t0 + B - 1) / B;  // batches of the walk (the last ones may be virtual)
+  int i = 0;
+  bool ok = true;
+  for (; i < nsteps; ++i) {
+    const int tb = t0 + i * B;
+    const int n = i < nb ? min(B, st.te - tb) : 0;  // real tokens of this batch
+    int p1[B];
 #pragma unroll
-    for (int d = 0; d < kConvAhead; ++d) {
-      const int t = t0 + d;
-      pr[d] = -1;
-      if (t < te) {
-        rx[d].load(x + static_cast<size_t>(t) * a.C + 8 * q);
-        rd[d].load(dy + static_cast<size_t>(t) * a.C + 8 * q);
-        pr[d] = K > 1 ? pred_of<K>(a, t, 1) : t - 1;
-      }
+    for (int u = 0; u < B; ++u) p1[u] = u < n ? (K > 1 ? pred_of<K>(a, tb + u, 1) : tb + u - 1) : -1;
+    if (i < nb) {
+      ok = mbar_wait(&bar[i % kConvBufs], (i / kConvBufs) & 1, &abort_s, a.status, kSiteConv + __LINE__);
+      if (!__syncthreads_and(ok)) break;
     }
-    Window<T, K> win;
-    for (int tb = t0; tb < t1 + K - 1; tb += kConvAhead) {
+    if (valid) {
 #pragma unroll
-      for (int d = 0; d < kConvAhead; ++d) {
-        const int t = tb + d;
-        if (t >= t1 + K - 1) break;
+      for (int u = 0; u < B; ++u) {
+        const int t = tb + u;
+        if (t >= tend) break;
         float g[8];
         bool step = false;
-        if (t < te) {
+        if (u < n) {
           float xt[8];
-          rx[d].widen(xt);
-          rd[d].widen(g);
-          const int p1 = pr[d];
-          const int tn = t + kConvAhead;
-          if (tn < te) {
-            rx[d].load(x + static_cast<size_t>(tn) * a.C + 8 * q);
-            rd[d].load(dy + static_cast<size_t>(tn) * a.C + 8 * q);
-            pr[d] = K > 1 ? pred_of<K>(a, tn, 1) : tn - 1;
-          }
-          step = p1 == t - 1;
+          Vec8<T>::load(reinterpret_cast<const T*>(st.row(i, 0, u)) + 8 * threadIdx.x, xt);
+          Vec8<T>::load(reinterpret_cast<const T*>(st.row(i, 1, u)) + 8 * threadIdx.x, g);
+          step = p1[u] == t - 1;
           if (t > t0 && step)
             win.shift(xt);
           else
@@ -341,31 +373,39 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_fused_kernel(const Conv
 #pragma unroll
         for (int j = 0; j < 8; ++j) gh[0][j] = g[j];
         cont = (cont << 1) | (step ? 1u : 0u);
-        // token u = t - (K-1) now has all of its run readers u .. t
-        const int u = t - (K - 1);
-        if (u >= t0 && u < a.N && !(__ldg(a.irr_bits + (u >> 5)) >> (u & 31) & 1u)) {
+        // token u0 = t - (K-1) now has all of its run readers u0 .. t
+        const int u0 = t - (K - 1);
+        if (u0 >= t0 && u0 < a.N && !(__ldg(a.irr_bits + (u0 >> 5)) >> (u0 & 31) & 1u)) {
           float o[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) o[j] = tp.w[j][K - 1] * gh[K - 1][j];  // k = 0: u itself
+          for (int j = 0; j < 8; ++j) o[j] = tp.w[j][K - 1] * gh[K - 1][j];  // k = 0: u0 itself
           bool run = true;
 #pragma unroll
           for (int k = 1; k < K; ++k) {
-            run = run && ((cont >> (K - 1 - k)) & 1u);  // u + k follows u + k - 1
+            run = run && ((cont >> (K - 1 - k)) & 1u);  // u0 + k follows u0 + k - 1
             if (run) {
 #pragma unroll
               for (int j = 0; j < 8; ++j) o[j] = fmaf(tp.w[j][K - 1 - k], gh[K - 1 - k][j], o[j]);
             }
           }
-          Vec8<T>::store(dx + static_cast<size_t>(u) * a.C + 8 * q, o);
+          Vec8<T>::store(dx + static_cast<size_t>(u0) * a.C + 8 * q, o);
         }
       }
     }
+    if (i < nb) {
+      __syncthreads();  // every thread is done with this batch's buffer
+      if (threadIdx.x == 0 && i + kConvBufs < nb) st.issue(i + kConvBufs);
+    }
   }
-  float* part = a.partial + static_cast<size_t>(blockIdx.x) * (K + 1) * a.C;
+  if (!ok && threadIdx.x == 0)  // gave up a wait: let the copies in flight land
+    for (int k = i; k < nb && k < i + kConvBufs; ++k) mbar_drain(&bar[k % kConvBufs], (k / kConvBufs) & 1);
+  if (valid) {
+    float* part = a.partial + static_cast<size_t>(blockIdx.x) * (K + 1) * a.C;
 #pragma unroll
-  for (int k = 0; k <= K; ++k)
+    for (int k = 0; k <= K; ++k)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) part[static_cast<size_t>(k) * a.C + 8 * q + j] = acc[k][j];
+      for (int j = 0; j < 8; ++j) part[static_cast<size_t>(k) * a.C + 8 * q + j] = acc[k][j];
+  }
 }
 
 // dx of the irregular tokens: the gather over every (t, k) with pred_k(t) = u
@@ -557,71 +597,98 @@ size_t conv_bwd_workspace(int N, int C, int K) {
   return static_cast<size_t>(kConvPartialBlocks) * (K + 1) * C * 4 + 256;
 }
 
+// dynamic shared memory of the staged kernels, set once per instantiation
+template <typename F>
+cudaError_t smem_attr(F* kernel, uint32_t bytes, bool& done) {
+  if (done) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done = true;
+  return e;
+}
+
+constexpr uint32_t kFwdSmem = kConvBufs * kConvBatchBytes;      // x
+constexpr uint32_t kBwdSmem = kConvBufs * 2 * kConvBatchBytes;  // x and dy
+
 template <int K>
-void conv_fwd_k(const ConvArgs& a, dim3 grid) {
-  if (a.f32)
-    conv_fwd_kernel<float, K><<<grid, kConvThreads, 0, a.stream>>>(a);
-  else
-    conv_fwd_kernel<__nv_bfloat16, K><<<grid, kConvThreads, 0, a.stream>>>(a);
+cudaError_t conv_fwd_k(const ConvArgs& a, dim3 grid) {
+  static bool done[2] = {false, false};
+  cudaError_t e;
+  if (a.f32) {
+    if ((e = smem_attr(conv_fwd_kernel<float, K>, kFwdSmem, done[1])) != cudaSuccess) return e;
+    conv_fwd_kernel<float, K><<<grid, kConvThreads, kFwdSmem, a.stream>>>(a);
+  } else {
+    if ((e = smem_attr(conv_fwd_kernel<__nv_bfloat16, K>, kFwdSmem, done[0])) != cudaSuccess) return e;
+    conv_fwd_kernel<__nv_bfloat16, K><<<grid, kConvThreads, kFwdSmem, a.stream>>>(a);
+  }
+  return cudaGetLastError();
 }
 
 template <int K>
-void conv_bwd_k(const ConvArgs& a, dim3 grid, dim3 pgrid) {
+cudaError_t conv_bwd_k(const ConvArgs& a, dim3 grid, dim3 pgrid) {
+  static bool done[2] = {false, false};
   const dim3 igrid(a.num_irr < 1024 ? (a.num_irr > 0 ? a.num_irr : 1) : 1024, grid.y);
+  cudaError_t e;
   if (a.f32) {
-    conv_bwd_fused_kernel<float, K><<<pgrid, kConvThreads, 0, a.stream>>>(a);
+    if ((e = smem_attr(conv_bwd_fused_kernel<float, K>, kBwdSmem, done[1])) != cudaSuccess) return e;
+    conv_bwd_fused_kernel<float, K><<<pgrid, kConvThreads, kBwdSmem, a.stream>>>(a);
     if (a.num_irr > 0) conv_bwd_dx_irregular_kernel<float, K><<<igrid, kConvThreads, 0, a.stream>>>(a);
   } else {
-    conv_bwd_fused_kernel<__nv_bfloat16, K><<<pgrid, kConvThreads, 0, a.stream>>>(a);
+    if ((e = smem_attr(conv_bwd_fused_kernel<__nv_bfloat16, K>, kBwdSmem, done[0])) != cudaSuccess) return e;
+    conv_bwd_fused_kernel<__nv_bfloat16, K><<<pgrid, kConvThreads, kBwdSmem, a.stream>>>(a);
     if (a.num_irr > 0)
       conv_bwd_dx_irregular_kernel<__nv_bfloat16, K><<<igrid, kConvThreads, 0, a.stream>>>(a);
   }
+  return cudaGetLastError();
 }
 
-// blocks: groups of 256 channel chunks (y) times token strides (x), about
-// eight blocks per SM in all
-dim3 conv_grid(const ConvArgs& a) {
+// blocks: groups of 256 channel chunks (y) times token ranges (x), `per_sm`
+// blocks per SM in all (the forward keeps two 256-thread blocks per SM, the
+// backward one: its walk holds about 190 registers a thread)
+dim3 conv_grid(const ConvArgs& a, int per_sm) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 1;
   const int groups = (a.C / 8 + kConvThreads - 1) / kConvThreads;
-  int tx = sms * 8 / groups;
+  int tx = sms * per_sm / groups;
   tx = tx < 1 ? 1 : (tx > a.N ? a.N : tx);
   return dim3(tx, groups);
 }
 
 cudaError_t launch_conv_fwd(const ConvArgs& a) {
-  const dim3 grid = conv_grid(a);
+  const dim3 grid = conv_grid(a, 2);
   switch (a.K) {
-    case 1: conv_fwd_k<1>(a, grid); break;
-    case 2: conv_fwd_k<2>(a, grid); break;
-    case 3: conv_fwd_k<3>(a, grid); break;
-    case 4: conv_fwd_k<4>(a, grid); break;
-    case 5: conv_fwd_k<5>(a, grid); break;
-    case 6: conv_fwd_k<6>(a, grid); break;
-    case 7: conv_fwd_k<7>(a, grid); break;
-    case 8: conv_fwd_k<8>(a, grid); break;
+    case 1: return conv_fwd_k<1>(a, grid);
+    case 2: return conv_fwd_k<2>(a, grid);
+    case 3: return conv_fwd_k<3>(a, grid);
+    case 4: return conv_fwd_k<4>(a, grid);
+    case 5: return conv_fwd_k<5>(a, grid);
+    case 6: return conv_fwd_k<6>(a, grid);
+    case 7: return conv_fwd_k<7>(a, grid);
+    case 8: return conv_fwd_k<8>(a, grid);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_conv_bwd(ConvArgs a) {
-  const dim3 grid = conv_grid(a);
-  const int pblocks = a.N < kConvPartialBlocks ? a.N : kConvPartialBlocks;
-  const dim3 pgrid(pblocks, grid.y);
+  const dim3 grid = conv_grid(a, 8);  // the irregular tokens' gather
+  const dim3 pgrid = conv_grid(a, 1);
+  const int pblocks = static_cast<int>(pgrid.x) < kConvPartialBlocks ? static_cast<int>(pgrid.x)
+                                                                     : kConvPartialBlocks;
+  const dim3 pg(pblocks, pgrid.y);
+  cudaError_t e;
   switch (a.K) {
-    case 1: conv_bwd_k<1>(a, grid, pgrid); break;
-    case 2: conv_bwd_k<2>(a, grid, pgrid); break;
-    case 3: conv_bwd_k<3>(a, grid, pgrid); break;
-    case 4: conv_bwd_k<4>(a, grid, pgrid); break;
-    case 5: conv_bwd_k<5>(a, grid, pgrid); break;
-    case 6: conv_bwd_k<6>(a, grid, pgrid); break;
-    case 7: conv_bwd_k<7>(a, grid, pgrid); break;
-    case 8: conv_bwd_k<8>(a, grid, pgrid); break;
+    case 1: e = conv_bwd_k<1>(a, grid, pg); break;
+    case 2: e = conv_bwd_k<2>(a, grid, pg); break;
+    case 3: e = conv_bwd_k<3>(a, grid, pg); break;
+    case 4: e = conv_bwd_k<4>(a, grid, pg); break;
+    case 5: e = conv_bwd_k<5>(a, grid, pg); break;
+    case 6: e = conv_bwd_k<6>(a, grid, pg); break;
+    case 7: e = conv_bwd_k<7>(a, grid, pg); break;
+    case 8: e = conv_bwd_k<8>(a, grid, pg); break;
     default: return cudaErrorInvalidValue;
   }
+  if (e != cudaSuccess) return e;
   const int total = (a.K + 1) * a.C;
   const int rblocks = (total + kConvThreads - 1) / kConvThreads;
   conv_bwd_dw_reduce_kernel<<<rblocks, kConvThreads, 0, a.stream>>>(a, pblocks);

@@ -40,6 +40,7 @@ struct ConvArgs {
   float* dweight;        // [C, K]
   float* dbias;          // [C] or nullptr
   float* partial;        // workspace: per token range, the sums of dweight and dbias
+  int* status;           // device status word (a bounded wait that gives up)
   int N, C, K, act, f32;
   cudaStream_t stream;
 };
