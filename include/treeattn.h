@@ -470,8 +470,9 @@ tree_status_t tree_gdn_fwd(const tree_plan_t* plan, const void* q, const void* k
  * current device: TREE_ERR_TIMEOUT if a kernel gave up a bounded wait since
  * the last check (the message names the wait: 10000 + source line in the
  * forward kernel file, 20000 + line in the backward one, 30000 + warp for
- * the work ring), TREE_ERR_INVALID_ARG if tree_weighted_ce met a token id >=
- * vocab, TREE_ERR_CUDA on a CUDA error, else TREE_OK. */
+ * the work ring, 40000 + line in the conv kernel file), TREE_ERR_INVALID_ARG
+ * if tree_weighted_ce met a token id >= vocab, TREE_ERR_CUDA on a CUDA error,
+ * else TREE_OK. */
 tree_status_t tree_status_sync(tree_stream_t stream);
 
 /* Message for the last failing call on this thread ("" if none). */

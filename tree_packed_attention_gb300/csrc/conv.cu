@@ -140,13 +140,22 @@ struct Window {
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[0][j] = xt[j];
   }
+  // the pre-activation, channels in packed pairs
   __device__ __forceinline__ void pre(const Taps<K>& tp, const float (&b)[8], float (&z)[8]) const {
+    float2 z2[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) z[j] = b[j];
+    for (int jp = 0; jp < 4; ++jp) z2[jp] = make_float2(b[2 * jp], b[2 * jp + 1]);
 #pragma unroll
     for (int k = 0; k < K; ++k)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) z[j] = fmaf(tp.w[j][K - 1 - k], v[k][j], z[j]);
+      for (int jp = 0; jp < 4; ++jp)
+        z2[jp] = __ffma2_rn(make_float2(tp.w[2 * jp][K - 1 - k], tp.w[2 * jp + 1][K - 1 - k]),
+                            make_float2(v[k][2 * jp], v[k][2 * jp + 1]), z2[jp]);
+#pragma unroll
+    for (int jp = 0; jp < 4; ++jp) {
+      z[2 * jp] = z2[jp].x;
+      z[2 * jp + 1] = z2[jp].y;
+    }
   }
 };
 
@@ -358,7 +367,13 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_fused_kernel(const Conv
 #pragma unroll
             for (int k = 0; k < K; ++k)
 #pragma unroll
-              for (int j = 0; j < 8; ++j) acc[k][j] = fmaf(g[j], win.v[k][j], acc[k][j]);
+              for (int jp = 0; jp < 4; ++jp) {
+                const float2 r2 = __ffma2_rn(make_float2(g[2 * jp], g[2 * jp + 1]),
+                                             make_float2(win.v[k][2 * jp], win.v[k][2 * jp + 1]),
+                                             make_float2(acc[k][2 * jp], acc[k][2 * jp + 1]));
+                acc[k][2 * jp] = r2.x;
+                acc[k][2 * jp + 1] = r2.y;
+              }
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[K][j] += g[j];
           }
@@ -376,17 +391,27 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_fused_kernel(const Conv
         // token u0 = t - (K-1) now has all of its run readers u0 .. t
         const int u0 = t - (K - 1);
         if (u0 >= t0 && u0 < a.N && !(__ldg(a.irr_bits + (u0 >> 5)) >> (u0 & 31) & 1u)) {
-          float o[8];
+          float2 o2[4];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) o[j] = tp.w[j][K - 1] * gh[K - 1][j];  // k = 0: u0 itself
+          for (int jp = 0; jp < 4; ++jp)  // k = 0: u0 itself
+            o2[jp] = __fmul2_rn(make_float2(tp.w[2 * jp][K - 1], tp.w[2 * jp + 1][K - 1]),
+                                make_float2(gh[K - 1][2 * jp], gh[K - 1][2 * jp + 1]));
           bool run = true;
 #pragma unroll
           for (int k = 1; k < K; ++k) {
             run = run && ((cont >> (K - 1 - k)) & 1u);  // u0 + k follows u0 + k - 1
             if (run) {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) o[j] = fmaf(tp.w[j][K - 1 - k], gh[K - 1 - k][j], o[j]);
+              for (int jp = 0; jp < 4; ++jp)
+                o2[jp] = __ffma2_rn(make_float2(tp.w[2 * jp][K - 1 - k], tp.w[2 * jp + 1][K - 1 - k]),
+                                    make_float2(gh[K - 1 - k][2 * jp], gh[K - 1 - k][2 * jp + 1]), o2[jp]);
             }
+          }
+          float o[8];
+#pragma unroll
+          for (int jp = 0; jp < 4; ++jp) {
+            o[2 * jp] = o2[jp].x;
+            o[2 * jp + 1] = o2[jp].y;
           }
           Vec8<T>::store(dx + static_cast<size_t>(u0) * a.C + 8 * q, o);
         }
