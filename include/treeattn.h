@@ -154,14 +154,19 @@ tree_status_t tree_plan_build(const int32_t* segment_parents, const int32_t* seg
  * parent's gateway and the cut node's ancestors within the parent are
  * visible, the parent's other subtrees are not); the partition's own keys
  * keep the tree mask (eq. 14). past_visible is a host array of past_len bytes
- * (copied); past_len == 0 gives the plan of tree_plan_build.
- * Errors as tree_plan_build, and past_len < 0, or a NULL past_visible with
- * past_len > 0 -> TREE_ERR_INVALID_ARG.
+ * (copied). pos_offset (App. B.4 eq. 17) is added to every position id, so
+ * that a root of the partition continues the positions of the path above it:
+ * pass tree_partition's pos_offset of the partition, and the position ids
+ * (TREE_FIELD_POS_ID, tree_rope) equal those of the same tokens in the whole
+ * trie. past_len == 0 and pos_offset == 0 give the plan of tree_plan_build.
+ * Errors as tree_plan_build, and past_len < 0, pos_offset < 0, or a NULL
+ * past_visible with past_len > 0 -> TREE_ERR_INVALID_ARG; pos_offset plus the
+ * token count above 2^31-1 -> TREE_ERR_OVERFLOW.
  */
 tree_status_t tree_plan_build_partition(const int32_t* segment_parents,
                                         const int32_t* segment_lengths, int32_t num_segments,
                                         const uint8_t* past_visible, int32_t past_len,
-                                        tree_plan_t** out);
+                                        int32_t pos_offset, tree_plan_t** out);
 
 /* Sizes of a plan (host). */
 tree_status_t tree_plan_info(const tree_plan_t* plan, tree_plan_info_t* out);

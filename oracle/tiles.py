@@ -209,9 +209,12 @@ def gateway_fields(N, past_visible, bn: int = 128):
     return kend, kt
 
 
-def plan_fields(parents, lengths, bm: int = 128, bn: int = 128, past_visible=None) -> dict:
+def plan_fields(parents, lengths, bm: int = 128, bn: int = 128, past_visible=None,
+                pos_offset: int = 0) -> dict:
     """Every plan field as int32/int64 numpy arrays, named as in the C-ABI
-    (with ``past_visible``, those of a partition plan with that gateway)."""
+    (with ``past_visible``, those of a partition plan with that gateway; with
+    ``pos_offset``, position ids shifted by it as App. B.4 eq. 17 starts a
+    child partition's positions)."""
     parents_l, lengths_l = T.validate(parents, lengths)
     S = len(parents_l)
     N = sum(lengths_l)
@@ -273,7 +276,7 @@ def plan_fields(parents, lengths, bm: int = 128, bn: int = 128, past_visible=Non
         qp_ptr.append(len(qp_kt))
     qp_order = list(reversed(range(n_pairs)))
 
-    pos_id = T.position_ids(parents_l, lengths_l)
+    pos_id = [p + pos_offset for p in T.position_ids(parents_l, lengths_l)]
     gq_ptr, gp_ptr, gt_kind, gt_atom, gt_bidx, gt_bounds = _gathered_fields(parents_l, lengths_l,
                                                                           past_visible)
     gw_kend, gw_kt = ([], []) if past_visible is None or len(past_visible) == 0 else \

@@ -175,3 +175,27 @@ def test_agentic_trie_partitioned_at_16384_tokens():
     assert checked >= 1
     _check("dk summed over pieces vs whole", dk_sum, dk_full.double().cpu())
     _check("dv summed over pieces vs whole", dv_sum, dv_full.double().cpu())
+
+
+def test_rope_on_pieces_equals_rope_on_the_whole_trie():
+    """App. B.4 eq. 17: with the planner's pos_offset, RoPE applied to each
+    piece of workload 4 (cut at 16,384 tokens) gives bit for bit what RoPE on
+    the whole trie gives for the same tokens (same position ids, same kernel)."""
+    _need_gpu()
+    w = treegen.workload(4)
+    N = w.num_tokens
+    full = tpa.tree_plan_build(w.parents, w.lengths)
+    r = tpa.tree_partition(full, 16384)
+    Xs = pieces(w.parents, w.lengths, [int(x) for x in r["part_of_segment"]])
+    x = treegen.draw_tensors(N, w.hq, w.hkv, w.head_dim, w.dtype, 3)[0].cuda()
+    whole = tpa.tree_rope(full, x.clone())
+    for i, X in enumerate(Xs):
+        plan = tpa.tree_plan_build_partition(X["parents"], X["lengths"], X["vis"],
+                                             int(r["pos_offset"][i]))
+        tok = torch.as_tensor(to_np(X["tokens"]), device="cuda")
+        got = tpa.tree_rope(plan, x[tok].contiguous())
+        assert torch.equal(got, whole[tok]), i
+        if i and r["pos_offset"][i] > 0:  # without the offset the rotation differs
+            plain = tpa.tree_plan_build_partition(X["parents"], X["lengths"], X["vis"])
+            assert not torch.equal(tpa.tree_rope(plain, x[tok].contiguous()), whole[tok])
+    tpa.tree_status_sync()

@@ -17,6 +17,7 @@ import tree_packed_attention_gb300 as tpa
 from oracle import attention as A
 from oracle import gateway as GW
 from oracle import mask as M
+from oracle import partition as PT
 from oracle import tiles as TL
 from partition_util import cut_forest, pieces, to_np
 
@@ -143,15 +144,56 @@ def test_partition_plans_match_the_oracle_bit_for_bit():
             assert np.array_equal(got[name], ref[name]), name
 
 
+def test_partition_positions_continue_the_path_above():
+    """App. B.4 eq. 17: a partition plan built with the planner's pos_offset
+    gives every token the position id it has in the whole trie (eq. 9), so
+    RoPE on the pieces equals RoPE on the whole trie; the oracle's plan fields
+    agree."""
+    cases = [(p, L, None) for p, L, _ in _cases()]
+    w4 = treegen.workload(4)
+    cases.append((w4.parents.tolist(), w4.lengths.tolist(), 16384))
+    cases.append(([-1, 0, 1, 1, 0, 4], [40, 30, 20, 50, 10, 60], 64))
+    for parents, lengths, cap in cases:
+        whole = tpa.tree_plan_build(parents, lengths)
+        cap = cap or max(max(lengths), sum(lengths) // 3)
+        r = tpa.tree_partition(whole, cap)
+        pos = whole.field("pos_id")
+        got_pieces = pieces(parents, lengths, [int(x) for x in r["part_of_segment"]])
+        assert len(got_pieces) == r["num_parts"]
+        for i, X in enumerate(got_pieces):
+            off = int(r["pos_offset"][i])
+            _check_piece(X, off, pos)
+            if r["parent"][i] < 0:
+                assert off == 0
+    # hand-made and random cuts, offsets from the eq. 17 recursion
+    for parents, lengths, part in _cases():
+        pos = tpa.tree_plan_build(parents, lengths).field("pos_id")
+        rec = PT.partition_records(parents, lengths, part)
+        for X in pieces(parents, lengths, part):
+            _check_piece(X, rec[part[X["segs"][0]]]["pos_offset"], pos)
+
+
+def _check_piece(X, off, pos):
+    plan = tpa.tree_plan_build_partition(X["parents"], X["lengths"], X["vis"], off)
+    assert np.array_equal(plan.field("pos_id"), pos[X["tokens"]])
+    if len(X["tokens"]) < 5000:
+        ref = TL.plan_fields(X["parents"], X["lengths"], past_visible=X["vis"], pos_offset=off)
+        assert np.array_equal(plan.field("pos_id"), ref["pos_id"])
+
+
 def test_partition_plan_arguments_are_checked():
     import ctypes
     h = ctypes.c_void_p()
     p = np.array([-1], np.int32)
     L = np.array([4], np.int32)
-    assert tpa.lib.tree_plan_build_partition(p.ctypes.data, L.ctypes.data, 1, None, -1,
+    assert tpa.lib.tree_plan_build_partition(p.ctypes.data, L.ctypes.data, 1, None, -1, 0,
                                              ctypes.byref(h)) == 1
-    assert tpa.lib.tree_plan_build_partition(p.ctypes.data, L.ctypes.data, 1, None, 3,
+    assert tpa.lib.tree_plan_build_partition(p.ctypes.data, L.ctypes.data, 1, None, 3, 0,
                                              ctypes.byref(h)) == 1
+    assert tpa.lib.tree_plan_build_partition(p.ctypes.data, L.ctypes.data, 1, None, 0, -1,
+                                             ctypes.byref(h)) == 1
+    assert tpa.lib.tree_plan_build_partition(p.ctypes.data, L.ctypes.data, 1, None, 0,
+                                             2 ** 31 - 4, ctypes.byref(h)) == 4  # overflow
     plan = tpa.tree_plan_build_partition([-1], [4], [1, 1])
     # a plan with a gateway is refused by the plain calls (before any device use)
     st = tpa.lib.tree_attn_fwd(plan.handle, None, None, None, None, None, 1, 1, 128, 1, 0.0, None)

@@ -37,23 +37,24 @@ __all__ = [
 class Plan:
     """Owns a ``tree_plan_t``: the host plan and, once uploaded, its device copy."""
 
-    def __init__(self, segment_parents, segment_lengths, past_visible=None):
+    def __init__(self, segment_parents, segment_lengths, past_visible=None, pos_offset=0):
         parents = np.ascontiguousarray(np.asarray(segment_parents, dtype=np.int32))
         lengths = np.ascontiguousarray(np.asarray(segment_lengths, dtype=np.int32))
         if parents.shape != lengths.shape or parents.ndim != 1:
             raise ValueError("segment_parents and segment_lengths must be 1-D and of equal length")
         h = C.c_void_p()
-        if past_visible is None:
+        if past_visible is None and pos_offset == 0:
             check(lib.tree_plan_build(parents.ctypes.data, lengths.ctypes.data, int(parents.size),
                                       C.byref(h)))
         else:
-            vis = np.ascontiguousarray(np.asarray(past_visible, dtype=bool).astype(np.uint8))
+            vis = np.ascontiguousarray(np.asarray([] if past_visible is None else past_visible,
+                                                  dtype=bool).astype(np.uint8))
             if vis.ndim != 1:
                 raise ValueError("past_visible must be 1-D")
             check(lib.tree_plan_build_partition(parents.ctypes.data, lengths.ctypes.data,
                                                 int(parents.size),
                                                 vis.ctypes.data if vis.size else None,
-                                                int(vis.size), C.byref(h)))
+                                                int(vis.size), int(pos_offset), C.byref(h)))
         self._h = h
         info = PlanInfo()
         check(lib.tree_plan_info(self._h, C.byref(info)))
@@ -90,11 +91,11 @@ def tree_plan_build(segment_parents, segment_lengths) -> Plan:
     return Plan(segment_parents, segment_lengths)
 
 
-def tree_plan_build_partition(segment_parents, segment_lengths, past_visible) -> Plan:
+def tree_plan_build_partition(segment_parents, segment_lengths, past_visible, pos_offset=0) -> Plan:
     """Plan of one partition (§3.3; App. B): its own segments plus a gateway of
     len(past_visible) cached keys, key j visible to every row iff past_visible[j]
-    (App. B.3 eq. 16)."""
-    return Plan(segment_parents, segment_lengths, past_visible)
+    (App. B.3 eq. 16); position ids start at pos_offset (App. B.4 eq. 17)."""
+    return Plan(segment_parents, segment_lengths, past_visible, pos_offset)
 
 
 def _stream_ptr(stream):

@@ -99,7 +99,7 @@ def _load():
         "tree_conv_bwd": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, sz, vp]),
         "tree_status_sync": (i32, [vp]),
         "tree_last_error": (C.c_char_p, []),
-        "tree_plan_build_partition": (i32, [vp, vp, i32, vp, i32, C.POINTER(vp)]),
+        "tree_plan_build_partition": (i32, [vp, vp, i32, vp, i32, i32, C.POINTER(vp)]),
         "tree_attn_fwd_gateway": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, C.c_float,
                                         vp]),
         "tree_attn_bwd_gateway": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,

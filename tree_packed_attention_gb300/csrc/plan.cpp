@@ -283,7 +283,8 @@ void build_gateway(tree_plan* p, const uint8_t* visible, int32_t past_len) {
 }
 
 tree_status_t build(const int32_t* parents, const int32_t* lengths, int32_t S, tree_plan* p,
-                    const uint8_t* past_visible = nullptr, int32_t past_len = 0) {
+                    const uint8_t* past_visible = nullptr, int32_t past_len = 0,
+                    int32_t pos_offset = 0) {
   auto& F = p->field;
   // ---- validation
   for (int32_t s = 0; s < S; ++s) {
@@ -300,6 +301,8 @@ tree_status_t build(const int32_t* parents, const int32_t* lengths, int32_t S, t
   }
   if (n_tokens > std::numeric_limits<int32_t>::max() - kBlockM)
     return fail(TREE_ERR_OVERFLOW, "more than 2^31-129 tokens");
+  if (n_tokens + pos_offset > std::numeric_limits<int32_t>::max())
+    return fail(TREE_ERR_OVERFLOW, "position ids past 2^31-1");
   const int32_t N = static_cast<int32_t>(n_tokens);
 
   // ---- children (ascending id) and roots (ascending id)
@@ -354,7 +357,7 @@ tree_status_t build(const int32_t* parents, const int32_t* lengths, int32_t S, t
       const int32_t par = parents[s];
       if (par < 0) {
         depth[s] = 0;
-        pos_base[s] = 0;
+        pos_base[s] = pos_offset;
         trie_id[s] = root_rank++;
       } else {  // the parent precedes its children in pre-order
         depth[s] = depth[par] + 1;
@@ -545,18 +548,19 @@ using namespace treeattn;
 namespace {
 tree_status_t plan_entry(const int32_t* segment_parents, const int32_t* segment_lengths,
                          int32_t num_segments, const uint8_t* past_visible, int32_t past_len,
-                         tree_plan_t** out) {
+                         int32_t pos_offset, tree_plan_t** out) {
   if (!out) return fail(TREE_ERR_INVALID_ARG, "out is NULL");
   if (num_segments < 0) return fail(TREE_ERR_INVALID_ARG, "num_segments < 0");
   if (num_segments > 0 && (!segment_parents || !segment_lengths))
     return fail(TREE_ERR_INVALID_ARG, "NULL parents or lengths");
   if (past_len < 0) return fail(TREE_ERR_INVALID_ARG, "past_len < 0");
   if (past_len > 0 && !past_visible) return fail(TREE_ERR_INVALID_ARG, "NULL past_visible");
+  if (pos_offset < 0) return fail(TREE_ERR_INVALID_ARG, "pos_offset < 0");
   tree_plan* p = new (std::nothrow) tree_plan();
   if (!p) return fail(TREE_ERR_OOM, "out of host memory");
   tree_status_t st;
   try {
-    st = build(segment_parents, segment_lengths, num_segments, p, past_visible, past_len);
+    st = build(segment_parents, segment_lengths, num_segments, p, past_visible, past_len, pos_offset);
   } catch (const std::bad_alloc&) {
     st = fail(TREE_ERR_OOM, "out of host memory");
   }
@@ -573,14 +577,16 @@ tree_status_t plan_entry(const int32_t* segment_parents, const int32_t* segment_
 extern "C" tree_status_t tree_plan_build(const int32_t* segment_parents,
                                          const int32_t* segment_lengths, int32_t num_segments,
                                          tree_plan_t** out) {
-  return plan_entry(segment_parents, segment_lengths, num_segments, nullptr, 0, out);
+  return plan_entry(segment_parents, segment_lengths, num_segments, nullptr, 0, 0, out);
 }
 
 extern "C" tree_status_t tree_plan_build_partition(const int32_t* segment_parents,
                                                    const int32_t* segment_lengths,
                                                    int32_t num_segments, const uint8_t* past_visible,
-                                                   int32_t past_len, tree_plan_t** out) {
-  return plan_entry(segment_parents, segment_lengths, num_segments, past_visible, past_len, out);
+                                                   int32_t past_len, int32_t pos_offset,
+                                                   tree_plan_t** out) {
+  return plan_entry(segment_parents, segment_lengths, num_segments, past_visible, past_len,
+                    pos_offset, out);
 }
 
 extern "C" tree_status_t tree_plan_info(const tree_plan_t* p, tree_plan_info_t* out) {
