@@ -43,39 +43,56 @@ constexpr int kConvBufs = 3;
 constexpr int kSiteConv = 40000;  // status word of a conv wait that gave up: 40000 + line
 constexpr int kConvPartialBlocks = 512;  // token ranges of the backward (and its dweight / dbias sums)
 
-template <typename T>
-struct Vec8;
-template <>
-struct Vec8<__nv_bfloat16> {
-  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&v)[8]) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+// V consecutive channels of one row (V = 4 or 8: one 8- or 16-byte access
+// in bf16, one or two 16-byte accesses in fp32)
+template <typename T, int V>
+struct Vec;
+template <int V>
+struct Vec<__nv_bfloat16, V> {
+  static_assert(V == 4 || V == 8, "4 or 8 channels");
+  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&v)[V]) {
+    uint32_t w[V / 2];
+    if constexpr (V == 8) {
+      const uint4 u = *reinterpret_cast<const uint4*>(p);
+      w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+    } else {
+      const uint2 u = *reinterpret_cast<const uint2*>(p);
+      w[0] = u.x; w[1] = u.y;
+    }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < V / 2; ++j) {
       const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));
       v[2 * j] = f.x;
       v[2 * j + 1] = f.y;
     }
   }
-  static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&v)[8]) {
-    uint32_t w[4];
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&v)[V]) {
+    uint32_t w[V / 2];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < V / 2; ++j) {
       const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
       w[j] = *reinterpret_cast<const uint32_t*>(&b);
     }
-    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    if constexpr (V == 8)
+      *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    else
+      *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
   }
 };
-template <>
-struct Vec8<float> {
-  static __device__ __forceinline__ void load(const float* p, float (&v)[8]) {
-    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+template <int V>
+struct Vec<float, V> {
+  static_assert(V == 4 || V == 8, "4 or 8 channels");
+  static __device__ __forceinline__ void load(const float* p, float (&v)[V]) {
+#pragma unroll
+    for (int h = 0; h < V / 4; ++h) {
+      const float4 a = reinterpret_cast<const float4*>(p)[h];
+      v[4 * h] = a.x; v[4 * h + 1] = a.y; v[4 * h + 2] = a.z; v[4 * h + 3] = a.w;
+    }
   }
-  static __device__ __forceinline__ void store(float* p, const float (&v)[8]) {
-    reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
-    reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+  static __device__ __forceinline__ void store(float* p, const float (&v)[V]) {
+#pragma unroll
+    for (int h = 0; h < V / 4; ++h)
+      reinterpret_cast<float4*>(p)[h] = make_float4(v[4 * h], v[4 * h + 1], v[4 * h + 2], v[4 * h + 3]);
   }
 };
 
@@ -88,17 +105,17 @@ __device__ __forceinline__ float silu_grad(float z) {
   return s * (1.f + z * (1.f - s));
 }
 
-// Each thread owns one chunk of 8 channels (q) for the whole launch and keeps
+// Each thread owns one chunk of V channels (q) for the whole launch and keeps
 // their K weights (and biases) in registers; blocks stride over tokens, and
 // blockIdx.y picks the group of 256 chunks.
-template <int K>
+template <int K, int V = 8>
 struct Taps {
-  float w[8][K];
+  float w[V][K];
   __device__ __forceinline__ void load(const float* weight, int q) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < V; ++j)
 #pragma unroll
-      for (int k = 0; k < K; ++k) w[j][k] = __ldg(weight + (8 * q + j) * K + k);
+      for (int k = 0; k < K; ++k) w[j][k] = __ldg(weight + (V * q + j) * K + k);
   }
 };
 
@@ -108,51 +125,51 @@ __device__ __forceinline__ int pred_of(const ConvArgs& a, int t, int k) {
   return k == 0 ? t : __ldg(a.pred + static_cast<size_t>(t) * (K - 1) + (k - 1));
 }
 
-// The K rows token t reads, x[pred_k(t)] for k = 0..K-1, for one chunk of 8
+// The K rows token t reads, x[pred_k(t)] for k = 0..K-1, for one chunk of V
 // channels. A thread walks a contiguous token range: when t's immediate path
 // predecessor is t-1 (inside a segment, or a first child right after its
 // parent) the window shifts by one row; otherwise it is reloaded from the
 // predecessor table (segment starts). The next token's row and predecessor
 // are loaded one token ahead.
-template <typename T, int K>
+template <typename T, int K, int V = 8>
 struct Window {
-  float v[K][8];
-  __device__ __forceinline__ void reload(const ConvArgs& a, int t, int q, const float (&xt)[8]) {
+  float v[K][V];
+  __device__ __forceinline__ void reload(const ConvArgs& a, int t, int q, const float (&xt)[V]) {
     const T* x = static_cast<const T*>(a.x);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[0][j] = xt[j];
+    for (int j = 0; j < V; ++j) v[0][j] = xt[j];
 #pragma unroll
     for (int k = 1; k < K; ++k) {
       const int u = pred_of<K>(a, t, k);
       if (u < 0) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[k][j] = 0.f;  // before the root
+        for (int j = 0; j < V; ++j) v[k][j] = 0.f;  // before the root
       } else {
-        Vec8<T>::load(x + static_cast<size_t>(u) * a.C + 8 * q, v[k]);
+        Vec<T, V>::load(x + static_cast<size_t>(u) * a.C + V * q, v[k]);
       }
     }
   }
-  __device__ __forceinline__ void shift(const float (&xt)[8]) {
+  __device__ __forceinline__ void shift(const float (&xt)[V]) {
 #pragma unroll
     for (int k = K - 1; k > 0; --k)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[k][j] = v[k - 1][j];
+      for (int j = 0; j < V; ++j) v[k][j] = v[k - 1][j];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[0][j] = xt[j];
+    for (int j = 0; j < V; ++j) v[0][j] = xt[j];
   }
   // the pre-activation, channels in packed pairs
-  __device__ __forceinline__ void pre(const Taps<K>& tp, const float (&b)[8], float (&z)[8]) const {
-    float2 z2[4];
+  __device__ __forceinline__ void pre(const Taps<K, V>& tp, const float (&b)[V], float (&z)[V]) const {
+    float2 z2[V / 2];
 #pragma unroll
-    for (int jp = 0; jp < 4; ++jp) z2[jp] = make_float2(b[2 * jp], b[2 * jp + 1]);
+    for (int jp = 0; jp < V / 2; ++jp) z2[jp] = make_float2(b[2 * jp], b[2 * jp + 1]);
 #pragma unroll
     for (int k = 0; k < K; ++k)
 #pragma unroll
-      for (int jp = 0; jp < 4; ++jp)
+      for (int jp = 0; jp < V / 2; ++jp)
         z2[jp] = __ffma2_rn(make_float2(tp.w[2 * jp][K - 1 - k], tp.w[2 * jp + 1][K - 1 - k]),
                             make_float2(v[k][2 * jp], v[k][2 * jp + 1]), z2[jp]);
 #pragma unroll
-    for (int jp = 0; jp < 4; ++jp) {
+    for (int jp = 0; jp < V / 2; ++jp) {
       z[2 * jp] = z2[jp].x;
       z[2 * jp + 1] = z2[jp].y;
     }
@@ -169,9 +186,9 @@ __device__ __forceinline__ void token_range(const ConvArgs& a, int& t0, int& t1)
 // Bulk-copy staging of NT token-major tensors for one block: batch i (tokens
 // tb .. tb+n-1) of tensor s sits at buf + (i % kConvBufs) * NT * kConvBatchBytes
 // + s * kConvBatchBytes, token u of the batch at u * (row stride).
-template <typename T, int NT>
+template <typename T, int NT, int V = 8>
 struct Stage {
-  static constexpr uint32_t kStride = kConvThreads * 8 * sizeof(T);  // smem bytes per token row
+  static constexpr uint32_t kStride = kConvThreads * V * sizeof(T);  // smem bytes per token row
   static constexpr int kBatch = static_cast<int>(kConvBatchBytes / kStride);
   uint8_t* buf;
   uint64_t* bar;       // [kConvBufs]
@@ -245,7 +262,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_fwd_kernel(const ConvArgs a
         if (u >= n) break;
         const int t = tb + u;
         float xt[8];
-        Vec8<T>::load(reinterpret_cast<const T*>(st.row(i, 0, u)) + 8 * threadIdx.x, xt);
+        Vec<T, 8>::load(reinterpret_cast<const T*>(st.row(i, 0, u)) + 8 * threadIdx.x, xt);
         if (t > st.t0 && p1[u] == t - 1)
           win.shift(xt);
         else
@@ -256,7 +273,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_fwd_kernel(const ConvArgs a
 #pragma unroll
           for (int j = 0; j < 8; ++j) z[j] = silu(z[j]);
         }
-        Vec8<T>::store(y + static_cast<size_t>(t) * a.C + 8 * q, z);
+        Vec<T, 8>::store(y + static_cast<size_t>(t) * a.C + 8 * q, z);
       }
     }
     __syncthreads();  // every thread is done with this batch's buffer
@@ -265,6 +282,10 @@ __global__ void __launch_bounds__(kConvThreads) conv_fwd_kernel(const ConvArgs a
   if (i < nb && threadIdx.x == 0)  // gave up a wait: let the copies in flight land
     for (int k = i; k < nb && k < i + kConvBufs; ++k) mbar_drain(&bar[k % kConvBufs], (k / kConvBufs) & 1);
 }
+
+// Blocks per SM of the backward's walk: two for up to 5 taps at 4 channels a
+// thread (at most 128 registers, no spills); one otherwise.
+constexpr int conv_bwd_blocks_per_sm(int K, int V) { return V == 4 && K <= 5 ? 2 : 1; }
 
 // The backward in one pass over each block's token range, in DFS order:
 //   g[t]  = dy[t] * act'(pre_t), from the window that the forward also walks;
@@ -278,23 +299,24 @@ __global__ void __launch_bounds__(kConvThreads) conv_fwd_kernel(const ConvArgs a
 //   conv_bwd_dx_irregular_kernel. The walk runs K-1 tokens past the range
 //   (g only) so the range's last tokens see their readers; g never leaves
 //   registers.
-template <typename T, int K>
-__global__ void __launch_bounds__(kConvThreads) conv_bwd_fused_kernel(const ConvArgs a) {
+template <typename T, int K, int V>
+__global__ void __launch_bounds__(kConvThreads, conv_bwd_blocks_per_sm(K, V))
+    conv_bwd_fused_kernel(const ConvArgs a) {
   extern __shared__ __align__(128) uint8_t cbuf[];
   __shared__ uint64_t bar[kConvBufs];
   __shared__ int abort_s;
   const int q = blockIdx.y * kConvThreads + threadIdx.x;
-  const bool valid = q < a.C / 8;
+  const bool valid = q < a.C / V;
   int t0, t1;
   token_range(a, t0, t1);
-  Stage<T, 2> st;
+  Stage<T, 2, V> st;
   st.buf = cbuf;
   st.bar = bar;
   st.src[0] = static_cast<const T*>(a.x);
   st.src[1] = static_cast<const T*>(a.dy);
   st.C = a.C;
-  st.g0 = blockIdx.y * kConvThreads * 8;
-  st.row_bytes = static_cast<uint32_t>(min(kConvThreads * 8, a.C - st.g0) * sizeof(T));
+  st.g0 = blockIdx.y * kConvThreads * V;
+  st.row_bytes = static_cast<uint32_t>(min(kConvThreads * V, a.C - st.g0) * sizeof(T));
   st.t0 = t0;
   st.te = t0 < t1 ? min(a.N, t1 + K - 1) : t0;  // K-1 tokens past the range: their g
   if (threadIdx.x == 0) {
@@ -306,27 +328,27 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_fused_kernel(const Conv
   const int nb = st.t0 < st.te ? st.batches() : 0;
   if (threadIdx.x == 0)
     for (int i = 0; i < kConvBufs && i < nb; ++i) st.issue(i);
-  Taps<K> tp;
-  float b[8];
+  Taps<K, V> tp;
+  float b[V];
   if (valid) {
     tp.load(a.weight, q);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) b[j] = a.bias ? __ldg(a.bias + 8 * q + j) : 0.f;
+    for (int j = 0; j < V; ++j) b[j] = a.bias ? __ldg(a.bias + V * q + j) : 0.f;
   }
   T* dx = static_cast<T*>(a.dx);
-  float acc[K + 1][8];
+  float acc[K + 1][V];
 #pragma unroll
   for (int k = 0; k <= K; ++k)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[k][j] = 0.f;
-  float gh[K][8];  // gh[k] = g of the token k steps back in DFS order
+    for (int j = 0; j < V; ++j) acc[k][j] = 0.f;
+  float gh[K][V];  // gh[k] = g of the token k steps back in DFS order
 #pragma unroll
   for (int k = 0; k < K; ++k)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) gh[k][j] = 0.f;
+    for (int j = 0; j < V; ++j) gh[k][j] = 0.f;
   uint32_t cont = 0;  // bit k: the token k steps back follows its DFS predecessor on its path
-  Window<T, K> win;
-  constexpr int B = Stage<T, 2>::kBatch;
+  Window<T, K, V> win;
+  constexpr int B = Stage<T, 2, V>::kBatch;
   const int tend = t0 < t1 ? t1 + K - 1 : t0;  // walk end, virtual tokens past N included
   const int nsteps = (tend - t0 + B - 1) / B;  // batches of the walk (the last ones may be virtual)
   int i = 0;
@@ -346,28 +368,28 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_fused_kernel(const Conv
       for (int u = 0; u < B; ++u) {
         const int t = tb + u;
         if (t >= tend) break;
-        float g[8];
+        float g[V];
         bool step = false;
         if (u < n) {
-          float xt[8];
-          Vec8<T>::load(reinterpret_cast<const T*>(st.row(i, 0, u)) + 8 * threadIdx.x, xt);
-          Vec8<T>::load(reinterpret_cast<const T*>(st.row(i, 1, u)) + 8 * threadIdx.x, g);
+          float xt[V];
+          Vec<T, V>::load(reinterpret_cast<const T*>(st.row(i, 0, u)) + V * threadIdx.x, xt);
+          Vec<T, V>::load(reinterpret_cast<const T*>(st.row(i, 1, u)) + V * threadIdx.x, g);
           step = p1[u] == t - 1;
           if (t > t0 && step)
             win.shift(xt);
           else
             win.reload(a, t, q, xt);
           if (a.act == 1) {
-            float z[8];
+            float z[V];
             win.pre(tp, b, z);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) g[j] *= silu_grad(z[j]);
+            for (int j = 0; j < V; ++j) g[j] *= silu_grad(z[j]);
           }
           if (t < t1) {
 #pragma unroll
             for (int k = 0; k < K; ++k)
 #pragma unroll
-              for (int jp = 0; jp < 4; ++jp) {
+              for (int jp = 0; jp < V / 2; ++jp) {
                 const float2 r2 = __ffma2_rn(make_float2(g[2 * jp], g[2 * jp + 1]),
                                              make_float2(win.v[k][2 * jp], win.v[k][2 * jp + 1]),
                                              make_float2(acc[k][2 * jp], acc[k][2 * jp + 1]));
@@ -375,25 +397,25 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_fused_kernel(const Conv
                 acc[k][2 * jp + 1] = r2.y;
               }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[K][j] += g[j];
+            for (int j = 0; j < V; ++j) acc[K][j] += g[j];
           }
         } else {  // past the last token: no readers
 #pragma unroll
-          for (int j = 0; j < 8; ++j) g[j] = 0.f;
+          for (int j = 0; j < V; ++j) g[j] = 0.f;
         }
 #pragma unroll
         for (int k = K - 1; k > 0; --k)
 #pragma unroll
-          for (int j = 0; j < 8; ++j) gh[k][j] = gh[k - 1][j];
+          for (int j = 0; j < V; ++j) gh[k][j] = gh[k - 1][j];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) gh[0][j] = g[j];
+        for (int j = 0; j < V; ++j) gh[0][j] = g[j];
         cont = (cont << 1) | (step ? 1u : 0u);
         // token u0 = t - (K-1) now has all of its run readers u0 .. t
         const int u0 = t - (K - 1);
         if (u0 >= t0 && u0 < a.N && !(__ldg(a.irr_bits + (u0 >> 5)) >> (u0 & 31) & 1u)) {
-          float2 o2[4];
+          float2 o2[V / 2];
 #pragma unroll
-          for (int jp = 0; jp < 4; ++jp)  // k = 0: u0 itself
+          for (int jp = 0; jp < V / 2; ++jp)  // k = 0: u0 itself
             o2[jp] = __fmul2_rn(make_float2(tp.w[2 * jp][K - 1], tp.w[2 * jp + 1][K - 1]),
                                 make_float2(gh[K - 1][2 * jp], gh[K - 1][2 * jp + 1]));
           bool run = true;
@@ -402,18 +424,18 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_fused_kernel(const Conv
             run = run && ((cont >> (K - 1 - k)) & 1u);  // u0 + k follows u0 + k - 1
             if (run) {
 #pragma unroll
-              for (int jp = 0; jp < 4; ++jp)
+              for (int jp = 0; jp < V / 2; ++jp)
                 o2[jp] = __ffma2_rn(make_float2(tp.w[2 * jp][K - 1 - k], tp.w[2 * jp + 1][K - 1 - k]),
                                     make_float2(gh[K - 1 - k][2 * jp], gh[K - 1 - k][2 * jp + 1]), o2[jp]);
             }
           }
-          float o[8];
+          float o[V];
 #pragma unroll
-          for (int jp = 0; jp < 4; ++jp) {
+          for (int jp = 0; jp < V / 2; ++jp) {
             o[2 * jp] = o2[jp].x;
             o[2 * jp + 1] = o2[jp].y;
           }
-          Vec8<T>::store(dx + static_cast<size_t>(u0) * a.C + 8 * q, o);
+          Vec<T, V>::store(dx + static_cast<size_t>(u0) * a.C + V * q, o);
         }
       }
     }
@@ -429,7 +451,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_fused_kernel(const Conv
 #pragma unroll
     for (int k = 0; k <= K; ++k)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) part[static_cast<size_t>(k) * a.C + 8 * q + j] = acc[k][j];
+      for (int j = 0; j < V; ++j) part[static_cast<size_t>(k) * a.C + V * q + j] = acc[k][j];
   }
 }
 
@@ -454,10 +476,10 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_dx_irregular_kernel(con
     for (int e = e0; e < e1; ++e) {
       const int packed = __ldg(a.succ + e), t = packed >> 3, k = packed & 7;
       float g[8];
-      Vec8<T>::load(dy + static_cast<size_t>(t) * a.C + 8 * q, g);
+      Vec<T, 8>::load(dy + static_cast<size_t>(t) * a.C + 8 * q, g);
       if (a.act == 1) {
         float xt[8];
-        Vec8<T>::load(x + static_cast<size_t>(t) * a.C + 8 * q, xt);
+        Vec<T, 8>::load(x + static_cast<size_t>(t) * a.C + 8 * q, xt);
         Window<T, K> win;
         win.reload(a, t, q, xt);
         float z[8];
@@ -472,7 +494,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_dx_irregular_kernel(con
         for (int j = 0; j < 8; ++j) o[j] = fmaf(tp.w[j][K - 1 - kk], g[j], o[j]);
       }
     }
-    Vec8<T>::store(dx + static_cast<size_t>(u) * a.C + 8 * q, o);
+    Vec<T, 8>::store(dx + static_cast<size_t>(u) * a.C + 8 * q, o);
   }
 }
 
@@ -633,6 +655,10 @@ cudaError_t smem_attr(F* kernel, uint32_t bytes, bool& done) {
 
 constexpr uint32_t kFwdSmem = kConvBufs * kConvBatchBytes;      // x
 constexpr uint32_t kBwdSmem = kConvBufs * 2 * kConvBatchBytes;  // x and dy
+// Channels per thread in the backward's walk: 4, so that its per-thread state
+// (the window, the last K gradients, the dweight / dbias sums and the taps)
+// fits two 256-thread blocks per SM (for up to 5 taps).
+constexpr int kBwdChannels = 4;
 
 template <int K>
 cudaError_t conv_fwd_k(const ConvArgs& a, dim3 grid) {
@@ -654,27 +680,30 @@ cudaError_t conv_bwd_k(const ConvArgs& a, dim3 grid, dim3 pgrid) {
   const dim3 igrid(a.num_irr < 1024 ? (a.num_irr > 0 ? a.num_irr : 1) : 1024, grid.y);
   cudaError_t e;
   if (a.f32) {
-    if ((e = smem_attr(conv_bwd_fused_kernel<float, K>, kBwdSmem, done[1])) != cudaSuccess) return e;
-    conv_bwd_fused_kernel<float, K><<<pgrid, kConvThreads, kBwdSmem, a.stream>>>(a);
+    if ((e = smem_attr(conv_bwd_fused_kernel<float, K, kBwdChannels>, kBwdSmem, done[1])) != cudaSuccess)
+      return e;
+    conv_bwd_fused_kernel<float, K, kBwdChannels><<<pgrid, kConvThreads, kBwdSmem, a.stream>>>(a);
     if (a.num_irr > 0) conv_bwd_dx_irregular_kernel<float, K><<<igrid, kConvThreads, 0, a.stream>>>(a);
   } else {
-    if ((e = smem_attr(conv_bwd_fused_kernel<__nv_bfloat16, K>, kBwdSmem, done[0])) != cudaSuccess) return e;
-    conv_bwd_fused_kernel<__nv_bfloat16, K><<<pgrid, kConvThreads, kBwdSmem, a.stream>>>(a);
+    if ((e = smem_attr(conv_bwd_fused_kernel<__nv_bfloat16, K, kBwdChannels>, kBwdSmem, done[0])) !=
+        cudaSuccess)
+      return e;
+    conv_bwd_fused_kernel<__nv_bfloat16, K, kBwdChannels><<<pgrid, kConvThreads, kBwdSmem, a.stream>>>(a);
     if (a.num_irr > 0)
       conv_bwd_dx_irregular_kernel<__nv_bfloat16, K><<<igrid, kConvThreads, 0, a.stream>>>(a);
   }
   return cudaGetLastError();
 }
 
-// blocks: groups of 256 channel chunks (y) times token ranges (x), `per_sm`
-// blocks per SM in all (the forward keeps two 256-thread blocks per SM, the
-// backward one: its walk holds about 190 registers a thread)
-dim3 conv_grid(const ConvArgs& a, int per_sm) {
+// blocks: groups of 256 chunks of `chans` channels (y) times token ranges
+// (x), `per_sm` blocks per SM in all (two 256-thread blocks per SM for the
+// forward and the backward's walk)
+dim3 conv_grid(const ConvArgs& a, int per_sm, int chans = 8) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 1;
-  const int groups = (a.C / 8 + kConvThreads - 1) / kConvThreads;
+  const int groups = (a.C / chans + kConvThreads - 1) / kConvThreads;
   int tx = sms * per_sm / groups;
   tx = tx < 1 ? 1 : (tx > a.N ? a.N : tx);
   return dim3(tx, groups);
@@ -697,7 +726,7 @@ cudaError_t launch_conv_fwd(const ConvArgs& a) {
 
 cudaError_t launch_conv_bwd(ConvArgs a) {
   const dim3 grid = conv_grid(a, 8);  // the irregular tokens' gather
-  const dim3 pgrid = conv_grid(a, 1);
+  const dim3 pgrid = conv_grid(a, a.K <= 5 ? 2 : 1, kBwdChannels);
   const int pblocks = static_cast<int>(pgrid.x) < kConvPartialBlocks ? static_cast<int>(pgrid.x)
                                                                      : kConvPartialBlocks;
   const dim3 pg(pblocks, pgrid.y);
