@@ -669,16 +669,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_shared();
         mbar_arrive(&bar_stage_full[s]);
-        if (issuer) {
-          if (!(ok = mbar_wait(&bar_stage_full[s], halves & 1, abort, p.status, kSiteFwd + __LINE__)))
-            break;
-          tma_store_3d(&map_o, stage, hf * 64, h, qt * 128);
-          bulk_commit_group();
-          bulk_wait_group_read<0>();
-          mbar_arrive(&bar_stage_free[s]);
+        if (issuer) {  // (a wait that gives up leaves the loop below, with the whole warp)
+          ok = mbar_wait(&bar_stage_full[s], halves & 1, abort, p.status, kSiteFwd + __LINE__);
+          if (ok) {
+            tma_store_3d(&map_o, stage, hf * 64, h, qt * 128);
+            bulk_commit_group();
+            bulk_wait_group_read<0>();
+            mbar_arrive(&bar_stage_free[s]);
+          }
         }
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
       }
-      if (!__all_sync(0xffffffffu, ok)) break;
+      if (!ok) break;
       if (i < p.N)
         p.lse[static_cast<size_t>(h) * p.N + i] =
             l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
