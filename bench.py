@@ -718,7 +718,7 @@ def gdn_arm(args):
         "tokens_per_s": N / (ms * 1e-3),
         "roofline": {"bound": "alu", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
                      "peak_source": "152 SMs x 128 FP32 lanes x 2 flops x sampled SM clock", "traffic": None},
-        "clocks": cs, "gpu_launches": args.steps,
+        "clocks": cs, "gpu_launches": args.steps * plan.info["gdn_levels"],
     }))
 
 

@@ -73,6 +73,8 @@ typedef struct {
   int64_t num_gathered_tiles; /* entries of TREE_FIELD_GT_KIND (both unit sizes) */
   int64_t past_len;       /* gateway keys of a partition plan (0 otherwise) */
   int64_t past_visible;   /* of which visible to the partition's rows */
+  int64_t gdn_levels;     /* launches of tree_gdn_fwd: 1 + the most segments with several
+                             children on one root-to-leaf path (0 for an empty plan) */
 } tree_plan_info_t;
 
 /* Plan fields readable with tree_plan_get. All are int32 arrays. */
@@ -462,6 +464,8 @@ tree_status_t tree_weighted_ce(const tree_plan_t* plan, const void* logits, void
  *    state after each segment's last token (what a child partition's gateway
  *    carries, App. B.7); also the routing's own store of parent states.
  *  - Arithmetic in fp32 (CUDA cores); o rounded once to its dtype.
+ *  - Launches: tree_plan_info's gdn_levels kernels in stream order, one per
+ *    level of branch points (sibling branches run side by side).
  * Asynchronous on `stream`; the plan must be on the current device. Errors:
  * head_dim != 128 or hv > 65535 -> TREE_ERR_UNSUPPORTED; NULL plan or pointer,
  * bad dtype, hv % hk != 0, misaligned pointers -> TREE_ERR_INVALID_ARG; plan

@@ -227,3 +227,36 @@ def test_weighted_ce_host_checks():
     assert L(plan.handle, None, None, None, None, 8, 1, 1.0, None, None, None) == 1
     assert b"NULL" in tpa.lib.tree_last_error()
     assert L(None, None, None, None, None, 8, 1, 1.0, None, None, None) == 1
+
+
+def test_gdn_levels_count_branch_points_on_paths():
+    """The GDN forward launches once per level: 1 + the most segments with
+    several children met on one root-to-leaf path (a chain of only children is
+    one unit)."""
+    rng = np.random.default_rng(5)
+    cases = [([-1], [3]), ([-1, 0, 1, 2], [2, 2, 2, 2]), ([-1, 0, 0], [4, 1, 1]),
+             ([-1, -1, 0, 0, 1], [1, 2, 3, 4, 5]), ([], [])]
+    for _ in range(40):
+        S = int(rng.integers(1, 30))
+        parents = [-1] + [int(rng.integers(-1, s)) if rng.random() < 0.1 else int(rng.integers(0, s))
+                          for s in range(1, S)]
+        cases.append((parents, [int(x) for x in rng.integers(1, 9, S)]))
+    for i in (1, 2, 3, 4, 5):
+        w = treegen.workload(i)
+        cases.append((w.parents.tolist(), w.lengths.tolist()))
+    for parents, lengths in cases:
+        S = len(parents)
+        nchild = [0] * S
+        for p in parents:
+            if p >= 0:
+                nchild[p] += 1
+        best = 0
+        for s in range(S):
+            if nchild[s] == 0:  # a leaf: count the branch points above it
+                n, a = 0, parents[s]
+                while a >= 0:
+                    n += nchild[a] >= 2
+                    a = parents[a]
+                best = max(best, n + 1)
+        plan = tpa.tree_plan_build(parents, lengths)
+        assert plan.info["gdn_levels"] == best, (parents, lengths)

@@ -50,7 +50,7 @@ class PlanInfo(C.Structure):
     _fields_ = [(name, C.c_int64) for name in (
         "num_tokens", "num_segments", "num_tries", "block_m", "block_n", "num_q_tiles",
         "num_k_tiles", "nnz_tiles", "num_pairs", "nnz_pair_tiles", "num_ancestors",
-        "visible_pairs", "num_gathered_tiles", "past_len", "past_visible")]
+        "visible_pairs", "num_gathered_tiles", "past_len", "past_visible", "gdn_levels")]
 
 
 class TreeAttnError(RuntimeError):

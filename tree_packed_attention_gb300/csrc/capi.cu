@@ -133,12 +133,11 @@ extern "C" tree_status_t tree_plan_to_device(tree_plan_t* p, tree_stream_t strea
     total += (slot_elems(s) * 4 + 255) / 256 * 256;
   }
   // the GDN segment table, built from the DFS layout
-  std::vector<int32_t> seg_table(static_cast<size_t>(p->S) * 4), trie_seg_ptr(static_cast<size_t>(p->R) + 1, 0);
+  std::vector<int32_t> seg_table(static_cast<size_t>(p->S) * 4);
   {
     const auto& order = p->field[TREE_FIELD_DFS_ORDER];
     const auto& start = p->field[TREE_FIELD_SEG_START];
     const auto& tseg = p->field[TREE_FIELD_TOKEN_SEG];
-    const auto& trie = p->field[TREE_FIELD_TRIE_ID];
     const auto& ap = p->field[TREE_FIELD_ANC_PTR];
     const auto& ai = p->field[TREE_FIELD_ANC_IDX];
     std::vector<int32_t> len(static_cast<size_t>(p->S), 0);
@@ -149,32 +148,20 @@ extern "C" tree_status_t tree_plan_to_device(tree_plan_t* p, tree_stream_t strea
       seg_table[4 * d + 1] = start[s];
       seg_table[4 * d + 2] = len[s];
       seg_table[4 * d + 3] = ap[s + 1] > ap[s] ? ai[ap[s + 1] - 1] : -1;
-      ++trie_seg_ptr[trie[s] + 1];
     }
-    for (int32_t r = 0; r < p->R; ++r) trie_seg_ptr[r + 1] += trie_seg_ptr[r];
-  }
-  // tries by descending token count (ties by index), for the GDN launch order
-  std::vector<int32_t> trie_order(static_cast<size_t>(p->R));
-  {
-    const auto& cu = p->field[TREE_FIELD_CU_SEQLENS];
-    for (int32_t r = 0; r < p->R; ++r) trie_order[r] = r;
-    std::stable_sort(trie_order.begin(), trie_order.end(),
-                     [&](int32_t x, int32_t y) { return cu[x + 1] - cu[x] > cu[y + 1] - cu[y]; });
   }
   const size_t off_segs = total;
   total += (seg_table.size() * 4 + 255) / 256 * 256;
-  const size_t off_tptr = total;
-  total += (trie_seg_ptr.size() * 4 + 255) / 256 * 256;
-  const size_t off_torder = total;
-  total += (trie_order.size() * 4 + 255) / 256 * 256;
+  const size_t off_units = total;
+  total += (p->gdn_units.size() * 4 + 255) / 256 * 256;
   std::vector<uint8_t> host(total, 0);
   for (size_t s = 0; s < sizeof(slots) / sizeof(slots[0]); ++s) {
     const auto& v = p->field[slots[s].f];
     if (!v.empty()) std::memcpy(host.data() + offs[s], v.data(), v.size() * 4);
   }
   std::memcpy(host.data() + off_segs, seg_table.data(), seg_table.size() * 4);
-  std::memcpy(host.data() + off_tptr, trie_seg_ptr.data(), trie_seg_ptr.size() * 4);
-  if (!trie_order.empty()) std::memcpy(host.data() + off_torder, trie_order.data(), trie_order.size() * 4);
+  if (!p->gdn_units.empty())
+    std::memcpy(host.data() + off_units, p->gdn_units.data(), p->gdn_units.size() * 4);
   void* block = nullptr;
   e = cudaMalloc(&block, total);
   if (e != cudaSuccess) {
@@ -191,8 +178,7 @@ extern "C" tree_status_t tree_plan_to_device(tree_plan_t* p, tree_stream_t strea
   for (size_t s = 0; s < sizeof(slots) / sizeof(slots[0]); ++s)
     *slots[s].dst = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(block) + offs[s]);
   d.seg_table = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(block) + off_segs);
-  d.trie_seg_ptr = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(block) + off_tptr);
-  d.trie_order = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(block) + off_torder);
+  d.gdn_units = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(block) + off_units);
   d.block = block;
   d.bytes = total;
   d.device = cur;
@@ -346,10 +332,9 @@ extern "C" tree_status_t tree_gdn_fwd(const tree_plan_t* p, const void* q, const
   a.o = o;
   a.states = segment_states;
   a.segs = reinterpret_cast<const int4*>(p->dev.seg_table);
-  a.trie_ptr = p->dev.trie_seg_ptr;
-  a.cu = p->dev.cu_seqlens;
-  a.trie_order = p->dev.trie_order;
-  a.R = p->R;
+  a.units = reinterpret_cast<const int4*>(p->dev.gdn_units);
+  a.level_ptr = p->gdn_level_ptr.data();
+  a.levels = static_cast<int>(p->gdn_level_ptr.size()) - 1;
   a.hk = hk;
   a.hv = hv;
   a.group = hv / hk;

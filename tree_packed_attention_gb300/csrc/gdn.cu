@@ -9,8 +9,9 @@
 //   S_t = exp(g_t) S_{t-1} + k_t (beta_t (v_t - exp(g_t) S_{t-1}^T k_t))^T
 //   o_t = S_t^T q_t
 // Columns of S evolve independently given the token, and each column's two
-// products over Dk split into partial sums, so a CTA owns one head of one trie
-// and each group of kCols adjacent lanes kCols value columns, c + (128 /
+// products over Dk split into partial sums, so a CTA owns one head of one
+// unit (a chain of segments, each the only child of the one before) and each
+// group of kCols adjacent lanes kCols value columns, c + (128 /
 // kCols) m: the lane of part p holds rows 4 kCols x + 4p .. +3 of those
 // columns (128 fp32 registers in all), and the group adds its partial
 // products with log2(kCols) shuffles. Each lane reads only its share of a
@@ -27,13 +28,15 @@
 // S' += k (delta / A); when A would fall below 2^-40 (or one decay does) the
 // token takes the plain update, S' = (A exp(g)) S' + k delta^T, and A is 1
 // again. Scaled back by A, the rounding stays that of the plain recurrence.
-// The CTA walks the trie's tokens in DFS order, 32 at a time staged in shared
+// The CTA walks the unit's tokens in DFS order, 32 at a time staged in shared
 // memory as fp32 (with k . q per token); at a segment's first token the state
-// is the initial state (a root), kept in registers (the segment right before
-// it in DFS order is its parent), or reloaded from the parent's saved end
-// state, and the products come from a pass of their own (likewise after a
-// chunk's last token); every segment's end state is written out. Tries are
-// launched longest first.
+// is the initial state (a root), kept in registers (its parent is the segment
+// before it), or, at the unit's first segment, its parent's end state, and the
+// products come from a pass of their own (likewise after a chunk's last
+// token); every segment's end state is written out. The units of one level
+// (its branch-point depth: the children of a segment with several children
+// start new units, one level below) are one launch, longest first, so sibling
+// branches run side by side once their parent's state exists.
 //
 // 3 Dk Dv fused multiply-adds per token and head (the state update and the
 // two products), issued as packed fp32 pairs; the staged rows each lane reads
@@ -179,12 +182,13 @@ __device__ __forceinline__ void update(float2 (&S)[kCols][kPairs], const float* 
 constexpr float kMinScale = 9.094947e-13f;  // 2^-40: the smallest A the registers carry
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 3) tree_gdn_fwd_kernel(const GdnArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) tree_gdn_fwd_kernel(const GdnArgs a, int unit0) {
   __shared__ __align__(16) float sk[kChunk][kD];
   __shared__ __align__(16) float sq[kChunk][kD];
   __shared__ __align__(16) float sv[kChunk][kD];
   __shared__ float sa[kChunk], sb[kChunk], skq[kChunk];  // exp(g), beta, k . q
-  const int r = __ldg(a.trie_order + blockIdx.x), h = blockIdx.y;
+  const int4 unit = a.units[unit0 + blockIdx.x];  // this CTA's chain of segments
+  const int h = blockIdx.y;
   const int part = threadIdx.x % kCols;  // which rows of its columns this lane holds
   const int cb = threadIdx.x / kCols;    // its columns: cb + (kD / kCols) m
   const int hq = h / a.group;
@@ -200,9 +204,8 @@ __global__ void __launch_bounds__(kThreads, 3) tree_gdn_fwd_kernel(const GdnArgs
     return (kStep * x + 4 * part + 2 * y + e) * kD + cb + (kD / kCols) * c;
   };
 
-  const int d0 = __ldg(a.trie_ptr + r), d1 = __ldg(a.trie_ptr + r + 1);
-  if (d0 >= d1) return;
-  const int T0 = __ldg(a.cu + r), T1 = __ldg(a.cu + r + 1);  // the trie's DFS tokens
+  const int d0 = unit.x, d1 = unit.y;    // its DFS positions
+  const int T0 = unit.z, T1 = unit.w;    // and tokens
   float2 S[kCols][kPairs];  // S'[c][2x + y] = rows kStep x + 4 part + 2y, +1 of column c
   float A = 1.f;            // the state is A times the registers
   int d = d0;
@@ -336,13 +339,20 @@ __global__ void __launch_bounds__(kThreads, 3) tree_gdn_fwd_kernel(const GdnArgs
 
 }  // namespace
 
+// One launch per level: a level's units start from end states that the
+// launches before it wrote (stream order).
 cudaError_t launch_gdn_fwd(const GdnArgs& a) {
-  const dim3 grid(a.R, a.hv);
-  if (a.f32)
-    tree_gdn_fwd_kernel<float><<<grid, kThreads, 0, a.stream>>>(a);
-  else
-    tree_gdn_fwd_kernel<__nv_bfloat16><<<grid, kThreads, 0, a.stream>>>(a);
-  return cudaGetLastError();
+  for (int l = 0; l < a.levels; ++l) {
+    const int u0 = a.level_ptr[l], n = a.level_ptr[l + 1] - u0;
+    const dim3 grid(n, a.hv);
+    if (a.f32)
+      tree_gdn_fwd_kernel<float><<<grid, kThreads, 0, a.stream>>>(a, u0);
+    else
+      tree_gdn_fwd_kernel<__nv_bfloat16><<<grid, kThreads, 0, a.stream>>>(a, u0);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace treeattn

@@ -78,10 +78,9 @@ struct GdnArgs {
   void* o;             // [N, hv, 128]
   float* states;       // [S, hv, 128, 128]: each segment's end state
   const int4* segs;    // per DFS position: (segment id, first token, length, parent id)
-  const int32_t* trie_ptr;  // [R+1] DFS positions of each trie
-  const int32_t* cu;        // [R+1] token range of each trie
-  const int32_t* trie_order;  // [R] tries by descending token count
-  int R, hk, hv, group, f32;
+  const int4* units;   // (first DFS position, end position, first token, end token), by level
+  const int32_t* level_ptr;  // host: units of level l are level_ptr[l] .. level_ptr[l+1]
+  int levels, hk, hv, group, f32;
   cudaStream_t stream;
 };
 cudaError_t launch_gdn_fwd(const GdnArgs& a);

@@ -282,6 +282,54 @@ void build_gateway(tree_plan* p, const uint8_t* visible, int32_t past_len) {
   }
 }
 
+// Units and levels of the GDN forward's level-by-level launch (tree_plan::
+// gdn_units): a segment starts a unit unless it is the only child of its
+// parent (then it follows the parent in DFS order and continues its state).
+void build_gdn_units(tree_plan* p, const int32_t* parents) {
+  const int32_t S = p->S;
+  const auto& order = p->field[TREE_FIELD_DFS_ORDER];
+  const auto& start = p->field[TREE_FIELD_SEG_START];
+  std::vector<int32_t> nchild(S, 0), unit_of(S, -1), level;
+  for (int32_t s = 0; s < S; ++s)
+    if (parents[s] >= 0) ++nchild[parents[s]];
+  std::vector<int32_t> u;  // 4 per unit, DFS order
+  for (int32_t d = 0; d < S; ++d) {
+    const int32_t s = order[d], par = parents[s];
+    if (par >= 0 && nchild[par] == 1) {  // continues its parent's unit (at d - 1)
+      const int32_t id = unit_of[par];
+      unit_of[s] = id;
+      u[4 * id + 1] = d + 1;
+      continue;
+    }
+    const int32_t id = static_cast<int32_t>(level.size());
+    unit_of[s] = id;
+    level.push_back(par < 0 ? 0 : level[unit_of[par]] + 1);
+    u.insert(u.end(), {d, d + 1, start[s], 0});
+  }
+  // a unit's tokens end where its last segment's own tokens end
+  std::vector<int32_t> seg_len(S, 0);
+  for (int32_t t : p->field[TREE_FIELD_TOKEN_SEG]) ++seg_len[t];
+  const int32_t U = static_cast<int32_t>(level.size());
+  for (int32_t id = 0; id < U; ++id) {
+    const int32_t last = order[u[4 * id + 1] - 1];
+    u[4 * id + 3] = start[last] + seg_len[last];
+  }
+  std::vector<int32_t> idx(U);
+  for (int32_t i = 0; i < U; ++i) idx[i] = i;
+  std::stable_sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) {
+    if (level[a] != level[b]) return level[a] < level[b];
+    return u[4 * a + 3] - u[4 * a + 2] > u[4 * b + 3] - u[4 * b + 2];
+  });
+  const int32_t L = U ? 1 + *std::max_element(level.begin(), level.end()) : 0;
+  p->gdn_units.resize(static_cast<size_t>(U) * 4);
+  p->gdn_level_ptr.assign(static_cast<size_t>(L) + 1, 0);
+  for (int32_t i = 0; i < U; ++i) {
+    for (int c = 0; c < 4; ++c) p->gdn_units[4 * i + c] = u[4 * idx[i] + c];
+    ++p->gdn_level_ptr[level[idx[i]] + 1];
+  }
+  for (int32_t l = 0; l < L; ++l) p->gdn_level_ptr[l + 1] += p->gdn_level_ptr[l];
+}
+
 tree_status_t build(const int32_t* parents, const int32_t* lengths, int32_t S, tree_plan* p,
                     const uint8_t* past_visible = nullptr, int32_t past_len = 0,
                     int32_t pos_offset = 0) {
@@ -526,6 +574,7 @@ tree_status_t build(const int32_t* parents, const int32_t* lengths, int32_t S, t
   p->visible_pairs = visible;
 
   if (past_len > 0) build_gateway(p, past_visible, past_len);
+  build_gdn_units(p, parents);
   // ---- gathered key tiles: q-tiles first, then q-tile pairs, one table
   {
     const size_t est = static_cast<size_t>(nnz) * 3 / 2 + 16;  // about nnz + nnz / 2 tiles
@@ -606,6 +655,7 @@ extern "C" tree_status_t tree_plan_info(const tree_plan_t* p, tree_plan_info_t* 
   out->num_gathered_tiles = static_cast<int64_t>(p->field[TREE_FIELD_GT_KIND].size());
   out->past_len = p->past_len;
   out->past_visible = p->past_visible;
+  out->gdn_levels = p->gdn_level_ptr.empty() ? 0 : static_cast<int64_t>(p->gdn_level_ptr.size()) - 1;
   return TREE_OK;
 }
 

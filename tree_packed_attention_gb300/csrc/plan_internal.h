@@ -47,10 +47,10 @@ struct DevicePlan {
   const int32_t* subtree_end = nullptr;  // [S]
   const int32_t* cu_seqlens = nullptr;   // [R+1]
   // GDN state routing: per DFS position (segment, first token, length,
-  // parent or -1) as int4, and the DFS positions of each trie [R+1]
+  // parent or -1) as int4, and the units of the level-by-level launch (see
+  // tree_plan::gdn_units) as int4
   const int32_t* seg_table = nullptr;
-  const int32_t* trie_seg_ptr = nullptr;
-  const int32_t* trie_order = nullptr;  // [R] tries by descending token count
+  const int32_t* gdn_units = nullptr;
 };
 
 // Tables of the tree-correct causal conv for one kernel size (conv.cu): the
@@ -80,6 +80,14 @@ struct tree_plan {
   int64_t past_visible = 0;  // of which visible
   std::vector<std::pair<int32_t, int32_t>> gw_runs;  // visible gateway key runs [a, b)
   std::vector<int32_t> field[TREE_FIELD_COUNT];
+  // GDN state routing, one launch per level: a unit is a maximal chain of
+  // segments each the only child of the one before (consecutive in DFS
+  // order), as (first DFS position, end position, first token, end token);
+  // roots' units are level 0 and a unit's level is one more than its
+  // parent's. Units are ordered by level, then by tokens (most first);
+  // gdn_level_ptr[l] .. gdn_level_ptr[l+1] are level l's.
+  std::vector<int32_t> gdn_units;
+  std::vector<int32_t> gdn_level_ptr;
   treeattn::DevicePlan dev;
   treeattn::ConvTables conv;
 };
