@@ -108,3 +108,22 @@ def test_weighted_ce_sampled_rows_on_the_grpo_workload():
     loss, row_loss, _ = _check(z, tokens, lam, w.parents, w.lengths, 1.0, rows=rows)
     # the total is the fixed-order sum of the row losses
     assert abs(float(loss) - float(row_loss.double().sum())) <= 1e-6 * max(1.0, abs(float(loss)))
+
+
+@pytest.mark.parametrize("V,dtype", [(8, torch.bfloat16), (151936, torch.bfloat16),
+                                     (151936, torch.float32), (262144, torch.float32)])
+def test_weighted_ce_short_and_long_rows(V, dtype):
+    """The smallest vocabulary (8) and long rows (bf16 and fp32 V = 151,936, fp32
+    V = 262,144: a 1 MB row, far past what the kernel's second pass finds in
+    L2): every row against the oracle, and a second call bit for bit the same."""
+    _need_gpu()
+    parents, lengths = treegen.tiny_trie(2)
+    z, tokens, lam = _inputs(parents, lengths, V, dtype, 17, lam_kind="any")
+    _check(z, tokens, lam, parents, lengths, 0.5)
+    plan = tpa.tree_plan_build(parents, lengths)
+    zd, td, ld = z.cuda(), tokens.cuda(), lam.cuda()
+    a = tpa.tree_weighted_ce(plan, zd, td, ld, grad_scale=0.5)
+    b = tpa.tree_weighted_ce(plan, zd, td, ld, grad_scale=0.5)
+    tpa.tree_status_sync()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
