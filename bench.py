@@ -513,16 +513,14 @@ def rope_arm(args):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     nbytes = 2 * (q.numel() + k.numel()) * q.element_size()  # read and write each element once
     for _ in range(args.warmup):
-        tpa.tree_rope(plan, q)
-        tpa.tree_rope(plan, k)
+        tpa.tree_rope_qk(plan, q, k)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(0) as clocks:
         for a, b in ev:
             flush.zero_()
             a.record(stream)
-            tpa.tree_rope(plan, q)
-            tpa.tree_rope(plan, k)
+            tpa.tree_rope_qk(plan, q, k)  # q and k in one launch
             b.record(stream)
         torch.cuda.synchronize()
     tpa.tree_status_sync()
@@ -540,8 +538,8 @@ def rope_arm(args):
                    "l2": "inputs larger than L2, and L2 flushed between steps"},
         "roofline": {"bound": "hbm", "kernel": "tree_rope_kernel", "achieved": gbs, "peak": peak,
                      "unit": "GB/s", "frac": gbs / peak, "peak_source": f"{kind} copy bandwidth",
-                     "traffic": traffic},  # the step's two launches together
-        "bytes_per_step": nbytes, "clocks": clocks.summary(), "gpu_launches": 2 * args.steps,
+                     "traffic": traffic},  # the step's one launch (q and k)
+        "bytes_per_step": nbytes, "clocks": clocks.summary(), "gpu_launches": args.steps,
     }))
 
 

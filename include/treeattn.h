@@ -414,6 +414,15 @@ tree_status_t tree_rope(const tree_plan_t* plan, void* x, int32_t heads, int32_t
                         tree_dtype_t dtype, float base, int32_t rotate_half, int32_t inverse,
                         tree_stream_t stream);
 
+/* tree_rope on a layer's queries and keys in one launch: q device [N, q_heads,
+ * head_dim] and k device [N, k_heads, head_dim] of the same dtype, each
+ * rotated in place exactly as tree_rope would (bit for bit), with each
+ * token's sines and cosines computed once for both. Errors as tree_rope, and
+ * NULL k, k_heads <= 0 or q and k sharing an element -> TREE_ERR_INVALID_ARG. */
+tree_status_t tree_rope_qk(const tree_plan_t* plan, void* q, int32_t q_heads, void* k,
+                           int32_t k_heads, int32_t head_dim, tree_dtype_t dtype, float base,
+                           int32_t rotate_half, int32_t inverse, tree_stream_t stream);
+
 /* Fused weighted next-token cross-entropy over the trie, loss and gradient in
  * one pass ("Tree Training" §3.1 eq. 3-5: the tree loss is sum_t lambda_t *
  * l_t over unique tokens; §3.2 "Loss Weights").

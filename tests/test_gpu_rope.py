@@ -97,3 +97,25 @@ def test_rope_inverse_round_trip_and_autograd():
     ref = R.rope(gy.double().cpu().numpy(), pos, 10000.0, True, inverse=True)
     _check(xr.grad, ref, torch.float32, "grad")
     assert torch.equal(x, xr.detach())  # the input is not modified in place
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("rotate_half", [False, True])
+@pytest.mark.parametrize("D", [128, 40])
+def test_rope_qk_equals_two_calls(dtype, rotate_half, D):
+    """tree_rope_qk rotates q and k in one launch exactly as two tree_rope calls
+    (D = 128: the 16-byte chunk path; D = 40: the per-pair path), forward and
+    inverse."""
+    _need_gpu()
+    parents, lengths = treegen.grpo_tree(1, prompt=150, n_leaves=3, lo=20, hi=90)
+    plan = tpa.tree_plan_build(parents, lengths)
+    N = plan.num_tokens
+    for inverse in (False, True):
+        q = _draw(N, 6, D, dtype, 1).cuda()
+        k = _draw(N, 2, D, dtype, 2).cuda()
+        q1, k1 = q.clone(), k.clone()
+        tpa.tree_rope(plan, q1, rotate_half=rotate_half, inverse=inverse)
+        tpa.tree_rope(plan, k1, rotate_half=rotate_half, inverse=inverse)
+        tpa.tree_rope_qk(plan, q, k, rotate_half=rotate_half, inverse=inverse)
+        tpa.tree_status_sync()
+        assert torch.equal(q, q1) and torch.equal(k, k1)

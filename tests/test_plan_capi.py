@@ -197,6 +197,15 @@ def test_path_weights_and_rope_validate_their_arguments():
     assert lib.tree_rope(plan.handle, None, 2, 64, 1, float("inf"), 0, 0, None) == 1
     assert lib.tree_rope(plan.handle, None, 2, 64, 1, 10000.0, 2, 0, None) == 1  # rotate_half
     assert lib.tree_rope(plan.handle, None, 2, 64, 1, 10000.0, 0, 3, None) == 1  # inverse
+    # tree_rope_qk: a missing or overlapping second tensor is refused before any
+    # device use (host buffers stand in for the tensors; the plan is not uploaded,
+    # so a call that got past these checks would stop at TREE_ERR_NOT_ON_DEVICE)
+    buf = np.zeros(plan.info["num_tokens"] * 4 * 64 + 64, dtype=np.float32)
+    a0 = buf.ctypes.data
+    assert lib.tree_rope_qk(plan.handle, a0, 2, None, 2, 64, 0, 10000.0, 0, 0, None) == 1
+    assert lib.tree_rope_qk(plan.handle, a0, 2, a0 + 64, 2, 64, 0, 10000.0, 0, 0, None) == 1
+    assert b"overlap" in lib.tree_last_error()
+    assert lib.tree_rope_qk(plan.handle, a0, 2, a0, 0, 64, 0, 10000.0, 0, 0, None) == 1  # heads
     assert lib.tree_rope(plan.handle, None, 2, 64, 1, 10000.0, 0, 0, None) == 1  # NULL x
     assert lib.tree_rope(plan.handle, 20, 2, 64, 1, 10000.0, 0, 0, None) == 1  # misaligned
 

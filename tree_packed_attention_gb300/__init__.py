@@ -27,7 +27,7 @@ __all__ = [
     "Plan", "tree_plan_build", "tree_plan_build_partition", "tree_attn_fwd_gateway",
     "tree_attn_bwd_gateway", "tree_attn_fwd", "tree_attn_bwd", "tree_attn_bwd_dq",
     "tree_attn_bwd_dkdv", "tree_attn_bwd_workspace_bytes",
-    "tree_weights", "tree_weights_paths", "tree_partition", "tree_rope", "tree_rope_apply",
+    "tree_weights", "tree_weights_paths", "tree_partition", "tree_rope", "tree_rope_qk", "tree_rope_apply",
     "TreeRopeFn", "tree_conv_fwd", "tree_conv_bwd", "tree_conv", "TreeConvFn",
     "tree_weighted_ce", "tree_gdn_fwd", "tree_status_sync", "TreeAttnFn", "tree_attention", "TreeAttnError",
     "FIELDS", "EXPORTS", "LIB_PATH",
@@ -427,6 +427,27 @@ def tree_rope(plan: Plan, x, base: float = 10000.0, rotate_half: bool = False,
     check(lib.tree_rope(plan.handle, x.data_ptr(), x.shape[1], x.shape[2], _dtype_code(x),
                         float(base), int(bool(rotate_half)), int(bool(inverse)), s))
     return x
+
+
+def tree_rope_qk(plan: Plan, q, k, base: float = 10000.0, rotate_half: bool = False,
+                 inverse: bool = False, stream=None):
+    """tree_rope on q [N, Hq, D] and k [N, Hk, D] (same dtype) in one launch, in
+    place, bit for bit as two tree_rope calls; returns (q, k)."""
+    import torch
+
+    for name, x in (("q", q), ("k", k)):
+        if x.dim() != 3 or x.shape[0] != plan.num_tokens:
+            raise ValueError(f"{name} must be [N={plan.num_tokens}, H, D], got {tuple(x.shape)}")
+        if x.dtype not in (torch.bfloat16, torch.float32):
+            raise TypeError(f"{name} must be bf16 or fp32, got {x.dtype}")
+        _check_tensor(name, x, tuple(x.shape), q.dtype)
+    if k.shape[2] != q.shape[2]:
+        raise ValueError(f"q and k head_dim differ: {q.shape[2]} and {k.shape[2]}")
+    s = _stream_ptr(stream)
+    plan.to_device(s)
+    check(lib.tree_rope_qk(plan.handle, q.data_ptr(), q.shape[1], k.data_ptr(), k.shape[1], q.shape[2],
+                           _dtype_code(q), float(base), int(bool(rotate_half)), int(bool(inverse)), s))
+    return q, k
 
 
 def tree_weighted_ce(plan: Plan, logits, tokens, lam, grad_scale: float = 1.0, in_place: bool = False,

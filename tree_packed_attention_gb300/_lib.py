@@ -40,7 +40,7 @@ EXPORTS = [
     "tree_plan_to_device", "tree_plan_destroy", "tree_attn_fwd", "tree_attn_bwd_workspace_bytes",
     "tree_attn_bwd", "tree_attn_bwd_dq", "tree_attn_bwd_dkdv", "tree_attn_bwd_static_scratch",
     "tree_weights", "tree_weights_paths", "tree_partition", "tree_conv_prepare", "tree_conv_fwd",
-    "tree_conv_bwd_workspace_bytes", "tree_conv_bwd", "tree_rope", "tree_status_sync",
+    "tree_conv_bwd_workspace_bytes", "tree_conv_bwd", "tree_rope", "tree_rope_qk", "tree_status_sync",
     "tree_last_error", "tree_plan_build_partition", "tree_attn_fwd_gateway", "tree_attn_bwd_gateway",
     "tree_weighted_ce", "tree_gdn_fwd",
 ]
@@ -93,6 +93,7 @@ def _load():
         "tree_weights_paths": (i32, [vp, vp, i32, vp]),
         "tree_partition": (i32, [vp, i64, vp, vp, C.POINTER(i32), C.POINTER(i64)]),
         "tree_rope": (i32, [vp, vp, i32, i32, i32, C.c_float, i32, i32, vp]),
+        "tree_rope_qk": (i32, [vp, vp, i32, vp, i32, i32, i32, C.c_float, i32, i32, vp]),
         "tree_conv_prepare": (i32, [vp, i32, vp]),
         "tree_conv_fwd": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, vp]),
         "tree_conv_bwd_workspace_bytes": (sz, [vp, i32]),

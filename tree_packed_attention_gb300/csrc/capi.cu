@@ -345,11 +345,13 @@ extern "C" tree_status_t tree_gdn_fwd(const tree_plan_t* p, const void* q, const
   return TREE_OK;
 }
 
-extern "C" tree_status_t tree_rope(const tree_plan_t* p, void* x, int32_t heads, int32_t head_dim,
-                                   tree_dtype_t dtype, float base, int32_t rotate_half,
-                                   int32_t inverse, tree_stream_t stream) {
+namespace {
+
+tree_status_t rope_entry(const tree_plan_t* p, void* x, int32_t heads, void* x2, int32_t heads2,
+                         int32_t head_dim, tree_dtype_t dtype, float base, int32_t rotate_half,
+                         int32_t inverse, tree_stream_t stream) {
   if (!p) return fail(TREE_ERR_INVALID_ARG, "NULL plan");
-  if (heads <= 0) return fail(TREE_ERR_INVALID_ARG, "heads must be positive");
+  if (heads <= 0 || (x2 && heads2 <= 0)) return fail(TREE_ERR_INVALID_ARG, "heads must be positive");
   if (!rope_shape_ok(head_dim))
     return fail(TREE_ERR_UNSUPPORTED, "head_dim must be even and at most 128");
   if (dtype != TREE_DTYPE_BF16 && dtype != TREE_DTYPE_F32)
@@ -359,16 +361,40 @@ extern "C" tree_status_t tree_rope(const tree_plan_t* p, void* x, int32_t heads,
     return fail(TREE_ERR_INVALID_ARG, "rotate_half and inverse must be 0 or 1");
   if (p->N == 0) return TREE_OK;
   if (!x) return fail(TREE_ERR_INVALID_ARG, "NULL tensor pointer");
-  if (!aligned16(x)) return fail(TREE_ERR_INVALID_ARG, "tensor pointer must be 16-byte aligned");
-  if (static_cast<int64_t>(p->N) * heads * head_dim > (int64_t{1} << 40))
+  if (!aligned16(x) || (x2 && !aligned16(x2)))
+    return fail(TREE_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  const size_t elem = dtype == TREE_DTYPE_F32 ? 4 : 2;
+  if (static_cast<int64_t>(p->N) * heads * head_dim > (int64_t{1} << 40) ||
+      (x2 && static_cast<int64_t>(p->N) * heads2 * head_dim > (int64_t{1} << 40)))
     return fail(TREE_ERR_OVERFLOW, "tensor too large");
+  if (x2) {  // the two tensors must not share an element
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(x), a1 = a0 + static_cast<size_t>(p->N) * heads * head_dim * elem;
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(x2), b1 = b0 + static_cast<size_t>(p->N) * heads2 * head_dim * elem;
+    if (a0 < b1 && b0 < a1) return fail(TREE_ERR_INVALID_ARG, "the two tensors overlap");
+  }
   tree_status_t st = check_plan_on_device(p);
   if (st != TREE_OK) return st;
-  RopeArgs a{p->dev.pos_id, x, p->N, heads, head_dim, rotate_half, inverse,
+  RopeArgs a{p->dev.pos_id, x, x2, p->N, heads, x2 ? heads2 : 0, head_dim, rotate_half, inverse,
              dtype == TREE_DTYPE_F32 ? 1 : 0, base, static_cast<cudaStream_t>(stream)};
   cudaError_t e = launch_rope(a);
   if (e != cudaSuccess) return cuda_fail(e, "tree_rope launch");
   return TREE_OK;
+}
+
+}  // namespace
+
+extern "C" tree_status_t tree_rope(const tree_plan_t* p, void* x, int32_t heads, int32_t head_dim,
+                                   tree_dtype_t dtype, float base, int32_t rotate_half,
+                                   int32_t inverse, tree_stream_t stream) {
+  return rope_entry(p, x, heads, nullptr, 0, head_dim, dtype, base, rotate_half, inverse, stream);
+}
+
+extern "C" tree_status_t tree_rope_qk(const tree_plan_t* p, void* q, int32_t q_heads, void* k,
+                                      int32_t k_heads, int32_t head_dim, tree_dtype_t dtype,
+                                      float base, int32_t rotate_half, int32_t inverse,
+                                      tree_stream_t stream) {
+  if (!k) return fail(TREE_ERR_INVALID_ARG, "NULL tensor pointer");
+  return rope_entry(p, q, q_heads, k, k_heads, head_dim, dtype, base, rotate_half, inverse, stream);
 }
 
 namespace {

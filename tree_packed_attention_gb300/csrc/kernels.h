@@ -15,7 +15,8 @@ SchedSlot* next_sched_slot();
 struct RopeArgs {
   const int32_t* pos;  // device [N]
   void* x;             // device [N, heads, head_dim]
-  int N, heads, head_dim, rotate_half, inverse, f32;
+  void* x2;            // device [N, heads2, head_dim] or nullptr: rotated in the same pass
+  int N, heads, heads2, head_dim, rotate_half, inverse, f32;
   float base;
   cudaStream_t stream;
 };

@@ -14,7 +14,7 @@
 // HBM bandwidth bounds it: rows move in 16-byte chunks and each token's sines
 // and cosines are computed once and shared by all its heads. The angle is
 // formed and reduced modulo 2 pi in fp64 (positions reach 10^5 radians at
-// theta_0 = 1, beyond fp32's resolution), then sincosf works on [0, 2 pi).
+// theta_0 = 1, beyond fp32's resolution), then sincosf works on about [0, 2 pi).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -31,7 +31,8 @@ constexpr int kRopeMaxPairs = 64;  // head_dim <= 128
 struct RopeParams {
   const int32_t* pos;  // [N] position ids (eq. 9)
   void* x;             // [N, H, D]
-  int N, H, D, rotate_half, f32;
+  void* x2;            // [N, H2, D] or nullptr (H2 = 0): the same tokens' second tensor
+  int N, H, H2, D, rotate_half, f32;
   float sign;          // +1 forward, -1 inverse
   double theta[kRopeMaxPairs];
 };
@@ -100,17 +101,24 @@ struct Raw8<float> {
   }
 };
 
+// The angle pos * theta_i reduced by a whole number of turns, in fp64. The
+// turn count comes from a multiply by 1 / (2 pi), not a division (fp64 runs
+// at a small fraction of the fp32 rate here): near a multiple of 2 pi it may
+// be one off, which leaves r just outside [0, 2 pi) and the same sine and
+// cosine.
 __device__ __forceinline__ void angle_sincos(const RopeParams& p, int32_t pos, int i, float& s, float& c) {
   const double two_pi = 6.283185307179586476925286766559;
+  const double inv_two_pi = 0.15915494309189533576888376337251;
   const double a = static_cast<double>(pos) * p.theta[i];
-  const float r = static_cast<float>(a - two_pi * floor(a / two_pi));  // [0, 2 pi)
+  const float r = static_cast<float>(fma(-two_pi, floor(a * inv_two_pi), a));
   sincosf(r, &s, &c);
   s *= p.sign;
 }
 
 // Vector path (head_dim a multiple of 16): a block takes kRopeTokens tokens at
 // a time, first fills a table of their sines and cosines in shared memory,
-// then streams their rows in 8-element chunks. Interleaved pairs: a chunk
+// then streams their rows (the heads of x, then those of x2) in 8-element
+// chunks. Interleaved pairs: a chunk
 // holds pairs 4q..4q+3. Split halves: a work unit is chunk q of the first
 // half and chunk q of the second (pairs 8q..8q+7).
 constexpr int kRopeTokens = 8;
@@ -124,6 +132,7 @@ __global__ void __launch_bounds__(kRopeThreads, 4) tree_rope_vec_kernel(const Ro
   const int pairs = p.D / 2;
   const int units_per_row = p.rotate_half ? p.D / 16 : p.D / 8;
   T* x = static_cast<T*>(p.x);
+  T* x2 = static_cast<T*>(p.x2);
   for (int t0 = blockIdx.x * kRopeTokens; t0 < p.N; t0 += gridDim.x * kRopeTokens) {
     __syncthreads();  // the previous tokens' table is no longer read
     for (int e = threadIdx.x; e < kRopeTokens * pairs; e += kRopeThreads) {
@@ -137,7 +146,18 @@ __global__ void __launch_bounds__(kRopeThreads, 4) tree_rope_vec_kernel(const Ro
     // kUnroll units per thread at a time, all loads issued before any use,
     // so enough bytes are in flight to cover the memory latency
     const int tokens_here = p.N - t0 < kRopeTokens ? p.N - t0 : kRopeTokens;
-    const int live = tokens_here * p.H * units_per_row;  // units are token-major
+    // units: those of x's rows (token-major), then those of x2's
+    const int live1 = tokens_here * p.H * units_per_row;
+    const int live = live1 + tokens_here * p.H2 * units_per_row;
+    // unit u's chunk q, its row, and the row's token within the table
+    auto locate = [&](int u, int& q, int& tt) -> T* {
+      const bool second = u >= live1;
+      const int uu = second ? u - live1 : u, H = second ? p.H2 : p.H;
+      q = uu % units_per_row;
+      const int rest = uu / units_per_row;  // row of the block's tokens, token-major
+      tt = rest / H;
+      return (second ? x2 : x) + (static_cast<size_t>(t0) * H + rest) * p.D;
+    };
     constexpr int kUnroll = rope_unroll<T>();
     for (int u0 = threadIdx.x; u0 < live; u0 += kRopeThreads * kUnroll) {
       Raw8<T> ra[kUnroll], rb[kUnroll];
@@ -145,8 +165,8 @@ __global__ void __launch_bounds__(kRopeThreads, 4) tree_rope_vec_kernel(const Ro
       for (int k = 0; k < kUnroll; ++k) {
         const int u = u0 + k * kRopeThreads;
         if (u >= live) continue;
-        const int q = u % units_per_row, rest = u / units_per_row;
-        const T* row = x + (static_cast<size_t>(t0) * p.H + rest) * p.D;
+        int q, tt;
+        const T* row = locate(u, q, tt);
         ra[k].load(row + 8 * q);
         if (p.rotate_half) rb[k].load(row + pairs + 8 * q);
       }
@@ -154,8 +174,8 @@ __global__ void __launch_bounds__(kRopeThreads, 4) tree_rope_vec_kernel(const Ro
       for (int k = 0; k < kUnroll; ++k) {
         const int u = u0 + k * kRopeThreads;
         if (u >= live) continue;
-        const int q = u % units_per_row, rest = u / units_per_row, tt = rest / p.H;
-        T* row = x + (static_cast<size_t>(t0) * p.H + rest) * p.D;
+        int q, tt;
+        T* row = locate(u, q, tt);
         float a[8];
         ra[k].widen(a);
         if (p.rotate_half) {
@@ -184,12 +204,13 @@ __global__ void __launch_bounds__(kRopeThreads) tree_rope_kernel(const RopeParam
   const int i = threadIdx.x % pairs, g = threadIdx.x / pairs;
   if (g >= groups) return;  // pairs that do not divide 256 leave a few threads idle
   T* x = static_cast<T*>(p.x);
+  T* x2 = static_cast<T*>(p.x2);
   for (int t = blockIdx.x; t < p.N; t += gridDim.x) {
     float s, c;
     angle_sincos(p, __ldg(p.pos + t), i, s, c);
-    T* row = x + static_cast<size_t>(t) * p.H * p.D;
-    for (int h = g; h < p.H; h += groups) {
-      T* e = row + static_cast<size_t>(h) * p.D;
+    for (int h = g; h < p.H + p.H2; h += groups) {
+      T* e = h < p.H ? x + (static_cast<size_t>(t) * p.H + h) * p.D
+                     : x2 + (static_cast<size_t>(t) * p.H2 + (h - p.H)) * p.D;
       T* ea = p.rotate_half ? e + i : e + 2 * i;
       T* eb = p.rotate_half ? e + i + pairs : e + 2 * i + 1;
       float va = ld(ea), vb = ld(eb);
@@ -208,8 +229,10 @@ cudaError_t launch_rope(const RopeArgs& a) {
   RopeParams p;
   p.pos = a.pos;
   p.x = a.x;
+  p.x2 = a.x2;
   p.N = a.N;
   p.H = a.heads;
+  p.H2 = a.x2 ? a.heads2 : 0;
   p.D = a.head_dim;
   p.rotate_half = a.rotate_half;
   p.f32 = a.f32;
