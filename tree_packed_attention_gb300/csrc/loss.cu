@@ -13,12 +13,14 @@
 // One CTA per logits row (persistent over rows). Pass 1 streams the row once
 // with 16-byte loads and keeps a running (max, sum of exponentials) per thread,
 // merged across the CTA; the row's predictions are then collected by walking
-// the children of r's segment; pass 2 streams the row again (it is still in
-// L2: two CTAs per SM keep about 2 x 152 rows in flight) and writes dz with the
-// targets' one-hot terms folded in, so each element is rounded once and dz may
+// the children of r's segment; pass 2 streams the row again, mostly from L2
+// (pass 1 loads with an evict-last policy; pass 2's loads and the dz stores
+// are marked as last uses, so the dz stream does not evict the rows; two CTAs
+// per SM keep about 2 x 152 rows in flight), and writes dz with the targets'
+// one-hot terms folded in, so each element is rounded once and dz may
 // overwrite z. The row losses are summed in a fixed order by a second kernel.
 //
-// HBM traffic per row: V elements read (pass 1; pass 2 hits L2) and V written.
+// HBM traffic per row: V elements read (pass 1; most of pass 2 hits L2) and V written.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -41,7 +43,21 @@ __device__ __forceinline__ float ex2f(float x) {
 }
 
 // 16 bytes of a row as floats: 8 bf16 or 4 fp32.
-__device__ __forceinline__ uint4 ld16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+// pass 1: keep the row in L2 for pass 2 (evict-last policy)
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint4 ld16_keep(const void* p, uint64_t pol) {
+  uint4 r;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(pol));
+  return r;
+}
+// pass 2: the row's last read, and dz, need not stay in L2
+__device__ __forceinline__ uint4 ld16_last(const void* p) { return __ldcs(reinterpret_cast<const uint4*>(p)); }
 
 template <typename T>
 struct Vec;
@@ -61,7 +77,7 @@ struct Vec<__nv_bfloat16> {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
       asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w[i]) : "f"(f[2 * i + 1]), "f"(f[2 * i]));
-    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    __stcs(reinterpret_cast<uint4*>(p), make_uint4(w[0], w[1], w[2], w[3]));
   }
   __device__ static float one(const __nv_bfloat16* p) { return __bfloat162float(p[0]); }
 };
@@ -75,7 +91,7 @@ struct Vec<float> {
     f[3] = __uint_as_float(u.w);
   }
   __device__ static void store(float* p, const float (&f)[4]) {
-    *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+    __stcs(reinterpret_cast<float4*>(p), make_float4(f[0], f[1], f[2], f[3]));
   }
   __device__ static float one(const float* p) { return p[0]; }
 };
@@ -111,6 +127,7 @@ __global__ void __launch_bounds__(kCeThreads, 2)
   __shared__ float s_lse, s_w;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int V = p.V;
+  const uint64_t keep = policy_evict_last();
   for (int r = blockIdx.x; r < p.N; r += gridDim.x) {
     const T* zr = z + static_cast<size_t>(r) * V;
     // ---- pass 1: running max and sum of exponentials
@@ -120,7 +137,7 @@ __global__ void __launch_bounds__(kCeThreads, 2)
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int v = v0 + u * kCeThreads * E;
-        if (v < V) raw[u] = ld16(zr + v);
+        if (v < V) raw[u] = ld16_keep(zr + v, keep);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -213,7 +230,7 @@ __global__ void __launch_bounds__(kCeThreads, 2)
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int v = v0 + u * kCeThreads * E;
-          if (v < V) raw[u] = ld16(zr + v);
+          if (v < V) raw[u] = ld16_last(zr + v);
         }
       }
 #pragma unroll
