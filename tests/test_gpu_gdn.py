@@ -84,3 +84,32 @@ def test_gdn_on_the_grpo_workload_trie():
     ro, rs = GD.tree_forward(q, k, v, g, beta, w.parents, w.lengths, s0)
     _close("o", o, ro, bf16_store=True)
     _close("segment states", states, rs)
+
+
+def test_gdn_reset_gates_and_many_branch_levels():
+    """Gates that wipe the state (g = -30: one step's decay below 2^-40, so the
+    kernel renormalises; g = -200: the decay underflows fp32 to 0, the state
+    is reset to k delta^T), on a single token, a heap-shaped tree and a spine
+    whose every segment branches (20 levels of branch points, one launch
+    each), against the oracle in fp64."""
+    _need_gpu()
+    rng = np.random.default_rng(5)
+    spine = [-1] + [2 * ((s - 1) // 2) for s in range(1, 41)]  # segment 2m: a leaf 2m+1 and 2m+2
+    cases = [([-1], [1]),
+             ([-1] + [(s - 1) // 2 for s in range(1, 31)], [int(x) for x in rng.integers(1, 4, 31)]),
+             (spine, [int(x) for x in rng.integers(1, 6, len(spine))])]
+    for n, (parents, lengths) in enumerate(cases):
+        N = int(np.sum(lengths))
+        q, k, v, g, beta, s0 = treegen.draw_gdn(N, 1, 2, 128, "fp32", 40 + n)
+        pick = torch.as_tensor(rng.random((N, 2)))
+        g = torch.where(pick < 0.15, torch.full_like(g, -30.0), g)
+        g = torch.where(pick > 0.9, torch.full_like(g, -200.0), g)
+        plan = tpa.tree_plan_build(parents, lengths)
+        if n == 2:
+            assert plan.info["gdn_levels"] >= 20
+        o, states = tpa.tree_gdn_fwd(plan, q.cuda(), k.cuda(), v.cuda(), g.cuda(), beta.cuda(), s0.cuda())
+        tpa.tree_status_sync()
+        ro, rs = GD.tree_forward(q, k, v, g, beta, parents, lengths, s0)
+        assert torch.isfinite(o).all() and torch.isfinite(states).all()
+        _close("o", o, ro)
+        _close("segment states", states, rs)

@@ -127,3 +127,23 @@ def test_weighted_ce_short_and_long_rows(V, dtype):
     tpa.tree_status_sync()
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_weighted_ce_extreme_and_flat_rows(dtype):
+    """Logits up to about 1e5 in magnitude (each row's softmax all but
+    one-hot, every other exponential underflowing), rows whose logits are
+    all equal (a uniform softmax), and rows with one spike of 3e4 over zeros,
+    with the g/K weights: against the oracle in fp64 at the same tolerances
+    as ordinary logits, since the kernel subtracts the row maximum before the
+    exponent (an error that grew with |z| would fail here)."""
+    _need_gpu()
+    parents, lengths = treegen.tiny_trie(1)
+    z, tokens, lam = _inputs(parents, lengths, 4096, torch.float32, 23)
+    z = z * 5e3
+    z[1::5] = 7.0
+    z[2::5] = 0.0
+    z[2::5, 11] = 3e4
+    z = z.to(dtype)
+    loss, row_loss, dz = _check(z, tokens, lam, parents, lengths, 1.0)
+    assert torch.isfinite(dz).all() and torch.isfinite(row_loss).all()

@@ -20,6 +20,10 @@
 // one-hot terms folded in, so each element is rounded once and dz may
 // overwrite z. The row losses are summed in a fixed order by a second kernel.
 //
+// Both passes form each exponent from z - max (exact near the max), so the
+// softmax's relative error does not grow with the logits' magnitude; the loss
+// takes (max - z_x) + ln(sum) without rounding lse itself.
+//
 // HBM traffic per row: V elements read (pass 1; most of pass 2 hits L2) and V written.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -124,7 +128,7 @@ __global__ void __launch_bounds__(kCeThreads, 2)
   __shared__ int tgt_x[kCeMaxTargets];
   __shared__ float tgt_w[kCeMaxTargets];
   __shared__ int s_ntgt;
-  __shared__ float s_lse, s_w;
+  __shared__ float s_m, s_l2, s_w;  // row max, log2 of the row's sum of 2^((z - max) log2e)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int V = p.V;
   const uint64_t keep = policy_evict_last();
@@ -152,9 +156,10 @@ __global__ void __launch_bounds__(kCeThreads, 2)
           s *= ex2f((m - vm) * kLog2e);
           m = vm;
         }
-        const float nm = -m * kLog2e;
+        // z - max first (exact near the max), so that the exponent's error
+        // does not grow with the logits' magnitude
 #pragma unroll
-        for (int e = 0; e < E; ++e) s += ex2f(fmaf(f[e], kLog2e, nm));
+        for (int e = 0; e < E; ++e) s += ex2f((f[e] - m) * kLog2e);
       }
     }
 #pragma unroll
@@ -178,7 +183,7 @@ __global__ void __launch_bounds__(kCeThreads, 2)
         merge(m, s, m2, s2);
       }
       if (lane == 0) {
-        const float lse = m + logf(s);
+        const float ls = logf(s);  // lse = m + ls, kept apart
         // ---- the predictions made from row r (successor walk, fixed order)
         float loss = 0.f, w_sum = 0.f;
         int nt = 0;
@@ -191,7 +196,7 @@ __global__ void __launch_bounds__(kCeThreads, 2)
           }
           const float w = p.lam[t];
           if (w == 0.f) return;
-          loss += w * (lse - Vec<T>::one(zr + x));
+          loss += w * ((m - Vec<T>::one(zr + x)) + ls);
           w_sum += w;
           for (int j = 0; j < nt; ++j)
             if (tgt_x[j] == x) {
@@ -215,14 +220,15 @@ __global__ void __launch_bounds__(kCeThreads, 2)
         }
         p.row_loss[r] = loss;
         s_ntgt = nt;
-        s_lse = lse;
+        s_m = m;
+        s_l2 = ls * kLog2e;
         s_w = w_sum;
       }
     }
     __syncthreads();
     // ---- pass 2: dz = gs * (W * softmax - one-hot terms)
     const int nt = s_ntgt;
-    const float a = p.gs * s_w, nl = -s_lse * kLog2e;
+    const float a = p.gs * s_w, mr = s_m, nl2 = -s_l2;
     T* dr = dz + static_cast<size_t>(r) * V;
     for (int v0 = tid * E; v0 < V; v0 += kCeThreads * E * U) {
       uint4 raw[U];
@@ -241,7 +247,7 @@ __global__ void __launch_bounds__(kCeThreads, 2)
         if (a != 0.f) {
           Vec<T>::unpack(raw[u], f);
 #pragma unroll
-          for (int e = 0; e < E; ++e) f[e] = a * ex2f(fmaf(f[e], kLog2e, nl));
+          for (int e = 0; e < E; ++e) f[e] = a * ex2f(fmaf(f[e] - mr, kLog2e, nl2));
         } else {
 #pragma unroll
           for (int e = 0; e < E; ++e) f[e] = 0.f;
