@@ -119,3 +119,26 @@ def test_rope_qk_equals_two_calls(dtype, rotate_half, D):
         tpa.tree_rope_qk(plan, q, k, rotate_half=rotate_half, inverse=inverse)
         tpa.tree_status_sync()
         assert torch.equal(q, q1) and torch.equal(k, k1)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_rope_at_positions_near_the_int32_limit(dtype):
+    """A partition plan whose positions start at the largest offset the plan
+    accepts (offset + N = 2^31 - 1): angles up to about 2.1e9 radians, formed
+    and reduced modulo 2 pi in fp64, rotate at the same tolerances as small
+    positions, in both pairings and both directions."""
+    _need_gpu()
+    w = treegen.workload(1, 0)
+    N = int(np.sum(w.lengths))
+    off = 2 ** 31 - 1 - N
+    plan = tpa.tree_plan_build_partition(w.parents, w.lengths, [], off)
+    pos = plan.field("pos_id").astype(np.int64)
+    assert pos.min() == off and pos.max() > 2 ** 31 - 1 - N // 2
+    assert np.array_equal(pos - off, np.asarray(T.position_ids(w.parents, w.lengths)))
+    x = _draw(N, 2, 128, dtype, 9)
+    for rotate_half in (False, True):
+        for inverse in (False, True):
+            got = tpa.tree_rope(plan, x.cuda(), 10000.0, rotate_half, inverse)
+            tpa.tree_status_sync()
+            ref = R.rope(x.double().numpy(), pos, 10000.0, rotate_half, inverse)
+            _check(got, ref, dtype, f"rotate_half={rotate_half} inverse={inverse}")
