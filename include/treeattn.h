@@ -488,10 +488,21 @@ tree_status_t tree_gdn_fwd(const tree_plan_t* plan, const void* q, const void* k
  * current device: TREE_ERR_TIMEOUT if a kernel gave up a bounded wait since
  * the last check (the message names the wait: 10000 + source line in the
  * forward kernel file, 20000 + line in the backward one, 30000 + warp for
- * the work ring, 40000 + line in the conv kernel file), TREE_ERR_INVALID_ARG
- * if tree_weighted_ce met a token id >= vocab, TREE_ERR_CUDA on a CUDA error,
- * else TREE_OK. */
+ * the work ring, 40000 + line in the conv kernel file, 50000 for
+ * tree_diag_wait_timeout), TREE_ERR_INVALID_ARG if tree_weighted_ce met a
+ * token id >= vocab, TREE_ERR_CUDA on a CUDA error, else TREE_OK. */
 tree_status_t tree_status_sync(tree_stream_t stream);
+
+/* Diagnostic of the failure path: launches one thread on `stream` that waits
+ * on an mbarrier nothing completes, through the bounded wait every kernel of
+ * the library uses, with a limit of limit_ns nanoseconds (1e3 to 1e10) of the
+ * GPU's global timer instead of the kernels' 4 s. The wait gives up, stores
+ * 50000 in the device status word and the kernel returns, leaving the context
+ * usable: the next tree_status_sync reports TREE_ERR_TIMEOUT naming wait site
+ * 50000 and clears the word. No fault, trap or hang is involved. Errors:
+ * limit_ns out of range -> TREE_ERR_INVALID_ARG (nothing is launched); a
+ * launch failure -> TREE_ERR_CUDA. */
+tree_status_t tree_diag_wait_timeout(int64_t limit_ns, tree_stream_t stream);
 
 /* Message for the last failing call on this thread ("" if none). */
 const char* tree_last_error(void);

@@ -269,3 +269,10 @@ def test_gdn_levels_count_branch_points_on_paths():
                 best = max(best, n + 1)
         plan = tpa.tree_plan_build(parents, lengths)
         assert plan.info["gdn_levels"] == best, (parents, lengths)
+
+
+def test_diagnostic_wait_checks_its_limit_before_any_launch():
+    # outside [1e3, 1e10] ns: refused on the host, nothing launched
+    for bad in (0, 999, -5, 10 ** 10 + 1):
+        assert tpa.lib.tree_diag_wait_timeout(bad, None) == 1
+        assert b"limit_ns" in tpa.lib.tree_last_error()

@@ -29,7 +29,7 @@ __all__ = [
     "tree_attn_bwd_dkdv", "tree_attn_bwd_workspace_bytes",
     "tree_weights", "tree_weights_paths", "tree_partition", "tree_rope", "tree_rope_qk", "tree_rope_apply",
     "TreeRopeFn", "tree_conv_fwd", "tree_conv_bwd", "tree_conv", "TreeConvFn",
-    "tree_weighted_ce", "tree_gdn_fwd", "tree_status_sync", "TreeAttnFn", "tree_attention", "TreeAttnError",
+    "tree_weighted_ce", "tree_gdn_fwd", "tree_status_sync", "tree_diag_wait_timeout", "TreeAttnFn", "tree_attention", "TreeAttnError",
     "FIELDS", "EXPORTS", "LIB_PATH",
 ]
 
@@ -520,6 +520,12 @@ def tree_gdn_fwd(plan: Plan, q, k, v, g, beta, initial_state=None, stream=None):
 def tree_status_sync(stream=None) -> None:
     """Wait for the stream; raise if a kernel gave up a bounded wait."""
     check(lib.tree_status_sync(_stream_ptr(stream)))
+
+
+def tree_diag_wait_timeout(limit_ns: int = 20_000_000, stream=None) -> None:
+    """Launch the diagnostic wait that gives up after ``limit_ns``; the next
+    ``tree_status_sync`` raises TREE_ERR_TIMEOUT naming wait site 50000."""
+    check(lib.tree_diag_wait_timeout(int(limit_ns), _stream_ptr(stream)))
 
 
 def _make_autograd():

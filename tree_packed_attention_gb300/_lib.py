@@ -42,7 +42,7 @@ EXPORTS = [
     "tree_weights", "tree_weights_paths", "tree_partition", "tree_conv_prepare", "tree_conv_fwd",
     "tree_conv_bwd_workspace_bytes", "tree_conv_bwd", "tree_rope", "tree_rope_qk", "tree_status_sync",
     "tree_last_error", "tree_plan_build_partition", "tree_attn_fwd_gateway", "tree_attn_bwd_gateway",
-    "tree_weighted_ce", "tree_gdn_fwd",
+    "tree_weighted_ce", "tree_gdn_fwd", "tree_diag_wait_timeout",
 ]
 
 
@@ -99,6 +99,7 @@ def _load():
         "tree_conv_bwd_workspace_bytes": (sz, [vp, i32]),
         "tree_conv_bwd": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, sz, vp]),
         "tree_status_sync": (i32, [vp]),
+        "tree_diag_wait_timeout": (i32, [C.c_int64, vp]),
         "tree_last_error": (C.c_char_p, []),
         "tree_plan_build_partition": (i32, [vp, vp, i32, vp, i32, i32, C.POINTER(vp)]),
         "tree_attn_fwd_gateway": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, C.c_float,

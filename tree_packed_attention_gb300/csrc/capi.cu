@@ -608,6 +608,36 @@ extern "C" tree_status_t tree_attn_bwd_dkdv(const tree_plan_t* p, const void* do
                    grad_dtype, softmax_scale, workspace, workspace_bytes, stream, 2);
 }
 
+namespace treeattn {
+namespace {
+
+// One thread waits on an mbarrier that nothing completes, through the same
+// bounded wait as every kernel of the library, so that the wait gives up after
+// limit_ns, stores kSiteDiag in the status word and the kernel returns.
+__global__ void diag_wait_kernel(int* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_s;
+  dev::mbar_init(&bar, 1);
+  abort_s = 0;
+  dev::fence_mbar_init();
+  dev::mbar_wait(&bar, 0, &abort_s, status, dev::kSiteDiag, limit_ns);
+}
+
+}  // namespace
+}  // namespace treeattn
+
+extern "C" tree_status_t tree_diag_wait_timeout(int64_t limit_ns, tree_stream_t stream) {
+  if (limit_ns < 1000 || limit_ns > 10000000000ll)
+    return fail(TREE_ERR_INVALID_ARG, "limit_ns outside [1e3, 1e10]");
+  int* st = status_ptr();
+  if (!st) return fail(TREE_ERR_CUDA, "status word address");
+  diag_wait_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(st, static_cast<uint64_t>(limit_ns));
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "diagnostic wait launch");
+  set_error("");
+  return TREE_OK;
+}
+
 extern "C" tree_status_t tree_status_sync(tree_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");

@@ -12,12 +12,11 @@
 namespace treeattn {
 namespace dev {
 
-// Status word values (a kernel that gives up a wait stores one of these).
-constexpr int kStatusTimeout = 7;
-// A wait that gives up stores a code naming where it waited instead:
-// kSiteFwd / kSiteBwd + the source line of the wait in that kernel's file,
-// or kSiteRing + the warp for the work ring.
-constexpr int kSiteFwd = 10000, kSiteBwd = 20000, kSiteRing = 30000;
+// A wait that gives up stores a code naming where it waited in the device
+// status word: kSiteFwd / kSiteBwd + the source line of the wait in that
+// kernel's file, kSiteRing + the warp for the work ring, kSiteDiag for the
+// diagnostic wait that nothing completes.
+constexpr int kSiteFwd = 10000, kSiteBwd = 20000, kSiteRing = 30000, kSiteDiag = 50000;
 
 // A bounded wait gives up after this long (ns of %globaltimer).
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
@@ -63,17 +62,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity to complete. Gives up
-// (returns false) after kWaitLimitNs or once *abort is set by another thread;
-// on a timeout it sets *abort and the device status word.
+// (returns false) after limit_ns or once *abort is set by another thread; on
+// a timeout it sets *abort and stores `site` in the device status word.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          int* status, int site = kStatusTimeout) {
+                                          int* status, int site, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort = 1;
         if (status) atomicExch(status, site);
         return false;
