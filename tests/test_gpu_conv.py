@@ -44,7 +44,7 @@ def _cmp(got, ref, dtype, name, scale=None):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("K", [1, 2, 4, 8])
+@pytest.mark.parametrize("K", [1, 2, 4, 6, 8])
 def test_conv_forward_and_backward_match_oracle(dtype, K):
     _need_gpu()
     rng = np.random.default_rng(K)

@@ -49,12 +49,14 @@ template <typename T, int V>
 struct Vec;
 template <int V>
 struct Vec<__nv_bfloat16, V> {
-  static_assert(V == 4 || V == 8, "4 or 8 channels");
+  static_assert(V == 2 || V == 4 || V == 8, "2, 4 or 8 channels");
   static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&v)[V]) {
     uint32_t w[V / 2];
     if constexpr (V == 8) {
       const uint4 u = *reinterpret_cast<const uint4*>(p);
       w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+    } else if constexpr (V == 2) {
+      w[0] = *reinterpret_cast<const uint32_t*>(p);
     } else {
       const uint2 u = *reinterpret_cast<const uint2*>(p);
       w[0] = u.x; w[1] = u.y;
@@ -75,14 +77,22 @@ struct Vec<__nv_bfloat16, V> {
     }
     if constexpr (V == 8)
       *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    else if constexpr (V == 2)
+      *reinterpret_cast<uint32_t*>(p) = w[0];
     else
       *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
   }
 };
 template <int V>
 struct Vec<float, V> {
-  static_assert(V == 4 || V == 8, "4 or 8 channels");
+  static_assert(V == 2 || V == 4 || V == 8, "2, 4 or 8 channels");
   static __device__ __forceinline__ void load(const float* p, float (&v)[V]) {
+    if constexpr (V == 2) {
+      const float2 a = *reinterpret_cast<const float2*>(p);
+      v[0] = a.x;
+      v[1] = a.y;
+      return;
+    }
 #pragma unroll
     for (int h = 0; h < V / 4; ++h) {
       const float4 a = reinterpret_cast<const float4*>(p)[h];
@@ -90,6 +100,10 @@ struct Vec<float, V> {
     }
   }
   static __device__ __forceinline__ void store(float* p, const float (&v)[V]) {
+    if constexpr (V == 2) {
+      *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+      return;
+    }
 #pragma unroll
     for (int h = 0; h < V / 4; ++h)
       reinterpret_cast<float4*>(p)[h] = make_float4(v[4 * h], v[4 * h + 1], v[4 * h + 2], v[4 * h + 3]);
@@ -189,7 +203,10 @@ __device__ __forceinline__ void token_range(const ConvArgs& a, int& t0, int& t1)
 template <typename T, int NT, int V = 8>
 struct Stage {
   static constexpr uint32_t kStride = kConvThreads * V * sizeof(T);  // smem bytes per token row
-  static constexpr int kBatch = static_cast<int>(kConvBatchBytes / kStride);
+  // tokens per batch: as many rows as kConvBatchBytes holds, at most 8
+  static constexpr int kBatch = static_cast<int>(kConvBatchBytes / kStride) < 8
+                                    ? static_cast<int>(kConvBatchBytes / kStride) : 8;
+  static constexpr uint32_t kBytes = kBatch * kStride;  // one tensor's batch buffer
   uint8_t* buf;
   uint64_t* bar;       // [kConvBufs]
   const T* src[NT];
@@ -205,11 +222,11 @@ struct Stage {
     for (int u = 0; u < n; ++u)
 #pragma unroll
       for (int k = 0; k < NT; ++k)
-        bulk_load(buf + (s * NT + k) * kConvBatchBytes + u * kStride,
+        bulk_load(buf + (s * NT + k) * kBytes + u * kStride,
                   src[k] + static_cast<size_t>(tb + u) * C + g0, row_bytes, b);
   }
   __device__ const uint8_t* row(int i, int k, int u) const {
-    return buf + ((i % kConvBufs) * NT + k) * kConvBatchBytes + u * kStride;
+    return buf + ((i % kConvBufs) * NT + k) * kBytes + u * kStride;
   }
 };
 
@@ -283,9 +300,13 @@ __global__ void __launch_bounds__(kConvThreads) conv_fwd_kernel(const ConvArgs a
     for (int k = i; k < nb && k < i + kConvBufs; ++k) mbar_drain(&bar[k % kConvBufs], (k / kConvBufs) & 1);
 }
 
-// Blocks per SM of the backward's walk: two for up to 5 taps at 4 channels a
-// thread (at most 128 registers, no spills); one otherwise.
-constexpr int conv_bwd_blocks_per_sm(int K, int V) { return V == 4 && K <= 5 ? 2 : 1; }
+// Blocks per SM of the backward's walk by registers: at 2 channels a thread
+// four for up to 4 taps (64 registers, no spills), three for 5 and 6 (at most
+// 85), two beyond; at 4 channels two for up to 5 taps; one otherwise. The
+// launch also caps it by shared memory (fp32 rows stage twice the bytes).
+constexpr int conv_bwd_blocks_per_sm(int K, int V) {
+  return V == 2 ? (K <= 4 ? 4 : K <= 6 ? 3 : 2) : (V == 4 && K <= 5 ? 2 : 1);
+}
 
 // The backward in one pass over each block's token range, in DFS order:
 //   g[t]  = dy[t] * act'(pre_t), from the window that the forward also walks;
@@ -654,11 +675,18 @@ cudaError_t smem_attr(F* kernel, uint32_t bytes, bool& done) {
 }
 
 constexpr uint32_t kFwdSmem = kConvBufs * kConvBatchBytes;      // x
-constexpr uint32_t kBwdSmem = kConvBufs * 2 * kConvBatchBytes;  // x and dy
-// Channels per thread in the backward's walk: 4, so that its per-thread state
-// (the window, the last K gradients, the dweight / dbias sums and the taps)
-// fits two 256-thread blocks per SM (for up to 5 taps).
-constexpr int kBwdChannels = 4;
+// Channels per thread in the backward's walk. Its per-thread state (the
+// window, the last K gradients, the dweight / dbias sums and the taps) at 4
+// channels fits two 256-thread blocks per SM up to 5 taps; beyond, 2 channels
+// keep two or three blocks per SM where 4 would leave one (6 taps: 1.90 ->
+// 1.66 ms on 131k tokens x 4096 channels). Up to 5 taps 4 channels are faster
+// than 2 (4 taps: 1.07 against 1.29 ms), as a thread's per-token overhead
+// then covers twice the channels.
+constexpr int bwd_channels(int K) { return K <= 5 ? 4 : 2; }
+template <typename T, int V>
+constexpr uint32_t bwd_smem() {  // x and dy
+  return kConvBufs * 2 * Stage<T, 2, V>::kBytes;
+}
 
 template <int K>
 cudaError_t conv_fwd_k(const ConvArgs& a, dim3 grid) {
@@ -670,27 +698,6 @@ cudaError_t conv_fwd_k(const ConvArgs& a, dim3 grid) {
   } else {
     if ((e = smem_attr(conv_fwd_kernel<__nv_bfloat16, K>, kFwdSmem, done[0])) != cudaSuccess) return e;
     conv_fwd_kernel<__nv_bfloat16, K><<<grid, kConvThreads, kFwdSmem, a.stream>>>(a);
-  }
-  return cudaGetLastError();
-}
-
-template <int K>
-cudaError_t conv_bwd_k(const ConvArgs& a, dim3 grid, dim3 pgrid) {
-  static bool done[2] = {false, false};
-  const dim3 igrid(a.num_irr < 1024 ? (a.num_irr > 0 ? a.num_irr : 1) : 1024, grid.y);
-  cudaError_t e;
-  if (a.f32) {
-    if ((e = smem_attr(conv_bwd_fused_kernel<float, K, kBwdChannels>, kBwdSmem, done[1])) != cudaSuccess)
-      return e;
-    conv_bwd_fused_kernel<float, K, kBwdChannels><<<pgrid, kConvThreads, kBwdSmem, a.stream>>>(a);
-    if (a.num_irr > 0) conv_bwd_dx_irregular_kernel<float, K><<<igrid, kConvThreads, 0, a.stream>>>(a);
-  } else {
-    if ((e = smem_attr(conv_bwd_fused_kernel<__nv_bfloat16, K, kBwdChannels>, kBwdSmem, done[0])) !=
-        cudaSuccess)
-      return e;
-    conv_bwd_fused_kernel<__nv_bfloat16, K, kBwdChannels><<<pgrid, kConvThreads, kBwdSmem, a.stream>>>(a);
-    if (a.num_irr > 0)
-      conv_bwd_dx_irregular_kernel<__nv_bfloat16, K><<<igrid, kConvThreads, 0, a.stream>>>(a);
   }
   return cudaGetLastError();
 }
@@ -707,6 +714,36 @@ dim3 conv_grid(const ConvArgs& a, int per_sm, int chans = 8) {
   int tx = sms * per_sm / groups;
   tx = tx < 1 ? 1 : (tx > a.N ? a.N : tx);
   return dim3(tx, groups);
+}
+
+// The walk over token ranges, then dx of the irregular tokens; *pblocks
+// gets the token ranges (blocks along x), whose dweight / dbias partial sums
+// the reduce kernel adds.
+template <int K>
+cudaError_t conv_bwd_k(const ConvArgs& a, dim3 grid, int* pblocks) {
+  constexpr int V = bwd_channels(K);
+  static bool done[2] = {false, false};
+  // blocks per SM: by registers, and by shared memory (228 KB per SM, 1 KB of
+  // it reserved per block)
+  const uint32_t smem = a.f32 ? bwd_smem<float, V>() : bwd_smem<__nv_bfloat16, V>();
+  const int by_smem = static_cast<int>(233472u / (smem + 1024u));
+  const int by_regs = conv_bwd_blocks_per_sm(K, V);
+  const dim3 pgrid = conv_grid(a, by_regs < by_smem ? by_regs : by_smem, V);
+  *pblocks = static_cast<int>(pgrid.x) < kConvPartialBlocks ? static_cast<int>(pgrid.x) : kConvPartialBlocks;
+  const dim3 pg(*pblocks, pgrid.y);
+  const dim3 igrid(a.num_irr < 1024 ? (a.num_irr > 0 ? a.num_irr : 1) : 1024, grid.y);
+  cudaError_t e;
+  if (a.f32) {
+    if ((e = smem_attr(conv_bwd_fused_kernel<float, K, V>, smem, done[1])) != cudaSuccess) return e;
+    conv_bwd_fused_kernel<float, K, V><<<pg, kConvThreads, smem, a.stream>>>(a);
+    if (a.num_irr > 0) conv_bwd_dx_irregular_kernel<float, K><<<igrid, kConvThreads, 0, a.stream>>>(a);
+  } else {
+    if ((e = smem_attr(conv_bwd_fused_kernel<__nv_bfloat16, K, V>, smem, done[0])) != cudaSuccess) return e;
+    conv_bwd_fused_kernel<__nv_bfloat16, K, V><<<pg, kConvThreads, smem, a.stream>>>(a);
+    if (a.num_irr > 0)
+      conv_bwd_dx_irregular_kernel<__nv_bfloat16, K><<<igrid, kConvThreads, 0, a.stream>>>(a);
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t launch_conv_fwd(const ConvArgs& a) {
@@ -726,20 +763,17 @@ cudaError_t launch_conv_fwd(const ConvArgs& a) {
 
 cudaError_t launch_conv_bwd(ConvArgs a) {
   const dim3 grid = conv_grid(a, 8);  // the irregular tokens' gather
-  const dim3 pgrid = conv_grid(a, a.K <= 5 ? 2 : 1, kBwdChannels);
-  const int pblocks = static_cast<int>(pgrid.x) < kConvPartialBlocks ? static_cast<int>(pgrid.x)
-                                                                     : kConvPartialBlocks;
-  const dim3 pg(pblocks, pgrid.y);
+  int pblocks = 0;
   cudaError_t e;
   switch (a.K) {
-    case 1: e = conv_bwd_k<1>(a, grid, pg); break;
-    case 2: e = conv_bwd_k<2>(a, grid, pg); break;
-    case 3: e = conv_bwd_k<3>(a, grid, pg); break;
-    case 4: e = conv_bwd_k<4>(a, grid, pg); break;
-    case 5: e = conv_bwd_k<5>(a, grid, pg); break;
-    case 6: e = conv_bwd_k<6>(a, grid, pg); break;
-    case 7: e = conv_bwd_k<7>(a, grid, pg); break;
-    case 8: e = conv_bwd_k<8>(a, grid, pg); break;
+    case 1: e = conv_bwd_k<1>(a, grid, &pblocks); break;
+    case 2: e = conv_bwd_k<2>(a, grid, &pblocks); break;
+    case 3: e = conv_bwd_k<3>(a, grid, &pblocks); break;
+    case 4: e = conv_bwd_k<4>(a, grid, &pblocks); break;
+    case 5: e = conv_bwd_k<5>(a, grid, &pblocks); break;
+    case 6: e = conv_bwd_k<6>(a, grid, &pblocks); break;
+    case 7: e = conv_bwd_k<7>(a, grid, &pblocks); break;
+    case 8: e = conv_bwd_k<8>(a, grid, &pblocks); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
