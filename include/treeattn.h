@@ -18,6 +18,13 @@
  *  - Streams: calls that take a stream enqueue work on it and return
  *    without waiting (stream-ordered). `stream` is a cudaStream_t passed as
  *    void* (NULL = the legacy default stream).
+ *  - Concurrency: the attention kernels hand out their work items from a
+ *    counter of a library-owned ring of 1024, one per launch in turn, which
+ *    the launch's last block puts back to zero. Launches may overlap on
+ *    different streams as long as fewer than 1024 are in flight at once. A
+ *    launch captured in a CUDA graph keeps the counter it was given, so
+ *    replays of one graph must not overlap one another (replays one after
+ *    another on a stream are fine).
  *  - Tensor layout: token-major, contiguous, in DFS order. q and o are
  *    [N, hq, D]; k and v are [N, hkv, D]; lse is [hq, N] fp32, natural log.
  *    Segment s occupies tokens [seg_start[s], seg_start[s] + lengths[s]).
