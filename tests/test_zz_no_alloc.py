@@ -61,3 +61,37 @@ def test_static_scratch_rejects_oversized_requests():
                                               DTYPE_BF16, 0.0, None)
     assert tpa._lib.STATUS_NAMES[st] == "TREE_ERR_UNSUPPORTED"
     assert b"scratch" in tpa.lib.tree_last_error()
+
+
+def test_static_scratch_at_its_size_limit():
+    """The packed 131,072-token workload with 64 q heads needs exactly
+    TREE_STATIC_SCRATCH_BYTES (two rows of 64 x 131,072 fp32): the largest
+    request the entry point takes runs bit for bit as tree_attn_bwd, and the
+    same trie with one token more is refused before any launch."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    w = treegen.workload(5)
+    plan = tpa.tree_plan_build(w.parents, w.lengths)
+    N, hq, hkv, D = w.num_tokens, w.hq, w.hkv, w.head_dim
+    assert tpa.tree_attn_bwd_workspace_bytes(plan, hq, D, torch.bfloat16) == 64 << 20
+    g = torch.Generator(device="cuda").manual_seed(5)
+    q, do = (torch.randn(N, hq, D, device="cuda", generator=g).to(torch.bfloat16) for _ in range(2))
+    k, v = (torch.randn(N, hkv, D, device="cuda", generator=g).to(torch.bfloat16) for _ in range(2))
+    o, lse = tpa.tree_attn_fwd(plan, q, k, v)
+    ref = tpa.tree_attn_bwd(plan, do, q, k, v, o, lse)
+    got = [torch.full_like(x, float("nan")) for x in ref]
+    st = tpa.lib.tree_attn_bwd_static_scratch(
+        plan.handle, do.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+        lse.data_ptr(), got[0].data_ptr(), got[1].data_ptr(), got[2].data_ptr(), hq, hkv, D,
+        DTYPE_BF16, DTYPE_BF16, 0.0, _stream())
+    assert st == 0, tpa.lib.tree_last_error()
+    tpa.tree_status_sync()
+    for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+        assert torch.equal(a, b), name
+    lengths = np.array(w.lengths).copy()
+    lengths[0] += 1
+    bigger = tpa.tree_plan_build(w.parents, lengths)
+    st = tpa.lib.tree_attn_bwd_static_scratch(bigger.handle, None, None, None, None, None, None,
+                                              None, None, None, hq, hkv, D, DTYPE_BF16, DTYPE_BF16,
+                                              0.0, None)
+    assert tpa._lib.STATUS_NAMES[st] == "TREE_ERR_UNSUPPORTED"
