@@ -394,6 +394,8 @@ size_t tree_conv_bwd_workspace_bytes(const tree_plan_t* plan, int32_t channels);
 
 /* dx, dweight (and dbias unless NULL) of the conv, overwritten (not
  * accumulated). The pre-activation is recomputed from x, weight and bias.
+ * An N = 0 plan (after tree_conv_prepare, which records the kernel size)
+ * zeroes dweight and dbias and launches no kernel.
  * Errors as tree_conv_fwd, and a workspace below
  * tree_conv_bwd_workspace_bytes -> TREE_ERR_INVALID_ARG. */
 tree_status_t tree_conv_bwd(const tree_plan_t* plan, const void* x, const float* weight,
@@ -412,7 +414,8 @@ tree_status_t tree_conv_bwd(const tree_plan_t* plan, const void* x, const float*
  *  - inverse = 1 turns by the opposite angle: the backward of the forward
  *    rotation (grad_x = R^T grad_y) and its exact inverse up to rounding.
  *  - Arithmetic in fp32 (angle reduced in fp64); bf16 results rounded once.
- * Asynchronous on `stream`; the plan must be on the current device.
+ * Asynchronous on `stream`; the plan must be on the current device (an N = 0
+ * plan does nothing, after the scalar checks; x may then be NULL).
  * Errors: head_dim odd or above 128 -> TREE_ERR_UNSUPPORTED; heads <= 0, a bad
  * dtype, base not finite and positive, rotate_half or inverse not 0/1, NULL
  * or misaligned x -> TREE_ERR_INVALID_ARG; plan not on the device ->

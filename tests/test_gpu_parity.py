@@ -240,6 +240,41 @@ def test_empty_plan_is_a_no_op():
     tpa.tree_status_sync()
 
 
+def test_every_call_on_an_empty_trie():
+    """An N = 0 plan through every call: each returns with empty outputs and
+    launches nothing that could fail on an empty grid; the conv backward's
+    dweight and dbias, which it overwrites, come back zero, and the
+    cross-entropy's total loss is 0."""
+    _need_gpu()
+    plan = tpa.tree_plan_build(np.zeros(0, np.int32), np.zeros(0, np.int32))
+
+    def z(*shape, dtype=torch.bfloat16):
+        return torch.zeros(*shape, dtype=dtype, device="cuda")
+
+    q, k = z(0, 4, 128), z(0, 2, 128)
+    o, lse = tpa.tree_attn_fwd(plan, q, k, k)
+    dq, dk, dv = tpa.tree_attn_bwd(plan, q, q, k, k, o, lse)
+    assert dq.shape == (0, 4, 128) and dk.shape == dv.shape == (0, 2, 128)
+    tpa.tree_rope(plan, q)
+    tpa.tree_rope_qk(plan, q, k)
+    x = z(0, 64)
+    w = torch.randn(64, 4, device="cuda")
+    b = torch.randn(64, device="cuda")
+    assert tpa.tree_conv_fwd(plan, x, w, b).shape == (0, 64)
+    dx, dw, db = tpa.tree_conv_bwd(plan, x, w, b, x)
+    assert dx.shape == (0, 64)
+    assert torch.equal(dw, torch.zeros_like(w)) and torch.equal(db, torch.zeros_like(b))
+    loss, row_loss, dz = tpa.tree_weighted_ce(plan, z(0, 16), torch.zeros(0, dtype=torch.int32,
+                                                                      device="cuda"),
+                                              z(0, dtype=torch.float32))
+    assert float(loss) == 0.0 and dz.shape == (0, 16) and row_loss.shape == (0,)
+    f32 = torch.float32
+    og, st = tpa.tree_gdn_fwd(plan, z(0, 1, 128, dtype=f32), z(0, 1, 128, dtype=f32),
+                              z(0, 2, 128, dtype=f32), z(0, 2, dtype=f32), z(0, 2, dtype=f32))
+    assert og.shape == (0, 2, 128) and st.shape == (0, 2, 128, 128)
+    tpa.tree_status_sync()
+
+
 # ------------------------------------------- full-size workloads, sampled
 
 def _sample_rows(parents, lengths, rng, n=12):

@@ -347,11 +347,12 @@ extern "C" tree_status_t tree_gdn_fwd(const tree_plan_t* p, const void* q, const
 
 namespace {
 
-tree_status_t rope_entry(const tree_plan_t* p, void* x, int32_t heads, void* x2, int32_t heads2,
+// pair: q and k in one call (x2 = k), checked like x
+tree_status_t rope_entry(const tree_plan_t* p, void* x, int32_t heads, void* x2, int32_t heads2, bool pair,
                          int32_t head_dim, tree_dtype_t dtype, float base, int32_t rotate_half,
                          int32_t inverse, tree_stream_t stream) {
   if (!p) return fail(TREE_ERR_INVALID_ARG, "NULL plan");
-  if (heads <= 0 || (x2 && heads2 <= 0)) return fail(TREE_ERR_INVALID_ARG, "heads must be positive");
+  if (heads <= 0 || (pair && heads2 <= 0)) return fail(TREE_ERR_INVALID_ARG, "heads must be positive");
   if (!rope_shape_ok(head_dim))
     return fail(TREE_ERR_UNSUPPORTED, "head_dim must be even and at most 128");
   if (dtype != TREE_DTYPE_BF16 && dtype != TREE_DTYPE_F32)
@@ -360,7 +361,7 @@ tree_status_t rope_entry(const tree_plan_t* p, void* x, int32_t heads, void* x2,
   if ((rotate_half != 0 && rotate_half != 1) || (inverse != 0 && inverse != 1))
     return fail(TREE_ERR_INVALID_ARG, "rotate_half and inverse must be 0 or 1");
   if (p->N == 0) return TREE_OK;
-  if (!x) return fail(TREE_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!x || (pair && !x2)) return fail(TREE_ERR_INVALID_ARG, "NULL tensor pointer");
   if (!aligned16(x) || (x2 && !aligned16(x2)))
     return fail(TREE_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   const size_t elem = dtype == TREE_DTYPE_F32 ? 4 : 2;
@@ -386,15 +387,14 @@ tree_status_t rope_entry(const tree_plan_t* p, void* x, int32_t heads, void* x2,
 extern "C" tree_status_t tree_rope(const tree_plan_t* p, void* x, int32_t heads, int32_t head_dim,
                                    tree_dtype_t dtype, float base, int32_t rotate_half,
                                    int32_t inverse, tree_stream_t stream) {
-  return rope_entry(p, x, heads, nullptr, 0, head_dim, dtype, base, rotate_half, inverse, stream);
+  return rope_entry(p, x, heads, nullptr, 0, false, head_dim, dtype, base, rotate_half, inverse, stream);
 }
 
 extern "C" tree_status_t tree_rope_qk(const tree_plan_t* p, void* q, int32_t q_heads, void* k,
                                       int32_t k_heads, int32_t head_dim, tree_dtype_t dtype,
                                       float base, int32_t rotate_half, int32_t inverse,
                                       tree_stream_t stream) {
-  if (!k) return fail(TREE_ERR_INVALID_ARG, "NULL tensor pointer");
-  return rope_entry(p, q, q_heads, k, k_heads, head_dim, dtype, base, rotate_half, inverse, stream);
+  return rope_entry(p, q, q_heads, k, k_heads, true, head_dim, dtype, base, rotate_half, inverse, stream);
 }
 
 namespace {
@@ -444,7 +444,10 @@ extern "C" tree_status_t tree_conv_prepare(tree_plan_t* p, int32_t kernel_size, 
   if (kernel_size < 1 || kernel_size > kConvMaxK)
     return fail(TREE_ERR_UNSUPPORTED, "kernel_size must be 1 to " + std::to_string(kConvMaxK));
   if (p->N >= (1 << 28)) return fail(TREE_ERR_OVERFLOW, "too many tokens for the conv tables");
-  if (p->N == 0) return TREE_OK;
+  if (p->N == 0) {  // no tables; the kernel size still sizes the weight gradient
+    p->conv.K = kernel_size;
+    return TREE_OK;
+  }
   return conv_tables_build(p, kernel_size, static_cast<cudaStream_t>(stream));
 }
 
@@ -473,7 +476,16 @@ extern "C" tree_status_t tree_conv_bwd(const tree_plan_t* p, const void* x, cons
                                        int32_t activation, void* workspace, size_t workspace_bytes,
                                        tree_stream_t stream) {
   tree_status_t st = conv_check(p, channels, dtype, activation);
-  if (st != TREE_OK || p->N == 0) return st;
+  if (st != TREE_OK) return st;
+  if (p->N == 0) {  // no tokens: dweight and dbias (overwritten, not accumulated) are zero
+    if (p->conv.K == 0) return fail(TREE_ERR_NOT_ON_DEVICE, "call tree_conv_prepare first");
+    if (!dweight) return fail(TREE_ERR_INVALID_ARG, "NULL pointer");
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(dweight, 0, static_cast<size_t>(channels) * p->conv.K * sizeof(float), s);
+    if (e == cudaSuccess && dbias) e = cudaMemsetAsync(dbias, 0, static_cast<size_t>(channels) * sizeof(float), s);
+    if (e != cudaSuccess) return cuda_fail(e, "tree_conv_bwd zero gradients");
+    return TREE_OK;
+  }
   if (!x || !weight || !dy || !dx || !dweight || !workspace) return fail(TREE_ERR_INVALID_ARG, "NULL pointer");
   if (!aligned16(x) || !aligned16(dy) || !aligned16(dx) || !aligned16(workspace))
     return fail(TREE_ERR_INVALID_ARG, "x, dy, dx and workspace must be 16-byte aligned");
