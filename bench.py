@@ -657,6 +657,136 @@ def ce_arm(args):
     }))
 
 
+def gateway_pieces(parents, lengths, part_of, plan):
+    """The pieces of a node-boundary partition with their gateways (App. B.2-B.3):
+    per piece its segments renumbered as a trie of its own, its tokens (global
+    DFS indices), and its gateway: the parent piece's gateway followed by the
+    parent piece's DFS tokens up to the end of the cut node, visible where they
+    lie on the chain from the parent piece's root down to the cut node (the
+    parent's own gateway keeps the visibility it had for the parent)."""
+    order = [int(s) for s in plan.field("dfs_order")]
+    start = plan.field("seg_start")
+    tok = {s: range(int(start[s]), int(start[s]) + int(lengths[s])) for s in order}
+    out, ids = {}, []
+    for s in order:
+        if part_of[s] not in ids:
+            ids.append(part_of[s])
+    for pid in ids:
+        segs = [s for s in order if part_of[s] == pid]
+        local = {s: n for n, s in enumerate(segs)}
+        lp = [local[parents[s]] if parents[s] >= 0 and part_of[parents[s]] == pid else -1 for s in segs]
+        gw, vis = [], []
+        root = segs[0]
+        if parents[root] >= 0:
+            nc = parents[root]
+            pp = out[part_of[nc]]
+            chain, a = set(), nc
+            while a >= 0 and part_of[a] == part_of[nc]:
+                chain.add(a)
+                a = parents[a]
+            gw, vis = list(pp["gw"]), list(pp["vis"])
+            for s in pp["segs"]:
+                gw.extend(tok[s])
+                vis.extend([s in chain] * len(tok[s]))
+                if s == nc:
+                    break
+        out[pid] = {"segs": segs, "parents": lp, "lengths": [int(lengths[s]) for s in segs],
+                    "tokens": [t for s in segs for t in tok[s]], "gw": gw, "vis": vis}
+    return [out[pid] for pid in ids]
+
+
+def gateway_arm(args):
+    """--op gateway: partition-gateway attention (App. B.2-B.5). The workload's
+    trie (default 4: agentic, 65,536 tokens, 16 heads) cut by tree_partition into
+    pieces of at most --cap tokens; one step is the forward and backward of every
+    piece over its own keys and its gateway (its ancestors' cached keys), with
+    the gateway gradients accumulated in fp32. The figure counts each piece's
+    visible pairs, its own plus its rows times its visible gateway keys, which
+    together are the whole trie's, at 4·D (forward) + 10·D (backward) flops per
+    pair and q head; the whole trie in one call is timed the same way beside it."""
+    import torch
+
+    import treegen
+    import tree_packed_attention_gb300 as tpa
+
+    torch.cuda.set_device(0)
+    w = treegen.workload(args.workload)
+    whole = tpa.tree_plan_build(w.parents, w.lengths)
+    N, hq, hkv, D = w.num_tokens, w.hq, w.hkv, w.head_dim
+    r = tpa.tree_partition(whole, args.cap)
+    part = [int(x) for x in r["part_of_segment"]]
+    parents = [int(x) for x in w.parents]
+    Xs = gateway_pieces(parents, w.lengths, part, whole)
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    q, do = (torch.randn(N, hq, D, device="cuda", generator=gen).to(torch.bfloat16) for _ in range(2))
+    k, v = (torch.randn(N, hkv, D, device="cuda", generator=gen).to(torch.bfloat16) for _ in range(2))
+    runs, pairs = [], 0
+    for X in Xs:
+        t = torch.as_tensor(X["tokens"], dtype=torch.long, device="cuda")
+        g = torch.as_tensor(X["gw"], dtype=torch.long, device="cuda")
+        plan = tpa.tree_plan_build_partition(X["parents"], X["lengths"], X["vis"])
+        P = plan.info["past_len"]
+        acc = [torch.zeros(P, hkv, D, dtype=torch.float32, device="cuda") for _ in range(2)]
+        ws = torch.empty(max(tpa.tree_attn_bwd_workspace_bytes(plan, hq, D, torch.bfloat16), 16),
+                         dtype=torch.uint8, device="cuda")
+        runs.append((plan, q[t].contiguous(), k[t].contiguous(), v[t].contiguous(), do[t].contiguous(),
+                     k[g].contiguous(), v[g].contiguous(), acc, ws))
+        pairs += int(plan.info["visible_pairs"]) + len(X["tokens"]) * int(plan.info["past_visible"])
+    assert pairs == int(whole.info["visible_pairs"]), (pairs, whole.info["visible_pairs"])
+
+    def step_pieces():
+        for plan, qp, kp, vp, dop, pk, pv, acc, ws in runs:
+            acc[0].zero_()
+            acc[1].zero_()
+            o, lse = tpa.tree_attn_fwd_gateway(plan, qp, kp, vp, pk, pv)
+            tpa.tree_attn_bwd_gateway(plan, dop, qp, kp, vp, pk, pv, o, lse, acc[0], acc[1], workspace=ws)
+
+    ws_whole = torch.empty(tpa.tree_attn_bwd_workspace_bytes(whole, hq, D, torch.bfloat16), dtype=torch.uint8,
+                           device="cuda")
+
+    def step_whole():
+        o, lse = tpa.tree_attn_fwd(whole, q, k, v)
+        tpa.tree_attn_bwd(whole, do, q, k, v, o, lse, workspace=ws_whole)
+
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for e in ev:
+            flush.zero_()
+            e[0].record(stream)
+            fn()
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        tpa.tree_status_sync()
+        return statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+
+    with ClockSampler(0) as clocks:
+        ms = timed(step_pieces)
+    ms_whole = timed(step_whole)
+    flops = 14.0 * D * hq * pairs
+    tf = flops / (ms * 1e-3) / 1e12
+    peaks, kind = _peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    print(json.dumps({
+        "metric": "partition-gateway attention fwd+bwd over every piece, visible-pair TFLOP/s on 1 GB300",
+        "value": tf, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": N, "hq": hq, "hkv": hkv, "head_dim": D, "cap": args.cap,
+                   "pieces": len(Xs), "gateway_keys": int(sum(len(X["gw"]) for X in Xs)),
+                   "visible_pairs": pairs, "l2": "L2 flushed between steps"},
+        "whole_trie": {"ms": ms_whole, "tflops": flops / (ms_whole * 1e-3) / 1e12},
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                     "peak_source": f"{kind} bf16 dense (burst)", "traffic": None},
+        "clocks": clocks.summary(), "gpu_launches": 3 * len(Xs) * args.steps,
+    }))
+
+
 def gdn_arm(args):
     """--op gdn: the Gated DeltaNet forward with tree state routing (eq. 10,
     App. A.2) over the workload's trie, bf16 q/k/v, --gdn-heads query/key heads
@@ -759,10 +889,13 @@ def main():
     ap.add_argument("--extra-workloads", default="3,4",
                     help="comma-separated workloads also timed and reported under 'workloads' "
                          "('' for none)")
-    ap.add_argument("--op", default="attention", choices=["attention", "rope", "conv", "ce", "gdn", "partition"],
+    ap.add_argument("--op", default="attention", choices=["attention", "rope", "conv", "ce", "gdn", "partition",
+                                                         "gateway"],
                     help="attention (the default and the headline), rope (tree RoPE on q and k), "
                          "conv (the tree-correct causal conv), ce (the fused weighted cross-entropy; "
-                         "workload 6 unless --workload is given), gdn (GDN with tree state routing) "
+                         "workload 6 unless --workload is given), gdn (GDN with tree state routing), "
+                         "gateway (partition-gateway attention over the pieces of a --cap cut; "
+                         "workload 4 unless --workload is given), "
                          "or partition (the host planner, no GPU)")
     ap.add_argument("--gdn-heads", type=int, default=16, help="query/key heads for --op gdn (value heads: 2x)")
     ap.add_argument("--vocab", type=int, default=151936, help="vocabulary for --op ce")
@@ -781,6 +914,10 @@ def main():
         ce_arm(args)
     elif args.op == "partition":
         partition_arm(args)
+    elif args.op == "gateway":
+        if "--workload" not in sys.argv:
+            args.workload = 4
+        gateway_arm(args)
     elif args.impl == "reference":
         reference_arm(args)
     else:

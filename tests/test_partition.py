@@ -164,3 +164,33 @@ def test_gateway_lengths_and_peak_by_token_counting():
                 assert rec[i]["past_len"] == by_tokens[i] == r["past_len"][i]
             peak = _peak_by_tokens(parents, lengths, part)
             assert PO.peak_path_tokens(parents, lengths, part) == peak == r["peak_path_tokens"]
+
+
+def test_bench_gateway_pieces_follow_the_definition():
+    """bench.py builds the pieces it times (--op gateway) from the library's plan
+    fields; they must be the pieces of App. B.2-B.3 as the test helper builds
+    them from the definition, and their visible pairs, own plus gateway, must
+    add up to the whole trie's."""
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    from partition_util import pieces
+    rng = np.random.default_rng(31)
+    for _ in range(12):
+        S = int(rng.integers(2, 14))
+        parents = [-1] + [int(rng.integers(0, s)) for s in range(1, S)]
+        lengths = [int(x) for x in rng.integers(1, 90, S)]
+        whole = tpa.tree_plan_build(parents, lengths)
+        r = tpa.tree_partition(whole, max(max(lengths), sum(lengths) // 3))
+        part = [int(x) for x in r["part_of_segment"]]
+        got = bench.gateway_pieces(parents, lengths, part, whole)
+        ref = pieces(parents, lengths, part)
+        assert len(got) == len(ref) == r["num_parts"]
+        pairs = 0
+        for X, Y in zip(got, ref):
+            for key in ("parents", "lengths", "tokens", "gw", "vis"):
+                assert list(X[key]) == list(Y[key]), key
+            plan = tpa.tree_plan_build_partition(X["parents"], X["lengths"], X["vis"])
+            pairs += plan.info["visible_pairs"] + len(X["tokens"]) * plan.info["past_visible"]
+        assert pairs == whole.info["visible_pairs"]
