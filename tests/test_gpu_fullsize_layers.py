@@ -1,15 +1,20 @@
 """Full-size GPU parity of the tree-correct causal conv (App. A.3) and the GDN
 tree state routing (eq. 10, App. A.2) on the packed workload (32 tries,
-131,072 tokens), with the inputs and the launch configuration that
-`bench.py --op conv` and `bench.py --op gdn` time.
+131,072 tokens), and of the fused weighted cross-entropy (§3.1 eq. 3-5) on
+the packed shape at 32,768 tokens with a 151,936-entry vocabulary, with the
+inputs and the launch configurations that `bench.py --op conv`, `--op gdn`
+and `--op ce` time.
 
 Both layers are independent per channel (the conv is depthwise) or per value
 head (each GDN value head reads only its own query/key head), so the fp64
 oracle run on a sample of channels or value heads is exactly the oracle of
 the whole layer restricted to them: every token, every branch point and
 every segment end state of the sampled columns is compared, at the
-tolerances of the small-case tests.
+tolerances of the small-case tests. A cross-entropy row depends only on its
+own logits and the tokens that follow it on its paths, so sampled rows are
+compared one by one.
 """
+import numpy as np
 import pytest
 import torch
 
@@ -17,6 +22,7 @@ import treegen
 import tree_packed_attention_gb300 as tpa
 from oracle import conv as CV
 from oracle import gdn as GD
+from oracle import loss as LO
 
 pytestmark = pytest.mark.gpu
 
@@ -102,3 +108,42 @@ def test_gdn_full_size_sampled_value_heads():
             bound = 2e-4 + 1e-4 * ref.abs() + store * ref.abs()
             excess = float((d - bound).max())
             assert excess <= 0, f"{name} of value head {h}: max err {float(d.max()):.3g}"
+
+
+def test_weighted_ce_full_size_sampled_rows():
+    """bf16 logits [32768, 151936] drawn N(0, 9), every token predicted,
+    lambda = g/K: the row losses and dlogits of the rows before branch points
+    (several predictions each), of leaf ends (none), of the first and last
+    rows and of random rows, against the oracle; the total is the
+    fixed-order sum of all row losses. Tolerances as the small-case tests:
+    row losses 1e-5 relative + 1e-5, dlogits 1e-6 + (1e-5 + 2^-8) |ref|."""
+    _need_gpu()
+    w = treegen.workload(6)
+    plan = tpa.tree_plan_build(w.parents, w.lengths)
+    N, V = plan.num_tokens, 151936
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    z = torch.empty(N, V, dtype=torch.bfloat16, device="cuda")
+    for r0 in range(0, N, 4096):
+        r1 = min(N, r0 + 4096)
+        z[r0:r1] = (torch.randn(r1 - r0, V, device="cuda", generator=gen) * 3).to(torch.bfloat16)
+    tokens = torch.randint(0, V, (N,), device="cuda", generator=gen, dtype=torch.int32)
+    lam = torch.as_tensor(tpa.tree_weights(plan), device="cuda")
+    loss, row_loss, dz = tpa.tree_weighted_ce(plan, z, tokens, lam)
+    tpa.tree_status_sync()
+
+    succ = LO.path_successors(w.parents, w.lengths)
+    branch = [r for r in range(N) if len(succ[r]) > 1]
+    ends = [r for r in range(N) if not succ[r]]
+    rng = np.random.default_rng(0)
+    rows = sorted(set(branch[:96] + ends[:16] + [0, N - 1] + rng.integers(0, N, 64).tolist()))
+    # the oracle reads only the sampled rows' logits
+    zc = torch.empty(N, V, dtype=torch.bfloat16)
+    zc[rows] = z[rows].cpu()
+    _, rrow, rdz = LO.weighted_ce(zc, tokens.cpu().numpy(), lam.cpu().numpy().astype(np.float64),
+                                  w.parents, w.lengths, 1.0, rows=rows)
+    got_rows = row_loss.cpu().double()[rows]
+    assert torch.allclose(got_rows, rrow, rtol=1e-5, atol=1e-5), float((got_rows - rrow).abs().max())
+    got_dz = dz[rows].cpu().double()
+    bound = 1e-6 + (1e-5 + 2.0 ** -8) * rdz.abs()
+    assert float(((got_dz - rdz).abs() - bound).max()) <= 0, float((got_dz - rdz).abs().max())
+    assert abs(float(loss) - float(row_loss.double().sum())) <= 1e-6 * max(1.0, abs(float(loss)))
